@@ -1,0 +1,260 @@
+"""Float64 CPU oracle of the Kronecker-factored (K-FAC / AdaFisher-style) optimizer step.
+
+TEST INFRASTRUCTURE.  This module exists to check the CUDA path.  Only the
+tests, the package's smoke entry and the benchmark's CPU-baseline leg may
+import it; the library never does, and it shares no code with the library.
+
+Every quantity is float64.  Inputs arrive already rounded to their storage
+type (fp32 or bf16) and are promoted to float64 here.  Where a step has a
+plain definition it is written out as that definition, using NumPy matrix
+products as the only library primitive; the Cholesky factorisation and the
+triangular solves are the textbook column algorithms, written out.
+
+Sources (page title, section):
+  * Osawa et al., "Large-Scale Distributed Second-Order Optimization Using
+    Kronecker-Factored Approximate Curvature for Deep Convolutional Neural
+    Networks", §3.2: the Fisher of a layer is approximated by the Kronecker
+    product of a factor built from the layer's input activations (A) and one
+    built from its output gradients (G); its inverse is taken through the
+    inverses of the two factors.
+  * same page, §3.4: the factors are symmetric, so an N x N factor carries
+    N(N+1)/2 distinct entries.
+  * same page, §5.4: curvature refreshed less often than every step (stale
+    factors); BatchNorm Fisher approximated by its diagonal.
+  * "CAFIN: CUDA-accelerated Adaptive Fisher Information Matrix Network
+    Optimization via GPU-Native Kernel Fusion", Introduction: AdaFisher keeps
+    diagonal Kronecker factors as exponential moving averages; Kernel Fusion
+    Strategy: the fused step loads gradient and parameter, updates the EMA of
+    the diagonal Fisher blocks, preconditions the gradient, adds momentum and
+    weight decay, and writes the parameter in place.
+
+Where the pages leave a step open, this module takes the reading below (each
+one is also listed in the repository's design notes):
+  R1  EMA starts from zero (F_0 = 0); ``ema_init="first"`` gives F_1 = F_new.
+  R2  "decay xi" means the old value keeps weight xi: F <- xi F + (1-xi) F_new.
+  R3  factor scale s = 1/M, M = number of rows (batch, or B*H*W for conv).
+  R4  inverses are refreshed at step 1 and then every k steps; a step uses the
+      inverses of the latest refresh at or before it.
+  R5  update: u = P + lambda*W ; m <- mu*m + u ; W <- W - eta*m (m_0 = 0).
+  R6  damping: sqrt(gamma) added to the diagonal of each factor.
+  R7  diagonal step: P_ij = dW_ij / (g_i a_j + gamma), g and a the EMA diagonals.
+  R8  a layer with a bias carries it as the last column of W-hat = [W | b] and
+      its activations get a ones column: a-hat = [a | 1].
+
+Parity pins for every function live in tests/test_oracle.py.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import numpy as np
+
+
+class NotPositiveDefinite(ArithmeticError):
+    """Raised by :func:`cholesky_lower` with the 0-based failing column."""
+
+    def __init__(self, column: int):
+        super().__init__(f"leading minor {column + 1} is not positive definite")
+        self.column = column
+
+
+def _f64(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# factors (Osawa et al. §3.2; symmetry §3.4)
+
+def augment_ones(a, has_bias: int) -> np.ndarray:
+    """a-hat = [a | 1] when the layer has a bias (reading R8), else a."""
+    a = _f64(a)
+    if not has_bias:
+        return a
+    return np.concatenate([a, np.ones((a.shape[0], 1))], axis=1)
+
+
+def factor(x, has_bias: int = 0, scale: Optional[float] = None) -> np.ndarray:
+    """New factor s * x-hat^T x-hat for x of shape [M, d] (rows are samples).
+
+    A is built from input activations with has_bias; G from output gradients
+    with has_bias = 0.  The result is symmetrised as (F + F^T)/2 so that it is
+    symmetric to the last bit.
+    """
+    xh = augment_ones(x, has_bias)
+    M = xh.shape[0]
+    s = 1.0 / M if scale is None else float(scale)
+    F = s * (xh.T @ xh)
+    return 0.5 * (F + F.T)
+
+
+def ema(old, new, decay: float) -> np.ndarray:
+    """Running factor by exponential moving average (reading R2)."""
+    return decay * _f64(old) + (1.0 - decay) * _f64(new)
+
+
+# ---------------------------------------------------------------------------
+# damped inverse (Osawa et al. §3.2: inverse through the factor inverses)
+
+def damped(F, damping: float) -> np.ndarray:
+    """F + sqrt(gamma) I (reading R6)."""
+    F = _f64(F)
+    return F + math.sqrt(damping) * np.eye(F.shape[0])
+
+
+def cholesky_lower(S) -> np.ndarray:
+    """Textbook column-by-column Cholesky: S = L L^T with L lower triangular.
+
+    Column j:  L[j,j] = sqrt(S[j,j] - sum_{k<j} L[j,k]^2),
+               L[i,j] = (S[i,j] - sum_{k<j} L[i,k] L[j,k]) / L[j,j]   (i > j).
+    Raises NotPositiveDefinite(j) when the pivot is not > 0 (or not finite).
+    """
+    S = _f64(S)
+    n = S.shape[0]
+    L = np.zeros_like(S)
+    for j in range(n):
+        d = S[j, j] - L[j, :j] @ L[j, :j]
+        if not (d > 0.0 and math.isfinite(d)):
+            raise NotPositiveDefinite(j)
+        L[j, j] = math.sqrt(d)
+        if j + 1 < n:
+            L[j + 1:, j] = (S[j + 1:, j] - L[j + 1:, :j] @ L[j, :j]) / L[j, j]
+    return L
+
+
+def lower_inverse(L) -> np.ndarray:
+    """X = L^{-1} by forward substitution on the identity, row by row.
+
+    Row i of L X = I gives X[i, :] = (e_i - sum_{k<i} L[i,k] X[k, :]) / L[i,i];
+    X is lower triangular, so only columns <= i are formed.
+    """
+    L = _f64(L)
+    n = L.shape[0]
+    X = np.zeros_like(L)
+    for i in range(n):
+        r = -(L[i, :i] @ X[:i, :i + 1])
+        r[i] += 1.0
+        X[i, :i + 1] = r / L[i, i]
+    return X
+
+
+def spd_inverse_from_cholesky(L) -> np.ndarray:
+    """S^{-1} = L^{-T} L^{-1}: forward substitution on I, then the transpose product."""
+    X = lower_inverse(L)
+    Sinv = X.T @ X
+    return 0.5 * (Sinv + Sinv.T)
+
+
+def damped_inverse(F, damping: float) -> np.ndarray:
+    """(F + sqrt(gamma) I)^{-1} via the textbook Cholesky and substitutions."""
+    return spd_inverse_from_cholesky(cholesky_lower(damped(F, damping)))
+
+
+# ---------------------------------------------------------------------------
+# preconditioning and update
+
+def grad_hat(grad_w, grad_b=None) -> np.ndarray:
+    """dW-hat = [dW | db] (reading R8)."""
+    gw = _f64(grad_w)
+    if grad_b is None:
+        return gw
+    return np.concatenate([gw, _f64(grad_b).reshape(-1, 1)], axis=1)
+
+
+def precondition(Ginv, gw_hat, Ainv) -> np.ndarray:
+    """Natural-gradient direction P = G_d^{-1} . dW-hat . A_d^{-1} (Osawa et al. §3.2)."""
+    return _f64(Ginv) @ _f64(gw_hat) @ _f64(Ainv)
+
+
+def momentum_update(P, W_hat, m, lr, momentum, weight_decay):
+    """u = P + lambda W ; m <- mu m + u ; W <- W - eta m  (reading R5).
+
+    Returns (W_new, m_new).  Follows the CAFIN briefing's fused order: apply
+    the preconditioner, then momentum and weight decay, then write W.
+    """
+    u = _f64(P) + weight_decay * _f64(W_hat)
+    m_new = momentum * _f64(m) + u
+    W_new = _f64(W_hat) - lr * m_new
+    return W_new, m_new
+
+
+# ---------------------------------------------------------------------------
+# diagonal path (CAFIN Introduction / Kernel Fusion Strategy; Osawa et al. §5.4 BN)
+
+def diag_factor(x, has_bias: int = 0, scale: Optional[float] = None) -> np.ndarray:
+    """diag(s * x-hat^T x-hat): s * sum_r x[r, j]^2 per column (ones column -> s*M)."""
+    xh = augment_ones(x, has_bias)
+    M = xh.shape[0]
+    s = 1.0 / M if scale is None else float(scale)
+    return s * np.sum(xh * xh, axis=0)
+
+
+def diag_precondition(gw_hat, gs, as_, damping: float) -> np.ndarray:
+    """P_ij = dW_ij / (g_i a_j + gamma)  (reading R7)."""
+    return _f64(gw_hat) / (np.outer(_f64(gs), _f64(as_)) + damping)
+
+
+# ---------------------------------------------------------------------------
+# the whole per-layer step
+
+class LayerState:
+    """State of one layer: running factors, inverses, momentum and parameters."""
+
+    def __init__(self, kind: str, d_out: int, d_in: int, has_bias: int, w0, b0=None):
+        self.kind, self.o, self.d_in, self.has_bias = kind, d_out, d_in, has_bias
+        self.n = d_in + has_bias
+        self.W = grad_hat(w0, b0 if has_bias else None).copy()   # [o, n]
+        self.m = np.zeros((d_out, self.n))
+        self.t = 0
+        if kind == "kron":
+            self.A = np.zeros((self.n, self.n))
+            self.G = np.zeros((d_out, d_out))
+            self.Ainv = self.Ginv = None
+        else:
+            self.gs = np.zeros(d_out)
+            self.as_ = np.zeros(self.n)
+        self.P = None
+
+
+class KfacOracle:
+    """Per-layer K-FAC / diagonal step, in the order the pages give it.
+
+    ``ema_init``: "zero" (reading R1) or "first" (F_1 = F_new).
+    """
+
+    def __init__(self, ema_decay, damping, lr, momentum, weight_decay,
+                 invert_every: int = 1, ema_init: str = "zero"):
+        self.xi, self.gamma = float(ema_decay), float(damping)
+        self.lr, self.mu, self.wd = float(lr), float(momentum), float(weight_decay)
+        self.k = int(invert_every)
+        self.ema_init = ema_init
+
+    def _blend(self, old, new, t):
+        if t == 1 and self.ema_init == "first":
+            return _f64(new).copy()
+        return ema(old, new, self.xi)
+
+    def step_kron(self, st: LayerState, a, g, grad_w, grad_b=None, scale=None):
+        """One K-FAC step; returns the preconditioned gradient P [o, n]."""
+        st.t += 1
+        t = st.t
+        st.A = self._blend(st.A, factor(a, st.has_bias, scale), t)
+        st.G = self._blend(st.G, factor(g, 0, scale), t)
+        if (t - 1) % self.k == 0:                      # reading R4
+            st.Ainv = damped_inverse(st.A, self.gamma)
+            st.Ginv = damped_inverse(st.G, self.gamma)
+        P = precondition(st.Ginv, grad_hat(grad_w, grad_b if st.has_bias else None), st.Ainv)
+        st.W, st.m = momentum_update(P, st.W, st.m, self.lr, self.mu, self.wd)
+        st.P = P
+        return P
+
+    def step_diag(self, st: LayerState, g_new, a_new, grad_w, grad_b=None):
+        """One diagonal-Fisher step given the new diagonal factors; returns P."""
+        st.t += 1
+        st.gs = self._blend(st.gs, g_new, st.t)
+        st.as_ = self._blend(st.as_, a_new, st.t)
+        P = diag_precondition(grad_hat(grad_w, grad_b if st.has_bias else None),
+                              st.gs, st.as_, self.gamma)
+        st.W, st.m = momentum_update(P, st.W, st.m, self.lr, self.mu, self.wd)
+        st.P = P
+        return P

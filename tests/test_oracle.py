@@ -1,0 +1,281 @@
+"""Pins for the float64 oracle against facts fixed by the pages and by the mathematics.
+
+None of these re-type the oracle's own formula: each check uses brute force on
+tiny inputs, a closed form, an invariant, or an independent library routine
+(LAPACK through NumPy/SciPy) for a step the oracle writes out by hand.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.linalg
+
+import oracle as O
+import workloads as W
+
+RNG = np.random.default_rng(1234)
+
+
+# ---------------------------------------------------------------- factors
+
+def _brute_factor(x, has_bias, scale):
+    """Sum over rows of outer products, element by element, in exact rationals."""
+    M, d = len(x), len(x[0])
+    n = d + has_bias
+    col = lambda r, j: Fraction(x[r][j]) if j < d else Fraction(1)
+    s = Fraction(scale) if scale is not None else Fraction(1, M)
+    return [[s * sum(col(r, i) * col(r, j) for r in range(M)) for j in range(n)]
+            for i in range(n)]
+
+
+@pytest.mark.parametrize("M,d,has_bias", [(1, 1, 0), (3, 2, 1), (5, 4, 0), (8, 4, 1), (7, 3, 1)])
+def test_factor_brute_force(M, d, has_bias):
+    x = RNG.integers(-5, 6, size=(M, d)).astype(np.float64) / 4.0
+    F = O.factor(x, has_bias)
+    ref = _brute_factor(x.tolist(), has_bias, None)
+    for i in range(d + has_bias):
+        for j in range(d + has_bias):
+            assert abs(F[i, j] - float(ref[i][j])) <= 1e-15 * max(1.0, abs(float(ref[i][j])))
+
+
+def test_factor_custom_scale_and_shape():
+    x = RNG.standard_normal((6, 3))
+    F = O.factor(x, 1, scale=0.25)
+    assert F.shape == (4, 4)
+    ref = _brute_factor(x.tolist(), 1, 0.25)
+    assert np.allclose(F, np.array(ref, dtype=float), rtol=1e-14, atol=1e-14)
+
+
+def test_factor_symmetric_psd_and_bias_entries():
+    M, d = 200, 37
+    a = np.maximum(RNG.standard_normal((M, d)), 0)
+    A = O.factor(a, 1)
+    assert np.array_equal(A, A.T)                       # symmetric to the last bit
+    ev = np.linalg.eigvalsh(A)
+    assert ev.min() >= -A.shape[0] * np.finfo(float).eps * np.abs(ev).max()
+    assert A[d, d] == 1.0                               # s * M with s = 1/M
+    assert np.allclose(A[:d, d], a.mean(axis=0), rtol=1e-14, atol=1e-16)
+    assert np.allclose(np.diag(A)[:d], (a * a).mean(axis=0), rtol=1e-13)
+
+
+def test_factor_upper_triangle_count():
+    # Osawa et al. §3.4: an N x N symmetric factor has N(N+1)/2 distinct entries
+    A = O.factor(RNG.standard_normal((30, 11)), 1)
+    iu = np.triu_indices(12)
+    assert len(iu[0]) == 12 * 13 // 2
+    rebuilt = np.zeros_like(A)
+    rebuilt[iu] = A[iu]
+    rebuilt = rebuilt + np.triu(rebuilt, 1).T
+    assert np.array_equal(rebuilt, A)
+
+
+# ---------------------------------------------------------------- EMA
+
+@pytest.mark.parametrize("xi", [0.0, 0.5, 0.95])
+def test_ema_constant_input_closed_form(xi):
+    C = RNG.standard_normal((5, 5))
+    F0 = RNG.standard_normal((5, 5))
+    F = F0.copy()
+    for t in range(1, 40):
+        F = O.ema(F, C, xi)
+        closed = C + xi ** t * (F0 - C)
+        assert np.allclose(F, closed, rtol=1e-12, atol=1e-12)
+    if xi == 0.0:
+        assert np.array_equal(O.ema(F0, C, 0.0), C)
+
+
+def test_ema_zero_start_converges():
+    C = O.factor(RNG.standard_normal((50, 6)), 1)
+    F = np.zeros_like(C)
+    for _ in range(400):
+        F = O.ema(F, C, 0.95)
+    assert np.allclose(F, C, rtol=1e-8, atol=1e-8)
+
+
+# ---------------------------------------------------------------- Cholesky / inverse
+
+def test_cholesky_hand_examples():
+    L = O.cholesky_lower([[4.0, 2.0], [2.0, 2.0]])
+    assert np.array_equal(L, np.array([[2.0, 0.0], [1.0, 1.0]]))
+    L = O.cholesky_lower([[9.0, 3.0, 6.0], [3.0, 5.0, 6.0], [6.0, 6.0, 21.0]])
+    assert np.allclose(L, [[3, 0, 0], [1, 2, 0], [2, 2, 3.605551275463989]], atol=1e-15)
+
+
+@pytest.mark.parametrize("n", [1, 7, 64, 200])
+def test_cholesky_matches_lapack(n):
+    X = RNG.standard_normal((n + 5, n))
+    S = X.T @ X / (n + 5) + 0.1 * np.eye(n)
+    L = O.cholesky_lower(S)
+    assert np.allclose(L, np.linalg.cholesky(S), rtol=1e-12, atol=1e-13)
+    assert np.abs(L @ L.T - S).max() <= 1e-13 * np.abs(S).max()
+    assert np.array_equal(L, np.tril(L))
+
+
+def test_cholesky_not_pd_column():
+    with pytest.raises(O.NotPositiveDefinite) as e:
+        O.cholesky_lower(np.diag([1.0, 2.0, -1.0, 3.0]))
+    assert e.value.column == 2
+    with pytest.raises(O.NotPositiveDefinite) as e:
+        O.cholesky_lower([[1.0, 2.0], [2.0, 1.0]])
+    assert e.value.column == 1
+    with pytest.raises(O.NotPositiveDefinite) as e:
+        O.cholesky_lower([[float("nan")]])
+    assert e.value.column == 0
+
+
+@pytest.mark.parametrize("n", [1, 5, 70])
+def test_lower_inverse_vs_solve_triangular(n):
+    L = np.tril(RNG.standard_normal((n, n))) + 3 * np.eye(n)
+    X = O.lower_inverse(L)
+    ref = scipy.linalg.solve_triangular(L, np.eye(n), lower=True)
+    assert np.allclose(X, ref, rtol=1e-12, atol=1e-13)
+    assert np.allclose(L @ X, np.eye(n), atol=1e-13)
+
+
+@pytest.mark.parametrize("n", [3, 40, 257])
+def test_damped_inverse_vs_lapack(n):
+    A = O.factor(np.maximum(RNG.standard_normal((n // 2 + 3, n - 1)), 0), 1)
+    gamma = 1e-3
+    Ainv = O.damped_inverse(A, gamma)
+    Ad = A + math.sqrt(gamma) * np.eye(n)
+    ref = np.linalg.inv(Ad)
+    assert np.linalg.norm(Ainv - ref) <= 1e-10 * np.linalg.norm(ref)
+    assert np.abs(Ad @ Ainv - np.eye(n)).max() <= 1e-10
+    assert np.array_equal(Ainv, Ainv.T)
+
+
+def test_damped_inverse_of_zero_factor():
+    n = 9
+    Ainv = O.damped_inverse(np.zeros((n, n)), 1e-3)
+    assert np.allclose(Ainv, np.eye(n) / math.sqrt(1e-3), rtol=1e-15, atol=0)
+
+
+# ---------------------------------------------------------------- preconditioning
+
+@pytest.mark.parametrize("o,d,has_bias", [(1, 1, 1), (3, 4, 1), (6, 8, 1), (5, 9, 0), (4, 2, 0)])
+def test_precondition_kronecker_identity(o, d, has_bias):
+    """vec_r(G P A) = (G kron A^T) vec_r(P): solve with the materialised Kronecker matrix."""
+    M, gamma = 12, 1e-2
+    a = RNG.standard_normal((M, d))
+    g = RNG.standard_normal((M, o)) * 0.1
+    A, G = O.factor(a, has_bias), O.factor(g, 0)
+    gw = RNG.standard_normal((o, d))
+    gb = RNG.standard_normal(o) if has_bias else None
+    gh = O.grad_hat(gw, gb)
+    P = O.precondition(O.damped_inverse(G, gamma), gh, O.damped_inverse(A, gamma))
+    Ad = A + math.sqrt(gamma) * np.eye(d + has_bias)
+    Gd = G + math.sqrt(gamma) * np.eye(o)
+    K = np.kron(Gd, Ad.T)
+    vecP = np.linalg.solve(K, gh.reshape(-1))
+    assert np.allclose(P.reshape(-1), vecP, rtol=1e-10, atol=1e-12)
+
+
+def test_full_path_reduces_to_diag_path_on_diagonal_inputs():
+    """Rows +-c_k e_k make a-hat^T a-hat exactly diagonal, ones column included.
+
+    With diagonal factors the full path divides by (g_i+sqrt(gamma))(a_j+sqrt(gamma));
+    the diagonal path divides by (g_i a_j + gamma).  Feeding the diagonal path
+    g' = g + sqrt(gamma), a' = a + sqrt(gamma), gamma' = 0 must give the same P.
+    """
+    d, o, gamma = 5, 3, 1e-3
+    ca, cg = RNG.uniform(0.5, 2.0, d), RNG.uniform(0.01, 0.1, o)
+    a = np.concatenate([np.diag(ca), -np.diag(ca)])             # [2d, d]
+    g = np.concatenate([np.diag(cg), -np.diag(cg)])             # [2o, o]
+    # pad both to the same row count with zero rows (zero rows add nothing)
+    M = 2 * max(d, o)
+    a = np.vstack([a, np.zeros((M - len(a), d))])
+    g = np.vstack([g, np.zeros((M - len(g), o))])
+    A, G = O.factor(a, 1), O.factor(g, 0)
+    assert np.count_nonzero(A - np.diag(np.diag(A))) == 0
+    assert np.count_nonzero(G - np.diag(np.diag(G))) == 0
+    assert np.allclose(np.diag(A), O.diag_factor(a, 1), rtol=1e-15)
+    assert np.allclose(np.diag(G), O.diag_factor(g, 0), rtol=1e-15)
+    gh = O.grad_hat(RNG.standard_normal((o, d)), RNG.standard_normal(o))
+    P_full = O.precondition(O.damped_inverse(G, gamma), gh, O.damped_inverse(A, gamma))
+    sg = math.sqrt(gamma)
+    P_diag = O.diag_precondition(gh, np.diag(G) + sg, np.diag(A) + sg, 0.0)
+    assert np.allclose(P_full, P_diag, rtol=1e-12, atol=0)
+
+
+# ---------------------------------------------------------------- diagonal step
+
+def test_diag_factor_brute_force():
+    x = RNG.integers(-3, 4, size=(6, 4)).astype(float)
+    v = O.diag_factor(x, 1)
+    for j in range(4):
+        assert math.isclose(v[j], sum(float(x[r, j]) ** 2 for r in range(6)) / 6, rel_tol=4e-16)
+    assert v[4] == 1.0
+
+
+def test_diag_step_elementwise_closed_form():
+    o, n = 4, 3
+    gw = RNG.standard_normal((o, n))
+    W = RNG.standard_normal((o, n))
+    m = RNG.standard_normal((o, n))
+    gs, as_ = RNG.uniform(0, 1, o), RNG.uniform(0, 1, n)
+    gamma, eta, mu, lam = 1e-3, 0.1, 0.9, 5e-4
+    P = O.diag_precondition(gw, gs, as_, gamma)
+    Wn, mn = O.momentum_update(P, W, m, eta, mu, lam)
+    for i in range(o):
+        for j in range(n):
+            p = gw[i, j] / (gs[i] * as_[j] + gamma)
+            mm = mu * m[i, j] + (p + lam * W[i, j])
+            assert math.isclose(P[i, j], p, rel_tol=1e-15)
+            assert math.isclose(mn[i, j], mm, rel_tol=1e-14)
+            assert math.isclose(Wn[i, j], W[i, j] - eta * mm, rel_tol=1e-14, abs_tol=1e-15)
+
+
+def test_update_special_cases():
+    o, n = 3, 5
+    gw, W = RNG.standard_normal((o, n)), RNG.standard_normal((o, n))
+    gs, as_ = RNG.uniform(0.1, 1, o), RNG.uniform(0.1, 1, n)
+    P = O.diag_precondition(gw, gs, as_, 1e-3)
+    Wn, _ = O.momentum_update(P, W, np.zeros((o, n)), 0.0, 0.9, 5e-4)
+    assert np.array_equal(Wn, W)                                    # eta = 0
+    Wn, mn = O.momentum_update(P, W, np.zeros((o, n)), 0.1, 0.0, 0.0)
+    assert np.allclose(Wn, W - 0.1 * gw / (np.outer(gs, as_) + 1e-3), rtol=1e-14)
+
+
+# ---------------------------------------------------------------- whole step
+
+def _c1_run(steps=10, invert_every=1, ema_init="zero"):
+    cfg = W.get_config("c1")
+    hp = cfg.hp
+    orc = O.KfacOracle(hp.ema_decay, hp.damping, hp.lr, hp.momentum, hp.weight_decay,
+                       invert_every, ema_init)
+    L = cfg.layers[0]
+    w0, b0 = W.initial_params(cfg, 0)
+    st = O.LayerState("kron", L.d_out, L.d_in, L.has_bias, w0, b0)
+    hist = []
+    for t in range(1, steps + 1):
+        x = W.layer_inputs(cfg, 0, t)
+        orc.step_kron(st, x["a"], x["g"], x["grad_w"], x["grad_b"])
+        hist.append((st.A.copy(), st.Ainv.copy(), st.W.copy()))
+    return cfg, st, hist
+
+
+def test_refresh_schedule():
+    _, _, hist = _c1_run(steps=8, invert_every=3)
+    refreshed = [t for t in range(1, 8) if not np.array_equal(hist[t][1], hist[t - 1][1])]
+    assert [t + 1 for t in refreshed] == [4, 7]                 # steps 1, 4, 7 refresh
+
+
+def test_ema_init_first_and_zero():
+    cfg = W.get_config("c1")
+    x = W.layer_inputs(cfg, 0, 1)
+    _, st, _ = _c1_run(steps=1, ema_init="first")
+    assert np.allclose(st.A, O.factor(x["a"], 1), rtol=1e-15)
+    _, st, _ = _c1_run(steps=1, ema_init="zero")
+    assert np.allclose(st.A, 0.05 * O.factor(x["a"], 1), rtol=1e-14)
+
+
+def test_c1_golden_trajectory():
+    """Regression record of the oracle's c1 run (written by tests/golden/make_golden.py)."""
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "c1_oracle_trajectory.npz")
+    ref = np.load(path)
+    _, st, hist = _c1_run()
+    for t in range(10):
+        assert np.allclose(hist[t][2], ref["W"][t], rtol=1e-12, atol=1e-15)
+    assert np.allclose(st.A, ref["A"], rtol=1e-12, atol=1e-15)
