@@ -1,0 +1,482 @@
+"""Benchmark of the Kronecker-factored optimizer step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mlp4|...] [--impl reference]
+
+One step = the whole hot path over one batch of synthetic inputs:
+  K1  factor update (A and G, EMA) for every KRON layer
+  K2+K3 damped inverses of every factor, on the steps the refresh cadence selects
+  K4  precondition + fused momentum / weight-decay update for every KRON layer
+  K5+K6 diagonal factors + fused diagonal step for every DIAG layer (for layer
+        sets without DIAG layers, the diagonal twins of the KRON layers)
+Inputs are resident in HBM when the timed region starts; L2 is flushed between
+steps outside the per-step CUDA events.  Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as Wl  # noqa: E402
+
+METRIC = "K-FAC precond steps/s; factor-GEMM TFLOP/s & diag-step GB/s vs GB300 peak"
+WORKLOADS = {"mlp4": "c2", "single_linear": "c1", "resnet18": "c3", "resnet50": "c4",
+             "resnet50_bf16": "c4bf16", "transformer4": "c5"}
+# fallback roofline denominators when MEASURED_PEAKS.json is absent
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TF32_PER_BF16 = 1.1 / 2.25          # nominal dense ratio
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # FFMA lanes x 2 flop x max SM clock
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=40)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="mlp4", choices=sorted(WORKLOADS))
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            out = {}
+            for k in FALLBACK:
+                v = d.get(k)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                out[k] = float(v) if v is not None else None
+            if all(v is not None for v in out.values()):
+                return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK), "fallback"
+
+
+def bench_config(workload):
+    cfg = Wl.get_config(WORKLOADS[workload])
+    layers = list(cfg.layers)
+    if not cfg.diag_layers:
+        import dataclasses
+        layers += [dataclasses.replace(l, name=l.name + "_diag", kind="diag") for l in cfg.layers]
+    return cfg, layers
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def algorithmic(layers, k):
+    """Per-step algorithmic flops and bytes of each phase (fp32 state, input dtype as given)."""
+    f = {"factor_flop": 0.0, "factor_bytes": 0.0, "invert_flop": 0.0, "precond_flop": 0.0,
+         "precond_bytes": 0.0, "diag_bytes": 0.0, "diagfac_bytes": 0.0}
+    for l in layers:
+        elt = 2 if l.in_dtype == "bf16" else 4
+        n, o, M = l.n, l.d_out, l.rows
+        if l.kind == "kron":
+            # upper triangle only: M * n(n+1) flop (2 per FMA) per factor
+            f["factor_flop"] += M * n * (n + 1) + M * o * (o + 1)
+            f["factor_bytes"] += M * (l.d_in + o) * elt + 2 * 4 * (n * n + o * o)
+            f["invert_flop"] += (n ** 3 + o ** 3) / k     # Cholesky n^3/3 + L^-1 n^3/3 + X^T X n^3/3
+            f["precond_flop"] += 2 * o * n * n + 2 * o * o * n
+            f["precond_bytes"] += 4 * (n * n + o * o + 2 * o * n) + 4 * 3 * o * n
+        else:
+            f["diag_bytes"] += 20 * o * n + 8 * (o + n)
+            if l.act != "bn":
+                f["diagfac_bytes"] += M * (l.d_in + o) * elt
+    return f
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def blas_threads():
+    """Threads the oracle's BLAS uses (NumPy's bundled OpenBLAS), else the affinity count."""
+    import ctypes
+    try:
+        for line in open("/proc/self/maps"):
+            if "openblas" in line and ".so" in line:
+                lib = ctypes.CDLL(line.split()[-1])
+                for fn in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                           "openblas_get_num_threads"):
+                    if hasattr(lib, fn):
+                        return int(getattr(lib, fn)())
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def oracle_steps_per_s(cfg, layers, budget_s=20.0):
+    """Time the float64 oracle as it stands on a bounded sample of the workload.
+
+    Sample: one K-FAC step of as many KRON layers as fit the budget (factor
+    build, precondition, update) plus one refresh (both damped inverses) of the
+    first of them; the diagonal path of the same layers.  Per-layer times are
+    scaled to the whole layer set, with the refresh amortised by the cadence."""
+    import oracle as O
+    hp = cfg.hp
+    orc = O.KfacOracle(hp.ema_decay, hp.damping, hp.lr, hp.momentum, hp.weight_decay, 1)
+    kron = [l for l in layers if l.kind == "kron"]
+    diag = [l for l in layers if l.kind == "diag"]
+    t_total, sampled, t0 = 0.0, [], time.perf_counter()
+    cost = lambda l: l.rows * (l.n ** 2 + l.d_out ** 2) + l.n ** 3 + l.d_out ** 3
+    per_layer = {}
+    for l in sorted(kron, key=cost)[: max(1, len(kron))]:
+        if time.perf_counter() - t0 > budget_s and sampled:
+            break
+        li = cfg.layers.index(l) if l in cfg.layers else 0
+        x = Wl.layer_inputs(cfg, li, 1, rows=l.rows)
+        st = O.LayerState("kron", l.d_out, l.d_in, l.has_bias,
+                          np.zeros((l.d_out, l.d_in)), np.zeros(l.d_out) if l.has_bias else None)
+        ts = time.perf_counter()
+        st.A = O.ema(st.A, O.factor(x["a"], l.has_bias), orc.xi)
+        st.G = O.ema(st.G, O.factor(x["g"], 0), orc.xi)
+        tf = time.perf_counter()
+        st.Ainv = O.damped_inverse(st.A, orc.gamma)
+        st.Ginv = O.damped_inverse(st.G, orc.gamma)
+        ti = time.perf_counter()
+        P = O.precondition(st.Ginv, O.grad_hat(x["grad_w"], x["grad_b"]), st.Ainv)
+        st.W, st.m = O.momentum_update(P, st.W, st.m, orc.lr, orc.mu, orc.wd)
+        tp = time.perf_counter()
+        per_layer[l.name] = (tf - ts) + (tp - ti) + (ti - tf) / cfg.invert_every
+        sampled.append(l.name)
+    # scale the sampled layers' time to the whole set by the flop-weighted cost
+    done = [l for l in kron if l.name in per_layer]
+    scale = sum(cost(l) for l in kron) / max(1.0, sum(cost(l) for l in done))
+    t_total = sum(per_layer.values()) * scale
+    t_d = 0.0
+    for l in diag[:4]:
+        x = Wl.layer_inputs(cfg, 0, 1, rows=min(l.rows, 4096)) if l.act != "bn" else None
+        st = O.LayerState("diag", l.d_out, l.d_in, l.has_bias, np.zeros((l.d_out, l.d_in)),
+                          np.zeros(l.d_out) if l.has_bias else None)
+        gw = np.zeros((l.d_out, l.d_in))
+        gn, an = np.ones(l.d_out), np.ones(l.n)
+        ts = time.perf_counter()
+        orc.step_diag(st, gn, an, gw, np.zeros(l.d_out) if l.has_bias else None)
+        t_d += time.perf_counter() - ts
+    if diag:
+        t_total += t_d * len(diag) / min(4, len(diag))
+    sample = (f"oracle fp64: factor+precond+update of {len(done)}/{len(kron)} KRON layers "
+              f"({', '.join(sampled[:4])}{'...' if len(sampled) > 4 else ''}) with one refresh "
+              f"amortised by {cfg.invert_every}, diag step of {min(4, len(diag))}/{len(diag)} "
+              f"DIAG layers; scaled to the full layer set by flop-weighted cost")
+    return 1.0 / t_total, sample, time.perf_counter() - t0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank, world, peaks, peak_kind):
+    import torch
+    import second_order_optimizer_gb300 as K
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    cfg, layers = bench_config(args.workload)
+    hp = cfg.hp
+    k = cfg.invert_every
+    kd = lambda l: K.KFAC_BF16 if l.in_dtype == "bf16" else K.KFAC_F32
+    descs = [(K.KFAC_KRON if l.kind == "kron" else K.KFAC_DIAG, l.d_out, l.d_in, l.has_bias, kd(l))
+             for l in layers]
+    max_rows = max(l.rows for l in layers)
+    h = K.Kfac(descs, ema_decay=hp.ema_decay, damping=hp.damping, lr=hp.lr, momentum=hp.momentum,
+               weight_decay=hp.weight_decay, max_rows=max_rows, device=dev)
+    # inputs: two seeded batches per layer, resident in HBM, used alternately
+    base = {l.name.replace("_diag", ""): i for i, l in enumerate(cfg.layers)}
+    srcidx = [base.get(l.name.replace("_diag", ""), i) for i, l in enumerate(layers)]
+    NB = 2
+    data = []
+    for b in range(NB):
+        per = []
+        for li, l in enumerate(layers):
+            x = Wl.layer_inputs_torch(cfg, srcidx[li], 1 + b + 1000 * rank, dev)
+            per.append(x)
+        data.append(per)
+    params = []
+    for li, l in enumerate(layers):
+        w, bb = Wl.initial_params_torch(cfg, srcidx[li], dev)
+        params.append((w.contiguous(), bb))
+    gnew = [torch.empty(l.d_out, device=dev) if l.kind == "diag" else None for l in layers]
+    anew = [torch.empty(l.n, device=dev) if l.kind == "diag" else None for l in layers]
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(t, x, ev=None):
+        if ev: ev[0].record(stream)
+        for li, l in enumerate(layers):
+            if l.kind == "kron":
+                h.update_factors(li, x[li]["a"], x[li]["g"])
+        if ev: ev[1].record(stream)
+        if (t - 1) % k == 0:
+            h.invert(-1)
+        if ev: ev[2].record(stream)
+        for li, l in enumerate(layers):
+            if l.kind == "kron":
+                pw, pb = params[li]
+                h.precondition(li, x[li]["grad_w"], x[li]["grad_b"], None, None, pw, pb)
+        if ev: ev[3].record(stream)
+        for li, l in enumerate(layers):
+            if l.kind == "diag":
+                pw, pb = params[li]
+                if l.act == "bn":
+                    gn, an = x[li]["g_new"], x[li]["a_new"]
+                else:
+                    h.diag_factors(li, x[li]["a"], x[li]["g"], gnew[li], anew[li])
+                    gn, an = gnew[li], anew[li]
+                h.diag_step(li, gn, an, x[li]["grad_w"], x[li]["grad_b"], pw, pb)
+        if ev: ev[4].record(stream)
+
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        step(t, data[t % NB])
+    torch.cuda.synchronize()
+    code = h.get_status()[0]
+    if code:
+        raise RuntimeError(f"device status {code} after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    l0 = K.launch_count()
+    wall0 = time.perf_counter()
+    refreshed = []
+    for i in range(args.steps):
+        t += 1
+        refreshed.append((t - 1) % k == 0)
+        flush.zero_()                         # L2 flush outside the step's events
+        step(t, data[t % NB], evs[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    launches = K.launch_count() - l0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    code = h.get_status()[0]
+    if code:
+        raise RuntimeError(f"device status {code} in the timed region")
+    ph = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
+                   for i in range(args.steps)])  # ms: factor, invert, precond, diag
+    ms_step = float(ph.sum(axis=1).mean())
+    if world > 1:
+        tt = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(tt.item())
+
+    acc = algorithmic(layers, k)
+    phase_ms = ph.mean(axis=0)
+    # invert phase: average over the steps that refreshed
+    refresh_steps = [i for i in range(args.steps) if refreshed[i]]
+    inv_ms_refresh = float(np.mean([ph[i, 1] for i in refresh_steps])) if refresh_steps else 0.0
+    factor_tfs = acc["factor_flop"] / (phase_ms[0] * 1e-3) / 1e12
+    diag_gbs = (acc["diag_bytes"] + acc["diagfac_bytes"]) / (phase_ms[3] * 1e-3) / 1e9 if phase_ms[3] > 0 else 0.0
+    precond_tfs = acc["precond_flop"] / (phase_ms[2] * 1e-3) / 1e12
+    phases = {"factor_ms": round(float(phase_ms[0]), 4), "invert_ms_per_step": round(float(phase_ms[1]), 4),
+              "invert_ms_per_refresh": round(inv_ms_refresh, 4),
+              "precond_ms": round(float(phase_ms[2]), 4), "diag_ms": round(float(phase_ms[3]), 4),
+              "factor_tflops": round(factor_tfs, 3), "precond_tflops": round(precond_tfs, 3),
+              "diag_gbs": round(diag_gbs, 1)}
+    # dominant phase -> roofline
+    names = ["factor", "invert", "precond", "diag"]
+    dom = names[int(np.argmax(phase_ms))]
+    if dom == "diag":
+        roof = {"bound": "hbm", "achieved": round(diag_gbs, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "kernel": "diag_factor_kernel + diag_step_kernel"}
+    else:
+        flop = {"factor": acc["factor_flop"], "invert": acc["invert_flop"] * k,
+                "precond": acc["precond_flop"]}[dom]
+        ms = {"factor": phase_ms[0], "invert": inv_ms_refresh, "precond": phase_ms[2]}[dom]
+        ach = flop / (ms * 1e-3) / 1e12
+        roof = {"bound": "alu", "achieved": round(ach, 3), "peak": round(FP32_ALU_TFLOPS, 1),
+                "unit": "TFLOP/s", "kernel": {"factor": "syrk_simt_kernel",
+                                              "invert": "chol_*/tri_level_*/syrk_simt_kernel",
+                                              "precond": "precond_x_kernel + precond_p_kernel"}[dom]}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = None
+    roof["phase"] = dom
+    roof["peak_source"] = ("derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz"
+                           if roof["bound"] == "alu" else f"{peak_kind} MEASURED_PEAKS / fallback")
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, h, layers, data[0], params, k, t, dev, step)
+    return {
+        "ms_per_step": ms_step, "phases": phases, "roofline": roof, "clocks": clocks,
+        "gpu_launches": int(launches), "wall_s": wall, "e2e": e2e,
+        "config": {"workload": cfg.name + ("+diag_twins" if not cfg.diag_layers else ""),
+                   "kron_layers": sum(l.kind == "kron" for l in layers),
+                   "diag_layers": sum(l.kind == "diag" for l in layers),
+                   "invert_every": k, "max_rows": max_rows,
+                   "l2": "flushed between steps (256 MiB write, outside the per-step events)"},
+    }
+
+
+def run_e2e(args, h, layers, x_dev, params, k, t, dev, step):
+    """Same step through the public API from pinned host buffers: H2D of every input,
+    the step, D2H of every updated parameter, all inside the timed region."""
+    import torch
+    host = []
+    h2d = 0
+    for li, l in enumerate(layers):
+        d = {}
+        for key, v in x_dev[li].items():
+            if v is None:
+                d[key] = None
+                continue
+            hb = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+            hb.copy_(v)
+            d[key] = hb
+            h2d += v.numel() * v.element_size()
+        host.append(d)
+    outs = [(torch.empty(p[0].shape, pin_memory=True),
+             torch.empty(p[1].shape, pin_memory=True) if p[1] is not None else None) for p in params]
+    d2h = sum(p[0].numel() * 4 + (p[1].numel() * 4 if p[1] is not None else 0) for p in params)
+    stage = [{kk: (torch.empty_like(v, device=dev) if v is not None else None)
+              for kk, v in d.items()} for d in host]
+    steps = max(3, min(args.steps, 20))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        t += 1
+        for li in range(len(layers)):
+            for kk, v in host[li].items():
+                if v is not None:
+                    stage[li][kk].copy_(v, non_blocking=True)
+        step(t, stage)
+        for (pw, pb), (ow, ob) in zip(params, outs):
+            ow.copy_(pw, non_blocking=True)
+            if pb is not None:
+                ob.copy_(pb, non_blocking=True)
+        torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": round(1.0 / dt, 3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    peaks, peak_kind = load_peaks()
+    cfg, layers = bench_config(args.workload)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        per_step = []
+        sample = None
+        for _ in range(args.warmup):
+            pass  # the oracle has nothing to warm up
+        t0 = time.perf_counter()
+        for _ in range(max(1, args.steps)):
+            v, sample, _ = oracle_steps_per_s(cfg, layers, budget_s=max(2.0, 60.0 / max(1, args.steps)))
+            per_step.append(1.0 / v)
+            if time.perf_counter() - t0 > 150:
+                break
+        value = 1.0 / statistics.median(per_step)
+        cores = blas_threads()
+        line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "steps/s",
+                "n_gpus": args.gpus, "steps": len(per_step), "warmup": args.warmup,
+                "ms_per_step": round(1e3 / value, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": cfg.name, "invert_every": cfg.invert_every},
+                "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": cores,
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": round(value, 6), "unit": "steps/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    res = run_gpu(args, rank, world, peaks, peak_kind)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sample, spent = oracle_steps_per_s(cfg, layers, budget_s=20.0)
+        cpu = {"value": round(v, 6), "unit": "steps/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": sample, "seconds": round(spent, 1)}
+    if rank == 0:
+        value = world * 1e3 / res["ms_per_step"]
+        line = {"metric": METRIC, "value": round(value, 3), "unit": "steps/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(res["ms_per_step"], 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": res["config"], "phases": res["phases"], "roofline": res["roofline"],
+                "cpu_baseline": cpu, "e2e": res["e2e"], "gpu_launches": res["gpu_launches"],
+                "clocks": res["clocks"], "peaks": {"source": peak_kind, **peaks}}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,191 @@
+/*
+ * kfac.h -- C ABI of the GB300 (sm_103a) Kronecker-factored optimizer step.
+ *
+ * The library computes, per layer, the K-FAC step described in Osawa et al.,
+ * "Large-Scale Distributed Second-Order Optimization Using Kronecker-Factored
+ * Approximate Curvature for Deep Convolutional Neural Networks" (§3.2: the
+ * layer Fisher is approximated by the Kronecker product of a factor A built
+ * from the layer's input activations and a factor G built from its output
+ * gradients, and inverted through the inverses of the two factors), and the
+ * fused diagonal-Fisher step of the CAFIN briefing ("CAFIN: CUDA-accelerated
+ * Adaptive Fisher Information Matrix Network Optimization via GPU-Native
+ * Kernel Fusion", Kernel Fusion Strategy: load gradient and parameter, update
+ * the EMA of the diagonal Fisher blocks, precondition, add momentum and weight
+ * decay, write the parameter in place).
+ *
+ * Notation per layer: d_in input width, n = d_in + has_bias (A is n x n),
+ * o = d_out (G is o x o), M rows (batch; B*H_out*W_out for an unfolded
+ * convolution; tokens), s = factor scale (default 1/M), xi EMA decay, gamma
+ * damping, eta learning rate, mu momentum, lambda weight decay.
+ *
+ * Conventions for every entry point:
+ *   - Matrices are row-major.  "ld" arguments are leading dimensions in
+ *     elements (>= the row length).
+ *   - Every device pointer is owned by the caller.  The library allocates no
+ *     device memory: all state (factors, inverses, momentum, diagonal vectors,
+ *     status word) and all scratch live in the caller's workspace, whose size
+ *     kfac_workspace_size() returns.  Device pointers must be aligned to their
+ *     element size; 16-byte alignment enables the vectorised paths.
+ *   - Work is enqueued on the given stream and the call returns without
+ *     synchronising.  Only kfac_get_status() synchronises.
+ *   - Argument and state errors are returned synchronously and enqueue nothing.
+ *     Errors found on the device (a non positive-definite pivot, a pipeline
+ *     wait that timed out) are recorded in a device status word and reported by
+ *     kfac_get_status().  NaN inputs propagate; they are not checked.
+ *   - A handle is not thread-safe.  Calls on one handle must be ordered (same
+ *     stream, or streams the caller orders).
+ */
+#ifndef KFAC_H
+#define KFAC_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KFAC_OK = 0,
+  KFAC_ERR_INVALID_ARG = 1,  /* bad pointer, size, layer index or hparam          */
+  KFAC_ERR_WORKSPACE = 2,    /* workspace too small or misaligned                  */
+  KFAC_ERR_STATE = 3,        /* e.g. precondition before the first invert          */
+  KFAC_ERR_NOT_PD = 4,       /* device: damped factor not positive definite        */
+  KFAC_ERR_TIMEOUT = 5,      /* device: a bounded pipeline wait gave up            */
+  KFAC_ERR_CUDA = 6,         /* a CUDA runtime call or launch failed               */
+  KFAC_ERR_UNSUPPORTED = 7   /* valid request this build does not implement        */
+} kfac_status;
+
+typedef enum { KFAC_KRON = 0, KFAC_DIAG = 1 } kfac_kind;
+typedef enum { KFAC_F32 = 0, KFAC_BF16 = 1 } kfac_dtype;
+/* Arithmetic of the preconditioning GEMMs.  3XTF32: fp32 operands split into
+ * two TF32 halves, three tensor-core products, fp32 accumulation (matches fp32
+ * to ~1e-6).  BF16: inverses and gradients rounded to bf16, fp32 accumulation. */
+typedef enum { KFAC_MATH_3XTF32 = 0, KFAC_MATH_BF16 = 1 } kfac_math;
+/* Start of the running averages: ZERO gives F_1 = (1-xi) F_new; FIRST gives F_1 = F_new. */
+typedef enum { KFAC_EMA_INIT_ZERO = 0, KFAC_EMA_INIT_FIRST = 1 } kfac_ema_init;
+
+typedef struct {
+  int kind;      /* kfac_kind                                                     */
+  int d_out;     /* o >= 1                                                        */
+  int d_in;      /* >= 1                                                          */
+  int has_bias;  /* 0/1: bias is the last column of W-hat = [W | b]; a gets a ones column */
+  int in_dtype;  /* kfac_dtype of the activations a and output gradients g (KRON)  */
+} kfac_layer_desc;
+
+typedef struct {
+  double ema_decay;     /* xi in [0,1): F <- xi F + (1-xi) F_new                     */
+  double damping;       /* gamma > 0: KRON inverts F + sqrt(gamma) I; DIAG divides by g a + gamma */
+  double lr;            /* eta                                                       */
+  double momentum;      /* mu                                                        */
+  double weight_decay;  /* lambda: u = P + lambda W ; m <- mu m + u ; W <- W - eta m */
+  int ema_init;         /* kfac_ema_init                                             */
+  int math;             /* kfac_math                                                 */
+} kfac_hparams;
+
+typedef struct kfac_ctx* kfac_handle;
+
+/* Which piece of per-layer state kfac_state_info() locates (all fp32, row-major). */
+typedef enum {
+  KFAC_STATE_A = 0,      /* KRON: running A, n x n, full symmetric                 */
+  KFAC_STATE_G = 1,      /* KRON: running G, o x o                                 */
+  KFAC_STATE_AINV = 2,   /* KRON: (A + sqrt(gamma) I)^{-1} of the latest refresh    */
+  KFAC_STATE_GINV = 3,   /* KRON: (G + sqrt(gamma) I)^{-1}                          */
+  KFAC_STATE_MOMENTUM = 4,  /* both: m, weight part [o x d_in] then bias part [o]  */
+  KFAC_STATE_GDIAG = 5,  /* DIAG: running g diagonal, o                             */
+  KFAC_STATE_ADIAG = 6   /* DIAG: running a diagonal, n                             */
+} kfac_state_which;
+
+/* Bytes of device workspace needed for these layers (256-byte multiple).
+ * max_rows: the largest M any kfac_update_factors / kfac_diag_factors call
+ * will pass for any layer (sizes the row-block scratch). */
+kfac_status kfac_workspace_size(const kfac_layer_desc* layers, int n_layers,
+                                const kfac_hparams* hp, int64_t max_rows, size_t* bytes);
+
+/* Create a handle over a caller-owned workspace (>= kfac_workspace_size bytes,
+ * 256-byte aligned).  Zero-fills all state (synchronously, on the legacy
+ * default stream) and records the layer table.  The device that is current at
+ * this call is the device of every later call. */
+kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_hparams* hp,
+                        int64_t max_rows, void* d_workspace, size_t bytes, kfac_handle* out);
+
+/* Replace the hyper-parameters (schedules such as warm-up damping).  The new
+ * damping takes effect at the next kfac_invert. */
+kfac_status kfac_set_hparams(kfac_handle h, const kfac_hparams* hp);
+
+/* K1: fold new factors into the running A and G of a KRON layer.
+ *   A <- xi A + (1-xi) s [a 1]^T [a 1]     (ones column only if has_bias)
+ *   G <- xi G + (1-xi) s g^T g
+ * a: [rows x d_in] with leading dimension lda; g: [rows x d_out], ldg; both of
+ * the layer's in_dtype.  scale <= 0 means s = 1/rows.  1 <= rows <= max_rows.
+ * Osawa et al. §3.2 (factors), §3.4 (symmetry: only the upper triangle is
+ * computed; the lower is its mirror); CAFIN Introduction (EMA of the factors). */
+kfac_status kfac_update_factors(kfac_handle h, int layer, const void* a, int64_t lda,
+                                const void* g, int64_t ldg, int64_t rows, double scale,
+                                cudaStream_t stream);
+
+/* K5: new diagonal factors of a layer from its a and g (any kind):
+ *   g_new[i] = s sum_r g[r,i]^2 (o entries); a_new[j] = s sum_r a[r,j]^2, and
+ *   a_new[d_in] = s*rows when has_bias (n entries).  Written to caller buffers.
+ * CAFIN Introduction (AdaFisher's diagonal Kronecker factors). */
+kfac_status kfac_diag_factors(kfac_handle h, int layer, const void* a, int64_t lda,
+                              const void* g, int64_t ldg, int64_t rows, double scale,
+                              float* g_new, float* a_new, cudaStream_t stream);
+
+/* K2+K3: damped inverses (F + sqrt(gamma) I)^{-1} for F in {A, G} of one KRON
+ * layer, or of every KRON layer when layer == -1 (one batched pass), by
+ * blocked Cholesky and a blocked triangular inverse.  A non positive-definite
+ * pivot sets KFAC_ERR_NOT_PD in the status word (layer, 0-based column).
+ * Osawa et al. §3.2 (inverse through the factor inverses), §5.4 (refresh
+ * every few steps, so this call is made every k-th step by the caller). */
+kfac_status kfac_invert(kfac_handle h, int layer, cudaStream_t stream);
+
+/* K4: preconditioned gradient P = Ginv . [dW | db] . Ainv of a KRON layer.
+ * grad_w: [o x d_in] fp32, ld ldgw; grad_b: [o] (required iff has_bias).
+ * out_w [o x d_in] (ld d_in) / out_b [o]: P, nullable when param_w is given.
+ * param_w [o x d_in] (ld d_in) / param_b [o]: nullable; when given the update
+ *   u = P + lambda W ; m <- mu m + u ; W <- W - eta m   is applied in place
+ * (m is library state).  Returns KFAC_ERR_STATE before the layer's first
+ * kfac_invert.  CAFIN Kernel Fusion Strategy (precondition, momentum, weight
+ * decay, in-place write); Osawa et al. §3.2. */
+kfac_status kfac_precondition(kfac_handle h, int layer, const float* grad_w, int64_t ldgw,
+                              const float* grad_b, float* out_w, float* out_b,
+                              float* param_w, float* param_b, cudaStream_t stream);
+
+/* K6: fused diagonal-Fisher step of a DIAG layer, one streaming pass:
+ *   gs <- xi gs + (1-xi) g_new ; as <- xi as + (1-xi) a_new     (library state)
+ *   P_ij = [dW | db]_ij / (gs_i as_j + gamma)
+ *   u = P + lambda W ; m <- mu m + u ; W <- W - eta m           (W in place)
+ * g_new [o], a_new [n] (e.g. from kfac_diag_factors, or supplied by the caller
+ * for BatchNorm: o = channels, d_in = 1, has_bias = 1, W = scale, b = shift).
+ * grad_w/param_w: [o x d_in] contiguous; grad_b/param_b: [o] iff has_bias.
+ * out_w/out_b: optional copy of P (nullable).  CAFIN Kernel Fusion Strategy;
+ * Osawa et al. §5.4 (BatchNorm Fisher taken as diagonal). */
+kfac_status kfac_diag_step(kfac_handle h, int layer, const float* g_new, const float* a_new,
+                           const float* grad_w, const float* grad_b,
+                           float* param_w, float* param_b, float* out_w, float* out_b,
+                           cudaStream_t stream);
+
+/* Synchronise the device and report the first device-side error since the
+ * last call (then clear it).  bad_layer / info (nullable) receive the layer
+ * and, for KFAC_ERR_NOT_PD, the 0-based column of the failing pivot. */
+kfac_status kfac_get_status(kfac_handle h, int* bad_layer, int* info);
+
+/* Byte offset (within the workspace) and size of one piece of layer state,
+ * for checkpointing through the caller's own copies. */
+kfac_status kfac_state_info(kfac_handle h, int layer, int which, size_t* offset, size_t* bytes);
+
+/* Release the handle (host memory only; the workspace stays the caller's). */
+kfac_status kfac_destroy(kfac_handle h);
+
+/* Static description of a status code. */
+const char* kfac_status_string(kfac_status s);
+
+/* Diagnostics: number of kernels this library has launched in this process. */
+unsigned long long kfac_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KFAC_H */

@@ -1,0 +1,162 @@
+"""Python binding of libkfac (the GB300 Kronecker-factored optimizer step).
+
+Argument marshalling only: every step of the optimizer runs in the library's
+CUDA kernels.  Tensors supply device pointers; the stream is torch's current
+stream unless one is given.  There is no CPU path: if the shared library is
+missing, importing this package raises.
+
+Function names follow the C ABI in include/kfac.h.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+from ._lib import (LIB, KFAC_KRON, KFAC_DIAG, KFAC_F32, KFAC_BF16, KFAC_MATH_3XTF32,
+                   KFAC_MATH_BF16, KFAC_EMA_INIT_ZERO, KFAC_EMA_INIT_FIRST, KFAC_STATE_A,
+                   KFAC_STATE_G, KFAC_STATE_AINV, KFAC_STATE_GINV, KFAC_STATE_MOMENTUM,
+                   KFAC_STATE_GDIAG, KFAC_STATE_ADIAG, LayerDesc, HParams, KfacError,
+                   status_string, launch_count)
+
+__all__ = ["Kfac", "LayerDesc", "HParams", "KfacError", "status_string", "launch_count",
+           "KFAC_KRON", "KFAC_DIAG", "KFAC_F32", "KFAC_BF16", "KFAC_MATH_3XTF32",
+           "KFAC_MATH_BF16", "KFAC_EMA_INIT_ZERO", "KFAC_EMA_INIT_FIRST", "LIB"]
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise KfacError(code, what)
+
+
+class Kfac:
+    """One handle over a workspace tensor that holds all optimizer state.
+
+    ``layers``: sequence of (kind, d_out, d_in, has_bias, in_dtype) tuples or LayerDesc.
+    """
+
+    def __init__(self, layers: Sequence, ema_decay=0.95, damping=1e-3, lr=1e-2, momentum=0.9,
+                 weight_decay=5e-4, ema_init=KFAC_EMA_INIT_ZERO, math=KFAC_MATH_3XTF32,
+                 max_rows: int = 1, device=None):
+        import torch
+        descs = [l if isinstance(l, LayerDesc) else LayerDesc(*l) for l in layers]
+        self.n_layers = len(descs)
+        self._descs = (LayerDesc * self.n_layers)(*descs)
+        self._hp = HParams(ema_decay, damping, lr, momentum, weight_decay, ema_init, math)
+        self.max_rows = int(max_rows)
+        nbytes = ctypes.c_size_t(0)
+        _check(LIB.kfac_workspace_size(self._descs, self.n_layers, ctypes.byref(self._hp),
+                                       self.max_rows, ctypes.byref(nbytes)), "kfac_workspace_size")
+        self.workspace_bytes = nbytes.value
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        # 256-byte alignment: torch's caching allocator returns 512-byte aligned blocks
+        self.workspace = torch.empty(self.workspace_bytes, dtype=torch.uint8, device=dev)
+        self._h = ctypes.c_void_p()
+        with torch.cuda.device(dev):
+            _check(LIB.kfac_create(self._descs, self.n_layers, ctypes.byref(self._hp), self.max_rows,
+                                   ctypes.c_void_p(self.workspace.data_ptr()),
+                                   self.workspace_bytes, ctypes.byref(self._h)), "kfac_create")
+
+    # -- lifecycle -----------------------------------------------------------
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            LIB.kfac_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_hparams(self, ema_decay=None, damping=None, lr=None, momentum=None,
+                    weight_decay=None):
+        hp = self._hp
+        for name, v in (("ema_decay", ema_decay), ("damping", damping), ("lr", lr),
+                        ("momentum", momentum), ("weight_decay", weight_decay)):
+            if v is not None:
+                setattr(hp, name, float(v))
+        _check(LIB.kfac_set_hparams(self._h, ctypes.byref(hp)), "kfac_set_hparams")
+
+    # -- the five verbs ---------------------------------------------------------
+    def update_factors(self, layer: int, a, g, rows: Optional[int] = None, scale: float = 0.0,
+                       stream=None, lda: Optional[int] = None, ldg: Optional[int] = None):
+        rows = a.shape[0] if rows is None else rows
+        lda = a.stride(0) if lda is None else lda
+        ldg = g.stride(0) if ldg is None else ldg
+        _check(LIB.kfac_update_factors(self._h, layer, _ptr(a), lda, _ptr(g), ldg, rows,
+                                       float(scale), _stream(stream)), "kfac_update_factors")
+
+    def diag_factors(self, layer: int, a, g, g_new, a_new, rows: Optional[int] = None,
+                     scale: float = 0.0, stream=None):
+        rows = a.shape[0] if rows is None else rows
+        _check(LIB.kfac_diag_factors(self._h, layer, _ptr(a), a.stride(0), _ptr(g), g.stride(0),
+                                     rows, float(scale), _ptr(g_new), _ptr(a_new),
+                                     _stream(stream)), "kfac_diag_factors")
+
+    def invert(self, layer: int = -1, stream=None):
+        _check(LIB.kfac_invert(self._h, layer, _stream(stream)), "kfac_invert")
+
+    def precondition(self, layer: int, grad_w, grad_b=None, out_w=None, out_b=None,
+                     param_w=None, param_b=None, stream=None):
+        _check(LIB.kfac_precondition(self._h, layer, _ptr(grad_w), grad_w.stride(0), _ptr(grad_b),
+                                     _ptr(out_w), _ptr(out_b), _ptr(param_w), _ptr(param_b),
+                                     _stream(stream)), "kfac_precondition")
+
+    def diag_step(self, layer: int, g_new, a_new, grad_w, grad_b, param_w, param_b,
+                  out_w=None, out_b=None, stream=None):
+        _check(LIB.kfac_diag_step(self._h, layer, _ptr(g_new), _ptr(a_new), _ptr(grad_w),
+                                  _ptr(grad_b), _ptr(param_w), _ptr(param_b), _ptr(out_w),
+                                  _ptr(out_b), _stream(stream)), "kfac_diag_step")
+
+    # -- status and state --------------------------------------------------------
+    def get_status(self):
+        """Synchronises; returns (code, layer, info) of the first device error (code 0: none)."""
+        layer, info = ctypes.c_int(-1), ctypes.c_int(0)
+        code = LIB.kfac_get_status(self._h, ctypes.byref(layer), ctypes.byref(info))
+        return code, layer.value, info.value
+
+    def state_info(self, layer: int, which: int):
+        off, nb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+        _check(LIB.kfac_state_info(self._h, layer, which, ctypes.byref(off), ctypes.byref(nb)),
+               "kfac_state_info")
+        return off.value, nb.value
+
+    def state(self, layer: int, which: int):
+        """A float32 view of one piece of layer state inside the workspace (no copy)."""
+        import torch
+        off, nb = self.state_info(layer, which)
+        d = self._descs[layer]
+        n = d.d_in + d.has_bias
+        v = self.workspace[off:off + nb].view(torch.float32)
+        shapes = {KFAC_STATE_A: (n, n), KFAC_STATE_G: (d.d_out, d.d_out),
+                  KFAC_STATE_AINV: (n, n), KFAC_STATE_GINV: (d.d_out, d.d_out),
+                  KFAC_STATE_GDIAG: (d.d_out,), KFAC_STATE_ADIAG: (n,)}
+        if which == KFAC_STATE_MOMENTUM:
+            return v  # [o*d_in] weight part then [o] bias part
+        return v.view(*shapes[which])
+
+    def momentum(self, layer: int):
+        """(m_w [o, d_in], m_b [o] or None) views of the momentum buffer."""
+        d = self._descs[layer]
+        v = self.state(layer, KFAC_STATE_MOMENTUM)
+        mw = v[:d.d_out * d.d_in].view(d.d_out, d.d_in)
+        mb = v[d.d_out * d.d_in:] if d.has_bias else None
+        return mw, mb

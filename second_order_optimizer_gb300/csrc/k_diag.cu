@@ -1,0 +1,249 @@
+// K5: diagonal factors   g_new[i] = s sum_r g[r,i]^2,  a_new[j] = s sum_r a[r,j]^2 (+ s*M bias)
+// K6: fused diagonal-Fisher step (one streaming pass over the layer's parameters)
+//
+// "CAFIN: CUDA-accelerated Adaptive Fisher Information Matrix Network
+// Optimization via GPU-Native Kernel Fusion", Introduction (AdaFisher keeps
+// diagonal Kronecker factors as EMAs) and Kernel Fusion Strategy (one kernel
+// loads gradient and parameter into registers, updates the EMA of the diagonal
+// Fisher blocks, preconditions, adds momentum and weight decay, and writes the
+// parameter in place).  Osawa et al., §5.4: BatchNorm's Fisher is taken as
+// diagonal, which is the same step with o = channels, d_in = 1 and a bias.
+//
+// K6 reads dW, W, m (12 B/param) and writes W, m (8 B/param): 20 B per
+// parameter at the HBM roofline.  The per-row and per-column EMA factors are
+// recomputed in registers from the old state and the new diagonal; the last
+// CTA to finish (a ticket) stores the new EMA vectors, so one launch suffices
+// and no CTA ever reads a vector another CTA has already overwritten.
+#include "kfac_internal.cuh"
+
+#include <algorithm>
+
+namespace kfac {
+
+namespace {
+
+constexpr int kDiagThreads = 256;
+constexpr int64_t kK5RowsPerSplit = 1024;
+constexpr int kK5Threads = 256;
+
+struct DiagParams {
+  int o, d_in, has_bias;
+  float xi, one_minus_xi, gamma, eta, mu, lambda;
+  const float* g_new;
+  const float* a_new;
+  const float* gw;
+  const float* gb;
+  float* pw;
+  float* pb;
+  float* ow;
+  float* ob;
+  float* mw;  // momentum, weight part [o x d_in]
+  float* mb;  // momentum, bias part [o]
+  float* gs;  // running g diagonal [o]
+  float* as;  // running a diagonal [n]
+  int* ticket;
+};
+
+__device__ __forceinline__ float ema1(float xi, float omx, float old, float nw) {
+  return fmaf(xi, old, omx * nw);
+}
+
+// One parameter: returns the new W, updates m, optionally stores P.
+__device__ __forceinline__ void diag_elem(const DiagParams& p, float gsi, float asj, float gw,
+                                          float& w, float& m, float* pout) {
+  const float pr = gw / fmaf(gsi, asj, p.gamma);
+  const float u = fmaf(p.lambda, w, pr);
+  m = fmaf(p.mu, m, u);
+  w = fmaf(-p.eta, m, w);
+  if (pout) *pout = pr;
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kDiagThreads) diag_step_kernel(DiagParams p) {
+  const int64_t nw = (int64_t)p.o * p.d_in;
+  const int64_t units = VEC ? nw / 4 : nw;
+  const int64_t total = units + (p.has_bias ? p.o : 0);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < total; u += stride) {
+    if (u < units) {
+      if (VEC) {
+        const int64_t e = u * 4;
+        const int i = (int)(e / p.d_in), j = (int)(e % p.d_in);
+        const float gsi = ema1(p.xi, p.one_minus_xi, __ldg(p.gs + i), __ldg(p.g_new + i));
+        const float4 as4 = __ldg(reinterpret_cast<const float4*>(p.as + j));
+        const float4 an4 = __ldg(reinterpret_cast<const float4*>(p.a_new + j));
+        const float4 g4 = __ldcs(reinterpret_cast<const float4*>(p.gw + e));
+        float4 w4 = __ldcs(reinterpret_cast<const float4*>(p.pw + e));
+        float4 m4 = __ldcs(reinterpret_cast<const float4*>(p.mw + e));
+        float4 p4;
+        diag_elem(p, gsi, ema1(p.xi, p.one_minus_xi, as4.x, an4.x), g4.x, w4.x, m4.x, &p4.x);
+        diag_elem(p, gsi, ema1(p.xi, p.one_minus_xi, as4.y, an4.y), g4.y, w4.y, m4.y, &p4.y);
+        diag_elem(p, gsi, ema1(p.xi, p.one_minus_xi, as4.z, an4.z), g4.z, w4.z, m4.z, &p4.z);
+        diag_elem(p, gsi, ema1(p.xi, p.one_minus_xi, as4.w, an4.w), g4.w, w4.w, m4.w, &p4.w);
+        __stcs(reinterpret_cast<float4*>(p.pw + e), w4);
+        __stcs(reinterpret_cast<float4*>(p.mw + e), m4);
+        if (p.ow) __stcs(reinterpret_cast<float4*>(p.ow + e), p4);
+      } else {
+        const int i = (int)(u / p.d_in), j = (int)(u % p.d_in);
+        const float gsi = ema1(p.xi, p.one_minus_xi, p.gs[i], p.g_new[i]);
+        const float asj = ema1(p.xi, p.one_minus_xi, p.as[j], p.a_new[j]);
+        float w = p.pw[u], m = p.mw[u];
+        diag_elem(p, gsi, asj, p.gw[u], w, m, p.ow ? p.ow + u : nullptr);
+        p.pw[u] = w;
+        p.mw[u] = m;
+      }
+    } else {  // bias column j = d_in
+      const int i = (int)(u - units);
+      const float gsi = ema1(p.xi, p.one_minus_xi, p.gs[i], p.g_new[i]);
+      const float asj = ema1(p.xi, p.one_minus_xi, p.as[p.d_in], p.a_new[p.d_in]);
+      float w = p.pb[i], m = p.mb[i];
+      diag_elem(p, gsi, asj, p.gb[i], w, m, p.ob ? p.ob + i : nullptr);
+      p.pb[i] = w;
+      p.mb[i] = m;
+    }
+  }
+  // last CTA stores the new EMA vectors (every other CTA has finished reading them)
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(p.ticket, 1) == (int)gridDim.x - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < p.o; i += blockDim.x)
+    p.gs[i] = ema1(p.xi, p.one_minus_xi, __ldcg(p.gs + i), p.g_new[i]);
+  const int n = p.d_in + p.has_bias;
+  for (int j = threadIdx.x; j < n; j += blockDim.x)
+    p.as[j] = ema1(p.xi, p.one_minus_xi, __ldcg(p.as + j), p.a_new[j]);
+  if (threadIdx.x == 0) *p.ticket = 0;
+}
+
+// K5 ------------------------------------------------------------------------
+struct DiagFactorParams {
+  const void* a;
+  const void* g;
+  int64_t lda, ldg, rows, rows_per_split;
+  int d_in, o, has_bias, splits, col_blocks;
+  float s;
+  float* part;     // [splits][d_in + o]
+  int* tickets;    // [col_blocks]
+  float* g_new;
+  float* a_new;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kK5Threads) diag_factor_kernel(DiagFactorParams p) {
+  const int cb = blockIdx.x, split = blockIdx.y;
+  const int c = cb * kK5Threads + threadIdx.x;   // 0..d_in-1: a columns; d_in..: g columns
+  const int ncols = p.d_in + p.o;
+  const int64_t r0 = (int64_t)split * p.rows_per_split;
+  const int64_t r1 = min(p.rows, r0 + p.rows_per_split);
+  if (c < ncols) {
+    const T* base = c < p.d_in ? static_cast<const T*>(p.a) + c
+                               : static_cast<const T*>(p.g) + (c - p.d_in);
+    const int64_t ld = c < p.d_in ? p.lda : p.ldg;
+    float acc = 0.f;
+    for (int64_t r = r0; r < r1; ++r) {
+      const float v = to_f32<T>(base[r * ld]);
+      acc = fmaf(v, v, acc);
+    }
+    p.part[(size_t)split * ncols + c] = acc;
+  }
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(p.tickets + cb, 1) == p.splits - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (c < ncols) {
+    float v = 0.f;
+    for (int s = 0; s < p.splits; ++s) v += __ldcg(p.part + (size_t)s * ncols + c);
+    v *= p.s;
+    if (c < p.d_in) p.a_new[c] = v;
+    else p.g_new[c - p.d_in] = v;
+  }
+  if (cb == 0 && threadIdx.x == 0 && p.has_bias) p.a_new[p.d_in] = p.s * (float)p.rows;
+  if (threadIdx.x == 0) p.tickets[cb] = 0;
+}
+
+}  // namespace
+
+size_t k5_scratch_floats(int n_plus_o, int64_t max_rows) {
+  return (size_t)cdiv(max_rows, kK5RowsPerSplit) * (size_t)n_plus_o;
+}
+
+kfac_status launch_diag_factors(kfac_ctx* h, int layer, const void* a, int64_t lda,
+                                const void* g, int64_t ldg, int64_t rows, double scale,
+                                float* g_new, float* a_new, cudaStream_t st) {
+  const LayerInfo& L = h->layers[layer];
+  DiagFactorParams p{};
+  p.a = a;
+  p.g = g;
+  p.lda = lda;
+  p.ldg = ldg;
+  p.rows = rows;
+  p.rows_per_split = kK5RowsPerSplit;
+  p.splits = (int)cdiv(rows, kK5RowsPerSplit);
+  p.d_in = L.d_in;
+  p.o = L.o;
+  p.has_bias = L.has_bias;
+  p.col_blocks = (int)cdiv(L.d_in + L.o, kK5Threads);
+  p.s = (float)(scale > 0 ? scale : 1.0 / (double)rows);
+  p.part = h->at<float>(h->off_k5part);
+  p.tickets = h->at<int>(h->off_k5tickets);
+  p.g_new = g_new;
+  p.a_new = a_new;
+  if ((size_t)p.splits * (L.d_in + L.o) > h->k5part_floats) return KFAC_ERR_WORKSPACE;
+  dim3 grid(p.col_blocks, p.splits);
+  if (L.in_dtype == KFAC_BF16)
+    diag_factor_kernel<__nv_bfloat16><<<grid, kK5Threads, 0, st>>>(p);
+  else
+    diag_factor_kernel<float><<<grid, kK5Threads, 0, st>>>(p);
+  count_launch();
+  return check_launch();
+}
+
+kfac_status launch_diag_step(kfac_ctx* h, int layer, float decay, const float* g_new,
+                             const float* a_new, const float* gw, const float* gb, float* pw,
+                             float* pb, float* ow, float* ob, cudaStream_t st) {
+  const LayerInfo& L = h->layers[layer];
+  DiagParams p{};
+  p.o = L.o;
+  p.d_in = L.d_in;
+  p.has_bias = L.has_bias;
+  p.xi = decay;
+  p.one_minus_xi = 1.f - decay;
+  p.gamma = (float)h->hp.damping;
+  p.eta = (float)h->hp.lr;
+  p.mu = (float)h->hp.momentum;
+  p.lambda = (float)h->hp.weight_decay;
+  p.g_new = g_new;
+  p.a_new = a_new;
+  p.gw = gw;
+  p.gb = gb;
+  p.pw = pw;
+  p.pb = pb;
+  p.ow = ow;
+  p.ob = ob;
+  p.mw = h->at<float>(L.m);
+  p.mb = p.mw + (size_t)L.o * L.d_in;
+  p.gs = h->at<float>(L.gs);
+  p.as = h->at<float>(L.as);
+  p.ticket = h->at<int>(L.ticket);
+  auto al16 = [](const void* q) { return ((uintptr_t)q & 15) == 0; };
+  const bool vec = (L.d_in % 4 == 0) && al16(gw) && al16(pw) && al16(p.mw) && al16(p.as) &&
+                   al16(a_new) && (ow == nullptr || al16(ow));
+  const int64_t nw = (int64_t)L.o * L.d_in;
+  const int64_t units = (vec ? nw / 4 : nw) + (L.has_bias ? L.o : 0);
+  int64_t blocks = std::min<int64_t>(cdiv(units, kDiagThreads), (int64_t)kNumSMs * 8);
+  blocks = std::max<int64_t>(blocks, 1);
+  if (vec)
+    diag_step_kernel<true><<<(unsigned)blocks, kDiagThreads, 0, st>>>(p);
+  else
+    diag_step_kernel<false><<<(unsigned)blocks, kDiagThreads, 0, st>>>(p);
+  count_launch();
+  return check_launch();
+}
+
+}  // namespace kfac

@@ -1,0 +1,211 @@
+// K1: running Kronecker factors  F <- beta F + alpha x-hat^T x-hat  (upper triangle + mirror).
+//
+// Osawa et al., "Large-Scale Distributed Second-Order Optimization Using
+// Kronecker-Factored Approximate Curvature ...", §3.2 (A from the layer's input
+// activations, G from its output gradients) and §3.4 (a symmetric factor has
+// N(N+1)/2 distinct entries: only tiles on or above the diagonal are computed,
+// the epilogue writes each entry and its mirror).  The EMA of the CAFIN
+// briefing (Introduction) is the epilogue's beta*F_old + alpha*acc with
+// alpha = (1-xi) s, beta = xi.
+//
+// This translation unit holds the CUDA-core (FP32 FFMA) grouped SYRK used for
+// the inverse assembly Finv = X^T X and, for the factor update, whenever the
+// tensor-core path does not apply.  Split-K partial tiles are reduced by the
+// last CTA of each tile (a per-tile ticket), in fixed split order, so the
+// result is deterministic and no separate reduction launch is needed.
+#include "kfac_internal.cuh"
+#include "simt_gemm.cuh"
+#include "syrk_simt.cuh"
+
+#include <algorithm>
+
+namespace kfac {
+
+namespace {
+
+template <typename T>
+struct XhatLoader {  // (col, row) -> x-hat[row][col]
+  const T* x;
+  int64_t ld, M;
+  int d, n;
+  __device__ __forceinline__ float operator()(long long col, long long row) const {
+    if (row >= M || col >= n) return 0.f;
+    if (col >= d) return 1.f;  // the ones column (only present when n > d)
+    return to_f32<T>(x[row * ld + col]);
+  }
+};
+template <typename T>
+struct XhatLoaderT {  // (row, col) -> x-hat[row][col]
+  XhatLoader<T> l;
+  __device__ __forceinline__ float operator()(long long row, long long col) const {
+    return l(col, row);
+  }
+};
+
+__device__ __forceinline__ void tile_coords(int t, int nt, int* ti, int* tj) {
+  int r = 0;
+  while (t >= nt - r) {
+    t -= nt - r;
+    ++r;
+  }
+  *ti = r;
+  *tj = r + t;
+}
+
+__device__ __forceinline__ void syrk_store(const SyrkJob& j, int64_t gr, int64_t gc, float acc) {
+  if (gr >= j.n || gc >= j.n || gr > gc) return;
+  float* p = j.C + gr * j.n + gc;
+  float v = j.alpha * acc;
+  if (j.beta != 0.f) v = fmaf(j.beta, *p, v);
+  *p = v;
+  if (gr != gc) j.C[gc * j.n + gr] = v;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(SyrkTile::Tile::kThreads)
+syrk_simt_kernel(const SyrkJob* __restrict__ jobs, SyrkJob job0) {
+  using Tile = SyrkTile::Tile;
+  constexpr int BM = SyrkTile::BM, BN = SyrkTile::BN, TM = SyrkTile::TM, TN = SyrkTile::TN;
+  __shared__ float smem[Tile::kSmemFloats];
+  __shared__ int s_last;
+  const SyrkJob j = jobs ? jobs[blockIdx.y] : job0;
+  const int tiles = j.nt * (j.nt + 1) / 2;
+  if ((int)blockIdx.x >= tiles * j.splits) return;
+  const int tile = blockIdx.x / j.splits, split = blockIdx.x % j.splits;
+  int ti, tj;
+  tile_coords(tile, j.nt, &ti, &tj);
+  int64_t r0 = (int64_t)split * j.rows_per_split;
+  int64_t r1 = min(j.M, r0 + j.rows_per_split);
+  if (j.x_lower) r0 = max(r0, (int64_t)tj * BN);  // x[r][c] = 0 for r < c
+  float acc[TM][TN];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int k = 0; k < TN; ++k) acc[i][k] = 0.f;
+  XhatLoader<T> la{static_cast<const T*>(j.x), j.ld, j.M, j.d, j.n};
+  XhatLoaderT<T> lb{la};
+  if (r0 < r1) Tile::run(la, lb, (long long)ti * BM, (long long)tj * BN, r0, r1, acc, smem);
+
+  if (j.splits == 1) {
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+      for (int k = 0; k < TN; ++k)
+        syrk_store(j, (int64_t)ti * BM + Tile::row_of(i), (int64_t)tj * BN + Tile::col_of(k),
+                   acc[i][k]);
+    return;
+  }
+  float* part = j.part + (size_t)tile * j.splits * (BM * BN);
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int k = 0; k < TN; ++k)
+      part[(size_t)split * (BM * BN) + Tile::row_of(i) * BN + Tile::col_of(k)] = acc[i][k];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(&j.tickets[tile], 1) == j.splits - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int k = 0; k < TN; ++k) {
+      const int e = Tile::row_of(i) * BN + Tile::col_of(k);
+      float v = 0.f;
+      for (int s = 0; s < j.splits; ++s) v += __ldcg(part + (size_t)s * (BM * BN) + e);
+      syrk_store(j, (int64_t)ti * BM + Tile::row_of(i), (int64_t)tj * BN + Tile::col_of(k), v);
+    }
+  if (threadIdx.x == 0) j.tickets[tile] = 0;
+}
+
+}  // namespace
+
+kfac_status launch_syrk_simt(const SyrkJob* job, int njobs, bool bf16, cudaStream_t st) {
+  if (njobs != 1) return KFAC_ERR_INVALID_ARG;
+  const int tiles = job->nt * (job->nt + 1) / 2;
+  dim3 grid(tiles * job->splits, 1);
+  if (bf16)
+    syrk_simt_kernel<__nv_bfloat16><<<grid, SyrkTile::Tile::kThreads, 0, st>>>(nullptr, *job);
+  else
+    syrk_simt_kernel<float><<<grid, SyrkTile::Tile::kThreads, 0, st>>>(nullptr, *job);
+  count_launch();
+  return check_launch();
+}
+
+kfac_status launch_syrk_simt_grouped(const SyrkJob* d_jobs, int njobs, int max_tiles,
+                                     cudaStream_t st) {
+  if (njobs <= 0) return KFAC_OK;
+  dim3 grid(max_tiles, njobs);
+  syrk_simt_kernel<float><<<grid, SyrkTile::Tile::kThreads, 0, st>>>(d_jobs, SyrkJob{});
+  count_launch();
+  return check_launch();
+}
+
+namespace {
+constexpr int kTargetCtas = 2 * kNumSMs;
+constexpr int64_t kMaxRowsPerSplit = 8192;
+constexpr int64_t kMinRowsPerSplit = 256;
+}  // namespace
+
+// Split plan shared by the planner (scratch sizing) and the launcher: enough
+// CTAs to fill the GPU twice, at least kMinRowsPerSplit rows per split, and at
+// most kMaxRowsPerSplit rows summed by one thread (bounds fp32 error growth).
+static int64_t split_count_before_rounding(int n, int64_t rows) {
+  int nt = (int)cdiv(n, SyrkTile::BM);
+  int64_t tiles = (int64_t)nt * (nt + 1) / 2;
+  int64_t s = cdiv(kTargetCtas, tiles);
+  s = std::min<int64_t>(s, std::max<int64_t>(1, rows / kMinRowsPerSplit));
+  s = std::max<int64_t>(s, cdiv(rows, kMaxRowsPerSplit));
+  return std::max<int64_t>(s, 1);
+}
+
+void syrk_split_plan(int n, int64_t rows, int* splits_out, int64_t* rows_per_split_out) {
+  int64_t s = split_count_before_rounding(n, rows);
+  int64_t rps = cdiv(cdiv(rows, s), SyrkTile::BK) * SyrkTile::BK;
+  *splits_out = (int)cdiv(rows, rps);
+  *rows_per_split_out = rps;
+}
+
+size_t k1_scratch_floats(int n, int64_t max_rows, size_t* tickets) {
+  int nt = (int)cdiv(n, SyrkTile::BM);
+  int64_t tiles = (int64_t)nt * (nt + 1) / 2;
+  *tickets = (size_t)tiles;
+  // the split count never exceeds its value before rounding, which grows with rows
+  int64_t s = split_count_before_rounding(n, max_rows);
+  return s > 1 ? (size_t)(tiles * s) * SyrkTile::BM * SyrkTile::BN : 0;
+}
+
+kfac_status launch_update_factors(kfac_ctx* h, int layer, const void* a, int64_t lda,
+                                  const void* g, int64_t ldg, int64_t rows, double scale,
+                                  float decay, cudaStream_t st) {
+  const LayerInfo& L = h->layers[layer];
+  const double s = scale > 0 ? scale : 1.0 / (double)rows;
+  const float alpha = (float)((1.0 - (double)decay) * s);
+  for (int which = 0; which < 2; ++which) {
+    SyrkJob j{};
+    j.x = which == 0 ? a : g;
+    j.ld = which == 0 ? lda : ldg;
+    j.M = rows;
+    j.d = which == 0 ? L.d_in : L.o;
+    j.n = which == 0 ? L.n : L.o;
+    j.has_bias = which == 0 ? L.has_bias : 0;
+    j.x_lower = 0;
+    j.alpha = alpha;
+    j.beta = decay;
+    j.C = h->at<float>(which == 0 ? L.A : L.G);
+    j.nt = (int)cdiv(j.n, SyrkTile::BM);
+    syrk_split_plan(j.n, rows, &j.splits, &j.rows_per_split);
+    j.part = h->at<float>(h->off_part);
+    j.tickets = h->at<int>(h->off_tickets);
+    int64_t tiles = (int64_t)j.nt * (j.nt + 1) / 2;
+    if (j.splits > 1 &&
+        (size_t)(tiles * j.splits) * SyrkTile::BM * SyrkTile::BN > h->part_floats)
+      return KFAC_ERR_WORKSPACE;
+    kfac_status e = launch_syrk_simt(&j, 1, L.in_dtype == KFAC_BF16, st);
+    if (e != KFAC_OK) return e;
+  }
+  return KFAC_OK;
+}
+
+}  // namespace kfac

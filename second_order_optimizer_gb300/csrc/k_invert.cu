@@ -1,0 +1,293 @@
+// K2 + K3: damped inverses  F_d^{-1} = (F + sqrt(gamma) I)^{-1}  for every factor, batched.
+//
+// Osawa et al., "Large-Scale Distributed Second-Order Optimization Using
+// Kronecker-Factored Approximate Curvature ...", §3.2: the inverse of the
+// Kronecker-factored Fisher is taken through the inverses of the two factors;
+// §3.3 notes that this inverse work is the main overhead of K-FAC, and §5.4
+// that it need not be refreshed every step (the caller decides the cadence).
+// The pages give no inversion algorithm; this file uses the standard one for
+// symmetric positive-definite matrices:
+//
+//   1. L = lower(F) + sqrt(gamma) I                                 (prep)
+//   2. blocked right-looking Cholesky, block nb = 64, per block column k:
+//        diag:     L_kk = chol(L_kk) in shared memory; X_kk = L_kk^{-1}
+//        panel:    L_ik <- L_ik L_kk^{-T}                 (i > k)
+//        trailing: L_ij <- L_ij - L_ik L_jk^T              (i >= j > k, lower tiles)
+//   3. X = L^{-1} by recursive doubling over block pairs:
+//        X_BT = -X_BB (L_BT X_TT)        for pairs (T, B) of size s = 64, 128, ...
+//   4. F_d^{-1} = X^T X  (grouped SYRK, upper tiles + mirror)
+//
+// Every matrix of the batch runs the same step sequence; a matrix whose size
+// is already exhausted at a step returns at once.  A pivot that is not > 0 (or
+// not finite) is reported as KFAC_ERR_NOT_PD with its 0-based column, replaced
+// by 1 so the rest of the pass stays finite, and the result is flagged.
+#include "kfac_internal.cuh"
+#include "simt_gemm.cuh"
+#include "syrk_simt.cuh"
+
+#include <algorithm>
+
+namespace kfac {
+
+namespace {
+
+constexpr int NB = 64;
+using PTile = SimtTile<64, 64, 16, 4, 4>;   // 256 threads
+
+__global__ void __launch_bounds__(256) inv_prep_kernel(const InvJob* jobs, float sqrt_gamma) {
+  const InvJob J = jobs[blockIdx.y];
+  const int64_t nn = (int64_t)J.n * J.n;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / J.n, c = e % J.n;
+    float v = 0.f;
+    if (r > c) v = J.F[e];
+    else if (r == c) v = J.F[e] + sqrt_gamma;
+    J.L[e] = v;
+    J.X[e] = 0.f;
+  }
+}
+
+__global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int k,
+                                                        DevStatus* st) {
+  const InvJob J = jobs[blockIdx.x];
+  if (k >= J.n) return;
+  const int b = min(NB, J.n - k);
+  const int n = J.n;
+  __shared__ float S[NB][NB + 1];
+  __shared__ float T[NB][NB + 1];
+  const int tid = threadIdx.x;
+  for (int e = tid; e < NB * NB; e += blockDim.x) {
+    const int r = e / NB, c = e % NB;
+    S[r][c] = (r < b && c <= r) ? J.L[(int64_t)(k + r) * n + k + c] : 0.f;
+    T[r][c] = 0.f;
+  }
+  __syncthreads();
+  for (int j = 0; j < b; ++j) {
+    if (tid == 0) {
+      float d = S[j][j];
+      if (!(d > 0.f) || !isfinite(d)) {
+        report_error(st, KFAC_ERR_NOT_PD, J.layer, k + j);
+        d = 1.f;
+      }
+      S[j][j] = sqrtf(d);
+    }
+    __syncthreads();
+    const float piv = S[j][j];
+    for (int i = j + 1 + tid; i < b; i += blockDim.x) S[i][j] = S[i][j] / piv;
+    __syncthreads();
+    const int w = b - j - 1;
+    for (int e = tid; e < w * w; e += blockDim.x) {
+      const int r = j + 1 + e / w, c = j + 1 + e % w;
+      if (c <= r) S[r][c] = fmaf(-S[r][j], S[c][j], S[r][c]);
+    }
+    __syncthreads();
+  }
+  // T = S^{-1}: thread c forms column c by forward substitution
+  if (tid < b) {
+    const int c = tid;
+    for (int i = c; i < b; ++i) {
+      float v = (i == c) ? 1.f : 0.f;
+      for (int t = c; t < i; ++t) v = fmaf(-S[i][t], T[t][c], v);
+      T[i][c] = v / S[i][i];
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < b * b; e += blockDim.x) {
+    const int r = e / b, c = e % b;
+    const int64_t g = (int64_t)(k + r) * n + k + c;
+    J.L[g] = (c <= r) ? S[r][c] : 0.f;
+    J.X[g] = (c <= r) ? T[r][c] : 0.f;
+  }
+}
+
+// L[i, k:k+b] <- L[i, k:k+b] . X_kk^T for rows i in [k+b, n); one CTA owns a
+// 64-row block and all b <= 64 columns, so the in-place update is race-free.
+__global__ void __launch_bounds__(256) chol_panel_kernel(const InvJob* jobs, int k) {
+  const InvJob J = jobs[blockIdx.y];
+  const int n = J.n;
+  if (k + NB >= n) return;  // no rows below the last diagonal block
+  const int b = NB;
+  const int64_t r0 = (int64_t)k + b + (int64_t)blockIdx.x * 64;
+  if (r0 >= n) return;
+  __shared__ float smem[PTile::kSmemFloats];
+  float acc[4][4] = {};
+  StridedLoader la{J.L + k, n, 1, n, b};                       // (r, t) -> L[r][k+t]
+  StridedLoader lb{J.X + (int64_t)k * n + k, 1, n, b, b};      // (t, c) -> X[k+c][k+t]
+  PTile::run(la, lb, r0, 0, 0, b, acc, smem);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t r = r0 + PTile::row_of(i);
+      const int c = PTile::col_of(j);
+      if (r < n && c < b) J.L[r * n + k + c] = acc[i][j];
+    }
+}
+
+__device__ __forceinline__ void lower_tile_coords(int t, int* ti, int* tj) {
+  // t enumerates (ti, tj) with tj <= ti row by row: (0,0), (1,0), (1,1), (2,0), ...
+  int r = 0;
+  while (t > r) {
+    t -= r + 1;
+    ++r;
+  }
+  *ti = r;
+  *tj = t;
+}
+
+// L[i][j] -= sum_t L[i][k+t] L[j][k+t] over the trailing lower tiles.
+__global__ void __launch_bounds__(256) chol_trailing_kernel(const InvJob* jobs, int k) {
+  const InvJob J = jobs[blockIdx.y];
+  const int n = J.n;
+  const int64_t base = (int64_t)k + NB;
+  if (base >= n) return;
+  const int nt = (int)((n - base + 63) / 64);
+  if ((int)blockIdx.x >= nt * (nt + 1) / 2) return;
+  int ti, tj;
+  lower_tile_coords(blockIdx.x, &ti, &tj);
+  __shared__ float smem[PTile::kSmemFloats];
+  float acc[4][4] = {};
+  StridedLoader la{J.L + k, n, 1, n, NB};   // (i, t) -> L[i][k+t]
+  StridedLoader lb{J.L + k, 1, n, NB, n};   // (t, j) -> L[j][k+t]
+  PTile::run(la, lb, base + ti * 64, base + tj * 64, 0, NB, acc, smem);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t r = base + ti * 64 + PTile::row_of(i);
+      const int64_t c = base + tj * 64 + PTile::col_of(j);
+      if (r < n && c < n) J.L[r * n + c] -= acc[i][j];
+    }
+}
+
+// Locate the (pair, tile) of a CTA at doubling level s.  Pair p: T = [2ps, (2p+1)s),
+// B = [(2p+1)s, min((2p+2)s, n)); tiles cover B rows x T cols in 64 x 64 blocks.
+__device__ __forceinline__ bool level_tile(int n, int s, int t, int* T0, int* B0, int* B1,
+                                           int* tr, int* tc) {
+  for (int p = 0;; ++p) {
+    const int t0 = 2 * p * s, b0 = t0 + s;
+    if (b0 >= n) return false;
+    const int b1 = min(b0 + s, n);
+    const int rows = (b1 - b0 + 63) / 64, cols = s / 64;
+    if (t < rows * cols) {
+      *T0 = t0;
+      *B0 = b0;
+      *B1 = b1;
+      *tr = t / cols;
+      *tc = t % cols;
+      return true;
+    }
+    t -= rows * cols;
+  }
+}
+
+// Y[r][c] = sum_{t in T, t >= c} L[r][t] X[t][c]      (r in B, c in T)
+__global__ void __launch_bounds__(256) tri_level_y_kernel(const InvJob* jobs, int s) {
+  const InvJob J = jobs[blockIdx.y];
+  const int n = J.n;
+  int T0, B0, B1, tr, tc;
+  if (!level_tile(n, s, blockIdx.x, &T0, &B0, &B1, &tr, &tc)) return;
+  __shared__ float smem[PTile::kSmemFloats];
+  float acc[4][4] = {};
+  StridedLoader la{J.L, n, 1, B1, T0 + s};   // (r, t) -> L[r][t]
+  StridedLoader lb{J.X, n, 1, T0 + s, T0 + s};  // (t, c) -> X[t][c]
+  const int64_t m0 = B0 + tr * 64, c0 = T0 + tc * 64;
+  PTile::run(la, lb, m0, c0, c0, T0 + s, acc, smem);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t r = m0 + PTile::row_of(i), c = c0 + PTile::col_of(j);
+      if (r < B1) J.Y[r * n + c] = acc[i][j];
+    }
+}
+
+// X[r][c] = -sum_{t in B, t <= r} X[r][t] Y[t][c]      (r in B, c in T)
+__global__ void __launch_bounds__(256) tri_level_x_kernel(const InvJob* jobs, int s) {
+  const InvJob J = jobs[blockIdx.y];
+  const int n = J.n;
+  int T0, B0, B1, tr, tc;
+  if (!level_tile(n, s, blockIdx.x, &T0, &B0, &B1, &tr, &tc)) return;
+  __shared__ float smem[PTile::kSmemFloats];
+  float acc[4][4] = {};
+  StridedLoader la{J.X, n, 1, B1, B1};      // (r, t) -> X[r][t]
+  StridedLoader lb{J.Y, n, 1, B1, T0 + s};  // (t, c) -> Y[t][c]
+  const int64_t m0 = B0 + tr * 64, c0 = T0 + tc * 64;
+  const int64_t k1 = m0 + 64 < (int64_t)B1 ? m0 + 64 : (int64_t)B1;
+  PTile::run(la, lb, m0, c0, B0, k1, acc, smem);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t r = m0 + PTile::row_of(i), c = c0 + PTile::col_of(j);
+      if (r < B1) J.X[r * n + c] = -acc[i][j];
+    }
+}
+
+int level_tiles_host(int n, int s) {
+  int total = 0;
+  for (int p = 0;; ++p) {
+    const int b0 = (2 * p + 1) * s;
+    if (b0 >= n) break;
+    const int b1 = std::min(b0 + s, n);
+    total += ((b1 - b0 + 63) / 64) * (s / 64);
+  }
+  return total;
+}
+
+}  // namespace
+
+size_t inv_y_floats(int n) { return (size_t)n * n; }
+
+kfac_status launch_invert(kfac_ctx* h, int layer, cudaStream_t st) {
+  // job range: all KRON factors, or the two of one layer
+  const InvJob* d_all = h->at<InvJob>(h->off_invjobs);
+  const SyrkJob* d_syrk = h->at<SyrkJob>(h->off_invjobs + align_up(sizeof(InvJob) * h->n_invjobs));
+  int j0 = 0, nj = h->n_invjobs;
+  if (layer >= 0) {
+    j0 = -1;
+    for (int i = 0; i < h->n_invjobs; ++i)
+      if (h->invjobs_host[i].layer == layer) {
+        j0 = i;
+        break;
+      }
+    if (j0 < 0) return KFAC_ERR_INVALID_ARG;
+    nj = 2;
+  }
+  int nmax = 0;
+  for (int i = j0; i < j0 + nj; ++i) nmax = std::max(nmax, h->invjobs_host[i].n);
+  const InvJob* jobs = d_all + j0;
+  const float sg = (float)std::sqrt(h->hp.damping);
+
+  inv_prep_kernel<<<dim3((unsigned)std::min<int64_t>(cdiv((int64_t)nmax * nmax, 256), 1024), nj),
+                    256, 0, st>>>(jobs, sg);
+  count_launch();
+  if (kfac_status e = check_launch()) return e;
+
+  for (int k = 0; k < nmax; k += NB) {
+    chol_diag_kernel<<<nj, 256, 0, st>>>(jobs, k, h->status());
+    count_launch();
+    const int rest = nmax - k - NB;
+    if (rest > 0) {
+      const int rb = (int)cdiv(rest, 64);
+      chol_panel_kernel<<<dim3(rb, nj), 256, 0, st>>>(jobs, k);
+      chol_trailing_kernel<<<dim3(rb * (rb + 1) / 2, nj), 256, 0, st>>>(jobs, k);
+      count_launch(2);
+    }
+    if (kfac_status e = check_launch()) return e;
+  }
+  for (int s = NB; s < nmax; s *= 2) {
+    const int tiles = level_tiles_host(nmax, s);
+    int tmax = tiles;
+    for (int i = j0; i < j0 + nj; ++i) tmax = std::max(tmax, level_tiles_host(h->invjobs_host[i].n, s));
+    tri_level_y_kernel<<<dim3(tmax, nj), 256, 0, st>>>(jobs, s);
+    tri_level_x_kernel<<<dim3(tmax, nj), 256, 0, st>>>(jobs, s);
+    count_launch(2);
+    if (kfac_status e = check_launch()) return e;
+  }
+  const int ntm = (int)cdiv(nmax, SyrkTile::BM);
+  return launch_syrk_simt_grouped(d_syrk + j0, nj, ntm * (ntm + 1) / 2, st);
+}
+
+}  // namespace kfac

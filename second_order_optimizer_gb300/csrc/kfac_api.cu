@@ -1,0 +1,379 @@
+// Host side of the C ABI: argument checks, workspace layout, dispatch to the kernels.
+#include "kfac_internal.cuh"
+#include "syrk_simt.cuh"
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <new>
+
+namespace kfac {
+
+static std::atomic<unsigned long long> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add((unsigned long long)n); }
+kfac_status check_launch() {
+  return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
+}
+
+namespace {
+
+bool valid_hp(const kfac_hparams* hp) {
+  if (!hp) return false;
+  if (!(hp->ema_decay >= 0.0 && hp->ema_decay < 1.0)) return false;
+  if (!(hp->damping > 0.0) || !std::isfinite(hp->damping)) return false;
+  if (!std::isfinite(hp->lr) || !std::isfinite(hp->momentum) || !std::isfinite(hp->weight_decay))
+    return false;
+  if (hp->ema_init != KFAC_EMA_INIT_ZERO && hp->ema_init != KFAC_EMA_INIT_FIRST) return false;
+  if (hp->math != KFAC_MATH_3XTF32 && hp->math != KFAC_MATH_BF16) return false;
+  return true;
+}
+
+bool valid_desc(const kfac_layer_desc& d) {
+  if (d.kind != KFAC_KRON && d.kind != KFAC_DIAG) return false;
+  if (d.d_out < 1 || d.d_in < 1 || (d.has_bias != 0 && d.has_bias != 1)) return false;
+  if (d.in_dtype != KFAC_F32 && d.in_dtype != KFAC_BF16) return false;
+  if (d.d_out > (1 << 20) || d.d_in > (1 << 20)) return false;
+  return true;
+}
+
+struct Plan {
+  std::vector<LayerInfo> layers;
+  size_t off_status, off_part, part_floats, off_tickets, n_tickets, off_k4tmp, k4tmp_floats;
+  size_t off_k5part, k5part_floats, off_k5tickets, off_invjobs, total;
+  int n_invjobs, max_kron_n;
+};
+
+bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += align_up(bytes ? bytes : 1);
+    return o;
+  };
+  P->off_status = take(sizeof(DevStatus));
+  P->layers.clear();
+  size_t part = 0, tickets = 0, k4 = 0, k5 = 0, k5t = 0;
+  int ninv = 0, maxn = 0;
+  for (int i = 0; i < nl; ++i) {
+    const kfac_layer_desc& d = descs[i];
+    LayerInfo L{};
+    L.kind = d.kind;
+    L.o = d.d_out;
+    L.d_in = d.d_in;
+    L.n = d.d_in + d.has_bias;
+    L.has_bias = d.has_bias;
+    L.in_dtype = d.in_dtype;
+    const size_t n = L.n, o = L.o, f = sizeof(float);
+    L.m = take(o * n * f);
+    if (d.kind == KFAC_KRON) {
+      L.A = take(n * n * f);
+      L.G = take(o * o * f);
+      L.Ainv = take(n * n * f);
+      L.Ginv = take(o * o * f);
+      L.LA = take(n * n * f);
+      L.LG = take(o * o * f);
+      L.XA = take(n * n * f);
+      L.XG = take(o * o * f);
+      L.YA = take(inv_y_floats(L.n) * f);
+      L.YG = take(inv_y_floats(L.o) * f);
+      size_t t1 = 0, t2 = 0;
+      part = std::max(part, k1_scratch_floats(L.n, max_rows, &t1));
+      part = std::max(part, k1_scratch_floats(L.o, max_rows, &t2));
+      tickets = std::max({tickets, t1, t2});
+      k4 = std::max(k4, o * n);
+      ninv += 2;
+      maxn = std::max({maxn, L.n, L.o});
+    } else {
+      L.gs = take(o * f);
+      L.as = take(n * f);
+      L.ticket = take(sizeof(int));
+    }
+    k5 = std::max(k5, k5_scratch_floats(L.d_in + L.o, max_rows));
+    k5t = std::max(k5t, (size_t)cdiv(L.d_in + L.o, 256));
+    P->layers.push_back(L);
+  }
+  P->part_floats = part;
+  P->off_part = take(part * sizeof(float));
+  P->n_tickets = tickets;
+  P->off_tickets = take(tickets * sizeof(int));
+  P->k4tmp_floats = k4;
+  P->off_k4tmp = take(k4 * sizeof(float));
+  P->k5part_floats = k5;
+  P->off_k5part = take(k5 * sizeof(float));
+  P->off_k5tickets = take(k5t * sizeof(int));
+  P->off_invjobs = off;
+  take(align_up(sizeof(InvJob) * ninv) + sizeof(SyrkJob) * ninv);
+  P->n_invjobs = ninv;
+  P->max_kron_n = maxn;
+  P->total = off;
+  return true;
+}
+
+kfac_status ensure_device(const kfac_ctx* h) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
+  if (dev != h->device && cudaSetDevice(h->device) != cudaSuccess) return KFAC_ERR_CUDA;
+  return KFAC_OK;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+kfac_status check_layer(const kfac_ctx* h, int layer, int kind) {
+  if (!h) return KFAC_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= (int)h->layers.size()) return KFAC_ERR_INVALID_ARG;
+  if (kind >= 0 && h->layers[layer].kind != kind) return KFAC_ERR_INVALID_ARG;
+  return KFAC_OK;
+}
+
+kfac_status check_inputs(const kfac_ctx* h, const LayerInfo& L, const void* a, int64_t lda,
+                         const void* g, int64_t ldg, int64_t rows) {
+  const size_t es = L.in_dtype == KFAC_BF16 ? 2 : 4;
+  if (!a || !g || !aligned(a, es) || !aligned(g, es)) return KFAC_ERR_INVALID_ARG;
+  if (rows < 1 || rows > h->max_rows) return KFAC_ERR_INVALID_ARG;
+  if (lda < L.d_in || ldg < L.o) return KFAC_ERR_INVALID_ARG;
+  return KFAC_OK;
+}
+
+}  // namespace
+}  // namespace kfac
+
+using namespace kfac;
+
+extern "C" {
+
+const char* kfac_status_string(kfac_status s) {
+  switch (s) {
+    case KFAC_OK: return "ok";
+    case KFAC_ERR_INVALID_ARG: return "invalid argument";
+    case KFAC_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case KFAC_ERR_STATE: return "call out of order (e.g. precondition before invert)";
+    case KFAC_ERR_NOT_PD: return "damped factor is not positive definite";
+    case KFAC_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case KFAC_ERR_CUDA: return "CUDA runtime error";
+    case KFAC_ERR_UNSUPPORTED: return "unsupported by this build";
+  }
+  return "unknown status";
+}
+
+unsigned long long kfac_launch_count(void) { return g_launches.load(); }
+
+kfac_status kfac_workspace_size(const kfac_layer_desc* layers, int n_layers,
+                                const kfac_hparams* hp, int64_t max_rows, size_t* bytes) {
+  if (!layers || n_layers < 1 || !bytes || max_rows < 1 || !valid_hp(hp))
+    return KFAC_ERR_INVALID_ARG;
+  for (int i = 0; i < n_layers; ++i)
+    if (!valid_desc(layers[i])) return KFAC_ERR_INVALID_ARG;
+  Plan P;
+  make_plan(layers, n_layers, max_rows, &P);
+  *bytes = P.total;
+  return KFAC_OK;
+}
+
+kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_hparams* hp,
+                        int64_t max_rows, void* d_workspace, size_t bytes, kfac_handle* out) {
+  if (!out) return KFAC_ERR_INVALID_ARG;
+  *out = nullptr;
+  size_t need = 0;
+  if (kfac_status e = kfac_workspace_size(layers, n_layers, hp, max_rows, &need)) return e;
+  if (!d_workspace || !aligned(d_workspace, kAlign) || bytes < need) return KFAC_ERR_WORKSPACE;
+  Plan P;
+  make_plan(layers, n_layers, max_rows, &P);
+  kfac_ctx* h = new (std::nothrow) kfac_ctx();
+  if (!h) return KFAC_ERR_INVALID_ARG;
+  if (cudaGetDevice(&h->device) != cudaSuccess) {
+    delete h;
+    return KFAC_ERR_CUDA;
+  }
+  h->hp = *hp;
+  h->max_rows = max_rows;
+  h->ws = static_cast<char*>(d_workspace);
+  h->ws_bytes = bytes;
+  h->layers = P.layers;
+  h->off_status = P.off_status;
+  h->off_part = P.off_part;
+  h->part_floats = P.part_floats;
+  h->off_tickets = P.off_tickets;
+  h->n_tickets = P.n_tickets;
+  h->off_k4tmp = P.off_k4tmp;
+  h->k4tmp_floats = P.k4tmp_floats;
+  h->off_k5part = P.off_k5part;
+  h->k5part_floats = P.k5part_floats;
+  h->off_k5tickets = P.off_k5tickets;
+  h->off_invjobs = P.off_invjobs;
+  h->n_invjobs = P.n_invjobs;
+  h->max_kron_n = P.max_kron_n;
+  // inversion tables: for each KRON layer, its A then its G
+  std::vector<SyrkJob> sj;
+  for (int i = 0; i < n_layers; ++i) {
+    const LayerInfo& L = h->layers[i];
+    if (L.kind != KFAC_KRON) continue;
+    for (int w = 0; w < 2; ++w) {
+      InvJob j{};
+      const int n = w == 0 ? L.n : L.o;
+      j.F = h->at<float>(w == 0 ? L.A : L.G);
+      j.L = h->at<float>(w == 0 ? L.LA : L.LG);
+      j.X = h->at<float>(w == 0 ? L.XA : L.XG);
+      j.Y = h->at<float>(w == 0 ? L.YA : L.YG);
+      j.Finv = h->at<float>(w == 0 ? L.Ainv : L.Ginv);
+      j.n = n;
+      j.layer = i;
+      h->invjobs_host.push_back(j);
+      SyrkJob s{};
+      s.x = j.X;
+      s.ld = n;
+      s.M = n;
+      s.d = n;
+      s.n = n;
+      s.has_bias = 0;
+      s.x_lower = 1;
+      s.alpha = 1.f;
+      s.beta = 0.f;
+      s.C = j.Finv;
+      s.nt = (int)cdiv(n, SyrkTile::BM);
+      s.splits = 1;
+      s.rows_per_split = n;
+      sj.push_back(s);
+    }
+  }
+  bool ok = cudaMemset(d_workspace, 0, need) == cudaSuccess;
+  if (ok && !h->invjobs_host.empty()) {
+    ok = cudaMemcpy(h->ws + h->off_invjobs, h->invjobs_host.data(),
+                    sizeof(InvJob) * h->invjobs_host.size(), cudaMemcpyHostToDevice) == cudaSuccess;
+    ok = ok && cudaMemcpy(h->ws + h->off_invjobs + align_up(sizeof(InvJob) * h->n_invjobs),
+                          sj.data(), sizeof(SyrkJob) * sj.size(),
+                          cudaMemcpyHostToDevice) == cudaSuccess;
+  }
+  ok = ok && cudaDeviceSynchronize() == cudaSuccess;
+  if (!ok) {
+    delete h;
+    return KFAC_ERR_CUDA;
+  }
+  *out = h;
+  return KFAC_OK;
+}
+
+kfac_status kfac_set_hparams(kfac_handle h, const kfac_hparams* hp) {
+  if (!h || !valid_hp(hp)) return KFAC_ERR_INVALID_ARG;
+  h->hp = *hp;
+  return KFAC_OK;
+}
+
+kfac_status kfac_update_factors(kfac_handle h, int layer, const void* a, int64_t lda,
+                                const void* g, int64_t ldg, int64_t rows, double scale,
+                                cudaStream_t stream) {
+  if (kfac_status e = check_layer(h, layer, KFAC_KRON)) return e;
+  LayerInfo& L = h->layers[layer];
+  if (kfac_status e = check_inputs(h, L, a, lda, g, ldg, rows)) return e;
+  if (!std::isfinite(scale)) return KFAC_ERR_INVALID_ARG;
+  if (kfac_status e = ensure_device(h)) return e;
+  const bool first = L.t_factor == 0 && h->hp.ema_init == KFAC_EMA_INIT_FIRST;
+  const float decay = first ? 0.f : (float)h->hp.ema_decay;
+  kfac_status e = launch_update_factors(h, layer, a, lda, g, ldg, rows, scale, decay, stream);
+  if (e == KFAC_OK) ++L.t_factor;
+  return e;
+}
+
+kfac_status kfac_diag_factors(kfac_handle h, int layer, const void* a, int64_t lda,
+                              const void* g, int64_t ldg, int64_t rows, double scale,
+                              float* g_new, float* a_new, cudaStream_t stream) {
+  if (kfac_status e = check_layer(h, layer, -1)) return e;
+  const LayerInfo& L = h->layers[layer];
+  if (kfac_status e = check_inputs(h, L, a, lda, g, ldg, rows)) return e;
+  if (!g_new || !a_new || !aligned(g_new, 4) || !aligned(a_new, 4)) return KFAC_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return KFAC_ERR_INVALID_ARG;
+  if (kfac_status e = ensure_device(h)) return e;
+  return launch_diag_factors(h, layer, a, lda, g, ldg, rows, scale, g_new, a_new, stream);
+}
+
+kfac_status kfac_invert(kfac_handle h, int layer, cudaStream_t stream) {
+  if (!h) return KFAC_ERR_INVALID_ARG;
+  if (layer != -1 && check_layer(h, layer, KFAC_KRON) != KFAC_OK) return KFAC_ERR_INVALID_ARG;
+  if (h->n_invjobs == 0) return layer == -1 ? KFAC_OK : KFAC_ERR_INVALID_ARG;
+  if (kfac_status e = ensure_device(h)) return e;
+  kfac_status e = launch_invert(h, layer, stream);
+  if (e != KFAC_OK) return e;
+  for (int i = 0; i < (int)h->layers.size(); ++i)
+    if (h->layers[i].kind == KFAC_KRON && (layer == -1 || layer == i)) h->layers[i].inverted = true;
+  return KFAC_OK;
+}
+
+kfac_status kfac_precondition(kfac_handle h, int layer, const float* grad_w, int64_t ldgw,
+                              const float* grad_b, float* out_w, float* out_b, float* param_w,
+                              float* param_b, cudaStream_t stream) {
+  if (kfac_status e = check_layer(h, layer, KFAC_KRON)) return e;
+  const LayerInfo& L = h->layers[layer];
+  if (!grad_w || !aligned(grad_w, 4) || ldgw < L.d_in) return KFAC_ERR_INVALID_ARG;
+  if (L.has_bias && !grad_b) return KFAC_ERR_INVALID_ARG;
+  if (!out_w && !param_w) return KFAC_ERR_INVALID_ARG;
+  if (L.has_bias && out_w && !out_b) return KFAC_ERR_INVALID_ARG;
+  if (L.has_bias && param_w && !param_b) return KFAC_ERR_INVALID_ARG;
+  if (!L.inverted) return KFAC_ERR_STATE;
+  if (kfac_status e = ensure_device(h)) return e;
+  return launch_precondition(h, layer, grad_w, ldgw, L.has_bias ? grad_b : nullptr, out_w,
+                             L.has_bias ? out_b : nullptr, param_w,
+                             L.has_bias ? param_b : nullptr, stream);
+}
+
+kfac_status kfac_diag_step(kfac_handle h, int layer, const float* g_new, const float* a_new,
+                           const float* grad_w, const float* grad_b, float* param_w,
+                           float* param_b, float* out_w, float* out_b, cudaStream_t stream) {
+  if (kfac_status e = check_layer(h, layer, KFAC_DIAG)) return e;
+  LayerInfo& L = h->layers[layer];
+  if (!g_new || !a_new || !grad_w || !param_w) return KFAC_ERR_INVALID_ARG;
+  if (L.has_bias && (!grad_b || !param_b)) return KFAC_ERR_INVALID_ARG;
+  if (L.has_bias && out_w && !out_b) return KFAC_ERR_INVALID_ARG;
+  for (const void* p : {(const void*)g_new, (const void*)a_new, (const void*)grad_w,
+                        (const void*)param_w})
+    if (!aligned(p, 4)) return KFAC_ERR_INVALID_ARG;
+  if (kfac_status e = ensure_device(h)) return e;
+  const bool first = L.t_diag == 0 && h->hp.ema_init == KFAC_EMA_INIT_FIRST;
+  const float decay = first ? 0.f : (float)h->hp.ema_decay;
+  kfac_status e = launch_diag_step(h, layer, decay, g_new, a_new, grad_w,
+                                   L.has_bias ? grad_b : nullptr, param_w,
+                                   L.has_bias ? param_b : nullptr, out_w,
+                                   L.has_bias ? out_b : nullptr, stream);
+  if (e == KFAC_OK) ++L.t_diag;
+  return e;
+}
+
+kfac_status kfac_get_status(kfac_handle h, int* bad_layer, int* info) {
+  if (!h) return KFAC_ERR_INVALID_ARG;
+  if (kfac_status e = ensure_device(h)) return e;
+  if (cudaDeviceSynchronize() != cudaSuccess) return KFAC_ERR_CUDA;
+  DevStatus s{};
+  if (cudaMemcpy(&s, h->status(), sizeof(s), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return KFAC_ERR_CUDA;
+  if (bad_layer) *bad_layer = s.code ? s.layer : -1;
+  if (info) *info = s.code ? s.info : 0;
+  if (s.code) {
+    if (cudaMemset(h->status(), 0, sizeof(DevStatus)) != cudaSuccess) return KFAC_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return KFAC_ERR_CUDA;
+  }
+  return (kfac_status)s.code;
+}
+
+kfac_status kfac_state_info(kfac_handle h, int layer, int which, size_t* offset, size_t* bytes) {
+  if (check_layer(h, layer, -1) != KFAC_OK || !offset || !bytes) return KFAC_ERR_INVALID_ARG;
+  const LayerInfo& L = h->layers[layer];
+  const size_t f = sizeof(float), n = L.n, o = L.o;
+  const bool kron = L.kind == KFAC_KRON;
+  switch (which) {
+    case KFAC_STATE_A: if (!kron) return KFAC_ERR_INVALID_ARG; *offset = L.A; *bytes = n * n * f; break;
+    case KFAC_STATE_G: if (!kron) return KFAC_ERR_INVALID_ARG; *offset = L.G; *bytes = o * o * f; break;
+    case KFAC_STATE_AINV: if (!kron) return KFAC_ERR_INVALID_ARG; *offset = L.Ainv; *bytes = n * n * f; break;
+    case KFAC_STATE_GINV: if (!kron) return KFAC_ERR_INVALID_ARG; *offset = L.Ginv; *bytes = o * o * f; break;
+    case KFAC_STATE_MOMENTUM: *offset = L.m; *bytes = o * n * f; break;
+    case KFAC_STATE_GDIAG: if (kron) return KFAC_ERR_INVALID_ARG; *offset = L.gs; *bytes = o * f; break;
+    case KFAC_STATE_ADIAG: if (kron) return KFAC_ERR_INVALID_ARG; *offset = L.as; *bytes = n * f; break;
+    default: return KFAC_ERR_INVALID_ARG;
+  }
+  return KFAC_OK;
+}
+
+kfac_status kfac_destroy(kfac_handle h) {
+  if (!h) return KFAC_ERR_INVALID_ARG;
+  delete h;
+  return KFAC_OK;
+}
+
+}  // extern "C"

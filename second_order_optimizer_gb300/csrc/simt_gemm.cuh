@@ -1,0 +1,72 @@
+// FP32 CUDA-core tile product used by the Cholesky / triangular-inverse steps
+// (and as the fp32-exact fallback-free stepping stone for small problems).
+//
+// acc[TM][TN] += sum_{k in [k0,k1)} la(m0+m, k) * lb(k, n0+n)
+// with thread-owned rows m = ty + i*(BM/TM) and cols n = tx + j*(BN/TN)
+// (interleaved so that shared-memory reads are conflict-free).
+#pragma once
+#include <cuda_runtime.h>
+
+namespace kfac {
+
+template <int BM, int BN, int BK, int TM, int TN>
+struct SimtTile {
+  static constexpr int kThreads = (BM / TM) * (BN / TN);
+  static constexpr int kSmemFloats = BK * (BM + BN);
+
+  template <class LA, class LB>
+  __device__ __forceinline__ static void run(const LA& la, const LB& lb, long long m0, long long n0,
+                                             long long k0, long long k1, float (&acc)[TM][TN],
+                                             float* smem) {
+    float* As = smem;            // [BK][BM]
+    float* Bs = smem + BK * BM;  // [BK][BN]
+    const int tid = threadIdx.x;
+    const int tx = tid % (BN / TN), ty = tid / (BN / TN);
+    for (long long kk = k0; kk < k1; kk += BK) {
+#pragma unroll
+      for (int e = tid; e < BK * BM; e += kThreads) {
+        int k = e / BM, m = e % BM;
+        long long gk = kk + k;
+        As[e] = (gk < k1) ? la(m0 + m, gk) : 0.f;
+      }
+#pragma unroll
+      for (int e = tid; e < BK * BN; e += kThreads) {
+        int k = e / BN, n = e % BN;
+        long long gk = kk + k;
+        Bs[e] = (gk < k1) ? lb(gk, n0 + n) : 0.f;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < BK; ++k) {
+        float a[TM], b[TN];
+#pragma unroll
+        for (int i = 0; i < TM; ++i) a[i] = As[k * BM + ty + i * (BM / TM)];
+#pragma unroll
+        for (int j = 0; j < TN; ++j) b[j] = Bs[k * BN + tx + j * (BN / TN)];
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+          for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      }
+      __syncthreads();
+    }
+  }
+
+  __device__ __forceinline__ static int row_of(int i) {
+    return (threadIdx.x / (BN / TN)) + i * (BM / TM);
+  }
+  __device__ __forceinline__ static int col_of(int j) {
+    return (threadIdx.x % (BN / TN)) + j * (BN / TN);
+  }
+};
+
+// Strided fp32 operand: element (r, c) at p[r*rs + c*cs], zero outside [0,R) x [0,C).
+struct StridedLoader {
+  const float* p;
+  long long rs, cs, R, C;
+  __device__ __forceinline__ float operator()(long long r, long long c) const {
+    return (r < R && c < C) ? p[r * rs + c * cs] : 0.f;
+  }
+};
+
+}  // namespace kfac

@@ -1,0 +1,123 @@
+"""CPU checks of the C ABI: the library loads, exports every declared entry point,
+and the host-only calls (sizing, argument checks, status strings) behave.
+No compute call is made here (there is no GPU on this side)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kfac.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from second_order_optimizer_gb300 import build
+    build.build()
+    import second_order_optimizer_gb300._lib as L
+    return L
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kfac_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_five_verbs():
+    names = declared_functions()
+    for verb in ("kfac_create", "kfac_update_factors", "kfac_invert", "kfac_precondition",
+                 "kfac_diag_step"):
+        assert verb in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib.LIB, n), n
+    # and the binding declares a signature for each
+    assert {s[0] for s in lib.SIGNATURES} >= set(names)
+
+
+def test_binding_covers_exactly_the_header(lib):
+    assert {s[0] for s in lib.SIGNATURES} == set(declared_functions())
+
+
+def _descs(lib, layers):
+    arr = (lib.LayerDesc * len(layers))(*[lib.LayerDesc(*l) for l in layers])
+    return arr
+
+
+def _hp(lib, **kw):
+    d = dict(ema_decay=0.95, damping=1e-3, lr=1e-2, momentum=0.9, weight_decay=5e-4,
+             ema_init=0, math=0)
+    d.update(kw)
+    return lib.HParams(**d)
+
+
+def test_workspace_size_grows_with_layers(lib):
+    hp = _hp(lib)
+    out = ctypes.c_size_t(0)
+    small = _descs(lib, [(0, 32, 64, 1, 0)])
+    assert lib.LIB.kfac_workspace_size(small, 1, ctypes.byref(hp), 128, ctypes.byref(out)) == 0
+    s1 = out.value
+    assert s1 % 256 == 0
+    # at least the fp32 state: A, G, Ainv, Ginv, m
+    n, o = 65, 32
+    assert s1 >= 4 * (2 * n * n + 2 * o * o + o * n)
+    big = _descs(lib, [(0, 32, 64, 1, 0), (1, 1024, 1024, 1, 0)])
+    assert lib.LIB.kfac_workspace_size(big, 2, ctypes.byref(hp), 128, ctypes.byref(out)) == 0
+    assert out.value > s1 + 4 * 1024 * 1025
+
+
+def test_workspace_size_rejects_bad_arguments(lib):
+    hp = _hp(lib)
+    out = ctypes.c_size_t(0)
+    bad = [
+        ([(0, 0, 64, 1, 0)], hp),            # d_out = 0
+        ([(0, 4, 0, 1, 0)], hp),             # d_in = 0
+        ([(2, 4, 4, 1, 0)], hp),             # kind
+        ([(0, 4, 4, 2, 0)], hp),             # has_bias
+        ([(0, 4, 4, 1, 5)], hp),             # dtype
+        ([(0, 4, 4, 1, 0)], _hp(lib, ema_decay=1.0)),
+        ([(0, 4, 4, 1, 0)], _hp(lib, damping=0.0)),
+        ([(0, 4, 4, 1, 0)], _hp(lib, damping=float("nan"))),
+        ([(0, 4, 4, 1, 0)], _hp(lib, math=7)),
+    ]
+    for layers, h in bad:
+        d = _descs(lib, layers)
+        assert lib.LIB.kfac_workspace_size(d, 1, ctypes.byref(h), 16, ctypes.byref(out)) == 1
+    d = _descs(lib, [(0, 4, 4, 1, 0)])
+    assert lib.LIB.kfac_workspace_size(d, 0, ctypes.byref(hp), 16, ctypes.byref(out)) == 1
+    assert lib.LIB.kfac_workspace_size(d, 1, ctypes.byref(hp), 0, ctypes.byref(out)) == 1
+
+
+def test_null_handle_calls_fail_cleanly(lib):
+    L = lib.LIB
+    assert L.kfac_invert(None, -1, None) == 1
+    assert L.kfac_destroy(None) == 1
+    assert L.kfac_get_status(None, None, None) == 1
+    assert L.kfac_update_factors(None, 0, None, 1, None, 1, 1, 0.0, None) == 1
+    assert L.kfac_precondition(None, 0, None, 1, None, None, None, None, None, None) == 1
+    assert L.kfac_diag_step(None, 0, None, None, None, None, None, None, None, None, None) == 1
+
+
+def test_create_rejects_small_or_misaligned_workspace(lib):
+    hp = _hp(lib)
+    d = _descs(lib, [(0, 8, 8, 1, 0)])
+    h = ctypes.c_void_p()
+    # too small: rejected before touching the device
+    assert lib.LIB.kfac_create(d, 1, ctypes.byref(hp), 16, ctypes.c_void_p(0x1000), 16,
+                               ctypes.byref(h)) == 2
+    assert lib.LIB.kfac_create(d, 1, ctypes.byref(hp), 16, ctypes.c_void_p(0x1001), 1 << 30,
+                               ctypes.byref(h)) == 2
+    assert h.value is None
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = lib.status_string(code)
+        assert isinstance(s, str) and s
+    assert lib.status_string(0) == "ok"

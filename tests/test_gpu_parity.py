@@ -1,0 +1,310 @@
+"""GPU parity of every kernel of the step against the float64 oracle, through the C ABI.
+
+Tolerances (relative Frobenius unless stated):
+  factors A, G (fp32 or bf16 inputs, oracle fed the same rounded inputs)  1e-5
+  preconditioned gradient P and updated W                                 1e-4
+  diagonal step P, W, m (same fp32 diagonal vectors on both sides)        1e-6 elementwise
+     (relative to max(|x*|, 1e-3 max|x*|), since m and W are sums that can cancel)
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from gpu_helpers import to_dev, to_np, rel_fro, max_rel_elem, bf16_tensor
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import second_order_optimizer_gb300 as K  # noqa: E402
+
+HP = dict(ema_decay=0.95, damping=1e-3, lr=1e-2, momentum=0.9, weight_decay=5e-4)
+RNG = np.random.default_rng(7)
+
+
+def _orc(**kw):
+    hp = dict(HP)
+    hp.update(kw)
+    return O.KfacOracle(hp["ema_decay"], hp["damping"], hp["lr"], hp["momentum"],
+                        hp["weight_decay"], kw.get("invert_every", 1))
+
+
+def _inputs(M, d_in, o, act="relu", g_std=1e-3, dtype="f32"):
+    a = RNG.standard_normal((M, d_in))
+    if act == "relu":
+        a = np.maximum(a, 0)
+    a = W.round_input(a, dtype)
+    g = W.round_input(RNG.standard_normal((M, o)) * g_std, dtype)
+    return a, g
+
+
+def _dev_in(x, dtype):
+    return bf16_tensor(x) if dtype == "bf16" else to_dev(x)
+
+
+# ------------------------------------------------------------------ K1 factors
+
+@pytest.mark.parametrize("M,d_in,o,bias,dtype", [
+    (1000, 300, 200, 1, "f32"), (129, 7, 130, 0, "f32"), (5000, 64, 16, 1, "f32"),
+    (1, 1, 1, 1, "f32"), (777, 257, 129, 1, "bf16"), (20000, 27, 64, 1, "f32"),
+])
+def test_factor_update_matches_oracle(M, d_in, o, bias, dtype):
+    kd = K.KFAC_BF16 if dtype == "bf16" else K.KFAC_F32
+    h = K.Kfac([(K.KFAC_KRON, o, d_in, bias, kd)], max_rows=M, **HP)
+    A = np.zeros((d_in + bias,) * 2)
+    G = np.zeros((o, o))
+    for step in range(3):
+        a, g = _inputs(M, d_in, o, dtype=dtype)
+        h.update_factors(0, _dev_in(a, dtype), _dev_in(g, dtype))
+        A = O.ema(A, O.factor(a, bias), 0.95)
+        G = O.ema(G, O.factor(g, 0), 0.95)
+        Ag, Gg = to_np(h.state(0, K.KFAC_STATE_A)), to_np(h.state(0, K.KFAC_STATE_G))
+        assert rel_fro(Ag, A) <= 1e-5, (step, rel_fro(Ag, A))
+        assert rel_fro(Gg, G) <= 1e-5, (step, rel_fro(Gg, G))
+        assert np.array_equal(Ag, Ag.T) and np.array_equal(Gg, Gg.T)
+    assert h.get_status()[0] == 0
+
+
+def test_factor_ema_init_first_and_custom_scale():
+    M, d_in, o = 300, 40, 24
+    h = K.Kfac([(K.KFAC_KRON, o, d_in, 1, K.KFAC_F32)], max_rows=M,
+               ema_init=K.KFAC_EMA_INIT_FIRST, **HP)
+    a, g = _inputs(M, d_in, o)
+    h.update_factors(0, to_dev(a), to_dev(g), scale=0.125)
+    assert rel_fro(to_np(h.state(0, K.KFAC_STATE_A)), O.factor(a, 1, scale=0.125)) <= 1e-5
+    assert rel_fro(to_np(h.state(0, K.KFAC_STATE_G)), O.factor(g, 0, scale=0.125)) <= 1e-5
+
+
+def test_factor_constant_input_converges():
+    """EMA of a constant factor converges to it (closed form C + xi^t (0 - C))."""
+    M, d_in, o = 256, 33, 17
+    h = K.Kfac([(K.KFAC_KRON, o, d_in, 1, K.KFAC_F32)], max_rows=M, **HP)
+    a, g = _inputs(M, d_in, o)
+    da, dg = to_dev(a), to_dev(g)
+    C = O.factor(a, 1)
+    for t in range(1, 121):
+        h.update_factors(0, da, dg)
+    Ag = to_np(h.state(0, K.KFAC_STATE_A))
+    assert rel_fro(Ag, C * (1 - 0.95 ** 120)) <= 1e-5
+
+
+def test_factor_strided_input():
+    M, d_in, o = 400, 50, 20
+    h = K.Kfac([(K.KFAC_KRON, o, d_in, 1, K.KFAC_F32)], max_rows=M, **HP)
+    big_a, big_g = _inputs(M, d_in + 13, o + 5)
+    ta, tg = to_dev(big_a), to_dev(big_g)
+    h.update_factors(0, ta[:, :d_in], tg[:, :o])
+    assert rel_fro(to_np(h.state(0, K.KFAC_STATE_A)), 0.05 * O.factor(big_a[:, :d_in], 1)) <= 1e-5
+    assert rel_fro(to_np(h.state(0, K.KFAC_STATE_G)), 0.05 * O.factor(big_g[:, :o], 0)) <= 1e-5
+
+
+# ------------------------------------------------------------------ K2/K3 inverse
+
+@pytest.mark.parametrize("n_in,o", [(0, 1), (27, 64), (63, 5), (64, 100), (128, 129), (299, 300),
+                                    (512, 65)])
+def test_invert_matches_oracle(n_in, o):
+    """Ainv/Ginv vs the oracle's textbook Cholesky inverse of the same (GPU) factor."""
+    bias = 1
+    d_in = max(n_in, 1)
+    M = 2 * (d_in + 1) + 3
+    h = K.Kfac([(K.KFAC_KRON, o, d_in, bias, K.KFAC_F32)], max_rows=M, ema_init=K.KFAC_EMA_INIT_FIRST, **HP)
+    a, g = _inputs(M, d_in, o, g_std=0.1)
+    h.update_factors(0, to_dev(a), to_dev(g))
+    h.invert(0)
+    assert h.get_status()[0] == 0
+    for wf, wi in ((K.KFAC_STATE_A, K.KFAC_STATE_AINV), (K.KFAC_STATE_G, K.KFAC_STATE_GINV)):
+        F = to_np(h.state(0, wf))
+        Finv = to_np(h.state(0, wi))
+        ref = O.damped_inverse(F, HP["damping"])
+        assert np.array_equal(Finv, Finv.T)
+        assert rel_fro(Finv, ref) <= 1e-4, rel_fro(Finv, ref)
+
+
+def test_invert_all_layers_batched():
+    layers = [(K.KFAC_KRON, 70, 200, 1, K.KFAC_F32), (K.KFAC_DIAG, 8, 8, 1, K.KFAC_F32),
+              (K.KFAC_KRON, 10, 3, 0, K.KFAC_F32), (K.KFAC_KRON, 300, 129, 1, K.KFAC_F32)]
+    M = 700
+    h = K.Kfac(layers, max_rows=M, **HP)
+    for li, (kind, o, d_in, bias, _) in enumerate(layers):
+        if kind == K.KFAC_KRON:
+            a, g = _inputs(M, d_in, o, g_std=0.05)
+            h.update_factors(li, to_dev(a), to_dev(g))
+    h.invert(-1)
+    assert h.get_status()[0] == 0
+    for li, (kind, *_rest) in enumerate(layers):
+        if kind != K.KFAC_KRON:
+            continue
+        for wf, wi in ((K.KFAC_STATE_A, K.KFAC_STATE_AINV), (K.KFAC_STATE_G, K.KFAC_STATE_GINV)):
+            F = to_np(h.state(li, wf))
+            assert rel_fro(to_np(h.state(li, wi)), O.damped_inverse(F, HP["damping"])) <= 1e-4
+
+
+def test_invert_reports_not_positive_definite():
+    """A factor made indefinite on the host: the device reports layer and column, no fault."""
+    d_in, o = 100, 70
+    h = K.Kfac([(K.KFAC_KRON, 5, 5, 1, K.KFAC_F32), (K.KFAC_KRON, o, d_in, 1, K.KFAC_F32)],
+               max_rows=8, **HP)
+    n = d_in + 1
+    Abad = np.eye(n)
+    Abad[77, 77] = -1.0
+    h.state(1, K.KFAC_STATE_A).copy_(to_dev(Abad.astype(np.float32)))
+    h.invert(-1)
+    code, layer, info = h.get_status()
+    assert (code, layer, info) == (4, 1, 77)
+    assert h.get_status()[0] == 0          # cleared by the read
+    h.state(1, K.KFAC_STATE_A).copy_(to_dev(np.eye(n, dtype=np.float32)))
+    h.invert(1)
+    assert h.get_status()[0] == 0
+    ref = np.eye(n) / (1 + math.sqrt(HP["damping"]))
+    assert rel_fro(to_np(h.state(1, K.KFAC_STATE_AINV)), ref) <= 1e-6
+
+
+# ------------------------------------------------------------------ K4 precondition
+
+@pytest.mark.parametrize("M,d_in,o,bias", [(600, 200, 150, 1), (300, 65, 1, 1), (90, 33, 70, 0)])
+def test_precondition_and_update_match_oracle(M, d_in, o, bias):
+    h = K.Kfac([(K.KFAC_KRON, o, d_in, bias, K.KFAC_F32)], max_rows=M, **HP)
+    st = O.LayerState("kron", o, d_in, bias, np.zeros((o, d_in)), np.zeros(o) if bias else None)
+    orc = _orc()
+    w0 = (RNG.standard_normal((o, d_in)) * 0.1).astype(np.float32)
+    b0 = (RNG.standard_normal(o) * 0.1).astype(np.float32) if bias else None
+    st.W = O.grad_hat(w0, b0).copy()
+    pw, pb = to_dev(w0), (to_dev(b0) if bias else None)
+    with pytest.raises(K.KfacError):
+        h.precondition(0, to_dev(w0), pb, out_w=torch.empty_like(pw), out_b=pb)  # before invert
+    for t in range(3):
+        a, g = _inputs(M, d_in, o)
+        gw = (RNG.standard_normal((o, d_in)) * 1e-3).astype(np.float32)
+        gb = (RNG.standard_normal(o) * 1e-3).astype(np.float32) if bias else None
+        h.update_factors(0, to_dev(a), to_dev(g))
+        if t == 0:
+            h.invert(0)
+        ow = torch.empty(o, d_in, device="cuda")
+        ob = torch.empty(o, device="cuda") if bias else None
+        h.precondition(0, to_dev(gw), to_dev(gb) if bias else None, ow, ob, pw, pb)
+        P = orc.step_kron(st, a, g, gw, gb)
+        Pg = O.grad_hat(to_np(ow), to_np(ob) if bias else None)
+        assert rel_fro(Pg, P) <= 1e-4, (t, rel_fro(Pg, P))
+        Wg = O.grad_hat(to_np(pw), to_np(pb) if bias else None)
+        assert rel_fro(Wg, st.W) <= 1e-4
+        mw, mb = h.momentum(0)
+        assert rel_fro(O.grad_hat(to_np(mw), to_np(mb) if bias else None), st.m) <= 1e-4
+    assert h.get_status()[0] == 0
+
+
+# ------------------------------------------------------------------ K5 / K6 diagonal
+
+@pytest.mark.parametrize("M,d_in,o,bias,dtype", [(3000, 257, 100, 1, "f32"), (50, 3, 2, 0, "f32"),
+                                                 (2500, 640, 64, 1, "bf16")])
+def test_diag_factors_match_oracle(M, d_in, o, bias, dtype):
+    kd = K.KFAC_BF16 if dtype == "bf16" else K.KFAC_F32
+    h = K.Kfac([(K.KFAC_DIAG, o, d_in, bias, kd)], max_rows=M, **HP)
+    a, g = _inputs(M, d_in, o, act="normal", dtype=dtype)
+    gn = torch.empty(o, device="cuda")
+    an = torch.empty(d_in + bias, device="cuda")
+    h.diag_factors(0, _dev_in(a, dtype), _dev_in(g, dtype), gn, an)
+    assert max_rel_elem(to_np(gn), O.diag_factor(g, 0), 0) <= 2e-6
+    assert max_rel_elem(to_np(an), O.diag_factor(a, bias), 0) <= 2e-6
+
+
+@pytest.mark.parametrize("o,d_in,bias", [(64, 256, 1), (33, 5, 1), (128, 1, 1), (7, 12, 0),
+                                         (300, 1024, 1)])
+def test_diag_step_elementwise(o, d_in, bias):
+    h = K.Kfac([(K.KFAC_DIAG, o, d_in, bias, K.KFAC_F32)], max_rows=1, **HP)
+    n = d_in + bias
+    st = O.LayerState("diag", o, d_in, bias, np.zeros((o, d_in)), np.zeros(o) if bias else None)
+    orc = _orc()
+    w0 = (RNG.standard_normal((o, d_in)) * 0.1).astype(np.float32)
+    b0 = (RNG.standard_normal(o) * 0.1).astype(np.float32) if bias else None
+    st.W = O.grad_hat(w0, b0).copy()
+    pw, pb = to_dev(w0), (to_dev(b0) if bias else None)
+    for t in range(4):
+        gn = RNG.uniform(0, 2e-6, o).astype(np.float32)
+        an = RNG.uniform(0, 2, n).astype(np.float32)
+        gw = (RNG.standard_normal((o, d_in)) * 1e-3).astype(np.float32)
+        gb = (RNG.standard_normal(o) * 1e-3).astype(np.float32) if bias else None
+        ow = torch.empty(o, d_in, device="cuda")
+        ob = torch.empty(o, device="cuda") if bias else None
+        h.diag_step(0, to_dev(gn), to_dev(an), to_dev(gw), to_dev(gb) if bias else None, pw, pb,
+                    ow, ob)
+        P = orc.step_diag(st, gn, an, gw, gb)
+        bo = lambda x, y: O.grad_hat(to_np(x), to_np(y) if bias else None)
+        assert max_rel_elem(bo(ow, ob), P) <= 1e-6
+        assert max_rel_elem(bo(pw, pb), st.W) <= 1e-6
+        mw, mb = h.momentum(0)
+        assert max_rel_elem(bo(mw, mb), st.m) <= 1e-6
+        assert max_rel_elem(to_np(h.state(0, K.KFAC_STATE_GDIAG)), st.gs) <= 1e-6
+        assert max_rel_elem(to_np(h.state(0, K.KFAC_STATE_ADIAG)), st.as_) <= 1e-6
+
+
+# ------------------------------------------------------------------ whole configs
+
+def _run_config_small(cfg_name, steps, check_every=1):
+    cfg = W.get_config(cfg_name)
+    hp = cfg.hp
+    kinds = [K.KFAC_KRON if l.kind == "kron" else K.KFAC_DIAG for l in cfg.layers]
+    descs = [(k, l.d_out, l.d_in, l.has_bias, K.KFAC_BF16 if l.in_dtype == "bf16" else K.KFAC_F32)
+             for k, l in zip(kinds, cfg.layers)]
+    h = K.Kfac(descs, max_rows=max(l.rows for l in cfg.layers), ema_decay=hp.ema_decay,
+               damping=hp.damping, lr=hp.lr, momentum=hp.momentum, weight_decay=hp.weight_decay)
+    orc = O.KfacOracle(hp.ema_decay, hp.damping, hp.lr, hp.momentum, hp.weight_decay,
+                       cfg.invert_every)
+    states, params = [], []
+    for li, l in enumerate(cfg.layers):
+        src = 0 if cfg_name == "c1" else li       # c1's two layers share one set of inputs
+        w0, b0 = W.initial_params(cfg, src)
+        states.append(O.LayerState(l.kind, l.d_out, l.d_in, l.has_bias, w0, b0))
+        params.append((to_dev(w0), to_dev(b0) if l.has_bias else None))
+    worst = {"A": 0.0, "G": 0.0, "P": 0.0, "W": 0.0, "Wdiag": 0.0}
+    for t in range(1, steps + 1):
+        for li, l in enumerate(cfg.layers):
+            src = 0 if cfg_name == "c1" else li
+            x = W.layer_inputs(cfg, src, t)
+            gb = x["grad_b"]
+            pw, pb = params[li]
+            if l.kind == "kron":
+                h.update_factors(li, to_dev(x["a"]), to_dev(x["g"]))
+                if (t - 1) % cfg.invert_every == 0:
+                    h.invert(li)
+                ow = torch.empty(l.d_out, l.d_in, device="cuda")
+                ob = torch.empty(l.d_out, device="cuda") if l.has_bias else None
+                h.precondition(li, to_dev(x["grad_w"]), to_dev(gb) if l.has_bias else None,
+                               ow, ob, pw, pb)
+                P = orc.step_kron(states[li], x["a"], x["g"], x["grad_w"], gb)
+                if t % check_every == 0 or t == steps:
+                    worst["A"] = max(worst["A"], rel_fro(to_np(h.state(li, K.KFAC_STATE_A)), states[li].A))
+                    worst["G"] = max(worst["G"], rel_fro(to_np(h.state(li, K.KFAC_STATE_G)), states[li].G))
+                    worst["P"] = max(worst["P"], rel_fro(
+                        O.grad_hat(to_np(ow), to_np(ob) if l.has_bias else None), P))
+                    worst["W"] = max(worst["W"], rel_fro(
+                        O.grad_hat(to_np(pw), to_np(pb) if l.has_bias else None), states[li].W))
+            else:
+                gn = torch.empty(l.d_out, device="cuda")
+                an = torch.empty(l.n, device="cuda")
+                h.diag_factors(li, to_dev(x["a"]), to_dev(x["g"]), gn, an)
+                h.diag_step(li, gn, an, to_dev(x["grad_w"]), to_dev(gb), pw, pb)
+                orc.step_diag(states[li], O.diag_factor(x["g"]), O.diag_factor(x["a"], l.has_bias),
+                              x["grad_w"], gb)
+                worst["Wdiag"] = max(worst["Wdiag"], max_rel_elem(
+                    O.grad_hat(to_np(pw), to_np(pb)), states[li].W))
+    assert h.get_status()[0] == 0
+    return worst
+
+
+def test_single_linear_layer_both_paths_10_steps():
+    worst = _run_config_small("c1", 10)
+    assert worst["A"] <= 1e-5 and worst["G"] <= 1e-5, worst
+    assert worst["P"] <= 1e-4 and worst["W"] <= 1e-4, worst
+    assert worst["Wdiag"] <= 1e-6, worst
+
+
+def test_mlp4_full_size_two_refreshes():
+    """4-layer MLP at full size (1024 wide, batch 1024), 11 steps: inverses refreshed at 1 and 11."""
+    worst = _run_config_small("c2", 11, check_every=5)
+    assert worst["A"] <= 1e-5 and worst["G"] <= 1e-5, worst
+    assert worst["P"] <= 1e-4 and worst["W"] <= 1e-4, worst
