@@ -9,7 +9,7 @@ LIB_PATH = os.path.join(_HERE, "libkfac.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python -m second_order_optimizer_gb300.build` "
+        f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"` "
         "(there is no CPU implementation of this library)")
 
 LIB = ctypes.CDLL(LIB_PATH)

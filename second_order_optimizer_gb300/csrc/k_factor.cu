@@ -182,30 +182,12 @@ kfac_status launch_update_factors(kfac_ctx* h, int layer, const void* a, int64_t
   const LayerInfo& L = h->layers[layer];
   const double s = scale > 0 ? scale : 1.0 / (double)rows;
   const float alpha = (float)((1.0 - (double)decay) * s);
-  for (int which = 0; which < 2; ++which) {
-    SyrkJob j{};
-    j.x = which == 0 ? a : g;
-    j.ld = which == 0 ? lda : ldg;
-    j.M = rows;
-    j.d = which == 0 ? L.d_in : L.o;
-    j.n = which == 0 ? L.n : L.o;
-    j.has_bias = which == 0 ? L.has_bias : 0;
-    j.x_lower = 0;
-    j.alpha = alpha;
-    j.beta = decay;
-    j.C = h->at<float>(which == 0 ? L.A : L.G);
-    j.nt = (int)cdiv(j.n, SyrkTile::BM);
-    syrk_split_plan(j.n, rows, &j.splits, &j.rows_per_split);
-    j.part = h->at<float>(h->off_part);
-    j.tickets = h->at<int>(h->off_tickets);
-    int64_t tiles = (int64_t)j.nt * (j.nt + 1) / 2;
-    if (j.splits > 1 &&
-        (size_t)(tiles * j.splits) * SyrkTile::BM * SyrkTile::BN > h->part_floats)
-      return KFAC_ERR_WORKSPACE;
-    kfac_status e = launch_syrk_simt(&j, 1, L.in_dtype == KFAC_BF16, st);
-    if (e != KFAC_OK) return e;
-  }
-  return KFAC_OK;
+  const bool bf16 = L.in_dtype == KFAC_BF16;
+  kfac_status e = launch_syrk_tc(h, layer, a, lda, rows, L.d_in, L.n, L.has_bias, bf16, alpha,
+                                 decay, h->at<float>(L.A), st);
+  if (e != KFAC_OK) return e;
+  return launch_syrk_tc(h, layer, g, ldg, rows, L.o, L.o, 0, bf16, alpha, decay,
+                        h->at<float>(L.G), st);
 }
 
 }  // namespace kfac

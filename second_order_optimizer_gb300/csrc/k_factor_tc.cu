@@ -1,0 +1,451 @@
+// K1 on the tensor cores: F <- beta F + alpha X X^T  (upper tiles + mirror), X = x-hat^T.
+//
+// Osawa et al., "Large-Scale Distributed Second-Order Optimization Using
+// Kronecker-Factored Approximate Curvature ...": §3.2 (A from activations, G from
+// output gradients), §3.4 (Tensor Cores for the Kronecker-factor computation;
+// a symmetric N x N factor has N(N+1)/2 distinct entries, so only tiles on or
+// above the diagonal are computed and the epilogue writes each entry and its
+// mirror).  CAFIN briefing, Introduction: EMA of the factors, fused into the
+// epilogue as beta*F_old + alpha*acc.
+//
+// Two kernels:
+//  pack:  x-hat [M x n] (row-major, any ld, fp32 or bf16, ones column virtual)
+//         -> X = x-hat^T [n x Kp], K-major, so both MMA operands are K-major
+//         tiles.  fp32 input is split into TF32 halves hi = rna(x),
+//         lo = rna(x - hi) (3xTF32: hi*hi + hi*lo + lo*hi carries ~21 bits).
+//  syrk:  one 128 x 128 output tile per CTA (split-K over rows when the
+//         triangle has fewer tiles than SMs), warp-specialised:
+//           warp 0  TMA producer   (SW128 tiles of 128 rows x 128 bytes)
+//           warp 1  MMA issuer     (tcgen05.mma, accumulator in TMEM)
+//           warps 2-5 epilogue     (tcgen05.ld; 128 threads = 128 TMEM lanes)
+//         The accumulator is double-buffered in TMEM and drained into fp32
+//         registers every `ksub` rows, so no TMEM accumulation runs longer
+//         than ksub rows whatever the tensor core's internal rounding.
+//         Output goes through shared memory so both the tile and its mirror
+//         are written with coalesced stores.
+#include "kfac_internal.cuh"
+#include "tc_prims.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+namespace kfac {
+
+namespace {
+
+template <bool kBF16>
+struct TcCfg {
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int ELT = kBF16 ? 2 : 4;
+  static constexpr int BK = 128 / ELT;            // k elements per 128-byte row
+  static constexpr int KMMA = 32 / ELT;           // k elements per MMA (32 bytes)
+  static constexpr int TILE_BYTES = BM * 128;     // one operand tile: 16 KB
+  static constexpr int OPS = kBF16 ? 2 : 4;       // A(hi), B(hi), [A lo, B lo]
+  static constexpr int STAGE_BYTES = OPS * TILE_BYTES;
+  static constexpr int STAGES = kBF16 ? 6 : 3;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int THREADS = 192;
+  static constexpr int TPAD = BN + 1;             // output staging row pitch (floats)
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+  static_assert((size_t)BM * TPAD * 4 <= (size_t)STAGES * STAGE_BYTES, "staging fits");
+};
+
+struct SyrkTcParams {
+  int n;                 // output dimension
+  int64_t K;             // reduction length (rows of x)
+  int nt;                // tiles per side
+  int splits;
+  int64_t k_per_split;   // multiple of ksub
+  int ksub;              // rows per TMEM drain (multiple of BK)
+  float alpha, beta;
+  float* C;
+  float* part;
+  int* tickets;
+  DevStatus* status;
+  int layer;
+};
+
+__device__ __forceinline__ void upper_tile(int t, int nt, int* ti, int* tj) {
+  int r = 0;
+  while (t >= nt - r) {
+    t -= nt - r;
+    ++r;
+  }
+  *ti = r;
+  *tj = r + t;
+}
+
+template <bool kBF16>
+__global__ void __launch_bounds__(TcCfg<kBF16>::THREADS, 1)
+syrk_tc_kernel(const __grid_constant__ CUtensorMap map_hi,
+               const __grid_constant__ CUtensorMap map_lo, SyrkTcParams p) {
+  using C = TcCfg<kBF16>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_last = reinterpret_cast<int*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
+  int ti, tj;
+  upper_tile(tile, p.nt, &ti, &tj);
+  const bool diag = ti == tj;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&acc_full[b], 1);
+      tc::mbar_init(&acc_empty[b], 128);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+    tc::tma_prefetch_desc(&map_hi);
+    if (!kBF16) tc::tma_prefetch_desc(&map_lo);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int64_t kbeg = (int64_t)split * p.k_per_split;
+  const int64_t kend = min(p.K, kbeg + p.k_per_split);
+  const int nkb = kend > kbeg ? (int)((kend - kbeg + C::BK - 1) / C::BK) : 0;
+  const int kb_per_sub = p.ksub / C::BK;
+  const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
+  auto stage_ptr = [&](int s, int op) { return smem + (size_t)s * C::STAGE_BYTES + op * C::TILE_BYTES; };
+
+  if (warp == 0) {
+    if (lane == 0) {  // ------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      const uint32_t bytes = (diag ? C::OPS / 2 : C::OPS) * C::TILE_BYTES;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+          *abort_flag = 1;
+          report_error(p.status, KFAC_ERR_TIMEOUT, p.layer, 1);
+          break;
+        }
+        const int k0 = (int)(kbeg + (int64_t)kb * C::BK);
+        tc::mbar_expect_tx(&full[stage], bytes);
+        tc::tma_load_2d(stage_ptr(stage, 0), &map_hi, &full[stage], k0, ti * C::BM);
+        if (!diag) tc::tma_load_2d(stage_ptr(stage, 1), &map_hi, &full[stage], k0, tj * C::BN);
+        if (!kBF16) {
+          tc::tma_load_2d(stage_ptr(stage, 2), &map_lo, &full[stage], k0, ti * C::BM);
+          if (!diag) tc::tma_load_2d(stage_ptr(stage, 3), &map_lo, &full[stage], k0, tj * C::BN);
+        }
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = tc::make_idesc(kBF16 ? 1 : 2, C::BM, C::BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int sub = 0; sub < nsub && ok; ++sub) {
+        const int buf = sub & 1;
+        if (!tc::mbar_wait(&acc_empty[buf], ((sub >> 1) & 1) ^ 1, abort_flag)) {
+          report_error(p.status, KFAC_ERR_TIMEOUT, p.layer, 2);
+          *abort_flag = 1;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * C::BN);
+        const int kb0 = sub * kb_per_sub, kb1 = min(nkb, kb0 + kb_per_sub);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!tc::mbar_wait(&full[stage], phase, abort_flag)) {
+            report_error(p.status, KFAC_ERR_TIMEOUT, p.layer, 3);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t a_hi = tc::smem_u32(stage_ptr(stage, 0));
+          const uint32_t b_hi = diag ? a_hi : tc::smem_u32(stage_ptr(stage, 1));
+          const uint32_t a_lo = tc::smem_u32(stage_ptr(stage, 2));
+          const uint32_t b_lo = diag ? a_lo : tc::smem_u32(stage_ptr(stage, 3));
+#pragma unroll
+          for (int kk = 0; kk < C::BK / C::KMMA; ++kk) {
+            const uint32_t off = kk * 32;
+            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+            if (kBF16) {
+              tc::umma_f16(d, tc::sdesc_kmajor_sw128(a_hi + off), tc::sdesc_kmajor_sw128(b_hi + off),
+                           idesc, acc);
+            } else {
+              tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_hi + off),
+                            tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
+              tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_hi + off),
+                            tc::sdesc_kmajor_sw128(b_lo + off), idesc, 1u);
+              tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_lo + off),
+                            tc::sdesc_kmajor_sw128(b_hi + off), idesc, 1u);
+            }
+          }
+          tc::umma_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (ok) tc::umma_commit(&acc_full[buf]);
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ epilogue warps
+  float* T = reinterpret_cast<float*>(smem);  // [BM][TPAD], reuses the stage buffers
+  if (warp >= 2) {
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    float sum[C::BN];
+#pragma unroll
+    for (int c = 0; c < C::BN; ++c) sum[c] = 0.f;
+    for (int sub = 0; sub < nsub; ++sub) {
+      const int buf = sub & 1;
+      if (!tc::mbar_wait(&acc_full[buf], (sub >> 1) & 1, abort_flag)) {
+        report_error(p.status, KFAC_ERR_TIMEOUT, p.layer, 4);
+        *abort_flag = 1;
+        break;
+      }
+      tc::tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < C::BN / 32; ++cc) {
+        float v[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::BN + cc * 32), v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sum[cc * 32 + i] += v[i];
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&acc_empty[buf]);
+    }
+    // all MMAs have completed (their last commit was waited on), so the stage
+    // buffers are free: stage the tile for coalesced output
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+#pragma unroll
+    for (int c = 0; c < C::BN; ++c) T[row * C::TPAD + c] = sum[c];
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  if (*abort_flag) return;
+
+  const int nth = C::THREADS;
+  if (p.splits > 1) {
+    float* part = p.part + (size_t)tile * p.splits * (C::BM * C::BN);
+    for (int e = threadIdx.x; e < C::BM * C::BN; e += nth)
+      part[(size_t)split * (C::BM * C::BN) + e] = T[(e / C::BN) * C::TPAD + e % C::BN];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) *s_last = (atomicAdd(&p.tickets[tile], 1) == p.splits - 1);
+    __syncthreads();
+    if (!*s_last) return;
+    __threadfence();
+    for (int e = threadIdx.x; e < C::BM * C::BN; e += nth) {
+      float v = 0.f;
+      for (int s = 0; s < p.splits; ++s) v += __ldcg(part + (size_t)s * (C::BM * C::BN) + e);
+      T[(e / C::BN) * C::TPAD + e % C::BN] = v;
+    }
+    if (threadIdx.x == 0) p.tickets[tile] = 0;
+    __syncthreads();
+  }
+  // tile entries (r <= c): F[r][c] = alpha*acc + beta*F[r][c]; T keeps the result
+  const int r0 = ti * C::BM, c0 = tj * C::BN;
+  for (int e = threadIdx.x; e < C::BM * C::BN; e += nth) {
+    const int r = e / C::BN, c = e % C::BN;
+    const int gr = r0 + r, gc = c0 + c;
+    if (gr >= p.n || gc >= p.n || gr > gc) continue;
+    float* dst = p.C + (int64_t)gr * p.n + gc;
+    float v = p.alpha * T[r * C::TPAD + c];
+    if (p.beta != 0.f) v = fmaf(p.beta, *dst, v);
+    *dst = v;
+    T[r * C::TPAD + c] = v;
+  }
+  __syncthreads();
+  // mirrors (gr < gc): F[gc][gr], coalesced over gr
+  for (int e = threadIdx.x; e < C::BM * C::BN; e += nth) {
+    const int c = e / C::BM, r = e % C::BM;
+    const int gr = r0 + r, gc = c0 + c;
+    if (gr >= p.n || gc >= p.n || gr >= gc) continue;
+    p.C[(int64_t)gc * p.n + gr] = T[r * C::TPAD + c];
+  }
+}
+
+// ------------------------------------------------------------------- pack
+// X[c][r] = x-hat[r][c] for c < n, r < M; fp32 -> (hi, lo) TF32 halves; bf16 -> copy.
+template <typename T, bool kSplit>
+__global__ void __launch_bounds__(256) pack_kernel(const T* __restrict__ x, int64_t ld, int64_t M,
+                                                    int d, int n, int64_t Kp, void* out_hi,
+                                                    void* out_lo) {
+  __shared__ float tile[32][33];
+  const int64_t r0 = (int64_t)blockIdx.x * 32;
+  const int c0 = blockIdx.y * 32;
+  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;  // 32 x 8
+  for (int i = ty; i < 32; i += 8) {
+    const int64_t r = r0 + i;
+    const int c = c0 + tx;
+    float v = 0.f;
+    if (r < M && c < n) v = c < d ? to_f32<T>(x[r * ld + c]) : 1.f;
+    tile[i][tx] = v;
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int c = c0 + i;
+    const int64_t r = r0 + tx;
+    if (c >= n || r >= Kp) continue;
+    const float v = tile[tx][i];
+    if (kSplit) {
+      const float hi = tc::to_tf32(v);
+      const float lo = tc::to_tf32(v - hi);
+      static_cast<float*>(out_hi)[(int64_t)c * Kp + r] = hi;
+      static_cast<float*>(out_lo)[(int64_t)c * Kp + r] = lo;
+    } else {
+      static_cast<__nv_bfloat16*>(out_hi)[(int64_t)c * Kp + r] = __float2bfloat16_rn(v);
+    }
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [rows x cols] row-major matrix (cols contiguous, pitch in elements), box of
+// 128 rows x 128 bytes, 128-byte swizzle, out-of-range elements read as zero.
+bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t rows, int64_t cols,
+              int64_t pitch) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int elt = bf16 ? 2 : 4;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(pitch * elt)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / elt), 128u};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                  const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool kBF16>
+bool set_smem_attr() {
+  static bool done = false;
+  static bool ok = false;
+  if (!done) {
+    ok = cudaFuncSetAttribute(syrk_tc_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)TcCfg<kBF16>::SMEM) == cudaSuccess;
+    done = true;
+  }
+  return ok;
+}
+
+constexpr int kKsubTf32 = 128;   // rows per TMEM drain on the fp32 path
+
+}  // namespace
+
+int64_t tc_pack_pitch(int64_t rows, bool bf16) { return cdiv(rows, bf16 ? 8 : 4) * (bf16 ? 8 : 4); }
+
+size_t tc_pack_bytes(int n, int64_t max_rows, bool bf16) {
+  const int64_t Kp = tc_pack_pitch(max_rows, bf16);
+  return (size_t)n * Kp * (bf16 ? 2 : 8);
+}
+
+void tc_split_plan(int n, int64_t K, bool bf16, int* splits, int64_t* kps, int* ksub) {
+  const int nt = (int)cdiv(n, 128);
+  const int64_t tiles = (int64_t)nt * (nt + 1) / 2;
+  const int bk = bf16 ? 64 : 32;
+  int64_t s = std::max<int64_t>(1, kNumSMs / tiles);
+  s = std::min<int64_t>(s, std::max<int64_t>(1, K / 256));
+  const int64_t unit = bf16 ? bk : kKsubTf32;
+  int64_t per = cdiv(cdiv(K, s), unit) * unit;
+  *splits = (int)cdiv(K, per);
+  *kps = per;
+  *ksub = bf16 ? (int)std::min<int64_t>(per, 1 << 30) : kKsubTf32;
+}
+
+size_t tc_part_floats(int n, int64_t max_rows, bool bf16) {
+  const int nt = (int)cdiv(n, 128);
+  const int64_t tiles = (int64_t)nt * (nt + 1) / 2;
+  const int64_t s = std::max<int64_t>(1, kNumSMs / tiles);  // upper bound of the plan
+  (void)max_rows;
+  (void)bf16;
+  return s > 1 ? (size_t)(tiles * s) * 128 * 128 : 0;
+}
+
+// F <- beta F + alpha x-hat^T x-hat on the tensor cores.
+kfac_status launch_syrk_tc(kfac_ctx* h, int layer, const void* x, int64_t ld, int64_t rows, int d,
+                           int n, int has_bias, bool bf16, float alpha, float beta, float* F,
+                           cudaStream_t st) {
+  const int64_t Kp = tc_pack_pitch(rows, bf16);
+  if ((size_t)n * Kp * (bf16 ? 2 : 8) > h->tcpack_bytes) return KFAC_ERR_WORKSPACE;
+  void* hi = h->ws + h->off_tcpack;
+  void* lo = bf16 ? nullptr : (void*)(h->ws + h->off_tcpack + (size_t)n * Kp * 4);
+  {
+    dim3 grid((unsigned)cdiv(Kp, 32), (unsigned)cdiv(n, 32));
+    if (bf16)
+      pack_kernel<__nv_bfloat16, false><<<grid, 256, 0, st>>>(
+          static_cast<const __nv_bfloat16*>(x), ld, rows, d, n, Kp, hi, nullptr);
+    else
+      pack_kernel<float, true><<<grid, 256, 0, st>>>(static_cast<const float*>(x), ld, rows, d,
+                                                     n, Kp, hi, lo);
+    count_launch();
+    if (kfac_status e = check_launch()) return e;
+  }
+  CUtensorMap mh, ml;
+  if (!make_map(&mh, hi, bf16, n, rows, Kp)) return KFAC_ERR_CUDA;
+  if (!bf16 && !make_map(&ml, lo, false, n, rows, Kp)) return KFAC_ERR_CUDA;
+  if (bf16) ml = mh;
+  SyrkTcParams p{};
+  p.n = n;
+  p.K = rows;
+  p.nt = (int)cdiv(n, 128);
+  tc_split_plan(n, rows, bf16, &p.splits, &p.k_per_split, &p.ksub);
+  p.alpha = alpha;
+  p.beta = beta;
+  p.C = F;
+  p.part = h->at<float>(h->off_part);
+  p.tickets = h->at<int>(h->off_tickets);
+  p.status = h->status();
+  p.layer = layer;
+  const int64_t tiles = (int64_t)p.nt * (p.nt + 1) / 2;
+  if (p.splits > 1 && (size_t)(tiles * p.splits) * 128 * 128 > h->part_floats)
+    return KFAC_ERR_WORKSPACE;
+  if (p.splits > 1 && (size_t)tiles > h->n_tickets) return KFAC_ERR_WORKSPACE;
+  const unsigned grid = (unsigned)(tiles * p.splits);
+  if (bf16) {
+    if (!set_smem_attr<true>()) return KFAC_ERR_CUDA;
+    syrk_tc_kernel<true><<<grid, TcCfg<true>::THREADS, TcCfg<true>::SMEM, st>>>(mh, ml, p);
+  } else {
+    if (!set_smem_attr<false>()) return KFAC_ERR_CUDA;
+    syrk_tc_kernel<false><<<grid, TcCfg<false>::THREADS, TcCfg<false>::SMEM, st>>>(mh, ml, p);
+  }
+  count_launch();
+  return check_launch();
+}
+
+}  // namespace kfac

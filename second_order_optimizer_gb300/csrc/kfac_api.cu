@@ -40,6 +40,7 @@ struct Plan {
   std::vector<LayerInfo> layers;
   size_t off_status, off_part, part_floats, off_tickets, n_tickets, off_k4tmp, k4tmp_floats;
   size_t off_k5part, k5part_floats, off_k5tickets, off_invjobs, total;
+  size_t off_tcpack, tcpack_bytes;
   int n_invjobs, max_kron_n;
 };
 
@@ -52,7 +53,7 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
   };
   P->off_status = take(sizeof(DevStatus));
   P->layers.clear();
-  size_t part = 0, tickets = 0, k4 = 0, k5 = 0, k5t = 0;
+  size_t part = 0, tickets = 0, k4 = 0, k5 = 0, k5t = 0, tcpack = 0;
   int ninv = 0, maxn = 0;
   for (int i = 0; i < nl; ++i) {
     const kfac_layer_desc& d = descs[i];
@@ -79,6 +80,9 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
       size_t t1 = 0, t2 = 0;
       part = std::max(part, k1_scratch_floats(L.n, max_rows, &t1));
       part = std::max(part, k1_scratch_floats(L.o, max_rows, &t2));
+      const bool bf = d.in_dtype == KFAC_BF16;
+      part = std::max({part, tc_part_floats(L.n, max_rows, bf), tc_part_floats(L.o, max_rows, bf)});
+      tcpack = std::max({tcpack, tc_pack_bytes(L.n, max_rows, bf), tc_pack_bytes(L.o, max_rows, bf)});
       tickets = std::max({tickets, t1, t2});
       k4 = std::max(k4, o * n);
       ninv += 2;
@@ -96,6 +100,8 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
   P->off_part = take(part * sizeof(float));
   P->n_tickets = tickets;
   P->off_tickets = take(tickets * sizeof(int));
+  P->tcpack_bytes = tcpack;
+  P->off_tcpack = take(tcpack);
   P->k4tmp_floats = k4;
   P->off_k4tmp = take(k4 * sizeof(float));
   P->k5part_floats = k5;
@@ -194,6 +200,8 @@ kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_
   h->part_floats = P.part_floats;
   h->off_tickets = P.off_tickets;
   h->n_tickets = P.n_tickets;
+  h->off_tcpack = P.off_tcpack;
+  h->tcpack_bytes = P.tcpack_bytes;
   h->off_k4tmp = P.off_k4tmp;
   h->k4tmp_floats = P.k4tmp_floats;
   h->off_k5part = P.off_k5part;

@@ -72,6 +72,8 @@ struct kfac_ctx {
   // K1 split-K scratch
   size_t off_part = 0, part_floats = 0;
   size_t off_tickets = 0, n_tickets = 0;
+  // K1 tensor-core operand pack (X = x-hat^T, TF32 halves or bf16)
+  size_t off_tcpack = 0, tcpack_bytes = 0;
   // K4 intermediate X = dW-hat . Ainv  (o x n, max over layers)
   size_t off_k4tmp = 0, k4tmp_floats = 0;
   // K5 row-split partials and tickets
@@ -110,6 +112,13 @@ kfac_status launch_invert(kfac_ctx* h, int layer, cudaStream_t s);
 kfac_status launch_precondition(kfac_ctx* h, int layer, const float* gw, int64_t ldgw,
                                 const float* gb, float* ow, float* ob, float* pw, float* pb,
                                 cudaStream_t s);
+
+// K1 on the tensor cores (tcgen05 + TMA)
+kfac_status launch_syrk_tc(kfac_ctx* h, int layer, const void* x, int64_t ld, int64_t rows, int d,
+                           int n, int has_bias, bool bf16, float alpha, float beta, float* F,
+                           cudaStream_t st);
+size_t tc_pack_bytes(int n, int64_t max_rows, bool bf16);
+size_t tc_part_floats(int n, int64_t max_rows, bool bf16);
 
 // scratch sizing helpers (used by the workspace planner)
 size_t k1_scratch_floats(int n, int64_t max_rows, size_t* tickets);

@@ -13,8 +13,8 @@ HEADER = os.path.join(ROOT, "include", "kfac.h")
 
 @pytest.fixture(scope="module")
 def lib():
-    from second_order_optimizer_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import second_order_optimizer_gb300._lib as L
     return L
 
@@ -121,3 +121,19 @@ def test_status_strings(lib):
         s = lib.status_string(code)
         assert isinstance(s, str) and s
     assert lib.status_string(0) == "ok"
+
+
+def test_package_refuses_to_load_without_the_library(tmp_path):
+    """No CPU fallback: a copy of the package without libkfac.so fails to import."""
+    import shutil
+    import subprocess
+    import sys
+    pkg = os.path.join(ROOT, "second_order_optimizer_gb300")
+    dst = tmp_path / "second_order_optimizer_gb300"
+    dst.mkdir()
+    for f in ("__init__.py", "_lib.py"):
+        shutil.copy(os.path.join(pkg, f), dst / f)
+    r = subprocess.run([sys.executable, "-c", "import second_order_optimizer_gb300"],
+                       cwd=tmp_path, capture_output=True, text=True)
+    assert r.returncode != 0
+    assert "libkfac.so is missing" in r.stderr
