@@ -23,8 +23,16 @@ namespace kfac {
 namespace {
 
 constexpr int kDiagThreads = 256;
-constexpr int64_t kK5RowsPerSplit = 1024;
 constexpr int kK5Threads = 256;
+constexpr int64_t kK5MinRows = 32;
+
+// Row splits of K5: enough CTAs to cover the GPU twice, at least kK5MinRows rows each.
+int64_t k5_splits(int ncols, int64_t rows) {
+  const int64_t cb = cdiv(ncols, kK5Threads);
+  int64_t s = cdiv(2 * kNumSMs, cb);
+  s = std::min<int64_t>(s, cdiv(rows, kK5MinRows));
+  return std::max<int64_t>(s, 1);
+}
 
 struct DiagParams {
   int o, d_in, has_bias;
@@ -142,10 +150,14 @@ __global__ void __launch_bounds__(kK5Threads) diag_factor_kernel(DiagFactorParam
     const T* base = c < p.d_in ? static_cast<const T*>(p.a) + c
                                : static_cast<const T*>(p.g) + (c - p.d_in);
     const int64_t ld = c < p.d_in ? p.lda : p.ldg;
-    float acc = 0.f;
+    // compensated (Kahan) sum: the kernel is bound by HBM, the extra flops are free
+    float acc = 0.f, comp = 0.f;
     for (int64_t r = r0; r < r1; ++r) {
       const float v = to_f32<T>(base[r * ld]);
-      acc = fmaf(v, v, acc);
+      const float y = fmaf(v, v, -comp);
+      const float t = acc + y;
+      comp = (t - acc) - y;
+      acc = t;
     }
     p.part[(size_t)split * ncols + c] = acc;
   }
@@ -157,8 +169,13 @@ __global__ void __launch_bounds__(kK5Threads) diag_factor_kernel(DiagFactorParam
   if (!s_last) return;
   __threadfence();
   if (c < ncols) {
-    float v = 0.f;
-    for (int s = 0; s < p.splits; ++s) v += __ldcg(p.part + (size_t)s * ncols + c);
+    float v = 0.f, comp = 0.f;
+    for (int s = 0; s < p.splits; ++s) {
+      const float y = __ldcg(p.part + (size_t)s * ncols + c) - comp;
+      const float t = v + y;
+      comp = (t - v) - y;
+      v = t;
+    }
     v *= p.s;
     if (c < p.d_in) p.a_new[c] = v;
     else p.g_new[c - p.d_in] = v;
@@ -170,7 +187,7 @@ __global__ void __launch_bounds__(kK5Threads) diag_factor_kernel(DiagFactorParam
 }  // namespace
 
 size_t k5_scratch_floats(int n_plus_o, int64_t max_rows) {
-  return (size_t)cdiv(max_rows, kK5RowsPerSplit) * (size_t)n_plus_o;
+  return (size_t)k5_splits(n_plus_o, max_rows) * (size_t)n_plus_o;
 }
 
 kfac_status launch_diag_factors(kfac_ctx* h, int layer, const void* a, int64_t lda,
@@ -183,8 +200,9 @@ kfac_status launch_diag_factors(kfac_ctx* h, int layer, const void* a, int64_t l
   p.lda = lda;
   p.ldg = ldg;
   p.rows = rows;
-  p.rows_per_split = kK5RowsPerSplit;
-  p.splits = (int)cdiv(rows, kK5RowsPerSplit);
+  const int64_t sp = k5_splits(L.d_in + L.o, rows);
+  p.rows_per_split = cdiv(rows, sp);
+  p.splits = (int)cdiv(rows, p.rows_per_split);
   p.d_in = L.d_in;
   p.o = L.o;
   p.has_bias = L.has_bias;

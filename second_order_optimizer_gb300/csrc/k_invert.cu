@@ -24,6 +24,7 @@
 #include "kfac_internal.cuh"
 #include "simt_gemm.cuh"
 #include "syrk_simt.cuh"
+#include "tc_prims.cuh"
 
 #include <algorithm>
 
@@ -225,6 +226,20 @@ __global__ void __launch_bounds__(256) tri_level_x_kernel(const InvJob* jobs, in
     }
 }
 
+// Finv -> TF32 halves with a 16-byte row pitch, the operand form of the K4 products.
+__global__ void __launch_bounds__(256) inv_split_kernel(const InvJob* jobs) {
+  const InvJob J = jobs[blockIdx.y];
+  const int64_t nn = (int64_t)J.n * J.n;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / J.n, c = e % J.n;
+    const float v = J.Finv[e];
+    const float hi = tc::to_tf32(v);
+    J.Finv_hi[r * J.np + c] = hi;
+    J.Finv_lo[r * J.np + c] = tc::to_tf32(v - hi);
+  }
+}
+
 int level_tiles_host(int n, int s) {
   int total = 0;
   for (int p = 0;; ++p) {
@@ -287,7 +302,11 @@ kfac_status launch_invert(kfac_ctx* h, int layer, cudaStream_t st) {
     if (kfac_status e = check_launch()) return e;
   }
   const int ntm = (int)cdiv(nmax, SyrkTile::BM);
-  return launch_syrk_simt_grouped(d_syrk + j0, nj, ntm * (ntm + 1) / 2, st);
+  if (kfac_status e = launch_syrk_simt_grouped(d_syrk + j0, nj, ntm * (ntm + 1) / 2, st)) return e;
+  inv_split_kernel<<<dim3((unsigned)std::min<int64_t>(cdiv((int64_t)nmax * nmax, 256), 1024), nj),
+                     256, 0, st>>>(jobs);
+  count_launch();
+  return check_launch();
 }
 
 }  // namespace kfac

@@ -77,14 +77,19 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
       L.XG = take(o * o * f);
       L.YA = take(inv_y_floats(L.n) * f);
       L.YG = take(inv_y_floats(L.o) * f);
+      const size_t np = (size_t)tc_pitch(L.n, false), op = (size_t)tc_pitch(L.o, false);
+      L.Ainv_hi = take(n * np * f);
+      L.Ainv_lo = take(n * np * f);
+      L.Ginv_hi = take(o * op * f);
+      L.Ginv_lo = take(o * op * f);
       size_t t1 = 0, t2 = 0;
       part = std::max(part, k1_scratch_floats(L.n, max_rows, &t1));
       part = std::max(part, k1_scratch_floats(L.o, max_rows, &t2));
       const bool bf = d.in_dtype == KFAC_BF16;
-      part = std::max({part, tc_part_floats(L.n, max_rows, bf), tc_part_floats(L.o, max_rows, bf)});
+      part = std::max(part, tc_part_floats());
       tcpack = std::max({tcpack, tc_pack_bytes(L.n, max_rows, bf), tc_pack_bytes(L.o, max_rows, bf)});
-      tickets = std::max({tickets, t1, t2});
-      k4 = std::max(k4, o * n);
+      tickets = std::max({tickets, t1, t2, (size_t)kNumSMs});
+      k4 = std::max(k4, 2 * o * np + 2 * n * op);
       ninv += 2;
       maxn = std::max({maxn, L.n, L.o});
     } else {
@@ -182,6 +187,7 @@ kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_
   size_t need = 0;
   if (kfac_status e = kfac_workspace_size(layers, n_layers, hp, max_rows, &need)) return e;
   if (!d_workspace || !aligned(d_workspace, kAlign) || bytes < need) return KFAC_ERR_WORKSPACE;
+  if (hp->math != KFAC_MATH_3XTF32) return KFAC_ERR_UNSUPPORTED;
   Plan P;
   make_plan(layers, n_layers, max_rows, &P);
   kfac_ctx* h = new (std::nothrow) kfac_ctx();
@@ -223,7 +229,10 @@ kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_
       j.X = h->at<float>(w == 0 ? L.XA : L.XG);
       j.Y = h->at<float>(w == 0 ? L.YA : L.YG);
       j.Finv = h->at<float>(w == 0 ? L.Ainv : L.Ginv);
+      j.Finv_hi = h->at<float>(w == 0 ? L.Ainv_hi : L.Ginv_hi);
+      j.Finv_lo = h->at<float>(w == 0 ? L.Ainv_lo : L.Ginv_lo);
       j.n = n;
+      j.np = (int)tc_pitch(n, false);
       j.layer = i;
       h->invjobs_host.push_back(j);
       SyrkJob s{};
@@ -262,6 +271,7 @@ kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_
 
 kfac_status kfac_set_hparams(kfac_handle h, const kfac_hparams* hp) {
   if (!h || !valid_hp(hp)) return KFAC_ERR_INVALID_ARG;
+  if (hp->math != KFAC_MATH_3XTF32) return KFAC_ERR_UNSUPPORTED;
   h->hp = *hp;
   return KFAC_OK;
 }

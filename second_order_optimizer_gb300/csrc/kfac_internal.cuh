@@ -43,8 +43,10 @@ struct InvJob {
   float* L;         // Cholesky factor, in place (n x n, lower; upper zeroed)
   float* X;         // L^{-1} (n x n, lower; upper zero)
   float* Y;         // level scratch (n x n/2 + tile slack)
-  float* Finv;      // result
-  int n;
+  float* Finv;      // result (n x n, pitch n)
+  float* Finv_hi;   // result as TF32 halves, pitch np (operands of the K4 products)
+  float* Finv_lo;
+  int n, np;
   int layer;
 };
 
@@ -52,6 +54,7 @@ struct LayerInfo {
   int kind, o, d_in, n, has_bias, in_dtype;
   // KRON state
   size_t A, G, Ainv, Ginv, LA, LG, XA, XG, YA, YG, m;
+  size_t Ainv_hi, Ainv_lo, Ginv_hi, Ginv_lo;   // pitch n_p / o_p (multiples of 4)
   // DIAG state
   size_t gs, as, ticket;
   // host-side counters
@@ -74,7 +77,7 @@ struct kfac_ctx {
   size_t off_tickets = 0, n_tickets = 0;
   // K1 tensor-core operand pack (X = x-hat^T, TF32 halves or bf16)
   size_t off_tcpack = 0, tcpack_bytes = 0;
-  // K4 intermediate X = dW-hat . Ainv  (o x n, max over layers)
+  // K4 scratch: dW-hat halves [o x n_p] x2, then X^T halves [n x o_p] x2
   size_t off_k4tmp = 0, k4tmp_floats = 0;
   // K5 row-split partials and tickets
   size_t off_k5part = 0, k5part_floats = 0;
@@ -113,12 +116,33 @@ kfac_status launch_precondition(kfac_ctx* h, int layer, const float* gw, int64_t
                                 const float* gb, float* ow, float* ob, float* pw, float* pb,
                                 cudaStream_t s);
 
-// K1 on the tensor cores (tcgen05 + TMA)
+// Tensor-core GEMM engine (tcgen05 + TMA): C[M x N] = A[M x K] . B[N x K]^T
+enum { TC_EPI_SYRK = 0, TC_EPI_SPLIT = 1, TC_EPI_PRECOND = 2 };
+struct TcOperand {       // K-major operand: rows x K, row pitch in elements (16-byte multiple)
+  const void* hi;        // fp32 TF32-high half, or bf16 values
+  const void* lo;        // fp32 TF32-low half (unused for bf16)
+  int64_t rows, pitch;
+};
+struct TcEpilogue {
+  float alpha, beta;     // SYRK: F <- beta F + alpha C (upper + mirror)
+  float* C;
+  int64_t ldc;
+  float* out_hi;         // SPLIT: C stored as TF32 halves, row pitch ldo
+  float* out_lo;
+  int64_t ldo;
+  int d_in;              // PRECOND: P = C (o x n); columns >= d_in are the bias
+  float eta, mu, lambda;
+  float *ow, *ob, *pw, *pb, *mw, *mb;
+};
+kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcOperand& A,
+                           const TcOperand& B, bool same_ab, bool upper, int64_t M, int64_t N,
+                           int64_t K, const TcEpilogue& e, cudaStream_t st);
 kfac_status launch_syrk_tc(kfac_ctx* h, int layer, const void* x, int64_t ld, int64_t rows, int d,
                            int n, int has_bias, bool bf16, float alpha, float beta, float* F,
                            cudaStream_t st);
+int64_t tc_pitch(int64_t cols, bool bf16);
 size_t tc_pack_bytes(int n, int64_t max_rows, bool bf16);
-size_t tc_part_floats(int n, int64_t max_rows, bool bf16);
+size_t tc_part_floats();
 
 // scratch sizing helpers (used by the workspace planner)
 size_t k1_scratch_floats(int n, int64_t max_rows, size_t* tickets);

@@ -1,4 +1,11 @@
-// K1 on the tensor cores: F <- beta F + alpha X X^T  (upper tiles + mirror), X = x-hat^T.
+// Tensor-core GEMM engine (tcgen05 + TMA) and the K1 factor update built on it.
+//
+//   C[M x N] = A[M x K] . B[N x K]^T, both operands K-major, fp32 accumulate,
+//   with one of three fused epilogues:
+//     SYRK     F <- beta F + alpha C on tiles on/above the diagonal, plus mirrors (K1,
+//              with A = B = X = x-hat^T)
+//     SPLIT    store C as TF32 halves (hi, lo), ready to be the next product's operand
+//     PRECOND  P = C; optional momentum / weight-decay / lr update of W in place (K4)
 //
 // Osawa et al., "Large-Scale Distributed Second-Order Optimization Using
 // Kronecker-Factored Approximate Curvature ...": §3.2 (A from activations, G from
@@ -52,19 +59,19 @@ struct TcCfg {
   static_assert((size_t)BM * TPAD * 4 <= (size_t)STAGES * STAGE_BYTES, "staging fits");
 };
 
-struct SyrkTcParams {
-  int n;                 // output dimension
-  int64_t K;             // reduction length (rows of x)
-  int nt;                // tiles per side
+struct GemmTcParams {
+  int64_t M, N, K;
+  int tiles_n;           // full grid: tile t -> (t / tiles_n, t % tiles_n)
+  int upper, nt;         // upper: tiles (ti <= tj) of an nt x nt triangle
+  int same_ab;           // A and B are the same operand (diagonal tiles load once)
   int splits;
   int64_t k_per_split;   // multiple of ksub
-  int ksub;              // rows per TMEM drain (multiple of BK)
-  float alpha, beta;
-  float* C;
+  int ksub;              // k elements per TMEM drain (multiple of BK)
   float* part;
   int* tickets;
   DevStatus* status;
   int layer;
+  TcEpilogue e;
 };
 
 __device__ __forceinline__ void upper_tile(int t, int nt, int* ti, int* tj) {
@@ -77,10 +84,12 @@ __device__ __forceinline__ void upper_tile(int t, int nt, int* ti, int* tj) {
   *tj = r + t;
 }
 
-template <bool kBF16>
+template <bool kBF16, int EPI>
 __global__ void __launch_bounds__(TcCfg<kBF16>::THREADS, 1)
-syrk_tc_kernel(const __grid_constant__ CUtensorMap map_hi,
-               const __grid_constant__ CUtensorMap map_lo, SyrkTcParams p) {
+gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
+               const __grid_constant__ CUtensorMap map_a_lo,
+               const __grid_constant__ CUtensorMap map_b_hi,
+               const __grid_constant__ CUtensorMap map_b_lo, GemmTcParams p) {
   using C = TcCfg<kBF16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -91,12 +100,18 @@ syrk_tc_kernel(const __grid_constant__ CUtensorMap map_hi,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_last = reinterpret_cast<int*>(tmem_slot + 2);
+  static_assert(EPI == TC_EPI_SYRK || !kBF16, "bf16 operands are used by the factor update only");
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
   int ti, tj;
-  upper_tile(tile, p.nt, &ti, &tj);
-  const bool diag = ti == tj;
+  if (p.upper) {
+    upper_tile(tile, p.nt, &ti, &tj);
+  } else {
+    ti = tile / p.tiles_n;
+    tj = tile % p.tiles_n;
+  }
+  const bool diag = p.same_ab && ti == tj;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -109,8 +124,12 @@ syrk_tc_kernel(const __grid_constant__ CUtensorMap map_hi,
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
-    tc::tma_prefetch_desc(&map_hi);
-    if (!kBF16) tc::tma_prefetch_desc(&map_lo);
+    tc::tma_prefetch_desc(&map_a_hi);
+    tc::tma_prefetch_desc(&map_b_hi);
+    if (!kBF16) {
+      tc::tma_prefetch_desc(&map_a_lo);
+      tc::tma_prefetch_desc(&map_b_lo);
+    }
   }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -141,11 +160,11 @@ syrk_tc_kernel(const __grid_constant__ CUtensorMap map_hi,
         }
         const int k0 = (int)(kbeg + (int64_t)kb * C::BK);
         tc::mbar_expect_tx(&full[stage], bytes);
-        tc::tma_load_2d(stage_ptr(stage, 0), &map_hi, &full[stage], k0, ti * C::BM);
-        if (!diag) tc::tma_load_2d(stage_ptr(stage, 1), &map_hi, &full[stage], k0, tj * C::BN);
+        tc::tma_load_2d(stage_ptr(stage, 0), &map_a_hi, &full[stage], k0, ti * C::BM);
+        if (!diag) tc::tma_load_2d(stage_ptr(stage, 1), &map_b_hi, &full[stage], k0, tj * C::BN);
         if (!kBF16) {
-          tc::tma_load_2d(stage_ptr(stage, 2), &map_lo, &full[stage], k0, ti * C::BM);
-          if (!diag) tc::tma_load_2d(stage_ptr(stage, 3), &map_lo, &full[stage], k0, tj * C::BN);
+          tc::tma_load_2d(stage_ptr(stage, 2), &map_a_lo, &full[stage], k0, ti * C::BM);
+          if (!diag) tc::tma_load_2d(stage_ptr(stage, 3), &map_b_lo, &full[stage], k0, tj * C::BN);
         }
         if (++stage == C::STAGES) {
           stage = 0;
@@ -264,25 +283,63 @@ syrk_tc_kernel(const __grid_constant__ CUtensorMap map_hi,
     if (threadIdx.x == 0) p.tickets[tile] = 0;
     __syncthreads();
   }
-  // tile entries (r <= c): F[r][c] = alpha*acc + beta*F[r][c]; T keeps the result
   const int r0 = ti * C::BM, c0 = tj * C::BN;
-  for (int e = threadIdx.x; e < C::BM * C::BN; e += nth) {
-    const int r = e / C::BN, c = e % C::BN;
-    const int gr = r0 + r, gc = c0 + c;
-    if (gr >= p.n || gc >= p.n || gr > gc) continue;
-    float* dst = p.C + (int64_t)gr * p.n + gc;
-    float v = p.alpha * T[r * C::TPAD + c];
-    if (p.beta != 0.f) v = fmaf(p.beta, *dst, v);
-    *dst = v;
-    T[r * C::TPAD + c] = v;
-  }
-  __syncthreads();
-  // mirrors (gr < gc): F[gc][gr], coalesced over gr
-  for (int e = threadIdx.x; e < C::BM * C::BN; e += nth) {
-    const int c = e / C::BM, r = e % C::BM;
-    const int gr = r0 + r, gc = c0 + c;
-    if (gr >= p.n || gc >= p.n || gr >= gc) continue;
-    p.C[(int64_t)gc * p.n + gr] = T[r * C::TPAD + c];
+  const TcEpilogue& E = p.e;
+  if (EPI == TC_EPI_SYRK) {
+    // tile entries (r <= c): F[r][c] = alpha*acc + beta*F[r][c]; T keeps the result
+    for (int e = threadIdx.x; e < C::BM * C::BN; e += nth) {
+      const int r = e / C::BN, c = e % C::BN;
+      const int64_t gr = r0 + r, gc = c0 + c;
+      if (gr >= p.M || gc >= p.N || gr > gc) continue;
+      float* dst = E.C + gr * E.ldc + gc;
+      float v = E.alpha * T[r * C::TPAD + c];
+      if (E.beta != 0.f) v = fmaf(E.beta, *dst, v);
+      *dst = v;
+      T[r * C::TPAD + c] = v;
+    }
+    __syncthreads();
+    // mirrors (gr < gc): F[gc][gr], coalesced over gr
+    for (int e = threadIdx.x; e < C::BM * C::BN; e += nth) {
+      const int c = e / C::BM, r = e % C::BM;
+      const int64_t gr = r0 + r, gc = c0 + c;
+      if (gr >= p.M || gc >= p.N || gr >= gc) continue;
+      E.C[gc * E.ldc + gr] = T[r * C::TPAD + c];
+    }
+  } else if (EPI == TC_EPI_SPLIT) {
+    for (int e = threadIdx.x; e < C::BM * C::BN; e += nth) {
+      const int r = e / C::BN, c = e % C::BN;
+      const int64_t gr = r0 + r, gc = c0 + c;
+      if (gr >= p.M || gc >= p.N) continue;
+      const float v = T[r * C::TPAD + c];
+      const float hi = tc::to_tf32(v);
+      E.out_hi[gr * E.ldo + gc] = hi;
+      E.out_lo[gr * E.ldo + gc] = tc::to_tf32(v - hi);
+    }
+  } else {  // TC_EPI_PRECOND: rows i < o, columns j < n = d_in + bias
+    for (int e = threadIdx.x; e < C::BM * C::BN; e += nth) {
+      const int r = e / C::BN, c = e % C::BN;
+      const int64_t i = r0 + r, j = c0 + c;
+      if (i >= p.M || j >= p.N) continue;
+      const float pr = T[r * C::TPAD + c];
+      if (j < E.d_in) {
+        const int64_t x = i * E.d_in + j;
+        if (E.ow) E.ow[x] = pr;
+        if (E.pw) {
+          const float w = E.pw[x];
+          const float m = fmaf(E.mu, E.mw[x], fmaf(E.lambda, w, pr));
+          E.mw[x] = m;
+          E.pw[x] = fmaf(-E.eta, m, w);
+        }
+      } else {
+        if (E.ob) E.ob[i] = pr;
+        if (E.pb) {
+          const float w = E.pb[i];
+          const float m = fmaf(E.mu, E.mb[i], fmaf(E.lambda, w, pr));
+          E.mb[i] = m;
+          E.pb[i] = fmaf(-E.eta, m, w);
+        }
+      }
+    }
   }
 }
 
@@ -352,56 +409,101 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t rows, int64_t
   return r == CUDA_SUCCESS;
 }
 
-template <bool kBF16>
+template <bool kBF16, int EPI>
 bool set_smem_attr() {
   static bool done = false;
   static bool ok = false;
   if (!done) {
-    ok = cudaFuncSetAttribute(syrk_tc_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    ok = cudaFuncSetAttribute(gemm_tc_kernel<kBF16, EPI>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)TcCfg<kBF16>::SMEM) == cudaSuccess;
     done = true;
   }
   return ok;
 }
 
-constexpr int kKsubTf32 = 128;   // rows per TMEM drain on the fp32 path
+constexpr int kKsubTf32 = 128;   // k elements per TMEM drain on the fp32 path
+
+template <bool kBF16, int EPI>
+kfac_status launch_kernel(unsigned grid, const CUtensorMap& ah, const CUtensorMap& al,
+                          const CUtensorMap& bh, const CUtensorMap& bl, const GemmTcParams& p,
+                          cudaStream_t st) {
+  if (!set_smem_attr<kBF16, EPI>()) return KFAC_ERR_CUDA;
+  gemm_tc_kernel<kBF16, EPI>
+      <<<grid, TcCfg<kBF16>::THREADS, TcCfg<kBF16>::SMEM, st>>>(ah, al, bh, bl, p);
+  count_launch();
+  return check_launch();
+}
 
 }  // namespace
 
-int64_t tc_pack_pitch(int64_t rows, bool bf16) { return cdiv(rows, bf16 ? 8 : 4) * (bf16 ? 8 : 4); }
+int64_t tc_pitch(int64_t cols, bool bf16) { return cdiv(cols, bf16 ? 8 : 4) * (bf16 ? 8 : 4); }
 
 size_t tc_pack_bytes(int n, int64_t max_rows, bool bf16) {
-  const int64_t Kp = tc_pack_pitch(max_rows, bf16);
+  const int64_t Kp = tc_pitch(max_rows, bf16);
   return (size_t)n * Kp * (bf16 ? 2 : 8);
 }
 
-void tc_split_plan(int n, int64_t K, bool bf16, int* splits, int64_t* kps, int* ksub) {
-  const int nt = (int)cdiv(n, 128);
-  const int64_t tiles = (int64_t)nt * (nt + 1) / 2;
-  const int bk = bf16 ? 64 : 32;
+size_t tc_part_floats() { return (size_t)kNumSMs * 128 * 128; }
+
+// Split-K plan: enough CTAs for one wave when the output has fewer tiles than
+// SMs, splits on ksub boundaries, at least 256 k-elements per split.
+void tc_split_plan(int64_t tiles, int64_t K, bool bf16, int* splits, int64_t* kps, int* ksub) {
   int64_t s = std::max<int64_t>(1, kNumSMs / tiles);
   s = std::min<int64_t>(s, std::max<int64_t>(1, K / 256));
-  const int64_t unit = bf16 ? bk : kKsubTf32;
-  int64_t per = cdiv(cdiv(K, s), unit) * unit;
+  const int64_t unit = bf16 ? 64 : kKsubTf32;
+  const int64_t per = cdiv(cdiv(K, s), unit) * unit;
   *splits = (int)cdiv(K, per);
   *kps = per;
   *ksub = bf16 ? (int)std::min<int64_t>(per, 1 << 30) : kKsubTf32;
 }
 
-size_t tc_part_floats(int n, int64_t max_rows, bool bf16) {
-  const int nt = (int)cdiv(n, 128);
-  const int64_t tiles = (int64_t)nt * (nt + 1) / 2;
-  const int64_t s = std::max<int64_t>(1, kNumSMs / tiles);  // upper bound of the plan
-  (void)max_rows;
-  (void)bf16;
-  return s > 1 ? (size_t)(tiles * s) * 128 * 128 : 0;
+kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcOperand& A,
+                           const TcOperand& B, bool same_ab, bool upper, int64_t M, int64_t N,
+                           int64_t K, const TcEpilogue& e, cudaStream_t st) {
+  CUtensorMap ah, al, bh, bl;
+  if (!make_map(&ah, A.hi, bf16, A.rows, K, A.pitch)) return KFAC_ERR_CUDA;
+  if (!make_map(&bh, B.hi, bf16, B.rows, K, B.pitch)) return KFAC_ERR_CUDA;
+  if (bf16) {
+    al = ah;
+    bl = bh;
+  } else {
+    if (!make_map(&al, A.lo, false, A.rows, K, A.pitch)) return KFAC_ERR_CUDA;
+    if (!make_map(&bl, B.lo, false, B.rows, K, B.pitch)) return KFAC_ERR_CUDA;
+  }
+  GemmTcParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.tiles_n = (int)cdiv(N, 128);
+  p.upper = upper ? 1 : 0;
+  p.nt = (int)cdiv(N, 128);
+  p.same_ab = same_ab ? 1 : 0;
+  const int64_t tiles = upper ? (int64_t)p.nt * (p.nt + 1) / 2 : cdiv(M, 128) * p.tiles_n;
+  tc_split_plan(tiles, K, bf16, &p.splits, &p.k_per_split, &p.ksub);
+  p.part = h->at<float>(h->off_part);
+  p.tickets = h->at<int>(h->off_tickets);
+  p.status = h->status();
+  p.layer = layer;
+  p.e = e;
+  if (p.splits > 1 && ((size_t)(tiles * p.splits) * 128 * 128 > h->part_floats ||
+                       (size_t)tiles > h->n_tickets))
+    return KFAC_ERR_WORKSPACE;
+  const unsigned grid = (unsigned)(tiles * p.splits);
+  if (epi == TC_EPI_SYRK)
+    return bf16 ? launch_kernel<true, TC_EPI_SYRK>(grid, ah, al, bh, bl, p, st)
+                : launch_kernel<false, TC_EPI_SYRK>(grid, ah, al, bh, bl, p, st);
+  if (bf16) return KFAC_ERR_UNSUPPORTED;
+  if (epi == TC_EPI_SPLIT) return launch_kernel<false, TC_EPI_SPLIT>(grid, ah, al, bh, bl, p, st);
+  return launch_kernel<false, TC_EPI_PRECOND>(grid, ah, al, bh, bl, p, st);
 }
 
-// F <- beta F + alpha x-hat^T x-hat on the tensor cores.
+// F <- beta F + alpha x-hat^T x-hat on the tensor cores (K1).
 kfac_status launch_syrk_tc(kfac_ctx* h, int layer, const void* x, int64_t ld, int64_t rows, int d,
                            int n, int has_bias, bool bf16, float alpha, float beta, float* F,
                            cudaStream_t st) {
-  const int64_t Kp = tc_pack_pitch(rows, bf16);
+  (void)has_bias;  // n > d exactly when the ones column is present
+  const int64_t Kp = tc_pitch(rows, bf16);
   if ((size_t)n * Kp * (bf16 ? 2 : 8) > h->tcpack_bytes) return KFAC_ERR_WORKSPACE;
   void* hi = h->ws + h->off_tcpack;
   void* lo = bf16 ? nullptr : (void*)(h->ws + h->off_tcpack + (size_t)n * Kp * 4);
@@ -416,36 +518,13 @@ kfac_status launch_syrk_tc(kfac_ctx* h, int layer, const void* x, int64_t ld, in
     count_launch();
     if (kfac_status e = check_launch()) return e;
   }
-  CUtensorMap mh, ml;
-  if (!make_map(&mh, hi, bf16, n, rows, Kp)) return KFAC_ERR_CUDA;
-  if (!bf16 && !make_map(&ml, lo, false, n, rows, Kp)) return KFAC_ERR_CUDA;
-  if (bf16) ml = mh;
-  SyrkTcParams p{};
-  p.n = n;
-  p.K = rows;
-  p.nt = (int)cdiv(n, 128);
-  tc_split_plan(n, rows, bf16, &p.splits, &p.k_per_split, &p.ksub);
-  p.alpha = alpha;
-  p.beta = beta;
-  p.C = F;
-  p.part = h->at<float>(h->off_part);
-  p.tickets = h->at<int>(h->off_tickets);
-  p.status = h->status();
-  p.layer = layer;
-  const int64_t tiles = (int64_t)p.nt * (p.nt + 1) / 2;
-  if (p.splits > 1 && (size_t)(tiles * p.splits) * 128 * 128 > h->part_floats)
-    return KFAC_ERR_WORKSPACE;
-  if (p.splits > 1 && (size_t)tiles > h->n_tickets) return KFAC_ERR_WORKSPACE;
-  const unsigned grid = (unsigned)(tiles * p.splits);
-  if (bf16) {
-    if (!set_smem_attr<true>()) return KFAC_ERR_CUDA;
-    syrk_tc_kernel<true><<<grid, TcCfg<true>::THREADS, TcCfg<true>::SMEM, st>>>(mh, ml, p);
-  } else {
-    if (!set_smem_attr<false>()) return KFAC_ERR_CUDA;
-    syrk_tc_kernel<false><<<grid, TcCfg<false>::THREADS, TcCfg<false>::SMEM, st>>>(mh, ml, p);
-  }
-  count_launch();
-  return check_launch();
+  TcOperand X{hi, lo, n, Kp};
+  TcEpilogue e{};
+  e.alpha = alpha;
+  e.beta = beta;
+  e.C = F;
+  e.ldc = n;
+  return launch_gemm_tc(h, layer, bf16, TC_EPI_SYRK, X, X, true, true, n, n, rows, e, st);
 }
 
 }  // namespace kfac

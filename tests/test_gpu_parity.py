@@ -3,8 +3,10 @@
 Tolerances (relative Frobenius unless stated):
   factors A, G (fp32 or bf16 inputs, oracle fed the same rounded inputs)  1e-5
   preconditioned gradient P and updated W                                 1e-4
-  diagonal step P, W, m (same fp32 diagonal vectors on both sides)        1e-6 elementwise
-     (relative to max(|x*|, 1e-3 max|x*|), since m and W are sums that can cancel)
+  diagonal factors (elementwise)                                          1e-5
+  diagonal step P, W, m, EMA vectors (same fp32 inputs and state)         1e-6 elementwise,
+     relative to the magnitude of the terms forming each element (m and W are sums
+     that can cancel); the free-running trajectory within 1e-6 relative Frobenius
 """
 import math
 
@@ -170,7 +172,7 @@ def test_invert_reports_not_positive_definite():
 def test_precondition_and_update_match_oracle(M, d_in, o, bias):
     h = K.Kfac([(K.KFAC_KRON, o, d_in, bias, K.KFAC_F32)], max_rows=M, **HP)
     st = O.LayerState("kron", o, d_in, bias, np.zeros((o, d_in)), np.zeros(o) if bias else None)
-    orc = _orc()
+    orc = _orc(invert_every=2)
     w0 = (RNG.standard_normal((o, d_in)) * 0.1).astype(np.float32)
     b0 = (RNG.standard_normal(o) * 0.1).astype(np.float32) if bias else None
     st.W = O.grad_hat(w0, b0).copy()
@@ -182,7 +184,7 @@ def test_precondition_and_update_match_oracle(M, d_in, o, bias):
         gw = (RNG.standard_normal((o, d_in)) * 1e-3).astype(np.float32)
         gb = (RNG.standard_normal(o) * 1e-3).astype(np.float32) if bias else None
         h.update_factors(0, to_dev(a), to_dev(g))
-        if t == 0:
+        if t % 2 == 0:
             h.invert(0)
         ow = torch.empty(o, d_in, device="cuda")
         ob = torch.empty(o, device="cuda") if bias else None
@@ -208,22 +210,42 @@ def test_diag_factors_match_oracle(M, d_in, o, bias, dtype):
     gn = torch.empty(o, device="cuda")
     an = torch.empty(d_in + bias, device="cuda")
     h.diag_factors(0, _dev_in(a, dtype), _dev_in(g, dtype), gn, an)
-    assert max_rel_elem(to_np(gn), O.diag_factor(g, 0), 0) <= 2e-6
-    assert max_rel_elem(to_np(an), O.diag_factor(a, bias), 0) <= 2e-6
+    # diagonal factors are factors: same 1e-5 bound, here held elementwise
+    assert max_rel_elem(to_np(gn), O.diag_factor(g, 0), 0) <= 1e-5
+    assert max_rel_elem(to_np(an), O.diag_factor(a, bias), 0) <= 1e-5
+
+
+def _componentwise(x, ref, scale):
+    """max |x - ref| / scale, scale = sum of the magnitudes of the terms forming ref."""
+    x, ref, scale = (np.asarray(v, np.float64) for v in (x, ref, scale))
+    return float(np.max(np.abs(x - ref) / np.maximum(scale, 1e-30)))
 
 
 @pytest.mark.parametrize("o,d_in,bias", [(64, 256, 1), (33, 5, 1), (128, 1, 1), (7, 12, 0),
                                          (300, 1024, 1)])
 def test_diag_step_elementwise(o, d_in, bias):
+    """Each step starts both sides from the GPU's fp32 state; every element of P, m, W and
+    of the EMA vectors must agree to 1e-6 relative to the magnitude of the terms that
+    form it (P = dW/(g a + gamma) is a quotient, so that is |P|; m = mu m + P + lambda W
+    is a sum, so that is mu|m| + |P| + lambda|W|; W - eta m: |W| + eta|m|)."""
     h = K.Kfac([(K.KFAC_DIAG, o, d_in, bias, K.KFAC_F32)], max_rows=1, **HP)
     n = d_in + bias
+    xi, gam, eta, mu, lam = (HP[k] for k in ("ema_decay", "damping", "lr", "momentum",
+                                             "weight_decay"))
     st = O.LayerState("diag", o, d_in, bias, np.zeros((o, d_in)), np.zeros(o) if bias else None)
     orc = _orc()
     w0 = (RNG.standard_normal((o, d_in)) * 0.1).astype(np.float32)
     b0 = (RNG.standard_normal(o) * 0.1).astype(np.float32) if bias else None
-    st.W = O.grad_hat(w0, b0).copy()
     pw, pb = to_dev(w0), (to_dev(b0) if bias else None)
+    bo = lambda x, y: O.grad_hat(to_np(x), to_np(y) if bias else None)
+    traj = O.LayerState("diag", o, d_in, bias, w0, b0)
     for t in range(4):
+        mw, mb = h.momentum(0)
+        st.W, st.m = bo(pw, pb), bo(mw, mb)
+        st.gs = to_np(h.state(0, K.KFAC_STATE_GDIAG))
+        st.as_ = to_np(h.state(0, K.KFAC_STATE_ADIAG))
+        st.t = t
+        W_old, m_old, gs_old, as_old = st.W.copy(), st.m.copy(), st.gs.copy(), st.as_.copy()
         gn = RNG.uniform(0, 2e-6, o).astype(np.float32)
         an = RNG.uniform(0, 2, n).astype(np.float32)
         gw = (RNG.standard_normal((o, d_in)) * 1e-3).astype(np.float32)
@@ -233,13 +255,17 @@ def test_diag_step_elementwise(o, d_in, bias):
         h.diag_step(0, to_dev(gn), to_dev(an), to_dev(gw), to_dev(gb) if bias else None, pw, pb,
                     ow, ob)
         P = orc.step_diag(st, gn, an, gw, gb)
-        bo = lambda x, y: O.grad_hat(to_np(x), to_np(y) if bias else None)
-        assert max_rel_elem(bo(ow, ob), P) <= 1e-6
-        assert max_rel_elem(bo(pw, pb), st.W) <= 1e-6
+        orc.step_diag(traj, gn, an, gw, gb)
         mw, mb = h.momentum(0)
-        assert max_rel_elem(bo(mw, mb), st.m) <= 1e-6
-        assert max_rel_elem(to_np(h.state(0, K.KFAC_STATE_GDIAG)), st.gs) <= 1e-6
-        assert max_rel_elem(to_np(h.state(0, K.KFAC_STATE_ADIAG)), st.as_) <= 1e-6
+        assert _componentwise(bo(ow, ob), P, np.abs(P)) <= 1e-6
+        assert _componentwise(bo(mw, mb), st.m, mu * np.abs(m_old) + np.abs(P) + lam * np.abs(W_old)) <= 1e-6
+        assert _componentwise(bo(pw, pb), st.W, np.abs(W_old) + eta * np.abs(st.m)) <= 1e-6
+        assert _componentwise(to_np(h.state(0, K.KFAC_STATE_GDIAG)), st.gs,
+                              xi * np.abs(gs_old) + (1 - xi) * np.abs(gn)) <= 1e-6
+        assert _componentwise(to_np(h.state(0, K.KFAC_STATE_ADIAG)), st.as_,
+                              xi * np.abs(as_old) + (1 - xi) * np.abs(an)) <= 1e-6
+    # and the free-running 4-step trajectory stays within 1e-6 (relative Frobenius)
+    assert rel_fro(bo(pw, pb), traj.W) <= 1e-6
 
 
 # ------------------------------------------------------------------ whole configs
@@ -290,7 +316,7 @@ def _run_config_small(cfg_name, steps, check_every=1):
                 h.diag_step(li, gn, an, to_dev(x["grad_w"]), to_dev(gb), pw, pb)
                 orc.step_diag(states[li], O.diag_factor(x["g"]), O.diag_factor(x["a"], l.has_bias),
                               x["grad_w"], gb)
-                worst["Wdiag"] = max(worst["Wdiag"], max_rel_elem(
+                worst["Wdiag"] = max(worst["Wdiag"], rel_fro(
                     O.grad_hat(to_np(pw), to_np(pb)), states[li].W))
     assert h.get_status()[0] == 0
     return worst
