@@ -69,6 +69,7 @@ syrk_simt_kernel(const SyrkJob* __restrict__ jobs, SyrkJob job0) {
   __shared__ float smem[Tile::kSmemFloats];
   __shared__ int s_last;
   const SyrkJob j = jobs ? jobs[blockIdx.y] : job0;
+  if (j.skip) return;
   const int tiles = j.nt * (j.nt + 1) / 2;
   if ((int)blockIdx.x >= tiles * j.splits) return;
   const int tile = blockIdx.x / j.splits, split = blockIdx.x % j.splits;

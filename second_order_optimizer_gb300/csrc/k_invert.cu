@@ -49,6 +49,13 @@ __global__ void __launch_bounds__(256) inv_prep_kernel(const InvJob* jobs, float
   }
 }
 
+// Diagonal block b x b (b <= 64) at (k, k): L_kk = chol(block) and X_kk = L_kk^{-1}
+// in one pass.  256 threads as a 16 x 16 grid; thread (ty, tx) owns rows
+// ty + 16i and columns tx + 16j (i, j < 4) of both S (-> L) and T (-> L^{-1}).
+// Step j: read column j, the pivot and row j of T; barrier; then
+//   S[r][j] = S[r][j]/sqrt(d),  S[r][c] -= l_rj l_cj        (j < c <= r)
+//   T[j][c] = T[j][c]/sqrt(d),  T[r][c] -= l_rj T[j][c]/sqrt(d)   (r > j, c <= j)
+// (right-looking Cholesky and forward elimination of [L | I] share the column).
 __global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int k,
                                                         DevStatus* st) {
   const InvJob J = jobs[blockIdx.x];
@@ -57,43 +64,49 @@ __global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int 
   const int n = J.n;
   __shared__ float S[NB][NB + 1];
   __shared__ float T[NB][NB + 1];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   for (int e = tid; e < NB * NB; e += blockDim.x) {
     const int r = e / NB, c = e % NB;
     S[r][c] = (r < b && c <= r) ? J.L[(int64_t)(k + r) * n + k + c] : 0.f;
-    T[r][c] = 0.f;
+    T[r][c] = (r == c) ? 1.f : 0.f;
   }
   __syncthreads();
   for (int j = 0; j < b; ++j) {
-    if (tid == 0) {
-      float d = S[j][j];
-      if (!(d > 0.f) || !isfinite(d)) {
-        report_error(st, KFAC_ERR_NOT_PD, J.layer, k + j);
-        d = 1.f;
+    float d = S[j][j];
+    float srj[4], scj[4], tjc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      srj[i] = S[ty + 16 * i][j];
+      scj[i] = S[tx + 16 * i][j];
+      tjc[i] = T[j][tx + 16 * i];
+    }
+    __syncthreads();
+    if (!(d > 0.f) || !isfinite(d)) {
+      if (tid == 0) report_error(st, KFAC_ERR_NOT_PD, J.layer, k + j);
+      d = 1.f;
+    }
+    const float sq = sqrtf(d);
+    const float inv = 1.f / sq;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = ty + 16 * i;
+      if (r >= b) continue;
+      const float lr = srj[i] * inv;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c = tx + 16 * q;
+        const float tj = tjc[q] * inv;              // final T[j][c]
+        if (r > j && c > j && c <= r) S[r][c] = fmaf(-lr, scj[q] * inv, S[r][c]);
+        if (c == j && r > j) S[r][c] = lr;
+        if (r == j && c == j) S[r][c] = sq;
+        if (c <= j) {
+          if (r == j) T[r][c] = tj;
+          else if (r > j) T[r][c] = fmaf(-lr, tj, T[r][c]);
+        }
       }
-      S[j][j] = sqrtf(d);
-    }
-    __syncthreads();
-    const float piv = S[j][j];
-    for (int i = j + 1 + tid; i < b; i += blockDim.x) S[i][j] = S[i][j] / piv;
-    __syncthreads();
-    const int w = b - j - 1;
-    for (int e = tid; e < w * w; e += blockDim.x) {
-      const int r = j + 1 + e / w, c = j + 1 + e % w;
-      if (c <= r) S[r][c] = fmaf(-S[r][j], S[c][j], S[r][c]);
     }
     __syncthreads();
   }
-  // T = S^{-1}: thread c forms column c by forward substitution
-  if (tid < b) {
-    const int c = tid;
-    for (int i = c; i < b; ++i) {
-      float v = (i == c) ? 1.f : 0.f;
-      for (int t = c; t < i; ++t) v = fmaf(-S[i][t], T[t][c], v);
-      T[i][c] = v / S[i][i];
-    }
-  }
-  __syncthreads();
   for (int e = tid; e < b * b; e += blockDim.x) {
     const int r = e / b, c = e % b;
     const int64_t g = (int64_t)(k + r) * n + k + c;
@@ -301,8 +314,22 @@ kfac_status launch_invert(kfac_ctx* h, int layer, cudaStream_t st) {
     count_launch(2);
     if (kfac_status e = check_launch()) return e;
   }
-  const int ntm = (int)cdiv(nmax, SyrkTile::BM);
-  if (kfac_status e = launch_syrk_simt_grouped(d_syrk + j0, nj, ntm * (ntm + 1) / 2, st)) return e;
+  // F_d^{-1} = X^T X: small factors in one grouped CUDA-core launch, large ones on the
+  // tensor cores (pack X^T into TF32 halves, 3xTF32 SYRK)
+  int nt_small = 0;
+  for (int i = j0; i < j0 + nj; ++i)
+    if (h->invjobs_host[i].n < kTcInverseMinN)
+      nt_small = std::max(nt_small, (int)cdiv(h->invjobs_host[i].n, SyrkTile::BM));
+  if (nt_small > 0)
+    if (kfac_status e = launch_syrk_simt_grouped(d_syrk + j0, nj, nt_small * (nt_small + 1) / 2, st))
+      return e;
+  for (int i = j0; i < j0 + nj; ++i) {
+    const InvJob& J = h->invjobs_host[i];
+    if (J.n < kTcInverseMinN) continue;
+    if (kfac_status e = launch_syrk_tc(h, J.layer, J.X, J.n, J.n, J.n, J.n, 0, false, 1.f, 0.f,
+                                       J.Finv, st))
+      return e;
+  }
   inv_split_kernel<<<dim3((unsigned)std::min<int64_t>(cdiv((int64_t)nmax * nmax, 256), 1024), nj),
                      256, 0, st>>>(jobs);
   count_launch();

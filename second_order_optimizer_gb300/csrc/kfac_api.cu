@@ -88,6 +88,9 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
       const bool bf = d.in_dtype == KFAC_BF16;
       part = std::max(part, tc_part_floats());
       tcpack = std::max({tcpack, tc_pack_bytes(L.n, max_rows, bf), tc_pack_bytes(L.o, max_rows, bf)});
+      // the inverse assembly packs X = L^{-1} (n x n, fp32) through the same buffer
+      if (L.n >= kTcInverseMinN) tcpack = std::max(tcpack, tc_pack_bytes(L.n, L.n, false));
+      if (L.o >= kTcInverseMinN) tcpack = std::max(tcpack, tc_pack_bytes(L.o, L.o, false));
       tickets = std::max({tickets, t1, t2, (size_t)kNumSMs});
       k4 = std::max(k4, 2 * o * np + 2 * n * op);
       ninv += 2;
@@ -249,6 +252,7 @@ kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_
       s.nt = (int)cdiv(n, SyrkTile::BM);
       s.splits = 1;
       s.rows_per_split = n;
+      s.skip = n >= kTcInverseMinN ? 1 : 0;
       sj.push_back(s);
     }
   }

@@ -11,6 +11,7 @@
 namespace kfac {
 
 constexpr int kNumSMs = 152;           // GB300: 2 dies x 76 SMs
+constexpr int kTcInverseMinN = 512;    // inverse assembly X^T X on the tensor cores from this n
 constexpr size_t kAlign = 256;
 
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }

@@ -24,6 +24,7 @@ struct SyrkJob {
   int64_t rows_per_split;
   float* part;           // splits > 1: partial tiles [tiles][splits][BM*BN]
   int* tickets;          // splits > 1: one counter per tile, zero between launches
+  int skip;              // grouped launches: job handled elsewhere (tensor-core path)
 };
 
 void syrk_split_plan(int n, int64_t rows, int* splits_out, int64_t* rows_per_split_out);

@@ -264,49 +264,82 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
   if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
   if (*abort_flag) return;
 
-  const int nth = C::THREADS;
+  // Epilogue loops run in batches of U elements per thread: all global loads of a
+  // batch are issued before any store, so load latency overlaps instead of
+  // serialising behind possibly-aliasing stores.
+  constexpr int nth = C::THREADS;
+  constexpr int NT = C::BM * C::BN;
+  constexpr int U = 16;
   if (p.splits > 1) {
-    float* part = p.part + (size_t)tile * p.splits * (C::BM * C::BN);
-    for (int e = threadIdx.x; e < C::BM * C::BN; e += nth)
-      part[(size_t)split * (C::BM * C::BN) + e] = T[(e / C::BN) * C::TPAD + e % C::BN];
+    float* part = p.part + (size_t)tile * p.splits * NT;
+    for (int e = threadIdx.x; e < NT; e += nth)
+      part[(size_t)split * NT + e] = T[(e / C::BN) * C::TPAD + e % C::BN];
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) *s_last = (atomicAdd(&p.tickets[tile], 1) == p.splits - 1);
     __syncthreads();
     if (!*s_last) return;
     __threadfence();
-    for (int e = threadIdx.x; e < C::BM * C::BN; e += nth) {
-      float v = 0.f;
-      for (int s = 0; s < p.splits; ++s) v += __ldcg(part + (size_t)s * (C::BM * C::BN) + e);
-      T[(e / C::BN) * C::TPAD + e % C::BN] = v;
+    for (int b0 = threadIdx.x; b0 < NT; b0 += nth * U) {
+      float acc[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = b0 + u * nth;
+        acc[u] = e < NT ? __ldcg(part + e) : 0.f;
+      }
+      for (int s = 1; s < p.splits; ++s) {
+        float v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int e = b0 + u * nth;
+          v[u] = e < NT ? __ldcg(part + (size_t)s * NT + e) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc[u] += v[u];
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = b0 + u * nth;
+        if (e < NT) T[(e / C::BN) * C::TPAD + e % C::BN] = acc[u];
+      }
     }
     if (threadIdx.x == 0) p.tickets[tile] = 0;
     __syncthreads();
   }
-  const int r0 = ti * C::BM, c0 = tj * C::BN;
+  const int64_t r0 = (int64_t)ti * C::BM, c0 = (int64_t)tj * C::BN;
   const TcEpilogue& E = p.e;
   if (EPI == TC_EPI_SYRK) {
     // tile entries (r <= c): F[r][c] = alpha*acc + beta*F[r][c]; T keeps the result
-    for (int e = threadIdx.x; e < C::BM * C::BN; e += nth) {
-      const int r = e / C::BN, c = e % C::BN;
-      const int64_t gr = r0 + r, gc = c0 + c;
-      if (gr >= p.M || gc >= p.N || gr > gc) continue;
-      float* dst = E.C + gr * E.ldc + gc;
-      float v = E.alpha * T[r * C::TPAD + c];
-      if (E.beta != 0.f) v = fmaf(E.beta, *dst, v);
-      *dst = v;
-      T[r * C::TPAD + c] = v;
+    for (int b0 = threadIdx.x; b0 < NT; b0 += nth * U) {
+      float old[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = b0 + u * nth;
+        const int64_t gr = r0 + e / C::BN, gc = c0 + e % C::BN;
+        const bool ok = e < NT && gr < p.M && gc < p.N && gr <= gc;
+        old[u] = (ok && E.beta != 0.f) ? E.C[gr * E.ldc + gc] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = b0 + u * nth;
+        const int r = e / C::BN, c = e % C::BN;
+        const int64_t gr = r0 + r, gc = c0 + c;
+        if (!(e < NT && gr < p.M && gc < p.N && gr <= gc)) continue;
+        const float v = fmaf(E.beta, old[u], E.alpha * T[r * C::TPAD + c]);
+        E.C[gr * E.ldc + gc] = v;
+        T[r * C::TPAD + c] = v;
+      }
     }
     __syncthreads();
     // mirrors (gr < gc): F[gc][gr], coalesced over gr
-    for (int e = threadIdx.x; e < C::BM * C::BN; e += nth) {
+    for (int e = threadIdx.x; e < NT; e += nth) {
       const int c = e / C::BM, r = e % C::BM;
       const int64_t gr = r0 + r, gc = c0 + c;
       if (gr >= p.M || gc >= p.N || gr >= gc) continue;
       E.C[gc * E.ldc + gr] = T[r * C::TPAD + c];
     }
   } else if (EPI == TC_EPI_SPLIT) {
-    for (int e = threadIdx.x; e < C::BM * C::BN; e += nth) {
+    for (int e = threadIdx.x; e < NT; e += nth) {
       const int r = e / C::BN, c = e % C::BN;
       const int64_t gr = r0 + r, gc = c0 + c;
       if (gr >= p.M || gc >= p.N) continue;
@@ -316,27 +349,45 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
       E.out_lo[gr * E.ldo + gc] = tc::to_tf32(v - hi);
     }
   } else {  // TC_EPI_PRECOND: rows i < o, columns j < n = d_in + bias
-    for (int e = threadIdx.x; e < C::BM * C::BN; e += nth) {
-      const int r = e / C::BN, c = e % C::BN;
-      const int64_t i = r0 + r, j = c0 + c;
-      if (i >= p.M || j >= p.N) continue;
-      const float pr = T[r * C::TPAD + c];
-      if (j < E.d_in) {
-        const int64_t x = i * E.d_in + j;
-        if (E.ow) E.ow[x] = pr;
-        if (E.pw) {
-          const float w = E.pw[x];
-          const float m = fmaf(E.mu, E.mw[x], fmaf(E.lambda, w, pr));
-          E.mw[x] = m;
-          E.pw[x] = fmaf(-E.eta, m, w);
+    for (int b0 = threadIdx.x; b0 < NT; b0 += nth * U) {
+      float w[U], m[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = b0 + u * nth;
+        const int64_t i = r0 + e / C::BN, j = c0 + e % C::BN;
+        w[u] = m[u] = 0.f;
+        if (E.pw && e < NT && i < p.M && j < p.N) {
+          if (j < E.d_in) {
+            w[u] = E.pw[i * E.d_in + j];
+            m[u] = E.mw[i * E.d_in + j];
+          } else {
+            w[u] = E.pb[i];
+            m[u] = E.mb[i];
+          }
         }
-      } else {
-        if (E.ob) E.ob[i] = pr;
-        if (E.pb) {
-          const float w = E.pb[i];
-          const float m = fmaf(E.mu, E.mb[i], fmaf(E.lambda, w, pr));
-          E.mb[i] = m;
-          E.pb[i] = fmaf(-E.eta, m, w);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = b0 + u * nth;
+        const int r = e / C::BN, c = e % C::BN;
+        const int64_t i = r0 + r, j = c0 + c;
+        if (!(e < NT && i < p.M && j < p.N)) continue;
+        const float pr = T[r * C::TPAD + c];
+        const float mn = fmaf(E.mu, m[u], fmaf(E.lambda, w[u], pr));
+        const float wn = fmaf(-E.eta, mn, w[u]);
+        if (j < E.d_in) {
+          const int64_t x = i * E.d_in + j;
+          if (E.ow) E.ow[x] = pr;
+          if (E.pw) {
+            E.mw[x] = mn;
+            E.pw[x] = wn;
+          }
+        } else {
+          if (E.ob) E.ob[i] = pr;
+          if (E.pb) {
+            E.mb[i] = mn;
+            E.pb[i] = wn;
+          }
         }
       }
     }

@@ -227,7 +227,8 @@ def test_diag_step_elementwise(o, d_in, bias):
     """Each step starts both sides from the GPU's fp32 state; every element of P, m, W and
     of the EMA vectors must agree to 1e-6 relative to the magnitude of the terms that
     form it (P = dW/(g a + gamma) is a quotient, so that is |P|; m = mu m + P + lambda W
-    is a sum, so that is mu|m| + |P| + lambda|W|; W - eta m: |W| + eta|m|)."""
+    is a sum, so that is mu|m| + |P| + lambda|W|; W - eta m expands to
+    W - eta (mu m + P + lambda W): |W| + eta (mu|m| + |P| + lambda|W|))."""
     h = K.Kfac([(K.KFAC_DIAG, o, d_in, bias, K.KFAC_F32)], max_rows=1, **HP)
     n = d_in + bias
     xi, gam, eta, mu, lam = (HP[k] for k in ("ema_decay", "damping", "lr", "momentum",
@@ -259,7 +260,8 @@ def test_diag_step_elementwise(o, d_in, bias):
         mw, mb = h.momentum(0)
         assert _componentwise(bo(ow, ob), P, np.abs(P)) <= 1e-6
         assert _componentwise(bo(mw, mb), st.m, mu * np.abs(m_old) + np.abs(P) + lam * np.abs(W_old)) <= 1e-6
-        assert _componentwise(bo(pw, pb), st.W, np.abs(W_old) + eta * np.abs(st.m)) <= 1e-6
+        m_terms = mu * np.abs(m_old) + np.abs(P) + lam * np.abs(W_old)
+        assert _componentwise(bo(pw, pb), st.W, np.abs(W_old) + eta * m_terms) <= 1e-6
         assert _componentwise(to_np(h.state(0, K.KFAC_STATE_GDIAG)), st.gs,
                               xi * np.abs(gs_old) + (1 - xi) * np.abs(gn)) <= 1e-6
         assert _componentwise(to_np(h.state(0, K.KFAC_STATE_ADIAG)), st.as_,
