@@ -345,23 +345,29 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     # dominant phase -> roofline
     names = ["factor", "invert", "precond", "diag"]
     dom = names[int(np.argmax(phase_ms))]
+    tf32_peak = peaks["bf16_tflops"] * TF32_PER_BF16
     if dom == "diag":
         roof = {"bound": "hbm", "achieved": round(diag_gbs, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "kernel": "diag_factor_kernel + diag_step_kernel"}
-    else:
-        flop = {"factor": acc["factor_flop"], "invert": acc["invert_flop"] * k,
-                "precond": acc["precond_flop"]}[dom]
-        ms = {"factor": phase_ms[0], "invert": inv_ms_refresh, "precond": phase_ms[2]}[dom]
+    elif dom in ("factor", "precond"):
+        flop = acc["factor_flop"] if dom == "factor" else acc["precond_flop"]
+        ms = phase_ms[0] if dom == "factor" else phase_ms[2]
         ach = flop / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 3), "peak": round(tf32_peak, 1),
+                "unit": "TFLOP/s", "kernel": "gemm_tc_kernel (3xTF32, tcgen05)",
+                "issued_frac": round(3 * ach / tf32_peak, 4),
+                "note": "algorithmic flops (upper triangle for factors); 3xTF32 issues 3x"}
+    else:
+        ach = acc["invert_flop"] * k / (inv_ms_refresh * 1e-3) / 1e12
         roof = {"bound": "alu", "achieved": round(ach, 3), "peak": round(FP32_ALU_TFLOPS, 1),
-                "unit": "TFLOP/s", "kernel": {"factor": "syrk_simt_kernel",
-                                              "invert": "chol_*/tri_level_*/syrk_simt_kernel",
-                                              "precond": "precond_x_kernel + precond_p_kernel"}[dom]}
+                "unit": "TFLOP/s", "kernel": "chol_diag/chol_panel/chol_trailing/tri_level"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = None
     roof["phase"] = dom
-    roof["peak_source"] = ("derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz"
-                           if roof["bound"] == "alu" else f"{peak_kind} MEASURED_PEAKS / fallback")
+    roof["peak_source"] = {
+        "hbm": f"{peak_kind} HBM copy bandwidth",
+        "tensor": f"{peak_kind} bf16 dense x 1.1/2.25 (nominal TF32:bf16 ratio)",
+        "alu": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz"}[roof["bound"]]
 
     e2e = None
     if not args.no_e2e:

@@ -50,69 +50,93 @@ __global__ void __launch_bounds__(256) inv_prep_kernel(const InvJob* jobs, float
 }
 
 // Diagonal block b x b (b <= 64) at (k, k): L_kk = chol(block) and X_kk = L_kk^{-1}
-// in one pass.  256 threads as a 16 x 16 grid; thread (ty, tx) owns rows
-// ty + 16i and columns tx + 16j (i, j < 4) of both S (-> L) and T (-> L^{-1}).
-// Step j: read column j, the pivot and row j of T; barrier; then
-//   S[r][j] = S[r][j]/sqrt(d),  S[r][c] -= l_rj l_cj        (j < c <= r)
-//   T[j][c] = T[j][c]/sqrt(d),  T[r][c] -= l_rj T[j][c]/sqrt(d)   (r > j, c <= j)
-// (right-looking Cholesky and forward elimination of [L | I] share the column).
+// in one pass.  256 threads as a 16 x 16 grid; thread (ty, tx) keeps rows
+// ty + 16i and columns tx + 16q (i, q < 4) of both S (-> L) and T (-> L^{-1},
+// starting from I) in registers.  Step j: the owners publish column j of S and
+// row j of T to a double-buffered shared vector (one barrier per step), then
+// every thread updates its own elements:
+//   S[r][j] = S[r][j]/sqrt(d),  S[r][c] -= l_rj l_cj                 (j < c <= r)
+//   T[j][c] = T[j][c]/sqrt(d),  T[r][c] -= l_rj T[j][c]/sqrt(d)      (r > j, c <= j)
+// i.e. a right-looking Cholesky and the forward elimination of [L | I] sharing
+// the column l_j.
+__device__ __forceinline__ float pick4(const float (&v)[4], int q) {
+  return q == 0 ? v[0] : q == 1 ? v[1] : q == 2 ? v[2] : v[3];
+}
+
 __global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int k,
                                                         DevStatus* st) {
   const InvJob J = jobs[blockIdx.x];
   if (k >= J.n) return;
   const int b = min(NB, J.n - k);
   const int n = J.n;
-  __shared__ float S[NB][NB + 1];
-  __shared__ float T[NB][NB + 1];
+  __shared__ float colS[2][NB];
+  __shared__ float rowT[2][NB];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  for (int e = tid; e < NB * NB; e += blockDim.x) {
-    const int r = e / NB, c = e % NB;
-    S[r][c] = (r < b && c <= r) ? J.L[(int64_t)(k + r) * n + k + c] : 0.f;
-    T[r][c] = (r == c) ? 1.f : 0.f;
-  }
-  __syncthreads();
-  for (int j = 0; j < b; ++j) {
-    float d = S[j][j];
-    float srj[4], scj[4], tjc[4];
+  float S[4][4], T[4][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      srj[i] = S[ty + 16 * i][j];
-      scj[i] = S[tx + 16 * i][j];
-      tjc[i] = T[j][tx + 16 * i];
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = ty + 16 * i, c = tx + 16 * q;
+      S[i][q] = (r < b && c <= r) ? J.L[(int64_t)(k + r) * n + k + c] : 0.f;
+      T[i][q] = (r == c) ? 1.f : 0.f;
+    }
+  for (int j = 0; j < b; ++j) {
+    const int buf = j & 1;
+    if (tx == (j & 15)) {
+      const int q = j >> 4;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) colS[buf][ty + 16 * i] = pick4(S[i], q);
+    }
+    if (ty == (j & 15)) {
+      const int i = j >> 4;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float v = i == 0 ? T[0][q] : i == 1 ? T[1][q] : i == 2 ? T[2][q] : T[3][q];
+        rowT[buf][tx + 16 * q] = v;
+      }
     }
     __syncthreads();
+    float d = colS[buf][j];
     if (!(d > 0.f) || !isfinite(d)) {
       if (tid == 0) report_error(st, KFAC_ERR_NOT_PD, J.layer, k + j);
       d = 1.f;
     }
     const float sq = sqrtf(d);
     const float inv = 1.f / sq;
+    float lr[4], lc[4], tj[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      lr[i] = colS[buf][ty + 16 * i] * inv;
+      lc[i] = colS[buf][tx + 16 * i] * inv;
+      tj[i] = rowT[buf][tx + 16 * i] * inv;
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int r = ty + 16 * i;
-      if (r >= b) continue;
-      const float lr = srj[i] * inv;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int c = tx + 16 * q;
-        const float tj = tjc[q] * inv;              // final T[j][c]
-        if (r > j && c > j && c <= r) S[r][c] = fmaf(-lr, scj[q] * inv, S[r][c]);
-        if (c == j && r > j) S[r][c] = lr;
-        if (r == j && c == j) S[r][c] = sq;
+        if (r > j && c > j && c <= r) S[i][q] = fmaf(-lr[i], lc[q], S[i][q]);
+        else if (c == j && r > j) S[i][q] = lr[i];
+        else if (r == j && c == j) S[i][q] = sq;
         if (c <= j) {
-          if (r == j) T[r][c] = tj;
-          else if (r > j) T[r][c] = fmaf(-lr, tj, T[r][c]);
+          if (r == j) T[i][q] = tj[q];
+          else if (r > j) T[i][q] = fmaf(-lr[i], tj[q], T[i][q]);
         }
       }
     }
-    __syncthreads();
   }
-  for (int e = tid; e < b * b; e += blockDim.x) {
-    const int r = e / b, c = e % b;
-    const int64_t g = (int64_t)(k + r) * n + k + c;
-    J.L[g] = (c <= r) ? S[r][c] : 0.f;
-    J.X[g] = (c <= r) ? T[r][c] : 0.f;
-  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = ty + 16 * i, c = tx + 16 * q;
+      if (r >= b || c >= b) continue;
+      const int64_t g = (int64_t)(k + r) * n + k + c;
+      J.L[g] = (c <= r) ? S[i][q] : 0.f;
+      J.X[g] = (c <= r) ? T[i][q] : 0.f;
+    }
 }
 
 // L[i, k:k+b] <- L[i, k:k+b] . X_kk^T for rows i in [k+b, n); one CTA owns a

@@ -12,30 +12,46 @@ namespace kfac {
 template <int BM, int BN, int BK, int TM, int TN>
 struct SimtTile {
   static constexpr int kThreads = (BM / TM) * (BN / TN);
-  static constexpr int kSmemFloats = BK * (BM + BN);
+  static constexpr int kLA = BK * BM / kThreads;  // A elements per thread per k-chunk
+  static constexpr int kLB = BK * BN / kThreads;
+  static constexpr int kSmemFloats = 2 * BK * (BM + BN);   // double-buffered
+  static_assert(BK * BM % kThreads == 0 && BK * BN % kThreads == 0, "even split of loads");
 
+  // The next k-chunk is loaded into registers while the current one is being
+  // multiplied out of shared memory (one barrier per chunk).
   template <class LA, class LB>
   __device__ __forceinline__ static void run(const LA& la, const LB& lb, long long m0, long long n0,
                                              long long k0, long long k1, float (&acc)[TM][TN],
                                              float* smem) {
-    float* As = smem;            // [BK][BM]
-    float* Bs = smem + BK * BM;  // [BK][BN]
     const int tid = threadIdx.x;
     const int tx = tid % (BN / TN), ty = tid / (BN / TN);
+    float ra[kLA], rb[kLB];
+    auto fetch = [&](long long kk) {
+#pragma unroll
+      for (int u = 0; u < kLA; ++u) {
+        const int e = tid + u * kThreads;
+        const long long gk = kk + e / BM;
+        ra[u] = (gk < k1) ? la(m0 + e % BM, gk) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kLB; ++u) {
+        const int e = tid + u * kThreads;
+        const long long gk = kk + e / BN;
+        rb[u] = (gk < k1) ? lb(gk, n0 + e % BN) : 0.f;
+      }
+    };
+    if (k0 >= k1) return;
+    fetch(k0);
+    int buf = 0;
     for (long long kk = k0; kk < k1; kk += BK) {
+      float* As = smem + buf * BK * (BM + BN);  // [BK][BM]
+      float* Bs = As + BK * BM;                 // [BK][BN]
 #pragma unroll
-      for (int e = tid; e < BK * BM; e += kThreads) {
-        int k = e / BM, m = e % BM;
-        long long gk = kk + k;
-        As[e] = (gk < k1) ? la(m0 + m, gk) : 0.f;
-      }
+      for (int u = 0; u < kLA; ++u) As[tid + u * kThreads] = ra[u];
 #pragma unroll
-      for (int e = tid; e < BK * BN; e += kThreads) {
-        int k = e / BN, n = e % BN;
-        long long gk = kk + k;
-        Bs[e] = (gk < k1) ? lb(gk, n0 + n) : 0.f;
-      }
+      for (int u = 0; u < kLB; ++u) Bs[tid + u * kThreads] = rb[u];
       __syncthreads();
+      if (kk + BK < k1) fetch(kk + BK);
 #pragma unroll
       for (int k = 0; k < BK; ++k) {
         float a[TM], b[TN];
@@ -48,8 +64,9 @@ struct SimtTile {
 #pragma unroll
           for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
       }
-      __syncthreads();
+      buf ^= 1;
     }
+    __syncthreads();  // the caller may reuse smem after return
   }
 
   __device__ __forceinline__ static int row_of(int i) {
