@@ -182,6 +182,26 @@ kfac_status kfac_destroy(kfac_handle h);
 /* Static description of a status code. */
 const char* kfac_status_string(kfac_status s);
 
+/* K5 without a handle or workspace, for callers that cannot allocate device
+ * memory (no cudaMalloc, no caller-provided workspace): for instance code that
+ * runs under another framework's allocator, or a plug-in whose host owns all
+ * device allocations.  The paper has no counterpart to this entry point; it
+ * computes exactly what kfac_diag_factors computes for a layer with these
+ * dimensions (same kernel, same row splits, same results).
+ * Scratch: a static device array of about 1.4 MiB (partial sums) plus 4 KiB
+ * (counters) that every GPU which loads the library keeps until process exit.
+ * Limit: d_in + d_out <= 262144, else KFAC_ERR_WORKSPACE.  Allocates nothing:
+ * no cudaMalloc/cudaFree, no allocating library call.  The first call on a
+ * device looks up the array's device address on that device (make that first
+ * call before any stream capture).  Every call shares the one array and it
+ * keeps the last call's contents: calls that overlap on the GPU (other
+ * streams, other threads) race; order them.  Arguments as kfac_diag_factors
+ * plus the layer shape: in_dtype is a kfac_dtype, scale <= 0 means 1/rows. */
+kfac_status kfac_diag_factors_static(const void* a, int64_t lda, const void* g, int64_t ldg,
+                                     int64_t rows, int d_in, int d_out, int has_bias,
+                                     int in_dtype, double scale, float* g_new, float* a_new,
+                                     cudaStream_t stream);
+
 /* Diagnostics: number of kernels this library has launched in this process. */
 unsigned long long kfac_launch_count(void);
 

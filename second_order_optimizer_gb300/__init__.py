@@ -19,7 +19,7 @@ from ._lib import (LIB, KFAC_KRON, KFAC_DIAG, KFAC_F32, KFAC_BF16, KFAC_MATH_3XT
                    KFAC_STATE_GDIAG, KFAC_STATE_ADIAG, LayerDesc, HParams, KfacError,
                    status_string, launch_count)
 
-__all__ = ["Kfac", "LayerDesc", "HParams", "KfacError", "status_string", "launch_count",
+__all__ = ["Kfac", "diag_factors_static", "LayerDesc", "HParams", "KfacError", "status_string", "launch_count",
            "KFAC_KRON", "KFAC_DIAG", "KFAC_F32", "KFAC_BF16", "KFAC_MATH_3XTF32",
            "KFAC_MATH_BF16", "KFAC_EMA_INIT_ZERO", "KFAC_EMA_INIT_FIRST", "LIB"]
 
@@ -160,3 +160,16 @@ class Kfac:
         mw = v[:d.d_out * d.d_in].view(d.d_out, d.d_in)
         mb = v[d.d_out * d.d_in:] if d.has_bias else None
         return mw, mb
+
+
+def diag_factors_static(a, g, g_new, a_new, has_bias: int = 1, rows: Optional[int] = None,
+                        scale: float = 0.0, stream=None):
+    """kfac_diag_factors_static: the diagonal factors of one layer without a handle or
+    workspace (for callers that cannot allocate device memory; see include/kfac.h)."""
+    import torch
+    rows = a.shape[0] if rows is None else rows
+    dt = KFAC_BF16 if a.dtype == torch.bfloat16 else KFAC_F32
+    _check(LIB.kfac_diag_factors_static(_ptr(a), a.stride(0), _ptr(g), g.stride(0), rows,
+                                        a.shape[1], g.shape[1], has_bias, dt, float(scale),
+                                        _ptr(g_new), _ptr(a_new), _stream(stream)),
+           "kfac_diag_factors_static")

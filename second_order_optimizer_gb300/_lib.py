@@ -62,6 +62,8 @@ SIGNATURES = [
     ("kfac_destroy", _i, [_vp]),
     ("kfac_status_string", ctypes.c_char_p, [_i]),
     ("kfac_launch_count", ctypes.c_ulonglong, []),
+    ("kfac_diag_factors_static", _i, [_vp, _i64, _vp, _i64, _i64, _i, _i, _i, _i, _d, _vp, _vp,
+                                      _vp]),
 ]
 
 for _name, _res, _args in SIGNATURES:

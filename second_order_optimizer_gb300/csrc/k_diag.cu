@@ -17,6 +17,7 @@
 #include "kfac_internal.cuh"
 
 #include <algorithm>
+#include <mutex>
 
 namespace kfac {
 
@@ -265,3 +266,98 @@ kfac_status launch_diag_step(kfac_ctx* h, int layer, float decay, const float* g
 }
 
 }  // namespace kfac
+
+// ---------------------------------------------------------------------------
+// Workspace-free variant of K5 for callers that cannot allocate device memory.
+//
+// Some embedders cannot call cudaMalloc or hand the library a workspace: code
+// running inside another framework's allocator-controlled region, a plugin
+// host that owns every device allocation, or a process that must not grow its
+// device footprint after start-up.  For them the scratch of this one kernel
+// (row-split partial sums and per-column-block tickets) lives in file-scope
+// device arrays that every GPU loading the library holds until process exit.
+namespace kfac {
+namespace {
+
+constexpr int kStaticMaxCols = 262144;                  // d_in + d_out limit
+constexpr int kStaticMaxColBlocks = kStaticMaxCols / kK5Threads;   // 1024
+// splits * cols <= (ceil(2*SMs / blocks)) * blocks * 256 <= 2*SMs*256 + cols
+constexpr size_t kStaticScratchFloats = 2 * kNumSMs * kK5Threads + kStaticMaxCols;
+
+static __device__ __align__(256) float g_k5_static_part[kStaticScratchFloats];
+static __device__ __align__(256) int g_k5_static_tickets[kStaticMaxColBlocks];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mutex;
+float* g_static_part_ptr[kMaxDevices] = {};
+int* g_static_tickets_ptr[kMaxDevices] = {};
+
+// Device addresses of the static arrays on the current device, looked up once
+// per device (the names above are host-side stand-ins, not device addresses).
+kfac_status static_scratch(float** part, int** tickets) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KFAC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_static_mutex);
+  if (!g_static_part_ptr[dev]) {
+    void* p = nullptr;
+    void* t = nullptr;
+    if (cudaGetSymbolAddress(&p, g_k5_static_part) != cudaSuccess) return KFAC_ERR_CUDA;
+    if (cudaGetSymbolAddress(&t, g_k5_static_tickets) != cudaSuccess) return KFAC_ERR_CUDA;
+    g_static_part_ptr[dev] = static_cast<float*>(p);
+    g_static_tickets_ptr[dev] = static_cast<int*>(t);
+  }
+  *part = g_static_part_ptr[dev];
+  *tickets = g_static_tickets_ptr[dev];
+  return KFAC_OK;
+}
+
+}  // namespace
+}  // namespace kfac
+
+extern "C" kfac_status kfac_diag_factors_static(const void* a, int64_t lda, const void* g,
+                                                int64_t ldg, int64_t rows, int d_in, int d_out,
+                                                int has_bias, int in_dtype, double scale,
+                                                float* g_new, float* a_new, cudaStream_t stream) {
+  using namespace kfac;
+  if (!a || !g || !g_new || !a_new) return KFAC_ERR_INVALID_ARG;
+  if (d_in < 1 || d_out < 1 || (has_bias != 0 && has_bias != 1)) return KFAC_ERR_INVALID_ARG;
+  if (in_dtype != KFAC_F32 && in_dtype != KFAC_BF16) return KFAC_ERR_INVALID_ARG;
+  if (rows < 1 || lda < d_in || ldg < d_out || !(scale == scale)) return KFAC_ERR_INVALID_ARG;
+  const size_t es = in_dtype == KFAC_BF16 ? 2 : 4;
+  if ((uintptr_t)a % es || (uintptr_t)g % es || (uintptr_t)g_new % 4 || (uintptr_t)a_new % 4)
+    return KFAC_ERR_INVALID_ARG;
+  if ((int64_t)d_in + d_out > kStaticMaxCols) return KFAC_ERR_WORKSPACE;
+  float* part = nullptr;
+  int* tickets = nullptr;
+  if (kfac_status e = static_scratch(&part, &tickets)) return e;
+  DiagFactorParams p{};
+  p.a = a;
+  p.g = g;
+  p.lda = lda;
+  p.ldg = ldg;
+  p.rows = rows;
+  const int ncols = d_in + d_out;
+  const int64_t sp = k5_splits(ncols, rows);
+  p.rows_per_split = cdiv(rows, sp);
+  p.splits = (int)cdiv(rows, p.rows_per_split);
+  p.d_in = d_in;
+  p.o = d_out;
+  p.has_bias = has_bias;
+  p.col_blocks = (int)cdiv(ncols, kK5Threads);
+  p.s = (float)(scale > 0 ? scale : 1.0 / (double)rows);
+  p.part = part;
+  p.tickets = tickets;
+  p.g_new = g_new;
+  p.a_new = a_new;
+  if ((size_t)p.splits * ncols > kStaticScratchFloats) return KFAC_ERR_WORKSPACE;
+  // the tickets must start at zero; a call interrupted earlier may have left them dirty
+  if (cudaMemsetAsync(tickets, 0, sizeof(int) * p.col_blocks, stream) != cudaSuccess)
+    return KFAC_ERR_CUDA;
+  dim3 grid(p.col_blocks, p.splits);
+  if (in_dtype == KFAC_BF16)
+    diag_factor_kernel<__nv_bfloat16><<<grid, kK5Threads, 0, stream>>>(p);
+  else
+    diag_factor_kernel<float><<<grid, kK5Threads, 0, stream>>>(p);
+  count_launch();
+  return check_launch();
+}
