@@ -47,6 +47,13 @@ def parse():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    # single-kernel mode: time one phase on one layer shape (not the headline line)
+    p.add_argument("--micro", choices=["factor", "precond", "invert", "diag"], default=None)
+    p.add_argument("--n", type=int, default=8193, help="micro: A dimension (d_in + 1)")
+    p.add_argument("--o", type=int, default=2048, help="micro: G dimension (d_out)")
+    p.add_argument("--rows", type=int, default=16384, help="micro: rows M")
+    p.add_argument("--dtype", choices=["f32", "bf16"], default="bf16")
+    p.add_argument("--reps", type=int, default=10)
     return p.parse_args()
 
 
@@ -425,6 +432,82 @@ def run_e2e(args, h, layers, x_dev, params, k, t, dev, step):
             "d2h_bytes_per_step": int(d2h), "steps": steps}
 
 
+# ----------------------------------------------------------------------------- micro
+
+def run_micro(args, peaks, peak_kind):
+    """Time one phase on one layer shape with CUDA events (L2 flushed between reps)."""
+    import torch
+    import second_order_optimizer_gb300 as K
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n, o, M = args.n, args.o, args.rows
+    d_in = n - 1
+    kd = K.KFAC_BF16 if args.dtype == "bf16" else K.KFAC_F32
+    tdt = torch.bfloat16 if args.dtype == "bf16" else torch.float32
+    kind = K.KFAC_DIAG if args.micro == "diag" else K.KFAC_KRON
+    h = K.Kfac([(kind, o, d_in, 1, kd)], max_rows=M, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1)
+    a = torch.randn(M, d_in, generator=gen, device=dev).clamp_(min=0).to(tdt)
+    g = (torch.randn(M, o, generator=gen, device=dev) * 1e-4).to(tdt)
+    gw = torch.randn(o, d_in, generator=gen, device=dev) * 1e-6
+    gb = torch.randn(o, generator=gen, device=dev) * 1e-6
+    pw = torch.randn(o, d_in, generator=gen, device=dev) * 0.01
+    pb = torch.zeros(o, device=dev)
+    gn = torch.rand(o, generator=gen, device=dev) * 1e-8
+    an = torch.rand(n, generator=gen, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    if kind == K.KFAC_KRON:
+        h.update_factors(0, a, g)
+        h.invert(0)
+
+    def once():
+        if args.micro == "factor":
+            h.update_factors(0, a, g)
+        elif args.micro == "invert":
+            h.invert(0)
+        elif args.micro == "precond":
+            h.precondition(0, gw, gb, None, None, pw, pb)
+        else:
+            h.diag_step(0, gn, an, gw, gb, pw, pb)
+
+    for _ in range(3):
+        once()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        once()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    code = h.get_status()[0]
+    ms = float(np.median(ts))
+    elt = 2 if args.dtype == "bf16" else 4
+    tf32_peak = peaks["bf16_tflops"] * TF32_PER_BF16
+    if args.micro == "factor":
+        flop = M * n * (n + 1) + M * o * (o + 1)
+        peak = peaks["bf16_tflops"] if args.dtype == "bf16" else tf32_peak
+        res = {"tflops": flop / ms / 1e9, "peak_tflops": peak, "frac": flop / ms / 1e9 / peak,
+               "bytes_in": M * (d_in + o) * elt}
+    elif args.micro == "precond":
+        flop = 2 * o * n * n + 2 * o * o * n
+        res = {"tflops": flop / ms / 1e9, "peak_tflops": tf32_peak,
+               "frac": flop / ms / 1e9 / tf32_peak}
+    elif args.micro == "invert":
+        flop = n ** 3 + o ** 3
+        res = {"tflops": flop / ms / 1e9}
+    else:
+        byts = 20 * o * n + 8 * (o + n)
+        res = {"gbs": byts / ms / 1e6, "peak_gbs": peaks["hbm_gbs"],
+               "frac": byts / ms / 1e6 / peaks["hbm_gbs"]}
+    out = {"micro": args.micro, "n": n, "o": o, "rows": M, "dtype": args.dtype, "ms": round(ms, 4),
+           "status": code, "peaks": peak_kind, **{k: round(v, 4) for k, v in res.items()}}
+    print(json.dumps(out), flush=True)
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -432,6 +515,9 @@ def main():
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     peaks, peak_kind = load_peaks()
+    if args.micro:
+        run_micro(args, peaks, peak_kind)
+        return
     cfg, layers = bench_config(args.workload)
 
     if args.impl == "reference":
