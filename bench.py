@@ -47,6 +47,7 @@ def parse():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-graphs", action="store_true", help="time eager calls, not CUDA graphs")
     # single-kernel mode: time one phase on one layer shape (not the headline line)
     p.add_argument("--micro", choices=["factor", "precond", "invert", "diag"], default=None)
     p.add_argument("--n", type=int, default=8193, help="micro: A dimension (d_in + 1)")
@@ -271,20 +272,21 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(t, x, ev=None):
-        if ev: ev[0].record(stream)
+    def phase_factor(x):
         for li, l in enumerate(layers):
             if l.kind == "kron":
                 h.update_factors(li, x[li]["a"], x[li]["g"])
-        if ev: ev[1].record(stream)
-        if (t - 1) % k == 0:
-            h.invert(-1)
-        if ev: ev[2].record(stream)
+
+    def phase_invert():
+        h.invert(-1)
+
+    def phase_precond(x):
         for li, l in enumerate(layers):
             if l.kind == "kron":
                 pw, pb = params[li]
                 h.precondition(li, x[li]["grad_w"], x[li]["grad_b"], None, None, pw, pb)
-        if ev: ev[3].record(stream)
+
+    def phase_diag(x):
         for li, l in enumerate(layers):
             if l.kind == "diag":
                 pw, pb = params[li]
@@ -294,6 +296,18 @@ def run_gpu(args, rank, world, peaks, peak_kind):
                     h.diag_factors(li, x[li]["a"], x[li]["g"], gnew[li], anew[li])
                     gn, an = gnew[li], anew[li]
                 h.diag_step(li, gn, an, x[li]["grad_w"], x[li]["grad_b"], pw, pb)
+
+    def step(t, x, ev=None):
+        """The eager step through the public API (used for warm-up and end-to-end)."""
+        if ev: ev[0].record(stream)
+        phase_factor(x)
+        if ev: ev[1].record(stream)
+        if (t - 1) % k == 0:
+            phase_invert()
+        if ev: ev[2].record(stream)
+        phase_precond(x)
+        if ev: ev[3].record(stream)
+        phase_diag(x)
         if ev: ev[4].record(stream)
 
     t = 0
@@ -305,6 +319,45 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     if code:
         raise RuntimeError(f"device status {code} after warm-up")
 
+    # Each phase of each input batch is captured once into a CUDA graph; a timed step
+    # replays the four phase graphs (the inverse refresh only on refresh steps), with
+    # events on the replay stream between them.  Capture runs every library call once
+    # (that work is discarded by the steps that follow: the state evolves as usual).
+    graphs = {}
+    kernels_in = {}
+    if not args.no_graphs:
+        for b in range(NB):
+            for name, fn in (("factor", lambda b=b: phase_factor(data[b])),
+                             ("precond", lambda b=b: phase_precond(data[b])),
+                             ("diag", lambda b=b: phase_diag(data[b]))):
+                g = torch.cuda.CUDAGraph()
+                c0 = K.launch_count()
+                with torch.cuda.graph(g):
+                    fn()
+                graphs[(name, b)] = g
+                kernels_in[(name, b)] = K.launch_count() - c0
+        g = torch.cuda.CUDAGraph()
+        c0 = K.launch_count()
+        with torch.cuda.graph(g):
+            phase_invert()
+        graphs[("invert", 0)] = g
+        kernels_in[("invert", 0)] = K.launch_count() - c0
+        torch.cuda.synchronize()
+
+    def step_graph(t, b, ev):
+        ev[0].record(stream)
+        graphs[("factor", b)].replay()
+        ev[1].record(stream)
+        if (t - 1) % k == 0:
+            graphs[("invert", 0)].replay()
+        ev[2].record(stream)
+        graphs[("precond", b)].replay()
+        ev[3].record(stream)
+        graphs[("diag", b)].replay()
+        ev[4].record(stream)
+        return (kernels_in[("factor", b)] + kernels_in[("precond", b)] + kernels_in[("diag", b)]
+                + (kernels_in[("invert", 0)] if (t - 1) % k == 0 else 0))
+
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     sampler = ClockSampler(dev.index)
     if world > 1:
@@ -312,16 +365,20 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     torch.cuda.synchronize()
     sampler.start()
     l0 = K.launch_count()
+    graph_launches = 0
     wall0 = time.perf_counter()
     refreshed = []
     for i in range(args.steps):
         t += 1
         refreshed.append((t - 1) % k == 0)
         flush.zero_()                         # L2 flush outside the step's events
-        step(t, data[t % NB], evs[i])
+        if graphs:
+            graph_launches += step_graph(t, t % NB, evs[i])
+        else:
+            step(t, data[t % NB], evs[i])
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    launches = K.launch_count() - l0
+    launches = K.launch_count() - l0 + graph_launches
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
@@ -386,6 +443,7 @@ def run_gpu(args, rank, world, peaks, peak_kind):
                    "kron_layers": sum(l.kind == "kron" for l in layers),
                    "diag_layers": sum(l.kind == "diag" for l in layers),
                    "invert_every": k, "max_rows": max_rows,
+                   "cuda_graphs": not args.no_graphs,
                    "l2": "flushed between steps (256 MiB write, outside the per-step events)"},
     }
 

@@ -33,6 +33,7 @@
 #include "kfac_internal.cuh"
 #include "tc_prims.cuh"
 
+#include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -42,18 +43,21 @@ namespace kfac {
 
 namespace {
 
-template <bool kBF16>
+template <bool kBF16, int BN_>
 struct TcCfg {
-  static constexpr int BM = 128, BN = 128;
+  static constexpr int BM = 128, BN = BN_;         // UMMA 128 x BN per CTA (BN 128 or 256)
+  static constexpr int R = BN / BM;                // B tile = R stacked A-sized tiles
   static constexpr int ELT = kBF16 ? 2 : 4;
   static constexpr int BK = 128 / ELT;            // k elements per 128-byte row
   static constexpr int KMMA = 32 / ELT;           // k elements per MMA (32 bytes)
-  static constexpr int TILE_BYTES = BM * 128;     // one operand tile: 16 KB
-  static constexpr int OPS = kBF16 ? 2 : 4;       // A(hi), B(hi), [A lo, B lo]
-  static constexpr int STAGE_BYTES = OPS * TILE_BYTES;
-  static constexpr int STAGES = kBF16 ? 6 : 3;
-  static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr int THREADS = 192;
+  static constexpr int A_BYTES = BM * 128;        // A operand tile: 16 KB
+  static constexpr int B_BYTES = BN * 128;        // B operand tile: 32 KB
+  static constexpr int HALF_BYTES = A_BYTES + B_BYTES;           // hi (or bf16) part
+  static constexpr int STAGE_BYTES = kBF16 ? HALF_BYTES : 2 * HALF_BYTES;
+  static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;   // 192 KB of stages
+  static constexpr int TMEM_COLS = 2 * BN;        // double-buffered accumulator
+  static constexpr int EPI_WARPS = 4 * R;         // R per TMEM lane quarter, 128 columns each
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int TPAD = BN + 1;             // output staging row pitch (floats)
   static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
   static_assert((size_t)BM * TPAD * 4 <= (size_t)STAGES * STAGE_BYTES, "staging fits");
@@ -62,9 +66,11 @@ struct TcCfg {
 struct GemmTcParams {
   int64_t M, N, K;
   int tiles_n;           // full grid: tile t -> (t / tiles_n, t % tiles_n)
-  int upper, nt;         // upper: tiles (ti <= tj) of an nt x nt triangle
+  int upper;             // upper: only tiles reaching the upper triangle (SYRK, M == N)
+  int tiles_m;           // tile rows (128 each)
   int same_ab;           // A and B are the same operand (diagonal tiles load once)
   int splits;
+  int cluster_reduce;    // splits form one thread-block cluster, reduced through DSMEM
   int64_t k_per_split;   // multiple of ksub
   int ksub;              // k elements per TMEM drain (multiple of BK)
   float* part;
@@ -74,23 +80,34 @@ struct GemmTcParams {
   TcEpilogue e;
 };
 
-__device__ __forceinline__ void upper_tile(int t, int nt, int* ti, int* tj) {
-  int r = 0;
-  while (t >= nt - r) {
-    t -= nt - r;
-    ++r;
-  }
-  *ti = r;
-  *tj = r + t;
+// Tiles of 128 rows x (R*128) columns that reach the upper triangle: column block
+// tj holds row blocks ti <= R tj + R - 1 (and ti < tiles_m); t enumerates them
+// column by column.
+__host__ __device__ inline int64_t upper_tile_count(int tiles_m, int tiles_n, int R) {
+  int64_t c = 0;
+  for (int tj = 0; tj < tiles_n; ++tj) c += (R * tj + R < tiles_m ? R * tj + R : tiles_m);
+  return c;
 }
 
-template <bool kBF16, int EPI>
-__global__ void __launch_bounds__(TcCfg<kBF16>::THREADS, 1)
+__device__ __forceinline__ void upper_tile(int t, int tiles_m, int R, int* ti, int* tj) {
+  int j = 0;
+  for (;;) {
+    const int cnt = R * j + R < tiles_m ? R * j + R : tiles_m;
+    if (t < cnt) break;
+    t -= cnt;
+    ++j;
+  }
+  *ti = t;
+  *tj = j;
+}
+
+template <bool kBF16, int BN, int EPI>
+__global__ void __launch_bounds__(TcCfg<kBF16, BN>::THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
                const __grid_constant__ CUtensorMap map_a_lo,
                const __grid_constant__ CUtensorMap map_b_hi,
                const __grid_constant__ CUtensorMap map_b_lo, GemmTcParams p) {
-  using C = TcCfg<kBF16>;
+  using C = TcCfg<kBF16, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
@@ -106,12 +123,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
   const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
   int ti, tj;
   if (p.upper) {
-    upper_tile(tile, p.nt, &ti, &tj);
+    upper_tile(tile, p.tiles_m, C::R, &ti, &tj);
   } else {
     ti = tile / p.tiles_n;
     tj = tile % p.tiles_n;
   }
-  const bool diag = p.same_ab && ti == tj;
+  // A rows inside the B tile (same operand, ti / R == tj): read A out of B's smem
+  const int a_in_b = (p.same_ab && ti / C::R == tj) ? ti % C::R + 1 : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -120,7 +138,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&acc_full[b], 1);
-      tc::mbar_init(&acc_empty[b], 128);
+      tc::mbar_init(&acc_empty[b], 32 * C::EPI_WARPS);
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -145,13 +163,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
   const int nkb = kend > kbeg ? (int)((kend - kbeg + C::BK - 1) / C::BK) : 0;
   const int kb_per_sub = p.ksub / C::BK;
   const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
-  auto stage_ptr = [&](int s, int op) { return smem + (size_t)s * C::STAGE_BYTES + op * C::TILE_BYTES; };
+  // stage layout: [A hi 16 KB][B hi 32 KB] ([A lo][B lo] for 3xTF32)
+  auto a_ptr = [&](int s, int lo) {
+    return smem + (size_t)s * C::STAGE_BYTES + lo * C::HALF_BYTES;
+  };
+  auto b_ptr = [&](int s, int lo) { return a_ptr(s, lo) + C::A_BYTES; };
+  auto a_src = [&](int s, int lo) {  // where the MMA reads A from
+    return a_in_b ? b_ptr(s, lo) + (a_in_b - 1) * C::A_BYTES : a_ptr(s, lo);
+  };
 
   if (warp == 0) {
     if (lane == 0) {  // ------------------------------------------ TMA producer
       int stage = 0;
       uint32_t phase = 0;
-      const uint32_t bytes = (diag ? C::OPS / 2 : C::OPS) * C::TILE_BYTES;
+      const uint32_t bytes = (a_in_b ? C::B_BYTES : C::HALF_BYTES) * (kBF16 ? 1 : 2);
       for (int kb = 0; kb < nkb; ++kb) {
         if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
           *abort_flag = 1;
@@ -160,11 +185,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
         }
         const int k0 = (int)(kbeg + (int64_t)kb * C::BK);
         tc::mbar_expect_tx(&full[stage], bytes);
-        tc::tma_load_2d(stage_ptr(stage, 0), &map_a_hi, &full[stage], k0, ti * C::BM);
-        if (!diag) tc::tma_load_2d(stage_ptr(stage, 1), &map_b_hi, &full[stage], k0, tj * C::BN);
+        if (!a_in_b) tc::tma_load_2d(a_ptr(stage, 0), &map_a_hi, &full[stage], k0, ti * C::BM);
+        tc::tma_load_2d(b_ptr(stage, 0), &map_b_hi, &full[stage], k0, tj * C::BN);
         if (!kBF16) {
-          tc::tma_load_2d(stage_ptr(stage, 2), &map_a_lo, &full[stage], k0, ti * C::BM);
-          if (!diag) tc::tma_load_2d(stage_ptr(stage, 3), &map_b_lo, &full[stage], k0, tj * C::BN);
+          if (!a_in_b) tc::tma_load_2d(a_ptr(stage, 1), &map_a_lo, &full[stage], k0, ti * C::BM);
+          tc::tma_load_2d(b_ptr(stage, 1), &map_b_lo, &full[stage], k0, tj * C::BN);
         }
         if (++stage == C::STAGES) {
           stage = 0;
@@ -196,10 +221,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
             break;
           }
           tc::tc_fence_after();
-          const uint32_t a_hi = tc::smem_u32(stage_ptr(stage, 0));
-          const uint32_t b_hi = diag ? a_hi : tc::smem_u32(stage_ptr(stage, 1));
-          const uint32_t a_lo = tc::smem_u32(stage_ptr(stage, 2));
-          const uint32_t b_lo = diag ? a_lo : tc::smem_u32(stage_ptr(stage, 3));
+          const uint32_t a_hi = tc::smem_u32(a_src(stage, 0));
+          const uint32_t b_hi = tc::smem_u32(b_ptr(stage, 0));
+          const uint32_t a_lo = tc::smem_u32(a_src(stage, kBF16 ? 0 : 1));
+          const uint32_t b_lo = tc::smem_u32(b_ptr(stage, kBF16 ? 0 : 1));
 #pragma unroll
           for (int kk = 0; kk < C::BK / C::KMMA; ++kk) {
             const uint32_t off = kk * 32;
@@ -230,11 +255,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
   // ------------------------------------------------------------ epilogue warps
   float* T = reinterpret_cast<float*>(smem);  // [BM][TPAD], reuses the stage buffers
   if (warp >= 2) {
-    const int q = warp & 3;
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;          // column half: [128 h, 128 h + 128)
     const int row = 32 * q + lane;
-    float sum[C::BN];
+    float sum[128];
 #pragma unroll
-    for (int c = 0; c < C::BN; ++c) sum[c] = 0.f;
+    for (int c = 0; c < 128; ++c) sum[c] = 0.f;
     for (int sub = 0; sub < nsub; ++sub) {
       const int buf = sub & 1;
       if (!tc::mbar_wait(&acc_full[buf], (sub >> 1) & 1, abort_flag)) {
@@ -244,33 +270,74 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
       }
       tc::tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < C::BN / 32; ++cc) {
+      for (int cc = 0; cc < 4; ++cc) {
         float v[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::BN + cc * 32), v);
+        tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) +
+                          (uint32_t)(buf * C::BN + h * 128 + cc * 32), v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) sum[cc * 32 + i] += v[i];
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&acc_empty[buf]);
     }
-    // all MMAs have completed (their last commit was waited on), so the stage
+    // every MMA has completed (the last commit was waited on), so the stage
     // buffers are free: stage the tile for coalesced output
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * C::EPI_WARPS) : "memory");
 #pragma unroll
-    for (int c = 0; c < C::BN; ++c) T[row * C::TPAD + c] = sum[c];
+    for (int c = 0; c < 128; ++c) T[row * C::TPAD + h * 128 + c] = sum[c];
   }
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
-  if (*abort_flag) return;
 
   // Epilogue loops run in batches of U elements per thread: all global loads of a
   // batch are issued before any store, so load latency overlaps instead of
   // serialising behind possibly-aliasing stores.
   constexpr int nth = C::THREADS;
   constexpr int NT = C::BM * C::BN;
-  constexpr int U = 16;
-  if (p.splits > 1) {
+  constexpr int U = 8;
+  int row_lo = 0, row_hi = C::BM;   // rows of the tile this CTA finishes
+  if (p.cluster_reduce) {
+    // Split-K through distributed shared memory: the splits of this tile are the
+    // CTAs of one cluster; CTA `split` sums rows [row_lo, row_hi) of every
+    // member's staged tile, in member order, and finishes those rows.  Every
+    // member takes both cluster barriers, whatever happened before.
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    cl.sync();
+    const int S = p.splits;
+    const int rb = (C::BM + S - 1) / S;
+    row_lo = min(C::BM, split * rb);
+    row_hi = min(C::BM, row_lo + rb);
+    if (!*abort_flag) {
+      const float* src[8];
+      for (int q = 0; q < S; ++q) src[q] = cl.map_shared_rank(T, q);
+      const int n_el = (row_hi - row_lo) * C::BN;
+      for (int b0 = threadIdx.x; b0 < n_el; b0 += nth * U) {
+        float acc[U];
+        int idx[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int e = b0 + u * nth;
+          idx[u] = e < n_el ? (row_lo + e / C::BN) * C::TPAD + e % C::BN : 0;
+          acc[u] = 0.f;
+        }
+        for (int q = 0; q < S; ++q) {
+          float v[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) v[u] = src[q][idx[u]];
+#pragma unroll
+          for (int u = 0; u < U; ++u) acc[u] += v[u];
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (b0 + u * nth < n_el) T[idx[u]] = acc[u];
+      }
+    }
+    cl.sync();  // no member reads a peer's tile after this point
+    if (*abort_flag) return;
+  } else if (p.splits > 1) {
+    if (*abort_flag) return;
     float* part = p.part + (size_t)tile * p.splits * NT;
     for (int e = threadIdx.x; e < NT; e += nth)
       part[(size_t)split * NT + e] = T[(e / C::BN) * C::TPAD + e % C::BN];
@@ -305,18 +372,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
     }
     if (threadIdx.x == 0) p.tickets[tile] = 0;
     __syncthreads();
+  } else if (*abort_flag) {
+    return;
   }
+  __syncthreads();
+  const int e_lo = row_lo * C::BN, e_hi = row_hi * C::BN;
+  const int nrows = row_hi - row_lo;
   const int64_t r0 = (int64_t)ti * C::BM, c0 = (int64_t)tj * C::BN;
   const TcEpilogue& E = p.e;
   if (EPI == TC_EPI_SYRK) {
     // tile entries (r <= c): F[r][c] = alpha*acc + beta*F[r][c]; T keeps the result
-    for (int b0 = threadIdx.x; b0 < NT; b0 += nth * U) {
+    for (int b0 = e_lo + threadIdx.x; b0 < e_hi; b0 += nth * U) {
       float old[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int e = b0 + u * nth;
         const int64_t gr = r0 + e / C::BN, gc = c0 + e % C::BN;
-        const bool ok = e < NT && gr < p.M && gc < p.N && gr <= gc;
+        const bool ok = e < e_hi && gr < p.M && gc < p.N && gr <= gc;
         old[u] = (ok && E.beta != 0.f) ? E.C[gr * E.ldc + gc] : 0.f;
       }
 #pragma unroll
@@ -324,7 +396,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
         const int e = b0 + u * nth;
         const int r = e / C::BN, c = e % C::BN;
         const int64_t gr = r0 + r, gc = c0 + c;
-        if (!(e < NT && gr < p.M && gc < p.N && gr <= gc)) continue;
+        if (!(e < e_hi && gr < p.M && gc < p.N && gr <= gc)) continue;
         const float v = fmaf(E.beta, old[u], E.alpha * T[r * C::TPAD + c]);
         E.C[gr * E.ldc + gc] = v;
         T[r * C::TPAD + c] = v;
@@ -332,14 +404,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
     }
     __syncthreads();
     // mirrors (gr < gc): F[gc][gr], coalesced over gr
-    for (int e = threadIdx.x; e < NT; e += nth) {
-      const int c = e / C::BM, r = e % C::BM;
+    for (int e = threadIdx.x; e < nrows * C::BN; e += nth) {
+      const int c = e / nrows, r = row_lo + e % nrows;
       const int64_t gr = r0 + r, gc = c0 + c;
       if (gr >= p.M || gc >= p.N || gr >= gc) continue;
       E.C[gc * E.ldc + gr] = T[r * C::TPAD + c];
     }
   } else if (EPI == TC_EPI_SPLIT) {
-    for (int e = threadIdx.x; e < NT; e += nth) {
+    for (int e = e_lo + threadIdx.x; e < e_hi; e += nth) {
       const int r = e / C::BN, c = e % C::BN;
       const int64_t gr = r0 + r, gc = c0 + c;
       if (gr >= p.M || gc >= p.N) continue;
@@ -349,14 +421,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
       E.out_lo[gr * E.ldo + gc] = tc::to_tf32(v - hi);
     }
   } else {  // TC_EPI_PRECOND: rows i < o, columns j < n = d_in + bias
-    for (int b0 = threadIdx.x; b0 < NT; b0 += nth * U) {
+    for (int b0 = e_lo + threadIdx.x; b0 < e_hi; b0 += nth * U) {
       float w[U], m[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int e = b0 + u * nth;
         const int64_t i = r0 + e / C::BN, j = c0 + e % C::BN;
         w[u] = m[u] = 0.f;
-        if (E.pw && e < NT && i < p.M && j < p.N) {
+        if (E.pw && e < e_hi && i < p.M && j < p.N) {
           if (j < E.d_in) {
             w[u] = E.pw[i * E.d_in + j];
             m[u] = E.mw[i * E.d_in + j];
@@ -371,7 +443,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
         const int e = b0 + u * nth;
         const int r = e / C::BN, c = e % C::BN;
         const int64_t i = r0 + r, j = c0 + c;
-        if (!(e < NT && i < p.M && j < p.N)) continue;
+        if (!(e < e_hi && i < p.M && j < p.N)) continue;
         const float pr = T[r * C::TPAD + c];
         const float mn = fmaf(E.mu, m[u], fmaf(E.lambda, w[u], pr));
         const float wn = fmaf(-E.eta, mn, w[u]);
@@ -443,15 +515,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // [rows x cols] row-major matrix (cols contiguous, pitch in elements), box of
-// 128 rows x 128 bytes, 128-byte swizzle, out-of-range elements read as zero.
+// box_rows rows x 128 bytes, 128-byte swizzle, out-of-range elements read as zero.
 bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t rows, int64_t cols,
-              int64_t pitch) {
+              int64_t pitch, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   const int elt = bf16 ? 2 : 4;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(pitch * elt)};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / elt), 128u};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / elt), (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1u, 1u};
   CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                   const_cast<void*>(base), dims, strides, box, estr,
@@ -460,14 +532,14 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t rows, int64_t
   return r == CUDA_SUCCESS;
 }
 
-template <bool kBF16, int EPI>
+template <bool kBF16, int BN, int EPI>
 bool set_smem_attr() {
   static bool done = false;
   static bool ok = false;
   if (!done) {
-    ok = cudaFuncSetAttribute(gemm_tc_kernel<kBF16, EPI>,
+    ok = cudaFuncSetAttribute(gemm_tc_kernel<kBF16, BN, EPI>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)TcCfg<kBF16>::SMEM) == cudaSuccess;
+                              (int)TcCfg<kBF16, BN>::SMEM) == cudaSuccess;
     done = true;
   }
   return ok;
@@ -480,13 +552,30 @@ bool set_smem_attr() {
 constexpr int kKsubTf32 = 128;
 constexpr int kKsubBf16 = 256;
 
-template <bool kBF16, int EPI>
+template <bool kBF16, int BN, int EPI>
 kfac_status launch_kernel(unsigned grid, const CUtensorMap& ah, const CUtensorMap& al,
                           const CUtensorMap& bh, const CUtensorMap& bl, const GemmTcParams& p,
                           cudaStream_t st) {
-  if (!set_smem_attr<kBF16, EPI>()) return KFAC_ERR_CUDA;
-  gemm_tc_kernel<kBF16, EPI>
-      <<<grid, TcCfg<kBF16>::THREADS, TcCfg<kBF16>::SMEM, st>>>(ah, al, bh, bl, p);
+  if (!set_smem_attr<kBF16, BN, EPI>()) return KFAC_ERR_CUDA;
+  if (p.cluster_reduce) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(TcCfg<kBF16, BN>::THREADS);
+    cfg.dynamicSmemBytes = TcCfg<kBF16, BN>::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<kBF16, BN, EPI>, ah, al, bh, bl, p) != cudaSuccess)
+      return KFAC_ERR_CUDA;
+  } else {
+    gemm_tc_kernel<kBF16, BN, EPI>
+        <<<grid, TcCfg<kBF16, BN>::THREADS, TcCfg<kBF16, BN>::SMEM, st>>>(ah, al, bh, bl, p);
+  }
   count_launch();
   return check_launch();
 }
@@ -500,7 +589,7 @@ size_t tc_pack_bytes(int n, int64_t max_rows, bool bf16) {
   return (size_t)n * Kp * (bf16 ? 2 : 8);
 }
 
-size_t tc_part_floats() { return (size_t)kNumSMs * 128 * 128; }
+size_t tc_part_floats() { return (size_t)kNumSMs * 128 * 256; }
 
 // Split-K plan: enough CTAs for one wave when the output has fewer tiles than
 // SMs, splits on ksub boundaries, at least 256 k-elements per split.
@@ -514,44 +603,63 @@ void tc_split_plan(int64_t tiles, int64_t K, bool bf16, int* splits, int64_t* kp
   *ksub = (int)unit;
 }
 
+template <int BN>
+kfac_status dispatch(bool bf16, int epi, unsigned grid, const CUtensorMap& ah,
+                     const CUtensorMap& al, const CUtensorMap& bh, const CUtensorMap& bl,
+                     const GemmTcParams& p, cudaStream_t st) {
+  if (epi == TC_EPI_SYRK)
+    return bf16 ? launch_kernel<true, BN, TC_EPI_SYRK>(grid, ah, al, bh, bl, p, st)
+                : launch_kernel<false, BN, TC_EPI_SYRK>(grid, ah, al, bh, bl, p, st);
+  if (bf16) return KFAC_ERR_UNSUPPORTED;
+  if (epi == TC_EPI_SPLIT) return launch_kernel<false, BN, TC_EPI_SPLIT>(grid, ah, al, bh, bl, p, st);
+  return launch_kernel<false, BN, TC_EPI_PRECOND>(grid, ah, al, bh, bl, p, st);
+}
+
 kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcOperand& A,
                            const TcOperand& B, bool same_ab, bool upper, int64_t M, int64_t N,
                            int64_t K, const TcEpilogue& e, cudaStream_t st) {
+  constexpr int BM = 128;
+  // Tile width: 128 x 256 halves the shared-memory traffic per MMA flop of
+  // 128 x 128, which pays on long reductions or when there are tiles enough to
+  // fill the GPU; short, small products keep 128 x 128 for parallelism.
+  auto count = [&](int bn) {
+    const int tm = (int)cdiv(M, BM), tn = (int)cdiv(N, bn);
+    return upper ? upper_tile_count(tm, tn, bn / BM) : (int64_t)tm * tn;
+  };
+  const int BN = (K >= 8192 || count(256) >= kNumSMs) ? 256 : 128;
   CUtensorMap ah, al, bh, bl;
-  if (!make_map(&ah, A.hi, bf16, A.rows, K, A.pitch)) return KFAC_ERR_CUDA;
-  if (!make_map(&bh, B.hi, bf16, B.rows, K, B.pitch)) return KFAC_ERR_CUDA;
+  if (!make_map(&ah, A.hi, bf16, A.rows, K, A.pitch, BM)) return KFAC_ERR_CUDA;
+  if (!make_map(&bh, B.hi, bf16, B.rows, K, B.pitch, BN)) return KFAC_ERR_CUDA;
   if (bf16) {
     al = ah;
     bl = bh;
   } else {
-    if (!make_map(&al, A.lo, false, A.rows, K, A.pitch)) return KFAC_ERR_CUDA;
-    if (!make_map(&bl, B.lo, false, B.rows, K, B.pitch)) return KFAC_ERR_CUDA;
+    if (!make_map(&al, A.lo, false, A.rows, K, A.pitch, BM)) return KFAC_ERR_CUDA;
+    if (!make_map(&bl, B.lo, false, B.rows, K, B.pitch, BN)) return KFAC_ERR_CUDA;
   }
   GemmTcParams p{};
   p.M = M;
   p.N = N;
   p.K = K;
-  p.tiles_n = (int)cdiv(N, 128);
+  p.tiles_m = (int)cdiv(M, BM);
+  p.tiles_n = (int)cdiv(N, BN);
   p.upper = upper ? 1 : 0;
-  p.nt = (int)cdiv(N, 128);
   p.same_ab = same_ab ? 1 : 0;
-  const int64_t tiles = upper ? (int64_t)p.nt * (p.nt + 1) / 2 : cdiv(M, 128) * p.tiles_n;
+  const int64_t tiles = count(BN);
   tc_split_plan(tiles, K, bf16, &p.splits, &p.k_per_split, &p.ksub);
+  // up to 8 splits (the portable cluster size) reduce through distributed shared memory
+  p.cluster_reduce = (p.splits > 1 && p.splits <= 8) ? 1 : 0;
   p.part = h->at<float>(h->off_part);
   p.tickets = h->at<int>(h->off_tickets);
   p.status = h->status();
   p.layer = layer;
   p.e = e;
-  if (p.splits > 1 && ((size_t)(tiles * p.splits) * 128 * 128 > h->part_floats ||
+  if (p.splits > 1 && !p.cluster_reduce && ((size_t)(tiles * p.splits) * BM * BN > h->part_floats ||
                        (size_t)tiles > h->n_tickets))
     return KFAC_ERR_WORKSPACE;
   const unsigned grid = (unsigned)(tiles * p.splits);
-  if (epi == TC_EPI_SYRK)
-    return bf16 ? launch_kernel<true, TC_EPI_SYRK>(grid, ah, al, bh, bl, p, st)
-                : launch_kernel<false, TC_EPI_SYRK>(grid, ah, al, bh, bl, p, st);
-  if (bf16) return KFAC_ERR_UNSUPPORTED;
-  if (epi == TC_EPI_SPLIT) return launch_kernel<false, TC_EPI_SPLIT>(grid, ah, al, bh, bl, p, st);
-  return launch_kernel<false, TC_EPI_PRECOND>(grid, ah, al, bh, bl, p, st);
+  return BN == 256 ? dispatch<256>(bf16, epi, grid, ah, al, bh, bl, p, st)
+                   : dispatch<128>(bf16, epi, grid, ah, al, bh, bl, p, st);
 }
 
 // F <- beta F + alpha x-hat^T x-hat on the tensor cores (K1).
