@@ -85,6 +85,25 @@ def bench_config(workload):
     return cfg, layers
 
 
+# ----------------------------------------------------------------------------- multi-rank
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank time over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ms_per_step_max: float, world: int) -> float:
+    """Whole-job steps/s: every rank runs one replica step per step (weak scaling),
+    so the job completes `world` steps in the slowest rank's step time."""
+    return world * 1e3 / ms_per_step_max
+
+
 # ----------------------------------------------------------------------------- accounting
 
 def algorithmic(layers, k):
@@ -388,10 +407,7 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     ph = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
                    for i in range(args.steps)])  # ms: factor, invert, precond, diag
     ms_step = float(ph.sum(axis=1).mean())
-    if world > 1:
-        tt = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(tt.item())
+    ms_step = max_over_ranks(ms_step, dev)
 
     acc = algorithmic(layers, k)
     phase_ms = ph.mean(axis=0)
@@ -615,7 +631,7 @@ def main():
         cpu = {"value": round(v, 6), "unit": "steps/s", "cores": blas_threads(), "kind": "oracle",
                "sample": sample, "seconds": round(spent, 1)}
     if rank == 0:
-        value = world * 1e3 / res["ms_per_step"]
+        value = job_throughput(res["ms_per_step"], world)
         line = {"metric": METRIC, "value": round(value, 3), "unit": "steps/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(res["ms_per_step"], 4), "higher_is_better": True,
