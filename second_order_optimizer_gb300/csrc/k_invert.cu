@@ -49,134 +49,97 @@ __global__ void __launch_bounds__(256) inv_prep_kernel(const InvJob* jobs, float
   }
 }
 
-// One warp factors a 32 x 32 symmetric positive-definite block held in shared
-// memory (lower triangle read) and inverts its factor, entirely in registers:
-// lane i keeps row i of L (a[]) and column i of L^{-1} (t[]).
-//   Cholesky, column j:  l_jj = sqrt(a_jj); l_ij = a_ij / l_jj; a_ic -= l_ij l_cj (c <= i)
-//   inverse, row i:      T[i][c] = (delta_ic - sum_{t<i} L[i][t] T[t][c]) / L[i][i]
-// L[i][t] is broadcast from lane i by shuffles; a failing pivot is reported and
-// replaced by 1.  Writes L (upper zeroed) to Lout and L^{-1} to Tout (ld 65).
-__device__ __forceinline__ void chol_inv32_warp(const float* S, float* Lout, float* Tout,
-                                                DevStatus* st, int layer, int col0) {
-  const unsigned full = 0xffffffffu;
-  const int lane = threadIdx.x & 31;
-  float a[32];
-#pragma unroll
-  for (int c = 0; c < 32; ++c) a[c] = (c <= lane) ? S[lane * 65 + c] : 0.f;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    float d = __shfl_sync(full, a[j], j);
-    if (!(d > 0.f) || !isfinite(d)) {
-      if (lane == 0) report_error(st, KFAC_ERR_NOT_PD, layer, col0 + j);
-      d = 1.f;
-    }
-    const float sq = sqrtf(d);
-    const float lij = a[j] / sq;
-    if (lane == j) a[j] = sq;
-    else if (lane > j) a[j] = lij;
-#pragma unroll
-    for (int c = j + 1; c < 32; ++c) {
-      const float lcj = __shfl_sync(full, lij, c);
-      if (lane >= c) a[c] = fmaf(-lij, lcj, a[c]);
-    }
-  }
-  float t[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    float v = (lane == i) ? 1.f : 0.f;
-#pragma unroll
-    for (int q = 0; q < i; ++q) v = fmaf(-__shfl_sync(full, a[q], i), t[q], v);
-    const float lii = __shfl_sync(full, a[i], i);
-    t[i] = (i >= lane) ? v / lii : 0.f;
-  }
-#pragma unroll
-  for (int c = 0; c < 32; ++c) Lout[lane * 65 + c] = (c <= lane) ? a[c] : 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) Tout[i * 65 + lane] = t[i];
+// Diagonal block b x b (b <= 64) at (k, k): L_kk = chol(block) and X_kk = L_kk^{-1}
+// in one pass.  256 threads as a 16 x 16 grid; thread (ty, tx) keeps rows
+// ty + 16i and columns tx + 16q (i, q < 4) of both S (-> L) and T (-> L^{-1},
+// starting from I) in registers.  Step j: the owners publish column j of S and
+// row j of T to a double-buffered shared vector (one barrier per step), then
+// every thread updates its own elements:
+//   S[r][j] = S[r][j]/sqrt(d),  S[r][c] -= l_rj l_cj                 (j < c <= r)
+//   T[j][c] = T[j][c]/sqrt(d),  T[r][c] -= l_rj T[j][c]/sqrt(d)      (r > j, c <= j)
+// i.e. a right-looking Cholesky and the forward elimination of [L | I] sharing
+// the column l_j.
+// (A fully unrolled one-warp 32 x 32 variant kept every value in registers but
+// compiled to tens of KB of straight-line code; it ran 2x slower, stalled on
+// instruction fetch.  This loop form stays resident in the instruction cache.)
+__device__ __forceinline__ float pick4(const float (&v)[4], int q) {
+  return q == 0 ? v[0] : q == 1 ? v[1] : q == 2 ? v[2] : v[3];
 }
 
-// Diagonal block b x b (b <= 64) at (k, k): L_kk = chol(block), X_kk = L_kk^{-1}.
-// Recursive 2 x 2 split into 32 x 32 blocks (rows/cols >= b padded with I):
-//   [warp 0] L11, X11 = chol_inv(S11)
-//   L21 = S21 X11^T ;  S22 <- S22 - L21 L21^T
-//   [warp 0] L22, X22 = chol_inv(S22)
-//   Y = L21 X11 ;  X21 = -X22 Y
 __global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int k,
                                                         DevStatus* st) {
   const InvJob J = jobs[blockIdx.x];
   if (k >= J.n) return;
   const int b = min(NB, J.n - k);
   const int n = J.n;
-  __shared__ float S[NB][NB + 1];   // input block, then L
-  __shared__ float T[NB][NB + 1];   // L^{-1}
-  __shared__ float Y[32][33];
-  const int tid = threadIdx.x, warp = tid >> 5;
-  for (int e = tid; e < NB * NB; e += blockDim.x) {
-    const int r = e / NB, c = e % NB;
-    float v = (r == c) ? 1.f : 0.f;
-    if (r < b && c < b && c <= r) v = J.L[(int64_t)(k + r) * n + k + c];
-    S[r][c] = v;
-    T[r][c] = 0.f;
-  }
-  __syncthreads();
-  if (warp == 0) chol_inv32_warp(&S[0][0], &S[0][0], &T[0][0], st, J.layer, k);
-  __syncthreads();
-  // L21[r][c] = sum_t S21[r][t] X11[c][t]   (r, c < 32) ; 256 threads x 4 outputs
-  float l21[4];
+  __shared__ float colS[2][NB];
+  __shared__ float rowT[2][NB];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  float S[4][4], T[4][4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int e = tid + 256 * q, r = e >> 5, c = e & 31;
-    float acc = 0.f;
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int t = 0; t < 32; ++t) acc = fmaf(S[32 + r][t], T[c][t], acc);
-    l21[q] = acc;
-  }
-  __syncthreads();
+    for (int q = 0; q < 4; ++q) {
+      const int r = ty + 16 * i, c = tx + 16 * q;
+      S[i][q] = (r < b && c <= r) ? J.L[(int64_t)(k + r) * n + k + c] : 0.f;
+      T[i][q] = (r == c) ? 1.f : 0.f;
+    }
+  for (int j = 0; j < b; ++j) {
+    const int buf = j & 1;
+    if (tx == (j & 15)) {
+      const int q = j >> 4;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int e = tid + 256 * q, r = e >> 5, c = e & 31;
-    S[32 + r][c] = l21[q];
-  }
-  __syncthreads();
-  // S22[r][c] -= sum_t L21[r][t] L21[c][t]   (lower part, c <= r)
+      for (int i = 0; i < 4; ++i) colS[buf][ty + 16 * i] = pick4(S[i], q);
+    }
+    if (ty == (j & 15)) {
+      const int i = j >> 4;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int e = tid + 256 * q, r = e >> 5, c = e & 31;
-    if (c <= r) {
-      float acc = 0.f;
+      for (int q = 0; q < 4; ++q) {
+        const float v = i == 0 ? T[0][q] : i == 1 ? T[1][q] : i == 2 ? T[2][q] : T[3][q];
+        rowT[buf][tx + 16 * q] = v;
+      }
+    }
+    __syncthreads();
+    float d = colS[buf][j];
+    if (!(d > 0.f) || !isfinite(d)) {
+      if (tid == 0) report_error(st, KFAC_ERR_NOT_PD, J.layer, k + j);
+      d = 1.f;
+    }
+    const float sq = sqrtf(d);
+    const float inv = 1.f / sq;
+    float lr[4], lc[4], tj[4];
 #pragma unroll
-      for (int t = 0; t < 32; ++t) acc = fmaf(S[32 + r][t], S[32 + c][t], acc);
-      S[32 + r][32 + c] -= acc;
+    for (int i = 0; i < 4; ++i) {
+      lr[i] = colS[buf][ty + 16 * i] * inv;
+      lc[i] = colS[buf][tx + 16 * i] * inv;
+      tj[i] = rowT[buf][tx + 16 * i] * inv;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = ty + 16 * i;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c = tx + 16 * q;
+        if (r > j && c > j && c <= r) S[i][q] = fmaf(-lr[i], lc[q], S[i][q]);
+        else if (c == j && r > j) S[i][q] = lr[i];
+        else if (r == j && c == j) S[i][q] = sq;
+        if (c <= j) {
+          if (r == j) T[i][q] = tj[q];
+          else if (r > j) T[i][q] = fmaf(-lr[i], tj[q], T[i][q]);
+        }
+      }
     }
   }
-  __syncthreads();
-  if (warp == 0) chol_inv32_warp(&S[32][32], &S[32][32], &T[32][32], st, J.layer, k + 32);
-  __syncthreads();
-  // Y = L21 X11 ; X21 = -X22 Y
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int e = tid + 256 * q, r = e >> 5, c = e & 31;
-    float acc = 0.f;
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int t = 0; t < 32; ++t) acc = fmaf(S[32 + r][t], T[t][c], acc);
-    Y[r][c] = acc;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int e = tid + 256 * q, r = e >> 5, c = e & 31;
-    float acc = 0.f;
-#pragma unroll
-    for (int t = 0; t < 32; ++t) acc = fmaf(T[32 + r][32 + t], Y[t][c], acc);
-    T[32 + r][c] = -acc;
-  }
-  __syncthreads();
-  for (int e = tid; e < b * b; e += blockDim.x) {
-    const int r = e / b, c = e % b;
-    const int64_t g = (int64_t)(k + r) * n + k + c;
-    J.L[g] = (c <= r) ? S[r][c] : 0.f;
-    J.X[g] = (c <= r) ? T[r][c] : 0.f;
-  }
+    for (int q = 0; q < 4; ++q) {
+      const int r = ty + 16 * i, c = tx + 16 * q;
+      if (r >= b || c >= b) continue;
+      const int64_t g = (int64_t)(k + r) * n + k + c;
+      J.L[g] = (c <= r) ? S[i][q] : 0.f;
+      J.X[g] = (c <= r) ? T[i][q] : 0.f;
+    }
 }
 
 // L[i, k:k+b] <- L[i, k:k+b] . X_kk^T for rows i in [k+b, n); one CTA owns a
