@@ -291,19 +291,25 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    kron_idx = [li for li, l in enumerate(layers) if l.kind == "kron"]
+    # batches share one input dtype
+    kron_groups = {}
+    for li in kron_idx:
+        kron_groups.setdefault(layers[li].in_dtype, []).append(li)
+
     def phase_factor(x):
-        for li, l in enumerate(layers):
-            if l.kind == "kron":
-                h.update_factors(li, x[li]["a"], x[li]["g"])
+        for grp in kron_groups.values():
+            h.update_factors_batched(grp, [x[li]["a"] for li in grp], [x[li]["g"] for li in grp])
 
     def phase_invert():
         h.invert(-1)
 
     def phase_precond(x):
-        for li, l in enumerate(layers):
-            if l.kind == "kron":
-                pw, pb = params[li]
-                h.precondition(li, x[li]["grad_w"], x[li]["grad_b"], None, None, pw, pb)
+        if kron_idx:
+            h.precondition_batched(kron_idx, [x[li]["grad_w"] for li in kron_idx],
+                                   [x[li]["grad_b"] for li in kron_idx], None, None,
+                                   [params[li][0] for li in kron_idx],
+                                   [params[li][1] for li in kron_idx])
 
     def phase_diag(x):
         for li, l in enumerate(layers):

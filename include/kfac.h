@@ -125,6 +125,18 @@ kfac_status kfac_update_factors(kfac_handle h, int layer, const void* a, int64_t
                                 const void* g, int64_t ldg, int64_t rows, double scale,
                                 cudaStream_t stream);
 
+/* K1 for several KRON layers in one pass: the same result as calling
+ * kfac_update_factors(layers[i], a[i], lda[i], g[i], ldg[i], rows[i], scale)
+ * for each i, but all inputs are packed in one launch and all the factor
+ * products run as one grouped tensor-core launch, so small layers fill the GPU
+ * together.  Host arrays of length count; each layer at most once; all layers
+ * of one in_dtype.  Layers beyond what the workspace's batch scratch holds are
+ * processed in further groups. */
+kfac_status kfac_update_factors_batched(kfac_handle h, int count, const int* layers,
+                                        const void* const* a, const int64_t* lda,
+                                        const void* const* g, const int64_t* ldg,
+                                        const int64_t* rows, double scale, cudaStream_t stream);
+
 /* K5: new diagonal factors of a layer from its a and g (any kind):
  *   g_new[i] = s sum_r g[r,i]^2 (o entries); a_new[j] = s sum_r a[r,j]^2, and
  *   a_new[d_in] = s*rows when has_bias (n entries).  Written to caller buffers.
@@ -152,6 +164,18 @@ kfac_status kfac_invert(kfac_handle h, int layer, cudaStream_t stream);
 kfac_status kfac_precondition(kfac_handle h, int layer, const float* grad_w, int64_t ldgw,
                               const float* grad_b, float* out_w, float* out_b,
                               float* param_w, float* param_b, cudaStream_t stream);
+
+/* K4 for several KRON layers in one pass: the same result as calling
+ * kfac_precondition for each i with the i-th entries of the host arrays
+ * (grad_b, out_w, out_b, param_w, param_b may be NULL arrays, or hold NULL
+ * entries, under the same rules as the single call).  Each layer at most once.
+ * The gradients are packed in one launch and each of the two products runs
+ * as one grouped tensor-core launch over the layers. */
+kfac_status kfac_precondition_batched(kfac_handle h, int count, const int* layers,
+                                      const float* const* grad_w, const int64_t* ldgw,
+                                      const float* const* grad_b, float* const* out_w,
+                                      float* const* out_b, float* const* param_w,
+                                      float* const* param_b, cudaStream_t stream);
 
 /* K6: fused diagonal-Fisher step of a DIAG layer, one streaming pass:
  *   gs <- xi gs + (1-xi) g_new ; as <- xi as + (1-xi) a_new     (library state)

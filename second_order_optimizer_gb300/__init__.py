@@ -104,6 +104,17 @@ class Kfac:
         _check(LIB.kfac_update_factors(self._h, layer, _ptr(a), lda, _ptr(g), ldg, rows,
                                        float(scale), _stream(stream)), "kfac_update_factors")
 
+    def update_factors_batched(self, layers, a_list, g_list, scale: float = 0.0, stream=None):
+        """kfac_update_factors_batched over parallel lists of layers and input tensors."""
+        k = len(layers)
+        I64 = ctypes.c_int64 * k
+        P = ctypes.c_void_p * k
+        _check(LIB.kfac_update_factors_batched(
+            self._h, k, (ctypes.c_int * k)(*layers), P(*[_ptr(x) for x in a_list]),
+            I64(*[x.stride(0) for x in a_list]), P(*[_ptr(x) for x in g_list]),
+            I64(*[x.stride(0) for x in g_list]), I64(*[x.shape[0] for x in a_list]),
+            float(scale), _stream(stream)), "kfac_update_factors_batched")
+
     def diag_factors(self, layer: int, a, g, g_new, a_new, rows: Optional[int] = None,
                      scale: float = 0.0, stream=None):
         rows = a.shape[0] if rows is None else rows
@@ -119,6 +130,17 @@ class Kfac:
         _check(LIB.kfac_precondition(self._h, layer, _ptr(grad_w), grad_w.stride(0), _ptr(grad_b),
                                      _ptr(out_w), _ptr(out_b), _ptr(param_w), _ptr(param_b),
                                      _stream(stream)), "kfac_precondition")
+
+    def precondition_batched(self, layers, grad_w, grad_b=None, out_w=None, out_b=None,
+                             param_w=None, param_b=None, stream=None):
+        """kfac_precondition_batched over parallel lists (None, or lists that may hold None)."""
+        k = len(layers)
+        P = ctypes.c_void_p * k
+        arr = lambda xs: None if xs is None else P(*[_ptr(x) for x in xs])
+        _check(LIB.kfac_precondition_batched(
+            self._h, k, (ctypes.c_int * k)(*layers), arr(grad_w),
+            (ctypes.c_int64 * k)(*[x.stride(0) for x in grad_w]), arr(grad_b), arr(out_w),
+            arr(out_b), arr(param_w), arr(param_b), _stream(stream)), "kfac_precondition_batched")
 
     def diag_step(self, layer: int, g_new, a_new, grad_w, grad_b, param_w, param_b,
                   out_w=None, out_b=None, stream=None):

@@ -18,6 +18,7 @@
 #include "syrk_simt.cuh"
 
 #include <algorithm>
+#include <vector>
 
 namespace kfac {
 
@@ -189,6 +190,71 @@ kfac_status launch_update_factors(kfac_ctx* h, int layer, const void* a, int64_t
   if (e != KFAC_OK) return e;
   return launch_syrk_tc(h, layer, g, ldg, rows, L.o, L.o, 0, bf16, alpha, decay,
                         h->at<float>(L.G), st);
+}
+
+// Several layers' factor updates at once: every a and g of a group is packed in
+// one launch, then all their SYRKs run as one grouped tensor-core launch (tiles
+// of all layers fill the GPU together instead of each layer splitting K).  A
+// group is as many layers as the pack scratch holds.
+kfac_status launch_update_factors_batched(kfac_ctx* h, int count, const int* layers,
+                                          const void* const* a, const int64_t* lda,
+                                          const void* const* g, const int64_t* ldg,
+                                          const int64_t* rows, double scale, const float* decay,
+                                          cudaStream_t st) {
+  const bool bf16 = h->layers[layers[0]].in_dtype == KFAC_BF16;
+  const size_t elt = bf16 ? 2 : 8;  // packed bytes per element (bf16, or two TF32 halves)
+  std::vector<PackJob> pj;
+  std::vector<TcProblem> pr;
+  size_t used = 0;
+  auto flush = [&]() -> kfac_status {
+    if (pr.empty()) return KFAC_OK;
+    kfac_status e = launch_pack_grouped(pj.data(), (int)pj.size(), bf16, st);
+    if (e == KFAC_OK) e = launch_gemm_tc_grouped(h, bf16, TC_EPI_SYRK, pr.data(), (int)pr.size(), st);
+    pj.clear();
+    pr.clear();
+    used = 0;
+    return e;
+  };
+  for (int i = 0; i < count; ++i) {
+    const LayerInfo& L = h->layers[layers[i]];
+    const int64_t Kp = tc_pitch(rows[i], bf16);
+    const size_t bA = align_up((size_t)L.n * Kp * elt), bG = align_up((size_t)L.o * Kp * elt);
+    if (bA + bG > h->tcpack_bytes) return KFAC_ERR_WORKSPACE;
+    if (used + bA + bG > h->tcpack_bytes)
+      if (kfac_status e = flush()) return e;
+    const double s = scale > 0 ? scale : 1.0 / (double)rows[i];
+    const float alpha = (float)((1.0 - (double)decay[i]) * s);
+    for (int w = 0; w < 2; ++w) {
+      const int n = w == 0 ? L.n : L.o;
+      char* hi = h->ws + h->off_tcpack + used;
+      char* lo = bf16 ? nullptr : hi + (size_t)n * Kp * 4;
+      used += w == 0 ? bA : bG;
+      PackJob j{};
+      j.x = w == 0 ? a[i] : g[i];
+      j.ld = w == 0 ? lda[i] : ldg[i];
+      j.M = rows[i];
+      j.d = w == 0 ? L.d_in : L.o;
+      j.n = n;
+      j.Kp = Kp;
+      j.hi = hi;
+      j.lo = lo;
+      pj.push_back(j);
+      TcProblem q{};
+      q.A = TcOperand{hi, lo, n, Kp};
+      q.B = q.A;
+      q.same_ab = true;
+      q.upper = true;
+      q.M = q.N = n;
+      q.K = rows[i];
+      q.e.alpha = alpha;
+      q.e.beta = decay[i];
+      q.e.C = h->at<float>(w == 0 ? L.A : L.G);
+      q.e.ldc = n;
+      q.layer = layers[i];
+      pr.push_back(q);
+    }
+  }
+  return flush();
 }
 
 }  // namespace kfac

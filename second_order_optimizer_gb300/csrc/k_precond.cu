@@ -19,6 +19,8 @@
 #include "tc_prims.cuh"
 
 #include <algorithm>
+#include <cstring>
+#include <vector>
 
 namespace kfac {
 
@@ -36,6 +38,33 @@ __global__ void __launch_bounds__(256) gradhat_pack_kernel(const float* __restri
     const float h = tc::to_tf32(v);
     hi[i * np + j] = h;
     lo[i * np + j] = tc::to_tf32(v - h);
+  }
+}
+
+struct GradPackJob {
+  const float* gw;
+  const float* gb;
+  int64_t ld, np;
+  int o, d_in, n;
+  float* hi;
+  float* lo;
+};
+constexpr int kMaxGradPack = 16;
+struct GradPackGroup {
+  GradPackJob job[kMaxGradPack];
+};
+
+__global__ void __launch_bounds__(256) gradhat_pack_grouped_kernel(
+    const __grid_constant__ GradPackGroup g) {
+  const GradPackJob& J = g.job[blockIdx.y];
+  const int64_t total = (int64_t)J.o * J.n;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = e / J.n, j = e % J.n;
+    const float v = j < J.d_in ? J.gw[i * J.ld + j] : J.gb[i];
+    const float h = tc::to_tf32(v);
+    J.hi[i * J.np + j] = h;
+    J.lo[i * J.np + j] = tc::to_tf32(v - h);
   }
 }
 
@@ -82,6 +111,93 @@ kfac_status launch_precondition(kfac_ctx* h, int layer, const float* gw, int64_t
   e2.mb = e2.mw + (size_t)L.o * L.d_in;
   return launch_gemm_tc(h, layer, false, TC_EPI_PRECOND, Ginv, XT, false, false, L.o, L.n, L.o,
                         e2, st);
+}
+
+// Several layers at once: one pack launch for all gradients, then each of the two
+// products as one grouped tensor-core launch over all layers of the group.  A
+// group is as many layers as the scratch holds (at most 16).
+kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layers,
+                                        const float* const* gw, const int64_t* ldgw,
+                                        const float* const* gb, float* const* ow,
+                                        float* const* ob, float* const* pw, float* const* pb,
+                                        cudaStream_t st) {
+  std::vector<TcProblem> p1, p2;
+  GradPackGroup gp;
+  std::memset(&gp, 0, sizeof(gp));
+  int ng = 0;
+  int64_t max_elems = 0;
+  size_t used = 0;  // floats
+  auto flush = [&]() -> kfac_status {
+    if (ng == 0) return KFAC_OK;
+    const unsigned blocks = (unsigned)std::min<int64_t>(cdiv(max_elems, 256), 4 * kNumSMs);
+    gradhat_pack_grouped_kernel<<<dim3(blocks, ng), 256, 0, st>>>(gp);
+    count_launch();
+    kfac_status e = check_launch();
+    if (e == KFAC_OK) e = launch_gemm_tc_grouped(h, false, TC_EPI_SPLIT, p1.data(), ng, st);
+    if (e == KFAC_OK) e = launch_gemm_tc_grouped(h, false, TC_EPI_PRECOND, p2.data(), ng, st);
+    p1.clear();
+    p2.clear();
+    ng = 0;
+    max_elems = 0;
+    used = 0;
+    return e;
+  };
+  for (int i = 0; i < count; ++i) {
+    const LayerInfo& L = h->layers[layers[i]];
+    const int64_t np = tc_pitch(L.n, false), op = tc_pitch(L.o, false);
+    const size_t gfl = align_up((size_t)L.o * np * 4) / 4, xfl = align_up((size_t)L.n * op * 4) / 4;
+    const size_t need = 2 * gfl + 2 * xfl;
+    if (need > h->k4tmp_floats) return KFAC_ERR_WORKSPACE;
+    if (used + need > h->k4tmp_floats || ng == kMaxGradPack)
+      if (kfac_status e = flush()) return e;
+    float* g_hi = h->at<float>(h->off_k4tmp) + used;
+    float* g_lo = g_hi + gfl;
+    float* x_hi = g_lo + gfl;
+    float* x_lo = x_hi + xfl;
+    used += need;
+    GradPackJob& j = gp.job[ng];
+    j.gw = gw[i];
+    j.gb = gb[i];
+    j.ld = ldgw[i];
+    j.np = np;
+    j.o = L.o;
+    j.d_in = L.d_in;
+    j.n = L.n;
+    j.hi = g_hi;
+    j.lo = g_lo;
+    max_elems = std::max<int64_t>(max_elems, (int64_t)L.o * L.n);
+    TcProblem q1{};
+    q1.A = TcOperand{h->at<float>(L.Ainv_hi), h->at<float>(L.Ainv_lo), L.n, np};
+    q1.B = TcOperand{g_hi, g_lo, L.o, np};
+    q1.M = L.n;
+    q1.N = L.o;
+    q1.K = L.n;
+    q1.e.out_hi = x_hi;
+    q1.e.out_lo = x_lo;
+    q1.e.ldo = op;
+    q1.layer = layers[i];
+    p1.push_back(q1);
+    TcProblem q2{};
+    q2.A = TcOperand{h->at<float>(L.Ginv_hi), h->at<float>(L.Ginv_lo), L.o, op};
+    q2.B = TcOperand{x_hi, x_lo, L.n, op};
+    q2.M = L.o;
+    q2.N = L.n;
+    q2.K = L.o;
+    q2.e.d_in = L.d_in;
+    q2.e.eta = (float)h->hp.lr;
+    q2.e.mu = (float)h->hp.momentum;
+    q2.e.lambda = (float)h->hp.weight_decay;
+    q2.e.ow = ow ? ow[i] : nullptr;
+    q2.e.ob = ob ? ob[i] : nullptr;
+    q2.e.pw = pw ? pw[i] : nullptr;
+    q2.e.pb = pb ? pb[i] : nullptr;
+    q2.e.mw = h->at<float>(L.m);
+    q2.e.mb = q2.e.mw + (size_t)L.o * L.d_in;
+    q2.layer = layers[i];
+    p2.push_back(q2);
+    ++ng;
+  }
+  return flush();
 }
 
 }  // namespace kfac

@@ -54,6 +54,7 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
   P->off_status = take(sizeof(DevStatus));
   P->layers.clear();
   size_t part = 0, tickets = 0, k4 = 0, k5 = 0, k5t = 0, tcpack = 0;
+  size_t pack_sum = 0, k4_sum = 0;   // what a batch over every KRON layer would use
   int ninv = 0, maxn = 0;
   for (int i = 0; i < nl; ++i) {
     const kfac_layer_desc& d = descs[i];
@@ -91,8 +92,10 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
       // the inverse assembly packs X = L^{-1} (n x n, fp32) through the same buffer
       if (L.n >= kTcInverseMinN) tcpack = std::max(tcpack, tc_pack_bytes(L.n, L.n, false));
       if (L.o >= kTcInverseMinN) tcpack = std::max(tcpack, tc_pack_bytes(L.o, L.o, false));
+      pack_sum += align_up(tc_pack_bytes(L.n, max_rows, bf)) + align_up(tc_pack_bytes(L.o, max_rows, bf));
       tickets = std::max({tickets, t1, t2, (size_t)kNumSMs});
       k4 = std::max(k4, 2 * o * np + 2 * n * op);
+      k4_sum += align_up((2 * o * np + 2 * n * op) * sizeof(float)) / sizeof(float);
       ninv += 2;
       maxn = std::max({maxn, L.n, L.o});
     } else {
@@ -104,6 +107,9 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
     k5t = std::max(k5t, (size_t)cdiv(L.d_in + L.o, 256));
     P->layers.push_back(L);
   }
+  // batched calls pack a group of layers at once, within a fixed budget
+  tcpack = std::max(tcpack, std::min(pack_sum, kBatchScratchBudget));
+  k4 = std::max(k4, std::min(k4_sum, kBatchScratchBudget / sizeof(float)));
   P->part_floats = part;
   P->off_part = take(part * sizeof(float));
   P->n_tickets = tickets;
@@ -295,6 +301,34 @@ kfac_status kfac_update_factors(kfac_handle h, int layer, const void* a, int64_t
   return e;
 }
 
+kfac_status kfac_update_factors_batched(kfac_handle h, int count, const int* layers,
+                                        const void* const* a, const int64_t* lda,
+                                        const void* const* g, const int64_t* ldg,
+                                        const int64_t* rows, double scale, cudaStream_t stream) {
+  if (!h || count < 1 || !layers || !a || !lda || !g || !ldg || !rows || !std::isfinite(scale))
+    return KFAC_ERR_INVALID_ARG;
+  std::vector<char> seen(h->layers.size(), 0);
+  for (int i = 0; i < count; ++i) {
+    if (kfac_status e = check_layer(h, layers[i], KFAC_KRON)) return e;
+    if (seen[layers[i]]++) return KFAC_ERR_INVALID_ARG;   // a layer at most once per batch
+    const LayerInfo& L = h->layers[layers[i]];
+    if (L.in_dtype != h->layers[layers[0]].in_dtype) return KFAC_ERR_INVALID_ARG;
+    if (kfac_status e = check_inputs(h, L, a[i], lda[i], g[i], ldg[i], rows[i])) return e;
+  }
+  if (kfac_status e = ensure_device(h)) return e;
+  std::vector<float> decay(count);
+  for (int i = 0; i < count; ++i) {
+    const LayerInfo& L = h->layers[layers[i]];
+    const bool first = L.t_factor == 0 && h->hp.ema_init == KFAC_EMA_INIT_FIRST;
+    decay[i] = first ? 0.f : (float)h->hp.ema_decay;
+  }
+  kfac_status e = launch_update_factors_batched(h, count, layers, a, lda, g, ldg, rows, scale,
+                                                decay.data(), stream);
+  if (e == KFAC_OK)
+    for (int i = 0; i < count; ++i) ++h->layers[layers[i]].t_factor;
+  return e;
+}
+
 kfac_status kfac_diag_factors(kfac_handle h, int layer, const void* a, int64_t lda,
                               const void* g, int64_t ldg, int64_t rows, double scale,
                               float* g_new, float* a_new, cudaStream_t stream) {
@@ -334,6 +368,40 @@ kfac_status kfac_precondition(kfac_handle h, int layer, const float* grad_w, int
   return launch_precondition(h, layer, grad_w, ldgw, L.has_bias ? grad_b : nullptr, out_w,
                              L.has_bias ? out_b : nullptr, param_w,
                              L.has_bias ? param_b : nullptr, stream);
+}
+
+kfac_status kfac_precondition_batched(kfac_handle h, int count, const int* layers,
+                                      const float* const* grad_w, const int64_t* ldgw,
+                                      const float* const* grad_b, float* const* out_w,
+                                      float* const* out_b, float* const* param_w,
+                                      float* const* param_b, cudaStream_t stream) {
+  if (!h || count < 1 || !layers || !grad_w || !ldgw || (!out_w && !param_w))
+    return KFAC_ERR_INVALID_ARG;
+  std::vector<char> seen(h->layers.size(), 0);
+  std::vector<const float*> gb(count, nullptr);
+  std::vector<float*> ob(count, nullptr), pb(count, nullptr);
+  for (int i = 0; i < count; ++i) {
+    if (kfac_status e = check_layer(h, layers[i], KFAC_KRON)) return e;
+    if (seen[layers[i]]++) return KFAC_ERR_INVALID_ARG;
+    const LayerInfo& L = h->layers[layers[i]];
+    const float* bw = grad_b ? grad_b[i] : nullptr;
+    float* o_w = out_w ? out_w[i] : nullptr;
+    float* o_b = out_b ? out_b[i] : nullptr;
+    float* p_w = param_w ? param_w[i] : nullptr;
+    float* p_b = param_b ? param_b[i] : nullptr;
+    if (!grad_w[i] || !aligned(grad_w[i], 4) || ldgw[i] < L.d_in) return KFAC_ERR_INVALID_ARG;
+    if (L.has_bias && !bw) return KFAC_ERR_INVALID_ARG;
+    if (!o_w && !p_w) return KFAC_ERR_INVALID_ARG;
+    if (L.has_bias && o_w && !o_b) return KFAC_ERR_INVALID_ARG;
+    if (L.has_bias && p_w && !p_b) return KFAC_ERR_INVALID_ARG;
+    if (!L.inverted) return KFAC_ERR_STATE;
+    gb[i] = L.has_bias ? bw : nullptr;
+    ob[i] = L.has_bias ? o_b : nullptr;
+    pb[i] = L.has_bias ? p_b : nullptr;
+  }
+  if (kfac_status e = ensure_device(h)) return e;
+  return launch_precondition_batched(h, count, layers, grad_w, ldgw, gb.data(), out_w, ob.data(),
+                                     param_w, pb.data(), stream);
 }
 
 kfac_status kfac_diag_step(kfac_handle h, int layer, const float* g_new, const float* a_new,

@@ -110,12 +110,22 @@ kfac_status launch_diag_factors(kfac_ctx* h, int layer, const void* a, int64_t l
 kfac_status launch_diag_step(kfac_ctx* h, int layer, float decay, const float* g_new,
                              const float* a_new, const float* gw, const float* gb, float* pw,
                              float* pb, float* ow, float* ob, cudaStream_t s);
+kfac_status launch_update_factors_batched(kfac_ctx* h, int count, const int* layers,
+                                          const void* const* a, const int64_t* lda,
+                                          const void* const* g, const int64_t* ldg,
+                                          const int64_t* rows, double scale, const float* decay,
+                                          cudaStream_t s);
 // K2 / K3
 kfac_status launch_invert(kfac_ctx* h, int layer, cudaStream_t s);
 // K4
 kfac_status launch_precondition(kfac_ctx* h, int layer, const float* gw, int64_t ldgw,
                                 const float* gb, float* ow, float* ob, float* pw, float* pb,
                                 cudaStream_t s);
+kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layers,
+                                        const float* const* gw, const int64_t* ldgw,
+                                        const float* const* gb, float* const* ow,
+                                        float* const* ob, float* const* pw, float* const* pb,
+                                        cudaStream_t s);
 
 // Tensor-core GEMM engine (tcgen05 + TMA): C[M x N] = A[M x K] . B[N x K]^T
 enum { TC_EPI_SYRK = 0, TC_EPI_SPLIT = 1, TC_EPI_PRECOND = 2 };
@@ -138,10 +148,33 @@ struct TcEpilogue {
 kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcOperand& A,
                            const TcOperand& B, bool same_ab, bool upper, int64_t M, int64_t N,
                            int64_t K, const TcEpilogue& e, cudaStream_t st);
+// One product of a grouped launch.
+struct TcProblem {
+  TcOperand A, B;
+  bool same_ab, upper;
+  int64_t M, N, K;
+  TcEpilogue e;
+  int layer;
+};
+kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProblem* probs,
+                                   int count, cudaStream_t st);
 kfac_status launch_syrk_tc(kfac_ctx* h, int layer, const void* x, int64_t ld, int64_t rows, int d,
                            int n, int has_bias, bool bf16, float alpha, float beta, float* F,
                            cudaStream_t st);
 int64_t tc_pitch(int64_t cols, bool bf16);
+// x-hat -> X = x-hat^T (K-major; TF32 halves for fp32, bf16 copy), several at once
+struct PackJob {
+  const void* x;
+  int64_t ld, M;
+  int d, n;
+  int64_t Kp;
+  void* hi;
+  void* lo;
+};
+constexpr int kMaxPackJobs = 32;
+kfac_status launch_pack_grouped(const PackJob* jobs, int count, bool bf16, cudaStream_t st);
+// scratch of the batched entry points (a group of layers is packed together)
+constexpr size_t kBatchScratchBudget = size_t(256) << 20;
 size_t tc_pack_bytes(int n, int64_t max_rows, bool bf16);
 size_t tc_part_floats();
 

@@ -37,6 +37,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstring>
+#include <memory>
 #include <mutex>
 
 namespace kfac {
@@ -101,12 +103,13 @@ __device__ __forceinline__ void upper_tile(int t, int tiles_m, int R, int* ti, i
   *tj = j;
 }
 
+// One output tile (and one k-split of it).  `ticket_tile` indexes the split-K
+// partial buffer and tickets (unique across the launch).
 template <bool kBF16, int BN, int EPI>
-__global__ void __launch_bounds__(TcCfg<kBF16, BN>::THREADS, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
-               const __grid_constant__ CUtensorMap map_a_lo,
-               const __grid_constant__ CUtensorMap map_b_hi,
-               const __grid_constant__ CUtensorMap map_b_lo, GemmTcParams p) {
+__device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUtensorMap* map_a_lo,
+                                          const CUtensorMap* map_b_hi, const CUtensorMap* map_b_lo,
+                                          const GemmTcParams& p, const int tile, const int split,
+                                          const int ticket_tile) {
   using C = TcCfg<kBF16, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -120,7 +123,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
   static_assert(EPI == TC_EPI_SYRK || !kBF16, "bf16 operands are used by the factor update only");
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
   int ti, tj;
   if (p.upper) {
     upper_tile(tile, p.tiles_m, C::R, &ti, &tj);
@@ -142,11 +144,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
-    tc::tma_prefetch_desc(&map_a_hi);
-    tc::tma_prefetch_desc(&map_b_hi);
+    tc::tma_prefetch_desc(map_a_hi);
+    tc::tma_prefetch_desc(map_b_hi);
     if (!kBF16) {
-      tc::tma_prefetch_desc(&map_a_lo);
-      tc::tma_prefetch_desc(&map_b_lo);
+      tc::tma_prefetch_desc(map_a_lo);
+      tc::tma_prefetch_desc(map_b_lo);
     }
   }
   if (warp == 1) {
@@ -185,11 +187,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
         }
         const int k0 = (int)(kbeg + (int64_t)kb * C::BK);
         tc::mbar_expect_tx(&full[stage], bytes);
-        if (!a_in_b) tc::tma_load_2d(a_ptr(stage, 0), &map_a_hi, &full[stage], k0, ti * C::BM);
-        tc::tma_load_2d(b_ptr(stage, 0), &map_b_hi, &full[stage], k0, tj * C::BN);
+        if (!a_in_b) tc::tma_load_2d(a_ptr(stage, 0), map_a_hi, &full[stage], k0, ti * C::BM);
+        tc::tma_load_2d(b_ptr(stage, 0), map_b_hi, &full[stage], k0, tj * C::BN);
         if (!kBF16) {
-          if (!a_in_b) tc::tma_load_2d(a_ptr(stage, 1), &map_a_lo, &full[stage], k0, ti * C::BM);
-          tc::tma_load_2d(b_ptr(stage, 1), &map_b_lo, &full[stage], k0, tj * C::BN);
+          if (!a_in_b) tc::tma_load_2d(a_ptr(stage, 1), map_a_lo, &full[stage], k0, ti * C::BM);
+          tc::tma_load_2d(b_ptr(stage, 1), map_b_lo, &full[stage], k0, tj * C::BN);
         }
         if (++stage == C::STAGES) {
           stage = 0;
@@ -338,12 +340,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
     if (*abort_flag) return;
   } else if (p.splits > 1) {
     if (*abort_flag) return;
-    float* part = p.part + (size_t)tile * p.splits * NT;
+    float* part = p.part + (size_t)ticket_tile * p.splits * NT;
     for (int e = threadIdx.x; e < NT; e += nth)
       part[(size_t)split * NT + e] = T[(e / C::BN) * C::TPAD + e % C::BN];
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) *s_last = (atomicAdd(&p.tickets[tile], 1) == p.splits - 1);
+    if (threadIdx.x == 0) *s_last = (atomicAdd(&p.tickets[ticket_tile], 1) == p.splits - 1);
     __syncthreads();
     if (!*s_last) return;
     __threadfence();
@@ -370,7 +372,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
         if (e < NT) T[(e / C::BN) * C::TPAD + e % C::BN] = acc[u];
       }
     }
-    if (threadIdx.x == 0) p.tickets[tile] = 0;
+    if (threadIdx.x == 0) p.tickets[ticket_tile] = 0;
     __syncthreads();
   } else if (*abort_flag) {
     return;
@@ -466,15 +468,45 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
   }
 }
 
+template <bool kBF16, int BN, int EPI>
+__global__ void __launch_bounds__(TcCfg<kBF16, BN>::THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
+               const __grid_constant__ CUtensorMap map_a_lo,
+               const __grid_constant__ CUtensorMap map_b_hi,
+               const __grid_constant__ CUtensorMap map_b_lo, const __grid_constant__ GemmTcParams p) {
+  const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
+  gemm_body<kBF16, BN, EPI>(&map_a_hi, &map_a_lo, &map_b_hi, &map_b_lo, p, tile, split, tile);
+}
+
+// Several independent products in one launch (128 x 128 tiles): blocks are laid
+// out problem by problem, `splits` consecutive blocks per tile (one cluster when
+// the split-K is reduced through DSMEM).
+constexpr int kMaxGroup = 16;
+struct GroupedTc {
+  CUtensorMap maps[4 * kMaxGroup];  // per problem: A hi, A lo, B hi, B lo
+  GemmTcParams prob[kMaxGroup];
+  int tile_start[kMaxGroup + 1];
+  int count;
+  int splits;
+};
+
+template <bool kBF16, int EPI>
+__global__ void __launch_bounds__(TcCfg<kBF16, 128>::THREADS, 1)
+gemm_tc_grouped_kernel(const __grid_constant__ GroupedTc g) {
+  const int gt = blockIdx.x / g.splits, split = blockIdx.x % g.splits;
+  int q = 0;
+  while (q + 1 < g.count && gt >= g.tile_start[q + 1]) ++q;
+  gemm_body<kBF16, 128, EPI>(&g.maps[4 * q], &g.maps[4 * q + 1], &g.maps[4 * q + 2],
+                             &g.maps[4 * q + 3], g.prob[q], gt - g.tile_start[q], split, gt);
+}
+
 // ------------------------------------------------------------------- pack
 // X[c][r] = x-hat[r][c] for c < n, r < M; fp32 -> (hi, lo) TF32 halves; bf16 -> copy.
 template <typename T, bool kSplit>
-__global__ void __launch_bounds__(256) pack_kernel(const T* __restrict__ x, int64_t ld, int64_t M,
-                                                    int d, int n, int64_t Kp, void* out_hi,
-                                                    void* out_lo) {
+__device__ __forceinline__ void pack_tile(const T* __restrict__ x, int64_t ld, int64_t M, int d,
+                                          int n, int64_t Kp, void* out_hi, void* out_lo,
+                                          int64_t r0, int c0) {
   __shared__ float tile[32][33];
-  const int64_t r0 = (int64_t)blockIdx.x * 32;
-  const int c0 = blockIdx.y * 32;
   const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;  // 32 x 8
   for (int i = ty; i < 32; i += 8) {
     const int64_t r = r0 + i;
@@ -498,6 +530,28 @@ __global__ void __launch_bounds__(256) pack_kernel(const T* __restrict__ x, int6
       static_cast<__nv_bfloat16*>(out_hi)[(int64_t)c * Kp + r] = __float2bfloat16_rn(v);
     }
   }
+}
+
+template <typename T, bool kSplit>
+__global__ void __launch_bounds__(256) pack_kernel(const T* __restrict__ x, int64_t ld, int64_t M,
+                                                    int d, int n, int64_t Kp, void* out_hi,
+                                                    void* out_lo) {
+  pack_tile<T, kSplit>(x, ld, M, d, n, Kp, out_hi, out_lo, (int64_t)blockIdx.x * 32,
+                       blockIdx.y * 32);
+}
+
+struct PackGroup {
+  PackJob job[kMaxPackJobs];
+  int count;
+};
+
+template <typename T, bool kSplit>
+__global__ void __launch_bounds__(256) pack_grouped_kernel(const __grid_constant__ PackGroup g) {
+  const PackJob& J = g.job[blockIdx.z];
+  const int64_t r0 = (int64_t)blockIdx.x * 32;
+  const int c0 = blockIdx.y * 32;
+  if (r0 >= J.Kp || c0 >= J.n) return;
+  pack_tile<T, kSplit>(static_cast<const T*>(J.x), J.ld, J.M, J.d, J.n, J.Kp, J.hi, J.lo, r0, c0);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -584,6 +638,29 @@ kfac_status launch_kernel(unsigned grid, const CUtensorMap& ah, const CUtensorMa
 
 int64_t tc_pitch(int64_t cols, bool bf16) { return cdiv(cols, bf16 ? 8 : 4) * (bf16 ? 8 : 4); }
 
+kfac_status launch_pack_grouped(const PackJob* jobs, int count, bool bf16, cudaStream_t st) {
+  PackGroup g;
+  std::memset(&g, 0, sizeof(g));
+  for (int c0 = 0; c0 < count; c0 += kMaxPackJobs) {
+    const int cnt = std::min(kMaxPackJobs, count - c0);
+    int64_t kp = 0, nmax = 0;
+    for (int q = 0; q < cnt; ++q) {
+      g.job[q] = jobs[c0 + q];
+      kp = std::max(kp, jobs[c0 + q].Kp);
+      nmax = std::max<int64_t>(nmax, jobs[c0 + q].n);
+    }
+    g.count = cnt;
+    dim3 grid((unsigned)cdiv(kp, 32), (unsigned)cdiv(nmax, 32), (unsigned)cnt);
+    if (bf16)
+      pack_grouped_kernel<__nv_bfloat16, false><<<grid, 256, 0, st>>>(g);
+    else
+      pack_grouped_kernel<float, true><<<grid, 256, 0, st>>>(g);
+    count_launch();
+    if (kfac_status e = check_launch()) return e;
+  }
+  return KFAC_OK;
+}
+
 size_t tc_pack_bytes(int n, int64_t max_rows, bool bf16) {
   const int64_t Kp = tc_pitch(max_rows, bf16);
   return (size_t)n * Kp * (bf16 ? 2 : 8);
@@ -626,7 +703,7 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
     const int tm = (int)cdiv(M, BM), tn = (int)cdiv(N, bn);
     return upper ? upper_tile_count(tm, tn, bn / BM) : (int64_t)tm * tn;
   };
-  const int BN = (K >= 8192 || count(256) >= kNumSMs) ? 256 : 128;
+  const int BN = ((bf16 && K >= 8192) || count(256) >= kNumSMs) ? 256 : 128;
   CUtensorMap ah, al, bh, bl;
   if (!make_map(&ah, A.hi, bf16, A.rows, K, A.pitch, BM)) return KFAC_ERR_CUDA;
   if (!make_map(&bh, B.hi, bf16, B.rows, K, B.pitch, BN)) return KFAC_ERR_CUDA;
@@ -660,6 +737,109 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
   const unsigned grid = (unsigned)(tiles * p.splits);
   return BN == 256 ? dispatch<256>(bf16, epi, grid, ah, al, bh, bl, p, st)
                    : dispatch<128>(bf16, epi, grid, ah, al, bh, bl, p, st);
+}
+
+template <bool kBF16, int EPI>
+kfac_status launch_grouped_kernel(unsigned grid, const GroupedTc& g, cudaStream_t st) {
+  static bool attr_ok = cudaFuncSetAttribute(gemm_tc_grouped_kernel<kBF16, EPI>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)TcCfg<kBF16, 128>::SMEM) == cudaSuccess;
+  if (!attr_ok) return KFAC_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(TcCfg<kBF16, 128>::THREADS);
+  cfg.dynamicSmemBytes = TcCfg<kBF16, 128>::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = g.prob[0].cluster_reduce ? (unsigned)g.splits : 1u;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, gemm_tc_grouped_kernel<kBF16, EPI>, g) != cudaSuccess)
+    return KFAC_ERR_CUDA;
+  count_launch();
+  return check_launch();
+}
+
+// Independent products of one epilogue kind in as few launches as possible
+// (kMaxGroup per launch, 128 x 128 tiles).  All tiles of a launch share one
+// split-K count, chosen so that tiles x splits fill the GPU.
+kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProblem* probs,
+                                   int count, cudaStream_t st) {
+  if (count == 1) {
+    const TcProblem& q = probs[0];
+    return launch_gemm_tc(h, q.layer, bf16, epi, q.A, q.B, q.same_ab, q.upper, q.M, q.N, q.K,
+                          q.e, st);
+  }
+  constexpr int BM = 128, BN = 128;
+  std::unique_ptr<GroupedTc> g(new GroupedTc());
+  for (int c0 = 0; c0 < count; c0 += kMaxGroup) {
+    const int cnt = std::min(kMaxGroup, count - c0);
+    std::memset(g.get(), 0, sizeof(GroupedTc));
+    int64_t total = 0, kmax = 0;
+    for (int q = 0; q < cnt; ++q) {
+      const TcProblem& pr = probs[c0 + q];
+      const int tm = (int)cdiv(pr.M, BM), tn = (int)cdiv(pr.N, BN);
+      g->tile_start[q] = (int)total;
+      total += pr.upper ? upper_tile_count(tm, tn, 1) : (int64_t)tm * tn;
+      kmax = std::max(kmax, pr.K);
+    }
+    g->tile_start[cnt] = (int)total;
+    int64_t s = std::max<int64_t>(1, kNumSMs / total);
+    s = std::min<int64_t>(s, std::max<int64_t>(1, kmax / 256));
+    const int unit = bf16 ? kKsubBf16 : kKsubTf32;
+    const bool cluster = s >= 2 && s <= 8;
+    if (s > 1 && !cluster &&
+        ((size_t)(total * s) * BM * BN > h->part_floats || (size_t)total > h->n_tickets))
+      return KFAC_ERR_WORKSPACE;
+    g->count = cnt;
+    g->splits = (int)s;
+    for (int q = 0; q < cnt; ++q) {
+      const TcProblem& pr = probs[c0 + q];
+      CUtensorMap* m = &g->maps[4 * q];
+      if (!make_map(&m[0], pr.A.hi, bf16, pr.A.rows, pr.K, pr.A.pitch, BM)) return KFAC_ERR_CUDA;
+      if (!make_map(&m[2], pr.B.hi, bf16, pr.B.rows, pr.K, pr.B.pitch, BN)) return KFAC_ERR_CUDA;
+      if (bf16) {
+        m[1] = m[0];
+        m[3] = m[2];
+      } else {
+        if (!make_map(&m[1], pr.A.lo, false, pr.A.rows, pr.K, pr.A.pitch, BM)) return KFAC_ERR_CUDA;
+        if (!make_map(&m[3], pr.B.lo, false, pr.B.rows, pr.K, pr.B.pitch, BN)) return KFAC_ERR_CUDA;
+      }
+      GemmTcParams& pp = g->prob[q];
+      pp.M = pr.M;
+      pp.N = pr.N;
+      pp.K = pr.K;
+      pp.tiles_m = (int)cdiv(pr.M, BM);
+      pp.tiles_n = (int)cdiv(pr.N, BN);
+      pp.upper = pr.upper ? 1 : 0;
+      pp.same_ab = pr.same_ab ? 1 : 0;
+      pp.splits = (int)s;
+      pp.cluster_reduce = cluster ? 1 : 0;
+      pp.k_per_split = cdiv(cdiv(pr.K, s), unit) * unit;
+      pp.ksub = unit;
+      pp.part = h->at<float>(h->off_part);
+      pp.tickets = h->at<int>(h->off_tickets);
+      pp.status = h->status();
+      pp.layer = pr.layer;
+      pp.e = pr.e;
+    }
+    const unsigned grid = (unsigned)(total * s);
+    kfac_status e;
+    if (epi == TC_EPI_SYRK)
+      e = bf16 ? launch_grouped_kernel<true, TC_EPI_SYRK>(grid, *g, st)
+               : launch_grouped_kernel<false, TC_EPI_SYRK>(grid, *g, st);
+    else if (bf16)
+      e = KFAC_ERR_UNSUPPORTED;
+    else if (epi == TC_EPI_SPLIT)
+      e = launch_grouped_kernel<false, TC_EPI_SPLIT>(grid, *g, st);
+    else
+      e = launch_grouped_kernel<false, TC_EPI_PRECOND>(grid, *g, st);
+    if (e != KFAC_OK) return e;
+  }
+  return KFAC_OK;
 }
 
 // F <- beta F + alpha x-hat^T x-hat on the tensor cores (K1).

@@ -336,3 +336,83 @@ def test_mlp4_full_size_two_refreshes():
     worst = _run_config_small("c2", 11, check_every=5)
     assert worst["A"] <= 1e-5 and worst["G"] <= 1e-5, worst
     assert worst["P"] <= 1e-4 and worst["W"] <= 1e-4, worst
+
+
+# ------------------------------------------------------------------ batched entry points
+
+def _mixed_layers(dtype):
+    kd = K.KFAC_BF16 if dtype == "bf16" else K.KFAC_F32
+    shapes = [(1024, 1024, 1), (300, 150, 1), (64, 10, 1), (33, 70, 0), (513, 1000, 1)]
+    shapes += [(40 + 3 * i, 20 + 5 * i, i % 2) for i in range(15)]   # > 16 problems: 2+ groups
+    return [(K.KFAC_KRON, o, d, b, kd) for d, o, b in shapes]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_update_factors_batched_matches_single_calls(dtype):
+    descs = _mixed_layers(dtype)
+    M = 700
+    hb = K.Kfac(descs, max_rows=M, **HP)
+    hs = K.Kfac(descs, max_rows=M, **HP)
+    ins = [_inputs(M, d, o, dtype=dtype) for (_, o, d, b, _) in descs]
+    for step in range(2):
+        a_l = [_dev_in(a, dtype) for a, _ in ins]
+        g_l = [_dev_in(g, dtype) for _, g in ins]
+        hb.update_factors_batched(list(range(len(descs))), a_l, g_l)
+        for li in range(len(descs)):
+            hs.update_factors(li, a_l[li], g_l[li])
+    for li, (_, o, d, b, _) in enumerate(descs):
+        a, g = ins[li]
+        Aref = O.factor(a, b) * (1 - 0.95 ** 2)
+        for which, ref in ((K.KFAC_STATE_A, Aref), (K.KFAC_STATE_G, O.factor(g, 0) * (1 - 0.95 ** 2))):
+            xb, xs = to_np(hb.state(li, which)), to_np(hs.state(li, which))
+            assert rel_fro(xb, xs) <= 1e-6, (li, which)
+            assert rel_fro(xb, ref) <= 1e-5, (li, which)
+            assert np.array_equal(xb, xb.T)
+    assert hb.get_status()[0] == 0
+
+
+def test_precondition_batched_matches_single_calls():
+    descs = _mixed_layers("f32")
+    M = 500
+    hb = K.Kfac(descs, max_rows=M, **HP)
+    hs = K.Kfac(descs, max_rows=M, **HP)
+    n_l = len(descs)
+    ins = [_inputs(M, d, o, g_std=0.05) for (_, o, d, b, _) in descs]
+    for h in (hb, hs):
+        for li in range(n_l):
+            h.update_factors(li, to_dev(ins[li][0]), to_dev(ins[li][1]))
+        h.invert(-1)
+    gws = [to_dev((RNG.standard_normal((o, d)) * 1e-3).astype(np.float32)) for (_, o, d, b, _) in descs]
+    gbs = [to_dev((RNG.standard_normal(o) * 1e-3).astype(np.float32)) if b else None
+           for (_, o, d, b, _) in descs]
+    w0 = [(RNG.standard_normal((o, d)) * 0.1).astype(np.float32) for (_, o, d, b, _) in descs]
+    b0 = [(RNG.standard_normal(o) * 0.1).astype(np.float32) if b else None for (_, o, d, b, _) in descs]
+    pw_b = [to_dev(w) for w in w0]
+    pb_b = [to_dev(x) if x is not None else None for x in b0]
+    pw_s = [to_dev(w) for w in w0]
+    pb_s = [to_dev(x) if x is not None else None for x in b0]
+    ow_b = [torch.empty(o, d, device="cuda") for (_, o, d, b, _) in descs]
+    ob_b = [torch.empty(o, device="cuda") if b else None for (_, o, d, b, _) in descs]
+    hb.precondition_batched(list(range(n_l)), gws, gbs, ow_b, ob_b, pw_b, pb_b)
+    for li, (_, o, d, b, _) in enumerate(descs):
+        ow = torch.empty(o, d, device="cuda")
+        ob = torch.empty(o, device="cuda") if b else None
+        hs.precondition(li, gws[li], gbs[li], ow, ob, pw_s[li], pb_s[li])
+        gh = lambda w, x: O.grad_hat(to_np(w), to_np(x) if b else None)
+        assert rel_fro(gh(ow_b[li], ob_b[li]), gh(ow, ob)) <= 1e-6, li
+        assert rel_fro(gh(pw_b[li], pb_b[li]), gh(pw_s[li], pb_s[li])) <= 1e-6, li
+        # and against the oracle's formula with the inverses in use
+        Pref = O.precondition(to_np(hb.state(li, K.KFAC_STATE_GINV)),
+                              gh(gws[li], gbs[li]), to_np(hb.state(li, K.KFAC_STATE_AINV)))
+        assert rel_fro(gh(ow_b[li], ob_b[li]), Pref) <= 1e-4, li
+    assert hb.get_status()[0] == 0
+
+
+def test_batched_calls_reject_duplicates_and_mixed_dtypes():
+    h = K.Kfac([(K.KFAC_KRON, 8, 8, 1, K.KFAC_F32), (K.KFAC_KRON, 8, 8, 1, K.KFAC_BF16)],
+               max_rows=16, **HP)
+    a = torch.zeros(16, 8, device="cuda")
+    with pytest.raises(K.KfacError):
+        h.update_factors_batched([0, 0], [a, a], [a, a])
+    with pytest.raises(K.KfacError):
+        h.update_factors_batched([0, 1], [a, a.bfloat16()], [a, a.bfloat16()])
