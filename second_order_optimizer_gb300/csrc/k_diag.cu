@@ -23,7 +23,7 @@ namespace kfac {
 
 namespace {
 
-constexpr int kDiagThreads = 256;
+constexpr int kDiagThreads = 1024;
 constexpr int kK5Threads = 256;
 constexpr int64_t kK5MinRows = 32;
 
@@ -255,7 +255,7 @@ kfac_status launch_diag_step(kfac_ctx* h, int layer, float decay, const float* g
                    al16(a_new) && (ow == nullptr || al16(ow));
   const int64_t nw = (int64_t)L.o * L.d_in;
   const int64_t units = (vec ? nw / 4 : nw) + (L.has_bias ? L.o : 0);
-  int64_t blocks = std::min<int64_t>(cdiv(units, kDiagThreads), (int64_t)kNumSMs * 4);
+  int64_t blocks = std::min<int64_t>(cdiv(units, kDiagThreads), (int64_t)kNumSMs);
   blocks = std::max<int64_t>(blocks, 1);
   if (vec)
     diag_step_kernel<true><<<(unsigned)blocks, kDiagThreads, 0, st>>>(p);

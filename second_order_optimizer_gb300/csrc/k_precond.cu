@@ -11,10 +11,12 @@
 //
 // Both products run on the tensor cores in 3xTF32 (fp32 accuracy):
 //   pack     dW-hat = [dW | db] -> TF32 halves [o x n_p]
-//   X^T  =   Ainv . dW-hat^T      M = n, N = o, K = n   epilogue stores X^T as TF32 halves
-//   P    =   Ginv . X             M = o, N = n, K = o   epilogue: P out and/or W, m update
-// Writing X^T (not X) keeps every operand K-major.  Ainv/Ginv halves are
-// produced once per refresh by the inverse pass.
+//   X    =   dW-hat . Ainv        M = o, N = n, K = n   epilogue stores X^T as TF32 halves
+//   P^T  =   X^T . Ginv           M = n, N = o, K = o   epilogue: P out and/or W, m update
+// (Ainv and Ginv are symmetric.)  Storing X^T keeps every operand K-major, and
+// with the products oriented this way each epilogue thread, which holds one
+// accumulator row, writes to consecutive addresses across a warp.  Ainv/Ginv
+// halves are produced once per refresh by the inverse pass.
 #include "kfac_internal.cuh"
 #include "tc_prims.cuh"
 
@@ -56,7 +58,7 @@ struct GradPackGroup {
 
 __global__ void __launch_bounds__(256) gradhat_pack_grouped_kernel(
     const __grid_constant__ GradPackGroup g) {
-  const GradPackJob& J = g.job[blockIdx.y];
+  const GradPackJob J = g.job[blockIdx.y];  // by value: no reloads after each store
   const int64_t total = (int64_t)J.o * J.n;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
@@ -87,14 +89,15 @@ kfac_status launch_precondition(kfac_ctx* h, int layer, const float* gw, int64_t
     count_launch();
     if (kfac_status e = check_launch()) return e;
   }
+  // X = grad-hat . Ainv  [o x n] (Ainv symmetric), stored transposed as X^T [n x o]
   TcOperand Ainv{h->at<float>(L.Ainv_hi), h->at<float>(L.Ainv_lo), L.n, np};
   TcOperand G{g_hi, g_lo, L.o, np};
   TcEpilogue e1{};
   e1.out_hi = x_hi;
   e1.out_lo = x_lo;
   e1.ldo = op;
-  if (kfac_status e = launch_gemm_tc(h, layer, false, TC_EPI_SPLIT, Ainv, G, false, false, L.n,
-                                     L.o, L.n, e1, st))
+  if (kfac_status e = launch_gemm_tc(h, layer, false, TC_EPI_SPLIT, G, Ainv, false, false, L.o,
+                                     L.n, L.n, e1, st))
     return e;
   TcOperand Ginv{h->at<float>(L.Ginv_hi), h->at<float>(L.Ginv_lo), L.o, op};
   TcOperand XT{x_hi, x_lo, L.n, op};
@@ -109,7 +112,8 @@ kfac_status launch_precondition(kfac_ctx* h, int layer, const float* gw, int64_t
   e2.pb = pb;
   e2.mw = h->at<float>(L.m);
   e2.mb = e2.mw + (size_t)L.o * L.d_in;
-  return launch_gemm_tc(h, layer, false, TC_EPI_PRECOND, Ginv, XT, false, false, L.o, L.n, L.o,
+  // P^T = X^T . Ginv  [n x o]: P = Ginv . X (Ginv symmetric), computed transposed
+  return launch_gemm_tc(h, layer, false, TC_EPI_PRECOND, XT, Ginv, false, false, L.n, L.o, L.o,
                         e2, st);
 }
 
@@ -167,10 +171,10 @@ kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layer
     j.lo = g_lo;
     max_elems = std::max<int64_t>(max_elems, (int64_t)L.o * L.n);
     TcProblem q1{};
-    q1.A = TcOperand{h->at<float>(L.Ainv_hi), h->at<float>(L.Ainv_lo), L.n, np};
-    q1.B = TcOperand{g_hi, g_lo, L.o, np};
-    q1.M = L.n;
-    q1.N = L.o;
+    q1.A = TcOperand{g_hi, g_lo, L.o, np};   // X = grad-hat . Ainv, stored as X^T
+    q1.B = TcOperand{h->at<float>(L.Ainv_hi), h->at<float>(L.Ainv_lo), L.n, np};
+    q1.M = L.o;
+    q1.N = L.n;
     q1.K = L.n;
     q1.e.out_hi = x_hi;
     q1.e.out_lo = x_lo;
@@ -178,10 +182,10 @@ kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layer
     q1.layer = layers[i];
     p1.push_back(q1);
     TcProblem q2{};
-    q2.A = TcOperand{h->at<float>(L.Ginv_hi), h->at<float>(L.Ginv_lo), L.o, op};
-    q2.B = TcOperand{x_hi, x_lo, L.n, op};
-    q2.M = L.o;
-    q2.N = L.n;
+    q2.A = TcOperand{x_hi, x_lo, L.n, op};   // P^T = X^T . Ginv
+    q2.B = TcOperand{h->at<float>(L.Ginv_hi), h->at<float>(L.Ginv_lo), L.o, op};
+    q2.M = L.n;
+    q2.N = L.o;
     q2.K = L.o;
     q2.e.d_in = L.d_in;
     q2.e.eta = (float)h->hp.lr;

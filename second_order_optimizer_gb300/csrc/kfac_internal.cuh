@@ -138,10 +138,10 @@ struct TcEpilogue {
   float alpha, beta;     // SYRK: F <- beta F + alpha C (upper + mirror)
   float* C;
   int64_t ldc;
-  float* out_hi;         // SPLIT: C stored as TF32 halves, row pitch ldo
+  float* out_hi;         // SPLIT: C^T stored as TF32 halves, out[c * ldo + r]
   float* out_lo;
   int64_t ldo;
-  int d_in;              // PRECOND: P = C (o x n); columns >= d_in are the bias
+  int d_in;              // PRECOND: C = P^T (n x o): C[j][i] = P[i][j]; j >= d_in is the bias
   float eta, mu, lambda;
   float *ow, *ob, *pw, *pb, *mw, *mb;
 };

@@ -4,8 +4,8 @@
 //   with one of three fused epilogues:
 //     SYRK     F <- beta F + alpha C on tiles on/above the diagonal, plus mirrors (K1,
 //              with A = B = X = x-hat^T)
-//     SPLIT    store C as TF32 halves (hi, lo), ready to be the next product's operand
-//     PRECOND  P = C; optional momentum / weight-decay / lr update of W in place (K4)
+//     SPLIT    store C^T as TF32 halves (hi, lo), ready to be the next product's operand
+//     PRECOND  P^T = C; optional momentum / weight-decay / lr update of W in place (K4)
 //
 // Osawa et al., "Large-Scale Distributed Second-Order Optimization Using
 // Kronecker-Factored Approximate Curvature ...": §3.2 (A from activations, G from
@@ -24,7 +24,8 @@
 //         triangle has fewer tiles than SMs), warp-specialised:
 //           warp 0  TMA producer   (SW128 tiles of 128 rows x 128 bytes)
 //           warp 1  MMA issuer     (tcgen05.mma, accumulator in TMEM)
-//           warps 2-5 epilogue     (tcgen05.ld; 128 threads = 128 TMEM lanes)
+//           warps 2-9 epilogue     (tcgen05.ld; two warps per 32-lane TMEM quarter,
+//                                   each holding half of the tile's columns)
 //         The accumulator is double-buffered in TMEM and drained into fp32
 //         registers every `ksub` rows, so no TMEM accumulation runs longer
 //         than ksub rows whatever the tensor core's internal rounding.
@@ -58,11 +59,20 @@ struct TcCfg {
   static constexpr int STAGE_BYTES = kBF16 ? HALF_BYTES : 2 * HALF_BYTES;
   static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;   // 192 KB of stages
   static constexpr int TMEM_COLS = 2 * BN;        // double-buffered accumulator
-  static constexpr int EPI_WARPS = 4 * R;         // R per TMEM lane quarter, 128 columns each
+  static constexpr int EPI_WARPS = 8;             // two per TMEM lane quarter
+  static constexpr int CW = BN / 2;               // accumulator columns per epilogue thread
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int TPAD = BN + 1;             // output staging row pitch (floats)
-  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
-  static_assert((size_t)BM * TPAD * 4 <= (size_t)STAGES * STAGE_BYTES, "staging fits");
+  // After the main loop the stage buffers hold the output tile T [BM][TPAD] and,
+  // behind it, the epilogue's global inputs (old F, or W and m) for RIN rows at a
+  // time, fetched with asynchronous copies.
+  static constexpr int T_BYTES = BM * TPAD * 4;
+  static constexpr int RIN = BN == 128 ? 128 : 32;
+  static constexpr int REGION = STAGES * STAGE_BYTES > T_BYTES + 2 * RIN * BN * 4
+                                    ? STAGES * STAGE_BYTES
+                                    : T_BYTES + 2 * RIN * BN * 4;
+  static constexpr size_t SMEM = 1024 + (size_t)REGION + 256;
+  static_assert(T_BYTES % 16 == 0, "input staging aligned");
 };
 
 struct GemmTcParams {
@@ -113,7 +123,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
   using C = TcCfg<kBF16, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::REGION);
   uint64_t* empty = full + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + 2;
@@ -255,47 +265,170 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
   }
 
   // ------------------------------------------------------------ epilogue warps
+  // Every epilogue writes C^T-oriented: the thread holding accumulator row gr
+  // writes base[gc * ld + gr] for its columns gc, so consecutive lanes (rows)
+  // store to consecutive addresses.  SYRK: that is the mirror F[gc][gr] (the
+  // direct half F[gr][gc] goes through shared memory); SPLIT: X^T; PRECOND: the
+  // product is computed transposed, C[j][i] = P[i][j], so W[i][j] = base[i d_in + j].
   float* T = reinterpret_cast<float*>(smem);  // [BM][TPAD], reuses the stage buffers
+  // By value: p lives in kernel parameter space (indexed by problem in the grouped
+  // kernel); read through a reference, every field would be reloaded after each
+  // global store, which the compiler cannot prove does not alias it.
+  const TcEpilogue E = p.e;
+  const int64_t pM = p.M, pN = p.N;
+  const int64_t r0 = (int64_t)ti * C::BM, c0 = (int64_t)tj * C::BN;
+  // register path (no split-K, 128-wide tiles): results go to global memory from
+  // the registers the accumulator was drained into
+  const bool reg = C::BN == 128 && p.splits == 1;
+  // global inputs of the register path, staged column-major ([BN][BM], lanes on
+  // rows) behind T: SYRK old F; PRECOND W then m
+  float* S = reinterpret_cast<float*>(smem + C::T_BYTES);
+  static_assert(C::BN != 128 || C::T_BYTES + 2 * C::BN * C::BM * 4 <= C::REGION, "staging fits");
   if (warp >= 2) {
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int h = (warp - 2) >> 2;          // column half: [128 h, 128 h + 128)
+    const int h = (warp - 2) >> 2;          // column half: [CW h, CW h + CW)
     const int row = 32 * q + lane;
-    float sum[128];
+    const int64_t gr = r0 + row;
+    if (reg && gr < pM) {
+      // Pull this thread's epilogue inputs into L2 while the main loop runs (it
+      // feeds from L2, so HBM is idle); without this every CTA of a wave fetches
+      // them from HBM in the same few microseconds at the end.
+      if (EPI == TC_EPI_SYRK && E.beta != 0.f) {
+        for (int c = 0; c < C::CW; ++c) {
+          const int64_t gc = c0 + h * C::CW + c;
+          if (gc < pN && gr <= gc) tc::prefetch_l2(E.C + gc * E.ldc + gr);
+        }
+      } else if (EPI == TC_EPI_PRECOND && E.pw && gr < E.d_in) {
+        for (int c = 0; c < C::CW; ++c) {
+          const int64_t i = c0 + h * C::CW + c;
+          if (i >= pN) break;
+          tc::prefetch_l2(E.pw + i * E.d_in + gr);
+          tc::prefetch_l2(E.mw + i * E.d_in + gr);
+        }
+      }
+    }
+    float sum[C::CW];
 #pragma unroll
-    for (int c = 0; c < 128; ++c) sum[c] = 0.f;
+    for (int c = 0; c < C::CW; ++c) sum[c] = 0.f;
+    bool drained = true;
     for (int sub = 0; sub < nsub; ++sub) {
       const int buf = sub & 1;
       if (!tc::mbar_wait(&acc_full[buf], (sub >> 1) & 1, abort_flag)) {
         report_error(p.status, KFAC_ERR_TIMEOUT, p.layer, 4);
         *abort_flag = 1;
+        drained = false;
         break;
       }
       tc::tc_fence_after();
+      if (reg && sub == nsub - 1 && gr < pM) {
+        // every MMA has completed: the stage buffers are free for the inputs
+        if (EPI == TC_EPI_SYRK && E.beta != 0.f) {
+#pragma unroll 8
+          for (int c = 0; c < C::CW; ++c) {
+            const int64_t gc = c0 + h * C::CW + c;
+            if (gc < pN && gr <= gc)
+              tc::cp_async4(S + (h * C::CW + c) * C::BM + row, E.C + gc * E.ldc + gr);
+          }
+        } else if (EPI == TC_EPI_PRECOND && E.pw) {
+#pragma unroll 8
+          for (int c = 0; c < C::CW; ++c) {
+            const int64_t i = c0 + h * C::CW + c;
+            if (i >= pN) continue;
+            const int sidx = (h * C::CW + c) * C::BM + row;
+            const bool wcol = gr < E.d_in;
+            tc::cp_async4(S + sidx, wcol ? E.pw + i * E.d_in + gr : E.pb + i);
+            tc::cp_async4(S + C::BN * C::BM + sidx, wcol ? E.mw + i * E.d_in + gr : E.mb + i);
+          }
+        }
+      }
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < C::CW / 32; ++cc) {
         float v[32];
         tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) +
-                          (uint32_t)(buf * C::BN + h * 128 + cc * 32), v);
+                          (uint32_t)(buf * C::BN + h * C::CW + cc * 32), v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) sum[cc * 32 + i] += v[i];
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&acc_empty[buf]);
     }
-    // every MMA has completed (the last commit was waited on), so the stage
-    // buffers are free: stage the tile for coalesced output
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * C::EPI_WARPS) : "memory");
+    if (reg && drained && gr < pM) {
+      tc::cp_async_wait_all();   // this thread's own copies
+      if (EPI == TC_EPI_SYRK) {
 #pragma unroll
-    for (int c = 0; c < 128; ++c) T[row * C::TPAD + h * 128 + c] = sum[c];
+        for (int c = 0; c < C::CW; ++c) {
+          const int64_t gc = c0 + h * C::CW + c;
+          const bool ok = gc < pN && gr <= gc;
+          const float old = (ok && E.beta != 0.f) ? S[(h * C::CW + c) * C::BM + row] : 0.f;
+          const float v = fmaf(E.beta, old, E.alpha * sum[c]);
+          sum[c] = v;
+          if (ok) E.C[gc * E.ldc + gr] = v;
+        }
+      } else if (EPI == TC_EPI_SPLIT) {
+#pragma unroll
+        for (int c = 0; c < C::CW; ++c) {
+          const int64_t gc = c0 + h * C::CW + c;
+          if (gc >= pN) continue;
+          const float hi = tc::to_tf32(sum[c]);
+          E.out_hi[gc * E.ldo + gr] = hi;
+          E.out_lo[gc * E.ldo + gr] = tc::to_tf32(sum[c] - hi);
+        }
+      } else {  // PRECOND: row gr = column j of P, column gc = row i
+        const bool wcol = gr < E.d_in;
+#pragma unroll
+        for (int c = 0; c < C::CW; ++c) {
+          const int64_t i = c0 + h * C::CW + c;
+          if (i >= pN) continue;
+          const int sidx = (h * C::CW + c) * C::BM + row;
+          const float pr = sum[c];
+          const float w = E.pw ? S[sidx] : 0.f;
+          const float m = E.pw ? S[C::BN * C::BM + sidx] : 0.f;
+          const float mn = fmaf(E.mu, m, fmaf(E.lambda, w, pr));
+          const float wn = fmaf(-E.eta, mn, w);
+          if (wcol) {
+            const int64_t x = i * E.d_in + gr;
+            if (E.ow) E.ow[x] = pr;
+            if (E.pw) {
+              E.mw[x] = mn;
+              E.pw[x] = wn;
+            }
+          } else {
+            if (E.ob) E.ob[i] = pr;
+            if (E.pb) {
+              E.mb[i] = mn;
+              E.pb[i] = wn;
+            }
+          }
+        }
+      }
+    }
+    if (!reg || EPI == TC_EPI_SYRK) {
+      // stage the tile for coalesced output (SYRK: the new values, for the direct half)
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * C::EPI_WARPS) : "memory");
+#pragma unroll
+      for (int c = 0; c < C::CW; ++c) T[row * C::TPAD + h * C::CW + c] = sum[c];
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  constexpr int nth = C::THREADS;
+  if (reg) {
+    if (EPI == TC_EPI_SYRK && !*abort_flag) {
+      // direct entries gr < gc from the staged new values, coalesced over gc
+#pragma unroll 4
+      for (int e = threadIdx.x; e < C::BM * C::BN; e += nth) {
+        const int r = e / C::BN, c = e % C::BN;
+        const int64_t gr = r0 + r, gc = c0 + c;
+        if (gr < pM && gc < pN && gr < gc) E.C[gr * E.ldc + gc] = T[r * C::TPAD + c];
+      }
+    }
+    return;
+  }
 
-  // Epilogue loops run in batches of U elements per thread: all global loads of a
+  // Split-K reduction loops run in batches of U elements per thread: all loads of a
   // batch are issued before any store, so load latency overlaps instead of
   // serialising behind possibly-aliasing stores.
-  constexpr int nth = C::THREADS;
   constexpr int NT = C::BM * C::BN;
   constexpr int U = 8;
   int row_lo = 0, row_hi = C::BM;   // rows of the tile this CTA finishes
@@ -378,77 +511,92 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
     return;
   }
   __syncthreads();
-  const int e_lo = row_lo * C::BN, e_hi = row_hi * C::BN;
+  // ---------------------------------------------- epilogue from the staged tile
+  // (split-K, or 256-wide tiles).  Rows [row_lo, row_hi) of T; transposed stores
+  // walk rows fastest (coalesced over gr); global inputs are fetched RC rows at a
+  // time with asynchronous copies into S (behind T).
   const int nrows = row_hi - row_lo;
-  const int64_t r0 = (int64_t)ti * C::BM, c0 = (int64_t)tj * C::BN;
-  const TcEpilogue& E = p.e;
   if (EPI == TC_EPI_SYRK) {
     // tile entries (r <= c): F[r][c] = alpha*acc + beta*F[r][c]; T keeps the result
-    for (int b0 = e_lo + threadIdx.x; b0 < e_hi; b0 += nth * U) {
-      float old[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int e = b0 + u * nth;
-        const int64_t gr = r0 + e / C::BN, gc = c0 + e % C::BN;
-        const bool ok = e < e_hi && gr < p.M && gc < p.N && gr <= gc;
-        old[u] = (ok && E.beta != 0.f) ? E.C[gr * E.ldc + gc] : 0.f;
+    constexpr int RC = (C::REGION - C::T_BYTES) / (C::BN * 4) < C::BM
+                           ? (C::REGION - C::T_BYTES) / (C::BN * 4) : C::BM;
+    for (int ca = row_lo; ca < row_hi; ca += RC) {
+      const int cb = min(row_hi, ca + RC);
+      const int ne = (cb - ca) * C::BN;
+      if (E.beta != 0.f) {
+#pragma unroll 4
+        for (int e = threadIdx.x; e < ne; e += nth) {
+          const int64_t gr = r0 + ca + e / C::BN, gc = c0 + e % C::BN;
+          if (gr < pM && gc < pN && gr <= gc) tc::cp_async4(S + e, E.C + gr * E.ldc + gc);
+        }
+        tc::cp_async_wait_all();
+        __syncthreads();
       }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int e = b0 + u * nth;
-        const int r = e / C::BN, c = e % C::BN;
+#pragma unroll 4
+      for (int e = threadIdx.x; e < ne; e += nth) {
+        const int r = ca + e / C::BN, c = e % C::BN;
         const int64_t gr = r0 + r, gc = c0 + c;
-        if (!(e < e_hi && gr < p.M && gc < p.N && gr <= gc)) continue;
-        const float v = fmaf(E.beta, old[u], E.alpha * T[r * C::TPAD + c]);
+        if (!(gr < pM && gc < pN && gr <= gc)) continue;
+        const float old = E.beta != 0.f ? S[e] : 0.f;
+        const float v = fmaf(E.beta, old, E.alpha * T[r * C::TPAD + c]);
         E.C[gr * E.ldc + gc] = v;
         T[r * C::TPAD + c] = v;
       }
+      __syncthreads();
     }
-    __syncthreads();
     // mirrors (gr < gc): F[gc][gr], coalesced over gr
+#pragma unroll 4
     for (int e = threadIdx.x; e < nrows * C::BN; e += nth) {
       const int c = e / nrows, r = row_lo + e % nrows;
       const int64_t gr = r0 + r, gc = c0 + c;
-      if (gr >= p.M || gc >= p.N || gr >= gc) continue;
+      if (gr >= pM || gc >= pN || gr >= gc) continue;
       E.C[gc * E.ldc + gr] = T[r * C::TPAD + c];
     }
   } else if (EPI == TC_EPI_SPLIT) {
-    for (int e = e_lo + threadIdx.x; e < e_hi; e += nth) {
-      const int r = e / C::BN, c = e % C::BN;
+#pragma unroll 4
+    for (int e = threadIdx.x; e < nrows * C::BN; e += nth) {
+      const int c = e / nrows, r = row_lo + e % nrows;
       const int64_t gr = r0 + r, gc = c0 + c;
-      if (gr >= p.M || gc >= p.N) continue;
+      if (gr >= pM || gc >= pN) continue;
       const float v = T[r * C::TPAD + c];
       const float hi = tc::to_tf32(v);
-      E.out_hi[gr * E.ldo + gc] = hi;
-      E.out_lo[gr * E.ldo + gc] = tc::to_tf32(v - hi);
+      E.out_hi[gc * E.ldo + gr] = hi;
+      E.out_lo[gc * E.ldo + gr] = tc::to_tf32(v - hi);
     }
-  } else {  // TC_EPI_PRECOND: rows i < o, columns j < n = d_in + bias
-    for (int b0 = e_lo + threadIdx.x; b0 < e_hi; b0 += nth * U) {
-      float w[U], m[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int e = b0 + u * nth;
-        const int64_t i = r0 + e / C::BN, j = c0 + e % C::BN;
-        w[u] = m[u] = 0.f;
-        if (E.pw && e < e_hi && i < p.M && j < p.N) {
+  } else {  // TC_EPI_PRECOND: tile row gr = column j of P (j >= d_in: bias), column gc = row i
+    constexpr int RC = (C::REGION - C::T_BYTES) / (2 * C::BN * 4) < C::BM
+                           ? (C::REGION - C::T_BYTES) / (2 * C::BN * 4) : C::BM;
+    float* Sw = S;
+    float* Sm = S + RC * C::BN;
+    for (int ca = row_lo; ca < row_hi; ca += RC) {
+      const int cb = min(row_hi, ca + RC);
+      const int nr = cb - ca;
+      const int ne = nr * C::BN;
+      if (E.pw) {
+#pragma unroll 4
+        for (int e = threadIdx.x; e < ne; e += nth) {
+          const int64_t j = r0 + ca + e % nr, i = c0 + e / nr;
+          if (!(j < pM && i < pN)) continue;
           if (j < E.d_in) {
-            w[u] = E.pw[i * E.d_in + j];
-            m[u] = E.mw[i * E.d_in + j];
+            tc::cp_async4(Sw + e, E.pw + i * E.d_in + j);
+            tc::cp_async4(Sm + e, E.mw + i * E.d_in + j);
           } else {
-            w[u] = E.pb[i];
-            m[u] = E.mb[i];
+            tc::cp_async4(Sw + e, E.pb + i);
+            tc::cp_async4(Sm + e, E.mb + i);
           }
         }
+        tc::cp_async_wait_all();
+        __syncthreads();
       }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int e = b0 + u * nth;
-        const int r = e / C::BN, c = e % C::BN;
-        const int64_t i = r0 + r, j = c0 + c;
-        if (!(e < e_hi && i < p.M && j < p.N)) continue;
+#pragma unroll 4
+      for (int e = threadIdx.x; e < ne; e += nth) {
+        const int r = ca + e % nr, c = e / nr;
+        const int64_t j = r0 + r, i = c0 + c;
+        if (!(j < pM && i < pN)) continue;
+        const float w = E.pw ? Sw[e] : 0.f, m = E.pw ? Sm[e] : 0.f;
         const float pr = T[r * C::TPAD + c];
-        const float mn = fmaf(E.mu, m[u], fmaf(E.lambda, w[u], pr));
-        const float wn = fmaf(-E.eta, mn, w[u]);
+        const float mn = fmaf(E.mu, m, fmaf(E.lambda, w, pr));
+        const float wn = fmaf(-E.eta, mn, w);
         if (j < E.d_in) {
           const int64_t x = i * E.d_in + j;
           if (E.ow) E.ow[x] = pr;
@@ -464,6 +612,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
           }
         }
       }
+      __syncthreads();
     }
   }
 }
@@ -547,7 +696,7 @@ struct PackGroup {
 
 template <typename T, bool kSplit>
 __global__ void __launch_bounds__(256) pack_grouped_kernel(const __grid_constant__ PackGroup g) {
-  const PackJob& J = g.job[blockIdx.z];
+  const PackJob J = g.job[blockIdx.z];
   const int64_t r0 = (int64_t)blockIdx.x * 32;
   const int c0 = blockIdx.y * 32;
   if (r0 >= J.Kp || c0 >= J.n) return;
