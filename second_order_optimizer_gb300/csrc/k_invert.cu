@@ -49,22 +49,25 @@ __global__ void __launch_bounds__(256) inv_prep_kernel(const InvJob* jobs, float
   }
 }
 
-// Diagonal block b x b (b <= 64) at (k, k): L_kk = chol(block) and X_kk = L_kk^{-1}
-// in one pass.  256 threads as a 16 x 16 grid; thread (ty, tx) keeps rows
-// ty + 16i and columns tx + 16q (i, q < 4) of both S (-> L) and T (-> L^{-1},
-// starting from I) in registers.  Step j: the owners publish column j of S and
-// row j of T to a double-buffered shared vector (one barrier per step), then
-// every thread updates its own elements:
-//   S[r][j] = S[r][j]/sqrt(d),  S[r][c] -= l_rj l_cj                 (j < c <= r)
-//   T[j][c] = T[j][c]/sqrt(d),  T[r][c] -= l_rj T[j][c]/sqrt(d)      (r > j, c <= j)
-// i.e. a right-looking Cholesky and the forward elimination of [L | I] sharing
-// the column l_j.
-// (A fully unrolled one-warp 32 x 32 variant kept every value in registers but
-// compiled to tens of KB of straight-line code; it ran 2x slower, stalled on
-// instruction fetch.  This loop form stays resident in the instruction cache.)
-__device__ __forceinline__ float pick4(const float (&v)[4], int q) {
-  return q == 0 ? v[0] : q == 1 ? v[1] : q == 2 ? v[2] : v[3];
-}
+// Diagonal block b x b (b <= 64) at (k, k): L_kk = chol(block) and X_kk = L_kk^{-1}.
+// The block sits in shared memory (rows >= b padded with the identity) and is
+// factored in 16-column sub-panels:
+//   (a) one warp factors the 16 x 16 diagonal sub-block D and inverts it: lane r
+//       holds row r of D and of D^{-1} in registers; each column's multipliers
+//       reach the other lanes by warp shuffles, so the 16 dependent steps need
+//       no block barrier;
+//   (b) the rows below become L_below = A_below D^{-T} (a product with D^{-1});
+//   (c) the trailing lower triangle: A <- A - L_below L_below^T.
+// X_kk's diagonal 16-blocks are the D^{-1}; its off-diagonal blocks follow by
+// doubling over block pairs, X_BT = -X_BB (L_BT X_TT).  A pivot that is not > 0
+// and finite is recorded (first failing column), replaced by 1, and reported
+// once per sub-panel.
+// (A per-column version that kept the whole block in registers of 256 threads
+// paid a block barrier and shared-memory round trip per column, ~1500 cycles per
+// column on GB300; this one spends ~220 cycles per column in the warp.)
+constexpr int SB = 16;       // sub-panel width
+constexpr int AP = NB + 1;   // shared row pitch (floats)
+constexpr unsigned kFull = 0xffffffffu;
 
 __global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int k,
                                                         DevStatus* st) {
@@ -72,74 +75,132 @@ __global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int 
   if (k >= J.n) return;
   const int b = min(NB, J.n - k);
   const int n = J.n;
-  __shared__ float colS[2][NB];
-  __shared__ float rowT[2][NB];
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  float S[4][4], T[4][4];
+  __shared__ float A[NB * AP];
+  __shared__ float X[NB * AP];
+  __shared__ float Y[32 * 33];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int u = 0; u < NB * NB / 256; ++u) {
+    const int e = tid + 256 * u;
+    const int r = e / NB, c = e % NB;
+    float v = 0.f;
+    if (r < b && c <= r) v = J.L[(int64_t)(k + r) * n + k + c];
+    else if (r == c) v = 1.f;
+    A[r * AP + c] = v;
+    X[r * AP + c] = 0.f;
+  }
+  __syncthreads();
+  for (int p = 0; p < NB / SB; ++p) {
+    const int o = p * SB;
+    if (warp == 0) {   // (a)
+      const int r = lane & (SB - 1);   // lanes 16..31 mirror 0..15
+      float s[SB], t[SB];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r = ty + 16 * i, c = tx + 16 * q;
-      S[i][q] = (r < b && c <= r) ? J.L[(int64_t)(k + r) * n + k + c] : 0.f;
-      T[i][q] = (r == c) ? 1.f : 0.f;
-    }
-  for (int j = 0; j < b; ++j) {
-    const int buf = j & 1;
-    if (tx == (j & 15)) {
-      const int q = j >> 4;
+      for (int c = 0; c < SB; ++c) {
+        s[c] = (c <= r) ? A[(o + r) * AP + o + c] : 0.f;
+        t[c] = (c == r) ? 1.f : 0.f;
+      }
+      int bad = -1;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) colS[buf][ty + 16 * i] = pick4(S[i], q);
-    }
-    if (ty == (j & 15)) {
-      const int i = j >> 4;
+      for (int j = 0; j < SB; ++j) {
+        float d = __shfl_sync(kFull, s[j], j);
+        const bool ok = d > 0.f && d <= 3.402823466e38f;   // positive and finite
+        bad = (!ok && bad < 0) ? j : bad;
+        d = ok ? d : 1.f;
+        const float inv = rsqrtf(d), sq = d * inv;
+        const float l = r > j ? s[j] * inv : 0.f;
+        s[j] = r == j ? sq : (r > j ? l : s[j]);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float v = i == 0 ? T[0][q] : i == 1 ? T[1][q] : i == 2 ? T[2][q] : T[3][q];
-        rowT[buf][tx + 16 * q] = v;
+        for (int c = j + 1; c < SB; ++c) s[c] = fmaf(-l, __shfl_sync(kFull, l, c), s[c]);
+#pragma unroll
+        for (int c = 0; c <= j; ++c) {
+          const float tj = __shfl_sync(kFull, t[c], j) * inv;
+          t[c] = r == j ? tj : fmaf(-l, tj, t[c]);
+        }
+      }
+      if (bad >= 0 && o + bad < b && lane == 0)
+        report_error(st, KFAC_ERR_NOT_PD, J.layer, k + o + bad);
+      if (lane < SB) {
+#pragma unroll
+        for (int c = 0; c < SB; ++c)
+          if (c <= r) {
+            A[(o + r) * AP + o + c] = s[c];
+            X[(o + r) * AP + o + c] = t[c];
+          }
       }
     }
     __syncthreads();
-    float d = colS[buf][j];
-    if (!(d > 0.f) || !isfinite(d)) {
-      if (tid == 0) report_error(st, KFAC_ERR_NOT_PD, J.layer, k + j);
-      d = 1.f;
-    }
-    const float sq = sqrtf(d);
-    const float inv = 1.f / sq;
-    float lr[4], lc[4], tj[4];
+    const int nr = NB - o - SB;   // rows below the sub-block
+    if (nr > 0) {
+      // (b) thread: column c = tid % 16 with row c of D^{-1} in registers
+      float outv[3];
+      {
+        const int c = tid % SB;
+        float dr[SB];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      lr[i] = colS[buf][ty + 16 * i] * inv;
-      lc[i] = colS[buf][tx + 16 * i] * inv;
-      tj[i] = rowT[buf][tx + 16 * i] * inv;
-    }
+        for (int m = 0; m < SB; ++m) dr[m] = X[(o + c) * AP + o + m];   // 0 for m > c
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = ty + 16 * i;
+        for (int u = 0; u < 3; ++u) {
+          const int i = o + SB + tid / SB + 16 * u;
+          float acc = 0.f;
+          if (i < NB) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int c = tx + 16 * q;
-        if (r > j && c > j && c <= r) S[i][q] = fmaf(-lr[i], lc[q], S[i][q]);
-        else if (c == j && r > j) S[i][q] = lr[i];
-        else if (r == j && c == j) S[i][q] = sq;
-        if (c <= j) {
-          if (r == j) T[i][q] = tj[q];
-          else if (r > j) T[i][q] = fmaf(-lr[i], tj[q], T[i][q]);
+            for (int m = 0; m < SB; ++m) acc = fmaf(A[i * AP + o + m], dr[m], acc);
+          }
+          outv[u] = acc;
         }
       }
+      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < 3; ++u) {
+        const int i = o + SB + tid / SB + 16 * u;
+        if (i < NB) A[i * AP + o + tid % SB] = outv[u];
+      }
+      __syncthreads();
+      // (c) thread: column jj with row jj of L_below in registers; rows i >= jj
+      const int jj = o + SB + (tid & 63);
+      if (jj < NB) {
+        float lj[SB];
+#pragma unroll
+        for (int m = 0; m < SB; ++m) lj[m] = A[jj * AP + o + m];
+        for (int i = o + SB + (tid >> 6); i < NB; i += 4) {
+          if (i < jj) continue;
+          float acc = A[i * AP + jj];
+#pragma unroll
+          for (int m = 0; m < SB; ++m) acc = fmaf(-A[i * AP + o + m], lj[m], acc);
+          A[i * AP + jj] = acc;
+        }
+      }
+      __syncthreads();
     }
   }
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r = ty + 16 * i, c = tx + 16 * q;
-      if (r >= b || c >= b) continue;
-      const int64_t g = (int64_t)(k + r) * n + k + c;
-      J.L[g] = (c <= r) ? S[i][q] : 0.f;
-      J.X[g] = (c <= r) ? T[i][q] : 0.f;
+  // X off-diagonal blocks: pairs (T, B) of size sz, X_BT = -X_BB (L_BT X_TT)
+  for (int sz = SB; sz < NB; sz *= 2) {
+    const int ne = (NB / (2 * sz)) * sz * sz;
+    for (int e = tid; e < ne; e += 256) {
+      const int pr = e / (sz * sz), i = (e / sz) % sz, c = e % sz;
+      const int T0 = pr * 2 * sz, B0 = T0 + sz;
+      float acc = 0.f;
+      for (int m = c; m < sz; ++m) acc = fmaf(A[(B0 + i) * AP + T0 + m], X[(T0 + m) * AP + T0 + c], acc);
+      Y[(pr * sz + i) * 33 + c] = acc;
     }
+    __syncthreads();
+    for (int e = tid; e < ne; e += 256) {
+      const int pr = e / (sz * sz), i = (e / sz) % sz, c = e % sz;
+      const int T0 = pr * 2 * sz, B0 = T0 + sz;
+      float acc = 0.f;
+      for (int m = 0; m <= i; ++m) acc = fmaf(X[(B0 + i) * AP + B0 + m], Y[(pr * sz + m) * 33 + c], acc);
+      X[(B0 + i) * AP + T0 + c] = -acc;
+    }
+    __syncthreads();
+  }
+#pragma unroll 4
+  for (int e = tid; e < b * b; e += 256) {
+    const int r = e / b, c = e % b;
+    const int64_t g = (int64_t)(k + r) * n + k + c;
+    J.L[g] = (c <= r) ? A[r * AP + c] : 0.f;
+    J.X[g] = (c <= r) ? X[r * AP + c] : 0.f;
+  }
 }
 
 // L[i, k:k+b] <- L[i, k:k+b] . X_kk^T for rows i in [k+b, n); one CTA owns a
