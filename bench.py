@@ -311,16 +311,23 @@ def run_gpu(args, rank, world, peaks, peak_kind):
                                    [params[li][0] for li in kron_idx],
                                    [params[li][1] for li in kron_idx])
 
+    diag_idx = [li for li, l in enumerate(layers) if l.kind == "diag"]
+    k5_groups = {}   # layers whose diagonal factors come from a and g, by input dtype
+    for li in diag_idx:
+        if layers[li].act != "bn":
+            k5_groups.setdefault(layers[li].in_dtype, []).append(li)
+
     def phase_diag(x):
-        for li, l in enumerate(layers):
-            if l.kind == "diag":
-                pw, pb = params[li]
-                if l.act == "bn":
-                    gn, an = x[li]["g_new"], x[li]["a_new"]
-                else:
-                    h.diag_factors(li, x[li]["a"], x[li]["g"], gnew[li], anew[li])
-                    gn, an = gnew[li], anew[li]
-                h.diag_step(li, gn, an, x[li]["grad_w"], x[li]["grad_b"], pw, pb)
+        for grp in k5_groups.values():
+            h.diag_factors_batched(grp, [x[li]["a"] for li in grp], [x[li]["g"] for li in grp],
+                                   [gnew[li] for li in grp], [anew[li] for li in grp])
+        if diag_idx:
+            bn = lambda li: layers[li].act == "bn"
+            h.diag_step_batched(
+                diag_idx, [x[li]["g_new"] if bn(li) else gnew[li] for li in diag_idx],
+                [x[li]["a_new"] if bn(li) else anew[li] for li in diag_idx],
+                [x[li]["grad_w"] for li in diag_idx], [x[li]["grad_b"] for li in diag_idx],
+                [params[li][0] for li in diag_idx], [params[li][1] for li in diag_idx])
 
     def step(t, x, ev=None):
         """The eager step through the public API (used for warm-up and end-to-end)."""

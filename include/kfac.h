@@ -145,6 +145,19 @@ kfac_status kfac_diag_factors(kfac_handle h, int layer, const void* a, int64_t l
                               const void* g, int64_t ldg, int64_t rows, double scale,
                               float* g_new, float* a_new, cudaStream_t stream);
 
+/* K5 for several layers in one launch: the same result as calling
+ * kfac_diag_factors(layers[i], a[i], lda[i], g[i], ldg[i], rows[i], scale,
+ * g_new[i], a_new[i]) for each i, up to the order of the floating-point sums
+ * over rows (each column is still summed with compensation, then the row
+ * splits in fixed order).  Host arrays of length count; each layer at most
+ * once; all layers of one in_dtype.  Groups beyond the workspace's K5 scratch
+ * or 64 layers are processed in further launches. */
+kfac_status kfac_diag_factors_batched(kfac_handle h, int count, const int* layers,
+                                      const void* const* a, const int64_t* lda,
+                                      const void* const* g, const int64_t* ldg,
+                                      const int64_t* rows, double scale, float* const* g_new,
+                                      float* const* a_new, cudaStream_t stream);
+
 /* K2+K3: damped inverses (F + sqrt(gamma) I)^{-1} for F in {A, G} of one KRON
  * layer, or of every KRON layer when layer == -1 (one batched pass), by
  * blocked Cholesky and a blocked triangular inverse.  A non positive-definite
@@ -190,6 +203,19 @@ kfac_status kfac_diag_step(kfac_handle h, int layer, const float* g_new, const f
                            const float* grad_w, const float* grad_b,
                            float* param_w, float* param_b, float* out_w, float* out_b,
                            cudaStream_t stream);
+
+/* K6 for several DIAG layers in one streaming launch: bit-for-bit the result
+ * of calling kfac_diag_step for each i with the i-th entries of the host
+ * arrays (grad_b, param_b, out_w, out_b may be NULL arrays or hold NULL
+ * entries under the same rules as the single call).  Each layer at most once;
+ * up to 64 layers per launch, more in further launches.  One ticket orders the
+ * write-back of every layer's EMA vectors after all reads. */
+kfac_status kfac_diag_step_batched(kfac_handle h, int count, const int* layers,
+                                   const float* const* g_new, const float* const* a_new,
+                                   const float* const* grad_w, const float* const* grad_b,
+                                   float* const* param_w, float* const* param_b,
+                                   float* const* out_w, float* const* out_b,
+                                   cudaStream_t stream);
 
 /* Synchronise the device and report the first device-side error since the
  * last call (then clear it).  bad_layer / info (nullable) receive the layer

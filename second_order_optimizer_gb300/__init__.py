@@ -122,6 +122,19 @@ class Kfac:
                                      rows, float(scale), _ptr(g_new), _ptr(a_new),
                                      _stream(stream)), "kfac_diag_factors")
 
+    def diag_factors_batched(self, layers, a_list, g_list, g_new, a_new, scale: float = 0.0,
+                             stream=None):
+        """kfac_diag_factors_batched over parallel lists of layers, inputs and output vectors."""
+        k = len(layers)
+        I64 = ctypes.c_int64 * k
+        P = ctypes.c_void_p * k
+        _check(LIB.kfac_diag_factors_batched(
+            self._h, k, (ctypes.c_int * k)(*layers), P(*[_ptr(x) for x in a_list]),
+            I64(*[x.stride(0) for x in a_list]), P(*[_ptr(x) for x in g_list]),
+            I64(*[x.stride(0) for x in g_list]), I64(*[x.shape[0] for x in a_list]),
+            float(scale), P(*[_ptr(x) for x in g_new]), P(*[_ptr(x) for x in a_new]),
+            _stream(stream)), "kfac_diag_factors_batched")
+
     def invert(self, layer: int = -1, stream=None):
         _check(LIB.kfac_invert(self._h, layer, _stream(stream)), "kfac_invert")
 
@@ -147,6 +160,17 @@ class Kfac:
         _check(LIB.kfac_diag_step(self._h, layer, _ptr(g_new), _ptr(a_new), _ptr(grad_w),
                                   _ptr(grad_b), _ptr(param_w), _ptr(param_b), _ptr(out_w),
                                   _ptr(out_b), _stream(stream)), "kfac_diag_step")
+
+    def diag_step_batched(self, layers, g_new, a_new, grad_w, grad_b, param_w, param_b,
+                          out_w=None, out_b=None, stream=None):
+        """kfac_diag_step_batched over parallel lists (None, or lists that may hold None)."""
+        k = len(layers)
+        P = ctypes.c_void_p * k
+        arr = lambda xs: None if xs is None else P(*[_ptr(x) for x in xs])
+        _check(LIB.kfac_diag_step_batched(
+            self._h, k, (ctypes.c_int * k)(*layers), arr(g_new), arr(a_new), arr(grad_w),
+            arr(grad_b), arr(param_w), arr(param_b), arr(out_w), arr(out_b), _stream(stream)),
+            "kfac_diag_step_batched")
 
     # -- status and state --------------------------------------------------------
     def get_status(self):

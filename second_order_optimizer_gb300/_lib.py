@@ -55,10 +55,14 @@ SIGNATURES = [
     ("kfac_update_factors", _i, [_vp, _i, _vp, _i64, _vp, _i64, _i64, _d, _vp]),
     ("kfac_update_factors_batched", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _d, _vp]),
     ("kfac_diag_factors", _i, [_vp, _i, _vp, _i64, _vp, _i64, _i64, _d, _vp, _vp, _vp]),
+    ("kfac_diag_factors_batched", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _d, _vp, _vp,
+                                       _vp]),
     ("kfac_invert", _i, [_vp, _i, _vp]),
     ("kfac_precondition", _i, [_vp, _i, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     ("kfac_precondition_batched", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     ("kfac_diag_step", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    ("kfac_diag_step_batched", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                    _vp]),
     ("kfac_get_status", _i, [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     ("kfac_state_info", _i, [_vp, _i, _i, ctypes.POINTER(_sz), ctypes.POINTER(_sz)]),
     ("kfac_destroy", _i, [_vp]),

@@ -17,6 +17,8 @@
 #include "kfac_internal.cuh"
 
 #include <algorithm>
+#include <cmath>
+#include <cstring>
 #include <mutex>
 
 namespace kfac {
@@ -67,64 +69,122 @@ __device__ __forceinline__ void diag_elem(const DiagParams& p, float gsi, float 
   if (pout) *pout = pr;
 }
 
+// Unit u of one layer: VEC: four consecutive weights (u < o d_in / 4), else one
+// weight; the last o units are the bias column j = d_in.
 template <bool VEC>
-__global__ void __launch_bounds__(kDiagThreads) diag_step_kernel(DiagParams p) {
+__device__ __forceinline__ void diag_unit(const DiagParams& p, int64_t u) {
   const int64_t nw = (int64_t)p.o * p.d_in;
   const int64_t units = VEC ? nw / 4 : nw;
-  const int64_t total = units + (p.has_bias ? p.o : 0);
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < total; u += stride) {
-    if (u < units) {
-      if (VEC) {
-        const int64_t e = u * 4;
-        const int i = (int)(e / p.d_in), j = (int)(e % p.d_in);
-        const float gsi = ema1(p.xi, p.one_minus_xi, __ldg(p.gs + i), __ldg(p.g_new + i));
-        const float4 as4 = __ldg(reinterpret_cast<const float4*>(p.as + j));
-        const float4 an4 = __ldg(reinterpret_cast<const float4*>(p.a_new + j));
-        const float4 g4 = __ldcs(reinterpret_cast<const float4*>(p.gw + e));
-        float4 w4 = __ldcs(reinterpret_cast<const float4*>(p.pw + e));
-        float4 m4 = __ldcs(reinterpret_cast<const float4*>(p.mw + e));
-        float4 p4;
-        diag_elem(p, gsi, ema1(p.xi, p.one_minus_xi, as4.x, an4.x), g4.x, w4.x, m4.x, &p4.x);
-        diag_elem(p, gsi, ema1(p.xi, p.one_minus_xi, as4.y, an4.y), g4.y, w4.y, m4.y, &p4.y);
-        diag_elem(p, gsi, ema1(p.xi, p.one_minus_xi, as4.z, an4.z), g4.z, w4.z, m4.z, &p4.z);
-        diag_elem(p, gsi, ema1(p.xi, p.one_minus_xi, as4.w, an4.w), g4.w, w4.w, m4.w, &p4.w);
-        __stcs(reinterpret_cast<float4*>(p.pw + e), w4);
-        __stcs(reinterpret_cast<float4*>(p.mw + e), m4);
-        if (p.ow) __stcs(reinterpret_cast<float4*>(p.ow + e), p4);
-      } else {
-        const int i = (int)(u / p.d_in), j = (int)(u % p.d_in);
-        const float gsi = ema1(p.xi, p.one_minus_xi, p.gs[i], p.g_new[i]);
-        const float asj = ema1(p.xi, p.one_minus_xi, p.as[j], p.a_new[j]);
-        float w = p.pw[u], m = p.mw[u];
-        diag_elem(p, gsi, asj, p.gw[u], w, m, p.ow ? p.ow + u : nullptr);
-        p.pw[u] = w;
-        p.mw[u] = m;
-      }
-    } else {  // bias column j = d_in
-      const int i = (int)(u - units);
+  if (u < units) {
+    if (VEC) {
+      const int64_t e = u * 4;
+      const int i = (int)(e / p.d_in), j = (int)(e % p.d_in);
+      const float gsi = ema1(p.xi, p.one_minus_xi, __ldg(p.gs + i), __ldg(p.g_new + i));
+      const float4 as4 = __ldg(reinterpret_cast<const float4*>(p.as + j));
+      const float4 an4 = __ldg(reinterpret_cast<const float4*>(p.a_new + j));
+      const float4 g4 = __ldcs(reinterpret_cast<const float4*>(p.gw + e));
+      float4 w4 = __ldcs(reinterpret_cast<const float4*>(p.pw + e));
+      float4 m4 = __ldcs(reinterpret_cast<const float4*>(p.mw + e));
+      float4 p4;
+      diag_elem(p, gsi, ema1(p.xi, p.one_minus_xi, as4.x, an4.x), g4.x, w4.x, m4.x, &p4.x);
+      diag_elem(p, gsi, ema1(p.xi, p.one_minus_xi, as4.y, an4.y), g4.y, w4.y, m4.y, &p4.y);
+      diag_elem(p, gsi, ema1(p.xi, p.one_minus_xi, as4.z, an4.z), g4.z, w4.z, m4.z, &p4.z);
+      diag_elem(p, gsi, ema1(p.xi, p.one_minus_xi, as4.w, an4.w), g4.w, w4.w, m4.w, &p4.w);
+      __stcs(reinterpret_cast<float4*>(p.pw + e), w4);
+      __stcs(reinterpret_cast<float4*>(p.mw + e), m4);
+      if (p.ow) __stcs(reinterpret_cast<float4*>(p.ow + e), p4);
+    } else {
+      const int i = (int)(u / p.d_in), j = (int)(u % p.d_in);
       const float gsi = ema1(p.xi, p.one_minus_xi, p.gs[i], p.g_new[i]);
-      const float asj = ema1(p.xi, p.one_minus_xi, p.as[p.d_in], p.a_new[p.d_in]);
-      float w = p.pb[i], m = p.mb[i];
-      diag_elem(p, gsi, asj, p.gb[i], w, m, p.ob ? p.ob + i : nullptr);
-      p.pb[i] = w;
-      p.mb[i] = m;
+      const float asj = ema1(p.xi, p.one_minus_xi, p.as[j], p.a_new[j]);
+      float w = p.pw[u], m = p.mw[u];
+      diag_elem(p, gsi, asj, p.gw[u], w, m, p.ow ? p.ow + u : nullptr);
+      p.pw[u] = w;
+      p.mw[u] = m;
     }
+  } else {  // bias column j = d_in
+    const int i = (int)(u - units);
+    const float gsi = ema1(p.xi, p.one_minus_xi, p.gs[i], p.g_new[i]);
+    const float asj = ema1(p.xi, p.one_minus_xi, p.as[p.d_in], p.a_new[p.d_in]);
+    float w = p.pb[i], m = p.mb[i];
+    diag_elem(p, gsi, asj, p.gb[i], w, m, p.ob ? p.ob + i : nullptr);
+    p.pb[i] = w;
+    p.mb[i] = m;
   }
-  // last CTA stores the new EMA vectors (every other CTA has finished reading them)
-  __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(p.ticket, 1) == (int)gridDim.x - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+}
+
+__device__ __forceinline__ int64_t diag_units(const DiagParams& p, bool vec) {
+  const int64_t nw = (int64_t)p.o * p.d_in;
+  return (vec ? nw / 4 : nw) + (p.has_bias ? p.o : 0);
+}
+
+// The new EMA vectors of one layer (called by the last CTA only).
+__device__ void diag_store_ema(const DiagParams& p) {
   for (int i = threadIdx.x; i < p.o; i += blockDim.x)
     p.gs[i] = ema1(p.xi, p.one_minus_xi, __ldcg(p.gs + i), p.g_new[i]);
   const int n = p.d_in + p.has_bias;
   for (int j = threadIdx.x; j < n; j += blockDim.x)
     p.as[j] = ema1(p.xi, p.one_minus_xi, __ldcg(p.as + j), p.a_new[j]);
+}
+
+// True in every thread of the last CTA to finish (every other CTA has finished
+// reading the old EMA vectors); that CTA also resets the ticket.
+__device__ __forceinline__ bool last_cta(int* ticket) {
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1) == (int)gridDim.x - 1);
+  __syncthreads();
+  if (!s_last) return false;
+  __threadfence();
+  return true;
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kDiagThreads) diag_step_kernel(DiagParams p) {
+  const int64_t total = diag_units(p, VEC);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < total; u += stride)
+    diag_unit<VEC>(p, u);
+  if (!last_cta(p.ticket)) return;
+  diag_store_ema(p);
   if (threadIdx.x == 0) *p.ticket = 0;
+}
+
+// Several layers in one launch: the layers' units are concatenated (job q owns
+// global units [start[q], start[q+1])); a thread walks its units in increasing
+// order and reloads the job only when it crosses into the next one.
+constexpr int kMaxDiagGroup = 64;
+struct DiagGroup {
+  DiagParams job[kMaxDiagGroup];
+  int64_t start[kMaxDiagGroup + 1];
+  int vec[kMaxDiagGroup];
+  int count;
+  int* ticket;
+};
+
+__global__ void __launch_bounds__(kDiagThreads)
+diag_step_grouped_kernel(const __grid_constant__ DiagGroup g) {
+  const int64_t total = g.start[g.count];
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int q = -1;
+  int64_t qbeg = 0, qend = 0;
+  int vec = 0;
+  DiagParams P{};
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < total; u += stride) {
+    if (u >= qend) {
+      do ++q; while (u >= g.start[q + 1]);
+      P = g.job[q];   // by value: registers, not parameter-space reloads
+      qbeg = g.start[q];
+      qend = g.start[q + 1];
+      vec = g.vec[q];
+    }
+    if (vec) diag_unit<true>(P, u - qbeg);
+    else diag_unit<false>(P, u - qbeg);
+  }
+  if (!last_cta(g.ticket)) return;
+  for (int q2 = 0; q2 < g.count; ++q2) diag_store_ema(g.job[q2]);
+  if (threadIdx.x == 0) *g.ticket = 0;
 }
 
 // K5 ------------------------------------------------------------------------
@@ -141,8 +201,7 @@ struct DiagFactorParams {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(kK5Threads) diag_factor_kernel(DiagFactorParams p) {
-  const int cb = blockIdx.x, split = blockIdx.y;
+__device__ __forceinline__ void diag_factor_body(const DiagFactorParams& p, int cb, int split) {
   const int c = cb * kK5Threads + threadIdx.x;   // 0..d_in-1: a columns; d_in..: g columns
   const int ncols = p.d_in + p.o;
   const int64_t r0 = (int64_t)split * p.rows_per_split;
@@ -185,48 +244,64 @@ __global__ void __launch_bounds__(kK5Threads) diag_factor_kernel(DiagFactorParam
   if (threadIdx.x == 0) p.tickets[cb] = 0;
 }
 
+template <typename T>
+__global__ void __launch_bounds__(kK5Threads) diag_factor_kernel(DiagFactorParams p) {
+  diag_factor_body<T>(p, blockIdx.x, blockIdx.y);
+}
+
+// Several layers in one launch: job q owns blocks [block_start[q], block_start[q+1]),
+// laid out split-major over its column blocks, with its own partials and tickets.
+constexpr int kMaxK5Group = 64;
+struct DiagFactorGroup {
+  DiagFactorParams job[kMaxK5Group];
+  int block_start[kMaxK5Group + 1];
+  int count;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kK5Threads)
+diag_factor_grouped_kernel(const __grid_constant__ DiagFactorGroup g) {
+  int q = 0;
+  while (q + 1 < g.count && (int)blockIdx.x >= g.block_start[q + 1]) ++q;
+  const DiagFactorParams J = g.job[q];
+  const int lb = (int)blockIdx.x - g.block_start[q];
+  diag_factor_body<T>(J, lb % J.col_blocks, lb / J.col_blocks);
+}
+
 }  // namespace
 
 size_t k5_scratch_floats(int n_plus_o, int64_t max_rows) {
   return (size_t)k5_splits(n_plus_o, max_rows) * (size_t)n_plus_o;
 }
 
-kfac_status launch_diag_factors(kfac_ctx* h, int layer, const void* a, int64_t lda,
-                                const void* g, int64_t ldg, int64_t rows, double scale,
-                                float* g_new, float* a_new, cudaStream_t st) {
-  const LayerInfo& L = h->layers[layer];
+namespace {
+
+DiagFactorParams k5_params(const LayerInfo& L, const void* a, int64_t lda, const void* g,
+                           int64_t ldg, int64_t rows, double scale, float* g_new, float* a_new,
+                           int64_t splits, float* part, int* tickets) {
   DiagFactorParams p{};
   p.a = a;
   p.g = g;
   p.lda = lda;
   p.ldg = ldg;
   p.rows = rows;
-  const int64_t sp = k5_splits(L.d_in + L.o, rows);
-  p.rows_per_split = cdiv(rows, sp);
+  p.rows_per_split = cdiv(rows, splits);
   p.splits = (int)cdiv(rows, p.rows_per_split);
   p.d_in = L.d_in;
   p.o = L.o;
   p.has_bias = L.has_bias;
   p.col_blocks = (int)cdiv(L.d_in + L.o, kK5Threads);
   p.s = (float)(scale > 0 ? scale : 1.0 / (double)rows);
-  p.part = h->at<float>(h->off_k5part);
-  p.tickets = h->at<int>(h->off_k5tickets);
+  p.part = part;
+  p.tickets = tickets;
   p.g_new = g_new;
   p.a_new = a_new;
-  if ((size_t)p.splits * (L.d_in + L.o) > h->k5part_floats) return KFAC_ERR_WORKSPACE;
-  dim3 grid(p.col_blocks, p.splits);
-  if (L.in_dtype == KFAC_BF16)
-    diag_factor_kernel<__nv_bfloat16><<<grid, kK5Threads, 0, st>>>(p);
-  else
-    diag_factor_kernel<float><<<grid, kK5Threads, 0, st>>>(p);
-  count_launch();
-  return check_launch();
+  return p;
 }
 
-kfac_status launch_diag_step(kfac_ctx* h, int layer, float decay, const float* g_new,
-                             const float* a_new, const float* gw, const float* gb, float* pw,
-                             float* pb, float* ow, float* ob, cudaStream_t st) {
-  const LayerInfo& L = h->layers[layer];
+DiagParams k6_params(kfac_ctx* h, const LayerInfo& L, float decay, const float* g_new,
+                     const float* a_new, const float* gw, const float* gb, float* pw, float* pb,
+                     float* ow, float* ob, bool* vec) {
   DiagParams p{};
   p.o = L.o;
   p.d_in = L.d_in;
@@ -251,18 +326,145 @@ kfac_status launch_diag_step(kfac_ctx* h, int layer, float decay, const float* g
   p.as = h->at<float>(L.as);
   p.ticket = h->at<int>(L.ticket);
   auto al16 = [](const void* q) { return ((uintptr_t)q & 15) == 0; };
-  const bool vec = (L.d_in % 4 == 0) && al16(gw) && al16(pw) && al16(p.mw) && al16(p.as) &&
-                   al16(a_new) && (ow == nullptr || al16(ow));
+  *vec = (L.d_in % 4 == 0) && al16(gw) && al16(pw) && al16(p.mw) && al16(p.as) && al16(a_new) &&
+         (ow == nullptr || al16(ow));
+  return p;
+}
+
+int64_t k6_units(const LayerInfo& L, bool vec) {
   const int64_t nw = (int64_t)L.o * L.d_in;
-  const int64_t units = (vec ? nw / 4 : nw) + (L.has_bias ? L.o : 0);
-  int64_t blocks = std::min<int64_t>(cdiv(units, kDiagThreads), (int64_t)kNumSMs);
-  blocks = std::max<int64_t>(blocks, 1);
-  if (vec)
-    diag_step_kernel<true><<<(unsigned)blocks, kDiagThreads, 0, st>>>(p);
+  return (vec ? nw / 4 : nw) + (L.has_bias ? L.o : 0);
+}
+
+unsigned k6_blocks(int64_t units) {
+  return (unsigned)std::max<int64_t>(std::min<int64_t>(cdiv(units, kDiagThreads), kNumSMs), 1);
+}
+
+}  // namespace
+
+kfac_status launch_diag_factors(kfac_ctx* h, int layer, const void* a, int64_t lda,
+                                const void* g, int64_t ldg, int64_t rows, double scale,
+                                float* g_new, float* a_new, cudaStream_t st) {
+  const LayerInfo& L = h->layers[layer];
+  DiagFactorParams p = k5_params(L, a, lda, g, ldg, rows, scale, g_new, a_new,
+                                 k5_splits(L.d_in + L.o, rows), h->at<float>(h->off_k5part),
+                                 h->at<int>(h->off_k5tickets));
+  if ((size_t)p.splits * (L.d_in + L.o) > h->k5part_floats) return KFAC_ERR_WORKSPACE;
+  dim3 grid(p.col_blocks, p.splits);
+  if (L.in_dtype == KFAC_BF16)
+    diag_factor_kernel<__nv_bfloat16><<<grid, kK5Threads, 0, st>>>(p);
   else
-    diag_step_kernel<false><<<(unsigned)blocks, kDiagThreads, 0, st>>>(p);
+    diag_factor_kernel<float><<<grid, kK5Threads, 0, st>>>(p);
   count_launch();
   return check_launch();
+}
+
+// Several layers (one input dtype) per launch.  Row splits are shared out so the
+// whole group covers the GPU about twice; each job gets its own partials and
+// tickets; a group is cut where the scratch or the job table is full.
+kfac_status launch_diag_factors_batched(kfac_ctx* h, int count, const int* layers,
+                                        const void* const* a, const int64_t* lda,
+                                        const void* const* g, const int64_t* ldg,
+                                        const int64_t* rows, double scale,
+                                        float* const* g_new, float* const* a_new,
+                                        cudaStream_t st) {
+  double work = 0;
+  for (int i = 0; i < count; ++i) {
+    const LayerInfo& L = h->layers[layers[i]];
+    work += (double)rows[i] * (L.d_in + L.o);
+  }
+  const bool bf16 = h->layers[layers[0]].in_dtype == KFAC_BF16;
+  DiagFactorGroup grp;
+  std::memset(&grp, 0, sizeof(grp));
+  size_t used_part = 0, used_tickets = 0;
+  int blocks = 0;
+  auto flush = [&]() -> kfac_status {
+    if (grp.count == 0) return KFAC_OK;
+    grp.block_start[grp.count] = blocks;
+    if (bf16)
+      diag_factor_grouped_kernel<__nv_bfloat16><<<blocks, kK5Threads, 0, st>>>(grp);
+    else
+      diag_factor_grouped_kernel<float><<<blocks, kK5Threads, 0, st>>>(grp);
+    count_launch();
+    grp.count = 0;
+    blocks = 0;
+    used_part = used_tickets = 0;
+    return check_launch();
+  };
+  for (int i = 0; i < count; ++i) {
+    const LayerInfo& L = h->layers[layers[i]];
+    const int ncols = L.d_in + L.o;
+    const int64_t cb = cdiv(ncols, kK5Threads);
+    const double share = (double)rows[i] * ncols / work;   // of 2 x SMs CTAs
+    int64_t splits = (int64_t)std::ceil(2.0 * kNumSMs * share / (double)cb);
+    splits = std::max<int64_t>(1, std::min<int64_t>(splits, cdiv(rows[i], kK5MinRows)));
+    const size_t need = (size_t)splits * ncols;
+    if (need > h->k5part_floats || (size_t)cb > h->k5tickets_ints) return KFAC_ERR_WORKSPACE;
+    if (grp.count == kMaxK5Group || used_part + need > h->k5part_floats ||
+        used_tickets + cb > h->k5tickets_ints)
+      if (kfac_status e = flush()) return e;
+    DiagFactorParams p = k5_params(L, a[i], lda[i], g[i], ldg[i], rows[i], scale, g_new[i],
+                                   a_new[i], splits, h->at<float>(h->off_k5part) + used_part,
+                                   h->at<int>(h->off_k5tickets) + used_tickets);
+    grp.job[grp.count] = p;
+    grp.block_start[grp.count] = blocks;
+    blocks += p.col_blocks * p.splits;
+    ++grp.count;
+    used_part += (size_t)p.splits * ncols;
+    used_tickets += (size_t)p.col_blocks;
+  }
+  return flush();
+}
+
+kfac_status launch_diag_step(kfac_ctx* h, int layer, float decay, const float* g_new,
+                             const float* a_new, const float* gw, const float* gb, float* pw,
+                             float* pb, float* ow, float* ob, cudaStream_t st) {
+  const LayerInfo& L = h->layers[layer];
+  bool vec = false;
+  DiagParams p = k6_params(h, L, decay, g_new, a_new, gw, gb, pw, pb, ow, ob, &vec);
+  const unsigned blocks = k6_blocks(k6_units(L, vec));
+  if (vec)
+    diag_step_kernel<true><<<blocks, kDiagThreads, 0, st>>>(p);
+  else
+    diag_step_kernel<false><<<blocks, kDiagThreads, 0, st>>>(p);
+  count_launch();
+  return check_launch();
+}
+
+// Several DIAG layers per launch (up to 64 per group); the ticket of the group's
+// first layer orders the EMA write-back.
+kfac_status launch_diag_step_batched(kfac_ctx* h, int count, const int* layers,
+                                     const float* decay, const float* const* g_new,
+                                     const float* const* a_new, const float* const* gw,
+                                     const float* const* gb, float* const* pw,
+                                     float* const* pb, float* const* ow, float* const* ob,
+                                     cudaStream_t st) {
+  DiagGroup grp;
+  std::memset(&grp, 0, sizeof(grp));
+  int64_t units = 0;
+  auto flush = [&]() -> kfac_status {
+    if (grp.count == 0) return KFAC_OK;
+    grp.start[grp.count] = units;
+    diag_step_grouped_kernel<<<k6_blocks(units), kDiagThreads, 0, st>>>(grp);
+    count_launch();
+    grp.count = 0;
+    units = 0;
+    return check_launch();
+  };
+  for (int i = 0; i < count; ++i) {
+    if (grp.count == kMaxDiagGroup)
+      if (kfac_status e = flush()) return e;
+    const LayerInfo& L = h->layers[layers[i]];
+    bool vec = false;
+    grp.job[grp.count] = k6_params(h, L, decay[i], g_new[i], a_new[i], gw[i], gb[i], pw[i],
+                                   pb[i], ow[i], ob[i], &vec);
+    if (grp.count == 0) grp.ticket = grp.job[0].ticket;
+    grp.vec[grp.count] = vec;
+    grp.start[grp.count] = units;
+    units += k6_units(L, vec);
+    ++grp.count;
+  }
+  return flush();
 }
 
 }  // namespace kfac

@@ -39,7 +39,7 @@ bool valid_desc(const kfac_layer_desc& d) {
 struct Plan {
   std::vector<LayerInfo> layers;
   size_t off_status, off_part, part_floats, off_tickets, n_tickets, off_k4tmp, k4tmp_floats;
-  size_t off_k5part, k5part_floats, off_k5tickets, off_invjobs, total;
+  size_t off_k5part, k5part_floats, off_k5tickets, k5tickets_ints, off_invjobs, total;
   size_t off_tcpack, tcpack_bytes;
   int n_invjobs, max_kron_n;
 };
@@ -104,7 +104,7 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
       L.ticket = take(sizeof(int));
     }
     k5 = std::max(k5, k5_scratch_floats(L.d_in + L.o, max_rows));
-    k5t = std::max(k5t, (size_t)cdiv(L.d_in + L.o, 256));
+    k5t += (size_t)cdiv(L.d_in + L.o, 256);   // batched K5: every layer's column blocks
     P->layers.push_back(L);
   }
   // batched calls pack a group of layers at once, within a fixed budget
@@ -118,9 +118,12 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
   P->off_tcpack = take(tcpack);
   P->k4tmp_floats = k4;
   P->off_k4tmp = take(k4 * sizeof(float));
+  // batched K5 spreads about 2 x SMs CTAs over the group, one part row per CTA
+  k5 = std::max(k5, (size_t)256 * (2 * kNumSMs + k5t));
   P->k5part_floats = k5;
   P->off_k5part = take(k5 * sizeof(float));
   P->off_k5tickets = take(k5t * sizeof(int));
+  P->k5tickets_ints = k5t;
   P->off_invjobs = off;
   take(align_up(sizeof(InvJob) * ninv) + sizeof(SyrkJob) * ninv);
   P->n_invjobs = ninv;
@@ -222,6 +225,7 @@ kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_
   h->off_k5part = P.off_k5part;
   h->k5part_floats = P.k5part_floats;
   h->off_k5tickets = P.off_k5tickets;
+  h->k5tickets_ints = P.k5tickets_ints;
   h->off_invjobs = P.off_invjobs;
   h->n_invjobs = P.n_invjobs;
   h->max_kron_n = P.max_kron_n;
@@ -341,6 +345,29 @@ kfac_status kfac_diag_factors(kfac_handle h, int layer, const void* a, int64_t l
   return launch_diag_factors(h, layer, a, lda, g, ldg, rows, scale, g_new, a_new, stream);
 }
 
+kfac_status kfac_diag_factors_batched(kfac_handle h, int count, const int* layers,
+                                      const void* const* a, const int64_t* lda,
+                                      const void* const* g, const int64_t* ldg,
+                                      const int64_t* rows, double scale, float* const* g_new,
+                                      float* const* a_new, cudaStream_t stream) {
+  if (!h || count < 1 || !layers || !a || !lda || !g || !ldg || !rows || !g_new || !a_new ||
+      !std::isfinite(scale))
+    return KFAC_ERR_INVALID_ARG;
+  std::vector<char> seen(h->layers.size(), 0);
+  for (int i = 0; i < count; ++i) {
+    if (kfac_status e = check_layer(h, layers[i], -1)) return e;
+    if (seen[layers[i]]++) return KFAC_ERR_INVALID_ARG;
+    const LayerInfo& L = h->layers[layers[i]];
+    if (L.in_dtype != h->layers[layers[0]].in_dtype) return KFAC_ERR_INVALID_ARG;
+    if (kfac_status e = check_inputs(h, L, a[i], lda[i], g[i], ldg[i], rows[i])) return e;
+    if (!g_new[i] || !a_new[i] || !aligned(g_new[i], 4) || !aligned(a_new[i], 4))
+      return KFAC_ERR_INVALID_ARG;
+  }
+  if (kfac_status e = ensure_device(h)) return e;
+  return launch_diag_factors_batched(h, count, layers, a, lda, g, ldg, rows, scale, g_new, a_new,
+                                     stream);
+}
+
 kfac_status kfac_invert(kfac_handle h, int layer, cudaStream_t stream) {
   if (!h) return KFAC_ERR_INVALID_ARG;
   if (layer != -1 && check_layer(h, layer, KFAC_KRON) != KFAC_OK) return KFAC_ERR_INVALID_ARG;
@@ -423,6 +450,48 @@ kfac_status kfac_diag_step(kfac_handle h, int layer, const float* g_new, const f
                                    L.has_bias ? param_b : nullptr, out_w,
                                    L.has_bias ? out_b : nullptr, stream);
   if (e == KFAC_OK) ++L.t_diag;
+  return e;
+}
+
+kfac_status kfac_diag_step_batched(kfac_handle h, int count, const int* layers,
+                                   const float* const* g_new, const float* const* a_new,
+                                   const float* const* grad_w, const float* const* grad_b,
+                                   float* const* param_w, float* const* param_b,
+                                   float* const* out_w, float* const* out_b,
+                                   cudaStream_t stream) {
+  if (!h || count < 1 || !layers || !g_new || !a_new || !grad_w || !param_w)
+    return KFAC_ERR_INVALID_ARG;
+  std::vector<char> seen(h->layers.size(), 0);
+  std::vector<const float*> gb(count, nullptr);
+  std::vector<float*> pb(count, nullptr), ow(count, nullptr), ob(count, nullptr);
+  std::vector<float> decay(count);
+  for (int i = 0; i < count; ++i) {
+    if (kfac_status e = check_layer(h, layers[i], KFAC_DIAG)) return e;
+    if (seen[layers[i]]++) return KFAC_ERR_INVALID_ARG;
+    const LayerInfo& L = h->layers[layers[i]];
+    const float* b_g = grad_b ? grad_b[i] : nullptr;
+    float* b_p = param_b ? param_b[i] : nullptr;
+    float* w_o = out_w ? out_w[i] : nullptr;
+    float* b_o = out_b ? out_b[i] : nullptr;
+    if (!g_new[i] || !a_new[i] || !grad_w[i] || !param_w[i]) return KFAC_ERR_INVALID_ARG;
+    if (L.has_bias && (!b_g || !b_p)) return KFAC_ERR_INVALID_ARG;
+    if (L.has_bias && w_o && !b_o) return KFAC_ERR_INVALID_ARG;
+    for (const void* p : {(const void*)g_new[i], (const void*)a_new[i], (const void*)grad_w[i],
+                          (const void*)param_w[i]})
+      if (!aligned(p, 4)) return KFAC_ERR_INVALID_ARG;
+    gb[i] = L.has_bias ? b_g : nullptr;
+    pb[i] = L.has_bias ? b_p : nullptr;
+    ow[i] = w_o;
+    ob[i] = L.has_bias ? b_o : nullptr;
+    const bool first = L.t_diag == 0 && h->hp.ema_init == KFAC_EMA_INIT_FIRST;
+    decay[i] = first ? 0.f : (float)h->hp.ema_decay;
+  }
+  if (kfac_status e = ensure_device(h)) return e;
+  kfac_status e = launch_diag_step_batched(h, count, layers, decay.data(), g_new, a_new, grad_w,
+                                           gb.data(), param_w, pb.data(), ow.data(), ob.data(),
+                                           stream);
+  if (e == KFAC_OK)
+    for (int i = 0; i < count; ++i) ++h->layers[layers[i]].t_diag;
   return e;
 }
 

@@ -82,7 +82,7 @@ struct kfac_ctx {
   size_t off_k4tmp = 0, k4tmp_floats = 0;
   // K5 row-split partials and tickets
   size_t off_k5part = 0, k5part_floats = 0;
-  size_t off_k5tickets = 0;
+  size_t off_k5tickets = 0, k5tickets_ints = 0;
   // inversion job table (all KRON factors, sorted by n descending)
   size_t off_invjobs = 0;
   int n_invjobs = 0;
@@ -110,6 +110,17 @@ kfac_status launch_diag_factors(kfac_ctx* h, int layer, const void* a, int64_t l
 kfac_status launch_diag_step(kfac_ctx* h, int layer, float decay, const float* g_new,
                              const float* a_new, const float* gw, const float* gb, float* pw,
                              float* pb, float* ow, float* ob, cudaStream_t s);
+kfac_status launch_diag_factors_batched(kfac_ctx* h, int count, const int* layers,
+                                        const void* const* a, const int64_t* lda,
+                                        const void* const* g, const int64_t* ldg,
+                                        const int64_t* rows, double scale,
+                                        float* const* g_new, float* const* a_new, cudaStream_t s);
+kfac_status launch_diag_step_batched(kfac_ctx* h, int count, const int* layers,
+                                     const float* decay, const float* const* g_new,
+                                     const float* const* a_new, const float* const* gw,
+                                     const float* const* gb, float* const* pw,
+                                     float* const* pb, float* const* ow, float* const* ob,
+                                     cudaStream_t s);
 kfac_status launch_update_factors_batched(kfac_ctx* h, int count, const int* layers,
                                           const void* const* a, const int64_t* lda,
                                           const void* const* g, const int64_t* ldg,

@@ -416,3 +416,98 @@ def test_batched_calls_reject_duplicates_and_mixed_dtypes():
         h.update_factors_batched([0, 0], [a, a], [a, a])
     with pytest.raises(K.KfacError):
         h.update_factors_batched([0, 1], [a, a.bfloat16()], [a, a.bfloat16()])
+
+
+def _diag_mix(n_layers, seed):
+    """Mixed shapes: d_in multiple of 4 or not (vector and scalar paths), with and without
+    bias, BatchNorm-like (d_in = 1), and a few large ones."""
+    rng = np.random.default_rng(seed)
+    shapes = [(1024, 1024, 1), (1, 256, 1), (1, 64, 1), (96, 50, 0), (1000, 7, 1)]
+    while len(shapes) < n_layers:
+        d = int(rng.integers(1, 200))
+        shapes.append((d, int(rng.integers(1, 120)), int(rng.integers(0, 2))))
+    return shapes
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_diag_factors_batched_matches_single_calls(dtype):
+    """70 layers (two launches of at most 64): against the single call and the oracle."""
+    kd = K.KFAC_BF16 if dtype == "bf16" else K.KFAC_F32
+    shapes = _diag_mix(70, 5)
+    descs = [(K.KFAC_DIAG if i % 3 else K.KFAC_KRON, o, d, b, kd) for i, (d, o, b) in enumerate(shapes)]
+    M = 600
+    h = K.Kfac(descs, max_rows=M, **HP)
+    ins = [_inputs(M, d, o, act="normal", dtype=dtype) for (d, o, b) in shapes]
+    a_l = [_dev_in(a, dtype) for a, _ in ins]
+    g_l = [_dev_in(g, dtype) for _, g in ins]
+    gn_b = [torch.empty(o, device="cuda") for (d, o, b) in shapes]
+    an_b = [torch.empty(d + b, device="cuda") for (d, o, b) in shapes]
+    h.diag_factors_batched(list(range(len(shapes))), a_l, g_l, gn_b, an_b)
+    for li, (d, o, b) in enumerate(shapes):
+        gn = torch.empty(o, device="cuda")
+        an = torch.empty(d + b, device="cuda")
+        h.diag_factors(li, a_l[li], g_l[li], gn, an)
+        a, g = ins[li]
+        assert max_rel_elem(to_np(gn_b[li]), to_np(gn), 0) <= 1e-6, li
+        assert max_rel_elem(to_np(an_b[li]), to_np(an), 0) <= 1e-6, li
+        assert max_rel_elem(to_np(gn_b[li]), O.diag_factor(g, 0), 0) <= 1e-5, li
+        assert max_rel_elem(to_np(an_b[li]), O.diag_factor(a, b), 0) <= 1e-5, li
+    assert h.get_status()[0] == 0
+
+
+def test_diag_step_batched_bitwise_equals_single_calls():
+    """70 DIAG layers, three steps: every output, parameter, momentum and EMA vector of the
+    batched launch equals the per-layer launch bit for bit (same arithmetic per element);
+    one layer is also followed against the oracle's step formulas."""
+    shapes = _diag_mix(70, 6)
+    descs = [(K.KFAC_DIAG, o, d, b, K.KFAC_F32) for (d, o, b) in shapes]
+    hb = K.Kfac(descs, max_rows=1, **HP)
+    hs = K.Kfac(descs, max_rows=1, **HP)
+    L = list(range(len(shapes)))
+    w0 = [(RNG.standard_normal((o, d)) * 0.1).astype(np.float32) for (d, o, b) in shapes]
+    b0 = [(RNG.standard_normal(o) * 0.1).astype(np.float32) if b else None for (d, o, b) in shapes]
+    pw_b, pw_s = [to_dev(w) for w in w0], [to_dev(w) for w in w0]
+    pb_b = [to_dev(x) if x is not None else None for x in b0]
+    pb_s = [to_dev(x) if x is not None else None for x in b0]
+    probe = 0   # the 1024 x 1024 layer
+    d0, o0, bb0 = shapes[probe]
+    traj = O.LayerState("diag", o0, d0, bb0, w0[probe].astype(np.float64),
+                        b0[probe].astype(np.float64))
+    orc = _orc()
+    for t in range(3):
+        gn = [to_dev(RNG.uniform(0, 2e-6, o).astype(np.float32)) for (d, o, b) in shapes]
+        an = [to_dev(RNG.uniform(0, 2, d + b).astype(np.float32)) for (d, o, b) in shapes]
+        gw = [to_dev((RNG.standard_normal((o, d)) * 1e-3).astype(np.float32)) for (d, o, b) in shapes]
+        gb = [to_dev((RNG.standard_normal(o) * 1e-3).astype(np.float32)) if b else None
+              for (d, o, b) in shapes]
+        ow_b = [torch.empty(o, d, device="cuda") for (d, o, b) in shapes]
+        ob_b = [torch.empty(o, device="cuda") if b else None for (d, o, b) in shapes]
+        hb.diag_step_batched(L, gn, an, gw, gb, pw_b, pb_b, ow_b, ob_b)
+        for li, (d, o, b) in enumerate(shapes):
+            ow = torch.empty(o, d, device="cuda")
+            ob = torch.empty(o, device="cuda") if b else None
+            hs.diag_step(li, gn[li], an[li], gw[li], gb[li], pw_s[li], pb_s[li], ow, ob)
+            assert torch.equal(ow_b[li], ow) and torch.equal(pw_b[li], pw_s[li]), (t, li)
+            if b:
+                assert torch.equal(ob_b[li], ob) and torch.equal(pb_b[li], pb_s[li]), (t, li)
+            for which in (K.KFAC_STATE_MOMENTUM, K.KFAC_STATE_GDIAG, K.KFAC_STATE_ADIAG):
+                assert torch.equal(hb.state(li, which), hs.state(li, which)), (t, li, which)
+        orc.step_diag(traj, to_np(gn[probe]), to_np(an[probe]), to_np(gw[probe]),
+                      to_np(gb[probe]))
+    got = O.grad_hat(to_np(pw_b[probe]), to_np(pb_b[probe]))
+    assert rel_fro(got, traj.W) <= 1e-6
+    assert hb.get_status()[0] == 0
+
+
+def test_batched_diag_calls_reject_duplicates_and_wrong_kinds():
+    h = K.Kfac([(K.KFAC_DIAG, 8, 8, 1, K.KFAC_F32), (K.KFAC_KRON, 8, 8, 1, K.KFAC_F32)],
+               max_rows=16, **HP)
+    a = torch.zeros(16, 8, device="cuda")
+    v8, v9 = torch.zeros(8, device="cuda"), torch.zeros(9, device="cuda")
+    w = torch.zeros(8, 8, device="cuda")
+    with pytest.raises(K.KfacError):
+        h.diag_factors_batched([0, 0], [a, a], [a, a], [v8, v8], [v9, v9])
+    with pytest.raises(K.KfacError):   # K6 is for DIAG layers only
+        h.diag_step_batched([0, 1], [v8, v8], [v9, v9], [w, w], [v8, v8], [w, w], [v8, v8])
+    with pytest.raises(K.KfacError):
+        h.diag_step_batched([0, 0], [v8, v8], [v9, v9], [w, w], [v8, v8], [w, w], [v8, v8])
