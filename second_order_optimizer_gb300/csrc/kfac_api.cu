@@ -93,7 +93,7 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
       if (L.n >= kTcInverseMinN) tcpack = std::max(tcpack, tc_pack_bytes(L.n, L.n, false));
       if (L.o >= kTcInverseMinN) tcpack = std::max(tcpack, tc_pack_bytes(L.o, L.o, false));
       pack_sum += align_up(tc_pack_bytes(L.n, max_rows, bf)) + align_up(tc_pack_bytes(L.o, max_rows, bf));
-      tickets = std::max({tickets, t1, t2, (size_t)kNumSMs});
+      tickets = std::max({tickets, t1, t2, (size_t)16 * kNumSMs});   // split-K: tile x cluster rank
       k4 = std::max(k4, 2 * o * np + 2 * n * op);
       k4_sum += align_up((2 * o * np + 2 * n * op) * sizeof(float)) / sizeof(float);
       ninv += 2;

@@ -81,12 +81,12 @@ struct GemmTcParams {
   int upper;             // upper: only tiles reaching the upper triangle (SYRK, M == N)
   int tiles_m;           // tile rows (128 each)
   int same_ab;           // A and B are the same operand (diagonal tiles load once)
-  int splits;
-  int cluster_reduce;    // splits form one thread-block cluster, reduced through DSMEM
+  int splits;            // k-splits per tile = csize x groups
+  int csize;             // splits per thread-block cluster, reduced through DSMEM (1: none)
   int64_t k_per_split;   // multiple of ksub
   int ksub;              // k elements per TMEM drain (multiple of BK)
-  float* part;
-  int* tickets;
+  float* part;           // this product's cluster partials [tile][groups][BM][BN]
+  int* tickets;          // this product's tickets [tile][csize]
   DevStatus* status;
   int layer;
   TcEpilogue e;
@@ -113,13 +113,11 @@ __device__ __forceinline__ void upper_tile(int t, int tiles_m, int R, int* ti, i
   *tj = j;
 }
 
-// One output tile (and one k-split of it).  `ticket_tile` indexes the split-K
-// partial buffer and tickets (unique across the launch).
+// One output tile (and one k-split of it).
 template <bool kBF16, int BN, int EPI>
 __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUtensorMap* map_a_lo,
                                           const CUtensorMap* map_b_hi, const CUtensorMap* map_b_lo,
-                                          const GemmTcParams& p, const int tile, const int split,
-                                          const int ticket_tile) {
+                                          const GemmTcParams& p, const int tile, const int split) {
   using C = TcCfg<kBF16, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -426,87 +424,98 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
     return;
   }
 
-  // Split-K reduction loops run in batches of U elements per thread: all loads of a
-  // batch are issued before any store, so load latency overlaps instead of
-  // serialising behind possibly-aliasing stores.
+  // Split-K: the tile's splits = csize x groups.  The csize splits of a cluster
+  // sum their staged tiles through distributed shared memory, member c keeping
+  // rows [row_lo, row_hi); with groups > 1 each member then writes its rows as a
+  // cluster partial, and the last of the groups to arrive (a ticket per row
+  // slice) sums the partials in group order and finishes those rows.  Fixed
+  // order throughout, so results are deterministic.
+  // Reduction loops run in batches of U elements per thread: all loads of a
+  // batch are issued before any store.
   constexpr int NT = C::BM * C::BN;
   constexpr int U = 8;
   int row_lo = 0, row_hi = C::BM;   // rows of the tile this CTA finishes
-  if (p.cluster_reduce) {
-    // Split-K through distributed shared memory: the splits of this tile are the
-    // CTAs of one cluster; CTA `split` sums rows [row_lo, row_hi) of every
-    // member's staged tile, in member order, and finishes those rows.  Every
-    // member takes both cluster barriers, whatever happened before.
-    namespace cg = cooperative_groups;
-    cg::cluster_group cl = cg::this_cluster();
-    cl.sync();
-    const int S = p.splits;
-    const int rb = (C::BM + S - 1) / S;
-    row_lo = min(C::BM, split * rb);
-    row_hi = min(C::BM, row_lo + rb);
-    if (!*abort_flag) {
-      const float* src[8];
-      for (int q = 0; q < S; ++q) src[q] = cl.map_shared_rank(T, q);
-      const int n_el = (row_hi - row_lo) * C::BN;
+  if (p.splits > 1) {
+    const int CS = p.csize, G = p.splits / p.csize;
+    int c = 0;
+    if (CS > 1) {
+      // Every member takes both cluster barriers, whatever happened before.
+      namespace cg = cooperative_groups;
+      cg::cluster_group cl = cg::this_cluster();
+      cl.sync();
+      c = (int)cl.block_rank();
+      const int rb = (C::BM + CS - 1) / CS;
+      row_lo = min(C::BM, c * rb);
+      row_hi = min(C::BM, row_lo + rb);
+      if (!*abort_flag) {
+        const float* src[8];
+        for (int q = 0; q < CS; ++q) src[q] = cl.map_shared_rank(T, q);
+        const int n_el = (row_hi - row_lo) * C::BN;
+        for (int b0 = threadIdx.x; b0 < n_el; b0 += nth * U) {
+          float acc[U];
+          int idx[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int e = b0 + u * nth;
+            idx[u] = e < n_el ? (row_lo + e / C::BN) * C::TPAD + e % C::BN : 0;
+            acc[u] = 0.f;
+          }
+          for (int q = 0; q < CS; ++q) {
+            float v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) v[u] = src[q][idx[u]];
+#pragma unroll
+            for (int u = 0; u < U; ++u) acc[u] += v[u];
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+            if (b0 + u * nth < n_el) T[idx[u]] = acc[u];
+        }
+      }
+      cl.sync();  // no member reads a peer's tile after this point
+    }
+    // An aborted CTA still takes its ticket, so the count stays consistent for
+    // later launches (the result is already flagged as an error).
+    const bool aborted = *abort_flag;
+    if (G > 1) {
+      const int gi = split / CS;
+      const int n_el = (row_hi - row_lo) * C::BN, e0 = row_lo * C::BN;
+      float* part = p.part + (size_t)tile * G * NT;
+      for (int e = threadIdx.x; e < n_el; e += nth)
+        part[(size_t)gi * NT + e0 + e] = T[(row_lo + e / C::BN) * C::TPAD + e % C::BN];
+      __threadfence();
+      __syncthreads();
+      int* ticket = p.tickets + tile * CS + c;
+      if (threadIdx.x == 0) *s_last = (atomicAdd(ticket, 1) == G - 1);
+      __syncthreads();
+      if (!*s_last) return;
+      __threadfence();
       for (int b0 = threadIdx.x; b0 < n_el; b0 += nth * U) {
         float acc[U];
-        int idx[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int e = b0 + u * nth;
-          idx[u] = e < n_el ? (row_lo + e / C::BN) * C::TPAD + e % C::BN : 0;
-          acc[u] = 0.f;
+          acc[u] = e < n_el ? __ldcg(part + e0 + e) : 0.f;
         }
-        for (int q = 0; q < S; ++q) {
+        for (int q = 1; q < G; ++q) {
           float v[U];
 #pragma unroll
-          for (int u = 0; u < U; ++u) v[u] = src[q][idx[u]];
+          for (int u = 0; u < U; ++u) {
+            const int e = b0 + u * nth;
+            v[u] = e < n_el ? __ldcg(part + (size_t)q * NT + e0 + e) : 0.f;
+          }
 #pragma unroll
           for (int u = 0; u < U; ++u) acc[u] += v[u];
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (b0 + u * nth < n_el) T[idx[u]] = acc[u];
-      }
-    }
-    cl.sync();  // no member reads a peer's tile after this point
-    if (*abort_flag) return;
-  } else if (p.splits > 1) {
-    if (*abort_flag) return;
-    float* part = p.part + (size_t)ticket_tile * p.splits * NT;
-    for (int e = threadIdx.x; e < NT; e += nth)
-      part[(size_t)split * NT + e] = T[(e / C::BN) * C::TPAD + e % C::BN];
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) *s_last = (atomicAdd(&p.tickets[ticket_tile], 1) == p.splits - 1);
-    __syncthreads();
-    if (!*s_last) return;
-    __threadfence();
-    for (int b0 = threadIdx.x; b0 < NT; b0 += nth * U) {
-      float acc[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int e = b0 + u * nth;
-        acc[u] = e < NT ? __ldcg(part + e) : 0.f;
-      }
-      for (int s = 1; s < p.splits; ++s) {
-        float v[U];
-#pragma unroll
         for (int u = 0; u < U; ++u) {
           const int e = b0 + u * nth;
-          v[u] = e < NT ? __ldcg(part + (size_t)s * NT + e) : 0.f;
+          if (e < n_el) T[(row_lo + e / C::BN) * C::TPAD + e % C::BN] = acc[u];
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) acc[u] += v[u];
       }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int e = b0 + u * nth;
-        if (e < NT) T[(e / C::BN) * C::TPAD + e % C::BN] = acc[u];
-      }
+      if (threadIdx.x == 0) *ticket = 0;
     }
-    if (threadIdx.x == 0) p.tickets[ticket_tile] = 0;
-    __syncthreads();
+    if (aborted) return;
   } else if (*abort_flag) {
     return;
   }
@@ -624,29 +633,29 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a_hi,
                const __grid_constant__ CUtensorMap map_b_hi,
                const __grid_constant__ CUtensorMap map_b_lo, const __grid_constant__ GemmTcParams p) {
   const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
-  gemm_body<kBF16, BN, EPI>(&map_a_hi, &map_a_lo, &map_b_hi, &map_b_lo, p, tile, split, tile);
+  gemm_body<kBF16, BN, EPI>(&map_a_hi, &map_a_lo, &map_b_hi, &map_b_lo, p, tile, split);
 }
 
 // Several independent products in one launch (128 x 128 tiles): blocks are laid
-// out problem by problem, `splits` consecutive blocks per tile (one cluster when
-// the split-K is reduced through DSMEM).
+// out problem by problem, each problem's `splits` consecutive blocks per tile
+// (csize of them form one cluster; csize is the same for the whole launch).
 constexpr int kMaxGroup = 16;
 struct GroupedTc {
   CUtensorMap maps[4 * kMaxGroup];  // per problem: A hi, A lo, B hi, B lo
   GemmTcParams prob[kMaxGroup];
-  int tile_start[kMaxGroup + 1];
+  int block_start[kMaxGroup + 1];
   int count;
-  int splits;
+  int csize;
 };
 
 template <bool kBF16, int EPI>
 __global__ void __launch_bounds__(TcCfg<kBF16, 128>::THREADS, 1)
 gemm_tc_grouped_kernel(const __grid_constant__ GroupedTc g) {
-  const int gt = blockIdx.x / g.splits, split = blockIdx.x % g.splits;
   int q = 0;
-  while (q + 1 < g.count && gt >= g.tile_start[q + 1]) ++q;
+  while (q + 1 < g.count && (int)blockIdx.x >= g.block_start[q + 1]) ++q;
+  const int local = (int)blockIdx.x - g.block_start[q], sp = g.prob[q].splits;
   gemm_body<kBF16, 128, EPI>(&g.maps[4 * q], &g.maps[4 * q + 1], &g.maps[4 * q + 2],
-                             &g.maps[4 * q + 3], g.prob[q], gt - g.tile_start[q], split, gt);
+                             &g.maps[4 * q + 3], g.prob[q], local / sp, local % sp);
 }
 
 // ------------------------------------------------------------------- pack
@@ -689,18 +698,24 @@ __global__ void __launch_bounds__(256) pack_kernel(const T* __restrict__ x, int6
                        blockIdx.y * 32);
 }
 
+// Job q owns blocks [block_start[q], block_start[q+1]): its 32 x 32 tiles,
+// row tiles fastest (a grid sized by the largest job in each dimension would
+// schedule mostly empty blocks when the jobs differ in size).
 struct PackGroup {
   PackJob job[kMaxPackJobs];
+  int64_t block_start[kMaxPackJobs + 1];
   int count;
 };
 
 template <typename T, bool kSplit>
 __global__ void __launch_bounds__(256) pack_grouped_kernel(const __grid_constant__ PackGroup g) {
-  const PackJob J = g.job[blockIdx.z];
-  const int64_t r0 = (int64_t)blockIdx.x * 32;
-  const int c0 = blockIdx.y * 32;
-  if (r0 >= J.Kp || c0 >= J.n) return;
-  pack_tile<T, kSplit>(static_cast<const T*>(J.x), J.ld, J.M, J.d, J.n, J.Kp, J.hi, J.lo, r0, c0);
+  const int64_t b = blockIdx.x;
+  int q = 0;
+  while (q + 1 < g.count && b >= g.block_start[q + 1]) ++q;
+  const PackJob J = g.job[q];
+  const int64_t local = b - g.block_start[q], rt = (J.Kp + 31) / 32;
+  pack_tile<T, kSplit>(static_cast<const T*>(J.x), J.ld, J.M, J.d, J.n, J.Kp, J.hi, J.lo,
+                       (local % rt) * 32, (int)(local / rt) * 32);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -760,7 +775,7 @@ kfac_status launch_kernel(unsigned grid, const CUtensorMap& ah, const CUtensorMa
                           const CUtensorMap& bh, const CUtensorMap& bl, const GemmTcParams& p,
                           cudaStream_t st) {
   if (!set_smem_attr<kBF16, BN, EPI>()) return KFAC_ERR_CUDA;
-  if (p.cluster_reduce) {
+  if (p.csize > 1) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(TcCfg<kBF16, BN>::THREADS);
@@ -768,7 +783,7 @@ kfac_status launch_kernel(unsigned grid, const CUtensorMap& ah, const CUtensorMa
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.splits;
+    attr[0].val.clusterDim.x = (unsigned)p.csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -792,14 +807,15 @@ kfac_status launch_pack_grouped(const PackJob* jobs, int count, bool bf16, cudaS
   std::memset(&g, 0, sizeof(g));
   for (int c0 = 0; c0 < count; c0 += kMaxPackJobs) {
     const int cnt = std::min(kMaxPackJobs, count - c0);
-    int64_t kp = 0, nmax = 0;
+    int64_t blocks = 0;
     for (int q = 0; q < cnt; ++q) {
       g.job[q] = jobs[c0 + q];
-      kp = std::max(kp, jobs[c0 + q].Kp);
-      nmax = std::max<int64_t>(nmax, jobs[c0 + q].n);
+      g.block_start[q] = blocks;
+      blocks += cdiv(jobs[c0 + q].Kp, 32) * cdiv(jobs[c0 + q].n, 32);
     }
+    g.block_start[cnt] = blocks;
     g.count = cnt;
-    dim3 grid((unsigned)cdiv(kp, 32), (unsigned)cdiv(nmax, 32), (unsigned)cnt);
+    const unsigned grid = (unsigned)blocks;
     if (bf16)
       pack_grouped_kernel<__nv_bfloat16, false><<<grid, 256, 0, st>>>(g);
     else
@@ -817,16 +833,23 @@ size_t tc_pack_bytes(int n, int64_t max_rows, bool bf16) {
 
 size_t tc_part_floats() { return (size_t)kNumSMs * 128 * 256; }
 
-// Split-K plan: enough CTAs for one wave when the output has fewer tiles than
-// SMs, splits on ksub boundaries, at least 256 k-elements per split.
-void tc_split_plan(int64_t tiles, int64_t K, bool bf16, int* splits, int64_t* kps, int* ksub) {
-  int64_t s = std::max<int64_t>(1, kNumSMs / tiles);
-  s = std::min<int64_t>(s, std::max<int64_t>(1, K / 256));
-  const int64_t unit = bf16 ? kKsubBf16 : kKsubTf32;
-  const int64_t per = cdiv(cdiv(K, s), unit) * unit;
-  *splits = (int)cdiv(K, per);
-  *kps = per;
-  *ksub = (int)unit;
+// Split-K shape for `s` wanted splits of a reduction of length K: clusters of
+// csize = min(8, s) splits (the portable cluster size) times `groups` cluster
+// partials, each split a whole number of ksub steps.  `max_groups` bounds the
+// cluster partials the scratch can hold.
+struct SplitShape {
+  int splits, csize;
+  int64_t kps;
+};
+SplitShape split_shape(int64_t s, int64_t K, int unit, int64_t max_groups, int csize_fixed = 0) {
+  SplitShape r;
+  s = std::max<int64_t>(1, std::min<int64_t>(s, std::max<int64_t>(1, K / 256)));
+  r.csize = csize_fixed > 0 ? csize_fixed : (int)std::min<int64_t>(8, s);
+  int64_t g = cdiv(s, r.csize);
+  g = std::max<int64_t>(1, std::min<int64_t>(g, max_groups));
+  r.splits = (int)(r.csize * g);
+  r.kps = cdiv(cdiv(K, r.splits), unit) * unit;
+  return r;
 }
 
 template <int BN>
@@ -872,17 +895,21 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
   p.upper = upper ? 1 : 0;
   p.same_ab = same_ab ? 1 : 0;
   const int64_t tiles = count(BN);
-  tc_split_plan(tiles, K, bf16, &p.splits, &p.k_per_split, &p.ksub);
-  // up to 8 splits (the portable cluster size) reduce through distributed shared memory
-  p.cluster_reduce = (p.splits > 1 && p.splits <= 8) ? 1 : 0;
+  // enough CTAs for one wave when the output has fewer tiles than SMs
+  const int unit = bf16 ? kKsubBf16 : kKsubTf32;
+  const int64_t max_groups =
+      std::max<int64_t>(1, std::min<int64_t>((int64_t)(h->part_floats / ((size_t)tiles * BM * BN)),
+                                             (int64_t)(h->n_tickets / ((size_t)tiles * 8))));
+  const SplitShape sh = split_shape(std::max<int64_t>(1, kNumSMs / tiles), K, unit, max_groups);
+  p.splits = sh.splits;
+  p.csize = sh.csize;
+  p.k_per_split = sh.kps;
+  p.ksub = unit;
   p.part = h->at<float>(h->off_part);
   p.tickets = h->at<int>(h->off_tickets);
   p.status = h->status();
   p.layer = layer;
   p.e = e;
-  if (p.splits > 1 && !p.cluster_reduce && ((size_t)(tiles * p.splits) * BM * BN > h->part_floats ||
-                       (size_t)tiles > h->n_tickets))
-    return KFAC_ERR_WORKSPACE;
   const unsigned grid = (unsigned)(tiles * p.splits);
   return BN == 256 ? dispatch<256>(bf16, epi, grid, ah, al, bh, bl, p, st)
                    : dispatch<128>(bf16, epi, grid, ah, al, bh, bl, p, st);
@@ -901,7 +928,7 @@ kfac_status launch_grouped_kernel(unsigned grid, const GroupedTc& g, cudaStream_
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = g.prob[0].cluster_reduce ? (unsigned)g.splits : 1u;
+  attr[0].val.clusterDim.x = (unsigned)g.csize;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -913,8 +940,11 @@ kfac_status launch_grouped_kernel(unsigned grid, const GroupedTc& g, cudaStream_
 }
 
 // Independent products of one epilogue kind in as few launches as possible
-// (kMaxGroup per launch, 128 x 128 tiles).  All tiles of a launch share one
-// split-K count, chosen so that tiles x splits fill the GPU.
+// (128 x 128 tiles, up to kMaxGroup products per launch).  Each product gets its
+// own split-K count so that every CTA carries about the same share of the
+// launch's k-steps; products that need no split and products that do go to
+// separate launches (the cluster size is a launch attribute), and a launch is
+// cut when the split-K scratch is full.
 kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProblem* probs,
                                    int count, cudaStream_t st) {
   if (count == 1) {
@@ -923,31 +953,65 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
                           q.e, st);
   }
   constexpr int BM = 128, BN = 128;
+  constexpr size_t NT = (size_t)BM * BN;
+  const int unit = bf16 ? kKsubBf16 : kKsubTf32;
+  std::vector<int64_t> tiles(count), want(count);
+  int64_t total_units = 0;
+  for (int q = 0; q < count; ++q) {
+    const TcProblem& pr = probs[q];
+    const int tm = (int)cdiv(pr.M, BM), tn = (int)cdiv(pr.N, BN);
+    tiles[q] = pr.upper ? upper_tile_count(tm, tn, 1) : (int64_t)tm * tn;
+    total_units += tiles[q] * cdiv(pr.K, unit);
+  }
+  // k-steps per CTA if the whole group were spread over one wave
+  const int64_t chunk = std::max<int64_t>(2, cdiv(total_units, kNumSMs));
+  for (int q = 0; q < count; ++q)
+    want[q] = std::max<int64_t>(1, cdiv(cdiv(probs[q].K, unit), chunk));
   std::unique_ptr<GroupedTc> g(new GroupedTc());
-  for (int c0 = 0; c0 < count; c0 += kMaxGroup) {
-    const int cnt = std::min(kMaxGroup, count - c0);
+  for (int pass = 0; pass < 2; ++pass) {   // pass 0: unsplit products; pass 1: split ones
+    const int csize = pass == 0 ? 1 : 8;
     std::memset(g.get(), 0, sizeof(GroupedTc));
-    int64_t total = 0, kmax = 0;
-    for (int q = 0; q < cnt; ++q) {
-      const TcProblem& pr = probs[c0 + q];
-      const int tm = (int)cdiv(pr.M, BM), tn = (int)cdiv(pr.N, BN);
-      g->tile_start[q] = (int)total;
-      total += pr.upper ? upper_tile_count(tm, tn, 1) : (int64_t)tm * tn;
-      kmax = std::max(kmax, pr.K);
-    }
-    g->tile_start[cnt] = (int)total;
-    int64_t s = std::max<int64_t>(1, kNumSMs / total);
-    s = std::min<int64_t>(s, std::max<int64_t>(1, kmax / 256));
-    const int unit = bf16 ? kKsubBf16 : kKsubTf32;
-    const bool cluster = s >= 2 && s <= 8;
-    if (s > 1 && !cluster &&
-        ((size_t)(total * s) * BM * BN > h->part_floats || (size_t)total > h->n_tickets))
-      return KFAC_ERR_WORKSPACE;
-    g->count = cnt;
-    g->splits = (int)s;
-    for (int q = 0; q < cnt; ++q) {
-      const TcProblem& pr = probs[c0 + q];
-      CUtensorMap* m = &g->maps[4 * q];
+    g->csize = csize;
+    int blocks = 0;
+    size_t part_used = 0, tick_used = 0;
+    auto flush = [&]() -> kfac_status {
+      if (g->count == 0) return KFAC_OK;
+      g->block_start[g->count] = blocks;
+      kfac_status e;
+      if (epi == TC_EPI_SYRK)
+        e = bf16 ? launch_grouped_kernel<true, TC_EPI_SYRK>(blocks, *g, st)
+                 : launch_grouped_kernel<false, TC_EPI_SYRK>(blocks, *g, st);
+      else if (bf16)
+        e = KFAC_ERR_UNSUPPORTED;
+      else if (epi == TC_EPI_SPLIT)
+        e = launch_grouped_kernel<false, TC_EPI_SPLIT>(blocks, *g, st);
+      else
+        e = launch_grouped_kernel<false, TC_EPI_PRECOND>(blocks, *g, st);
+      std::memset(g.get(), 0, sizeof(GroupedTc));
+      g->csize = csize;
+      blocks = 0;
+      part_used = tick_used = 0;
+      return e;
+    };
+    for (int q = 0; q < count; ++q) {
+      if ((want[q] > 1) != (pass == 1)) continue;
+      const TcProblem& pr = probs[q];
+      SplitShape sh{1, 1, cdiv(pr.K, unit) * unit};
+      if (pass == 1) {
+        // cluster partials this product may use: what the scratch holds by itself
+        const int64_t max_groups = std::max<int64_t>(
+            1, std::min<int64_t>((int64_t)(h->part_floats / (tiles[q] * NT)),
+                                 (int64_t)(h->n_tickets / (tiles[q] * csize))));
+        sh = split_shape(want[q], pr.K, unit, max_groups, csize);
+      }
+      const int G = sh.splits / sh.csize;
+      const size_t pneed = G > 1 ? (size_t)tiles[q] * G * NT : 0;
+      const size_t tneed = G > 1 ? (size_t)tiles[q] * csize : 0;
+      if (g->count == kMaxGroup || part_used + pneed > h->part_floats ||
+          tick_used + tneed > h->n_tickets)
+        if (kfac_status e = flush()) return e;
+      const int i = g->count;
+      CUtensorMap* m = &g->maps[4 * i];
       if (!make_map(&m[0], pr.A.hi, bf16, pr.A.rows, pr.K, pr.A.pitch, BM)) return KFAC_ERR_CUDA;
       if (!make_map(&m[2], pr.B.hi, bf16, pr.B.rows, pr.K, pr.B.pitch, BN)) return KFAC_ERR_CUDA;
       if (bf16) {
@@ -957,7 +1021,7 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
         if (!make_map(&m[1], pr.A.lo, false, pr.A.rows, pr.K, pr.A.pitch, BM)) return KFAC_ERR_CUDA;
         if (!make_map(&m[3], pr.B.lo, false, pr.B.rows, pr.K, pr.B.pitch, BN)) return KFAC_ERR_CUDA;
       }
-      GemmTcParams& pp = g->prob[q];
+      GemmTcParams& pp = g->prob[i];
       pp.M = pr.M;
       pp.N = pr.N;
       pp.K = pr.K;
@@ -965,28 +1029,22 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
       pp.tiles_n = (int)cdiv(pr.N, BN);
       pp.upper = pr.upper ? 1 : 0;
       pp.same_ab = pr.same_ab ? 1 : 0;
-      pp.splits = (int)s;
-      pp.cluster_reduce = cluster ? 1 : 0;
-      pp.k_per_split = cdiv(cdiv(pr.K, s), unit) * unit;
+      pp.splits = sh.splits;
+      pp.csize = sh.csize;
+      pp.k_per_split = sh.kps;
       pp.ksub = unit;
-      pp.part = h->at<float>(h->off_part);
-      pp.tickets = h->at<int>(h->off_tickets);
+      pp.part = h->at<float>(h->off_part) + part_used;
+      pp.tickets = h->at<int>(h->off_tickets) + tick_used;
       pp.status = h->status();
       pp.layer = pr.layer;
       pp.e = pr.e;
+      g->block_start[i] = blocks;
+      blocks += (int)(tiles[q] * sh.splits);
+      part_used += pneed;
+      tick_used += tneed;
+      ++g->count;
     }
-    const unsigned grid = (unsigned)(total * s);
-    kfac_status e;
-    if (epi == TC_EPI_SYRK)
-      e = bf16 ? launch_grouped_kernel<true, TC_EPI_SYRK>(grid, *g, st)
-               : launch_grouped_kernel<false, TC_EPI_SYRK>(grid, *g, st);
-    else if (bf16)
-      e = KFAC_ERR_UNSUPPORTED;
-    else if (epi == TC_EPI_SPLIT)
-      e = launch_grouped_kernel<false, TC_EPI_SPLIT>(grid, *g, st);
-    else
-      e = launch_grouped_kernel<false, TC_EPI_PRECOND>(grid, *g, st);
-    if (e != KFAC_OK) return e;
+    if (kfac_status e = flush()) return e;
   }
   return KFAC_OK;
 }
