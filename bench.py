@@ -441,13 +441,17 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     tf32_peak = peaks["bf16_tflops"] * TF32_PER_BF16
     if dom == "diag":
         roof = {"bound": "hbm", "achieved": round(diag_gbs, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "kernel": "diag_factor_kernel + diag_step_kernel"}
+                "unit": "GB/s", "kernel": "diag_factor_grouped_kernel + diag_step_grouped_kernel"}
     elif dom in ("factor", "precond"):
         flop = acc["factor_flop"] if dom == "factor" else acc["precond_flop"]
         ms = phase_ms[0] if dom == "factor" else phase_ms[2]
         ach = flop / (ms * 1e-3) / 1e12
+        kern = ("pack_grouped_kernel + gemm_tc_grouped_kernel<SYRK> (3xTF32, tcgen05)"
+                if dom == "factor" else
+                "gradhat_pack_grouped_kernel + gemm_tc_grouped_kernel<SPLIT> + "
+                "gemm_tc_grouped_kernel<PRECOND> (3xTF32, tcgen05)")
         roof = {"bound": "tensor", "achieved": round(ach, 3), "peak": round(tf32_peak, 1),
-                "unit": "TFLOP/s", "kernel": "gemm_tc_kernel (3xTF32, tcgen05)",
+                "unit": "TFLOP/s", "kernel": kern, "timed": "one batched library call (the phase)",
                 "issued_frac": round(3 * ach / tf32_peak, 4),
                 "note": "algorithmic flops (upper triangle for factors); 3xTF32 issues 3x"}
     else:

@@ -95,7 +95,9 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
       pack_sum += align_up(tc_pack_bytes(L.n, max_rows, bf)) + align_up(tc_pack_bytes(L.o, max_rows, bf));
       tickets = std::max({tickets, t1, t2, (size_t)16 * kNumSMs});   // split-K: tile x cluster rank
       k4 = std::max(k4, 2 * o * np + 2 * n * op);
-      k4_sum += align_up((2 * o * np + 2 * n * op) * sizeof(float)) / sizeof(float);
+      // batched K4 aligns each of its four arrays (dW-hat and X^T halves) separately
+      k4_sum += 2 * (align_up(o * np * sizeof(float)) + align_up(n * op * sizeof(float))) /
+                sizeof(float);
       ninv += 2;
       maxn = std::max({maxn, L.n, L.o});
     } else {
