@@ -658,6 +658,327 @@ gemm_tc_grouped_kernel(const __grid_constant__ GroupedTc g) {
                              &g.maps[4 * q + 3], g.prob[q], local / sp, local % sp);
 }
 
+// ------------------------------------------------------- persistent grouped
+// The grouped products without split-K, one CTA per SM looping over tiles
+// (tile t, t + gridDim.x, ...).  The TMA and MMA warps run on into the next
+// tile while the drain warps finish the previous tile's epilogue: the TMEM
+// accumulator is a ring of 4 buffers (512 columns), so the MMA can run up to
+// four drain periods ahead.  The stage buffers stay busy meanwhile, so these
+// epilogues read their global inputs straight into registers (lanes on rows,
+// coalesced; prefetched into L2 when the tile starts) and the SYRK direct half
+// is transposed through a per-warp 32 x 33 buffer.
+template <bool kBF16>
+struct PersistCfg {
+  using C = TcCfg<kBF16, 128>;
+  static constexpr int ACC = 4;
+  static constexpr int TMEM_COLS = ACC * 128;
+  static constexpr int XP = 33;                                   // transpose pitch
+  static constexpr int XPOSE_BYTES = C::EPI_WARPS * 32 * XP * 4;
+  static constexpr size_t SMEM = 1024 + (size_t)C::STAGES * C::STAGE_BYTES + XPOSE_BYTES + 256;
+  static_assert(SMEM <= 232448, "fits the per-CTA shared memory");
+};
+
+__device__ __forceinline__ void grouped_tile(const GroupedTc& g, int t, int* q, int* ti, int* tj) {
+  int k = 0;
+  while (k + 1 < g.count && t >= g.block_start[k + 1]) ++k;
+  const int local = t - g.block_start[k];
+  const GemmTcParams& p = g.prob[k];
+  if (p.upper) {
+    upper_tile(local, p.tiles_m, 1, ti, tj);
+  } else {
+    *ti = local / p.tiles_n;
+    *tj = local % p.tiles_n;
+  }
+  *q = k;
+}
+
+template <bool kBF16, int EPI>
+__global__ void __launch_bounds__(TcCfg<kBF16, 128>::THREADS, 1)
+gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
+  using C = TcCfg<kBF16, 128>;
+  using PC = PersistCfg<kBF16>;
+  constexpr int CW = C::CW;   // 64 columns per drain thread
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  float* xbuf = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + PC::XPOSE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + PC::ACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + PC::ACC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int total = g.block_start[g.count];
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < PC::ACC; ++b) {
+      tc::mbar_init(&acc_full[b], 1);
+      tc::mbar_init(&acc_empty[b], 32 * C::EPI_WARPS);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, PC::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto a_ptr = [&](int s, int lo) { return smem + (size_t)s * C::STAGE_BYTES + lo * C::HALF_BYTES; };
+  auto b_ptr = [&](int s, int lo) { return a_ptr(s, lo) + C::A_BYTES; };
+  auto nkb_of = [&](int q) { return (int)((g.prob[q].K + C::BK - 1) / C::BK); };
+  const int kb_per_sub = g.prob[0].ksub / C::BK;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int q, ti, tj;
+        grouped_tile(g, t, &q, &ti, &tj);
+        const CUtensorMap* m = &g.maps[4 * q];
+        const bool a_in_b = g.prob[q].same_ab && ti == tj;
+        const uint32_t bytes = (a_in_b ? C::B_BYTES : C::HALF_BYTES) * (kBF16 ? 1 : 2);
+        const int nkb = nkb_of(q);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+            *abort_flag = 1;
+            report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 11);
+            ok = false;
+            break;
+          }
+          const int k0 = kb * C::BK;
+          tc::mbar_expect_tx(&full[stage], bytes);
+          if (!a_in_b) tc::tma_load_2d(a_ptr(stage, 0), &m[0], &full[stage], k0, ti * C::BM);
+          tc::tma_load_2d(b_ptr(stage, 0), &m[2], &full[stage], k0, tj * C::BN);
+          if (!kBF16) {
+            if (!a_in_b) tc::tma_load_2d(a_ptr(stage, 1), &m[1], &full[stage], k0, ti * C::BM);
+            tc::tma_load_2d(b_ptr(stage, 1), &m[3], &full[stage], k0, tj * C::BN);
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = tc::make_idesc(kBF16 ? 1 : 2, C::BM, C::BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int gsub = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int q, ti, tj;
+        grouped_tile(g, t, &q, &ti, &tj);
+        const bool a_in_b = g.prob[q].same_ab && ti == tj;
+        const int nkb = nkb_of(q);
+        const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
+        for (int sub = 0; sub < nsub && ok; ++sub, ++gsub) {
+          const int buf = gsub % PC::ACC, use = gsub / PC::ACC;
+          if (!tc::mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag)) {
+            report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 12);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t d = tmem + (uint32_t)(buf * C::BN);
+          const int kb0 = sub * kb_per_sub, kb1 = min(nkb, kb0 + kb_per_sub);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!tc::mbar_wait(&full[stage], phase, abort_flag)) {
+              report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 13);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            tc::tc_fence_after();
+            const uint32_t a_hi = tc::smem_u32(a_in_b ? b_ptr(stage, 0) : a_ptr(stage, 0));
+            const uint32_t b_hi = tc::smem_u32(b_ptr(stage, 0));
+            const uint32_t a_lo = tc::smem_u32(a_in_b ? b_ptr(stage, kBF16 ? 0 : 1)
+                                                      : a_ptr(stage, kBF16 ? 0 : 1));
+            const uint32_t b_lo = tc::smem_u32(b_ptr(stage, kBF16 ? 0 : 1));
+#pragma unroll
+            for (int kk = 0; kk < C::BK / C::KMMA; ++kk) {
+              const uint32_t off = kk * 32;
+              const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+              if (kBF16) {
+                tc::umma_f16(d, tc::sdesc_kmajor_sw128(a_hi + off),
+                             tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
+              } else {
+                tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_hi + off),
+                              tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
+                tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_hi + off),
+                              tc::sdesc_kmajor_sw128(b_lo + off), idesc, 1u);
+                tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_lo + off),
+                              tc::sdesc_kmajor_sw128(b_hi + off), idesc, 1u);
+              }
+            }
+            tc::umma_commit(&empty[stage]);
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (ok) tc::umma_commit(&acc_full[buf]);
+        }
+      }
+    }
+  } else {  // ------------------------------------------------ drain + epilogue
+    const int qd = warp & 3;                 // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;           // column half: [CW h, CW h + CW)
+    const int row = 32 * qd + lane;
+    float* xb = xbuf + (warp - 2) * 32 * PC::XP;
+    int gsub = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int q, ti, tj;
+      grouped_tile(g, t, &q, &ti, &tj);
+      const TcEpilogue E = g.prob[q].e;   // by value (see gemm_body)
+      const int64_t pM = g.prob[q].M, pN = g.prob[q].N;
+      const int64_t r0 = (int64_t)ti * C::BM, c0 = (int64_t)tj * C::BN + h * CW;
+      const int64_t gr = r0 + row;
+      const int nkb = nkb_of(q);
+      const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
+      if (gr < pM) {   // the tile's epilogue inputs into L2 while the drains run
+        if (EPI == TC_EPI_SYRK && E.beta != 0.f) {
+          for (int c = 0; c < CW; ++c) {
+            const int64_t gc = c0 + c;
+            if (gc < pN && gr <= gc) tc::prefetch_l2(E.C + gc * E.ldc + gr);
+          }
+        } else if (EPI == TC_EPI_PRECOND && E.pw && gr < E.d_in) {
+          for (int c = 0; c < CW; ++c) {
+            const int64_t i = c0 + c;
+            if (i >= pN) break;
+            tc::prefetch_l2(E.pw + i * E.d_in + gr);
+            tc::prefetch_l2(E.mw + i * E.d_in + gr);
+          }
+        }
+      }
+      float sum[CW];
+#pragma unroll
+      for (int c = 0; c < CW; ++c) sum[c] = 0.f;
+      for (int sub = 0; sub < nsub; ++sub, ++gsub) {
+        const int buf = gsub % PC::ACC, use = gsub / PC::ACC;
+        if (!tc::mbar_wait(&acc_full[buf], use & 1, abort_flag)) {
+          report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 14);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < CW / 32; ++cc) {
+          float v[32];
+          tc::tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) +
+                            (uint32_t)(buf * C::BN + h * CW + cc * 32), v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sum[cc * 32 + i] += v[i];
+        }
+        tc::tc_fence_before();
+        tc::mbar_arrive(&acc_empty[buf]);
+      }
+      if (!ok) break;
+      if (EPI == TC_EPI_SYRK) {
+        // mirror F[gc][gr] from registers, old value from the same place
+#pragma unroll
+        for (int cc = 0; cc < CW; cc += 16) {
+          float old[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int64_t gc = c0 + cc + u;
+            const bool okc = gr < pM && gc < pN && gr <= gc;
+            old[u] = (okc && E.beta != 0.f) ? __ldcg(E.C + gc * E.ldc + gr) : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int64_t gc = c0 + cc + u;
+            const float v = fmaf(E.beta, old[u], E.alpha * sum[cc + u]);
+            sum[cc + u] = v;
+            if (gr < pM && gc < pN && gr <= gc) E.C[gc * E.ldc + gr] = v;
+          }
+        }
+        // direct half F[gr][gc] (gr < gc): 32 x 32 blocks transposed through the
+        // warp's buffer so that lanes run along gc
+#pragma unroll
+        for (int j2 = 0; j2 < CW / 32; ++j2) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) xb[lane * PC::XP + c] = sum[j2 * 32 + c];
+          __syncwarp();
+          const int64_t gcol = c0 + j2 * 32 + lane;
+#pragma unroll 8
+          for (int r = 0; r < 32; ++r) {
+            const int64_t grr = r0 + 32 * qd + r;
+            if (grr < pM && gcol < pN && grr < gcol) E.C[grr * E.ldc + gcol] = xb[r * PC::XP + lane];
+          }
+          __syncwarp();
+        }
+      } else if (EPI == TC_EPI_SPLIT) {
+        if (gr < pM) {
+#pragma unroll
+          for (int c = 0; c < CW; ++c) {
+            const int64_t gc = c0 + c;
+            if (gc >= pN) continue;
+            const float hi = tc::to_tf32(sum[c]);
+            E.out_hi[gc * E.ldo + gr] = hi;
+            E.out_lo[gc * E.ldo + gr] = tc::to_tf32(sum[c] - hi);
+          }
+        }
+      } else {  // PRECOND: row gr = column j of P, column gc = row i
+        const bool wcol = gr < E.d_in;
+        if (gr < pM) {
+#pragma unroll
+          for (int cc = 0; cc < CW; cc += 16) {
+            float w[16], m[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const int64_t i = c0 + cc + u;
+              w[u] = m[u] = 0.f;
+              if (E.pw && i < pN) {
+                w[u] = wcol ? __ldcg(E.pw + i * E.d_in + gr) : __ldcg(E.pb + i);
+                m[u] = wcol ? __ldcg(E.mw + i * E.d_in + gr) : __ldcg(E.mb + i);
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const int64_t i = c0 + cc + u;
+              if (i >= pN) continue;
+              const float pr = sum[cc + u];
+              const float mn = fmaf(E.mu, m[u], fmaf(E.lambda, w[u], pr));
+              const float wn = fmaf(-E.eta, mn, w[u]);
+              if (wcol) {
+                const int64_t x = i * E.d_in + gr;
+                if (E.ow) E.ow[x] = pr;
+                if (E.pw) {
+                  E.mw[x] = mn;
+                  E.pw[x] = wn;
+                }
+              } else {
+                if (E.ob) E.ob[i] = pr;
+                if (E.pb) {
+                  E.mb[i] = mn;
+                  E.pb[i] = wn;
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, PC::TMEM_COLS);
+}
+
 // ------------------------------------------------------------------- pack
 // X[c][r] = x-hat[r][c] for c < n, r < M; fp32 -> (hi, lo) TF32 halves; bf16 -> copy.
 template <typename T, bool kSplit>
@@ -916,7 +1237,22 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
 }
 
 template <bool kBF16, int EPI>
+kfac_status launch_persistent_kernel(const GroupedTc& g, cudaStream_t st) {
+  static bool attr_ok = cudaFuncSetAttribute(gemm_tc_persistent_kernel<kBF16, EPI>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)PersistCfg<kBF16>::SMEM) == cudaSuccess;
+  if (!attr_ok) return KFAC_ERR_CUDA;
+  const int total = g.block_start[g.count];
+  const unsigned grid = (unsigned)std::min<int>(total, kNumSMs);
+  gemm_tc_persistent_kernel<kBF16, EPI>
+      <<<grid, TcCfg<kBF16, 128>::THREADS, PersistCfg<kBF16>::SMEM, st>>>(g);
+  count_launch();
+  return check_launch();
+}
+
+template <bool kBF16, int EPI>
 kfac_status launch_grouped_kernel(unsigned grid, const GroupedTc& g, cudaStream_t st) {
+  if (g.csize == 1 && g.prob[0].splits == 1) return launch_persistent_kernel<kBF16, EPI>(g, st);
   static bool attr_ok = cudaFuncSetAttribute(gemm_tc_grouped_kernel<kBF16, EPI>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)TcCfg<kBF16, 128>::SMEM) == cudaSuccess;
