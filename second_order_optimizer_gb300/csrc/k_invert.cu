@@ -27,6 +27,7 @@
 #include "tc_prims.cuh"
 
 #include <algorithm>
+#include <vector>
 
 namespace kfac {
 
@@ -238,16 +239,30 @@ __device__ __forceinline__ void lower_tile_coords(int t, int* ti, int* tj) {
   *tj = t;
 }
 
-// L[i][j] -= sum_t L[i][k+t] L[j][k+t] over the trailing lower tiles.
-__global__ void __launch_bounds__(256) chol_trailing_kernel(const InvJob* jobs, int k) {
+// L[i][j] -= sum_t L[i][k+t] L[j][k+t] over the trailing lower tiles (ti >= tj,
+// counted from the first trailing block).  part: 0 all tiles; 1 the first block
+// column only (tj = 0: what the next diagonal block and panel need); 2 the rest
+// (tj >= 1), which may run alongside the next diagonal block and panel.
+__global__ void __launch_bounds__(256) chol_trailing_kernel(const InvJob* jobs, int k, int part) {
   const InvJob J = jobs[blockIdx.y];
   const int n = J.n;
   const int64_t base = (int64_t)k + NB;
   if (base >= n) return;
   const int nt = (int)((n - base + 63) / 64);
-  if ((int)blockIdx.x >= nt * (nt + 1) / 2) return;
   int ti, tj;
-  lower_tile_coords(blockIdx.x, &ti, &tj);
+  if (part == 1) {
+    if ((int)blockIdx.x >= nt) return;
+    ti = blockIdx.x;
+    tj = 0;
+  } else if (part == 2) {
+    if ((int)blockIdx.x >= (nt - 1) * nt / 2) return;
+    lower_tile_coords(blockIdx.x, &ti, &tj);
+    ++ti;
+    ++tj;
+  } else {
+    if ((int)blockIdx.x >= nt * (nt + 1) / 2) return;
+    lower_tile_coords(blockIdx.x, &ti, &tj);
+  }
   __shared__ float smem[PTile::kSmemFloats];
   float acc[4][4] = {};
   StridedLoader la{J.L + k, n, 1, n, NB};   // (i, t) -> L[i][k+t]
@@ -381,6 +396,14 @@ kfac_status launch_invert(kfac_ctx* h, int layer, cudaStream_t st) {
   count_launch();
   if (kfac_status e = check_launch()) return e;
 
+  // Cholesky with one block of lookahead: after the panel of step k, the
+  // trailing update of the next block column runs on the caller's stream (the
+  // next diagonal block needs it), the rest on the side stream, concurrently
+  // with the next diagonal block and panel.  Events: the side stream waits for
+  // each panel; the next block column's update waits for the previous rest,
+  // which also writes that column.
+  bool rest_pending = false;
+  auto sync_err = [](cudaError_t e) { return e == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA; };
   for (int k = 0; k < nmax; k += NB) {
     chol_diag_kernel<<<nj, 256, 0, st>>>(jobs, k, h->status());
     count_launch();
@@ -388,11 +411,27 @@ kfac_status launch_invert(kfac_ctx* h, int layer, cudaStream_t st) {
     if (rest > 0) {
       const int rb = (int)cdiv(rest, 64);
       chol_panel_kernel<<<dim3(rb, nj), 256, 0, st>>>(jobs, k);
-      chol_trailing_kernel<<<dim3(rb * (rb + 1) / 2, nj), 256, 0, st>>>(jobs, k);
-      count_launch(2);
+      count_launch();
+      if (rb > 1) {
+        if (kfac_status e = sync_err(cudaEventRecord(h->ev_panel, st))) return e;
+        if (kfac_status e = sync_err(cudaStreamWaitEvent(h->side_stream, h->ev_panel, 0))) return e;
+      }
+      if (rest_pending)
+        if (kfac_status e = sync_err(cudaStreamWaitEvent(st, h->ev_rest, 0))) return e;
+      chol_trailing_kernel<<<dim3(rb, nj), 256, 0, st>>>(jobs, k, 1);
+      count_launch();
+      rest_pending = false;
+      if (rb > 1) {
+        chol_trailing_kernel<<<dim3((rb - 1) * rb / 2, nj), 256, 0, h->side_stream>>>(jobs, k, 2);
+        count_launch();
+        if (kfac_status e = sync_err(cudaEventRecord(h->ev_rest, h->side_stream))) return e;
+        rest_pending = true;
+      }
     }
     if (kfac_status e = check_launch()) return e;
   }
+  if (rest_pending)
+    if (kfac_status e = sync_err(cudaStreamWaitEvent(st, h->ev_rest, 0))) return e;
   for (int s = NB; s < nmax; s *= 2) {
     const int tiles = level_tiles_host(nmax, s);
     int tmax = tiles;
@@ -411,13 +450,14 @@ kfac_status launch_invert(kfac_ctx* h, int layer, cudaStream_t st) {
   if (nt_small > 0)
     if (kfac_status e = launch_syrk_simt_grouped(d_syrk + j0, nj, nt_small * (nt_small + 1) / 2, st))
       return e;
+  std::vector<SyrkSpec> big;
   for (int i = j0; i < j0 + nj; ++i) {
     const InvJob& J = h->invjobs_host[i];
     if (J.n < kTcInverseMinN) continue;
-    if (kfac_status e = launch_syrk_tc(h, J.layer, J.X, J.n, J.n, J.n, J.n, 0, false, 1.f, 0.f,
-                                       J.Finv, st))
-      return e;
+    big.push_back(SyrkSpec{J.X, J.n, J.n, J.n, J.n, J.layer, 1.f, 0.f, J.Finv});
   }
+  if (!big.empty())
+    if (kfac_status e = launch_syrk_tc_batched(h, big.data(), (int)big.size(), st)) return e;
   inv_split_kernel<<<dim3((unsigned)std::min<int64_t>(cdiv((int64_t)nmax * nmax, 256), 1024), nj),
                      256, 0, st>>>(jobs);
   count_launch();

@@ -54,7 +54,7 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
   P->off_status = take(sizeof(DevStatus));
   P->layers.clear();
   size_t part = 0, tickets = 0, k4 = 0, k5 = 0, k5t = 0, tcpack = 0;
-  size_t pack_sum = 0, k4_sum = 0;   // what a batch over every KRON layer would use
+  size_t pack_sum = 0, k4_sum = 0, inv_pack_sum = 0;   // what a batch over every KRON layer would use
   int ninv = 0, maxn = 0;
   for (int i = 0; i < nl; ++i) {
     const kfac_layer_desc& d = descs[i];
@@ -88,10 +88,18 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
       part = std::max(part, k1_scratch_floats(L.o, max_rows, &t2));
       const bool bf = d.in_dtype == KFAC_BF16;
       part = std::max(part, tc_part_floats());
-      tcpack = std::max({tcpack, tc_pack_bytes(L.n, max_rows, bf), tc_pack_bytes(L.o, max_rows, bf)});
+      // a batched group of one layer holds its A and G packs at once
+      tcpack = std::max(tcpack, align_up(tc_pack_bytes(L.n, max_rows, bf)) +
+                                    align_up(tc_pack_bytes(L.o, max_rows, bf)));
       // the inverse assembly packs X = L^{-1} (n x n, fp32) through the same buffer
-      if (L.n >= kTcInverseMinN) tcpack = std::max(tcpack, tc_pack_bytes(L.n, L.n, false));
-      if (L.o >= kTcInverseMinN) tcpack = std::max(tcpack, tc_pack_bytes(L.o, L.o, false));
+      if (L.n >= kTcInverseMinN) {
+        tcpack = std::max(tcpack, tc_pack_bytes(L.n, L.n, false));
+        inv_pack_sum += align_up(tc_pack_bytes(L.n, L.n, false));
+      }
+      if (L.o >= kTcInverseMinN) {
+        tcpack = std::max(tcpack, tc_pack_bytes(L.o, L.o, false));
+        inv_pack_sum += align_up(tc_pack_bytes(L.o, L.o, false));
+      }
       pack_sum += align_up(tc_pack_bytes(L.n, max_rows, bf)) + align_up(tc_pack_bytes(L.o, max_rows, bf));
       tickets = std::max({tickets, t1, t2, (size_t)16 * kNumSMs});   // split-K: tile x cluster rank
       k4 = std::max(k4, 2 * o * np + 2 * n * op);
@@ -111,6 +119,7 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
   }
   // batched calls pack a group of layers at once, within a fixed budget
   tcpack = std::max(tcpack, std::min(pack_sum, kBatchScratchBudget));
+  tcpack = std::max(tcpack, std::min(inv_pack_sum, kBatchScratchBudget));
   k4 = std::max(k4, std::min(k4_sum, kBatchScratchBudget / sizeof(float)));
   P->part_floats = part;
   P->off_part = take(part * sizeof(float));
@@ -231,6 +240,14 @@ kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_
   h->off_invjobs = P.off_invjobs;
   h->n_invjobs = P.n_invjobs;
   h->max_kron_n = P.max_kron_n;
+  if (P.n_invjobs > 0) {
+    if (cudaStreamCreateWithFlags(&h->side_stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_panel, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_rest, cudaEventDisableTiming) != cudaSuccess) {
+      kfac_destroy(h);
+      return KFAC_ERR_CUDA;
+    }
+  }
   // inversion tables: for each KRON layer, its A then its G
   std::vector<SyrkJob> sj;
   for (int i = 0; i < n_layers; ++i) {
@@ -533,6 +550,9 @@ kfac_status kfac_state_info(kfac_handle h, int layer, int which, size_t* offset,
 
 kfac_status kfac_destroy(kfac_handle h) {
   if (!h) return KFAC_ERR_INVALID_ARG;
+  if (h->side_stream) cudaStreamDestroy(h->side_stream);
+  if (h->ev_panel) cudaEventDestroy(h->ev_panel);
+  if (h->ev_rest) cudaEventDestroy(h->ev_rest);
   delete h;
   return KFAC_OK;
 }

@@ -88,6 +88,10 @@ struct kfac_ctx {
   int n_invjobs = 0;
   std::vector<kfac::InvJob> invjobs_host;
   int max_kron_n = 0;
+  // inversion lookahead: the bulk of each trailing update runs on a second
+  // stream, ordered against the caller's stream by two events
+  cudaStream_t side_stream = nullptr;
+  cudaEvent_t ev_panel = nullptr, ev_rest = nullptr;
 
   kfac::DevStatus* status() const { return reinterpret_cast<kfac::DevStatus*>(ws + off_status); }
   template <typename T> T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
@@ -184,6 +188,18 @@ struct PackJob {
 };
 constexpr int kMaxPackJobs = 32;
 kfac_status launch_pack_grouped(const PackJob* jobs, int count, bool bf16, cudaStream_t st);
+// Several F <- beta F + alpha x-hat^T x-hat products (fp32 inputs, 3xTF32): the
+// packs of a group run as one launch and the products as grouped launches; a
+// group is as many as the pack scratch holds.
+struct SyrkSpec {
+  const float* x;
+  int64_t ld, rows;
+  int d, n, layer;
+  float alpha, beta;
+  float* F;
+};
+kfac_status launch_syrk_tc_batched(kfac_ctx* h, const SyrkSpec* specs, int count, cudaStream_t st);
+size_t inv_y_floats(int n);
 // scratch of the batched entry points (a group of layers is packed together)
 constexpr size_t kBatchScratchBudget = size_t(256) << 20;
 size_t tc_pack_bytes(int n, int64_t max_rows, bool bf16);
@@ -192,6 +208,5 @@ size_t tc_part_floats();
 // scratch sizing helpers (used by the workspace planner)
 size_t k1_scratch_floats(int n, int64_t max_rows, size_t* tickets);
 size_t k5_scratch_floats(int n_plus_o, int64_t max_rows);
-size_t inv_y_floats(int n);
 
 }  // namespace kfac

@@ -1414,4 +1414,55 @@ kfac_status launch_syrk_tc(kfac_ctx* h, int layer, const void* x, int64_t ld, in
   return launch_gemm_tc(h, layer, bf16, TC_EPI_SYRK, X, X, true, true, n, n, rows, e, st);
 }
 
+kfac_status launch_syrk_tc_batched(kfac_ctx* h, const SyrkSpec* specs, int count,
+                                   cudaStream_t st) {
+  std::vector<PackJob> pj;
+  std::vector<TcProblem> pr;
+  size_t used = 0;
+  auto flush = [&]() -> kfac_status {
+    if (pr.empty()) return KFAC_OK;
+    kfac_status e = launch_pack_grouped(pj.data(), (int)pj.size(), false, st);
+    if (e == KFAC_OK) e = launch_gemm_tc_grouped(h, false, TC_EPI_SYRK, pr.data(), (int)pr.size(), st);
+    pj.clear();
+    pr.clear();
+    used = 0;
+    return e;
+  };
+  for (int i = 0; i < count; ++i) {
+    const SyrkSpec& q = specs[i];
+    const int64_t Kp = tc_pitch(q.rows, false);
+    const size_t raw = (size_t)q.n * Kp * 8, bytes = align_up(raw);   // next job starts aligned
+    if (raw > h->tcpack_bytes) return KFAC_ERR_WORKSPACE;
+    if (used + raw > h->tcpack_bytes || (int)pr.size() == kMaxPackJobs)
+      if (kfac_status e = flush()) return e;
+    char* hi = h->ws + h->off_tcpack + used;
+    char* lo = hi + (size_t)q.n * Kp * 4;
+    used += bytes;
+    PackJob j{};
+    j.x = q.x;
+    j.ld = q.ld;
+    j.M = q.rows;
+    j.d = q.d;
+    j.n = q.n;
+    j.Kp = Kp;
+    j.hi = hi;
+    j.lo = lo;
+    pj.push_back(j);
+    TcProblem t{};
+    t.A = TcOperand{hi, lo, q.n, Kp};
+    t.B = t.A;
+    t.same_ab = true;
+    t.upper = true;
+    t.M = t.N = q.n;
+    t.K = q.rows;
+    t.e.alpha = q.alpha;
+    t.e.beta = q.beta;
+    t.e.C = q.F;
+    t.e.ldc = q.n;
+    t.layer = q.layer;
+    pr.push_back(t);
+  }
+  return flush();
+}
+
 }  // namespace kfac
