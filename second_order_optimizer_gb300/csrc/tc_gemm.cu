@@ -981,32 +981,44 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
 
 // ------------------------------------------------------------------- pack
 // X[c][r] = x-hat[r][c] for c < n, r < M; fp32 -> (hi, lo) TF32 halves; bf16 -> copy.
+// One CTA moves a tile of kPackRows rows x 32 columns through shared memory
+// (row pitch 33: conflict-free both ways): loads run along columns (coalesced
+// rows of x-hat), stores along rows (coalesced rows of X); each thread keeps
+// kPackRows / 8 loads in flight.
+constexpr int kPackRows = 128;
 template <typename T, bool kSplit>
 __device__ __forceinline__ void pack_tile(const T* __restrict__ x, int64_t ld, int64_t M, int d,
                                           int n, int64_t Kp, void* out_hi, void* out_lo,
                                           int64_t r0, int c0) {
-  __shared__ float tile[32][33];
+  __shared__ float tile[kPackRows][33];
   const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;  // 32 x 8
-  for (int i = ty; i < 32; i += 8) {
-    const int64_t r = r0 + i;
+  float v[kPackRows / 8];
+#pragma unroll
+  for (int u = 0; u < kPackRows / 8; ++u) {
+    const int64_t r = r0 + ty + 8 * u;
     const int c = c0 + tx;
-    float v = 0.f;
-    if (r < M && c < n) v = c < d ? to_f32<T>(x[r * ld + c]) : 1.f;
-    tile[i][tx] = v;
+    v[u] = 0.f;
+    if (r < M && c < n) v[u] = c < d ? to_f32<T>(x[r * ld + c]) : 1.f;
   }
+#pragma unroll
+  for (int u = 0; u < kPackRows / 8; ++u) tile[ty + 8 * u][tx] = v[u];
   __syncthreads();
-  for (int i = ty; i < 32; i += 8) {
-    const int c = c0 + i;
-    const int64_t r = r0 + tx;
-    if (c >= n || r >= Kp) continue;
-    const float v = tile[tx][i];
-    if (kSplit) {
-      const float hi = tc::to_tf32(v);
-      const float lo = tc::to_tf32(v - hi);
-      static_cast<float*>(out_hi)[(int64_t)c * Kp + r] = hi;
-      static_cast<float*>(out_lo)[(int64_t)c * Kp + r] = lo;
-    } else {
-      static_cast<__nv_bfloat16*>(out_hi)[(int64_t)c * Kp + r] = __float2bfloat16_rn(v);
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {          // warp ty writes columns ty, ty + 8, ...
+    const int c = c0 + ty + 8 * cc;
+    if (c >= n) continue;
+#pragma unroll
+    for (int rr = 0; rr < kPackRows / 32; ++rr) {
+      const int64_t r = r0 + 32 * rr + tx;
+      if (r >= Kp) continue;
+      const float w = tile[32 * rr + tx][ty + 8 * cc];
+      if (kSplit) {
+        const float hi = tc::to_tf32(w);
+        static_cast<float*>(out_hi)[(int64_t)c * Kp + r] = hi;
+        static_cast<float*>(out_lo)[(int64_t)c * Kp + r] = tc::to_tf32(w - hi);
+      } else {
+        static_cast<__nv_bfloat16*>(out_hi)[(int64_t)c * Kp + r] = __float2bfloat16_rn(w);
+      }
     }
   }
 }
@@ -1015,11 +1027,11 @@ template <typename T, bool kSplit>
 __global__ void __launch_bounds__(256) pack_kernel(const T* __restrict__ x, int64_t ld, int64_t M,
                                                     int d, int n, int64_t Kp, void* out_hi,
                                                     void* out_lo) {
-  pack_tile<T, kSplit>(x, ld, M, d, n, Kp, out_hi, out_lo, (int64_t)blockIdx.x * 32,
+  pack_tile<T, kSplit>(x, ld, M, d, n, Kp, out_hi, out_lo, (int64_t)blockIdx.x * kPackRows,
                        blockIdx.y * 32);
 }
 
-// Job q owns blocks [block_start[q], block_start[q+1]): its 32 x 32 tiles,
+// Job q owns blocks [block_start[q], block_start[q+1]): its kPackRows x 32 tiles,
 // row tiles fastest (a grid sized by the largest job in each dimension would
 // schedule mostly empty blocks when the jobs differ in size).
 struct PackGroup {
@@ -1034,9 +1046,9 @@ __global__ void __launch_bounds__(256) pack_grouped_kernel(const __grid_constant
   int q = 0;
   while (q + 1 < g.count && b >= g.block_start[q + 1]) ++q;
   const PackJob J = g.job[q];
-  const int64_t local = b - g.block_start[q], rt = (J.Kp + 31) / 32;
+  const int64_t local = b - g.block_start[q], rt = (J.Kp + kPackRows - 1) / kPackRows;
   pack_tile<T, kSplit>(static_cast<const T*>(J.x), J.ld, J.M, J.d, J.n, J.Kp, J.hi, J.lo,
-                       (local % rt) * 32, (int)(local / rt) * 32);
+                       (local % rt) * kPackRows, (int)(local / rt) * 32);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1132,7 +1144,7 @@ kfac_status launch_pack_grouped(const PackJob* jobs, int count, bool bf16, cudaS
     for (int q = 0; q < cnt; ++q) {
       g.job[q] = jobs[c0 + q];
       g.block_start[q] = blocks;
-      blocks += cdiv(jobs[c0 + q].Kp, 32) * cdiv(jobs[c0 + q].n, 32);
+      blocks += cdiv(jobs[c0 + q].Kp, kPackRows) * cdiv(jobs[c0 + q].n, 32);
     }
     g.block_start[cnt] = blocks;
     g.count = cnt;
@@ -1395,7 +1407,7 @@ kfac_status launch_syrk_tc(kfac_ctx* h, int layer, const void* x, int64_t ld, in
   void* hi = h->ws + h->off_tcpack;
   void* lo = bf16 ? nullptr : (void*)(h->ws + h->off_tcpack + (size_t)n * Kp * 4);
   {
-    dim3 grid((unsigned)cdiv(Kp, 32), (unsigned)cdiv(n, 32));
+    dim3 grid((unsigned)cdiv(Kp, kPackRows), (unsigned)cdiv(n, 32));
     if (bf16)
       pack_kernel<__nv_bfloat16, false><<<grid, 256, 0, st>>>(
           static_cast<const __nv_bfloat16*>(x), ld, rows, d, n, Kp, hi, nullptr);
