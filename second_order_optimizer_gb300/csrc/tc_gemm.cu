@@ -83,6 +83,7 @@ struct GemmTcParams {
   int same_ab;           // A and B are the same operand (diagonal tiles load once)
   int splits;            // k-splits per tile = csize x groups
   int csize;             // splits per thread-block cluster, reduced through DSMEM (1: none)
+  int mc;                // cluster pairs share the B tile by TMA multicast (no split-K)
   int64_t k_per_split;   // multiple of ksub
   int ksub;              // k elements per TMEM drain (multiple of BK)
   float* part;           // this product's cluster partials [tile][groups][BM][BN]
@@ -99,6 +100,32 @@ __host__ __device__ inline int64_t upper_tile_count(int tiles_m, int tiles_n, in
   int64_t c = 0;
   for (int tj = 0; tj < tiles_n; ++tj) c += (R * tj + R < tiles_m ? R * tj + R : tiles_m);
   return c;
+}
+
+// Multicast pairs: tiles column by column, each column's tile count padded to
+// even so that a cluster pair (consecutive blocks) always shares the column tj
+// (the B tile).  A padding slot computes its partner's tile and writes nothing.
+__host__ __device__ inline int mc_column_tiles(int tiles_m, int R, bool upper, int tj) {
+  const int c = upper ? (R * tj + R < tiles_m ? R * tj + R : tiles_m) : tiles_m;
+  return c + (c & 1);
+}
+__host__ __device__ inline int64_t mc_tile_count(int tiles_m, int tiles_n, int R, bool upper) {
+  int64_t c = 0;
+  for (int tj = 0; tj < tiles_n; ++tj) c += mc_column_tiles(tiles_m, R, upper, tj);
+  return c;
+}
+__device__ __forceinline__ void mc_tile(int t, int tiles_m, int tiles_n, int R, bool upper, int* ti,
+                                        int* tj, bool* pad) {
+  int j = 0;
+  for (; j < tiles_n; ++j) {
+    const int cp = mc_column_tiles(tiles_m, R, upper, j);
+    if (t < cp) break;
+    t -= cp;
+  }
+  const int cnt = upper ? (R * j + R < tiles_m ? R * j + R : tiles_m) : tiles_m;
+  *pad = t >= cnt;
+  *ti = *pad ? cnt - 1 : t;
+  *tj = j;
 }
 
 __device__ __forceinline__ void upper_tile(int t, int tiles_m, int R, int* ti, int* tj) {
@@ -132,7 +159,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   int ti, tj;
-  if (p.upper) {
+  bool pad = false;   // multicast padding slot: computes, writes nothing
+  const int mc_rank = p.mc ? (int)(blockIdx.x & 1) : 0;
+  if (p.mc) {
+    mc_tile(tile, p.tiles_m, p.tiles_n, C::R, p.upper != 0, &ti, &tj, &pad);
+  } else if (p.upper) {
     upper_tile(tile, p.tiles_m, C::R, &ti, &tj);
   } else {
     ti = tile / p.tiles_n;
@@ -144,7 +175,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       tc::mbar_init(&full[s], 1);
-      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&empty[s], p.mc ? 2 : 1);   // multicast: both CTAs release a stage
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&acc_full[b], 1);
@@ -165,6 +196,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
   }
   tc::tc_fence_before();
   __syncthreads();
+  // multicast: the peer's barriers must be initialised before either CTA loads
+  if (p.mc) cooperative_groups::this_cluster().sync();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -187,6 +220,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
       int stage = 0;
       uint32_t phase = 0;
       const uint32_t bytes = (a_in_b ? C::B_BYTES : C::HALF_BYTES) * (kBF16 ? 1 : 2);
+      // multicast: this CTA loads half of the B tile's rows into both CTAs
+      const int b_off = mc_rank * (C::B_BYTES / 2), b_row = tj * C::BN + mc_rank * (C::BN / 2);
       for (int kb = 0; kb < nkb; ++kb) {
         if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
           *abort_flag = 1;
@@ -196,10 +231,16 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
         const int k0 = (int)(kbeg + (int64_t)kb * C::BK);
         tc::mbar_expect_tx(&full[stage], bytes);
         if (!a_in_b) tc::tma_load_2d(a_ptr(stage, 0), map_a_hi, &full[stage], k0, ti * C::BM);
-        tc::tma_load_2d(b_ptr(stage, 0), map_b_hi, &full[stage], k0, tj * C::BN);
+        if (p.mc)
+          tc::tma_load_2d_mc(b_ptr(stage, 0) + b_off, map_b_hi, &full[stage], k0, b_row, 3);
+        else
+          tc::tma_load_2d(b_ptr(stage, 0), map_b_hi, &full[stage], k0, tj * C::BN);
         if (!kBF16) {
           if (!a_in_b) tc::tma_load_2d(a_ptr(stage, 1), map_a_lo, &full[stage], k0, ti * C::BM);
-          tc::tma_load_2d(b_ptr(stage, 1), map_b_lo, &full[stage], k0, tj * C::BN);
+          if (p.mc)
+            tc::tma_load_2d_mc(b_ptr(stage, 1) + b_off, map_b_lo, &full[stage], k0, b_row, 3);
+          else
+            tc::tma_load_2d(b_ptr(stage, 1), map_b_lo, &full[stage], k0, tj * C::BN);
         }
         if (++stage == C::STAGES) {
           stage = 0;
@@ -251,7 +292,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
                             tc::sdesc_kmajor_sw128(b_hi + off), idesc, 1u);
             }
           }
-          tc::umma_commit(&empty[stage]);
+          if (p.mc)
+            tc::umma_commit_mc(&empty[stage], 3);
+          else
+            tc::umma_commit(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
@@ -318,7 +362,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
         break;
       }
       tc::tc_fence_after();
-      if (reg && sub == nsub - 1 && gr < pM) {
+      if (reg && sub == nsub - 1 && gr < pM && !pad) {
         // every MMA has completed: the stage buffers are free for the inputs
         if (EPI == TC_EPI_SYRK && E.beta != 0.f) {
 #pragma unroll 8
@@ -350,7 +394,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
       tc::tc_fence_before();
       tc::mbar_arrive(&acc_empty[buf]);
     }
-    if (reg && drained && gr < pM) {
+    if (reg && drained && gr < pM && !pad) {
       tc::cp_async_wait_all();   // this thread's own copies
       if (EPI == TC_EPI_SYRK) {
 #pragma unroll
@@ -410,6 +454,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  // multicast: every MMA of both CTAs has completed once both pass this point,
+  // so no peer load or stage release can still land in this CTA's shared memory
+  if (p.mc) {
+    cooperative_groups::this_cluster().sync();
+    if (pad) return;
+  }
   constexpr int nth = C::THREADS;
   if (reg) {
     if (EPI == TC_EPI_SYRK && !*abort_flag) {
@@ -1108,7 +1158,7 @@ kfac_status launch_kernel(unsigned grid, const CUtensorMap& ah, const CUtensorMa
                           const CUtensorMap& bh, const CUtensorMap& bl, const GemmTcParams& p,
                           cudaStream_t st) {
   if (!set_smem_attr<kBF16, BN, EPI>()) return KFAC_ERR_CUDA;
-  if (p.csize > 1) {
+  if (p.csize > 1 || p.mc) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(TcCfg<kBF16, BN>::THREADS);
@@ -1116,7 +1166,7 @@ kfac_status launch_kernel(unsigned grid, const CUtensorMap& ah, const CUtensorMa
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.csize;
+    attr[0].val.clusterDim.x = p.mc ? 2u : (unsigned)p.csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -1209,15 +1259,20 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
     return upper ? upper_tile_count(tm, tn, bn / BM) : (int64_t)tm * tn;
   };
   const int BN = ((bf16 && K >= 8192) || count(256) >= kNumSMs) ? 256 : 128;
+  // With at least a wave of tiles and no split-K, neighbouring tiles of one
+  // column run as a cluster pair that loads the shared B tile once: each CTA
+  // fetches half of its rows and multicasts them to both.
+  const bool mc = count(BN) >= kNumSMs;
+  const int b_box = mc ? BN / 2 : BN;
   CUtensorMap ah, al, bh, bl;
   if (!make_map(&ah, A.hi, bf16, A.rows, K, A.pitch, BM)) return KFAC_ERR_CUDA;
-  if (!make_map(&bh, B.hi, bf16, B.rows, K, B.pitch, BN)) return KFAC_ERR_CUDA;
+  if (!make_map(&bh, B.hi, bf16, B.rows, K, B.pitch, b_box)) return KFAC_ERR_CUDA;
   if (bf16) {
     al = ah;
     bl = bh;
   } else {
     if (!make_map(&al, A.lo, false, A.rows, K, A.pitch, BM)) return KFAC_ERR_CUDA;
-    if (!make_map(&bl, B.lo, false, B.rows, K, B.pitch, BN)) return KFAC_ERR_CUDA;
+    if (!make_map(&bl, B.lo, false, B.rows, K, B.pitch, b_box)) return KFAC_ERR_CUDA;
   }
   GemmTcParams p{};
   p.M = M;
@@ -1243,7 +1298,11 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
   p.status = h->status();
   p.layer = layer;
   p.e = e;
-  const unsigned grid = (unsigned)(tiles * p.splits);
+  unsigned grid = (unsigned)(tiles * p.splits);
+  if (mc) {   // tiles >= SMs: split_shape gave one split
+    p.mc = 1;
+    grid = (unsigned)mc_tile_count(p.tiles_m, p.tiles_n, BN / BM, upper);
+  }
   return BN == 256 ? dispatch<256>(bf16, epi, grid, ah, al, bh, bl, p, st)
                    : dispatch<128>(bf16, epi, grid, ah, al, bh, bl, p, st);
 }
