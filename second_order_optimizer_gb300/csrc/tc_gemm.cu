@@ -1288,7 +1288,26 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
   const int64_t max_groups =
       std::max<int64_t>(1, std::min<int64_t>((int64_t)(h->part_floats / ((size_t)tiles * BM * BN)),
                                              (int64_t)(h->n_tickets / ((size_t)tiles * 8))));
-  const SplitShape sh = split_shape(std::max<int64_t>(1, kNumSMs / tiles), K, unit, max_groups);
+  // Fewer tiles than SMs: the split count minimising wave-quantised time,
+  // ceil(tiles s / SMs) x (1/s + c0), where c0 is a CTA's fixed cost (prologue,
+  // epilogue, reduction: ~8 us measured) relative to the tile's whole main loop
+  // at the tensor rate of one SM.
+  int64_t want = 1;
+  if (tiles < kNumSMs) {
+    const double sm_rate = (bf16 ? 2.25e15 : 1.1e15 / 3.0) / kNumSMs;   // flop/s per SM
+    const double t_tile = 2.0 * BM * BN * (double)K / sm_rate;          // seconds
+    const double c0 = 8e-6 / t_tile;
+    double best = 1.0 + c0;
+    const int64_t smax = std::max<int64_t>(1, std::min<int64_t>(K / 256, 4 * kNumSMs));
+    for (int64_t sp = 2; sp <= smax; ++sp) {
+      const double cost = (double)cdiv(tiles * sp, kNumSMs) * (1.0 / (double)sp + c0);
+      if (cost < best - 1e-12) {
+        best = cost;
+        want = sp;
+      }
+    }
+  }
+  const SplitShape sh = split_shape(want, K, unit, max_groups);
   p.splits = sh.splits;
   p.csize = sh.csize;
   p.k_per_split = sh.kps;
