@@ -27,6 +27,7 @@
 #include "tc_prims.cuh"
 
 #include <algorithm>
+#include <cstring>
 #include <vector>
 
 namespace kfac {
@@ -34,6 +35,8 @@ namespace kfac {
 namespace {
 
 constexpr int NB = 64;
+constexpr int kOuterW = 512;      // outer panel width of the two-level Cholesky
+constexpr int kOuterMaxN = 1536;  // handles whose factors are all this small stay one panel
 using PTile = SimtTile<64, 64, 16, 4, 4>;   // 256 threads
 
 __global__ void __launch_bounds__(256) inv_prep_kernel(const InvJob* jobs, float sqrt_gamma) {
@@ -42,10 +45,9 @@ __global__ void __launch_bounds__(256) inv_prep_kernel(const InvJob* jobs, float
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
        e += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = e / J.n, c = e % J.n;
-    float v = 0.f;
-    if (r > c) v = J.F[e];
-    else if (r == c) v = J.F[e] + sqrt_gamma;
-    J.L[e] = v;
+    // both triangles (F is symmetric): the tensor-core trailing updates of large
+    // factors read either triangle and keep the trailing block symmetric
+    J.L[e] = r == c ? J.F[e] + sqrt_gamma : J.F[e];
     J.X[e] = 0.f;
   }
 }
@@ -240,28 +242,34 @@ __device__ __forceinline__ void lower_tile_coords(int t, int* ti, int* tj) {
 }
 
 // L[i][j] -= sum_t L[i][k+t] L[j][k+t] over the trailing lower tiles (ti >= tj,
-// counted from the first trailing block).  part: 0 all tiles; 1 the first block
-// column only (tj = 0: what the next diagonal block and panel need); 2 the rest
-// (tj >= 1), which may run alongside the next diagonal block and panel.
-__global__ void __launch_bounds__(256) chol_trailing_kernel(const InvJob* jobs, int k, int part) {
+// counted from the first trailing block), for block columns below `cend` (the
+// end of the current outer panel; the tensor cores update the rest).  part: 1
+// the first block column only (tj = 0: what the next diagonal block and panel
+// need); 2 the others (tj >= 1), which may run alongside the next diagonal
+// block and panel.
+__global__ void __launch_bounds__(256) chol_trailing_kernel(const InvJob* jobs, int k, int part,
+                                                            int cend) {
   const InvJob J = jobs[blockIdx.y];
   const int n = J.n;
   const int64_t base = (int64_t)k + NB;
   if (base >= n) return;
   const int nt = (int)((n - base + 63) / 64);
+  const int nc = min(nt, (int)((min(cend, n) - base + 63) / 64));   // block columns to update
+  if (nc <= 0) return;
   int ti, tj;
   if (part == 1) {
     if ((int)blockIdx.x >= nt) return;
     ti = blockIdx.x;
     tj = 0;
-  } else if (part == 2) {
-    if ((int)blockIdx.x >= (nt - 1) * nt / 2) return;
-    lower_tile_coords(blockIdx.x, &ti, &tj);
-    ++ti;
-    ++tj;
   } else {
-    if ((int)blockIdx.x >= nt * (nt + 1) / 2) return;
-    lower_tile_coords(blockIdx.x, &ti, &tj);
+    int t = blockIdx.x, j = 1;
+    for (; j < nc; ++j) {
+      if (t < nt - j) break;
+      t -= nt - j;
+    }
+    if (j >= nc) return;
+    tj = j;
+    ti = j + t;
   }
   __shared__ float smem[PTile::kSmemFloats];
   float acc[4][4] = {};
@@ -342,6 +350,34 @@ __global__ void __launch_bounds__(256) tri_level_x_kernel(const InvJob* jobs, in
     }
 }
 
+// Outer-panel operand for the tensor-core trailing update: the panel's rows
+// below it, P = L[cend:, K0:K0+W], already K-major (rows of L), split into TF32
+// halves with pitch W.
+struct PanelPack {
+  const float* src;
+  int64_t ld, rows;
+  float* hi;
+  float* lo;
+};
+constexpr int kMaxPanelPacks = 32;
+struct PanelPackGroup {
+  PanelPack job[kMaxPanelPacks];
+  int count, W;
+};
+
+__global__ void __launch_bounds__(256) panel_split_kernel(const __grid_constant__ PanelPackGroup g) {
+  const PanelPack P = g.job[blockIdx.y];
+  const int64_t total = P.rows * g.W;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / g.W, c = e % g.W;
+    const float v = P.src[r * P.ld + c];
+    const float hi = tc::to_tf32(v);
+    P.hi[e] = hi;
+    P.lo[e] = tc::to_tf32(v - hi);
+  }
+}
+
 // Finv -> TF32 halves with a 16-byte row pitch, the operand form of the K4 products.
 __global__ void __launch_bounds__(256) inv_split_kernel(const InvJob* jobs) {
   const InvJob J = jobs[blockIdx.y];
@@ -371,6 +407,67 @@ int level_tiles_host(int n, int s) {
 
 size_t inv_y_floats(int n) { return (size_t)n * n; }
 
+// L22 <- L22 - P P^T for every factor whose size reaches past the outer panel
+// [K0, K0 + W): P = L[K0 + W :, K0 : K0 + W] split into TF32 halves, then one
+// grouped 3xTF32 SYRK (upper tiles + mirror; the trailing block is kept
+// symmetric, so either triangle holds the old values).  Groups are cut where
+// the pack scratch is full.
+kfac_status launch_outer_update(kfac_ctx* h, int j0, int nj, int K0, int W, cudaStream_t st) {
+  const int cend = K0 + W;
+  PanelPackGroup pg;
+  std::memset(&pg, 0, sizeof(pg));
+  pg.W = W;
+  std::vector<TcProblem> pr;
+  size_t used = 0;
+  int64_t max_elems = 0;
+  auto flush = [&]() -> kfac_status {
+    if (pr.empty()) return KFAC_OK;
+    const unsigned blocks = (unsigned)std::min<int64_t>(cdiv(max_elems, 256), 4 * kNumSMs);
+    panel_split_kernel<<<dim3(blocks, pg.count), 256, 0, st>>>(pg);
+    count_launch();
+    kfac_status e = check_launch();
+    if (e == KFAC_OK) e = launch_gemm_tc_grouped(h, false, TC_EPI_SYRK, pr.data(), (int)pr.size(), st);
+    pr.clear();
+    pg.count = 0;
+    used = 0;
+    max_elems = 0;
+    return e;
+  };
+  for (int i = j0; i < j0 + nj; ++i) {
+    const InvJob& J = h->invjobs_host[i];
+    if (J.n <= cend) continue;
+    const int64_t m = J.n - cend;
+    const size_t raw = (size_t)m * W * 8, bytes = align_up(raw);
+    if (raw > h->tcpack_bytes) return KFAC_ERR_WORKSPACE;
+    if (used + raw > h->tcpack_bytes || pg.count == kMaxPanelPacks)
+      if (kfac_status e = flush()) return e;
+    float* hi = reinterpret_cast<float*>(h->ws + h->off_tcpack + used);
+    float* lo = hi + (size_t)m * W;
+    used += bytes;
+    PanelPack& pp = pg.job[pg.count++];
+    pp.src = J.L + (int64_t)cend * J.n + K0;
+    pp.ld = J.n;
+    pp.rows = m;
+    pp.hi = hi;
+    pp.lo = lo;
+    max_elems = std::max<int64_t>(max_elems, m * W);
+    TcProblem t{};
+    t.A = TcOperand{hi, lo, m, W};
+    t.B = t.A;
+    t.same_ab = true;
+    t.upper = true;
+    t.M = t.N = m;
+    t.K = W;
+    t.e.alpha = -1.f;
+    t.e.beta = 1.f;
+    t.e.C = J.L + (int64_t)cend * J.n + cend;
+    t.e.ldc = J.n;
+    t.layer = J.layer;
+    pr.push_back(t);
+  }
+  return flush();
+}
+
 kfac_status launch_invert(kfac_ctx* h, int layer, cudaStream_t st) {
   // job range: all KRON factors, or the two of one layer
   const InvJob* d_all = h->at<InvJob>(h->off_invjobs);
@@ -396,42 +493,61 @@ kfac_status launch_invert(kfac_ctx* h, int layer, cudaStream_t st) {
   count_launch();
   if (kfac_status e = check_launch()) return e;
 
-  // Cholesky with one block of lookahead: after the panel of step k, the
-  // trailing update of the next block column runs on the caller's stream (the
-  // next diagonal block needs it), the rest on the side stream, concurrently
-  // with the next diagonal block and panel.  Events: the side stream waits for
-  // each panel; the next block column's update waits for the previous rest,
-  // which also writes that column.
+  // Cholesky in outer panels of kOuterW columns (the whole matrix when every
+  // factor is at most kOuterMaxN): inside a panel, 64-column steps with one
+  // block of lookahead -- after the panel of step k, the trailing update of the
+  // next block column runs on the caller's stream (the next diagonal block
+  // needs it), the panel's other columns on the side stream, concurrently with
+  // the next diagonal block and panel (events: the side stream waits for each
+  // panel; the next block column's update waits for the previous side work,
+  // which also writes that column).  After each outer panel the tensor cores
+  // update the whole trailing block with it: L22 <- L22 - P P^T, K = kOuterW.
   bool rest_pending = false;
   auto sync_err = [](cudaError_t e) { return e == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA; };
-  for (int k = 0; k < nmax; k += NB) {
-    chol_diag_kernel<<<nj, 256, 0, st>>>(jobs, k, h->status());
-    count_launch();
-    const int rest = nmax - k - NB;
-    if (rest > 0) {
-      const int rb = (int)cdiv(rest, 64);
-      chol_panel_kernel<<<dim3(rb, nj), 256, 0, st>>>(jobs, k);
+  auto join_side = [&]() -> kfac_status {
+    if (!rest_pending) return KFAC_OK;
+    rest_pending = false;
+    return sync_err(cudaStreamWaitEvent(st, h->ev_rest, 0));
+  };
+  const int W = nmax > kOuterMaxN ? kOuterW : (int)cdiv(nmax, NB) * NB;
+  for (int K0 = 0; K0 < nmax; K0 += W) {
+    const int cend = K0 + W;
+    for (int k = K0; k < std::min(cend, nmax); k += NB) {
+      chol_diag_kernel<<<nj, 256, 0, st>>>(jobs, k, h->status());
       count_launch();
-      if (rb > 1) {
-        if (kfac_status e = sync_err(cudaEventRecord(h->ev_panel, st))) return e;
-        if (kfac_status e = sync_err(cudaStreamWaitEvent(h->side_stream, h->ev_panel, 0))) return e;
-      }
-      if (rest_pending)
-        if (kfac_status e = sync_err(cudaStreamWaitEvent(st, h->ev_rest, 0))) return e;
-      chol_trailing_kernel<<<dim3(rb, nj), 256, 0, st>>>(jobs, k, 1);
-      count_launch();
-      rest_pending = false;
-      if (rb > 1) {
-        chol_trailing_kernel<<<dim3((rb - 1) * rb / 2, nj), 256, 0, h->side_stream>>>(jobs, k, 2);
+      const int rest = nmax - k - NB;
+      if (rest > 0) {
+        const int rb = (int)cdiv(rest, 64);
+        chol_panel_kernel<<<dim3(rb, nj), 256, 0, st>>>(jobs, k);
         count_launch();
-        if (kfac_status e = sync_err(cudaEventRecord(h->ev_rest, h->side_stream))) return e;
-        rest_pending = true;
+        const int nc = (int)std::min<int64_t>(rb, cdiv(std::min(cend, nmax) - (k + NB), 64));
+        if (nc > 1) {
+          if (kfac_status e = sync_err(cudaEventRecord(h->ev_panel, st))) return e;
+          if (kfac_status e = sync_err(cudaStreamWaitEvent(h->side_stream, h->ev_panel, 0))) return e;
+        }
+        if (nc >= 1) {
+          if (kfac_status e = join_side()) return e;
+          chol_trailing_kernel<<<dim3(rb, nj), 256, 0, st>>>(jobs, k, 1, cend);
+          count_launch();
+        }
+        if (nc > 1) {
+          int64_t tiles = 0;
+          for (int j = 1; j < nc; ++j) tiles += rb - j;
+          chol_trailing_kernel<<<dim3((unsigned)tiles, nj), 256, 0, h->side_stream>>>(jobs, k, 2,
+                                                                                      cend);
+          count_launch();
+          if (kfac_status e = sync_err(cudaEventRecord(h->ev_rest, h->side_stream))) return e;
+          rest_pending = true;
+        }
       }
+      if (kfac_status e = check_launch()) return e;
     }
-    if (kfac_status e = check_launch()) return e;
+    if (cend < nmax) {
+      if (kfac_status e = join_side()) return e;
+      if (kfac_status e = launch_outer_update(h, j0, nj, K0, W, st)) return e;
+    }
   }
-  if (rest_pending)
-    if (kfac_status e = sync_err(cudaStreamWaitEvent(st, h->ev_rest, 0))) return e;
+  if (kfac_status e = join_side()) return e;
   for (int s = NB; s < nmax; s *= 2) {
     const int tiles = level_tiles_host(nmax, s);
     int tmax = tiles;
