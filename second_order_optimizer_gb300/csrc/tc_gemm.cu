@@ -1381,6 +1381,23 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
   constexpr int BM = 128, BN = 128;
   constexpr size_t NT = (size_t)BM * BN;
   const int unit = bf16 ? kKsubBf16 : kKsubTf32;
+  // A product that fills a wave of 128 x 256 tiles by itself runs on its own
+  // (wide tiles, multicast pairs); the rest share grouped launches.
+  std::vector<TcProblem> small;
+  for (int q = 0; q < count; ++q) {
+    const TcProblem& pr = probs[q];
+    const int tm = (int)cdiv(pr.M, BM), tn = (int)cdiv(pr.N, 256);
+    const int64_t wide = pr.upper ? upper_tile_count(tm, tn, 2) : (int64_t)tm * tn;
+    if (wide >= kNumSMs) {
+      if (kfac_status e = launch_gemm_tc(h, pr.layer, bf16, epi, pr.A, pr.B, pr.same_ab, pr.upper,
+                                         pr.M, pr.N, pr.K, pr.e, st))
+        return e;
+    } else {
+      small.push_back(pr);
+    }
+  }
+  if (small.empty()) return KFAC_OK;
+  if ((int)small.size() < count) return launch_gemm_tc_grouped(h, bf16, epi, small.data(), (int)small.size(), st);
   std::vector<int64_t> tiles(count), want(count);
   int64_t total_units = 0;
   for (int q = 0; q < count; ++q) {
