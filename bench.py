@@ -482,7 +482,8 @@ def run_gpu(args, rank, world, peaks, peak_kind):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, layers, data[0], params_flat, srcidx, t, dev, step)
+        e2e = run_e2e(args, layers, data[0], params_flat, srcidx, t, dev,
+                      (phase_factor, phase_invert, phase_precond, phase_diag), k)
     return {
         "ms_per_step": ms_step, "phases": phases, "roofline": roof, "clocks": clocks,
         "gpu_launches": int(launches), "wall_s": wall, "e2e": e2e,
@@ -495,12 +496,15 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     }
 
 
-def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, step):
+def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k):
     """Same step through the public API from pinned host memory: every step copies its
     inputs host -> device and reads every updated parameter back, inside the timed
     region.  The inputs of all layers are one packed pinned buffer (a diagonal twin
     shares its layer's tensors, so they are copied once), double-buffered on the
-    device: the next step's copy runs on a copy stream while this step computes."""
+    device: the next step's copy runs on a copy stream while this step computes.
+    The parameter read-back also runs on the copy stream; the next step's factor
+    update (and refresh) overlap it, and its parameter updates wait for it."""
+    phase_factor, phase_invert, phase_precond, phase_diag = phases
     import torch
     first = {}
     for li in range(len(layers)):
@@ -534,6 +538,7 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, step):
     copy = torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event(), torch.cuda.Event()]
     ev_used = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_done, ev_out = torch.cuda.Event(), torch.cuda.Event()
     steps = max(3, min(args.steps, 20))
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -551,14 +556,25 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, step):
                     copy.wait_event(ev_used[nb_])   # the step that read that buffer is done
                 stage[nb_].copy_(host, non_blocking=True)
                 ev_in[nb_].record(copy)
-        step(t, xs[b])
+        x = xs[b]
+        phase_factor(x)
+        if (t - 1) % k == 0:
+            phase_invert()
+        if i >= 1:
+            main.wait_event(ev_out)            # previous step's parameters are read back
+        phase_precond(x)
+        phase_diag(x)
         ev_used[b].record(main)
-        outs.copy_(params_flat, non_blocking=True)
+        ev_done.record(main)
+        with torch.cuda.stream(copy):
+            copy.wait_event(ev_done)
+            outs.copy_(params_flat, non_blocking=True)
+            ev_out.record(copy)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
     return {"value": round(1.0 / dt, 3), "unit": "steps/s", "h2d_bytes_per_step": int(total),
             "d2h_bytes_per_step": int(params_flat.numel() * 4), "steps": steps,
-            "pipelined": "next step's H2D overlaps this step's compute (copy stream, double buffer)"}
+            "pipelined": "copy stream: next step H2D during this step, parameter D2H during the next factor update"}
 
 
 # ----------------------------------------------------------------------------- micro
