@@ -210,15 +210,25 @@ __device__ __forceinline__ void diag_factor_body(const DiagFactorParams& p, int 
     const T* base = c < p.d_in ? static_cast<const T*>(p.a) + c
                                : static_cast<const T*>(p.g) + (c - p.d_in);
     const int64_t ld = c < p.d_in ? p.lda : p.ldg;
-    // compensated (Kahan) sum: the kernel is bound by HBM, the extra flops are free
+    // compensated (Kahan) sum: the kernel is bound by HBM, the extra flops are free.
+    // Rows in batches of 8: the loads of a batch are independent and issue
+    // together; the compensated adds then run in row order.
     float acc = 0.f, comp = 0.f;
-    for (int64_t r = r0; r < r1; ++r) {
-      const float v = to_f32<T>(base[r * ld]);
+    auto kahan = [&](float v) {
       const float y = fmaf(v, v, -comp);
       const float t = acc + y;
       comp = (t - acc) - y;
       acc = t;
+    };
+    int64_t r = r0;
+    for (; r + 8 <= r1; r += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = to_f32<T>(base[(r + u) * ld]);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) kahan(v[u]);
     }
+    for (; r < r1; ++r) kahan(to_f32<T>(base[r * ld]));
     p.part[(size_t)split * ncols + c] = acc;
   }
   __shared__ int s_last;
