@@ -72,6 +72,37 @@ constexpr int SB = 16;       // sub-panel width
 constexpr int AP = NB + 1;   // shared row pitch (floats)
 constexpr unsigned kFull = 0xffffffffu;
 
+// One doubling level of the 64 x 64 block inverse: for the pairs (T, B) of
+// size SZ, X_BT = -X_BB (L_BT X_TT).  The triangular operands hold exact zeros
+// outside their triangles, so every sum runs over the whole block length (same
+// nonzero terms in the same order) with fixed trip counts the compiler unrolls.
+template <int SZ>
+__device__ __forceinline__ void diag_inverse_level(const float* A, float* X, float* Y, int tid) {
+  constexpr int PER = (NB / (2 * SZ)) * SZ * SZ / 256;   // outputs per thread
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int e = tid + 256 * u;
+    const int pr = e / (SZ * SZ), i = (e / SZ) % SZ, c = e % SZ;
+    const int T0 = pr * 2 * SZ, B0 = T0 + SZ;
+    float acc = 0.f;
+#pragma unroll
+    for (int m = 0; m < SZ; ++m) acc = fmaf(A[(B0 + i) * AP + T0 + m], X[(T0 + m) * AP + T0 + c], acc);
+    Y[(pr * SZ + i) * 33 + c] = acc;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int e = tid + 256 * u;
+    const int pr = e / (SZ * SZ), i = (e / SZ) % SZ, c = e % SZ;
+    const int T0 = pr * 2 * SZ, B0 = T0 + SZ;
+    float acc = 0.f;
+#pragma unroll
+    for (int m = 0; m < SZ; ++m) acc = fmaf(X[(B0 + i) * AP + B0 + m], Y[(pr * SZ + m) * 33 + c], acc);
+    X[(B0 + i) * AP + T0 + c] = -acc;
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int k,
                                                         DevStatus* st) {
   const InvJob J = jobs[blockIdx.x];
@@ -177,26 +208,9 @@ __global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int 
       __syncthreads();
     }
   }
-  // X off-diagonal blocks: pairs (T, B) of size sz, X_BT = -X_BB (L_BT X_TT)
-  for (int sz = SB; sz < NB; sz *= 2) {
-    const int ne = (NB / (2 * sz)) * sz * sz;
-    for (int e = tid; e < ne; e += 256) {
-      const int pr = e / (sz * sz), i = (e / sz) % sz, c = e % sz;
-      const int T0 = pr * 2 * sz, B0 = T0 + sz;
-      float acc = 0.f;
-      for (int m = c; m < sz; ++m) acc = fmaf(A[(B0 + i) * AP + T0 + m], X[(T0 + m) * AP + T0 + c], acc);
-      Y[(pr * sz + i) * 33 + c] = acc;
-    }
-    __syncthreads();
-    for (int e = tid; e < ne; e += 256) {
-      const int pr = e / (sz * sz), i = (e / sz) % sz, c = e % sz;
-      const int T0 = pr * 2 * sz, B0 = T0 + sz;
-      float acc = 0.f;
-      for (int m = 0; m <= i; ++m) acc = fmaf(X[(B0 + i) * AP + B0 + m], Y[(pr * sz + m) * 33 + c], acc);
-      X[(B0 + i) * AP + T0 + c] = -acc;
-    }
-    __syncthreads();
-  }
+  // X off-diagonal blocks: pairs (T, B) of size 16, then 32
+  diag_inverse_level<SB>(A, X, Y, tid);
+  diag_inverse_level<2 * SB>(A, X, Y, tid);
 #pragma unroll 4
   for (int e = tid; e < b * b; e += 256) {
     const int r = e / b, c = e % b;
