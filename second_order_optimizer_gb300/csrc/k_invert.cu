@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(256) chol_panel_kernel(const InvJob* jobs, int
   float acc[4][4] = {};
   StridedLoader la{J.L + k, n, 1, n, b};                       // (r, t) -> L[r][k+t]
   StridedLoader lb{J.X + (int64_t)k * n + k, 1, n, b, b};      // (t, c) -> X[k+c][k+t]
-  PTile::run(la, lb, r0, 0, 0, b, acc, smem);
+  PTile::run<true, true>(la, lb, r0, 0, 0, b, acc, smem);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(256) chol_trailing_kernel(const InvJob* jobs, 
   float acc[4][4] = {};
   StridedLoader la{J.L + k, n, 1, n, NB};   // (i, t) -> L[i][k+t]
   StridedLoader lb{J.L + k, 1, n, NB, n};   // (t, j) -> L[j][k+t]
-  PTile::run(la, lb, base + ti * 64, base + tj * 64, 0, NB, acc, smem);
+  PTile::run<true, true>(la, lb, base + ti * 64, base + tj * 64, 0, NB, acc, smem);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(256) tri_level_y_kernel(const InvJob* jobs, in
   StridedLoader la{J.L, n, 1, B1, T0 + s};   // (r, t) -> L[r][t]
   StridedLoader lb{J.X, n, 1, T0 + s, T0 + s};  // (t, c) -> X[t][c]
   const int64_t m0 = B0 + tr * 64, c0 = T0 + tc * 64;
-  PTile::run(la, lb, m0, c0, c0, T0 + s, acc, smem);
+  PTile::run<true, false>(la, lb, m0, c0, c0, T0 + s, acc, smem);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(256) tri_level_x_kernel(const InvJob* jobs, in
   StridedLoader lb{J.Y, n, 1, B1, T0 + s};  // (t, c) -> Y[t][c]
   const int64_t m0 = B0 + tr * 64, c0 = T0 + tc * 64;
   const int64_t k1 = m0 + 64 < (int64_t)B1 ? m0 + 64 : (int64_t)B1;
-  PTile::run(la, lb, m0, c0, B0, k1, acc, smem);
+  PTile::run<true, false>(la, lb, m0, c0, B0, k1, acc, smem);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
