@@ -37,7 +37,7 @@ namespace {
 constexpr int NB = 64;
 constexpr int kOuterW = 512;      // outer panel width of the two-level Cholesky
 constexpr int kOuterMaxN = 1536;  // handles whose factors are all this small stay one panel
-using PTile = SimtTile<64, 64, 16, 4, 4>;   // 256 threads
+using PTile = SimtTile<64, 64, 32, 4, 4>;   // 256 threads, 32-deep k chunks
 
 __global__ void __launch_bounds__(256) inv_prep_kernel(const InvJob* jobs, float sqrt_gamma) {
   const InvJob J = jobs[blockIdx.y];
