@@ -32,8 +32,16 @@
  *     Errors found on the device (a non positive-definite pivot, a pipeline
  *     wait that timed out) are recorded in a device status word and reported by
  *     kfac_get_status().  NaN inputs propagate; they are not checked.
- *   - A handle is not thread-safe.  Calls on one handle must be ordered (same
- *     stream, or streams the caller orders).
+ *   - A handle is not thread-safe: its calls are issued from one thread.
+ *     On the device, calls on one handle must be ordered (same stream, or
+ *     streams the caller orders), with one exception: the factor update
+ *     (kfac_update_factors*), the preconditioning (kfac_precondition*) and
+ *     the diagonal path (kfac_diag_factors*, kfac_diag_step*) use disjoint
+ *     scratch and may overlap each other on different streams, as long as
+ *     each touches different state (a layer's factors are read only by
+ *     kfac_invert; preconditioning reads the inverses).  kfac_invert must not
+ *     overlap any other call on the handle: it reads the factors and writes
+ *     the inverses and shares the factor update's scratch.
  */
 #ifndef KFAC_H
 #define KFAC_H

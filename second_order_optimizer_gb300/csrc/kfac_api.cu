@@ -39,6 +39,7 @@ bool valid_desc(const kfac_layer_desc& d) {
 struct Plan {
   std::vector<LayerInfo> layers;
   size_t off_status, off_part, part_floats, off_tickets, n_tickets, off_k4tmp, k4tmp_floats;
+  size_t off_part_k4, off_tickets_k4;
   size_t off_k5part, k5part_floats, off_k5tickets, k5tickets_ints, off_invjobs, total;
   size_t off_tcpack, tcpack_bytes;
   int n_invjobs, max_kron_n;
@@ -125,6 +126,8 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
   P->off_part = take(part * sizeof(float));
   P->n_tickets = tickets;
   P->off_tickets = take(tickets * sizeof(int));
+  P->off_part_k4 = take(part * sizeof(float));
+  P->off_tickets_k4 = take(tickets * sizeof(int));
   P->tcpack_bytes = tcpack;
   P->off_tcpack = take(tcpack);
   P->k4tmp_floats = k4;
@@ -229,6 +232,8 @@ kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_
   h->part_floats = P.part_floats;
   h->off_tickets = P.off_tickets;
   h->n_tickets = P.n_tickets;
+  h->off_part_k4 = P.off_part_k4;
+  h->off_tickets_k4 = P.off_tickets_k4;
   h->off_tcpack = P.off_tcpack;
   h->tcpack_bytes = P.tcpack_bytes;
   h->off_k4tmp = P.off_k4tmp;

@@ -76,6 +76,9 @@ struct kfac_ctx {
   // K1 split-K scratch
   size_t off_part = 0, part_floats = 0;
   size_t off_tickets = 0, n_tickets = 0;
+  // the same again for the preconditioning products (SPLIT / PRECOND epilogues),
+  // so factor updates and preconditioning may run concurrently on two streams
+  size_t off_part_k4 = 0, off_tickets_k4 = 0;
   // K1 tensor-core operand pack (X = x-hat^T, TF32 halves or bf16)
   size_t off_tcpack = 0, tcpack_bytes = 0;
   // K4 scratch: dW-hat halves [o x n_p] x2, then X^T halves [n x o_p] x2

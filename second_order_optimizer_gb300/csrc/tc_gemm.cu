@@ -1312,8 +1312,8 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
   p.csize = sh.csize;
   p.k_per_split = sh.kps;
   p.ksub = unit;
-  p.part = h->at<float>(h->off_part);
-  p.tickets = h->at<int>(h->off_tickets);
+  p.part = h->at<float>(epi == TC_EPI_SYRK ? h->off_part : h->off_part_k4);
+  p.tickets = h->at<int>(epi == TC_EPI_SYRK ? h->off_tickets : h->off_tickets_k4);
   p.status = h->status();
   p.layer = layer;
   p.e = e;
@@ -1476,8 +1476,8 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
       pp.csize = sh.csize;
       pp.k_per_split = sh.kps;
       pp.ksub = unit;
-      pp.part = h->at<float>(h->off_part) + part_used;
-      pp.tickets = h->at<int>(h->off_tickets) + tick_used;
+      pp.part = h->at<float>(epi == TC_EPI_SYRK ? h->off_part : h->off_part_k4) + part_used;
+      pp.tickets = h->at<int>(epi == TC_EPI_SYRK ? h->off_tickets : h->off_tickets_k4) + tick_used;
       pp.status = h->status();
       pp.layer = pr.layer;
       pp.e = pr.e;
