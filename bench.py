@@ -519,7 +519,7 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, layers, data[0], params_flat, srcidx, t, dev,
-                      (phase_factor, phase_invert, phase_precond, phase_diag), k)
+                      (phase_factor, phase_invert, phase_precond, phase_diag), k, overlap)
     return {
         "ms_per_step": ms_step, "phases": phases, "roofline": roof, "clocks": clocks,
         "gpu_launches": int(launches), "wall_s": wall, "e2e": e2e,
@@ -535,14 +535,16 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     }
 
 
-def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k):
+def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap):
     """Same step through the public API from pinned host memory: every step copies its
     inputs host -> device and reads every updated parameter back, inside the timed
     region.  The inputs of all layers are one packed pinned buffer (a diagonal twin
     shares its layer's tensors, so they are copied once), double-buffered on the
     device: the next step's copy runs on a copy stream while this step computes.
     The parameter read-back also runs on the copy stream; the next step's factor
-    update (and refresh) overlap it, and its parameter updates wait for it."""
+    update (and refresh) overlap it, and its parameter updates wait for it.  On
+    steps without a refresh the factor update runs on a side stream alongside
+    the preconditioning and the diagonal step (as in the timed steps)."""
     phase_factor, phase_invert, phase_precond, phase_diag = phases
     import torch
     first = {}
@@ -578,6 +580,8 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k):
     ev_in = [torch.cuda.Event(), torch.cuda.Event()]
     ev_used = [torch.cuda.Event(), torch.cuda.Event()]
     ev_done, ev_out = torch.cuda.Event(), torch.cuda.Event()
+    fside = torch.cuda.Stream(dev)
+    ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
     steps = max(3, min(args.steps, 20))
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -596,13 +600,22 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k):
                 stage[nb_].copy_(host, non_blocking=True)
                 ev_in[nb_].record(copy)
         x = xs[b]
-        phase_factor(x)
-        if (t - 1) % k == 0:
-            phase_invert()
+        if overlap and (t - 1) % k != 0:       # factor update alongside the rest
+            ev_fork.record(main)
+            fside.wait_event(ev_fork)
+            with torch.cuda.stream(fside):
+                phase_factor(x)
+                ev_join.record(fside)
+        else:
+            phase_factor(x)
+            if (t - 1) % k == 0:
+                phase_invert()
         if i >= 1:
             main.wait_event(ev_out)            # previous step's parameters are read back
         phase_precond(x)
         phase_diag(x)
+        if overlap and (t - 1) % k != 0:
+            main.wait_event(ev_join)
         ev_used[b].record(main)
         ev_done.record(main)
         with torch.cuda.stream(copy):
