@@ -35,6 +35,29 @@ WORKLOADS = {"mlp4": "c2", "single_linear": "c1", "resnet18": "c3", "resnet50": 
 # fallback roofline denominators when MEASURED_PEAKS.json is absent
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TF32_PER_BF16 = 1.1 / 2.25          # nominal dense ratio
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of each phase's
+# launches in one step of the mlp4 workload, from one ncu capture of
+#   python bench.py --steps 2 --warmup 1 --no-e2e --no-cpu-baseline --no-overlap
+# (the last timed step's graph replay; ncu does not count writes that are still in
+# L2 when a kernel ends).  Valid only for the kernel sources with this digest: any
+# change to them reports null until the counters are taken again.
+MEASURED_TRAFFIC = {
+    "workload": "mlp4",
+    "sources_sha256": "5331a9eb514562ed9943b463e5234b9818dbb30c0b099edf0ff11b7d84eb5ab9",
+    "bytes": {"factor": 105.13e6, "precond": 148.66e6, "diag": 68.09e6},
+}
+
+
+def sources_digest() -> str:
+    import hashlib
+    d = os.path.join(ROOT, "second_order_optimizer_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(f.encode())
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # FFMA lanes x 2 flop x max SM clock
 
 
@@ -510,6 +533,12 @@ def run_gpu(args, rank, world, peaks, peak_kind):
                 "unit": "TFLOP/s", "kernel": "chol_diag/chol_panel/chol_trailing/tri_level"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = None
+    if (args.workload == MEASURED_TRAFFIC["workload"] and dom in MEASURED_TRAFFIC["bytes"]
+            and sources_digest() == MEASURED_TRAFFIC["sources_sha256"]):
+        roof["traffic"] = MEASURED_TRAFFIC["bytes"][dom]
+        roof["traffic_note"] = "DRAM bytes per step of the phase's launches (ncu, same sources)"
+        if dom == "precond":
+            roof["algorithmic_bytes"] = acc.get("precond_bytes")
     roof["phase"] = dom
     roof["peak_source"] = {
         "hbm": f"{peak_kind} HBM copy bandwidth",
