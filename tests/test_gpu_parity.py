@@ -514,3 +514,49 @@ def test_batched_diag_calls_reject_duplicates_and_wrong_kinds():
         h.diag_step_batched([0, 1], [v8, v8], [v9, v9], [w, w], [v8, v8], [w, w], [v8, v8])
     with pytest.raises(K.KfacError):
         h.diag_step_batched([0, 0], [v8, v8], [v9, v9], [w, w], [v8, v8], [w, w], [v8, v8])
+
+
+def test_factor_update_concurrent_with_preconditioning_and_diag_step():
+    """The factor update, preconditioning and the diagonal path use disjoint scratch:
+    run on two streams at once they leave exactly the state of running them in order
+    (split-K products included: a wide, short layer forces them in both phases)."""
+    descs = [(K.KFAC_KRON, 64, 700, 1, K.KFAC_F32), (K.KFAC_KRON, 300, 200, 1, K.KFAC_F32),
+             (K.KFAC_DIAG, 96, 128, 1, K.KFAC_F32)]
+    M = 4096
+    hs = [K.Kfac(descs, max_rows=M, **HP) for _ in range(2)]
+    ins = [_inputs(M, d, o) for (_, o, d, b, _) in descs]
+    a_l = [to_dev(a) for a, _ in ins]
+    g_l = [to_dev(g) for _, g in ins]
+    for h in hs:
+        h.update_factors_batched([0, 1], a_l[:2], g_l[:2])
+        h.invert(-1)
+    gws = [to_dev((RNG.standard_normal((o, d)) * 1e-3).astype(np.float32)) for (_, o, d, b, _) in descs]
+    gbs = [to_dev((RNG.standard_normal(o) * 1e-3).astype(np.float32)) for (_, o, d, b, _) in descs]
+    w0 = [(RNG.standard_normal((o, d)) * 0.1).astype(np.float32) for (_, o, d, b, _) in descs]
+    b0 = [(RNG.standard_normal(o) * 0.1).astype(np.float32) for (_, o, d, b, _) in descs]
+    pw = [[to_dev(w) for w in w0] for _ in range(2)]
+    pb = [[to_dev(x) for x in b0] for _ in range(2)]
+    gn = to_dev(RNG.uniform(0, 1e-6, 96).astype(np.float32))
+    an = to_dev(RNG.uniform(0, 2, 129).astype(np.float32))
+    # in order, one stream
+    h = hs[0]
+    h.update_factors_batched([0, 1], a_l[:2], g_l[:2])
+    h.precondition_batched([0, 1], gws[:2], gbs[:2], None, None, pw[0][:2], pb[0][:2])
+    h.diag_step(2, gn, an, gws[2], gbs[2], pw[0][2], pb[0][2])
+    torch.cuda.synchronize()
+    # overlapped: factor update on its own stream, the rest on another
+    h = hs[1]
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s1):
+        h.update_factors_batched([0, 1], a_l[:2], g_l[:2])
+    with torch.cuda.stream(s2):
+        h.precondition_batched([0, 1], gws[:2], gbs[:2], None, None, pw[1][:2], pb[1][:2])
+        h.diag_step(2, gn, an, gws[2], gbs[2], pw[1][2], pb[1][2])
+    torch.cuda.synchronize()
+    for li in range(2):
+        for which in (K.KFAC_STATE_A, K.KFAC_STATE_G, K.KFAC_STATE_MOMENTUM):
+            assert torch.equal(hs[0].state(li, which), hs[1].state(li, which)), (li, which)
+    for li in range(3):
+        assert torch.equal(pw[0][li], pw[1][li]) and torch.equal(pb[0][li], pb[1][li]), li
+    assert hs[0].get_status()[0] == 0 and hs[1].get_status()[0] == 0
