@@ -765,7 +765,8 @@ def main():
                 "n_gpus": args.gpus, "steps": len(per_step), "warmup": args.warmup,
                 "ms_per_step": round(1e3 / value, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": cfg.name, "invert_every": cfg.invert_every},
+                "config": {"workload": cfg.name + ("+diag_twins" if not cfg.diag_layers else ""),
+                           "invert_every": cfg.invert_every},
                 "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": cores,
                                  "kind": "oracle", "sample": sample},
                 "e2e": {"value": round(value, 6), "unit": "steps/s", "h2d_bytes_per_step": 0,
