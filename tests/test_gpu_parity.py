@@ -560,3 +560,46 @@ def test_factor_update_concurrent_with_preconditioning_and_diag_step():
     for li in range(3):
         assert torch.equal(pw[0][li], pw[1][li]) and torch.equal(pb[0][li], pb[1][li]), li
     assert hs[0].get_status()[0] == 0 and hs[1].get_status()[0] == 0
+
+
+def test_hyperparameter_schedules_through_set_hparams():
+    """Warm-up damping gamma(t), an lr/momentum schedule and a BatchNorm-style damping
+    rho_BN * gamma(t) for the diagonal layer, all applied with kfac_set_hparams between
+    calls (the values are read when a call is enqueued): 8 steps against the oracle
+    following the same schedule."""
+    d_in, o, M, rho_bn = 96, 48, 256, 4.0
+    h = K.Kfac([(K.KFAC_KRON, o, d_in, 1, K.KFAC_F32), (K.KFAC_DIAG, o, d_in, 1, K.KFAC_F32)],
+               max_rows=M, **HP)
+    orc_k, orc_d = _orc(invert_every=2), _orc()
+    w0 = (RNG.standard_normal((o, d_in)) * 0.1).astype(np.float32)
+    b0 = (RNG.standard_normal(o) * 0.1).astype(np.float32)
+    st_k = O.LayerState("kron", o, d_in, 1, w0, b0)
+    st_d = O.LayerState("diag", o, d_in, 1, w0, b0)
+    params = [(to_dev(w0), to_dev(b0)) for _ in range(2)]
+    for t in range(1, 9):
+        gamma = 1e-3 * (1.0 + 20.0 * 0.5 ** t)          # decaying warm-up damping
+        lr, mu = 1e-2 * min(1.0, t / 4), 0.9 if t > 2 else 0.5
+        a, g = _inputs(M, d_in, o)
+        gw = (g.T @ np.hstack([a, np.ones((M, 1))]) / M).astype(np.float32)
+        gwd, gbd = to_dev(np.ascontiguousarray(gw[:, :d_in])), to_dev(np.ascontiguousarray(gw[:, d_in]))
+        # K-FAC layer
+        h.set_hparams(damping=gamma, lr=lr, momentum=mu)
+        orc_k.gamma, orc_k.lr, orc_k.mu = gamma, lr, mu
+        h.update_factors(0, to_dev(a), to_dev(g))
+        if (t - 1) % 2 == 0:
+            h.invert(0)
+        h.precondition(0, gwd, gbd, None, None, *params[0])
+        orc_k.step_kron(st_k, a, g, gw[:, :d_in], gw[:, d_in])
+        # diagonal layer with its own damping
+        h.set_hparams(damping=rho_bn * gamma)
+        orc_d.gamma, orc_d.lr, orc_d.mu = rho_bn * gamma, lr, mu
+        gn = torch.empty(o, device="cuda")
+        an = torch.empty(d_in + 1, device="cuda")
+        h.diag_factors(1, to_dev(a), to_dev(g), gn, an)
+        h.diag_step(1, gn, an, gwd, gbd, *params[1])
+        orc_d.step_diag(st_d, O.diag_factor(g), O.diag_factor(a, 1), gw[:, :d_in], gw[:, d_in])
+    Wk = O.grad_hat(to_np(params[0][0]), to_np(params[0][1]))
+    Wd = O.grad_hat(to_np(params[1][0]), to_np(params[1][1]))
+    assert rel_fro(Wk, st_k.W) <= 1e-4
+    assert rel_fro(Wd, st_d.W) <= 1e-6
+    assert h.get_status()[0] == 0
