@@ -222,26 +222,29 @@ def blas_threads():
     return len(os.sched_getaffinity(0))
 
 
-def oracle_steps_per_s(cfg, layers, budget_s=20.0):
+def oracle_steps_per_s(cfg, layers, budget_s=20.0, min_s=10.0):
     """Time the float64 oracle as it stands on a bounded sample of the workload.
 
     Sample: one K-FAC step of as many KRON layers as fit the budget (factor
-    build, precondition, update) plus one refresh (both damped inverses) of the
-    first of them; the diagonal path of the same layers.  Per-layer times are
+    build, precondition, update) plus one refresh (both damped inverses) of
+    each of them; the diagonal path of the same layers.  Passes over the sampled
+    layers repeat until at least ``min_s`` seconds of CPU work have been timed,
+    and the per-layer times are averaged over the passes.  Per-layer times are
     scaled to the whole layer set, with the refresh amortised by the cadence."""
     import oracle as O
     hp = cfg.hp
     orc = O.KfacOracle(hp.ema_decay, hp.damping, hp.lr, hp.momentum, hp.weight_decay, 1)
     kron = [l for l in layers if l.kind == "kron"]
     diag = [l for l in layers if l.kind == "diag"]
-    t_total, sampled, t0 = 0.0, [], time.perf_counter()
     cost = lambda l: l.rows * (l.n ** 2 + l.d_out ** 2) + l.n ** 3 + l.d_out ** 3
-    per_layer = {}
-    for l in sorted(kron, key=cost)[: max(1, len(kron))]:
-        if time.perf_counter() - t0 > budget_s and sampled:
-            break
-        li = cfg.layers.index(l) if l in cfg.layers else 0
-        x = Wl.layer_inputs(cfg, li, 1, rows=l.rows)
+    t0 = time.perf_counter()
+    inputs = {}
+
+    def kron_once(l):
+        if l.name not in inputs:
+            li = cfg.layers.index(l) if l in cfg.layers else 0
+            inputs[l.name] = Wl.layer_inputs(cfg, li, 1, rows=l.rows)
+        x = inputs[l.name]
         st = O.LayerState("kron", l.d_out, l.d_in, l.has_bias,
                           np.zeros((l.d_out, l.d_in)), np.zeros(l.d_out) if l.has_bias else None)
         ts = time.perf_counter()
@@ -254,28 +257,44 @@ def oracle_steps_per_s(cfg, layers, budget_s=20.0):
         P = O.precondition(st.Ginv, O.grad_hat(x["grad_w"], x["grad_b"]), st.Ainv)
         st.W, st.m = O.momentum_update(P, st.W, st.m, orc.lr, orc.mu, orc.wd)
         tp = time.perf_counter()
-        per_layer[l.name] = (tf - ts) + (tp - ti) + (ti - tf) / cfg.invert_every
-        sampled.append(l.name)
-    # scale the sampled layers' time to the whole set by the flop-weighted cost
-    done = [l for l in kron if l.name in per_layer]
-    scale = sum(cost(l) for l in kron) / max(1.0, sum(cost(l) for l in done))
-    t_total = sum(per_layer.values()) * scale
-    t_d = 0.0
-    for l in diag[:4]:
-        x = Wl.layer_inputs(cfg, 0, 1, rows=min(l.rows, 4096)) if l.act != "bn" else None
+        return (tf - ts) + (tp - ti) + (ti - tf) / cfg.invert_every
+
+    def diag_once(l):
         st = O.LayerState("diag", l.d_out, l.d_in, l.has_bias, np.zeros((l.d_out, l.d_in)),
                           np.zeros(l.d_out) if l.has_bias else None)
         gw = np.zeros((l.d_out, l.d_in))
         gn, an = np.ones(l.d_out), np.ones(l.n)
         ts = time.perf_counter()
         orc.step_diag(st, gn, an, gw, np.zeros(l.d_out) if l.has_bias else None)
-        t_d += time.perf_counter() - ts
+        return time.perf_counter() - ts
+
+    # first pass: as many KRON layers (cheapest first) as fit the budget
+    sums, sampled = {}, []
+    for l in sorted(kron, key=cost):
+        if time.perf_counter() - t0 > budget_s and sampled:
+            break
+        sums[l.name] = kron_once(l)
+        sampled.append(l)
+    dsample = diag[:4]
+    dsum = sum(diag_once(l) for l in dsample)
+    passes = 1
+    # further passes over the same sample until enough CPU work has been timed
+    while time.perf_counter() - t0 < min_s:
+        for l in sampled:
+            sums[l.name] += kron_once(l)
+        dsum += sum(diag_once(l) for l in dsample)
+        passes += 1
+    # scale the sampled layers' time to the whole set by the flop-weighted cost
+    scale = sum(cost(l) for l in kron) / max(1.0, sum(cost(l) for l in sampled))
+    t_total = sum(sums.values()) / passes * scale
     if diag:
-        t_total += t_d * len(diag) / min(4, len(diag))
-    sample = (f"oracle fp64: factor+precond+update of {len(done)}/{len(kron)} KRON layers "
-              f"({', '.join(sampled[:4])}{'...' if len(sampled) > 4 else ''}) with one refresh "
-              f"amortised by {cfg.invert_every}, diag step of {min(4, len(diag))}/{len(diag)} "
-              f"DIAG layers; scaled to the full layer set by flop-weighted cost")
+        t_total += dsum / passes * len(diag) / len(dsample)
+    names = [l.name for l in sampled]
+    sample = (f"oracle fp64: factor+precond+update of {len(sampled)}/{len(kron)} KRON layers "
+              f"({', '.join(names[:4])}{'...' if len(names) > 4 else ''}) with one refresh "
+              f"amortised by {cfg.invert_every}, diag step of {len(dsample)}/{len(diag)} "
+              f"DIAG layers, {passes} pass(es) averaged; scaled to the full layer set by "
+              f"flop-weighted cost")
     return 1.0 / t_total, sample, time.perf_counter() - t0
 
 
@@ -755,7 +774,8 @@ def main():
             pass  # the oracle has nothing to warm up
         t0 = time.perf_counter()
         for _ in range(max(1, args.steps)):
-            v, sample, _ = oracle_steps_per_s(cfg, layers, budget_s=max(2.0, 60.0 / max(1, args.steps)))
+            v, sample, _ = oracle_steps_per_s(cfg, layers, budget_s=max(2.0, 60.0 / max(1, args.steps)),
+                                              min_s=0.0)
             per_step.append(1.0 / v)
             if time.perf_counter() - t0 > 150:
                 break
