@@ -40,6 +40,9 @@ one is also listed in the repository's design notes):
   R7  diagonal step: P_ij = dW_ij / (g_i a_j + gamma), g and a the EMA diagonals.
   R8  a layer with a bias carries it as the last column of W-hat = [W | b] and
       its activations get a ones column: a-hat = [a | 1].
+  R9  a convolution's activation rows are its zero-padded input patches, one
+      per (image, output position), columns in weight order (c, i, j); its
+      output-gradient rows are the channels at the same positions.
 
 Parity pins for every function live in tests/test_oracle.py.
 """
@@ -91,6 +94,58 @@ def factor(x, has_bias: int = 0, scale: Optional[float] = None) -> np.ndarray:
 def ema(old, new, decay: float) -> np.ndarray:
     """Running factor by exponential moving average (reading R2)."""
     return decay * _f64(old) + (1.0 - decay) * _f64(new)
+
+
+# ---------------------------------------------------------------------------
+# convolution layers (Osawa et al. §3.2, §5.1): a 2-D convolution is a linear
+# map applied at every output position, so its A factor is built from the input
+# patches, one row per (image, output position), and its G factor from the
+# output gradient at the same positions; M = B * H_out * W_out.
+
+def conv_out_size(size: int, kernel: int, stride: int, pad: int, dilation: int) -> int:
+    """Output extent of a 2-D convolution along one axis."""
+    return (size + 2 * pad - dilation * (kernel - 1) - 1) // stride + 1
+
+
+def im2col(x, kernel, stride=(1, 1), pad=(0, 0), dilation=(1, 1)) -> np.ndarray:
+    """Input patches of a 2-D convolution as rows: x [B, C, H, W] -> [B*Ho*Wo, C*kh*kw].
+
+    Row order (b, oh, ow); column order (c, i, j), the order of a weight
+    [o, C, kh, kw] flattened to [o, C*kh*kw].  Entry (row, column) is
+    x[b, c, oh*sh - ph + i*dh, ow*sw - pw + j*dw], zero outside the image.
+    """
+    x = _f64(x)
+    B, C, H, W = x.shape
+    (kh, kw), (sh, sw), (ph, pw), (dh, dw) = kernel, stride, pad, dilation
+    Ho = conv_out_size(H, kh, sh, ph, dh)
+    Wo = conv_out_size(W, kw, sw, pw, dw)
+    xp = np.zeros((B, C, H + 2 * ph, W + 2 * pw))
+    xp[:, :, ph:ph + H, pw:pw + W] = x
+    cols = np.empty((B, Ho, Wo, C, kh, kw))
+    for i in range(kh):
+        for j in range(kw):
+            win = xp[:, :, i * dh: i * dh + sh * (Ho - 1) + 1: sh,
+                     j * dw: j * dw + sw * (Wo - 1) + 1: sw]          # [B, C, Ho, Wo]
+            cols[:, :, :, :, i, j] = win.transpose(0, 2, 3, 1)
+    return cols.reshape(B * Ho * Wo, C * kh * kw)
+
+
+def output_rows(gy) -> np.ndarray:
+    """Output gradient [B, o, Ho, Wo] as rows [B*Ho*Wo, o], row order (b, oh, ow)."""
+    gy = _f64(gy)
+    return gy.transpose(0, 2, 3, 1).reshape(-1, gy.shape[1])
+
+
+def conv_factors(x, gy, kernel, stride=(1, 1), pad=(0, 0), dilation=(1, 1),
+                 has_bias: int = 1, scale: Optional[float] = None):
+    """New (A, G) of a 2-D convolution from its input x [B, C, H, W] and output
+    gradient gy [B, o, Ho, Wo]: A = s * [P 1]^T [P 1] with P = im2col(x),
+    G = s * R^T R with R = output_rows(gy), s = 1/(B*Ho*Wo) unless given."""
+    P = im2col(x, kernel, stride, pad, dilation)
+    R = output_rows(gy)
+    if P.shape[0] != R.shape[0]:
+        raise ValueError("input patches and output gradient rows differ")
+    return factor(P, has_bias, scale), factor(R, 0, scale)
 
 
 # ---------------------------------------------------------------------------

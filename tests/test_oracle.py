@@ -279,3 +279,94 @@ def test_c1_golden_trajectory():
     for t in range(10):
         assert np.allclose(hist[t][2], ref["W"][t], rtol=1e-12, atol=1e-15)
     assert np.allclose(st.A, ref["A"], rtol=1e-12, atol=1e-15)
+
+
+# ---------------------------------------------------------------- convolution layers
+
+CONV_GEOMS = [  # (B, C, H, W, kh, kw, sh, sw, ph, pw, dh, dw)
+    (2, 3, 5, 6, 3, 3, 1, 1, 1, 1, 1, 1),
+    (1, 2, 7, 5, 3, 2, 2, 1, 1, 0, 1, 1),
+    (2, 1, 9, 8, 3, 3, 2, 2, 2, 1, 2, 2),
+    (3, 4, 4, 4, 1, 1, 1, 1, 0, 0, 1, 1),
+    (1, 2, 11, 11, 7, 7, 2, 2, 3, 3, 1, 1),
+]
+
+
+@pytest.mark.parametrize("geom", CONV_GEOMS)
+def test_im2col_matches_torch_unfold(geom):
+    """The patch rows equal torch.nn.functional.unfold's columns (an independent
+    library routine), transposed to one row per (image, output position)."""
+    torch = pytest.importorskip("torch")
+    B, C, H, Wd, kh, kw, sh, sw, ph, pw, dh, dw = geom
+    x = RNG.standard_normal((B, C, H, Wd))
+    got = O.im2col(x, (kh, kw), (sh, sw), (ph, pw), (dh, dw))
+    u = torch.nn.functional.unfold(torch.from_numpy(x), (kh, kw), dilation=(dh, dw),
+                                   padding=(ph, pw), stride=(sh, sw))      # [B, C*kh*kw, L]
+    ref = u.transpose(1, 2).reshape(-1, C * kh * kw).numpy()
+    assert got.shape == ref.shape
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_im2col_brute_force():
+    """Every entry by its definition, with explicit bounds checks, on a tiny case."""
+    B, C, H, Wd, kh, kw, sh, sw, ph, pw, dh, dw = 2, 2, 5, 4, 3, 2, 2, 1, 1, 1, 1, 2
+    x = RNG.integers(-9, 10, size=(B, C, H, Wd)).astype(np.float64)
+    Ho = (H + 2 * ph - dh * (kh - 1) - 1) // sh + 1
+    Wo = (Wd + 2 * pw - dw * (kw - 1) - 1) // sw + 1
+    got = O.im2col(x, (kh, kw), (sh, sw), (ph, pw), (dh, dw))
+    assert got.shape == (B * Ho * Wo, C * kh * kw)
+    for b in range(B):
+        for oh in range(Ho):
+            for ow in range(Wo):
+                row = (b * Ho + oh) * Wo + ow
+                for c in range(C):
+                    for i in range(kh):
+                        for j in range(kw):
+                            y, xx = oh * sh - ph + i * dh, ow * sw - pw + j * dw
+                            v = x[b, c, y, xx] if 0 <= y < H and 0 <= xx < Wd else 0.0
+                            assert got[row, (c * kh + i) * kw + j] == v
+
+
+def test_conv_1x1_patches_are_the_pixels():
+    """A 1x1 convolution with unit stride and no padding sees each pixel's channel
+    vector: its patch rows are the input laid out as output rows."""
+    x = RNG.standard_normal((3, 5, 4, 6))
+    np.testing.assert_array_equal(O.im2col(x, (1, 1)), O.output_rows(x))
+
+
+@pytest.mark.parametrize("H,Wd", [(4, 4), (5, 7), (1, 3)])
+def test_conv_factor_of_constant_image_closed_form(H, Wd):
+    """On an all-ones image with a 3x3, pad-1, stride-1 kernel, taps with row
+    offsets i, i' (0..2) both fall inside the image at the output rows oh with
+    max(0, 1 - min(i, i')) <= oh <= min(H - 1, H - max(i, i')), and likewise for
+    columns; A's entry is that count over H*W, the bias column the single-tap count."""
+    C = 2
+    x = np.ones((1, C, H, Wd))
+    gy = np.zeros((1, 3, H, Wd))
+    A, _ = O.conv_factors(x, gy, (3, 3), (1, 1), (1, 1), (1, 1), has_bias=1)
+    M = H * Wd
+    n = C * 9 + 1
+    assert A.shape == (n, n)
+
+    def rows(ext, a, b):
+        lo, hi = max(0, 1 - min(a, b)), min(ext - 1, ext - max(a, b))
+        return max(0, hi - lo + 1)
+
+    for p in range(C * 9):
+        i, j = (p % 9) // 3, p % 3
+        assert A[p, n - 1] == pytest.approx(rows(H, i, i) * rows(Wd, j, j) / M, rel=1e-15)
+        for q in range(C * 9):
+            i2, j2 = (q % 9) // 3, q % 3
+            want = rows(H, i, i2) * rows(Wd, j, j2) / M
+            assert A[p, q] == pytest.approx(want, rel=1e-15, abs=1e-300)
+    assert A[n - 1, n - 1] == 1.0
+
+
+def test_conv_G_is_channel_covariance_over_positions():
+    """G sums g g^T over every (image, position): the same as contracting the
+    NCHW output gradient over batch and both spatial axes."""
+    gy = RNG.standard_normal((3, 4, 5, 2))
+    x = RNG.standard_normal((3, 2, 5, 2))
+    _, G = O.conv_factors(x, gy, (1, 1))
+    ref = np.einsum("bchw,bdhw->cd", gy, gy) / (3 * 5 * 2)
+    np.testing.assert_allclose(G, ref, rtol=1e-14, atol=0)
