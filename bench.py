@@ -31,7 +31,11 @@ import workloads as Wl  # noqa: E402
 
 METRIC = "K-FAC precond steps/s; factor-GEMM TFLOP/s & diag-step GB/s vs GB300 peak"
 WORKLOADS = {"mlp4": "c2", "single_linear": "c1", "resnet18": "c3", "resnet50": "c4",
-             "resnet50_bf16": "c4bf16", "transformer4": "c5"}
+             "resnet50_bf16": "c4bf16", "transformer4": "c5",
+             "resnet18_nchw": "c3", "resnet50_nchw": "c4", "resnet50_bf16_nchw": "c4bf16"}
+# workloads whose convolutions hand the library their NCHW input and output
+# gradient (kfac_update_factors_conv2d_batched) instead of unfolded matrices
+NCHW_WORKLOADS = {"resnet18_nchw", "resnet50_nchw", "resnet50_bf16_nchw"}
 # fallback roofline denominators when MEASURED_PEAKS.json is absent
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TF32_PER_BF16 = 1.1 / 2.25          # nominal dense ratio
@@ -131,8 +135,9 @@ def job_throughput(ms_per_step_max: float, world: int) -> float:
 
 # ----------------------------------------------------------------------------- accounting
 
-def algorithmic(layers, k):
-    """Per-step algorithmic flops and bytes of each phase (fp32 state, input dtype as given)."""
+def algorithmic(layers, k, nchw=False):
+    """Per-step algorithmic flops and bytes of each phase (fp32 state, input dtype as given).
+    nchw: convolutions read their NCHW input and output gradient, not unfolded matrices."""
     f = {"factor_flop": 0.0, "factor_bytes": 0.0, "invert_flop": 0.0, "precond_flop": 0.0,
          "precond_bytes": 0.0, "diag_bytes": 0.0, "diagfac_bytes": 0.0}
     for l in layers:
@@ -141,7 +146,12 @@ def algorithmic(layers, k):
         if l.kind == "kron":
             # upper triangle only: M * n(n+1) flop (2 per FMA) per factor
             f["factor_flop"] += M * n * (n + 1) + M * o * (o + 1)
-            f["factor_bytes"] += M * (l.d_in + o) * elt + 2 * 4 * (n * n + o * o)
+            if nchw and l.conv is not None:
+                c = l.conv
+                f["factor_bytes"] += (c.batch * c.c_in * c.h * c.w + M * o) * elt
+            else:
+                f["factor_bytes"] += M * (l.d_in + o) * elt
+            f["factor_bytes"] += 2 * 4 * (n * n + o * o)
             f["invert_flop"] += (n ** 3 + o ** 3) / k     # Cholesky n^3/3 + L^-1 n^3/3 + X^T X n^3/3
             f["precond_flop"] += 2 * o * n * n + 2 * o * o * n
             f["precond_bytes"] += 4 * (n * n + o * o + 2 * o * n) + 4 * 3 * o * n
@@ -222,7 +232,7 @@ def blas_threads():
     return len(os.sched_getaffinity(0))
 
 
-def oracle_steps_per_s(cfg, layers, budget_s=20.0, min_s=10.0):
+def oracle_steps_per_s(cfg, layers, budget_s=20.0, min_s=10.0, nchw=False):
     """Time the float64 oracle as it stands on a bounded sample of the workload.
 
     Sample: one K-FAC step of as many KRON layers as fit the budget (factor
@@ -230,7 +240,9 @@ def oracle_steps_per_s(cfg, layers, budget_s=20.0, min_s=10.0):
     each of them; the diagonal path of the same layers.  Passes over the sampled
     layers repeat until at least ``min_s`` seconds of CPU work have been timed,
     and the per-layer times are averaged over the passes.  Per-layer times are
-    scaled to the whole layer set, with the refresh amortised by the cadence."""
+    scaled to the whole layer set, with the refresh amortised by the cadence.
+    nchw: convolutions build their factors from NCHW draws through the oracle's
+    input patches, as the GPU arm's NCHW workloads do."""
     import oracle as O
     hp = cfg.hp
     orc = O.KfacOracle(hp.ema_decay, hp.damping, hp.lr, hp.momentum, hp.weight_decay, 1)
@@ -244,12 +256,20 @@ def oracle_steps_per_s(cfg, layers, budget_s=20.0, min_s=10.0):
         if l.name not in inputs:
             li = cfg.layers.index(l) if l in cfg.layers else 0
             inputs[l.name] = Wl.layer_inputs(cfg, li, 1, rows=l.rows)
+            if nchw and l.conv is not None:
+                inputs[l.name].update(Wl.conv_inputs(cfg, li, 1))
         x = inputs[l.name]
         st = O.LayerState("kron", l.d_out, l.d_in, l.has_bias,
                           np.zeros((l.d_out, l.d_in)), np.zeros(l.d_out) if l.has_bias else None)
         ts = time.perf_counter()
-        st.A = O.ema(st.A, O.factor(x["a"], l.has_bias), orc.xi)
-        st.G = O.ema(st.G, O.factor(x["g"], 0), orc.xi)
+        if "geom" in x:
+            c = x["geom"]
+            An, Gn = O.conv_factors(x["x"], x["gy"], (c.kh, c.kw), (c.sh, c.sw), (c.ph, c.pw),
+                                    (c.dh, c.dw), l.has_bias)
+        else:
+            An, Gn = O.factor(x["a"], l.has_bias), O.factor(x["g"], 0)
+        st.A = O.ema(st.A, An, orc.xi)
+        st.G = O.ema(st.G, Gn, orc.xi)
         tf = time.perf_counter()
         st.Ainv = O.damped_inverse(st.A, orc.gamma)
         st.Ginv = O.damped_inverse(st.G, orc.gamma)
@@ -320,10 +340,16 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     srcidx = [base.get(l.name.replace("_diag", ""), i) for i, l in enumerate(layers)]
     NB = 2
     data = []
+    nchw = args.workload in NCHW_WORKLOADS
+    is_conv = lambda l: nchw and l.kind == "kron" and l.conv is not None
     for b in range(NB):
         per = []
         for li, l in enumerate(layers):
             x = Wl.layer_inputs_torch(cfg, srcidx[li], 1 + b + 1000 * rank, dev)
+            if is_conv(l):      # NCHW input and output gradient replace the unfolded a, g
+                del x["a"], x["g"]
+                c = Wl.conv_inputs_torch(cfg, srcidx[li], 1 + b + 1000 * rank, dev)
+                x["x"], x["gy"] = c["x"], c["gy"]
             per.append(x)
         data.append(per)
     # all parameters live in one flat device buffer (256-byte aligned views), so the
@@ -351,13 +377,23 @@ def run_gpu(args, rank, world, peaks, peak_kind):
 
     kron_idx = [li for li, l in enumerate(layers) if l.kind == "kron"]
     # batches share one input dtype
-    kron_groups = {}
+    kron_groups, conv_groups, geoms = {}, {}, {}
     for li in kron_idx:
-        kron_groups.setdefault(layers[li].in_dtype, []).append(li)
+        l = layers[li]
+        if is_conv(l):
+            c = l.conv
+            geoms[li] = K.conv2d_geom((c.batch, c.c_in, c.h, c.w), (c.kh, c.kw), (c.sh, c.sw),
+                                      (c.ph, c.pw), (c.dh, c.dw))
+            conv_groups.setdefault(l.in_dtype, []).append(li)
+        else:
+            kron_groups.setdefault(l.in_dtype, []).append(li)
 
     def phase_factor(x):
         for grp in kron_groups.values():
             h.update_factors_batched(grp, [x[li]["a"] for li in grp], [x[li]["g"] for li in grp])
+        for grp in conv_groups.values():
+            h.update_factors_conv2d_batched(grp, [x[li]["x"] for li in grp],
+                                            [x[li]["gy"] for li in grp], [geoms[li] for li in grp])
 
     def phase_invert():
         h.invert(-1)
@@ -513,7 +549,7 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     ph = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
                    for i in range(seq_steps)])  # ms: factor, invert, precond, diag
 
-    acc = algorithmic(layers, k)
+    acc = algorithmic(layers, k, nchw)
     phase_ms = ph.mean(axis=0)
     phase_ms[1] = inv_ms_refresh / k   # invert, amortised over the refresh period
     factor_tfs = acc["factor_flop"] / (phase_ms[0] * 1e-3) / 1e12
@@ -571,7 +607,8 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     return {
         "ms_per_step": ms_step, "phases": phases, "roofline": roof, "clocks": clocks,
         "gpu_launches": int(launches), "wall_s": wall, "e2e": e2e,
-        "config": {"workload": cfg.name + ("+diag_twins" if not cfg.diag_layers else ""),
+        "config": {"workload": cfg.name + ("+diag_twins" if not cfg.diag_layers else "")
+                   + ("+nchw_conv_inputs" if nchw else ""),
                    "kron_layers": sum(l.kind == "kron" for l in layers),
                    "diag_layers": sum(l.kind == "diag" for l in layers),
                    "invert_every": k, "max_rows": max_rows,
@@ -775,7 +812,7 @@ def main():
         t0 = time.perf_counter()
         for _ in range(max(1, args.steps)):
             v, sample, _ = oracle_steps_per_s(cfg, layers, budget_s=max(2.0, 60.0 / max(1, args.steps)),
-                                              min_s=0.0)
+                                              min_s=0.0, nchw=args.workload in NCHW_WORKLOADS)
             per_step.append(1.0 / v)
             if time.perf_counter() - t0 > 150:
                 break
@@ -785,7 +822,8 @@ def main():
                 "n_gpus": args.gpus, "steps": len(per_step), "warmup": args.warmup,
                 "ms_per_step": round(1e3 / value, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": cfg.name + ("+diag_twins" if not cfg.diag_layers else ""),
+                "config": {"workload": cfg.name + ("+diag_twins" if not cfg.diag_layers else "")
+                           + ("+nchw_conv_inputs" if args.workload in NCHW_WORKLOADS else ""),
                            "invert_every": cfg.invert_every},
                 "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": cores,
                                  "kind": "oracle", "sample": sample},
@@ -800,7 +838,8 @@ def main():
     res = run_gpu(args, rank, world, peaks, peak_kind)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample, spent = oracle_steps_per_s(cfg, layers, budget_s=20.0)
+        v, sample, spent = oracle_steps_per_s(cfg, layers, budget_s=20.0,
+                                              nchw=args.workload in NCHW_WORKLOADS)
         cpu = {"value": round(v, 6), "unit": "steps/s", "cores": blas_threads(), "kind": "oracle",
                "sample": sample, "seconds": round(spent, 1)}
     if rank == 0:

@@ -145,6 +145,48 @@ kfac_status kfac_update_factors_batched(kfac_handle h, int count, const int* lay
                                         const void* const* g, const int64_t* ldg,
                                         const int64_t* rows, double scale, cudaStream_t stream);
 
+/* Geometry of a 2-D convolution (cross-correlation) over an NCHW input
+ * [batch, in_channels, in_h, in_w].  The output is [batch, d_out, out_h,
+ * out_w] with out = (in + 2 pad - dilation (kernel - 1) - 1) / stride + 1. */
+typedef struct {
+  int batch, in_channels, in_h, in_w;
+  int kernel_h, kernel_w;
+  int stride_h, stride_w;
+  int pad_h, pad_w;
+  int dilation_h, dilation_w;
+} kfac_conv2d_geom;
+
+/* K1 for a 2-D convolution layer straight from its NCHW tensors, without an
+ * unfolded input:
+ *   A <- xi A + (1-xi) s [P 1]^T [P 1],   G <- xi G + (1-xi) s R^T R,
+ * where P [M x in_channels*kernel_h*kernel_w] holds the zero-padded input
+ * patches, one row per (image b, output position oh, ow) in that order, columns
+ * in the order (channel c, kernel row i, kernel column j) of a weight
+ * [d_out, C, kh, kw] flattened, entry x[b, c, oh*stride_h - pad_h + i*dilation_h,
+ * ow*stride_w - pad_w + j*dilation_w] (0 outside the image); R [M x d_out] holds
+ * the output gradient at the same positions; M = batch*out_h*out_w.
+ * x: [batch, in_channels, in_h, in_w] contiguous; gy: [batch, d_out, out_h,
+ * out_w] contiguous; both of the layer's in_dtype.  scale <= 0 means s = 1/M.
+ * Requires d_in == in_channels*kernel_h*kernel_w, every size >= 1, pad >= 0,
+ * 1 <= M <= max_rows and each tensor below 2^31 elements; otherwise
+ * KFAC_ERR_INVALID_ARG before any launch.  The result equals
+ * kfac_update_factors on the unfolded P and R up to the order of sums.
+ * Osawa et al. §3.2 (the factors of a layer from its input activations and
+ * output gradients) and §5.1 (convolutional networks: one factor row per
+ * output position, M = B H_out W_out). */
+kfac_status kfac_update_factors_conv2d(kfac_handle h, int layer, const void* x, const void* gy,
+                                       const kfac_conv2d_geom* geom, double scale,
+                                       cudaStream_t stream);
+
+/* kfac_update_factors_conv2d for several KRON layers in one pass (one gather
+ * launch for all their inputs and one grouped product launch), as
+ * kfac_update_factors_batched does for row-major inputs.  Host arrays of
+ * length count; each layer at most once; all layers of one in_dtype. */
+kfac_status kfac_update_factors_conv2d_batched(kfac_handle h, int count, const int* layers,
+                                               const void* const* x, const void* const* gy,
+                                               const kfac_conv2d_geom* geoms, double scale,
+                                               cudaStream_t stream);
+
 /* K5: new diagonal factors of a layer from its a and g (any kind):
  *   g_new[i] = s sum_r g[r,i]^2 (o entries); a_new[j] = s sum_r a[r,j]^2, and
  *   a_new[d_in] = s*rows when has_bias (n entries).  Written to caller buffers.

@@ -16,10 +16,11 @@ from typing import Optional, Sequence
 from ._lib import (LIB, KFAC_KRON, KFAC_DIAG, KFAC_F32, KFAC_BF16, KFAC_MATH_3XTF32,
                    KFAC_MATH_BF16, KFAC_EMA_INIT_ZERO, KFAC_EMA_INIT_FIRST, KFAC_STATE_A,
                    KFAC_STATE_G, KFAC_STATE_AINV, KFAC_STATE_GINV, KFAC_STATE_MOMENTUM,
-                   KFAC_STATE_GDIAG, KFAC_STATE_ADIAG, LayerDesc, HParams, KfacError,
+                   KFAC_STATE_GDIAG, KFAC_STATE_ADIAG, LayerDesc, HParams, Conv2dGeom, KfacError,
                    status_string, launch_count)
 
-__all__ = ["Kfac", "diag_factors_static", "LayerDesc", "HParams", "KfacError", "status_string", "launch_count",
+__all__ = ["Kfac", "diag_factors_static", "conv2d_geom", "LayerDesc", "HParams", "Conv2dGeom",
+           "KfacError", "status_string", "launch_count",
            "KFAC_KRON", "KFAC_DIAG", "KFAC_F32", "KFAC_BF16", "KFAC_MATH_3XTF32",
            "KFAC_MATH_BF16", "KFAC_EMA_INIT_ZERO", "KFAC_EMA_INIT_FIRST", "LIB"]
 
@@ -39,6 +40,19 @@ def _stream(stream) -> Optional[int]:
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
+
+
+def _pair(v):
+    return (int(v), int(v)) if isinstance(v, int) else (int(v[0]), int(v[1]))
+
+
+def conv2d_geom(x_shape, kernel, stride=1, padding=0, dilation=1) -> Conv2dGeom:
+    """kfac_conv2d_geom for an NCHW input of shape x_shape (int or pair arguments,
+    as torch.nn.Conv2d takes them)."""
+    B, C, H, W = (int(v) for v in x_shape)
+    (kh, kw), (sh, sw), (ph, pw), (dh, dw) = (_pair(kernel), _pair(stride), _pair(padding),
+                                              _pair(dilation))
+    return Conv2dGeom(B, C, H, W, kh, kw, sh, sw, ph, pw, dh, dw)
 
 
 def _check(code: int, what: str):
@@ -114,6 +128,24 @@ class Kfac:
             I64(*[x.stride(0) for x in a_list]), P(*[_ptr(x) for x in g_list]),
             I64(*[x.stride(0) for x in g_list]), I64(*[x.shape[0] for x in a_list]),
             float(scale), _stream(stream)), "kfac_update_factors_batched")
+
+    def update_factors_conv2d(self, layer: int, x, gy, kernel, stride=1, padding=0, dilation=1,
+                              scale: float = 0.0, stream=None):
+        """kfac_update_factors_conv2d: x [B, C, H, W] and gy [B, o, Ho, Wo], both contiguous."""
+        geom = conv2d_geom(x.shape, kernel, stride, padding, dilation)
+        _check(LIB.kfac_update_factors_conv2d(self._h, layer, _ptr(x), _ptr(gy),
+                                              ctypes.byref(geom), float(scale), _stream(stream)),
+               "kfac_update_factors_conv2d")
+
+    def update_factors_conv2d_batched(self, layers, x_list, gy_list, geoms, scale: float = 0.0,
+                                      stream=None):
+        """kfac_update_factors_conv2d_batched; geoms: Conv2dGeom per layer (see conv2d_geom)."""
+        k = len(layers)
+        P = ctypes.c_void_p * k
+        _check(LIB.kfac_update_factors_conv2d_batched(
+            self._h, k, (ctypes.c_int * k)(*layers), P(*[_ptr(x) for x in x_list]),
+            P(*[_ptr(x) for x in gy_list]), (Conv2dGeom * k)(*geoms), float(scale),
+            _stream(stream)), "kfac_update_factors_conv2d_batched")
 
     def diag_factors(self, layer: int, a, g, g_new, a_new, rows: Optional[int] = None,
                      scale: float = 0.0, stream=None):

@@ -38,6 +38,12 @@ class HParams(ctypes.Structure):
                 ("math", ctypes.c_int)]
 
 
+class Conv2dGeom(ctypes.Structure):
+    _fields_ = [(nm, ctypes.c_int) for nm in
+                ("batch", "in_channels", "in_h", "in_w", "kernel_h", "kernel_w", "stride_h",
+                 "stride_w", "pad_h", "pad_w", "dilation_h", "dilation_w")]
+
+
 class KfacError(RuntimeError):
     def __init__(self, code: int, what: str):
         self.code = code
@@ -46,6 +52,7 @@ class KfacError(RuntimeError):
 
 _vp, _i, _i64, _d, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_size_t
 _pLD, _pHP = ctypes.POINTER(LayerDesc), ctypes.POINTER(HParams)
+_pCG = ctypes.POINTER(Conv2dGeom)
 
 # (name, restype, argtypes): one line per entry point of include/kfac.h
 SIGNATURES = [
@@ -54,6 +61,8 @@ SIGNATURES = [
     ("kfac_set_hparams", _i, [_vp, _pHP]),
     ("kfac_update_factors", _i, [_vp, _i, _vp, _i64, _vp, _i64, _i64, _d, _vp]),
     ("kfac_update_factors_batched", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _d, _vp]),
+    ("kfac_update_factors_conv2d", _i, [_vp, _i, _vp, _vp, _pCG, _d, _vp]),
+    ("kfac_update_factors_conv2d_batched", _i, [_vp, _i, _vp, _vp, _vp, _pCG, _d, _vp]),
     ("kfac_diag_factors", _i, [_vp, _i, _vp, _i64, _vp, _i64, _i64, _d, _vp, _vp, _vp]),
     ("kfac_diag_factors_batched", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _d, _vp, _vp,
                                        _vp]),

@@ -200,7 +200,7 @@ kfac_status launch_update_factors_batched(kfac_ctx* h, int count, const int* lay
                                           const void* const* a, const int64_t* lda,
                                           const void* const* g, const int64_t* ldg,
                                           const int64_t* rows, double scale, const float* decay,
-                                          cudaStream_t st) {
+                                          cudaStream_t st, const kfac_conv2d_geom* geoms) {
   const bool bf16 = h->layers[layers[0]].in_dtype == KFAC_BF16;
   const size_t elt = bf16 ? 2 : 8;  // packed bytes per element (bf16, or two TF32 halves)
   std::vector<PackJob> pj;
@@ -231,8 +231,20 @@ kfac_status launch_update_factors_batched(kfac_ctx* h, int count, const int* lay
       used += w == 0 ? bA : bG;
       PackJob j{};
       j.x = w == 0 ? a[i] : g[i];
-      j.ld = w == 0 ? lda[i] : ldg[i];
+      j.ld = geoms ? 0 : (w == 0 ? lda[i] : ldg[i]);
       j.M = rows[i];
+      if (geoms) {
+        const kfac_conv2d_geom& cg = geoms[i];
+        const int ho = conv_out(cg.in_h, cg.kernel_h, cg.stride_h, cg.pad_h, cg.dilation_h);
+        const int wo = conv_out(cg.in_w, cg.kernel_w, cg.stride_w, cg.pad_w, cg.dilation_w);
+        j.conv = 1;
+        if (w == 0)
+          j.cs = ConvSrc{cg.batch, cg.in_channels, cg.in_h, cg.in_w, cg.kernel_h, cg.kernel_w,
+                         cg.stride_h, cg.stride_w, cg.pad_h, cg.pad_w, cg.dilation_h,
+                         cg.dilation_w, ho, wo};
+        else  // the output gradient is its own 1x1 unit-stride "input"
+          j.cs = ConvSrc{cg.batch, L.o, ho, wo, 1, 1, 1, 1, 0, 0, 1, 1, ho, wo};
+      }
       j.d = w == 0 ? L.d_in : L.o;
       j.n = n;
       j.Kp = Kp;

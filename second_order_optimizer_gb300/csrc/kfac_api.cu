@@ -171,6 +171,29 @@ kfac_status check_inputs(const kfac_ctx* h, const LayerInfo& L, const void* a, i
   return KFAC_OK;
 }
 
+// A convolution layer's NCHW inputs: geometry, sizes and alignment.
+kfac_status check_conv(const kfac_ctx* h, const LayerInfo& L, const void* x, const void* gy,
+                       const kfac_conv2d_geom& g, int64_t* rows) {
+  const size_t es = L.in_dtype == KFAC_BF16 ? 2 : 4;
+  if (!x || !gy || !aligned(x, es) || !aligned(gy, es)) return KFAC_ERR_INVALID_ARG;
+  if (g.batch < 1 || g.in_channels < 1 || g.in_h < 1 || g.in_w < 1 || g.kernel_h < 1 ||
+      g.kernel_w < 1 || g.stride_h < 1 || g.stride_w < 1 || g.pad_h < 0 || g.pad_w < 0 ||
+      g.dilation_h < 1 || g.dilation_w < 1)
+    return KFAC_ERR_INVALID_ARG;
+  if ((int64_t)g.in_channels * g.kernel_h * g.kernel_w != L.d_in) return KFAC_ERR_INVALID_ARG;
+  const int ho = conv_out(g.in_h, g.kernel_h, g.stride_h, g.pad_h, g.dilation_h);
+  const int wo = conv_out(g.in_w, g.kernel_w, g.stride_w, g.pad_w, g.dilation_w);
+  if (ho < 1 || wo < 1) return KFAC_ERR_INVALID_ARG;
+  const int64_t lim = int64_t(1) << 31;
+  const int64_t nx = (int64_t)g.batch * g.in_channels * g.in_h * g.in_w;
+  const int64_t ny = (int64_t)g.batch * L.o * ho * wo;
+  if (nx >= lim || ny >= lim) return KFAC_ERR_INVALID_ARG;
+  const int64_t m = (int64_t)g.batch * ho * wo;
+  if (m < 1 || m > h->max_rows) return KFAC_ERR_INVALID_ARG;
+  *rows = m;
+  return KFAC_OK;
+}
+
 }  // namespace
 }  // namespace kfac
 
@@ -355,6 +378,42 @@ kfac_status kfac_update_factors_batched(kfac_handle h, int count, const int* lay
   if (e == KFAC_OK)
     for (int i = 0; i < count; ++i) ++h->layers[layers[i]].t_factor;
   return e;
+}
+
+kfac_status kfac_update_factors_conv2d_batched(kfac_handle h, int count, const int* layers,
+                                               const void* const* x, const void* const* gy,
+                                               const kfac_conv2d_geom* geoms, double scale,
+                                               cudaStream_t stream) {
+  if (!h || count < 1 || !layers || !x || !gy || !geoms || !std::isfinite(scale))
+    return KFAC_ERR_INVALID_ARG;
+  std::vector<char> seen(h->layers.size(), 0);
+  std::vector<int64_t> rows(count);
+  for (int i = 0; i < count; ++i) {
+    if (kfac_status e = check_layer(h, layers[i], KFAC_KRON)) return e;
+    if (seen[layers[i]]++) return KFAC_ERR_INVALID_ARG;
+    const LayerInfo& L = h->layers[layers[i]];
+    if (L.in_dtype != h->layers[layers[0]].in_dtype) return KFAC_ERR_INVALID_ARG;
+    if (kfac_status e = check_conv(h, L, x[i], gy[i], geoms[i], &rows[i])) return e;
+  }
+  if (kfac_status e = ensure_device(h)) return e;
+  std::vector<float> decay(count);
+  for (int i = 0; i < count; ++i) {
+    const LayerInfo& L = h->layers[layers[i]];
+    const bool first = L.t_factor == 0 && h->hp.ema_init == KFAC_EMA_INIT_FIRST;
+    decay[i] = first ? 0.f : (float)h->hp.ema_decay;
+  }
+  kfac_status e = launch_update_factors_batched(h, count, layers, x, nullptr, gy, nullptr,
+                                                rows.data(), scale, decay.data(), stream, geoms);
+  if (e == KFAC_OK)
+    for (int i = 0; i < count; ++i) ++h->layers[layers[i]].t_factor;
+  return e;
+}
+
+kfac_status kfac_update_factors_conv2d(kfac_handle h, int layer, const void* x, const void* gy,
+                                       const kfac_conv2d_geom* geom, double scale,
+                                       cudaStream_t stream) {
+  if (!geom) return KFAC_ERR_INVALID_ARG;
+  return kfac_update_factors_conv2d_batched(h, 1, &layer, &x, &gy, geom, scale, stream);
 }
 
 kfac_status kfac_diag_factors(kfac_handle h, int layer, const void* a, int64_t lda,

@@ -16,6 +16,11 @@ constexpr size_t kAlign = 256;
 
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+// output extent of a 2-D convolution along one axis (may be < 1 for bad geometry)
+inline int conv_out(int in, int k, int stride, int pad, int dil) {
+  const int64_t span = (int64_t)in + 2 * (int64_t)pad - (int64_t)dil * (k - 1) - 1;
+  return span < 0 ? 0 : (int)(span / stride + 1);
+}
 
 // Device status word: first error wins.
 struct DevStatus {
@@ -128,11 +133,15 @@ kfac_status launch_diag_step_batched(kfac_ctx* h, int count, const int* layers,
                                      const float* const* gb, float* const* pw,
                                      float* const* pb, float* const* ow, float* const* ob,
                                      cudaStream_t s);
+// geoms == nullptr: a[i], g[i] row-major with lda[i], ldg[i].  Otherwise a[i] is
+// the NCHW input and g[i] the NCHW output gradient of the convolution geoms[i]
+// (lda, ldg unused; rows[i] = batch * out_h * out_w).
 kfac_status launch_update_factors_batched(kfac_ctx* h, int count, const int* layers,
                                           const void* const* a, const int64_t* lda,
                                           const void* const* g, const int64_t* ldg,
                                           const int64_t* rows, double scale, const float* decay,
-                                          cudaStream_t s);
+                                          cudaStream_t s,
+                                          const kfac_conv2d_geom* geoms = nullptr);
 // K2 / K3
 kfac_status launch_invert(kfac_ctx* h, int layer, cudaStream_t s);
 // K4
@@ -180,7 +189,15 @@ kfac_status launch_syrk_tc(kfac_ctx* h, int layer, const void* x, int64_t ld, in
                            int n, int has_bias, bool bf16, float alpha, float beta, float* F,
                            cudaStream_t st);
 int64_t tc_pitch(int64_t cols, bool bf16);
-// x-hat -> X = x-hat^T (K-major; TF32 halves for fp32, bf16 copy), several at once
+// Source of a gathered pack: the input patches of a 2-D convolution over an
+// NCHW tensor [B, C, H, W] (output Ho x Wo), or, with a 1x1 unit-stride
+// geometry, the rows of an NCHW output gradient.
+struct ConvSrc {
+  int B, C, H, W, kh, kw, sh, sw, ph, pw, dh, dw, Ho, Wo;
+};
+// x-hat -> X = x-hat^T (K-major; TF32 halves for fp32, bf16 copy), several at once.
+// conv = 0: x-hat is row-major [M x d] with leading dimension ld (+ ones column);
+// conv = 1: x-hat's rows are gathered from the NCHW tensor x described by cs.
 struct PackJob {
   const void* x;
   int64_t ld, M;
@@ -188,6 +205,8 @@ struct PackJob {
   int64_t Kp;
   void* hi;
   void* lo;
+  int conv;
+  ConvSrc cs;
 };
 constexpr int kMaxPackJobs = 32;
 kfac_status launch_pack_grouped(const PackJob* jobs, int count, bool bf16, cudaStream_t st);

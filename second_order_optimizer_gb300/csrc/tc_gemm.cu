@@ -1081,6 +1081,80 @@ __global__ void __launch_bounds__(256) pack_kernel(const T* __restrict__ x, int6
                        blockIdx.y * 32);
 }
 
+// Gathered pack: X[c][r] for rows r of the input patches of a 2-D convolution
+// over the NCHW tensor x (column c = (channel, kernel row, kernel column), zero
+// outside the image; c = d is the ones column), or of an NCHW output gradient
+// (1x1, unit stride).  Consecutive rows are consecutive output positions, which
+// at unit stride are consecutive addresses of x, so loads and stores both run
+// along rows and no transpose is needed: thread t takes row r0 + t % kPackRows
+// and 16 of the tile's 32 columns, 16 loads in flight.  Each column's offset
+// into an image and its kernel displacement come from a table the CTA builds
+// once, so the per-element work is two bounds checks and an add.
+template <typename T, bool kSplit>
+__device__ __forceinline__ void pack_tile_conv(const T* __restrict__ x, const ConvSrc& g, int d,
+                                               int n, int64_t M, int64_t Kp, void* out_hi,
+                                               void* out_lo, int64_t r0, int c0) {
+  __shared__ int64_t col_off[32];
+  __shared__ int col_dy[32], col_dx[32];
+  if (threadIdx.x < 32) {
+    const int c = c0 + threadIdx.x;
+    int64_t off = -1;
+    int dy = 0, dx = 0;
+    if (c < d) {
+      const int khw = g.kh * g.kw, ci = c / khw, t = c - ci * khw, i = t / g.kw, j = t - i * g.kw;
+      dy = i * g.dh;
+      dx = j * g.dw;
+      off = (int64_t)ci * g.H * g.W + (int64_t)dy * g.W + dx;
+    }
+    col_off[threadIdx.x] = off;   // -1: ones column or past n
+    col_dy[threadIdx.x] = dy;
+    col_dx[threadIdx.x] = dx;
+  }
+  __syncthreads();
+  const int tr = threadIdx.x % kPackRows, half = threadIdx.x / kPackRows;
+  const int64_t r = r0 + tr;
+  const bool live = r < M;
+  int64_t base = 0;
+  int oy = 0, ox = 0;
+  if (live) {
+    const int64_t hw = (int64_t)g.Ho * g.Wo, img = r / hw;
+    const int p = (int)(r - img * hw), oh = p / g.Wo, ow = p - oh * g.Wo;
+    oy = oh * g.sh - g.ph;
+    ox = ow * g.sw - g.pw;
+    base = img * (int64_t)g.C * g.H * g.W + (int64_t)oy * g.W + ox;
+  }
+  float v[16];
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const int k = half * 16 + u, c = c0 + k;
+    float val = 0.f;
+    if (live && c < n) {
+      const int64_t off = col_off[k];
+      if (off < 0) {
+        val = 1.f;   // c == d: the ones column
+      } else {
+        const int y = oy + col_dy[k], xx = ox + col_dx[k];
+        if ((unsigned)y < (unsigned)g.H && (unsigned)xx < (unsigned)g.W)
+          val = to_f32<T>(x[base + off]);
+      }
+    }
+    v[u] = val;
+  }
+  if (r >= Kp) return;
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const int c = c0 + half * 16 + u;
+    if (c >= n) break;
+    if (kSplit) {
+      const float hi = tc::to_tf32(v[u]);
+      static_cast<float*>(out_hi)[(int64_t)c * Kp + r] = hi;
+      static_cast<float*>(out_lo)[(int64_t)c * Kp + r] = tc::to_tf32(v[u] - hi);
+    } else {
+      static_cast<__nv_bfloat16*>(out_hi)[(int64_t)c * Kp + r] = __float2bfloat16_rn(v[u]);
+    }
+  }
+}
+
 // Job q owns blocks [block_start[q], block_start[q+1]): its kPackRows x 32 tiles,
 // row tiles fastest (a grid sized by the largest job in each dimension would
 // schedule mostly empty blocks when the jobs differ in size).
@@ -1097,8 +1171,12 @@ __global__ void __launch_bounds__(256) pack_grouped_kernel(const __grid_constant
   while (q + 1 < g.count && b >= g.block_start[q + 1]) ++q;
   const PackJob J = g.job[q];
   const int64_t local = b - g.block_start[q], rt = (J.Kp + kPackRows - 1) / kPackRows;
-  pack_tile<T, kSplit>(static_cast<const T*>(J.x), J.ld, J.M, J.d, J.n, J.Kp, J.hi, J.lo,
-                       (local % rt) * kPackRows, (int)(local / rt) * 32);
+  if (J.conv)
+    pack_tile_conv<T, kSplit>(static_cast<const T*>(J.x), J.cs, J.d, J.n, J.M, J.Kp, J.hi, J.lo,
+                              (local % rt) * kPackRows, (int)(local / rt) * 32);
+  else
+    pack_tile<T, kSplit>(static_cast<const T*>(J.x), J.ld, J.M, J.d, J.n, J.Kp, J.hi, J.lo,
+                         (local % rt) * kPackRows, (int)(local / rt) * 32);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

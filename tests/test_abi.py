@@ -22,7 +22,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(kfac_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(kfac_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_five_verbs():
@@ -100,6 +100,9 @@ def test_null_handle_calls_fail_cleanly(lib):
     assert L.kfac_destroy(None) == 1
     assert L.kfac_get_status(None, None, None) == 1
     assert L.kfac_update_factors(None, 0, None, 1, None, 1, 1, 0.0, None) == 1
+    geom = lib.Conv2dGeom(1, 1, 3, 3, 3, 3, 1, 1, 1, 1, 1, 1)
+    assert L.kfac_update_factors_conv2d(None, 0, None, None, ctypes.byref(geom), 0.0, None) == 1
+    assert L.kfac_update_factors_conv2d(None, 0, None, None, None, 0.0, None) == 1
     assert L.kfac_precondition(None, 0, None, 1, None, None, None, None, None, None) == 1
     assert L.kfac_diag_step(None, 0, None, None, None, None, None, None, None, None, None) == 1
 

@@ -26,6 +26,34 @@ import numpy as np
 
 
 @dataclasses.dataclass(frozen=True)
+class ConvGeom:
+    """Geometry of a 2-D convolution over NCHW input [batch, c_in, h, w]."""
+    batch: int
+    c_in: int
+    h: int
+    w: int
+    kh: int
+    kw: int
+    sh: int = 1
+    sw: int = 1
+    ph: int = 0
+    pw: int = 0
+    dh: int = 1
+    dw: int = 1
+
+    @property
+    def h_out(self) -> int:
+        return (self.h + 2 * self.ph - self.dh * (self.kh - 1) - 1) // self.sh + 1
+
+    @property
+    def w_out(self) -> int:
+        return (self.w + 2 * self.pw - self.dw * (self.kw - 1) - 1) // self.sw + 1
+
+    def with_batch(self, batch: int) -> "ConvGeom":
+        return dataclasses.replace(self, batch=batch)
+
+
+@dataclasses.dataclass(frozen=True)
 class Layer:
     name: str
     kind: str            # "kron" (full Kronecker factors) or "diag" (diagonal Fisher)
@@ -35,6 +63,7 @@ class Layer:
     rows: int            # M: batch, or B*H_out*W_out for conv, or tokens
     act: str = "normal"  # "normal": a~N(0,1); "relu": max(N(0,1),0); "bn": BatchNorm layer
     in_dtype: str = "f32"  # "f32" or "bf16" for a and g
+    conv: Optional[ConvGeom] = None  # set for convolutions: rows = batch*h_out*w_out
 
     @property
     def n(self) -> int:
@@ -74,8 +103,10 @@ class Config:
         return [l for l in self.layers if l.kind == "diag"]
 
 
-def _conv(name, cin, cout, k, rows, act="relu", dt="f32"):
-    return Layer(name, "kron", cout, cin * k * k, 1, rows, act, dt)
+def _conv(name, cin, cout, k, rows, act="relu", dt="f32", geom=None):
+    if geom is not None:
+        assert geom.batch * geom.h_out * geom.w_out == rows and geom.c_in == cin
+    return Layer(name, "kron", cout, cin * k * k, 1, rows, act, dt, geom)
 
 
 def _bn(name, c, rows):
@@ -104,7 +135,7 @@ def resnet18_cifar() -> Config:
     """ResNet-18 (CIFAR stem) on 32x32 input, batch 128: 21 conv/fc layers + 20 BN."""
     B = 128
     L: List[Layer] = []
-    L.append(_conv("conv1", 3, 64, 3, B * 32 * 32))
+    L.append(_conv("conv1", 3, 64, 3, B * 32 * 32, geom=ConvGeom(B, 3, 32, 32, 3, 3, 1, 1, 1, 1)))
     L.append(_bn("bn1", 64, B * 32 * 32))
     cin, hw = 64, 32
     for stage, (c, stride) in enumerate([(64, 1), (128, 2), (256, 2), (512, 2)], 1):
@@ -112,12 +143,15 @@ def resnet18_cifar() -> Config:
             s = stride if blk == 0 else 1
             hw_out = hw // s
             rows = B * hw_out * hw_out
-            L.append(_conv(f"l{stage}.{blk}.conv1", cin, c, 3, rows))
+            L.append(_conv(f"l{stage}.{blk}.conv1", cin, c, 3, rows,
+                           geom=ConvGeom(B, cin, hw, hw, 3, 3, s, s, 1, 1)))
             L.append(_bn(f"l{stage}.{blk}.bn1", c, rows))
-            L.append(_conv(f"l{stage}.{blk}.conv2", c, c, 3, rows))
+            L.append(_conv(f"l{stage}.{blk}.conv2", c, c, 3, rows,
+                           geom=ConvGeom(B, c, hw_out, hw_out, 3, 3, 1, 1, 1, 1)))
             L.append(_bn(f"l{stage}.{blk}.bn2", c, rows))
             if blk == 0 and (s != 1 or cin != c):
-                L.append(_conv(f"l{stage}.{blk}.short", cin, c, 1, rows))
+                L.append(_conv(f"l{stage}.{blk}.short", cin, c, 1, rows,
+                               geom=ConvGeom(B, cin, hw, hw, 1, 1, s, s, 0, 0)))
                 L.append(_bn(f"l{stage}.{blk}.short_bn", c, rows))
             cin, hw = c, hw_out
     L.append(Layer("fc", "kron", 100, 512, 1, B, "relu"))
@@ -129,7 +163,8 @@ def resnet50_imagenet(dtype: str = "f32") -> Config:
     """ResNet-50 (v1.5: stride in the 3x3) on 224x224 input, batch 32: 54 + 53 BN."""
     B = 32
     L: List[Layer] = []
-    L.append(_conv("conv1", 3, 64, 7, B * 112 * 112, "normal", dtype))
+    L.append(_conv("conv1", 3, 64, 7, B * 112 * 112, "normal", dtype,
+                   ConvGeom(B, 3, 224, 224, 7, 7, 2, 2, 3, 3)))
     L.append(_bn("bn1", 64, B * 112 * 112))
     cin, hw = 64, 56
     for stage, (w, nblk, stride) in enumerate([(64, 3, 1), (128, 4, 2), (256, 6, 2), (512, 3, 2)], 1):
@@ -139,14 +174,18 @@ def resnet50_imagenet(dtype: str = "f32") -> Config:
             hw_out = hw // s
             r_in, r_out = B * hw * hw, B * hw_out * hw_out
             p = f"l{stage}.{blk}"
-            L.append(_conv(p + ".conv1", cin, w, 1, r_in, dt=dtype))
+            L.append(_conv(p + ".conv1", cin, w, 1, r_in, dt=dtype,
+                           geom=ConvGeom(B, cin, hw, hw, 1, 1)))
             L.append(_bn(p + ".bn1", w, r_in))
-            L.append(_conv(p + ".conv2", w, w, 3, r_out, dt=dtype))
+            L.append(_conv(p + ".conv2", w, w, 3, r_out, dt=dtype,
+                           geom=ConvGeom(B, w, hw, hw, 3, 3, s, s, 1, 1)))
             L.append(_bn(p + ".bn2", w, r_out))
-            L.append(_conv(p + ".conv3", w, out, 1, r_out, dt=dtype))
+            L.append(_conv(p + ".conv3", w, out, 1, r_out, dt=dtype,
+                           geom=ConvGeom(B, w, hw_out, hw_out, 1, 1)))
             L.append(_bn(p + ".bn3", out, r_out))
             if blk == 0:
-                L.append(_conv(p + ".down", cin, out, 1, r_out, dt=dtype))
+                L.append(_conv(p + ".down", cin, out, 1, r_out, dt=dtype,
+                               geom=ConvGeom(B, cin, hw, hw, 1, 1, s, s, 0, 0)))
                 L.append(_bn(p + ".down_bn", out, r_out))
             cin, hw = out, hw_out
     L.append(Layer("fc", "kron", 1000, 2048, 1, B, "relu", dtype))
@@ -271,6 +310,25 @@ def layer_inputs(cfg: Config, li: int, step: int, rows: Optional[int] = None):
     return out
 
 
+def conv_seed(cfg_index: int, layer_index: int, step: int) -> int:
+    """Seed of a convolution's NCHW draws (odd, so it never equals a seed_for value)."""
+    return 2 * seed_for(cfg_index, layer_index, step) + 1
+
+
+def conv_inputs(cfg: Config, li: int, step: int, batch: Optional[int] = None):
+    """NCHW input x [B, C, H, W] and output gradient gy [B, o, Ho, Wo] of a
+    convolution layer (float32 holding values of the layer's input dtype):
+    x from the layer's activation distribution, gy ~ N(0, g_std^2).  ``batch``
+    overrides B (small test cases)."""
+    L = cfg.layers[li]
+    cg = L.conv if batch is None else L.conv.with_batch(batch)
+    rng = np.random.Generator(np.random.PCG64(conv_seed(cfg.index, li, step)))
+    x = round_input(_act(rng, (cg.batch, cg.c_in, cg.h, cg.w), L.act), L.in_dtype)
+    gy = round_input(rng.standard_normal((cg.batch, L.d_out, cg.h_out, cg.w_out)) * cfg.g_std,
+                     L.in_dtype)
+    return {"x": x, "gy": gy, "geom": cg}
+
+
 # ----------------------------------------------------------------------------
 # Device draws for the large configs (torch is imported lazily)
 
@@ -315,3 +373,19 @@ def initial_params_torch(cfg: Config, li: int, device):
     w = torch.randn(L.d_out, L.d_in, generator=gen, device=device) * std
     b = torch.randn(L.d_out, generator=gen, device=device) * std if L.has_bias else None
     return w, b
+
+
+def conv_inputs_torch(cfg: Config, li: int, step: int, device, batch: Optional[int] = None):
+    """Same distributions as :func:`conv_inputs`, drawn on ``device`` with a seeded
+    torch.Generator; x and gy in the layer's input dtype."""
+    import torch
+    L = cfg.layers[li]
+    cg = L.conv if batch is None else L.conv.with_batch(batch)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(conv_seed(cfg.index, li, step))
+    tdt = torch.bfloat16 if L.in_dtype == "bf16" else torch.float32
+    x = torch.randn(cg.batch, cg.c_in, cg.h, cg.w, generator=gen, device=device)
+    if L.act == "relu":
+        x.clamp_(min=0.0)
+    gy = torch.randn(cg.batch, L.d_out, cg.h_out, cg.w_out, generator=gen, device=device)
+    return {"x": x.to(tdt), "gy": (gy * cfg.g_std).to(tdt), "geom": cg}
