@@ -43,6 +43,10 @@ one is also listed in the repository's design notes):
   R9  a convolution's activation rows are its zero-padded input patches, one
       per (image, output position), columns in weight order (c, i, j); its
       output-gradient rows are the channels at the same positions.
+  R10 stale factors: a step recomputes and re-inverts every factor during a
+      warm-up of w steps, afterwards A every k_A and G every k_G steps counted
+      from the end of the warm-up; a factor skipped on a step keeps both its
+      running value and its inverse.
 
 Parity pins for every function live in tests/test_oracle.py.
 """
@@ -250,6 +254,22 @@ def diag_precondition(gw_hat, gs, as_, damping: float) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# stale-factor schedule (Osawa et al. §5.4)
+
+def stale_refresh(t: int, warmup: int, every_a: int, every_g: int):
+    """Which factors a step t (1-based) recomputes and re-inverts (reading R10).
+
+    Every step during the first ``warmup`` steps, while the Fisher changes
+    fast; after that A every ``every_a`` steps and G every ``every_g`` steps
+    (the page observes that A fluctuates less than G, so every_a >= every_g is
+    the intended use), counted from the end of the warm-up.  Returns (A, G)."""
+    if t <= warmup:
+        return True, True
+    u = t - warmup
+    return u % every_a == 0, u % every_g == 0
+
+
+# ---------------------------------------------------------------------------
 # the whole per-layer step
 
 class LayerState:
@@ -299,6 +319,38 @@ class KfacOracle:
             st.Ainv = damped_inverse(st.A, self.gamma)
             st.Ginv = damped_inverse(st.G, self.gamma)
         P = precondition(st.Ginv, grad_hat(grad_w, grad_b if st.has_bias else None), st.Ainv)
+        st.W, st.m = momentum_update(P, st.W, st.m, self.lr, self.mu, self.wd)
+        st.P = P
+        return P
+
+    def step_kron_sched(self, st: LayerState, a, g, grad_w, grad_b=None, update=(True, True),
+                        refresh=(True, True), scale=None, shared_a: "LayerState" = None):
+        """One K-FAC step with an explicit per-factor schedule (Osawa et al. §5.4:
+        stale factors).  update = (A, G): fold the new factor into the running
+        one this step; refresh = (A, G): recompute that factor's damped inverse.
+        A factor not updated keeps its running value, one not refreshed keeps
+        the inverse of its latest refresh.  ``shared_a``: this layer has no A of
+        its own and preconditions with that layer's current A inverse (layers
+        fed the same input build the same A).  The EMA-first option counts each
+        factor's own updates.  Returns P [o, n]."""
+        st.t += 1
+        if shared_a is None:
+            if update[0]:
+                st.ta = getattr(st, "ta", 0) + 1
+                st.A = self._blend(st.A, factor(a, st.has_bias, scale), st.ta)
+            if refresh[0]:
+                st.Ainv = damped_inverse(st.A, self.gamma)
+            Ainv = st.Ainv
+        else:
+            Ainv = shared_a.Ainv
+        if update[1]:
+            st.tg = getattr(st, "tg", 0) + 1
+            st.G = self._blend(st.G, factor(g, 0, scale), st.tg)
+        if refresh[1]:
+            st.Ginv = damped_inverse(st.G, self.gamma)
+        if Ainv is None or st.Ginv is None:
+            raise ValueError("precondition before the first refresh of both factors")
+        P = precondition(st.Ginv, grad_hat(grad_w, grad_b if st.has_bias else None), Ainv)
         st.W, st.m = momentum_update(P, st.W, st.m, self.lr, self.mu, self.wd)
         st.P = P
         return P

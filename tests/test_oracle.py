@@ -370,3 +370,79 @@ def test_conv_G_is_channel_covariance_over_positions():
     _, G = O.conv_factors(x, gy, (1, 1))
     ref = np.einsum("bchw,bdhw->cd", gy, gy) / (3 * 5 * 2)
     np.testing.assert_allclose(G, ref, rtol=1e-14, atol=0)
+
+
+# ---------------------------------------------------------------- stale-factor schedule
+
+def test_stale_refresh_hand_example():
+    """warm-up 3, A every 4, G every 2: steps 1-3 both; then G at 5, 7, 9; A at 7, 11."""
+    got = [O.stale_refresh(t, 3, 4, 2) for t in range(1, 12)]
+    want = [(True, True)] * 3 + [(False, False), (False, True), (False, False), (True, True),
+                                 (False, False), (False, True), (False, False), (True, True)]
+    assert got == want
+
+
+@pytest.mark.parametrize("T,w,ka,kg", [(1000, 500, 20, 5), (37, 0, 7, 3), (10, 10, 3, 3)])
+def test_stale_refresh_counts_closed_form(T, w, ka, kg):
+    """Refreshes in T steps: w + floor((T - w)/k) for each factor."""
+    flags = [O.stale_refresh(t, w, ka, kg) for t in range(1, T + 1)]
+    assert sum(f[0] for f in flags) == w + (T - w) // ka
+    assert sum(f[1] for f in flags) == w + (T - w) // kg
+
+
+def _sched_layer(seed, o=5, d=4, bias=1):
+    rng = np.random.default_rng(seed)
+    w0 = rng.standard_normal((o, d))
+    b0 = rng.standard_normal(o)
+    return O.LayerState("kron", o, d, bias, w0, b0), rng
+
+
+def test_schedule_all_true_reduces_to_plain_step():
+    """update = refresh = (True, True) every step is the plain step with k = 1."""
+    orc = O.KfacOracle(0.9, 1e-2, 0.1, 0.9, 1e-3, invert_every=1)
+    s1, rng = _sched_layer(3)
+    s2, _ = _sched_layer(3)
+    for _ in range(4):
+        a, g = rng.standard_normal((20, 4)), rng.standard_normal((20, 5))
+        gw, gb = rng.standard_normal((5, 4)), rng.standard_normal(5)
+        P1 = orc.step_kron(s1, a, g, gw, gb)
+        P2 = orc.step_kron_sched(s2, a, g, gw, gb)
+        np.testing.assert_array_equal(P1, P2)
+        np.testing.assert_array_equal(s1.W, s2.W)
+
+
+def test_schedule_skipped_factor_keeps_value_and_inverse():
+    """A skipped update leaves the running factor unchanged; a skipped refresh
+    leaves the inverse unchanged, so P moves only through dW-hat and G."""
+    orc = O.KfacOracle(0.9, 1e-2, 0.1, 0.9, 1e-3)
+    st, rng = _sched_layer(5)
+    a, g = rng.standard_normal((20, 4)), rng.standard_normal((20, 5))
+    gw, gb = rng.standard_normal((5, 4)), rng.standard_normal(5)
+    orc.step_kron_sched(st, a, g, gw, gb)
+    A1, Ai1, G1 = st.A.copy(), st.Ainv.copy(), st.G.copy()
+    a2, g2 = 3 * rng.standard_normal((20, 4)), rng.standard_normal((20, 5))
+    P = orc.step_kron_sched(st, a2, g2, gw, gb, update=(False, True), refresh=(False, True))
+    np.testing.assert_array_equal(st.A, A1)
+    np.testing.assert_array_equal(st.Ainv, Ai1)
+    assert not np.array_equal(st.G, G1)
+    # P = Ginv dW Ainv with the new G inverse and the old A inverse, by LAPACK
+    Gd = st.G + math.sqrt(1e-2) * np.eye(5)
+    Ad = A1 + math.sqrt(1e-2) * np.eye(5)
+    ref = np.linalg.solve(Gd, np.linalg.solve(Ad.T, O.grad_hat(gw, gb).T).T)
+    np.testing.assert_allclose(P, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_shared_a_uses_the_source_inverse():
+    """A layer sharing another's A preconditions with the source's A inverse."""
+    orc = O.KfacOracle(0.9, 1e-2, 0.1, 0.9, 1e-3)
+    src, rng = _sched_layer(8)
+    tied, _ = _sched_layer(9)
+    a, g, g2 = (rng.standard_normal((20, 4)), rng.standard_normal((20, 5)),
+                rng.standard_normal((20, 5)))
+    gw, gb = rng.standard_normal((5, 4)), rng.standard_normal(5)
+    orc.step_kron_sched(src, a, g, gw, gb)
+    P = orc.step_kron_sched(tied, None, g2, gw, gb, shared_a=src)
+    Gd = O.factor(g2, 0) * 0.1 + math.sqrt(1e-2) * np.eye(5)      # zero-start EMA, xi = 0.9
+    Ad = O.factor(a, 1) * 0.1 + math.sqrt(1e-2) * np.eye(5)
+    ref = np.linalg.solve(Gd, np.linalg.solve(Ad.T, O.grad_hat(gw, gb).T).T)
+    np.testing.assert_allclose(P, ref, rtol=1e-10, atol=1e-12)
