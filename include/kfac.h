@@ -105,6 +105,9 @@ typedef enum {
   KFAC_STATE_ADIAG = 6   /* DIAG: running a diagonal, n                             */
 } kfac_state_which;
 
+/* Factors of a KRON layer, for kfac_invert_factors (bit mask). */
+typedef enum { KFAC_FACTOR_A = 1, KFAC_FACTOR_G = 2 } kfac_factor;
+
 /* Bytes of device workspace needed for these layers (256-byte multiple).
  * max_rows: the largest M any kfac_update_factors / kfac_diag_factors call
  * will pass for any layer (sizes the row-block scratch). */
@@ -127,6 +130,10 @@ kfac_status kfac_set_hparams(kfac_handle h, const kfac_hparams* hp);
  *   G <- xi G + (1-xi) s g^T g
  * a: [rows x d_in] with leading dimension lda; g: [rows x d_out], ldg; both of
  * the layer's in_dtype.  scale <= 0 means s = 1/rows.  1 <= rows <= max_rows.
+ * a may be NULL: A is left as it is (a stale factor, Osawa et al. §5.4, or a
+ * layer whose A is tied to another's, which requires it); g may be NULL
+ * likewise; not both.  With the EMA_INIT_FIRST option each factor's first
+ * update replaces it.
  * Osawa et al. §3.2 (factors), §3.4 (symmetry: only the upper triangle is
  * computed; the lower is its mirror); CAFIN Introduction (EMA of the factors). */
 kfac_status kfac_update_factors(kfac_handle h, int layer, const void* a, int64_t lda,
@@ -167,6 +174,7 @@ typedef struct {
  * the output gradient at the same positions; M = batch*out_h*out_w.
  * x: [batch, in_channels, in_h, in_w] contiguous; gy: [batch, d_out, out_h,
  * out_w] contiguous; both of the layer's in_dtype.  scale <= 0 means s = 1/M.
+ * x (gy) may be NULL to leave A (G) as it is, as in kfac_update_factors.
  * Requires d_in == in_channels*kernel_h*kernel_w, every size >= 1, pad >= 0,
  * 1 <= M <= max_rows and each tensor below 2^31 elements; otherwise
  * KFAC_ERR_INVALID_ARG before any launch.  The result equals
@@ -216,13 +224,38 @@ kfac_status kfac_diag_factors_batched(kfac_handle h, int count, const int* layer
  * every few steps, so this call is made every k-th step by the caller). */
 kfac_status kfac_invert(kfac_handle h, int layer, cudaStream_t stream);
 
+/* K2+K3 for a chosen factor: which = KFAC_FACTOR_A, KFAC_FACTOR_G or both
+ * (bit or).  The same as kfac_invert restricted to those factors, so A and G
+ * may be refreshed on their own cadences (Osawa et al. §5.4: after a warm-up
+ * the refreshes are made rarer, and A, which fluctuates less than G, may be
+ * refreshed less often).  A factor not refreshed keeps the inverse of its
+ * latest refresh.  A layer whose A is tied (kfac_tie_a_factor) has no A of its
+ * own: KFAC_FACTOR_A is ignored for it (its source's refresh covers it).
+ * which outside 1..3: KFAC_ERR_INVALID_ARG. */
+kfac_status kfac_invert_factors(kfac_handle h, int layer, int which, cudaStream_t stream);
+
+/* Tie layer's A factor to source's: from now on `layer` uses source's running
+ * A and A inverse (kfac_state_info reports source's), has no A update or
+ * inversion of its own, and its kfac_update_factors* calls must pass a NULL
+ * a (any other a: KFAC_ERR_INVALID_ARG).  For layers fed the same input (the
+ * query, key and value projections of an attention block), whose A factors
+ * are identical: the factor is built and inverted once.  Both KRON layers of
+ * the same n = d_in + has_bias, layer != source, source not itself tied, no
+ * layer tied to `layer`, and no factor update or inversion made yet on either
+ * (else KFAC_ERR_INVALID_ARG or KFAC_ERR_STATE).  Synchronous: rewrites the
+ * handle's inversion tables on the device, so call it before any work is
+ * enqueued on the handle.  Osawa et al. §3.2 (A is built from the layer's
+ * input activations alone). */
+kfac_status kfac_tie_a_factor(kfac_handle h, int layer, int source);
+
 /* K4: preconditioned gradient P = Ginv . [dW | db] . Ainv of a KRON layer.
  * grad_w: [o x d_in] fp32, ld ldgw; grad_b: [o] (required iff has_bias).
  * out_w [o x d_in] (ld d_in) / out_b [o]: P, nullable when param_w is given.
  * param_w [o x d_in] (ld d_in) / param_b [o]: nullable; when given the update
  *   u = P + lambda W ; m <- mu m + u ; W <- W - eta m   is applied in place
- * (m is library state).  Returns KFAC_ERR_STATE before the layer's first
- * kfac_invert.  CAFIN Kernel Fusion Strategy (precondition, momentum, weight
+ * (m is library state).  Returns KFAC_ERR_STATE until both of the layer's
+ * inverses exist (for a tied A, its source's).  CAFIN Kernel Fusion Strategy
+ * (precondition, momentum, weight
  * decay, in-place write); Osawa et al. §3.2. */
 kfac_status kfac_precondition(kfac_handle h, int layer, const float* grad_w, int64_t ldgw,
                               const float* grad_b, float* out_w, float* out_b,

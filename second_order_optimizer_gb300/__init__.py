@@ -14,6 +14,7 @@ import os
 from typing import Optional, Sequence
 
 from ._lib import (LIB, KFAC_KRON, KFAC_DIAG, KFAC_F32, KFAC_BF16, KFAC_MATH_3XTF32,
+                   KFAC_FACTOR_A, KFAC_FACTOR_G,
                    KFAC_MATH_BF16, KFAC_EMA_INIT_ZERO, KFAC_EMA_INIT_FIRST, KFAC_STATE_A,
                    KFAC_STATE_G, KFAC_STATE_AINV, KFAC_STATE_GINV, KFAC_STATE_MOMENTUM,
                    KFAC_STATE_GDIAG, KFAC_STATE_ADIAG, LayerDesc, HParams, Conv2dGeom, KfacError,
@@ -22,7 +23,8 @@ from ._lib import (LIB, KFAC_KRON, KFAC_DIAG, KFAC_F32, KFAC_BF16, KFAC_MATH_3XT
 __all__ = ["Kfac", "diag_factors_static", "conv2d_geom", "LayerDesc", "HParams", "Conv2dGeom",
            "KfacError", "status_string", "launch_count",
            "KFAC_KRON", "KFAC_DIAG", "KFAC_F32", "KFAC_BF16", "KFAC_MATH_3XTF32",
-           "KFAC_MATH_BF16", "KFAC_EMA_INIT_ZERO", "KFAC_EMA_INIT_FIRST", "LIB"]
+           "KFAC_MATH_BF16", "KFAC_EMA_INIT_ZERO", "KFAC_EMA_INIT_FIRST", "KFAC_FACTOR_A",
+           "KFAC_FACTOR_G", "LIB"]
 
 
 def _ptr(t) -> Optional[int]:
@@ -112,27 +114,34 @@ class Kfac:
     # -- the five verbs ---------------------------------------------------------
     def update_factors(self, layer: int, a, g, rows: Optional[int] = None, scale: float = 0.0,
                        stream=None, lda: Optional[int] = None, ldg: Optional[int] = None):
-        rows = a.shape[0] if rows is None else rows
-        lda = a.stride(0) if lda is None else lda
-        ldg = g.stride(0) if ldg is None else ldg
+        """a or g may be None: that factor is left as it is."""
+        rows = (a if a is not None else g).shape[0] if rows is None else rows
+        lda = (a.stride(0) if a is not None else 0) if lda is None else lda
+        ldg = (g.stride(0) if g is not None else 0) if ldg is None else ldg
         _check(LIB.kfac_update_factors(self._h, layer, _ptr(a), lda, _ptr(g), ldg, rows,
                                        float(scale), _stream(stream)), "kfac_update_factors")
 
     def update_factors_batched(self, layers, a_list, g_list, scale: float = 0.0, stream=None):
-        """kfac_update_factors_batched over parallel lists of layers and input tensors."""
+        """kfac_update_factors_batched over parallel lists of layers and input tensors
+        (an entry of a_list or g_list may be None: that factor is left as it is)."""
         k = len(layers)
         I64 = ctypes.c_int64 * k
         P = ctypes.c_void_p * k
+        st = lambda x: x.stride(0) if x is not None else 0
+        rows = [(x if x is not None else y).shape[0] for x, y in zip(a_list, g_list)]
         _check(LIB.kfac_update_factors_batched(
             self._h, k, (ctypes.c_int * k)(*layers), P(*[_ptr(x) for x in a_list]),
-            I64(*[x.stride(0) for x in a_list]), P(*[_ptr(x) for x in g_list]),
-            I64(*[x.stride(0) for x in g_list]), I64(*[x.shape[0] for x in a_list]),
+            I64(*[st(x) for x in a_list]), P(*[_ptr(x) for x in g_list]),
+            I64(*[st(x) for x in g_list]), I64(*rows),
             float(scale), _stream(stream)), "kfac_update_factors_batched")
 
     def update_factors_conv2d(self, layer: int, x, gy, kernel, stride=1, padding=0, dilation=1,
-                              scale: float = 0.0, stream=None):
-        """kfac_update_factors_conv2d: x [B, C, H, W] and gy [B, o, Ho, Wo], both contiguous."""
-        geom = conv2d_geom(x.shape, kernel, stride, padding, dilation)
+                              scale: float = 0.0, stream=None, in_shape=None):
+        """kfac_update_factors_conv2d: x [B, C, H, W] and gy [B, o, Ho, Wo], both contiguous.
+        Either may be None to leave that factor as it is; with x None the geometry
+        takes the input's shape from in_shape."""
+        geom = conv2d_geom(x.shape if x is not None else in_shape, kernel, stride, padding,
+                           dilation)
         _check(LIB.kfac_update_factors_conv2d(self._h, layer, _ptr(x), _ptr(gy),
                                               ctypes.byref(geom), float(scale), _stream(stream)),
                "kfac_update_factors_conv2d")
@@ -167,8 +176,17 @@ class Kfac:
             float(scale), P(*[_ptr(x) for x in g_new]), P(*[_ptr(x) for x in a_new]),
             _stream(stream)), "kfac_diag_factors_batched")
 
-    def invert(self, layer: int = -1, stream=None):
-        _check(LIB.kfac_invert(self._h, layer, _stream(stream)), "kfac_invert")
+    def invert(self, layer: int = -1, stream=None, which: int = KFAC_FACTOR_A | KFAC_FACTOR_G):
+        """kfac_invert, or kfac_invert_factors for which = KFAC_FACTOR_A or KFAC_FACTOR_G."""
+        if which == KFAC_FACTOR_A | KFAC_FACTOR_G:
+            _check(LIB.kfac_invert(self._h, layer, _stream(stream)), "kfac_invert")
+        else:
+            _check(LIB.kfac_invert_factors(self._h, layer, which, _stream(stream)),
+                   "kfac_invert_factors")
+
+    def tie_a_factor(self, layer: int, source: int):
+        """kfac_tie_a_factor: layer uses source's A (same input); synchronous."""
+        _check(LIB.kfac_tie_a_factor(self._h, layer, source), "kfac_tie_a_factor")
 
     def precondition(self, layer: int, grad_w, grad_b=None, out_w=None, out_b=None,
                      param_w=None, param_b=None, stream=None):

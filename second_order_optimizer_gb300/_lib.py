@@ -18,6 +18,7 @@ KFAC_KRON, KFAC_DIAG = 0, 1
 KFAC_F32, KFAC_BF16 = 0, 1
 KFAC_MATH_3XTF32, KFAC_MATH_BF16 = 0, 1
 KFAC_EMA_INIT_ZERO, KFAC_EMA_INIT_FIRST = 0, 1
+KFAC_FACTOR_A, KFAC_FACTOR_G = 1, 2
 (KFAC_STATE_A, KFAC_STATE_G, KFAC_STATE_AINV, KFAC_STATE_GINV, KFAC_STATE_MOMENTUM,
  KFAC_STATE_GDIAG, KFAC_STATE_ADIAG) = range(7)
 
@@ -67,6 +68,8 @@ SIGNATURES = [
     ("kfac_diag_factors_batched", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _d, _vp, _vp,
                                        _vp]),
     ("kfac_invert", _i, [_vp, _i, _vp]),
+    ("kfac_invert_factors", _i, [_vp, _i, _i, _vp]),
+    ("kfac_tie_a_factor", _i, [_vp, _i, _i]),
     ("kfac_precondition", _i, [_vp, _i, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     ("kfac_precondition_batched", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     ("kfac_diag_step", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),

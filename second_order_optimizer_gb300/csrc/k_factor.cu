@@ -180,26 +180,32 @@ size_t k1_scratch_floats(int n, int64_t max_rows, size_t* tickets) {
 
 kfac_status launch_update_factors(kfac_ctx* h, int layer, const void* a, int64_t lda,
                                   const void* g, int64_t ldg, int64_t rows, double scale,
-                                  float decay, cudaStream_t st) {
+                                  float decay_a, float decay_g, cudaStream_t st) {
   const LayerInfo& L = h->layers[layer];
   const double s = scale > 0 ? scale : 1.0 / (double)rows;
-  const float alpha = (float)((1.0 - (double)decay) * s);
   const bool bf16 = L.in_dtype == KFAC_BF16;
-  kfac_status e = launch_syrk_tc(h, layer, a, lda, rows, L.d_in, L.n, L.has_bias, bf16, alpha,
-                                 decay, h->at<float>(L.A), st);
-  if (e != KFAC_OK) return e;
-  return launch_syrk_tc(h, layer, g, ldg, rows, L.o, L.o, 0, bf16, alpha, decay,
+  if (a) {
+    const float alpha = (float)((1.0 - (double)decay_a) * s);
+    kfac_status e = launch_syrk_tc(h, layer, a, lda, rows, L.d_in, L.n, L.has_bias, bf16, alpha,
+                                   decay_a, h->at<float>(L.A), st);
+    if (e != KFAC_OK) return e;
+  }
+  if (!g) return KFAC_OK;
+  const float alpha = (float)((1.0 - (double)decay_g) * s);
+  return launch_syrk_tc(h, layer, g, ldg, rows, L.o, L.o, 0, bf16, alpha, decay_g,
                         h->at<float>(L.G), st);
 }
 
 // Several layers' factor updates at once: every a and g of a group is packed in
 // one launch, then all their SYRKs run as one grouped tensor-core launch (tiles
 // of all layers fill the GPU together instead of each layer splitting K).  A
-// group is as many layers as the pack scratch holds.
+// group is as many layers as the pack scratch holds.  A null a[i] (g[i]) leaves
+// that layer's A (G) as it is.
 kfac_status launch_update_factors_batched(kfac_ctx* h, int count, const int* layers,
                                           const void* const* a, const int64_t* lda,
                                           const void* const* g, const int64_t* ldg,
-                                          const int64_t* rows, double scale, const float* decay,
+                                          const int64_t* rows, double scale,
+                                          const float* decay_a, const float* decay_g,
                                           cudaStream_t st, const kfac_conv2d_geom* geoms) {
   const bool bf16 = h->layers[layers[0]].in_dtype == KFAC_BF16;
   const size_t elt = bf16 ? 2 : 8;  // packed bytes per element (bf16, or two TF32 halves)
@@ -218,19 +224,23 @@ kfac_status launch_update_factors_batched(kfac_ctx* h, int count, const int* lay
   for (int i = 0; i < count; ++i) {
     const LayerInfo& L = h->layers[layers[i]];
     const int64_t Kp = tc_pitch(rows[i], bf16);
-    const size_t bA = align_up((size_t)L.n * Kp * elt), bG = align_up((size_t)L.o * Kp * elt);
+    const size_t bA = a[i] ? align_up((size_t)L.n * Kp * elt) : 0;
+    const size_t bG = g[i] ? align_up((size_t)L.o * Kp * elt) : 0;
     if (bA + bG > h->tcpack_bytes) return KFAC_ERR_WORKSPACE;
     if (used + bA + bG > h->tcpack_bytes)
       if (kfac_status e = flush()) return e;
     const double s = scale > 0 ? scale : 1.0 / (double)rows[i];
-    const float alpha = (float)((1.0 - (double)decay[i]) * s);
     for (int w = 0; w < 2; ++w) {
+      const void* src = w == 0 ? a[i] : g[i];
+      if (!src) continue;
+      const float decay = w == 0 ? decay_a[i] : decay_g[i];
+      const float alpha = (float)((1.0 - (double)decay) * s);
       const int n = w == 0 ? L.n : L.o;
       char* hi = h->ws + h->off_tcpack + used;
       char* lo = bf16 ? nullptr : hi + (size_t)n * Kp * 4;
       used += w == 0 ? bA : bG;
       PackJob j{};
-      j.x = w == 0 ? a[i] : g[i];
+      j.x = src;
       j.ld = geoms ? 0 : (w == 0 ? lda[i] : ldg[i]);
       j.M = rows[i];
       if (geoms) {
@@ -259,7 +269,7 @@ kfac_status launch_update_factors_batched(kfac_ctx* h, int count, const int* lay
       q.M = q.N = n;
       q.K = rows[i];
       q.e.alpha = alpha;
-      q.e.beta = decay[i];
+      q.e.beta = decay;
       q.e.C = h->at<float>(w == 0 ? L.A : L.G);
       q.e.ldc = n;
       q.layer = layers[i];

@@ -482,21 +482,24 @@ kfac_status launch_outer_update(kfac_ctx* h, int j0, int nj, int K0, int W, cuda
   return flush();
 }
 
-kfac_status launch_invert(kfac_ctx* h, int layer, cudaStream_t st) {
-  // job range: all KRON factors, or the two of one layer
+kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
+  // job range: the table section of the wanted factors (both, A only, G only),
+  // whole or the entries of one layer (contiguous: a section is in layer order)
   const InvJob* d_all = h->at<InvJob>(h->off_invjobs);
   const SyrkJob* d_syrk = h->at<SyrkJob>(h->off_invjobs + align_up(sizeof(InvJob) * h->n_invjobs));
-  int j0 = 0, nj = h->n_invjobs;
+  const int sec = which == (KFAC_FACTOR_A | KFAC_FACTOR_G) ? 0 : which == KFAC_FACTOR_A ? 1 : 2;
+  int j0 = h->tab_start[sec], nj = h->tab_count[sec];
   if (layer >= 0) {
-    j0 = -1;
-    for (int i = 0; i < h->n_invjobs; ++i)
+    int first = -1, cnt = 0;
+    for (int i = j0; i < j0 + nj; ++i)
       if (h->invjobs_host[i].layer == layer) {
-        j0 = i;
-        break;
+        if (first < 0) first = i;
+        ++cnt;
       }
-    if (j0 < 0) return KFAC_ERR_INVALID_ARG;
-    nj = 2;
+    j0 = first;
+    nj = cnt;
   }
+  if (nj == 0) return KFAC_OK;   // nothing of that kind to refresh (a tied A)
   int nmax = 0;
   for (int i = j0; i < j0 + nj; ++i) nmax = std::max(nmax, h->invjobs_host[i].n);
   const InvJob* jobs = d_all + j0;

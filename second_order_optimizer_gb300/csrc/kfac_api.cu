@@ -107,7 +107,7 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
       // batched K4 aligns each of its four arrays (dW-hat and X^T halves) separately
       k4_sum += 2 * (align_up(o * np * sizeof(float)) + align_up(n * op * sizeof(float))) /
                 sizeof(float);
-      ninv += 2;
+      ninv += 4;   // three table sections: both factors, A only, G only
       maxn = std::max({maxn, L.n, L.o});
     } else {
       L.gs = take(o * f);
@@ -171,11 +171,107 @@ kfac_status check_inputs(const kfac_ctx* h, const LayerInfo& L, const void* a, i
   return KFAC_OK;
 }
 
+}  // namespace
+
+// The inversion job tables: section 0 holds A then G of every KRON layer,
+// section 1 every A, section 2 every G, layers in order in each; a layer whose A
+// is tied to another layer's contributes no A job.  Each InvJob has a parallel
+// SyrkJob (the CUDA-core X^T X of the small factors).  Written to the host copy
+// and, synchronously, to the device.
+kfac_status write_inv_tables(kfac_ctx* h) {
+  h->invjobs_host.clear();
+  std::vector<SyrkJob> sj;
+  auto add = [&](int i, int w) {
+    const LayerInfo& L = h->layers[i];
+    InvJob j{};
+    const int n = w == 0 ? L.n : L.o;
+    j.F = h->at<float>(w == 0 ? L.A : L.G);
+    j.L = h->at<float>(w == 0 ? L.LA : L.LG);
+    j.X = h->at<float>(w == 0 ? L.XA : L.XG);
+    j.Y = h->at<float>(w == 0 ? L.YA : L.YG);
+    j.Finv = h->at<float>(w == 0 ? L.Ainv : L.Ginv);
+    j.Finv_hi = h->at<float>(w == 0 ? L.Ainv_hi : L.Ginv_hi);
+    j.Finv_lo = h->at<float>(w == 0 ? L.Ainv_lo : L.Ginv_lo);
+    j.n = n;
+    j.np = (int)tc_pitch(n, false);
+    j.layer = i;
+    h->invjobs_host.push_back(j);
+    SyrkJob s{};
+    s.x = j.X;
+    s.ld = n;
+    s.M = n;
+    s.d = n;
+    s.n = n;
+    s.has_bias = 0;
+    s.x_lower = 1;
+    s.alpha = 1.f;
+    s.beta = 0.f;
+    s.C = j.Finv;
+    s.nt = (int)cdiv(n, SyrkTile::BM);
+    s.splits = 1;
+    s.rows_per_split = n;
+    s.skip = n >= kTcInverseMinN ? 1 : 0;
+    sj.push_back(s);
+  };
+  const int nl = (int)h->layers.size();
+  const int masks[3] = {3, 1, 2};
+  for (int sec = 0; sec < 3; ++sec) {
+    h->tab_start[sec] = (int)h->invjobs_host.size();
+    for (int i = 0; i < nl; ++i) {
+      const LayerInfo& L = h->layers[i];
+      if (L.kind != KFAC_KRON) continue;
+      if ((masks[sec] & 1) && L.tied_to < 0) add(i, 0);
+      if (masks[sec] & 2) add(i, 1);
+    }
+    h->tab_count[sec] = (int)h->invjobs_host.size() - h->tab_start[sec];
+  }
+  if ((int)h->invjobs_host.size() > h->n_invjobs) return KFAC_ERR_WORKSPACE;
+  if (h->invjobs_host.empty()) return KFAC_OK;
+  bool ok = cudaMemcpy(h->ws + h->off_invjobs, h->invjobs_host.data(),
+                       sizeof(InvJob) * h->invjobs_host.size(), cudaMemcpyHostToDevice) == cudaSuccess;
+  ok = ok && cudaMemcpy(h->ws + h->off_invjobs + align_up(sizeof(InvJob) * h->n_invjobs), sj.data(),
+                        sizeof(SyrkJob) * sj.size(), cudaMemcpyHostToDevice) == cudaSuccess;
+  return ok ? KFAC_OK : KFAC_ERR_CUDA;
+}
+
+namespace {
+
+// Inputs of a KRON factor update: a and g each nullable (that factor is left
+// as it is), not both; a tied layer takes no a.
+kfac_status check_factor_inputs(const kfac_ctx* h, const LayerInfo& L, const void* a,
+                                int64_t lda, const void* g, int64_t ldg, int64_t rows) {
+  const size_t es = L.in_dtype == KFAC_BF16 ? 2 : 4;
+  if (!a && !g) return KFAC_ERR_INVALID_ARG;
+  if (a && (L.tied_to >= 0 || !aligned(a, es) || lda < L.d_in)) return KFAC_ERR_INVALID_ARG;
+  if (g && (!aligned(g, es) || ldg < L.o)) return KFAC_ERR_INVALID_ARG;
+  if (rows < 1 || rows > h->max_rows) return KFAC_ERR_INVALID_ARG;
+  return KFAC_OK;
+}
+
+// EMA weights of the old A and G for this update (0 for a factor's first update
+// under EMA_INIT_FIRST), and the update counters afterwards.
+void factor_decays(const kfac_ctx* h, const LayerInfo& L, float* da, float* dg) {
+  const bool first_mode = h->hp.ema_init == KFAC_EMA_INIT_FIRST;
+  *da = first_mode && L.t_a == 0 ? 0.f : (float)h->hp.ema_decay;
+  *dg = first_mode && L.t_g == 0 ? 0.f : (float)h->hp.ema_decay;
+}
+// Both inverses a KRON layer preconditions with exist (a tied A: its source's).
+bool has_inverses(const kfac_ctx* h, const LayerInfo& L) {
+  const bool a = L.tied_to >= 0 ? h->layers[L.tied_to].inv_a : L.inv_a;
+  return a && L.inv_g;
+}
+void count_updates(LayerInfo& L, const void* a, const void* g) {
+  if (a) ++L.t_a;
+  if (g) ++L.t_g;
+}
+
 // A convolution layer's NCHW inputs: geometry, sizes and alignment.
 kfac_status check_conv(const kfac_ctx* h, const LayerInfo& L, const void* x, const void* gy,
                        const kfac_conv2d_geom& g, int64_t* rows) {
   const size_t es = L.in_dtype == KFAC_BF16 ? 2 : 4;
-  if (!x || !gy || !aligned(x, es) || !aligned(gy, es)) return KFAC_ERR_INVALID_ARG;
+  if (!x && !gy) return KFAC_ERR_INVALID_ARG;
+  if (x && (L.tied_to >= 0 || !aligned(x, es))) return KFAC_ERR_INVALID_ARG;
+  if (gy && !aligned(gy, es)) return KFAC_ERR_INVALID_ARG;
   if (g.batch < 1 || g.in_channels < 1 || g.in_h < 1 || g.in_w < 1 || g.kernel_h < 1 ||
       g.kernel_w < 1 || g.stride_h < 1 || g.stride_w < 1 || g.pad_h < 0 || g.pad_w < 0 ||
       g.dilation_h < 1 || g.dilation_w < 1)
@@ -276,54 +372,11 @@ kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_
       return KFAC_ERR_CUDA;
     }
   }
-  // inversion tables: for each KRON layer, its A then its G
-  std::vector<SyrkJob> sj;
-  for (int i = 0; i < n_layers; ++i) {
-    const LayerInfo& L = h->layers[i];
-    if (L.kind != KFAC_KRON) continue;
-    for (int w = 0; w < 2; ++w) {
-      InvJob j{};
-      const int n = w == 0 ? L.n : L.o;
-      j.F = h->at<float>(w == 0 ? L.A : L.G);
-      j.L = h->at<float>(w == 0 ? L.LA : L.LG);
-      j.X = h->at<float>(w == 0 ? L.XA : L.XG);
-      j.Y = h->at<float>(w == 0 ? L.YA : L.YG);
-      j.Finv = h->at<float>(w == 0 ? L.Ainv : L.Ginv);
-      j.Finv_hi = h->at<float>(w == 0 ? L.Ainv_hi : L.Ginv_hi);
-      j.Finv_lo = h->at<float>(w == 0 ? L.Ainv_lo : L.Ginv_lo);
-      j.n = n;
-      j.np = (int)tc_pitch(n, false);
-      j.layer = i;
-      h->invjobs_host.push_back(j);
-      SyrkJob s{};
-      s.x = j.X;
-      s.ld = n;
-      s.M = n;
-      s.d = n;
-      s.n = n;
-      s.has_bias = 0;
-      s.x_lower = 1;
-      s.alpha = 1.f;
-      s.beta = 0.f;
-      s.C = j.Finv;
-      s.nt = (int)cdiv(n, SyrkTile::BM);
-      s.splits = 1;
-      s.rows_per_split = n;
-      s.skip = n >= kTcInverseMinN ? 1 : 0;
-      sj.push_back(s);
-    }
-  }
   bool ok = cudaMemset(d_workspace, 0, need) == cudaSuccess;
-  if (ok && !h->invjobs_host.empty()) {
-    ok = cudaMemcpy(h->ws + h->off_invjobs, h->invjobs_host.data(),
-                    sizeof(InvJob) * h->invjobs_host.size(), cudaMemcpyHostToDevice) == cudaSuccess;
-    ok = ok && cudaMemcpy(h->ws + h->off_invjobs + align_up(sizeof(InvJob) * h->n_invjobs),
-                          sj.data(), sizeof(SyrkJob) * sj.size(),
-                          cudaMemcpyHostToDevice) == cudaSuccess;
-  }
+  ok = ok && write_inv_tables(h) == KFAC_OK;
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
-    delete h;
+    kfac_destroy(h);
     return KFAC_ERR_CUDA;
   }
   *out = h;
@@ -342,13 +395,13 @@ kfac_status kfac_update_factors(kfac_handle h, int layer, const void* a, int64_t
                                 cudaStream_t stream) {
   if (kfac_status e = check_layer(h, layer, KFAC_KRON)) return e;
   LayerInfo& L = h->layers[layer];
-  if (kfac_status e = check_inputs(h, L, a, lda, g, ldg, rows)) return e;
+  if (kfac_status e = check_factor_inputs(h, L, a, lda, g, ldg, rows)) return e;
   if (!std::isfinite(scale)) return KFAC_ERR_INVALID_ARG;
   if (kfac_status e = ensure_device(h)) return e;
-  const bool first = L.t_factor == 0 && h->hp.ema_init == KFAC_EMA_INIT_FIRST;
-  const float decay = first ? 0.f : (float)h->hp.ema_decay;
-  kfac_status e = launch_update_factors(h, layer, a, lda, g, ldg, rows, scale, decay, stream);
-  if (e == KFAC_OK) ++L.t_factor;
+  float da, dg;
+  factor_decays(h, L, &da, &dg);
+  kfac_status e = launch_update_factors(h, layer, a, lda, g, ldg, rows, scale, da, dg, stream);
+  if (e == KFAC_OK) count_updates(L, a, g);
   return e;
 }
 
@@ -364,19 +417,15 @@ kfac_status kfac_update_factors_batched(kfac_handle h, int count, const int* lay
     if (seen[layers[i]]++) return KFAC_ERR_INVALID_ARG;   // a layer at most once per batch
     const LayerInfo& L = h->layers[layers[i]];
     if (L.in_dtype != h->layers[layers[0]].in_dtype) return KFAC_ERR_INVALID_ARG;
-    if (kfac_status e = check_inputs(h, L, a[i], lda[i], g[i], ldg[i], rows[i])) return e;
+    if (kfac_status e = check_factor_inputs(h, L, a[i], lda[i], g[i], ldg[i], rows[i])) return e;
   }
   if (kfac_status e = ensure_device(h)) return e;
-  std::vector<float> decay(count);
-  for (int i = 0; i < count; ++i) {
-    const LayerInfo& L = h->layers[layers[i]];
-    const bool first = L.t_factor == 0 && h->hp.ema_init == KFAC_EMA_INIT_FIRST;
-    decay[i] = first ? 0.f : (float)h->hp.ema_decay;
-  }
+  std::vector<float> da(count), dg(count);
+  for (int i = 0; i < count; ++i) factor_decays(h, h->layers[layers[i]], &da[i], &dg[i]);
   kfac_status e = launch_update_factors_batched(h, count, layers, a, lda, g, ldg, rows, scale,
-                                                decay.data(), stream);
+                                                da.data(), dg.data(), stream);
   if (e == KFAC_OK)
-    for (int i = 0; i < count; ++i) ++h->layers[layers[i]].t_factor;
+    for (int i = 0; i < count; ++i) count_updates(h->layers[layers[i]], a[i], g[i]);
   return e;
 }
 
@@ -396,16 +445,13 @@ kfac_status kfac_update_factors_conv2d_batched(kfac_handle h, int count, const i
     if (kfac_status e = check_conv(h, L, x[i], gy[i], geoms[i], &rows[i])) return e;
   }
   if (kfac_status e = ensure_device(h)) return e;
-  std::vector<float> decay(count);
-  for (int i = 0; i < count; ++i) {
-    const LayerInfo& L = h->layers[layers[i]];
-    const bool first = L.t_factor == 0 && h->hp.ema_init == KFAC_EMA_INIT_FIRST;
-    decay[i] = first ? 0.f : (float)h->hp.ema_decay;
-  }
+  std::vector<float> da(count), dg(count);
+  for (int i = 0; i < count; ++i) factor_decays(h, h->layers[layers[i]], &da[i], &dg[i]);
   kfac_status e = launch_update_factors_batched(h, count, layers, x, nullptr, gy, nullptr,
-                                                rows.data(), scale, decay.data(), stream, geoms);
+                                                rows.data(), scale, da.data(), dg.data(), stream,
+                                                geoms);
   if (e == KFAC_OK)
-    for (int i = 0; i < count; ++i) ++h->layers[layers[i]].t_factor;
+    for (int i = 0; i < count; ++i) count_updates(h->layers[layers[i]], x[i], gy[i]);
   return e;
 }
 
@@ -451,16 +497,49 @@ kfac_status kfac_diag_factors_batched(kfac_handle h, int count, const int* layer
                                      stream);
 }
 
-kfac_status kfac_invert(kfac_handle h, int layer, cudaStream_t stream) {
-  if (!h) return KFAC_ERR_INVALID_ARG;
+kfac_status kfac_invert_factors(kfac_handle h, int layer, int which, cudaStream_t stream) {
+  if (!h || which < 1 || which > 3) return KFAC_ERR_INVALID_ARG;
   if (layer != -1 && check_layer(h, layer, KFAC_KRON) != KFAC_OK) return KFAC_ERR_INVALID_ARG;
   if (h->n_invjobs == 0) return layer == -1 ? KFAC_OK : KFAC_ERR_INVALID_ARG;
   if (kfac_status e = ensure_device(h)) return e;
-  kfac_status e = launch_invert(h, layer, stream);
+  kfac_status e = launch_invert(h, layer, which, stream);
   if (e != KFAC_OK) return e;
-  for (int i = 0; i < (int)h->layers.size(); ++i)
-    if (h->layers[i].kind == KFAC_KRON && (layer == -1 || layer == i)) h->layers[i].inverted = true;
+  for (int i = 0; i < (int)h->layers.size(); ++i) {
+    LayerInfo& L = h->layers[i];
+    if (L.kind != KFAC_KRON || (layer != -1 && layer != i)) continue;
+    if ((which & KFAC_FACTOR_A) && L.tied_to < 0) L.inv_a = true;
+    if (which & KFAC_FACTOR_G) L.inv_g = true;
+  }
   return KFAC_OK;
+}
+
+kfac_status kfac_invert(kfac_handle h, int layer, cudaStream_t stream) {
+  return kfac_invert_factors(h, layer, KFAC_FACTOR_A | KFAC_FACTOR_G, stream);
+}
+
+kfac_status kfac_tie_a_factor(kfac_handle h, int layer, int source) {
+  if (!h || layer == source) return KFAC_ERR_INVALID_ARG;
+  if (kfac_status e = check_layer(h, layer, KFAC_KRON)) return e;
+  if (kfac_status e = check_layer(h, source, KFAC_KRON)) return e;
+  LayerInfo& L = h->layers[layer];
+  const LayerInfo& S = h->layers[source];
+  if (L.n != S.n || S.tied_to >= 0 || L.tied_to >= 0) return KFAC_ERR_INVALID_ARG;
+  for (const LayerInfo& X : h->layers)
+    if (X.tied_to == layer) return KFAC_ERR_INVALID_ARG;    // no chains
+  if (L.t_a || L.t_g || L.inv_a || L.inv_g || S.t_a || S.t_g || S.inv_a || S.inv_g)
+    return KFAC_ERR_STATE;
+  if (kfac_status e = ensure_device(h)) return e;
+  L.tied_to = source;
+  L.A = S.A;
+  L.LA = S.LA;
+  L.XA = S.XA;
+  L.YA = S.YA;
+  L.Ainv = S.Ainv;
+  L.Ainv_hi = S.Ainv_hi;
+  L.Ainv_lo = S.Ainv_lo;
+  kfac_status e = write_inv_tables(h);
+  if (e == KFAC_OK && cudaDeviceSynchronize() != cudaSuccess) e = KFAC_ERR_CUDA;
+  return e;
 }
 
 kfac_status kfac_precondition(kfac_handle h, int layer, const float* grad_w, int64_t ldgw,
@@ -473,7 +552,7 @@ kfac_status kfac_precondition(kfac_handle h, int layer, const float* grad_w, int
   if (!out_w && !param_w) return KFAC_ERR_INVALID_ARG;
   if (L.has_bias && out_w && !out_b) return KFAC_ERR_INVALID_ARG;
   if (L.has_bias && param_w && !param_b) return KFAC_ERR_INVALID_ARG;
-  if (!L.inverted) return KFAC_ERR_STATE;
+  if (!has_inverses(h, L)) return KFAC_ERR_STATE;
   if (kfac_status e = ensure_device(h)) return e;
   return launch_precondition(h, layer, grad_w, ldgw, L.has_bias ? grad_b : nullptr, out_w,
                              L.has_bias ? out_b : nullptr, param_w,
@@ -504,7 +583,7 @@ kfac_status kfac_precondition_batched(kfac_handle h, int count, const int* layer
     if (!o_w && !p_w) return KFAC_ERR_INVALID_ARG;
     if (L.has_bias && o_w && !o_b) return KFAC_ERR_INVALID_ARG;
     if (L.has_bias && p_w && !p_b) return KFAC_ERR_INVALID_ARG;
-    if (!L.inverted) return KFAC_ERR_STATE;
+    if (!has_inverses(h, L)) return KFAC_ERR_STATE;
     gb[i] = L.has_bias ? bw : nullptr;
     ob[i] = L.has_bias ? o_b : nullptr;
     pb[i] = L.has_bias ? p_b : nullptr;

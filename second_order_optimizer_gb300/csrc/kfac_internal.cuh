@@ -63,9 +63,10 @@ struct LayerInfo {
   size_t Ainv_hi, Ainv_lo, Ginv_hi, Ginv_lo;   // pitch n_p / o_p (multiples of 4)
   // DIAG state
   size_t gs, as, ticket;
-  // host-side counters
-  int64_t t_factor = 0, t_diag = 0;
-  bool inverted = false;
+  // host-side counters: updates of each factor, and whether each has an inverse
+  int64_t t_a = 0, t_g = 0, t_diag = 0;
+  bool inv_a = false, inv_g = false;
+  int tied_to = -1;   // KRON: the layer whose A (and A inverse) this layer uses, or -1
 };
 
 }  // namespace kfac
@@ -91,9 +92,12 @@ struct kfac_ctx {
   // K5 row-split partials and tickets
   size_t off_k5part = 0, k5part_floats = 0;
   size_t off_k5tickets = 0, k5tickets_ints = 0;
-  // inversion job table (all KRON factors, sorted by n descending)
+  // inversion job tables, three sections: [0] A then G of each KRON layer,
+  // [1] the A of each, [2] the G of each (layers in order; a layer whose A is
+  // tied to another's has no A job).  n_invjobs = capacity (4 per KRON layer).
   size_t off_invjobs = 0;
   int n_invjobs = 0;
+  int tab_start[3] = {0, 0, 0}, tab_count[3] = {0, 0, 0};
   std::vector<kfac::InvJob> invjobs_host;
   int max_kron_n = 0;
   // inversion lookahead: the bulk of each trailing update runs on a second
@@ -112,9 +116,10 @@ void count_launch(int n = 1);
 kfac_status check_launch();
 
 // K1
+// a or g null: that factor is left as it is
 kfac_status launch_update_factors(kfac_ctx* h, int layer, const void* a, int64_t lda,
                                   const void* g, int64_t ldg, int64_t rows, double scale,
-                                  float decay, cudaStream_t s);
+                                  float decay_a, float decay_g, cudaStream_t s);
 // K5 / K6
 kfac_status launch_diag_factors(kfac_ctx* h, int layer, const void* a, int64_t lda,
                                 const void* g, int64_t ldg, int64_t rows, double scale,
@@ -133,17 +138,21 @@ kfac_status launch_diag_step_batched(kfac_ctx* h, int count, const int* layers,
                                      const float* const* gb, float* const* pw,
                                      float* const* pb, float* const* ow, float* const* ob,
                                      cudaStream_t s);
-// geoms == nullptr: a[i], g[i] row-major with lda[i], ldg[i].  Otherwise a[i] is
+// geoms == nullptr: a[i], g[i] row-major with lda[i], ldg[i] (null: that factor
+// is left as it is).  Otherwise a[i] is
 // the NCHW input and g[i] the NCHW output gradient of the convolution geoms[i]
 // (lda, ldg unused; rows[i] = batch * out_h * out_w).
 kfac_status launch_update_factors_batched(kfac_ctx* h, int count, const int* layers,
                                           const void* const* a, const int64_t* lda,
                                           const void* const* g, const int64_t* ldg,
-                                          const int64_t* rows, double scale, const float* decay,
+                                          const int64_t* rows, double scale,
+                                          const float* decay_a, const float* decay_g,
                                           cudaStream_t s,
                                           const kfac_conv2d_geom* geoms = nullptr);
-// K2 / K3
-kfac_status launch_invert(kfac_ctx* h, int layer, cudaStream_t s);
+// K2 / K3: which = KFAC_FACTOR_A | KFAC_FACTOR_G; layer -1 = every KRON layer
+kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t s);
+// (re)write the inversion job tables on the host and the device (synchronous)
+kfac_status write_inv_tables(kfac_ctx* h);
 // K4
 kfac_status launch_precondition(kfac_ctx* h, int layer, const float* gw, int64_t ldgw,
                                 const float* gb, float* ow, float* ob, float* pw, float* pb,
