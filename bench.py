@@ -32,10 +32,25 @@ import workloads as Wl  # noqa: E402
 METRIC = "K-FAC precond steps/s; factor-GEMM TFLOP/s & diag-step GB/s vs GB300 peak"
 WORKLOADS = {"mlp4": "c2", "single_linear": "c1", "resnet18": "c3", "resnet50": "c4",
              "resnet50_bf16": "c4bf16", "transformer4": "c5",
-             "resnet18_nchw": "c3", "resnet50_nchw": "c4", "resnet50_bf16_nchw": "c4bf16"}
+             "resnet18_nchw": "c3", "resnet50_nchw": "c4", "resnet50_bf16_nchw": "c4bf16",
+             "transformer4_qkv_tied": "c5"}
 # workloads whose convolutions hand the library their NCHW input and output
 # gradient (kfac_update_factors_conv2d_batched) instead of unfolded matrices
 NCHW_WORKLOADS = {"resnet18_nchw", "resnet50_nchw", "resnet50_bf16_nchw"}
+# workloads whose key and value projections share the query projection's A
+# factor (kfac_tie_a_factor: the three read the same input)
+TIED_WORKLOADS = {"transformer4_qkv_tied"}
+
+
+def qkv_ties(layers):
+    """{tied layer index: source index}: b.k and b.v use b.q's A (KRON layers only)."""
+    pos = {l.name: i for i, l in enumerate(layers) if l.kind == "kron"}
+    ties = {}
+    for name, i in pos.items():
+        blk, _, proj = name.rpartition(".")
+        if proj in ("k", "v") and f"{blk}.q" in pos:
+            ties[i] = pos[f"{blk}.q"]
+    return ties
 # fallback roofline denominators when MEASURED_PEAKS.json is absent
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TF32_PER_BF16 = 1.1 / 2.25          # nominal dense ratio
@@ -135,24 +150,26 @@ def job_throughput(ms_per_step_max: float, world: int) -> float:
 
 # ----------------------------------------------------------------------------- accounting
 
-def algorithmic(layers, k, nchw=False):
+def algorithmic(layers, k, nchw=False, tied=()):
     """Per-step algorithmic flops and bytes of each phase (fp32 state, input dtype as given).
-    nchw: convolutions read their NCHW input and output gradient, not unfolded matrices."""
+    nchw: convolutions read their NCHW input and output gradient, not unfolded matrices.
+    tied: indices of layers whose A is another layer's (no A product or inverse)."""
     f = {"factor_flop": 0.0, "factor_bytes": 0.0, "invert_flop": 0.0, "precond_flop": 0.0,
          "precond_bytes": 0.0, "diag_bytes": 0.0, "diagfac_bytes": 0.0}
-    for l in layers:
+    for li, l in enumerate(layers):
         elt = 2 if l.in_dtype == "bf16" else 4
         n, o, M = l.n, l.d_out, l.rows
         if l.kind == "kron":
+            own_a = li not in tied
             # upper triangle only: M * n(n+1) flop (2 per FMA) per factor
-            f["factor_flop"] += M * n * (n + 1) + M * o * (o + 1)
+            f["factor_flop"] += M * n * (n + 1) * own_a + M * o * (o + 1)
             if nchw and l.conv is not None:
                 c = l.conv
                 f["factor_bytes"] += (c.batch * c.c_in * c.h * c.w + M * o) * elt
             else:
-                f["factor_bytes"] += M * (l.d_in + o) * elt
-            f["factor_bytes"] += 2 * 4 * (n * n + o * o)
-            f["invert_flop"] += (n ** 3 + o ** 3) / k     # Cholesky n^3/3 + L^-1 n^3/3 + X^T X n^3/3
+                f["factor_bytes"] += M * (l.d_in * own_a + o) * elt
+            f["factor_bytes"] += 2 * 4 * (n * n * own_a + o * o)
+            f["invert_flop"] += (n ** 3 * own_a + o ** 3) / k     # Cholesky n^3/3 + L^-1 n^3/3 + X^T X n^3/3
             f["precond_flop"] += 2 * o * n * n + 2 * o * o * n
             f["precond_bytes"] += 4 * (n * n + o * o + 2 * o * n) + 4 * 3 * o * n
         else:
@@ -232,7 +249,7 @@ def blas_threads():
     return len(os.sched_getaffinity(0))
 
 
-def oracle_steps_per_s(cfg, layers, budget_s=20.0, min_s=10.0, nchw=False):
+def oracle_steps_per_s(cfg, layers, budget_s=20.0, min_s=10.0, nchw=False, tied=False):
     """Time the float64 oracle as it stands on a bounded sample of the workload.
 
     Sample: one K-FAC step of as many KRON layers as fit the budget (factor
@@ -242,13 +259,17 @@ def oracle_steps_per_s(cfg, layers, budget_s=20.0, min_s=10.0, nchw=False):
     and the per-layer times are averaged over the passes.  Per-layer times are
     scaled to the whole layer set, with the refresh amortised by the cadence.
     nchw: convolutions build their factors from NCHW draws through the oracle's
-    input patches, as the GPU arm's NCHW workloads do."""
+    input patches, as the GPU arm's NCHW workloads do.  tied: key and value
+    projections use the query projection's A (no A of their own)."""
     import oracle as O
     hp = cfg.hp
     orc = O.KfacOracle(hp.ema_decay, hp.damping, hp.lr, hp.momentum, hp.weight_decay, 1)
     kron = [l for l in layers if l.kind == "kron"]
     diag = [l for l in layers if l.kind == "diag"]
-    cost = lambda l: l.rows * (l.n ** 2 + l.d_out ** 2) + l.n ** 3 + l.d_out ** 3
+    tied_names = ({layers[i].name for i in qkv_ties(layers)} if tied else set())
+    own_a = lambda l: l.name not in tied_names
+    cost = lambda l: (l.rows * (l.n ** 2 * own_a(l) + l.d_out ** 2) + l.n ** 3 * own_a(l)
+                      + l.d_out ** 3)
     t0 = time.perf_counter()
     inputs = {}
 
@@ -266,12 +287,15 @@ def oracle_steps_per_s(cfg, layers, budget_s=20.0, min_s=10.0, nchw=False):
             c = x["geom"]
             An, Gn = O.conv_factors(x["x"], x["gy"], (c.kh, c.kw), (c.sh, c.sw), (c.ph, c.pw),
                                     (c.dh, c.dw), l.has_bias)
-        else:
+        elif own_a(l):
             An, Gn = O.factor(x["a"], l.has_bias), O.factor(x["g"], 0)
-        st.A = O.ema(st.A, An, orc.xi)
+        else:
+            An, Gn = None, O.factor(x["g"], 0)
+        if An is not None:
+            st.A = O.ema(st.A, An, orc.xi)
         st.G = O.ema(st.G, Gn, orc.xi)
         tf = time.perf_counter()
-        st.Ainv = O.damped_inverse(st.A, orc.gamma)
+        st.Ainv = O.damped_inverse(st.A, orc.gamma) if own_a(l) else np.eye(l.n)
         st.Ginv = O.damped_inverse(st.G, orc.gamma)
         ti = time.perf_counter()
         P = O.precondition(st.Ginv, O.grad_hat(x["grad_w"], x["grad_b"]), st.Ainv)
@@ -335,6 +359,9 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     max_rows = max(l.rows for l in layers)
     h = K.Kfac(descs, ema_decay=hp.ema_decay, damping=hp.damping, lr=hp.lr, momentum=hp.momentum,
                weight_decay=hp.weight_decay, max_rows=max_rows, device=dev)
+    ties = qkv_ties(layers) if args.workload in TIED_WORKLOADS else {}
+    for li, src in ties.items():
+        h.tie_a_factor(li, src)
     # inputs: two seeded batches per layer, resident in HBM, used alternately
     base = {l.name.replace("_diag", ""): i for i, l in enumerate(cfg.layers)}
     srcidx = [base.get(l.name.replace("_diag", ""), i) for i, l in enumerate(layers)]
@@ -390,7 +417,8 @@ def run_gpu(args, rank, world, peaks, peak_kind):
 
     def phase_factor(x):
         for grp in kron_groups.values():
-            h.update_factors_batched(grp, [x[li]["a"] for li in grp], [x[li]["g"] for li in grp])
+            h.update_factors_batched(grp, [None if li in ties else x[li]["a"] for li in grp],
+                                     [x[li]["g"] for li in grp])
         for grp in conv_groups.values():
             h.update_factors_conv2d_batched(grp, [x[li]["x"] for li in grp],
                                             [x[li]["gy"] for li in grp], [geoms[li] for li in grp])
@@ -549,7 +577,7 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     ph = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
                    for i in range(seq_steps)])  # ms: factor, invert, precond, diag
 
-    acc = algorithmic(layers, k, nchw)
+    acc = algorithmic(layers, k, nchw, set(ties))
     phase_ms = ph.mean(axis=0)
     phase_ms[1] = inv_ms_refresh / k   # invert, amortised over the refresh period
     factor_tfs = acc["factor_flop"] / (phase_ms[0] * 1e-3) / 1e12
@@ -608,7 +636,8 @@ def run_gpu(args, rank, world, peaks, peak_kind):
         "ms_per_step": ms_step, "phases": phases, "roofline": roof, "clocks": clocks,
         "gpu_launches": int(launches), "wall_s": wall, "e2e": e2e,
         "config": {"workload": cfg.name + ("+diag_twins" if not cfg.diag_layers else "")
-                   + ("+nchw_conv_inputs" if nchw else ""),
+                   + ("+nchw_conv_inputs" if nchw else "")
+                   + ("+qkv_shared_A" if ties else ""),
                    "kron_layers": sum(l.kind == "kron" for l in layers),
                    "diag_layers": sum(l.kind == "diag" for l in layers),
                    "invert_every": k, "max_rows": max_rows,
@@ -812,7 +841,8 @@ def main():
         t0 = time.perf_counter()
         for _ in range(max(1, args.steps)):
             v, sample, _ = oracle_steps_per_s(cfg, layers, budget_s=max(2.0, 60.0 / max(1, args.steps)),
-                                              min_s=0.0, nchw=args.workload in NCHW_WORKLOADS)
+                                              min_s=0.0, nchw=args.workload in NCHW_WORKLOADS,
+                                              tied=args.workload in TIED_WORKLOADS)
             per_step.append(1.0 / v)
             if time.perf_counter() - t0 > 150:
                 break
@@ -823,7 +853,8 @@ def main():
                 "ms_per_step": round(1e3 / value, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": cfg.name + ("+diag_twins" if not cfg.diag_layers else "")
-                           + ("+nchw_conv_inputs" if args.workload in NCHW_WORKLOADS else ""),
+                           + ("+nchw_conv_inputs" if args.workload in NCHW_WORKLOADS else "")
+                           + ("+qkv_shared_A" if args.workload in TIED_WORKLOADS else ""),
                            "invert_every": cfg.invert_every},
                 "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": cores,
                                  "kind": "oracle", "sample": sample},
@@ -839,7 +870,8 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, sample, spent = oracle_steps_per_s(cfg, layers, budget_s=20.0,
-                                              nchw=args.workload in NCHW_WORKLOADS)
+                                              nchw=args.workload in NCHW_WORKLOADS,
+                                              tied=args.workload in TIED_WORKLOADS)
         cpu = {"value": round(v, 6), "unit": "steps/s", "cores": blas_threads(), "kind": "oracle",
                "sample": sample, "seconds": round(spent, 1)}
     if rank == 0:
