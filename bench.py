@@ -504,18 +504,30 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     # replays on a side stream alongside them.  Refresh steps run in order.
     side = torch.cuda.Stream(dev)
     ev_side = torch.cuda.Event()
+    dside = torch.cuda.Stream(dev)
+    ev_dside = torch.cuda.Event()
 
     def step_graph(t, b, ev, overlap):
         refresh = (t - 1) % k == 0
         ev[0].record(stream)
-        if overlap and not refresh:
-            side.wait_event(ev[0])
-            with torch.cuda.stream(side):
+        if overlap:
+            # the diagonal step touches only the DIAG layers: always alongside
+            dside.wait_event(ev[0])
+            with torch.cuda.stream(dside):
+                graphs[("diag", b)].replay()
+                ev_dside.record(dside)
+            if refresh:
                 graphs[("factor", b)].replay()
-                ev_side.record(side)
-            graphs[("precond", b)].replay()
-            graphs[("diag", b)].replay()
-            stream.wait_event(ev_side)
+                graphs[("invert", 0)].replay()
+                graphs[("precond", b)].replay()
+            else:
+                side.wait_event(ev[0])
+                with torch.cuda.stream(side):
+                    graphs[("factor", b)].replay()
+                    ev_side.record(side)
+                graphs[("precond", b)].replay()
+                stream.wait_event(ev_side)
+            stream.wait_event(ev_dside)
         else:
             graphs[("factor", b)].replay()
             ev[1].record(stream)
@@ -642,9 +654,10 @@ def run_gpu(args, rank, world, peaks, peak_kind):
                    "diag_layers": sum(l.kind == "diag" for l in layers),
                    "invert_every": k, "max_rows": max_rows,
                    "cuda_graphs": not args.no_graphs,
-                   "phase_overlap": "factor update alongside preconditioning + diagonal step on "
-                                    "steps without a refresh" if (not args.no_graphs and not args.no_overlap)
-                                    else "none",
+                   "phase_overlap": ("three streams: the diagonal step (DIAG layers) alongside "
+                                     "the KRON path every step; the factor update alongside "
+                                     "preconditioning on steps without a refresh")
+                                    if (not args.no_graphs and not args.no_overlap) else "none",
                    "l2": "flushed between steps (256 MiB write, outside the per-step events)"},
     }
 
@@ -695,6 +708,8 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
     ev_used = [torch.cuda.Event(), torch.cuda.Event()]
     ev_done, ev_out = torch.cuda.Event(), torch.cuda.Event()
     fside = torch.cuda.Stream(dev)
+    dside = torch.cuda.Stream(dev)
+    ev_djoin = torch.cuda.Event()
     ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
     steps = max(3, min(args.steps, 20))
     torch.cuda.synchronize()
@@ -714,6 +729,14 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
                 stage[nb_].copy_(host, non_blocking=True)
                 ev_in[nb_].record(copy)
         x = xs[b]
+        if overlap:                             # diagonal step alongside the KRON path
+            ev_fork.record(main)
+            dside.wait_event(ev_fork)
+            if i >= 1:
+                dside.wait_event(ev_out)        # previous step's parameters are read back
+            with torch.cuda.stream(dside):
+                phase_diag(x)
+                ev_djoin.record(dside)
         if overlap and (t - 1) % k != 0:       # factor update alongside the rest
             ev_fork.record(main)
             fside.wait_event(ev_fork)
@@ -727,9 +750,12 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
         if i >= 1:
             main.wait_event(ev_out)            # previous step's parameters are read back
         phase_precond(x)
-        phase_diag(x)
+        if not overlap:
+            phase_diag(x)
         if overlap and (t - 1) % k != 0:
             main.wait_event(ev_join)
+        if overlap:
+            main.wait_event(ev_djoin)
         ev_used[b].record(main)
         ev_done.record(main)
         with torch.cuda.stream(copy):

@@ -518,7 +518,7 @@ def test_batched_diag_calls_reject_duplicates_and_wrong_kinds():
 
 def test_factor_update_concurrent_with_preconditioning_and_diag_step():
     """The factor update, preconditioning and the diagonal path use disjoint scratch:
-    run on two streams at once they leave exactly the state of running them in order
+    run on three streams at once they leave exactly the state of running them in order
     (split-K products included: a wide, short layer forces them in both phases)."""
     descs = [(K.KFAC_KRON, 64, 700, 1, K.KFAC_F32), (K.KFAC_KRON, 300, 200, 1, K.KFAC_F32),
              (K.KFAC_DIAG, 96, 128, 1, K.KFAC_F32)]
@@ -542,18 +542,23 @@ def test_factor_update_concurrent_with_preconditioning_and_diag_step():
     h = hs[0]
     h.update_factors_batched([0, 1], a_l[:2], g_l[:2])
     h.precondition_batched([0, 1], gws[:2], gbs[:2], None, None, pw[0][:2], pb[0][:2])
+    k5 = [(torch.empty(96, device="cuda"), torch.empty(129, device="cuda")) for _ in range(2)]
+    h.diag_factors(2, a_l[2], g_l[2], k5[0][0], k5[0][1])
     h.diag_step(2, gn, an, gws[2], gbs[2], pw[0][2], pb[0][2])
     torch.cuda.synchronize()
-    # overlapped: factor update on its own stream, the rest on another
+    # overlapped: factor update, preconditioning and the diagonal path on three streams
     h = hs[1]
-    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1, s2, s3 = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     torch.cuda.synchronize()
     with torch.cuda.stream(s1):
         h.update_factors_batched([0, 1], a_l[:2], g_l[:2])
     with torch.cuda.stream(s2):
         h.precondition_batched([0, 1], gws[:2], gbs[:2], None, None, pw[1][:2], pb[1][:2])
+    with torch.cuda.stream(s3):
+        h.diag_factors(2, a_l[2], g_l[2], k5[1][0], k5[1][1])
         h.diag_step(2, gn, an, gws[2], gbs[2], pw[1][2], pb[1][2])
     torch.cuda.synchronize()
+    assert torch.equal(k5[0][0], k5[1][0]) and torch.equal(k5[0][1], k5[1][1])
     for li in range(2):
         for which in (K.KFAC_STATE_A, K.KFAC_STATE_G, K.KFAC_STATE_MOMENTUM):
             assert torch.equal(hs[0].state(li, which), hs[1].state(li, which)), (li, which)
