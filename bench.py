@@ -518,7 +518,9 @@ def run_gpu(args, rank, world, peaks, peak_kind):
                 ev_dside.record(dside)
             if refresh:
                 graphs[("factor", b)].replay()
+                ev[1].record(stream)
                 graphs[("invert", 0)].replay()
+                ev[2].record(stream)
                 graphs[("precond", b)].replay()
             else:
                 side.wait_event(ev[0])

@@ -142,6 +142,8 @@ __device__ __forceinline__ bool last_cta(int* ticket) {
 
 template <bool VEC>
 __global__ void __launch_bounds__(kDiagThreads) diag_step_kernel(DiagParams p) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = diag_units(p, VEC);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < total; u += stride)
@@ -165,6 +167,8 @@ struct DiagGroup {
 
 __global__ void __launch_bounds__(kDiagThreads)
 diag_step_grouped_kernel(const __grid_constant__ DiagGroup g) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = g.start[g.count];
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int q = -1;
@@ -256,6 +260,8 @@ __device__ __forceinline__ void diag_factor_body(const DiagFactorParams& p, int 
 
 template <typename T>
 __global__ void __launch_bounds__(kK5Threads) diag_factor_kernel(DiagFactorParams p) {
+  pdl_wait();
+  pdl_trigger();
   diag_factor_body<T>(p, blockIdx.x, blockIdx.y);
 }
 
@@ -271,6 +277,8 @@ struct DiagFactorGroup {
 template <typename T>
 __global__ void __launch_bounds__(kK5Threads)
 diag_factor_grouped_kernel(const __grid_constant__ DiagFactorGroup g) {
+  pdl_wait();
+  pdl_trigger();
   int q = 0;
   while (q + 1 < g.count && (int)blockIdx.x >= g.block_start[q + 1]) ++q;
   const DiagFactorParams J = g.job[q];
@@ -362,9 +370,9 @@ kfac_status launch_diag_factors(kfac_ctx* h, int layer, const void* a, int64_t l
   if ((size_t)p.splits * (L.d_in + L.o) > h->k5part_floats) return KFAC_ERR_WORKSPACE;
   dim3 grid(p.col_blocks, p.splits);
   if (L.in_dtype == KFAC_BF16)
-    diag_factor_kernel<__nv_bfloat16><<<grid, kK5Threads, 0, st>>>(p);
+    launch_pdl(diag_factor_kernel<__nv_bfloat16>, dim3(grid), dim3(kK5Threads), 0, st, p);
   else
-    diag_factor_kernel<float><<<grid, kK5Threads, 0, st>>>(p);
+    launch_pdl(diag_factor_kernel<float>, dim3(grid), dim3(kK5Threads), 0, st, p);
   count_launch();
   return check_launch();
 }
@@ -392,9 +400,9 @@ kfac_status launch_diag_factors_batched(kfac_ctx* h, int count, const int* layer
     if (grp.count == 0) return KFAC_OK;
     grp.block_start[grp.count] = blocks;
     if (bf16)
-      diag_factor_grouped_kernel<__nv_bfloat16><<<blocks, kK5Threads, 0, st>>>(grp);
+      launch_pdl(diag_factor_grouped_kernel<__nv_bfloat16>, dim3(blocks), dim3(kK5Threads), 0, st, grp);
     else
-      diag_factor_grouped_kernel<float><<<blocks, kK5Threads, 0, st>>>(grp);
+      launch_pdl(diag_factor_grouped_kernel<float>, dim3(blocks), dim3(kK5Threads), 0, st, grp);
     count_launch();
     grp.count = 0;
     blocks = 0;
@@ -434,9 +442,9 @@ kfac_status launch_diag_step(kfac_ctx* h, int layer, float decay, const float* g
   DiagParams p = k6_params(h, L, decay, g_new, a_new, gw, gb, pw, pb, ow, ob, &vec);
   const unsigned blocks = k6_blocks(k6_units(L, vec));
   if (vec)
-    diag_step_kernel<true><<<blocks, kDiagThreads, 0, st>>>(p);
+    launch_pdl(diag_step_kernel<true>, dim3(blocks), dim3(kDiagThreads), 0, st, p);
   else
-    diag_step_kernel<false><<<blocks, kDiagThreads, 0, st>>>(p);
+    launch_pdl(diag_step_kernel<false>, dim3(blocks), dim3(kDiagThreads), 0, st, p);
   count_launch();
   return check_launch();
 }
@@ -455,7 +463,7 @@ kfac_status launch_diag_step_batched(kfac_ctx* h, int count, const int* layers,
   auto flush = [&]() -> kfac_status {
     if (grp.count == 0) return KFAC_OK;
     grp.start[grp.count] = units;
-    diag_step_grouped_kernel<<<k6_blocks(units), kDiagThreads, 0, st>>>(grp);
+    launch_pdl(diag_step_grouped_kernel, dim3(k6_blocks(units)), dim3(kDiagThreads), 0, st, grp);
     count_launch();
     grp.count = 0;
     units = 0;

@@ -65,6 +65,8 @@ __device__ __forceinline__ void syrk_store(const SyrkJob& j, int64_t gr, int64_t
 template <typename T>
 __global__ void __launch_bounds__(SyrkTile::Tile::kThreads)
 syrk_simt_kernel(const SyrkJob* __restrict__ jobs, SyrkJob job0) {
+  pdl_wait();
+  pdl_trigger();
   using Tile = SyrkTile::Tile;
   constexpr int BM = SyrkTile::BM, BN = SyrkTile::BN, TM = SyrkTile::TM, TN = SyrkTile::TN;
   __shared__ float smem[Tile::kSmemFloats];
@@ -128,9 +130,9 @@ kfac_status launch_syrk_simt(const SyrkJob* job, int njobs, bool bf16, cudaStrea
   const int tiles = job->nt * (job->nt + 1) / 2;
   dim3 grid(tiles * job->splits, 1);
   if (bf16)
-    syrk_simt_kernel<__nv_bfloat16><<<grid, SyrkTile::Tile::kThreads, 0, st>>>(nullptr, *job);
+    launch_pdl(syrk_simt_kernel<__nv_bfloat16>, dim3(grid), dim3(SyrkTile::Tile::kThreads), 0, st, nullptr, *job);
   else
-    syrk_simt_kernel<float><<<grid, SyrkTile::Tile::kThreads, 0, st>>>(nullptr, *job);
+    launch_pdl(syrk_simt_kernel<float>, dim3(grid), dim3(SyrkTile::Tile::kThreads), 0, st, nullptr, *job);
   count_launch();
   return check_launch();
 }
@@ -139,7 +141,7 @@ kfac_status launch_syrk_simt_grouped(const SyrkJob* d_jobs, int njobs, int max_t
                                      cudaStream_t st) {
   if (njobs <= 0) return KFAC_OK;
   dim3 grid(max_tiles, njobs);
-  syrk_simt_kernel<float><<<grid, SyrkTile::Tile::kThreads, 0, st>>>(d_jobs, SyrkJob{});
+  launch_pdl(syrk_simt_kernel<float>, dim3(grid), dim3(SyrkTile::Tile::kThreads), 0, st, d_jobs, SyrkJob{});
   count_launch();
   return check_launch();
 }

@@ -40,6 +40,8 @@ constexpr int kOuterMaxN = 1536;  // handles whose factors are all this small st
 using PTile = SimtTile<64, 64, 32, 4, 4>;   // 256 threads, 32-deep k chunks
 
 __global__ void __launch_bounds__(256) inv_prep_kernel(const InvJob* jobs, float sqrt_gamma) {
+  pdl_wait();
+  pdl_trigger();
   const InvJob J = jobs[blockIdx.y];
   const int64_t nn = (int64_t)J.n * J.n;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
@@ -105,6 +107,8 @@ __device__ __forceinline__ void diag_inverse_level(const float* A, float* X, flo
 
 __global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int k,
                                                         DevStatus* st) {
+  pdl_wait();
+  pdl_trigger();
   const InvJob J = jobs[blockIdx.x];
   if (k >= J.n) return;
   const int b = min(NB, J.n - k);
@@ -223,6 +227,8 @@ __global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int 
 // L[i, k:k+b] <- L[i, k:k+b] . X_kk^T for rows i in [k+b, n); one CTA owns a
 // 64-row block and all b <= 64 columns, so the in-place update is race-free.
 __global__ void __launch_bounds__(256) chol_panel_kernel(const InvJob* jobs, int k) {
+  pdl_wait();
+  pdl_trigger();
   const InvJob J = jobs[blockIdx.y];
   const int n = J.n;
   if (k + NB >= n) return;  // no rows below the last diagonal block
@@ -263,6 +269,8 @@ __device__ __forceinline__ void lower_tile_coords(int t, int* ti, int* tj) {
 // block and panel.
 __global__ void __launch_bounds__(256) chol_trailing_kernel(const InvJob* jobs, int k, int part,
                                                             int cend) {
+  pdl_wait();
+  pdl_trigger();
   const InvJob J = jobs[blockIdx.y];
   const int n = J.n;
   const int64_t base = (int64_t)k + NB;
@@ -323,6 +331,8 @@ __device__ __forceinline__ bool level_tile(int n, int s, int t, int* T0, int* B0
 
 // Y[r][c] = sum_{t in T, t >= c} L[r][t] X[t][c]      (r in B, c in T)
 __global__ void __launch_bounds__(256) tri_level_y_kernel(const InvJob* jobs, int s) {
+  pdl_wait();
+  pdl_trigger();
   const InvJob J = jobs[blockIdx.y];
   const int n = J.n;
   int T0, B0, B1, tr, tc;
@@ -344,6 +354,8 @@ __global__ void __launch_bounds__(256) tri_level_y_kernel(const InvJob* jobs, in
 
 // X[r][c] = -sum_{t in B, t <= r} X[r][t] Y[t][c]      (r in B, c in T)
 __global__ void __launch_bounds__(256) tri_level_x_kernel(const InvJob* jobs, int s) {
+  pdl_wait();
+  pdl_trigger();
   const InvJob J = jobs[blockIdx.y];
   const int n = J.n;
   int T0, B0, B1, tr, tc;
@@ -380,6 +392,8 @@ struct PanelPackGroup {
 };
 
 __global__ void __launch_bounds__(256) panel_split_kernel(const __grid_constant__ PanelPackGroup g) {
+  pdl_wait();
+  pdl_trigger();
   const PanelPack P = g.job[blockIdx.y];
   const int64_t total = P.rows * g.W;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
@@ -394,6 +408,8 @@ __global__ void __launch_bounds__(256) panel_split_kernel(const __grid_constant_
 
 // Finv -> TF32 halves with a 16-byte row pitch, the operand form of the K4 products.
 __global__ void __launch_bounds__(256) inv_split_kernel(const InvJob* jobs) {
+  pdl_wait();
+  pdl_trigger();
   const InvJob J = jobs[blockIdx.y];
   const int64_t nn = (int64_t)J.n * J.n;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
@@ -437,7 +453,7 @@ kfac_status launch_outer_update(kfac_ctx* h, int j0, int nj, int K0, int W, cuda
   auto flush = [&]() -> kfac_status {
     if (pr.empty()) return KFAC_OK;
     const unsigned blocks = (unsigned)std::min<int64_t>(cdiv(max_elems, 256), 4 * kNumSMs);
-    panel_split_kernel<<<dim3(blocks, pg.count), 256, 0, st>>>(pg);
+    launch_pdl(panel_split_kernel, dim3(dim3(blocks, pg.count)), dim3(256), 0, st, pg);
     count_launch();
     kfac_status e = check_launch();
     if (e == KFAC_OK) e = launch_gemm_tc_grouped(h, false, TC_EPI_SYRK, pr.data(), (int)pr.size(), st);
@@ -505,8 +521,7 @@ kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
   const InvJob* jobs = d_all + j0;
   const float sg = (float)std::sqrt(h->hp.damping);
 
-  inv_prep_kernel<<<dim3((unsigned)std::min<int64_t>(cdiv((int64_t)nmax * nmax, 256), 1024), nj),
-                    256, 0, st>>>(jobs, sg);
+  launch_pdl(inv_prep_kernel, dim3(dim3((unsigned)std::min<int64_t>(cdiv((int64_t)nmax * nmax, 256), 1024), nj)), dim3(256), 0, st, jobs, sg);
   count_launch();
   if (kfac_status e = check_launch()) return e;
 
@@ -530,12 +545,12 @@ kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
   for (int K0 = 0; K0 < nmax; K0 += W) {
     const int cend = K0 + W;
     for (int k = K0; k < std::min(cend, nmax); k += NB) {
-      chol_diag_kernel<<<nj, 256, 0, st>>>(jobs, k, h->status());
+      launch_pdl(chol_diag_kernel, dim3(nj), dim3(256), 0, st, jobs, k, h->status());
       count_launch();
       const int rest = nmax - k - NB;
       if (rest > 0) {
         const int rb = (int)cdiv(rest, 64);
-        chol_panel_kernel<<<dim3(rb, nj), 256, 0, st>>>(jobs, k);
+        launch_pdl(chol_panel_kernel, dim3(dim3(rb, nj)), dim3(256), 0, st, jobs, k);
         count_launch();
         const int nc = (int)std::min<int64_t>(rb, cdiv(std::min(cend, nmax) - (k + NB), 64));
         if (nc > 1) {
@@ -544,14 +559,13 @@ kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
         }
         if (nc >= 1) {
           if (kfac_status e = join_side()) return e;
-          chol_trailing_kernel<<<dim3(rb, nj), 256, 0, st>>>(jobs, k, 1, cend);
+          launch_pdl(chol_trailing_kernel, dim3(dim3(rb, nj)), dim3(256), 0, st, jobs, k, 1, cend);
           count_launch();
         }
         if (nc > 1) {
           int64_t tiles = 0;
           for (int j = 1; j < nc; ++j) tiles += rb - j;
-          chol_trailing_kernel<<<dim3((unsigned)tiles, nj), 256, 0, h->side_stream>>>(jobs, k, 2,
-                                                                                      cend);
+          launch_pdl(chol_trailing_kernel, dim3(dim3((unsigned)tiles, nj)), dim3(256), 0, h->side_stream, jobs, k, 2, cend);
           count_launch();
           if (kfac_status e = sync_err(cudaEventRecord(h->ev_rest, h->side_stream))) return e;
           rest_pending = true;
@@ -569,8 +583,8 @@ kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
     const int tiles = level_tiles_host(nmax, s);
     int tmax = tiles;
     for (int i = j0; i < j0 + nj; ++i) tmax = std::max(tmax, level_tiles_host(h->invjobs_host[i].n, s));
-    tri_level_y_kernel<<<dim3(tmax, nj), 256, 0, st>>>(jobs, s);
-    tri_level_x_kernel<<<dim3(tmax, nj), 256, 0, st>>>(jobs, s);
+    launch_pdl(tri_level_y_kernel, dim3(dim3(tmax, nj)), dim3(256), 0, st, jobs, s);
+    launch_pdl(tri_level_x_kernel, dim3(dim3(tmax, nj)), dim3(256), 0, st, jobs, s);
     count_launch(2);
     if (kfac_status e = check_launch()) return e;
   }
@@ -591,8 +605,7 @@ kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
   }
   if (!big.empty())
     if (kfac_status e = launch_syrk_tc_batched(h, big.data(), (int)big.size(), st)) return e;
-  inv_split_kernel<<<dim3((unsigned)std::min<int64_t>(cdiv((int64_t)nmax * nmax, 256), 1024), nj),
-                     256, 0, st>>>(jobs);
+  launch_pdl(inv_split_kernel, dim3(dim3((unsigned)std::min<int64_t>(cdiv((int64_t)nmax * nmax, 256), 1024), nj)), dim3(256), 0, st, jobs);
   count_launch();
   return check_launch();
 }

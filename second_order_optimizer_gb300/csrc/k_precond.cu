@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(256) gradhat_pack_kernel(const float* __restri
                                                            const float* __restrict__ gb, int o,
                                                            int d_in, int n, int64_t np,
                                                            float* hi, float* lo) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = (int64_t)o * n;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
@@ -58,6 +60,8 @@ struct GradPackGroup {
 
 __global__ void __launch_bounds__(256) gradhat_pack_grouped_kernel(
     const __grid_constant__ GradPackGroup g) {
+  pdl_wait();
+  pdl_trigger();
   const GradPackJob J = g.job[blockIdx.y];  // by value: no reloads after each store
   const int64_t total = (int64_t)J.o * J.n;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
@@ -85,7 +89,7 @@ kfac_status launch_precondition(kfac_ctx* h, int layer, const float* gw, int64_t
   {
     const int64_t total = (int64_t)L.o * L.n;
     const unsigned blocks = (unsigned)std::min<int64_t>(cdiv(total, 256), 4 * kNumSMs);
-    gradhat_pack_kernel<<<blocks, 256, 0, st>>>(gw, ldgw, gb, L.o, L.d_in, L.n, np, g_hi, g_lo);
+    launch_pdl(gradhat_pack_kernel, dim3(blocks), dim3(256), 0, st, gw, ldgw, gb, L.o, L.d_in, L.n, np, g_hi, g_lo);
     count_launch();
     if (kfac_status e = check_launch()) return e;
   }
@@ -134,7 +138,7 @@ kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layer
   auto flush = [&]() -> kfac_status {
     if (ng == 0) return KFAC_OK;
     const unsigned blocks = (unsigned)std::min<int64_t>(cdiv(max_elems, 256), 4 * kNumSMs);
-    gradhat_pack_grouped_kernel<<<dim3(blocks, ng), 256, 0, st>>>(gp);
+    launch_pdl(gradhat_pack_grouped_kernel, dim3(dim3(blocks, ng)), dim3(256), 0, st, gp);
     count_launch();
     kfac_status e = check_launch();
     if (e == KFAC_OK) e = launch_gemm_tc_grouped(h, false, TC_EPI_SPLIT, p1.data(), ng, st);

@@ -22,6 +22,32 @@ inline int conv_out(int in, int k, int stride, int pad, int dil) {
   return span < 0 ? 0 : (int)(span / stride + 1);
 }
 
+// Programmatic dependent launch.  Every library kernel is launched with the
+// programmatic-serialisation attribute and starts with pdl_wait() (the grids
+// before it in the stream have completed and their writes are visible; a no-op
+// for an ordinary launch) and pdl_trigger() (the next grid may be scheduled
+// now: its blocks do their own setup, then wait).  Each kernel waits before any
+// early return, so "completed" stays transitive along the stream.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Device status word: first error wins.
 struct DevStatus {
   int code;    // kfac_status
