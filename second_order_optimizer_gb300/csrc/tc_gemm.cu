@@ -699,10 +699,6 @@ struct GroupedTc {
   int block_start[kMaxGroup + 1];
   int count;
   int csize;
-  // persistent (stream-K) launch: units per tile of each problem and the
-  // units' prefix over problems (unit_start[count] = all units)
-  int nsub[kMaxGroup];
-  int64_t unit_start[kMaxGroup + 1];
 };
 
 template <bool kBF16, int EPI>
@@ -716,22 +712,14 @@ gemm_tc_grouped_kernel(const __grid_constant__ GroupedTc g) {
 }
 
 // ------------------------------------------------------- persistent grouped
-// The grouped products without split-K, one CTA per SM.  Stream-K: the launch's
-// work is U units, a unit being one TMEM drain period (ksub k-elements) of one
-// tile; tiles are in launch order and a tile's units consecutive.  CTA c takes
-// units [U c / G, U (c + 1) / G), so every CTA carries the same share of the
-// main loops whatever the tile count (225 tiles on 152 SMs would otherwise give
-// half the CTAs two tiles and half one).  A tile whose units fall to two or more
-// CTAs is a split tile: each CTA writes its partial sum (slot 2c + 1 for the CTA
-// where the tile starts, 2c for the others), takes the tile's ticket, and the
-// last to arrive adds the partials in CTA order and runs the epilogue: no CTA
-// waits for another, and the result does not depend on arrival order.
-// The TMA and MMA warps run on into the next unit while the drain warps finish
-// the previous tile: the TMEM accumulator is a ring of 4 buffers (512
-// columns).  The stage buffers stay busy meanwhile, so the epilogues read
-// their global inputs straight into registers (lanes on rows, coalesced;
-// prefetched into L2 when a tile's units start) and the SYRK direct half is
-// transposed through a per-warp 32 x 33 buffer.
+// The grouped products without split-K, one CTA per SM looping over tiles
+// (tile t, t + gridDim.x, ...).  The TMA and MMA warps run on into the next
+// tile while the drain warps finish the previous tile's epilogue: the TMEM
+// accumulator is a ring of 4 buffers (512 columns), so the MMA can run up to
+// four drain periods ahead.  The stage buffers stay busy meanwhile, so these
+// epilogues read their global inputs straight into registers (lanes on rows,
+// coalesced; prefetched into L2 when the tile starts) and the SYRK direct half
+// is transposed through a per-warp 32 x 33 buffer.
 template <bool kBF16>
 struct PersistCfg {
   using C = TcCfg<kBF16, 128>;
@@ -757,30 +745,6 @@ __device__ __forceinline__ void grouped_tile(const GroupedTc& g, int t, int* q, 
   *q = k;
 }
 
-// Position of a stream-K unit: problem q, launch tile t, unit `sub` of the tile.
-struct UnitPos {
-  int q, t, sub;
-};
-__device__ __forceinline__ UnitPos unit_pos(const GroupedTc& g, int64_t u) {
-  UnitPos p;
-  p.q = 0;
-  while (p.q + 1 < g.count && u >= g.unit_start[p.q + 1]) ++p.q;
-  const int64_t local = u - g.unit_start[p.q];
-  p.t = g.block_start[p.q] + (int)(local / g.nsub[p.q]);
-  p.sub = (int)(local % g.nsub[p.q]);
-  return p;
-}
-__device__ __forceinline__ void unit_next(const GroupedTc& g, UnitPos* p) {
-  if (++p->sub < g.nsub[p->q]) return;
-  p->sub = 0;
-  if (++p->t >= g.block_start[p->q + 1]) ++p->q;
-}
-// First unit of CTA c of G over U units, and the CTA that owns unit u.
-__device__ __forceinline__ int64_t sk_first(int64_t U, int G, int c) { return U * c / G; }
-__device__ __forceinline__ int sk_owner(int64_t U, int G, int64_t u) {
-  return (int)(((u + 1) * G - 1) / U);
-}
-
 template <bool kBF16, int EPI>
 __global__ void __launch_bounds__(TcCfg<kBF16, 128>::THREADS, 1)
 gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
@@ -794,14 +758,10 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
   uint64_t* empty = full + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + PC::ACC;
-  uint64_t* seg_bar = acc_empty + PC::ACC;    // the drain warps' barrier around a ticket
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(seg_bar + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + PC::ACC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* s_last = reinterpret_cast<volatile int*>(tmem_slot + 2);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int64_t U = g.unit_start[g.count];
-  const int G = gridDim.x, cta = blockIdx.x;
-  const int64_t u_begin = sk_first(U, G, cta), u_end = sk_first(U, G, cta + 1);
+  const int total = g.block_start[g.count];
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -812,7 +772,6 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
       tc::mbar_init(&acc_full[b], 1);
       tc::mbar_init(&acc_empty[b], 32 * C::EPI_WARPS);
     }
-    tc::mbar_init(seg_bar, 32 * C::EPI_WARPS);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -836,15 +795,14 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      UnitPos up = unit_pos(g, u_begin);
-      for (int64_t u = u_begin; u < u_end && ok; ++u, unit_next(g, &up)) {
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         int q, ti, tj;
-        grouped_tile(g, up.t, &q, &ti, &tj);
+        grouped_tile(g, t, &q, &ti, &tj);
         const CUtensorMap* m = &g.maps[4 * q];
         const bool a_in_b = g.prob[q].same_ab && ti == tj;
         const uint32_t bytes = (a_in_b ? C::B_BYTES : C::HALF_BYTES) * (kBF16 ? 1 : 2);
-        const int kb0 = up.sub * kb_per_sub, kb1 = min(nkb_of(q), kb0 + kb_per_sub);
-        for (int kb = kb0; kb < kb1; ++kb) {
+        const int nkb = nkb_of(q);
+        for (int kb = 0; kb < nkb; ++kb) {
           if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
             *abort_flag = 1;
             report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 11);
@@ -873,57 +831,60 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
       uint32_t phase = 0;
       int gsub = 0;
       bool ok = true;
-      UnitPos up = unit_pos(g, u_begin);
-      for (int64_t u = u_begin; u < u_end && ok; ++u, unit_next(g, &up), ++gsub) {
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         int q, ti, tj;
-        grouped_tile(g, up.t, &q, &ti, &tj);
+        grouped_tile(g, t, &q, &ti, &tj);
         const bool a_in_b = g.prob[q].same_ab && ti == tj;
-        const int buf = gsub % PC::ACC, use = gsub / PC::ACC;
-        if (!tc::mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag)) {
-          report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 12);
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
-        tc::tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(buf * C::BN);
-        const int kb0 = up.sub * kb_per_sub, kb1 = min(nkb_of(q), kb0 + kb_per_sub);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!tc::mbar_wait(&full[stage], phase, abort_flag)) {
-            report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 13);
+        const int nkb = nkb_of(q);
+        const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
+        for (int sub = 0; sub < nsub && ok; ++sub, ++gsub) {
+          const int buf = gsub % PC::ACC, use = gsub / PC::ACC;
+          if (!tc::mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag)) {
+            report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 12);
             *abort_flag = 1;
             ok = false;
             break;
           }
           tc::tc_fence_after();
-          const uint32_t a_hi = tc::smem_u32(a_in_b ? b_ptr(stage, 0) : a_ptr(stage, 0));
-          const uint32_t b_hi = tc::smem_u32(b_ptr(stage, 0));
-          const uint32_t a_lo = tc::smem_u32(a_in_b ? b_ptr(stage, kBF16 ? 0 : 1)
-                                                    : a_ptr(stage, kBF16 ? 0 : 1));
-          const uint32_t b_lo = tc::smem_u32(b_ptr(stage, kBF16 ? 0 : 1));
+          const uint32_t d = tmem + (uint32_t)(buf * C::BN);
+          const int kb0 = sub * kb_per_sub, kb1 = min(nkb, kb0 + kb_per_sub);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!tc::mbar_wait(&full[stage], phase, abort_flag)) {
+              report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 13);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            tc::tc_fence_after();
+            const uint32_t a_hi = tc::smem_u32(a_in_b ? b_ptr(stage, 0) : a_ptr(stage, 0));
+            const uint32_t b_hi = tc::smem_u32(b_ptr(stage, 0));
+            const uint32_t a_lo = tc::smem_u32(a_in_b ? b_ptr(stage, kBF16 ? 0 : 1)
+                                                      : a_ptr(stage, kBF16 ? 0 : 1));
+            const uint32_t b_lo = tc::smem_u32(b_ptr(stage, kBF16 ? 0 : 1));
 #pragma unroll
-          for (int kk = 0; kk < C::BK / C::KMMA; ++kk) {
-            const uint32_t off = kk * 32;
-            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-            if (kBF16) {
-              tc::umma_f16(d, tc::sdesc_kmajor_sw128(a_hi + off),
-                           tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
-            } else {
-              tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_hi + off),
-                            tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
-              tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_hi + off),
-                            tc::sdesc_kmajor_sw128(b_lo + off), idesc, 1u);
-              tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_lo + off),
-                            tc::sdesc_kmajor_sw128(b_hi + off), idesc, 1u);
+            for (int kk = 0; kk < C::BK / C::KMMA; ++kk) {
+              const uint32_t off = kk * 32;
+              const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+              if (kBF16) {
+                tc::umma_f16(d, tc::sdesc_kmajor_sw128(a_hi + off),
+                             tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
+              } else {
+                tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_hi + off),
+                              tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
+                tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_hi + off),
+                              tc::sdesc_kmajor_sw128(b_lo + off), idesc, 1u);
+                tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_lo + off),
+                              tc::sdesc_kmajor_sw128(b_hi + off), idesc, 1u);
+              }
+            }
+            tc::umma_commit(&empty[stage]);
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1;
             }
           }
-          tc::umma_commit(&empty[stage]);
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+          if (ok) tc::umma_commit(&acc_full[buf]);
         }
-        if (ok) tc::umma_commit(&acc_full[buf]);
       }
     }
   } else {  // ------------------------------------------------ drain + epilogue
@@ -931,123 +892,73 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
     const int h = (warp - 2) >> 2;           // column half: [CW h, CW h + CW)
     const int row = 32 * qd + lane;
     float* xb = xbuf + (warp - 2) * 32 * PC::XP;
-    float* part = g.prob[0].part;            // stream-K partials: 2 slots of BM x BN per CTA
-    int* tickets = g.prob[0].tickets;        // one per split tile, by the CTA it starts in
-    uint32_t seg_phase = 0;
     int gsub = 0;
     bool ok = true;
-    float sum[CW];
-    int seg_sub0 = 0;                        // unit of the tile this CTA's segment starts at
-    UnitPos up = unit_pos(g, u_begin);
-    // the drain warps' barrier (bounded, like every wait here)
-    auto seg_sync = [&]() -> bool {
-      tc::mbar_arrive(seg_bar);
-      const bool r = tc::mbar_wait(seg_bar, seg_phase, abort_flag);
-      seg_phase ^= 1;
-      return r;
-    };
-    for (int64_t u = u_begin; u < u_end && ok; ++u, unit_next(g, &up), ++gsub) {
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       int q, ti, tj;
-      grouped_tile(g, up.t, &q, &ti, &tj);
+      grouped_tile(g, t, &q, &ti, &tj);
       const TcEpilogue E = g.prob[q].e;   // by value (see gemm_body)
       const int64_t pM = g.prob[q].M, pN = g.prob[q].N;
       const int64_t r0 = (int64_t)ti * C::BM, c0 = (int64_t)tj * C::BN + h * CW;
       const int64_t gr = r0 + row;
-      const int nsub = g.nsub[q];
-      if (u == u_begin || up.sub == 0) {   // a segment starts: zero the sum, prefetch
-        seg_sub0 = up.sub;
-#pragma unroll
-        for (int c = 0; c < CW; ++c) sum[c] = 0.f;
-        if (gr < pM) {   // the tile's epilogue inputs into L2 while the drains run
-          if (EPI == TC_EPI_SYRK && E.beta != 0.f) {
-            for (int c = 0; c < CW; ++c) {
-              const int64_t gc = c0 + c;
-              if (gc < pN && gr <= gc) tc::prefetch_l2(E.C + gc * E.ldc + gr);
-            }
-          } else if (EPI == TC_EPI_PRECOND && E.pw && gr < E.d_in) {
-            for (int c = 0; c < CW; ++c) {
-              const int64_t i = c0 + c;
-              if (i >= pN) break;
-              tc::prefetch_l2(E.pw + i * E.d_in + gr);
-              tc::prefetch_l2(E.mw + i * E.d_in + gr);
-            }
+      const int nkb = nkb_of(q);
+      const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
+      if (gr < pM) {   // the tile's epilogue inputs into L2 while the drains run
+        if (EPI == TC_EPI_SYRK && E.beta != 0.f) {
+          for (int c = 0; c < CW; ++c) {
+            const int64_t gc = c0 + c;
+            if (gc < pN && gr <= gc) tc::prefetch_l2(E.C + gc * E.ldc + gr);
+          }
+        } else if (EPI == TC_EPI_PRECOND && E.pw && gr < E.d_in) {
+          for (int c = 0; c < CW; ++c) {
+            const int64_t i = c0 + c;
+            if (i >= pN) break;
+            tc::prefetch_l2(E.pw + i * E.d_in + gr);
+            tc::prefetch_l2(E.mw + i * E.d_in + gr);
           }
         }
       }
-      const int buf = gsub % PC::ACC, use = gsub / PC::ACC;
-      if (!tc::mbar_wait(&acc_full[buf], use & 1, abort_flag)) {
-        report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 14);
-        *abort_flag = 1;
-        ok = false;
-        break;
-      }
-      tc::tc_fence_after();
+      float sum[CW];
 #pragma unroll
-      for (int cc = 0; cc < CW / 32; ++cc) {
-        float v[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) +
-                          (uint32_t)(buf * C::BN + h * CW + cc * 32), v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sum[cc * 32 + i] += v[i];
-      }
-      tc::tc_fence_before();
-      tc::mbar_arrive(&acc_empty[buf]);
-      const bool tile_end = up.sub == nsub - 1;
-      if (!tile_end && u != u_end - 1) continue;      // the segment goes on
-      if (!(seg_sub0 == 0 && tile_end)) {
-        // split tile: store this CTA's partial, take the ticket; the last CTA to
-        // arrive sums every partial in CTA order and runs the epilogue
-        const int64_t ut0 = g.unit_start[q] + (int64_t)(up.t - g.block_start[q]) * nsub;
-        const int cf = sk_owner(U, G, ut0), cl = sk_owner(U, G, ut0 + nsub - 1);
-        float* mine = part + (size_t)(cta == cf ? 2 * cta + 1 : 2 * cta) * (C::BM * C::BN);
-#pragma unroll
-        for (int c = 0; c < CW; ++c) mine[(size_t)(h * CW + c) * C::BM + row] = sum[c];
-        __threadfence();
-        if (!seg_sync()) {
-          report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 15);
+      for (int c = 0; c < CW; ++c) sum[c] = 0.f;
+      for (int sub = 0; sub < nsub; ++sub, ++gsub) {
+        const int buf = gsub % PC::ACC, use = gsub / PC::ACC;
+        if (!tc::mbar_wait(&acc_full[buf], use & 1, abort_flag)) {
+          report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 14);
           *abort_flag = 1;
           ok = false;
           break;
         }
-        if (threadIdx.x == 64) {
-          const int prev = atomicAdd(&tickets[cf], 1);
-          const int last = prev == cl - cf;
-          if (last) tickets[cf] = 0;   // ready for the next launch
-          *s_last = last;
-        }
-        if (!seg_sync()) {
-          report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 16);
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
-        if (!*s_last) continue;
-        __threadfence();
+        tc::tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < CW; ++c) sum[c] = 0.f;
-        for (int cc = cf; cc <= cl; ++cc) {
-          const float* src = part + (size_t)(cc == cf ? 2 * cc + 1 : 2 * cc) * (C::BM * C::BN);
+        for (int cc = 0; cc < CW / 32; ++cc) {
+          float v[32];
+          tc::tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) +
+                            (uint32_t)(buf * C::BN + h * CW + cc * 32), v);
 #pragma unroll
-          for (int c = 0; c < CW; ++c) sum[c] += __ldcg(src + (size_t)(h * CW + c) * C::BM + row);
+          for (int i = 0; i < 32; ++i) sum[cc * 32 + i] += v[i];
         }
+        tc::tc_fence_before();
+        tc::mbar_arrive(&acc_empty[buf]);
       }
+      if (!ok) break;
       if (EPI == TC_EPI_SYRK) {
         // mirror F[gc][gr] from registers, old value from the same place
 #pragma unroll
         for (int cc = 0; cc < CW; cc += 16) {
           float old[16];
 #pragma unroll
-          for (int v = 0; v < 16; ++v) {
-            const int64_t gc = c0 + cc + v;
+          for (int u = 0; u < 16; ++u) {
+            const int64_t gc = c0 + cc + u;
             const bool okc = gr < pM && gc < pN && gr <= gc;
-            old[v] = (okc && E.beta != 0.f) ? __ldcg(E.C + gc * E.ldc + gr) : 0.f;
+            old[u] = (okc && E.beta != 0.f) ? __ldcg(E.C + gc * E.ldc + gr) : 0.f;
           }
 #pragma unroll
-          for (int v = 0; v < 16; ++v) {
-            const int64_t gc = c0 + cc + v;
-            const float val = fmaf(E.beta, old[v], E.alpha * sum[cc + v]);
-            sum[cc + v] = val;
-            if (gr < pM && gc < pN && gr <= gc) E.C[gc * E.ldc + gr] = val;
+          for (int u = 0; u < 16; ++u) {
+            const int64_t gc = c0 + cc + u;
+            const float v = fmaf(E.beta, old[u], E.alpha * sum[cc + u]);
+            sum[cc + u] = v;
+            if (gr < pM && gc < pN && gr <= gc) E.C[gc * E.ldc + gr] = v;
           }
         }
         // direct half F[gr][gc] (gr < gc): 32 x 32 blocks transposed through the
@@ -1083,21 +994,21 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
           for (int cc = 0; cc < CW; cc += 16) {
             float w[16], m[16];
 #pragma unroll
-            for (int v = 0; v < 16; ++v) {
-              const int64_t i = c0 + cc + v;
-              w[v] = m[v] = 0.f;
+            for (int u = 0; u < 16; ++u) {
+              const int64_t i = c0 + cc + u;
+              w[u] = m[u] = 0.f;
               if (E.pw && i < pN) {
-                w[v] = wcol ? __ldcg(E.pw + i * E.d_in + gr) : __ldcg(E.pb + i);
-                m[v] = wcol ? __ldcg(E.mw + i * E.d_in + gr) : __ldcg(E.mb + i);
+                w[u] = wcol ? __ldcg(E.pw + i * E.d_in + gr) : __ldcg(E.pb + i);
+                m[u] = wcol ? __ldcg(E.mw + i * E.d_in + gr) : __ldcg(E.mb + i);
               }
             }
 #pragma unroll
-            for (int v = 0; v < 16; ++v) {
-              const int64_t i = c0 + cc + v;
+            for (int u = 0; u < 16; ++u) {
+              const int64_t i = c0 + cc + u;
               if (i >= pN) continue;
-              const float pr = sum[cc + v];
-              const float mn = fmaf(E.mu, m[v], fmaf(E.lambda, w[v], pr));
-              const float wn = fmaf(-E.eta, mn, w[v]);
+              const float pr = sum[cc + u];
+              const float mn = fmaf(E.mu, m[u], fmaf(E.lambda, w[u], pr));
+              const float wn = fmaf(-E.eta, mn, w[u]);
               if (wcol) {
                 const int64_t x = i * E.d_in + gr;
                 if (E.ow) E.ow[x] = pr;
@@ -1510,18 +1421,10 @@ kfac_status launch_persistent_kernel(const GroupedTc& g, cudaStream_t st) {
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)PersistCfg<kBF16>::SMEM) == cudaSuccess;
   if (!attr_ok) return KFAC_ERR_CUDA;
-  // stream-K units: one TMEM drain period of one tile each
-  GroupedTc gs = g;
-  gs.unit_start[0] = 0;
-  for (int q = 0; q < g.count; ++q) {
-    const int tiles = g.block_start[q + 1] - g.block_start[q];
-    gs.nsub[q] = (int)cdiv(g.prob[q].K, g.prob[q].ksub);
-    gs.unit_start[q + 1] = gs.unit_start[q] + (int64_t)tiles * gs.nsub[q];
-  }
-  const unsigned grid = (unsigned)std::min<int64_t>(gs.unit_start[g.count], kNumSMs);
-  if (grid == 0) return KFAC_OK;
+  const int total = g.block_start[g.count];
+  const unsigned grid = (unsigned)std::min<int>(total, kNumSMs);
   launch_pdl(gemm_tc_persistent_kernel<kBF16, EPI>, dim3(grid), dim3(TcCfg<kBF16, 128>::THREADS),
-             PersistCfg<kBF16>::SMEM, st, gs);
+             PersistCfg<kBF16>::SMEM, st, g);
   count_launch();
   return check_launch();
 }
