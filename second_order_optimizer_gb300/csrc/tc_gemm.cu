@@ -699,7 +699,6 @@ struct GroupedTc {
   int block_start[kMaxGroup + 1];
   int count;
   int csize;
-  int mc;   // persistent launch in cluster pairs sharing the B tile (tiles padded per column)
 };
 
 template <bool kBF16, int EPI>
@@ -732,17 +731,12 @@ struct PersistCfg {
   static_assert(SMEM <= 232448, "fits the per-CTA shared memory");
 };
 
-__device__ __forceinline__ void grouped_tile(const GroupedTc& g, int t, int* q, int* ti, int* tj,
-                                             bool* pad = nullptr) {
+__device__ __forceinline__ void grouped_tile(const GroupedTc& g, int t, int* q, int* ti, int* tj) {
   int k = 0;
   while (k + 1 < g.count && t >= g.block_start[k + 1]) ++k;
   const int local = t - g.block_start[k];
   const GemmTcParams& p = g.prob[k];
-  if (g.mc) {
-    bool pd;
-    mc_tile(local, p.tiles_m, p.tiles_n, 1, p.upper != 0, ti, tj, &pd);
-    if (pad) *pad = pd;
-  } else if (p.upper) {
+  if (p.upper) {
     upper_tile(local, p.tiles_m, 1, ti, tj);
   } else {
     *ti = local / p.tiles_n;
@@ -772,7 +766,7 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       tc::mbar_init(&full[s], 1);
-      tc::mbar_init(&empty[s], g.mc ? 2 : 1);   // multicast: both CTAs release a stage
+      tc::mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < PC::ACC; ++b) {
       tc::mbar_init(&acc_full[b], 1);
@@ -787,15 +781,10 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
   }
   tc::tc_fence_before();
   __syncthreads();
-  // multicast: the peer's barriers must be initialised before either CTA loads
-  if (g.mc) cooperative_groups::this_cluster().sync();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
   pdl_trigger();
-  // multicast pairs: blocks 2c and 2c + 1 form a cluster and take tiles t and
-  // t + 1 of one column; each loads half of the shared B tile's rows into both
-  const int mc_rank = g.mc ? (int)(blockIdx.x & 1) : 0;
   auto a_ptr = [&](int s, int lo) { return smem + (size_t)s * C::STAGE_BYTES + lo * C::HALF_BYTES; };
   auto b_ptr = [&](int s, int lo) { return a_ptr(s, lo) + C::A_BYTES; };
   auto nkb_of = [&](int q) { return (int)((g.prob[q].K + C::BK - 1) / C::BK); };
@@ -812,7 +801,6 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
         const CUtensorMap* m = &g.maps[4 * q];
         const bool a_in_b = g.prob[q].same_ab && ti == tj;
         const uint32_t bytes = (a_in_b ? C::B_BYTES : C::HALF_BYTES) * (kBF16 ? 1 : 2);
-        const int b_off = mc_rank * (C::B_BYTES / 2), b_row = tj * C::BN + mc_rank * (C::BN / 2);
         const int nkb = nkb_of(q);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
@@ -824,16 +812,10 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
           const int k0 = kb * C::BK;
           tc::mbar_expect_tx(&full[stage], bytes);
           if (!a_in_b) tc::tma_load_2d(a_ptr(stage, 0), &m[0], &full[stage], k0, ti * C::BM);
-          if (g.mc)
-            tc::tma_load_2d_mc(b_ptr(stage, 0) + b_off, &m[2], &full[stage], k0, b_row, 3);
-          else
-            tc::tma_load_2d(b_ptr(stage, 0), &m[2], &full[stage], k0, tj * C::BN);
+          tc::tma_load_2d(b_ptr(stage, 0), &m[2], &full[stage], k0, tj * C::BN);
           if (!kBF16) {
             if (!a_in_b) tc::tma_load_2d(a_ptr(stage, 1), &m[1], &full[stage], k0, ti * C::BM);
-            if (g.mc)
-              tc::tma_load_2d_mc(b_ptr(stage, 1) + b_off, &m[3], &full[stage], k0, b_row, 3);
-            else
-              tc::tma_load_2d(b_ptr(stage, 1), &m[3], &full[stage], k0, tj * C::BN);
+            tc::tma_load_2d(b_ptr(stage, 1), &m[3], &full[stage], k0, tj * C::BN);
           }
           if (++stage == C::STAGES) {
             stage = 0;
@@ -895,10 +877,7 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
                               tc::sdesc_kmajor_sw128(b_hi + off), idesc, 1u);
               }
             }
-            if (g.mc)
-              tc::umma_commit_mc(&empty[stage], 3);
-            else
-              tc::umma_commit(&empty[stage]);
+            tc::umma_commit(&empty[stage]);
             if (++stage == C::STAGES) {
               stage = 0;
               phase ^= 1;
@@ -917,10 +896,9 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       int q, ti, tj;
-      bool pad = false;   // multicast padding slot: computes its partner's tile, writes nothing
-      grouped_tile(g, t, &q, &ti, &tj, &pad);
+      grouped_tile(g, t, &q, &ti, &tj);
       const TcEpilogue E = g.prob[q].e;   // by value (see gemm_body)
-      const int64_t pM = pad ? 0 : g.prob[q].M, pN = g.prob[q].N;
+      const int64_t pM = g.prob[q].M, pN = g.prob[q].N;
       const int64_t r0 = (int64_t)ti * C::BM, c0 = (int64_t)tj * C::BN + h * CW;
       const int64_t gr = r0 + row;
       const int nkb = nkb_of(q);
@@ -1053,9 +1031,6 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
   }
   tc::tc_fence_before();
   __syncthreads();
-  // multicast: the peer may still be loading into this CTA's stages and
-  // signalling its barriers until it is done
-  if (g.mc) cooperative_groups::this_cluster().sync();
   if (warp == 1) tc::tmem_dealloc(tmem, PC::TMEM_COLS);
 }
 
@@ -1447,29 +1422,9 @@ kfac_status launch_persistent_kernel(const GroupedTc& g, cudaStream_t st) {
                                              (int)PersistCfg<kBF16>::SMEM) == cudaSuccess;
   if (!attr_ok) return KFAC_ERR_CUDA;
   const int total = g.block_start[g.count];
-  // with g.mc the grid is even: total is (columns padded), and so is kNumSMs
   const unsigned grid = (unsigned)std::min<int>(total, kNumSMs);
-  if (g.mc) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(TcCfg<kBF16, 128>::THREADS);
-    cfg.dynamicSmemBytes = PersistCfg<kBF16>::SMEM;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, gemm_tc_persistent_kernel<kBF16, EPI>, g) != cudaSuccess)
-      return KFAC_ERR_CUDA;
-  } else {
-    launch_pdl(gemm_tc_persistent_kernel<kBF16, EPI>, dim3(grid),
-               dim3(TcCfg<kBF16, 128>::THREADS), PersistCfg<kBF16>::SMEM, st, g);
-  }
+  launch_pdl(gemm_tc_persistent_kernel<kBF16, EPI>, dim3(grid), dim3(TcCfg<kBF16, 128>::THREADS),
+             PersistCfg<kBF16>::SMEM, st, g);
   count_launch();
   return check_launch();
 }
@@ -1546,25 +1501,11 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
   const int64_t chunk = std::max<int64_t>(2, cdiv(total_units, kNumSMs));
   for (int q = 0; q < count; ++q)
     want[q] = std::max<int64_t>(1, cdiv(cdiv(probs[q].K, unit), chunk));
-  // The unsplit products run persistent; with at least a wave of tiles they run
-  // as cluster pairs sharing the B tile (each CTA loads half of it into both),
-  // which cuts the operand traffic from L2 by a quarter, unless padding the
-  // columns to pairs would add a wave.
-  int64_t plain = 0, padded = 0;
-  for (int q = 0; q < count; ++q) {
-    if (want[q] > 1) continue;
-    const TcProblem& pr = probs[q];
-    plain += tiles[q];
-    padded += mc_tile_count((int)cdiv(pr.M, BM), (int)cdiv(pr.N, BN), 1, pr.upper);
-  }
-  const bool mc0 = plain >= kNumSMs && cdiv(padded, kNumSMs) <= cdiv(plain, kNumSMs);
   std::unique_ptr<GroupedTc> g(new GroupedTc());
   for (int pass = 0; pass < 2; ++pass) {   // pass 0: unsplit products; pass 1: split ones
     const int csize = pass == 0 ? 1 : 8;
-    const bool mc = pass == 0 && mc0;
     std::memset(g.get(), 0, sizeof(GroupedTc));
     g->csize = csize;
-    g->mc = mc;
     int blocks = 0;
     size_t part_used = 0, tick_used = 0;
     auto flush = [&]() -> kfac_status {
@@ -1582,7 +1523,6 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
         e = launch_grouped_kernel<false, TC_EPI_PRECOND>(blocks, *g, st);
       std::memset(g.get(), 0, sizeof(GroupedTc));
       g->csize = csize;
-      g->mc = mc;
       blocks = 0;
       part_used = tick_used = 0;
       return e;
@@ -1607,14 +1547,13 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
       const int i = g->count;
       CUtensorMap* m = &g->maps[4 * i];
       if (!make_map(&m[0], pr.A.hi, bf16, pr.A.rows, pr.K, pr.A.pitch, BM)) return KFAC_ERR_CUDA;
-      const int b_box = mc ? BN / 2 : BN;
-      if (!make_map(&m[2], pr.B.hi, bf16, pr.B.rows, pr.K, pr.B.pitch, b_box)) return KFAC_ERR_CUDA;
+      if (!make_map(&m[2], pr.B.hi, bf16, pr.B.rows, pr.K, pr.B.pitch, BN)) return KFAC_ERR_CUDA;
       if (bf16) {
         m[1] = m[0];
         m[3] = m[2];
       } else {
         if (!make_map(&m[1], pr.A.lo, false, pr.A.rows, pr.K, pr.A.pitch, BM)) return KFAC_ERR_CUDA;
-        if (!make_map(&m[3], pr.B.lo, false, pr.B.rows, pr.K, pr.B.pitch, b_box)) return KFAC_ERR_CUDA;
+        if (!make_map(&m[3], pr.B.lo, false, pr.B.rows, pr.K, pr.B.pitch, BN)) return KFAC_ERR_CUDA;
       }
       GemmTcParams& pp = g->prob[i];
       pp.M = pr.M;
@@ -1634,8 +1573,7 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
       pp.layer = pr.layer;
       pp.e = pr.e;
       g->block_start[i] = blocks;
-      blocks += mc ? (int)mc_tile_count(pp.tiles_m, pp.tiles_n, 1, pr.upper)
-                   : (int)(tiles[q] * sh.splits);
+      blocks += (int)(tiles[q] * sh.splits);
       part_used += pneed;
       tick_used += tneed;
       ++g->count;
