@@ -670,8 +670,9 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
     region.  The inputs of all layers are one packed pinned buffer (a diagonal twin
     shares its layer's tensors, so they are copied once), double-buffered on the
     device: the next step's copy runs on a copy stream while this step computes.
-    The parameter read-back also runs on the copy stream; the next step's factor
-    update (and refresh) overlap it, and its parameter updates wait for it.  On
+    The parameter read-back runs on a second copy stream (both directions at
+    once); the next step's factor update (and refresh) overlap it, and its
+    parameter updates wait for it.  On
     steps without a refresh the factor update runs on a side stream alongside
     the preconditioning and the diagonal step (as in the timed steps)."""
     phase_factor, phase_invert, phase_precond, phase_diag = phases
@@ -706,6 +707,7 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
     outs = torch.empty(params_flat.numel(), dtype=torch.float32, pin_memory=True)
     main = torch.cuda.current_stream(dev)
     copy = torch.cuda.Stream(dev)
+    copy_out = torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event(), torch.cuda.Event()]
     ev_used = [torch.cuda.Event(), torch.cuda.Event()]
     ev_done, ev_out = torch.cuda.Event(), torch.cuda.Event()
@@ -760,15 +762,16 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
             main.wait_event(ev_djoin)
         ev_used[b].record(main)
         ev_done.record(main)
-        with torch.cuda.stream(copy):
-            copy.wait_event(ev_done)
+        with torch.cuda.stream(copy_out):      # device -> host on its own stream, so it
+            copy_out.wait_event(ev_done)       # runs alongside the next step's host -> device
             outs.copy_(params_flat, non_blocking=True)
-            ev_out.record(copy)
+            ev_out.record(copy_out)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
     return {"value": round(1.0 / dt, 3), "unit": "steps/s", "h2d_bytes_per_step": int(total),
             "d2h_bytes_per_step": int(params_flat.numel() * 4), "steps": steps,
-            "pipelined": "copy stream: next step H2D during this step, parameter D2H during the next factor update"}
+            "pipelined": "two copy streams: the next step's H2D during this step, this step's "
+                         "parameter D2H during the next step's factor update (both directions at once)"}
 
 
 # ----------------------------------------------------------------------------- micro
