@@ -645,7 +645,8 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, layers, data[0], params_flat, srcidx, t, dev,
-                      (phase_factor, phase_invert, phase_precond, phase_diag), k, overlap)
+                      (phase_factor, phase_invert, phase_precond, phase_diag), k, overlap,
+                      graphs.get(("invert", 0)))
     return {
         "ms_per_step": ms_step, "phases": phases, "roofline": roof, "clocks": clocks,
         "gpu_launches": int(launches), "wall_s": wall, "e2e": e2e,
@@ -664,7 +665,8 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     }
 
 
-def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap):
+def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap,
+            invert_graph=None):
     """Same step through the public API from pinned host memory: every step copies its
     inputs host -> device and reads every updated parameter back, inside the timed
     region.  The inputs of all layers are one packed pinned buffer (a diagonal twin
@@ -674,7 +676,10 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
     once); the next step's factor update (and refresh) overlap it, and its
     parameter updates wait for it.  On
     steps without a refresh the factor update runs on a side stream alongside
-    the preconditioning and the diagonal step (as in the timed steps)."""
+    the preconditioning and the diagonal step (as in the timed steps).  With
+    CUDA graphs (the default) the library calls of each phase are captured once
+    per staging buffer and replayed, as the timed steps do; --no-graphs makes
+    them eagerly every step."""
     phase_factor, phase_invert, phase_precond, phase_diag = phases
     import torch
     first = {}
@@ -704,6 +709,24 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
         return [per_src[first[srcidx[li]]] for li in range(len(layers))]
 
     xs = [views(0), views(1)]
+    if invert_graph is not None:      # capture each phase on each staging buffer
+        import second_order_optimizer_gb300 as K  # noqa: F401
+        torch.cuda.synchronize()
+        gph = {}
+        for bb in range(2):
+            for name, fn in (("factor", phase_factor), ("precond", phase_precond),
+                             ("diag", phase_diag)):
+                gg = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gg):
+                    fn(xs[bb])
+                gph[(name, bb)] = gg
+        torch.cuda.synchronize()
+        run = lambda name, bb: gph[(name, bb)].replay()
+        run_invert = invert_graph.replay
+    else:
+        run = lambda name, bb: {"factor": phase_factor, "precond": phase_precond,
+                                "diag": phase_diag}[name](xs[bb])
+        run_invert = phase_invert
     outs = torch.empty(params_flat.numel(), dtype=torch.float32, pin_memory=True)
     main = torch.cuda.current_stream(dev)
     copy = torch.cuda.Stream(dev)
@@ -715,7 +738,7 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
     dside = torch.cuda.Stream(dev)
     ev_djoin = torch.cuda.Event()
     ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
-    steps = max(3, min(args.steps, 20))
+    steps = max(3, min(args.steps, 50))
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     with torch.cuda.stream(copy):
@@ -732,30 +755,29 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
                     copy.wait_event(ev_used[nb_])   # the step that read that buffer is done
                 stage[nb_].copy_(host, non_blocking=True)
                 ev_in[nb_].record(copy)
-        x = xs[b]
         if overlap:                             # diagonal step alongside the KRON path
             ev_fork.record(main)
             dside.wait_event(ev_fork)
             if i >= 1:
                 dside.wait_event(ev_out)        # previous step's parameters are read back
             with torch.cuda.stream(dside):
-                phase_diag(x)
+                run("diag", b)
                 ev_djoin.record(dside)
         if overlap and (t - 1) % k != 0:       # factor update alongside the rest
             ev_fork.record(main)
             fside.wait_event(ev_fork)
             with torch.cuda.stream(fside):
-                phase_factor(x)
+                run("factor", b)
                 ev_join.record(fside)
         else:
-            phase_factor(x)
+            run("factor", b)
             if (t - 1) % k == 0:
-                phase_invert()
+                run_invert()
         if i >= 1:
             main.wait_event(ev_out)            # previous step's parameters are read back
-        phase_precond(x)
+        run("precond", b)
         if not overlap:
-            phase_diag(x)
+            run("diag", b)
         if overlap and (t - 1) % k != 0:
             main.wait_event(ev_join)
         if overlap:
