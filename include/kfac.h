@@ -300,6 +300,15 @@ kfac_status kfac_diag_step_batched(kfac_handle h, int count, const int* layers,
                                    float* const* out_w, float* const* out_b,
                                    cudaStream_t stream);
 
+/* Failure-detection self-test: enqueue one kernel that waits, through the
+ * same bounded mbarrier wait every pipeline role of the library uses, for a
+ * phase that nothing completes.  The wait gives up after wait_cycles SM clocks
+ * (1 <= wait_cycles <= 2^31; the library's own waits give up after 2e9, about
+ * a second), records KFAC_ERR_TIMEOUT in the status word (layer -1, info 1)
+ * and the kernel returns: no fault, trap or endless loop, and the context
+ * stays usable.  kfac_get_status() then reports (and clears) it. */
+kfac_status kfac_selftest_timeout(kfac_handle h, int64_t wait_cycles, cudaStream_t stream);
+
 /* Synchronise the device and report the first device-side error since the
  * last call (then clear it).  bad_layer / info (nullable) receive the layer
  * and, for KFAC_ERR_NOT_PD, the 0-based column of the failing pivot. */

@@ -223,6 +223,12 @@ class Kfac:
             "kfac_diag_step_batched")
 
     # -- status and state --------------------------------------------------------
+    def selftest_timeout(self, wait_cycles: int, stream=None):
+        """kfac_selftest_timeout: a kernel whose bounded wait runs out; the status
+        word then holds KFAC_ERR_TIMEOUT (read it with get_status)."""
+        _check(LIB.kfac_selftest_timeout(self._h, int(wait_cycles), _stream(stream)),
+               "kfac_selftest_timeout")
+
     def get_status(self):
         """Synchronises; returns (code, layer, info) of the first device error (code 0: none)."""
         layer, info = ctypes.c_int(-1), ctypes.c_int(0)

@@ -75,6 +75,7 @@ SIGNATURES = [
     ("kfac_diag_step", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     ("kfac_diag_step_batched", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                     _vp]),
+    ("kfac_selftest_timeout", _i, [_vp, _i64, _vp]),
     ("kfac_get_status", _i, [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     ("kfac_state_info", _i, [_vp, _i, _i, ctypes.POINTER(_sz), ctypes.POINTER(_sz)]),
     ("kfac_destroy", _i, [_vp]),

@@ -657,6 +657,12 @@ kfac_status kfac_diag_step_batched(kfac_handle h, int count, const int* layers,
   return e;
 }
 
+kfac_status kfac_selftest_timeout(kfac_handle h, int64_t wait_cycles, cudaStream_t stream) {
+  if (!h || wait_cycles < 1 || wait_cycles > (int64_t(1) << 31)) return KFAC_ERR_INVALID_ARG;
+  if (kfac_status e = ensure_device(h)) return e;
+  return launch_wait_selftest(h, wait_cycles, stream);
+}
+
 kfac_status kfac_get_status(kfac_handle h, int* bad_layer, int* info) {
   if (!h) return KFAC_ERR_INVALID_ARG;
   if (kfac_status e = ensure_device(h)) return e;

@@ -224,6 +224,8 @@ kfac_status launch_syrk_tc(kfac_ctx* h, int layer, const void* x, int64_t ld, in
                            int n, int has_bias, bool bf16, float alpha, float beta, float* F,
                            cudaStream_t st);
 int64_t tc_pitch(int64_t cols, bool bf16);
+// one kernel whose bounded wait runs out (failure-detection self-test)
+kfac_status launch_wait_selftest(kfac_ctx* h, int64_t wait_cycles, cudaStream_t st);
 // Source of a gathered pack: the input patches of a 2-D convolution over an
 // NCHW tensor [B, C, H, W] (output Ho x Wo), or, with a 1x1 unit-stride
 // geometry, the rows of an NCHW output gradient.

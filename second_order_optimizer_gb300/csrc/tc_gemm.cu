@@ -1034,6 +1034,25 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
   if (warp == 1) tc::tmem_dealloc(tmem, PC::TMEM_COLS);
 }
 
+// ------------------------------------------------------------ wait self-test
+// One thread waits, through the same bounded wait as the GEMM pipeline's
+// roles, for an mbarrier phase that nothing completes: after `limit` clocks the
+// wait gives up, the kernel records KFAC_ERR_TIMEOUT and returns.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(DevStatus* st, long long limit) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !tc::mbar_wait(&bar, 0, &abort_flag, limit))
+    report_error(st, KFAC_ERR_TIMEOUT, -1, 1);
+}
+
 // ------------------------------------------------------------------- pack
 // X[c][r] = x-hat[r][c] for c < n, r < M; fp32 -> (hi, lo) TF32 halves; bf16 -> copy.
 // One CTA moves a tile of kPackRows rows x 32 columns through shared memory
@@ -1273,6 +1292,12 @@ kfac_status launch_kernel(unsigned grid, const CUtensorMap& ah, const CUtensorMa
 }  // namespace
 
 int64_t tc_pitch(int64_t cols, bool bf16) { return cdiv(cols, bf16 ? 8 : 4) * (bf16 ? 8 : 4); }
+
+kfac_status launch_wait_selftest(kfac_ctx* h, int64_t wait_cycles, cudaStream_t st) {
+  launch_pdl(wait_selftest_kernel, dim3(1), dim3(32), 0, st, h->status(), (long long)wait_cycles);
+  count_launch();
+  return check_launch();
+}
 
 kfac_status launch_pack_grouped(const PackJob* jobs, int count, bool bf16, cudaStream_t st) {
   PackGroup g;

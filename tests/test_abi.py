@@ -103,6 +103,9 @@ def test_null_handle_calls_fail_cleanly(lib):
     geom = lib.Conv2dGeom(1, 1, 3, 3, 3, 3, 1, 1, 1, 1, 1, 1)
     assert L.kfac_update_factors_conv2d(None, 0, None, None, ctypes.byref(geom), 0.0, None) == 1
     assert L.kfac_update_factors_conv2d(None, 0, None, None, None, 0.0, None) == 1
+    assert L.kfac_selftest_timeout(None, 1000, None) == 1
+    assert L.kfac_invert_factors(None, -1, 3, None) == 1
+    assert L.kfac_tie_a_factor(None, 1, 0) == 1
     assert L.kfac_precondition(None, 0, None, 1, None, None, None, None, None, None) == 1
     assert L.kfac_diag_step(None, 0, None, None, None, None, None, None, None, None, None) == 1
 

@@ -608,3 +608,22 @@ def test_hyperparameter_schedules_through_set_hparams():
     assert rel_fro(Wk, st_k.W) <= 1e-4
     assert rel_fro(Wd, st_d.W) <= 1e-6
     assert h.get_status()[0] == 0
+
+
+def test_bounded_wait_reports_timeout_and_the_context_stays_usable():
+    """Failure detection without a fault: a kernel waits, through the library's
+    bounded mbarrier wait, for a phase nothing completes; after ~1 ms of SM clocks
+    it records KFAC_ERR_TIMEOUT and returns.  The status is reported once, then
+    cleared, and the handle computes correctly afterwards."""
+    M, d_in, o = 256, 40, 24
+    h = K.Kfac([(K.KFAC_KRON, o, d_in, 1, K.KFAC_F32)], max_rows=M, **HP)
+    h.selftest_timeout(2_000_000)
+    code, layer, info = h.get_status()
+    assert (code, layer, info) == (5, -1, 1)
+    assert h.get_status()[0] == 0                      # reported once, then cleared
+    a, g = _inputs(M, d_in, o)
+    h.update_factors(0, to_dev(a), to_dev(g))
+    assert h.get_status()[0] == 0
+    assert rel_fro(to_np(h.state(0, K.KFAC_STATE_A)), 0.05 * O.factor(a, 1)) <= 1e-5
+    with pytest.raises(K.KfacError):
+        h.selftest_timeout(0)
