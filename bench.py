@@ -62,8 +62,8 @@ TF32_PER_BF16 = 1.1 / 2.25          # nominal dense ratio
 # change to them reports null until the counters are taken again.
 MEASURED_TRAFFIC = {
     "workload": "mlp4",
-    "sources_sha256": "5331a9eb514562ed9943b463e5234b9818dbb30c0b099edf0ff11b7d84eb5ab9",
-    "bytes": {"factor": 105.13e6, "precond": 148.66e6, "diag": 68.09e6},
+    "sources_sha256": "07d669027f24110225f12092480f5c06a4f9b6a7b2d1c3602f505312f3202cf7",
+    "bytes": {"factor": 105.79e6, "precond": 150.25e6, "diag": 68.04e6},
 }
 
 
