@@ -47,6 +47,12 @@ one is also listed in the repository's design notes):
       warm-up of w steps, afterwards A every k_A and G every k_G steps counted
       from the end of the warm-up; a factor skipped on a step keeps both its
       running value and its inverse.
+  R11 inverse-free update: K (K K^T in place of (F + sqrt(gamma) I)^{-1}) is
+      seeded from the Cholesky refresh (K = L^{-T}) and stepped by
+      K <- K (I - (beta/2)(K^T (F + sqrt(gamma) I) K - I)), beta in (0, 2);
+      the preconditioner uses K K^T.  The page states only that the update is
+      inverse-free and subtracts in the matrix-logarithm space; this first-order
+      exponential-map step on K's right factor is the plainest such update.
 
 Parity pins for every function live in tests/test_oracle.py.
 """
@@ -207,6 +213,34 @@ def spd_inverse_from_cholesky(L) -> np.ndarray:
 def damped_inverse(F, damping: float) -> np.ndarray:
     """(F + sqrt(gamma) I)^{-1} via the textbook Cholesky and substitutions."""
     return spd_inverse_from_cholesky(cholesky_lower(damped(F, damping)))
+
+
+# ---------------------------------------------------------------------------
+# inverse-free factor update ("Structured Inverse-Free Natural Gradient" page,
+# abstract: an inverse-free K-FAC update by subtraction in the matrix-logarithm
+# space instead of an inversion; reading R11 below)
+
+def ikfac_init(F, damping: float) -> np.ndarray:
+    """K = L^{-T} for F + sqrt(gamma) I = L L^T, so that K K^T = (F + sqrt(gamma) I)^{-1}
+    exactly (the factor left by a Cholesky refresh)."""
+    return lower_inverse(cholesky_lower(damped(F, damping))).T
+
+
+def ikfac_update(K, F, damping: float, beta: float) -> np.ndarray:
+    """One inverse-free step on K, where K K^T stands for (F + sqrt(gamma) I)^{-1}:
+    with E = K^T (F + sqrt(gamma) I) K - I (zero when K K^T is the exact inverse),
+    K <- K (I - (beta/2) E): the first-order form of K exp(-(beta/2) E), a
+    subtraction of (beta/2) E in the logarithm of K's right factor."""
+    K = _f64(K)
+    n = K.shape[0]
+    E = K.T @ damped(F, damping) @ K - np.eye(n)
+    return K @ (np.eye(n) - 0.5 * beta * E)
+
+
+def ikfac_inverse(K) -> np.ndarray:
+    """The preconditioning inverse K K^T."""
+    K = _f64(K)
+    return K @ K.T
 
 
 # ---------------------------------------------------------------------------

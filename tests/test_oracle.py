@@ -446,3 +446,61 @@ def test_shared_a_uses_the_source_inverse():
     Ad = O.factor(a, 1) * 0.1 + math.sqrt(1e-2) * np.eye(5)
     ref = np.linalg.solve(Gd, np.linalg.solve(Ad.T, O.grad_hat(gw, gb).T).T)
     np.testing.assert_allclose(P, ref, rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- inverse-free update
+
+def _spd(n, seed, cond=50.0):
+    rng = np.random.default_rng(seed)
+    Q, _ = np.linalg.qr(rng.standard_normal((n, n)))
+    return (Q * np.linspace(1.0, cond, n)) @ Q.T * 1e-2
+
+
+def test_ikfac_init_is_the_exact_inverse_factor():
+    F = _spd(7, 1)
+    K = O.ikfac_init(F, 1e-2)
+    Fd = F + 0.1 * np.eye(7)
+    np.testing.assert_allclose(K @ K.T, np.linalg.inv(Fd), rtol=1e-10, atol=1e-12)
+    assert np.allclose(np.tril(K, -1), 0.0)          # L^{-T} is upper triangular
+
+
+def test_ikfac_fixed_point():
+    """At K K^T = (F + sqrt(gamma) I)^{-1} the residual vanishes and K stays."""
+    F = _spd(9, 2)
+    K = O.ikfac_init(F, 1e-2)
+    np.testing.assert_allclose(O.ikfac_update(K, F, 1e-2, 0.7), K, rtol=0, atol=1e-12)
+
+
+def test_ikfac_scalar_closed_form():
+    """n = 1: k <- k (1 - (beta/2)(f_d k^2 - 1)), in exact rationals."""
+    k, f, gam, beta = Fraction(3, 4), Fraction(5, 2), Fraction(1, 16), Fraction(1, 2)
+    fd = f + Fraction(1, 4)                              # sqrt(1/16)
+    want = k * (1 - beta / 2 * (fd * k * k - 1))
+    got = O.ikfac_update(np.array([[float(k)]]), np.array([[float(f)]]), float(gam), float(beta))
+    assert got[0, 0] == pytest.approx(float(want), rel=1e-15)
+
+
+def test_ikfac_is_first_order_exponential_map():
+    """One step equals K expm(-(beta/2) E) up to O(beta^2) (scipy's expm): the
+    error falls by about 4x when beta halves."""
+    F = _spd(6, 3)
+    K0 = O.ikfac_init(_spd(6, 4), 1e-2)                  # the inverse factor of another F
+    E = K0.T @ (F + 0.1 * np.eye(6)) @ K0 - np.eye(6)
+    errs = []
+    for beta in (0.02, 0.01, 0.005):
+        exact = K0 @ scipy.linalg.expm(-0.5 * beta * E)
+        errs.append(np.linalg.norm(O.ikfac_update(K0, F, 1e-2, beta) - exact))
+    assert 3.5 < errs[0] / errs[1] < 4.5 and 3.5 < errs[1] / errs[2] < 4.5
+
+
+@pytest.mark.parametrize("beta", [0.5, 1.0, 1.5])
+def test_ikfac_iteration_converges_to_the_lapack_inverse(beta):
+    """Repeated steps with a fixed F drive K K^T to (F + sqrt(gamma) I)^{-1}
+    (np.linalg.inv), from the inverse factor of a nearby F."""
+    F1 = _spd(8, 5)
+    F2 = F1 + 0.2 * _spd(8, 6)
+    K = O.ikfac_init(F1, 1e-2)
+    for _ in range(60):
+        K = O.ikfac_update(K, F2, 1e-2, beta)
+    np.testing.assert_allclose(O.ikfac_inverse(K), np.linalg.inv(F2 + 0.1 * np.eye(8)),
+                               rtol=1e-9, atol=1e-9)
