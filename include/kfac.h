@@ -90,6 +90,8 @@ typedef struct {
   double weight_decay;  /* lambda: u = P + lambda W ; m <- mu m + u ; W <- W - eta m */
   int ema_init;         /* kfac_ema_init                                             */
   int math;             /* kfac_math                                                 */
+  int ikfac;            /* 0/1: keep inverse factors K for kfac_ikfac_update (fixed at
+                           kfac_create; 32 n^2 extra workspace bytes per n x n factor) */
 } kfac_hparams;
 
 typedef struct kfac_ctx* kfac_handle;
@@ -233,6 +235,23 @@ kfac_status kfac_invert(kfac_handle h, int layer, cudaStream_t stream);
  * own: KFAC_FACTOR_A is ignored for it (its source's refresh covers it).
  * which outside 1..3: KFAC_ERR_INVALID_ARG. */
 kfac_status kfac_invert_factors(kfac_handle h, int layer, int which, cudaStream_t stream);
+
+/* Inverse-free refresh ("Structured Inverse-Free Natural Gradient" page,
+ * abstract: an inverse-free K-FAC update that subtracts in the matrix-logarithm
+ * space instead of inverting).  For each factor F of the layer (or of every
+ * KRON layer, layer == -1) the handle keeps K with K K^T standing for
+ * (F + sqrt(gamma) I)^{-1}; one call takes the step
+ *   K <- K (I - (beta/2) (K^T (F + sqrt(gamma) I) K - I)),
+ * the first-order form of K exp(-(beta/2) E) (E vanishes at the exact inverse),
+ * and sets the layer's inverse to K K^T, which kfac_precondition then uses.
+ * Every product runs on the tensor cores (3xTF32); no factorisation.  K is
+ * seeded by each kfac_invert of the factor (K = L^{-T}, exactly the inverse
+ * factor), so a factor needs one kfac_invert before its first update.
+ * Requires a handle created with hp->ikfac = 1 (else KFAC_ERR_UNSUPPORTED),
+ * 0 < beta < 2 (else KFAC_ERR_INVALID_ARG), and an inverted factor (else
+ * KFAC_ERR_STATE).  A tied A is stepped with its source.  Like kfac_invert,
+ * it must not overlap other calls of the handle. */
+kfac_status kfac_ikfac_update(kfac_handle h, int layer, double beta, cudaStream_t stream);
 
 /* Tie layer's A factor to source's: from now on `layer` uses source's running
  * A and A inverse (kfac_state_info reports source's), has no A update or

@@ -70,12 +70,13 @@ class Kfac:
 
     def __init__(self, layers: Sequence, ema_decay=0.95, damping=1e-3, lr=1e-2, momentum=0.9,
                  weight_decay=5e-4, ema_init=KFAC_EMA_INIT_ZERO, math=KFAC_MATH_3XTF32,
-                 max_rows: int = 1, device=None):
+                 max_rows: int = 1, device=None, ikfac: int = 0):
         import torch
         descs = [l if isinstance(l, LayerDesc) else LayerDesc(*l) for l in layers]
         self.n_layers = len(descs)
         self._descs = (LayerDesc * self.n_layers)(*descs)
-        self._hp = HParams(ema_decay, damping, lr, momentum, weight_decay, ema_init, math)
+        self._hp = HParams(ema_decay, damping, lr, momentum, weight_decay, ema_init, math,
+                           int(ikfac))
         self.max_rows = int(max_rows)
         nbytes = ctypes.c_size_t(0)
         _check(LIB.kfac_workspace_size(self._descs, self.n_layers, ctypes.byref(self._hp),
@@ -183,6 +184,12 @@ class Kfac:
         else:
             _check(LIB.kfac_invert_factors(self._h, layer, which, _stream(stream)),
                    "kfac_invert_factors")
+
+    def ikfac_update(self, layer: int = -1, beta: float = 1.0, stream=None):
+        """kfac_ikfac_update: one inverse-free step of the inverse factors (handle
+        created with ikfac=1); the layer's inverses become K K^T."""
+        _check(LIB.kfac_ikfac_update(self._h, layer, float(beta), _stream(stream)),
+               "kfac_ikfac_update")
 
     def tie_a_factor(self, layer: int, source: int):
         """kfac_tie_a_factor: layer uses source's A (same input); synchronous."""

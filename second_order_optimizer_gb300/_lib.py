@@ -36,7 +36,7 @@ class HParams(ctypes.Structure):
     _fields_ = [("ema_decay", ctypes.c_double), ("damping", ctypes.c_double),
                 ("lr", ctypes.c_double), ("momentum", ctypes.c_double),
                 ("weight_decay", ctypes.c_double), ("ema_init", ctypes.c_int),
-                ("math", ctypes.c_int)]
+                ("math", ctypes.c_int), ("ikfac", ctypes.c_int)]
 
 
 class Conv2dGeom(ctypes.Structure):
@@ -69,6 +69,7 @@ SIGNATURES = [
                                        _vp]),
     ("kfac_invert", _i, [_vp, _i, _vp]),
     ("kfac_invert_factors", _i, [_vp, _i, _i, _vp]),
+    ("kfac_ikfac_update", _i, [_vp, _i, _d, _vp]),
     ("kfac_tie_a_factor", _i, [_vp, _i, _i]),
     ("kfac_precondition", _i, [_vp, _i, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     ("kfac_precondition_batched", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),

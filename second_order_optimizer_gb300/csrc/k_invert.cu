@@ -498,6 +498,8 @@ kfac_status launch_outer_update(kfac_ctx* h, int j0, int nj, int K0, int W, cuda
   return flush();
 }
 
+kfac_status launch_ikfac_seed(const InvJob* jobs, int nj, int nmax, cudaStream_t st);
+
 kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
   // job range: the table section of the wanted factors (both, A only, G only),
   // whole or the entries of one layer (contiguous: a section is in layer order)
@@ -606,6 +608,213 @@ kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
   if (!big.empty())
     if (kfac_status e = launch_syrk_tc_batched(h, big.data(), (int)big.size(), st)) return e;
   launch_pdl(inv_split_kernel, dim3(dim3((unsigned)std::min<int64_t>(cdiv((int64_t)nmax * nmax, 256), 1024), nj)), dim3(256), 0, st, jobs);
+  count_launch();
+  if (kfac_status e = check_launch()) return e;
+  // inverse-free update: K = X^T (so K K^T = X^T X = F_d^{-1}), and K^T = X
+  if (h->hp.ikfac) return launch_ikfac_seed(jobs, nj, nmax, st);
+  return KFAC_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Inverse-free update ("Structured Inverse-Free Natural Gradient" page,
+// abstract: an inverse-free K-FAC update by subtraction in the matrix-logarithm
+// space).  Per factor, K (K K^T standing for F_d^{-1}) takes the step
+//   K <- K (I - (beta/2)(K^T F_d K - I))
+// as tensor-core products with the transposed-store epilogue (C = A B^T on
+// K-major TF32-half operands, C^T stored as halves):
+//   S1 <- F_d                    (damped, split)
+//   S2 <- (F_d K)^T              A = S1, B = K^T
+//   S1 <- (K^T F_d K)^T          A = K^T, B = S2
+//   S1 <- (1 + beta/2) I - (beta/2) S1          (= M^T)
+//   K^T <- (K M)^T               A = K, B = S1
+//   K <- (K^T)^T                 (transpose of the halves)
+//   F_d^{-1} <- K K^T            SYRK, A = B = K; then its halves for K4.
+// Every array is n x np (np = n rounded up to 4, the TMA row pitch).
+
+namespace {
+
+constexpr int kTT = 32;   // transpose tile
+
+// K^T = X (lower, pitch n) and K = X^T, as TF32 halves.
+__global__ void __launch_bounds__(256) ik_seed_kernel(const InvJob* jobs) {
+  pdl_wait();
+  pdl_trigger();
+  const InvJob J = jobs[blockIdx.y];
+  const int tn = (J.n + kTT - 1) / kTT;
+  if ((int)blockIdx.x >= tn * tn) return;
+  const int r0 = (blockIdx.x / tn) * kTT, c0 = (blockIdx.x % tn) * kTT;
+  __shared__ float t[kTT][kTT + 1];
+  const int tx = threadIdx.x % kTT, ty = threadIdx.x / kTT;   // 32 x 8
+  for (int rr = ty; rr < kTT; rr += 8) {
+    const int r = r0 + rr, c = c0 + tx;
+    float v = 0.f;
+    if (r < J.n && c < J.n) {
+      v = J.X[(int64_t)r * J.n + c];
+      const float hi = tc::to_tf32(v);
+      J.Kt_hi[(int64_t)r * J.np + c] = hi;
+      J.Kt_lo[(int64_t)r * J.np + c] = tc::to_tf32(v - hi);
+    }
+    t[rr][tx] = v;
+  }
+  __syncthreads();
+  for (int cc = ty; cc < kTT; cc += 8) {   // K[c][r] = X[r][c]
+    const int c = c0 + cc, r = r0 + tx;
+    if (r < J.n && c < J.n) {
+      const float v = t[tx][cc];
+      const float hi = tc::to_tf32(v);
+      J.K_hi[(int64_t)c * J.np + r] = hi;
+      J.K_lo[(int64_t)c * J.np + r] = tc::to_tf32(v - hi);
+    }
+  }
+}
+
+// S1 <- split(F + sqrt(gamma) I)  (F: running factor, pitch n)
+__global__ void __launch_bounds__(256) ik_damped_split_kernel(const InvJob* jobs, float sqrt_gamma) {
+  pdl_wait();
+  pdl_trigger();
+  const InvJob J = jobs[blockIdx.y];
+  const int64_t nn = (int64_t)J.n * J.n;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / J.n, c = e % J.n;
+    const float v = J.F[e] + (r == c ? sqrt_gamma : 0.f);
+    const float hi = tc::to_tf32(v);
+    J.S1_hi[r * J.np + c] = hi;
+    J.S1_lo[r * J.np + c] = tc::to_tf32(v - hi);
+  }
+}
+
+// S1 <- split(c1 I - c2 S1)
+__global__ void __launch_bounds__(256) ik_affine_kernel(const InvJob* jobs, float c1, float c2) {
+  pdl_wait();
+  pdl_trigger();
+  const InvJob J = jobs[blockIdx.y];
+  const int64_t nn = (int64_t)J.n * J.n;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / J.n, c = e % J.n, x = r * J.np + c;
+    const float v = fmaf(-c2, J.S1_hi[x] + J.S1_lo[x], r == c ? c1 : 0.f);
+    const float hi = tc::to_tf32(v);
+    J.S1_hi[x] = hi;
+    J.S1_lo[x] = tc::to_tf32(v - hi);
+  }
+}
+
+// K <- (K^T)^T, both halves, through 32 x 33 shared tiles
+__global__ void __launch_bounds__(256) ik_transpose_kernel(const InvJob* jobs) {
+  pdl_wait();
+  pdl_trigger();
+  const InvJob J = jobs[blockIdx.y];
+  const int tn = (J.n + kTT - 1) / kTT;
+  if ((int)blockIdx.x >= tn * tn) return;
+  const int r0 = (blockIdx.x / tn) * kTT, c0 = (blockIdx.x % tn) * kTT;
+  __shared__ float th[kTT][kTT + 1], tl[kTT][kTT + 1];
+  const int tx = threadIdx.x % kTT, ty = threadIdx.x / kTT;
+  for (int rr = ty; rr < kTT; rr += 8) {
+    const int r = r0 + rr, c = c0 + tx;
+    const bool in = r < J.n && c < J.n;
+    th[rr][tx] = in ? J.Kt_hi[(int64_t)r * J.np + c] : 0.f;
+    tl[rr][tx] = in ? J.Kt_lo[(int64_t)r * J.np + c] : 0.f;
+  }
+  __syncthreads();
+  for (int cc = ty; cc < kTT; cc += 8) {
+    const int c = c0 + cc, r = r0 + tx;
+    if (r < J.n && c < J.n) {
+      J.K_hi[(int64_t)c * J.np + r] = th[tx][cc];
+      J.K_lo[(int64_t)c * J.np + r] = tl[tx][cc];
+    }
+  }
+}
+
+unsigned elem_blocks(int nmax) {
+  return (unsigned)std::min<int64_t>(cdiv((int64_t)nmax * nmax, 256), 1024);
+}
+unsigned tile_blocks(int nmax) {
+  const int64_t tn = cdiv(nmax, kTT);
+  return (unsigned)(tn * tn);
+}
+
+}  // namespace
+
+kfac_status launch_ikfac_seed(const InvJob* jobs, int nj, int nmax, cudaStream_t st) {
+  launch_pdl(ik_seed_kernel, dim3(tile_blocks(nmax), nj), dim3(256), 0, st, jobs);
+  count_launch();
+  return check_launch();
+}
+
+kfac_status launch_ikfac_update(kfac_ctx* h, int layer, float beta, cudaStream_t st) {
+  // the factors: section 0 of the job table (A and G of each layer; no tied A)
+  int j0 = h->tab_start[0], nj = h->tab_count[0];
+  if (layer >= 0) {
+    int first = -1, cnt = 0;
+    for (int i = j0; i < j0 + nj; ++i)
+      if (h->invjobs_host[i].layer == layer) {
+        if (first < 0) first = i;
+        ++cnt;
+      }
+    j0 = first;
+    nj = cnt;
+  }
+  if (nj <= 0) return KFAC_OK;
+  const InvJob* jobs = h->at<InvJob>(h->off_invjobs) + j0;
+  int nmax = 0;
+  for (int i = j0; i < j0 + nj; ++i) nmax = std::max(nmax, h->invjobs_host[i].n);
+  auto check = [](kfac_status e) { return e; };
+  launch_pdl(ik_damped_split_kernel, dim3(elem_blocks(nmax), nj), dim3(256), 0, st, jobs,
+             (float)std::sqrt(h->hp.damping));
+  count_launch();
+  if (kfac_status e = check_launch()) return e;
+  // one grouped launch per product, over every factor
+  auto products = [&](int which, std::vector<TcProblem>* out) {
+    out->clear();
+    for (int i = j0; i < j0 + nj; ++i) {
+      const InvJob& J = h->invjobs_host[i];
+      TcProblem q{};
+      q.M = q.N = q.K = J.n;
+      q.layer = J.layer;
+      if (which == 3) {              // F_d^{-1} <- K K^T
+        q.A = TcOperand{J.K_hi, J.K_lo, J.n, J.np};
+        q.B = q.A;
+        q.same_ab = true;
+        q.upper = true;
+        q.e.alpha = 1.f;
+        q.e.beta = 0.f;
+        q.e.C = J.Finv;
+        q.e.ldc = J.n;
+      } else {
+        const float* a_hi = which == 0 ? J.S1_hi : which == 1 ? J.Kt_hi : J.K_hi;
+        const float* a_lo = which == 0 ? J.S1_lo : which == 1 ? J.Kt_lo : J.K_lo;
+        const float* b_hi = which == 0 ? J.Kt_hi : which == 1 ? J.S2_hi : J.S1_hi;
+        const float* b_lo = which == 0 ? J.Kt_lo : which == 1 ? J.S2_lo : J.S1_lo;
+        q.A = TcOperand{a_hi, a_lo, J.n, J.np};
+        q.B = TcOperand{b_hi, b_lo, J.n, J.np};
+        q.e.out_hi = which == 0 ? J.S2_hi : which == 1 ? J.S1_hi : J.Kt_hi;
+        q.e.out_lo = which == 0 ? J.S2_lo : which == 1 ? J.S1_lo : J.Kt_lo;
+        q.e.ldo = J.np;
+      }
+      out->push_back(q);
+    }
+  };
+  std::vector<TcProblem> pr;
+  for (int which = 0; which < 3; ++which) {
+    products(which, &pr);
+    if (kfac_status e = check(launch_gemm_tc_grouped(h, false, TC_EPI_SPLIT, pr.data(),
+                                                     (int)pr.size(), st)))
+      return e;
+    if (which == 1) {   // S1 = (K^T F_d K)^T -> M^T = (1 + beta/2) I - (beta/2) S1
+      launch_pdl(ik_affine_kernel, dim3(elem_blocks(nmax), nj), dim3(256), 0, st, jobs,
+                 1.f + 0.5f * beta, 0.5f * beta);
+      count_launch();
+      if (kfac_status e = check_launch()) return e;
+    }
+  }
+  launch_pdl(ik_transpose_kernel, dim3(tile_blocks(nmax), nj), dim3(256), 0, st, jobs);
+  count_launch();
+  if (kfac_status e = check_launch()) return e;
+  products(3, &pr);
+  if (kfac_status e = launch_gemm_tc_grouped(h, false, TC_EPI_SYRK, pr.data(), (int)pr.size(), st))
+    return e;
+  launch_pdl(inv_split_kernel, dim3(elem_blocks(nmax), nj), dim3(256), 0, st, jobs);
   count_launch();
   return check_launch();
 }

@@ -25,6 +25,7 @@ bool valid_hp(const kfac_hparams* hp) {
     return false;
   if (hp->ema_init != KFAC_EMA_INIT_ZERO && hp->ema_init != KFAC_EMA_INIT_FIRST) return false;
   if (hp->math != KFAC_MATH_3XTF32 && hp->math != KFAC_MATH_BF16) return false;
+  if (hp->ikfac != 0 && hp->ikfac != 1) return false;
   return true;
 }
 
@@ -45,7 +46,8 @@ struct Plan {
   int n_invjobs, max_kron_n;
 };
 
-bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) {
+bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, const kfac_hparams* hp,
+               Plan* P) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -84,6 +86,9 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, Plan* P) 
       L.Ainv_lo = take(n * np * f);
       L.Ginv_hi = take(o * op * f);
       L.Ginv_lo = take(o * op * f);
+      for (int w = 0; w < 2; ++w)
+        for (int a = 0; a < 8; ++a)
+          L.ik[w][a] = hp->ikfac ? take((w == 0 ? n * np : o * op) * f) : 0;
       size_t t1 = 0, t2 = 0;
       part = std::max(part, k1_scratch_floats(L.n, max_rows, &t1));
       part = std::max(part, k1_scratch_floats(L.o, max_rows, &t2));
@@ -192,6 +197,10 @@ kfac_status write_inv_tables(kfac_ctx* h) {
     j.Finv = h->at<float>(w == 0 ? L.Ainv : L.Ginv);
     j.Finv_hi = h->at<float>(w == 0 ? L.Ainv_hi : L.Ginv_hi);
     j.Finv_lo = h->at<float>(w == 0 ? L.Ainv_lo : L.Ginv_lo);
+    if (h->hp.ikfac) {
+      float** dst[8] = {&j.K_hi, &j.K_lo, &j.Kt_hi, &j.Kt_lo, &j.S1_hi, &j.S1_lo, &j.S2_hi, &j.S2_lo};
+      for (int a = 0; a < 8; ++a) *dst[a] = h->at<float>(L.ik[w][a]);
+    }
     j.n = n;
     j.np = (int)tc_pitch(n, false);
     j.layer = i;
@@ -320,7 +329,7 @@ kfac_status kfac_workspace_size(const kfac_layer_desc* layers, int n_layers,
   for (int i = 0; i < n_layers; ++i)
     if (!valid_desc(layers[i])) return KFAC_ERR_INVALID_ARG;
   Plan P;
-  make_plan(layers, n_layers, max_rows, &P);
+  make_plan(layers, n_layers, max_rows, hp, &P);
   *bytes = P.total;
   return KFAC_OK;
 }
@@ -334,7 +343,7 @@ kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_
   if (!d_workspace || !aligned(d_workspace, kAlign) || bytes < need) return KFAC_ERR_WORKSPACE;
   if (hp->math != KFAC_MATH_3XTF32) return KFAC_ERR_UNSUPPORTED;
   Plan P;
-  make_plan(layers, n_layers, max_rows, &P);
+  make_plan(layers, n_layers, max_rows, hp, &P);
   kfac_ctx* h = new (std::nothrow) kfac_ctx();
   if (!h) return KFAC_ERR_INVALID_ARG;
   if (cudaGetDevice(&h->device) != cudaSuccess) {
@@ -385,6 +394,7 @@ kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_
 
 kfac_status kfac_set_hparams(kfac_handle h, const kfac_hparams* hp) {
   if (!h || !valid_hp(hp)) return KFAC_ERR_INVALID_ARG;
+  if (hp->ikfac != h->hp.ikfac) return KFAC_ERR_INVALID_ARG;   // fixed at creation
   if (hp->math != KFAC_MATH_3XTF32) return KFAC_ERR_UNSUPPORTED;
   h->hp = *hp;
   return KFAC_OK;
@@ -513,6 +523,21 @@ kfac_status kfac_invert_factors(kfac_handle h, int layer, int which, cudaStream_
   return KFAC_OK;
 }
 
+kfac_status kfac_ikfac_update(kfac_handle h, int layer, double beta, cudaStream_t stream) {
+  if (!h) return KFAC_ERR_INVALID_ARG;
+  if (!h->hp.ikfac) return KFAC_ERR_UNSUPPORTED;
+  if (!(beta > 0.0 && beta < 2.0)) return KFAC_ERR_INVALID_ARG;
+  if (layer != -1 && check_layer(h, layer, KFAC_KRON) != KFAC_OK) return KFAC_ERR_INVALID_ARG;
+  if (h->n_invjobs == 0) return layer == -1 ? KFAC_OK : KFAC_ERR_INVALID_ARG;
+  for (int i = 0; i < (int)h->layers.size(); ++i) {
+    const LayerInfo& L = h->layers[i];
+    if (L.kind != KFAC_KRON || (layer != -1 && layer != i)) continue;
+    if (!has_inverses(h, L)) return KFAC_ERR_STATE;   // K is seeded by kfac_invert
+  }
+  if (kfac_status e = ensure_device(h)) return e;
+  return launch_ikfac_update(h, layer, (float)beta, stream);
+}
+
 kfac_status kfac_invert(kfac_handle h, int layer, cudaStream_t stream) {
   return kfac_invert_factors(h, layer, KFAC_FACTOR_A | KFAC_FACTOR_G, stream);
 }
@@ -537,6 +562,7 @@ kfac_status kfac_tie_a_factor(kfac_handle h, int layer, int source) {
   L.Ainv = S.Ainv;
   L.Ainv_hi = S.Ainv_hi;
   L.Ainv_lo = S.Ainv_lo;
+  for (int a = 0; a < 8; ++a) L.ik[0][a] = S.ik[0][a];
   kfac_status e = write_inv_tables(h);
   if (e == KFAC_OK && cudaDeviceSynchronize() != cudaSuccess) e = KFAC_ERR_CUDA;
   return e;

@@ -78,6 +78,9 @@ struct InvJob {
   float* Finv;      // result (n x n, pitch n)
   float* Finv_hi;   // result as TF32 halves, pitch np (operands of the K4 products)
   float* Finv_lo;
+  // inverse-free update (handles created with ikfac): K and K^T as TF32 halves,
+  // and two scratch operands, all n x np; null otherwise
+  float *K_hi, *K_lo, *Kt_hi, *Kt_lo, *S1_hi, *S1_lo, *S2_hi, *S2_lo;
   int n, np;
   int layer;
 };
@@ -87,6 +90,7 @@ struct LayerInfo {
   // KRON state
   size_t A, G, Ainv, Ginv, LA, LG, XA, XG, YA, YG, m;
   size_t Ainv_hi, Ainv_lo, Ginv_hi, Ginv_lo;   // pitch n_p / o_p (multiples of 4)
+  size_t ik[2][8];   // ikfac: K hi/lo, K^T hi/lo, S1 hi/lo, S2 hi/lo of A (0) and G (1)
   // DIAG state
   size_t gs, as, ticket;
   // host-side counters: updates of each factor, and whether each has an inverse
@@ -177,6 +181,8 @@ kfac_status launch_update_factors_batched(kfac_ctx* h, int count, const int* lay
                                           const kfac_conv2d_geom* geoms = nullptr);
 // K2 / K3: which = KFAC_FACTOR_A | KFAC_FACTOR_G; layer -1 = every KRON layer
 kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t s);
+// inverse-free refresh of the factors of `layer` (-1: all)
+kfac_status launch_ikfac_update(kfac_ctx* h, int layer, float beta, cudaStream_t s);
 // (re)write the inversion job tables on the host and the device (synchronous)
 kfac_status write_inv_tables(kfac_ctx* h);
 // K4

@@ -85,6 +85,7 @@ def test_workspace_size_rejects_bad_arguments(lib):
         ([(0, 4, 4, 1, 0)], _hp(lib, damping=0.0)),
         ([(0, 4, 4, 1, 0)], _hp(lib, damping=float("nan"))),
         ([(0, 4, 4, 1, 0)], _hp(lib, math=7)),
+        ([(0, 4, 4, 1, 0)], _hp(lib, ikfac=2)),
     ]
     for layers, h in bad:
         d = _descs(lib, layers)
@@ -143,3 +144,15 @@ def test_package_refuses_to_load_without_the_library(tmp_path):
                        cwd=tmp_path, capture_output=True, text=True)
     assert r.returncode != 0
     assert "libkfac.so is missing" in r.stderr
+
+
+def test_workspace_holds_the_inverse_factors_when_asked(lib):
+    """ikfac = 1 adds the inverse factors and their scratch: 8 arrays of n x np
+    floats per n x n factor (np = n rounded up to 4)."""
+    d = _descs(lib, [(0, 100, 299, 1, 0)])            # A: 300 x 300, G: 100 x 100
+    out0, out1 = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.LIB.kfac_workspace_size(d, 1, ctypes.byref(_hp(lib)), 64, ctypes.byref(out0)) == 0
+    assert lib.LIB.kfac_workspace_size(d, 1, ctypes.byref(_hp(lib, ikfac=1)), 64,
+                                       ctypes.byref(out1)) == 0
+    want = 8 * 4 * (300 * 300 + 100 * 100)
+    assert want <= out1.value - out0.value <= want + 16 * 256
