@@ -33,13 +33,16 @@ METRIC = "K-FAC precond steps/s; factor-GEMM TFLOP/s & diag-step GB/s vs GB300 p
 WORKLOADS = {"mlp4": "c2", "single_linear": "c1", "resnet18": "c3", "resnet50": "c4",
              "resnet50_bf16": "c4bf16", "transformer4": "c5",
              "resnet18_nchw": "c3", "resnet50_nchw": "c4", "resnet50_bf16_nchw": "c4bf16",
-             "transformer4_qkv_tied": "c5"}
+             "transformer4_qkv_tied": "c5", "mlp4_ikfac": "c2"}
 # workloads whose convolutions hand the library their NCHW input and output
 # gradient (kfac_update_factors_conv2d_batched) instead of unfolded matrices
 NCHW_WORKLOADS = {"resnet18_nchw", "resnet50_nchw", "resnet50_bf16_nchw"}
 # workloads whose key and value projections share the query projection's A
 # factor (kfac_tie_a_factor: the three read the same input)
 TIED_WORKLOADS = {"transformer4_qkv_tied"}
+# workloads whose refreshes after the first are inverse-free steps
+# (kfac_ikfac_update, beta = 1) instead of Cholesky inversions
+IKFAC_WORKLOADS = {"mlp4_ikfac"}
 
 
 def qkv_ties(layers):
@@ -150,7 +153,7 @@ def job_throughput(ms_per_step_max: float, world: int) -> float:
 
 # ----------------------------------------------------------------------------- accounting
 
-def algorithmic(layers, k, nchw=False, tied=()):
+def algorithmic(layers, k, nchw=False, tied=(), ikfac=False):
     """Per-step algorithmic flops and bytes of each phase (fp32 state, input dtype as given).
     nchw: convolutions read their NCHW input and output gradient, not unfolded matrices.
     tied: indices of layers whose A is another layer's (no A product or inverse)."""
@@ -169,7 +172,9 @@ def algorithmic(layers, k, nchw=False, tied=()):
             else:
                 f["factor_bytes"] += M * (l.d_in * own_a + o) * elt
             f["factor_bytes"] += 2 * 4 * (n * n * own_a + o * o)
-            f["invert_flop"] += (n ** 3 * own_a + o ** 3) / k     # Cholesky n^3/3 + L^-1 n^3/3 + X^T X n^3/3
+            # Cholesky n^3/3 + L^-1 n^3/3 + X^T X n^3/3; inverse-free: three n^3 products
+            # (2 n^3 each) and K K^T (n^3, upper triangle)
+            f["invert_flop"] += (7 if ikfac else 1) * (n ** 3 * own_a + o ** 3) / k
             f["precond_flop"] += 2 * o * n * n + 2 * o * o * n
             f["precond_bytes"] += 4 * (n * n + o * o + 2 * o * n) + 4 * 3 * o * n
         else:
@@ -249,7 +254,8 @@ def blas_threads():
     return len(os.sched_getaffinity(0))
 
 
-def oracle_steps_per_s(cfg, layers, budget_s=20.0, min_s=10.0, nchw=False, tied=False):
+def oracle_steps_per_s(cfg, layers, budget_s=20.0, min_s=10.0, nchw=False, tied=False,
+                       ikfac=False):
     """Time the float64 oracle as it stands on a bounded sample of the workload.
 
     Sample: one K-FAC step of as many KRON layers as fit the budget (factor
@@ -260,7 +266,8 @@ def oracle_steps_per_s(cfg, layers, budget_s=20.0, min_s=10.0, nchw=False, tied=
     scaled to the whole layer set, with the refresh amortised by the cadence.
     nchw: convolutions build their factors from NCHW draws through the oracle's
     input patches, as the GPU arm's NCHW workloads do.  tied: key and value
-    projections use the query projection's A (no A of their own)."""
+    projections use the query projection's A (no A of their own).  ikfac: the
+    refresh is the oracle's inverse-free step instead of its inversion."""
     import oracle as O
     hp = cfg.hp
     orc = O.KfacOracle(hp.ema_decay, hp.damping, hp.lr, hp.momentum, hp.weight_decay, 1)
@@ -295,8 +302,13 @@ def oracle_steps_per_s(cfg, layers, budget_s=20.0, min_s=10.0, nchw=False, tied=
             st.A = O.ema(st.A, An, orc.xi)
         st.G = O.ema(st.G, Gn, orc.xi)
         tf = time.perf_counter()
-        st.Ainv = O.damped_inverse(st.A, orc.gamma) if own_a(l) else np.eye(l.n)
-        st.Ginv = O.damped_inverse(st.G, orc.gamma)
+        if ikfac:
+            KA, KG = np.eye(l.n), np.eye(l.d_out)
+            st.Ainv = O.ikfac_inverse(O.ikfac_update(KA, st.A, orc.gamma, 1.0)) if own_a(l) else KA
+            st.Ginv = O.ikfac_inverse(O.ikfac_update(KG, st.G, orc.gamma, 1.0))
+        else:
+            st.Ainv = O.damped_inverse(st.A, orc.gamma) if own_a(l) else np.eye(l.n)
+            st.Ginv = O.damped_inverse(st.G, orc.gamma)
         ti = time.perf_counter()
         P = O.precondition(st.Ginv, O.grad_hat(x["grad_w"], x["grad_b"]), st.Ainv)
         st.W, st.m = O.momentum_update(P, st.W, st.m, orc.lr, orc.mu, orc.wd)
@@ -357,8 +369,9 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     descs = [(K.KFAC_KRON if l.kind == "kron" else K.KFAC_DIAG, l.d_out, l.d_in, l.has_bias, kd(l))
              for l in layers]
     max_rows = max(l.rows for l in layers)
+    ikfac = args.workload in IKFAC_WORKLOADS
     h = K.Kfac(descs, ema_decay=hp.ema_decay, damping=hp.damping, lr=hp.lr, momentum=hp.momentum,
-               weight_decay=hp.weight_decay, max_rows=max_rows, device=dev)
+               weight_decay=hp.weight_decay, max_rows=max_rows, device=dev, ikfac=int(ikfac))
     ties = qkv_ties(layers) if args.workload in TIED_WORKLOADS else {}
     for li, src in ties.items():
         h.tie_a_factor(li, src)
@@ -426,6 +439,14 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     def phase_invert():
         h.invert(-1)
 
+    # the refresh the timed steps replay: the first refresh (a warm-up step) is a
+    # Cholesky inversion, which also seeds the inverse factors of an ikfac handle
+    def phase_refresh():
+        if ikfac:
+            h.ikfac_update(-1, beta=1.0)
+        else:
+            h.invert(-1)
+
     def phase_precond(x):
         if kron_idx:
             h.precondition_batched(kron_idx, [x[li]["grad_w"] for li in kron_idx],
@@ -457,7 +478,7 @@ def run_gpu(args, rank, world, peaks, peak_kind):
         phase_factor(x)
         if ev: ev[1].record(stream)
         if (t - 1) % k == 0:
-            phase_invert()
+            phase_invert() if t == 1 else phase_refresh()
         if ev: ev[2].record(stream)
         phase_precond(x)
         if ev: ev[3].record(stream)
@@ -493,7 +514,7 @@ def run_gpu(args, rank, world, peaks, peak_kind):
         g = torch.cuda.CUDAGraph()
         c0 = K.launch_count()
         with torch.cuda.graph(g):
-            phase_invert()
+            phase_refresh()
         graphs[("invert", 0)] = g
         kernels_in[("invert", 0)] = K.launch_count() - c0
         torch.cuda.synchronize()
@@ -591,7 +612,7 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     ph = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
                    for i in range(seq_steps)])  # ms: factor, invert, precond, diag
 
-    acc = algorithmic(layers, k, nchw, set(ties))
+    acc = algorithmic(layers, k, nchw, set(ties), ikfac)
     phase_ms = ph.mean(axis=0)
     phase_ms[1] = inv_ms_refresh / k   # invert, amortised over the refresh period
     factor_tfs = acc["factor_flop"] / (phase_ms[0] * 1e-3) / 1e12
@@ -645,14 +666,15 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, layers, data[0], params_flat, srcidx, t, dev,
-                      (phase_factor, phase_invert, phase_precond, phase_diag), k, overlap,
+                      (phase_factor, phase_refresh, phase_precond, phase_diag), k, overlap,
                       graphs.get(("invert", 0)))
     return {
         "ms_per_step": ms_step, "phases": phases, "roofline": roof, "clocks": clocks,
         "gpu_launches": int(launches), "wall_s": wall, "e2e": e2e,
         "config": {"workload": cfg.name + ("+diag_twins" if not cfg.diag_layers else "")
                    + ("+nchw_conv_inputs" if nchw else "")
-                   + ("+qkv_shared_A" if ties else ""),
+                   + ("+qkv_shared_A" if ties else "")
+                   + ("+inverse_free_refresh" if ikfac else ""),
                    "kron_layers": sum(l.kind == "kron" for l in layers),
                    "diag_layers": sum(l.kind == "diag" for l in layers),
                    "invert_every": k, "max_rows": max_rows,
@@ -895,7 +917,8 @@ def main():
         for _ in range(max(1, args.steps)):
             v, sample, _ = oracle_steps_per_s(cfg, layers, budget_s=max(2.0, 60.0 / max(1, args.steps)),
                                               min_s=0.0, nchw=args.workload in NCHW_WORKLOADS,
-                                              tied=args.workload in TIED_WORKLOADS)
+                                              tied=args.workload in TIED_WORKLOADS,
+                                              ikfac=args.workload in IKFAC_WORKLOADS)
             per_step.append(1.0 / v)
             if time.perf_counter() - t0 > 150:
                 break
@@ -907,7 +930,8 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": cfg.name + ("+diag_twins" if not cfg.diag_layers else "")
                            + ("+nchw_conv_inputs" if args.workload in NCHW_WORKLOADS else "")
-                           + ("+qkv_shared_A" if args.workload in TIED_WORKLOADS else ""),
+                           + ("+qkv_shared_A" if args.workload in TIED_WORKLOADS else "")
+                           + ("+inverse_free_refresh" if args.workload in IKFAC_WORKLOADS else ""),
                            "invert_every": cfg.invert_every},
                 "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": cores,
                                  "kind": "oracle", "sample": sample},
@@ -924,7 +948,8 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, sample, spent = oracle_steps_per_s(cfg, layers, budget_s=20.0,
                                               nchw=args.workload in NCHW_WORKLOADS,
-                                              tied=args.workload in TIED_WORKLOADS)
+                                              tied=args.workload in TIED_WORKLOADS,
+                                              ikfac=args.workload in IKFAC_WORKLOADS)
         cpu = {"value": round(v, 6), "unit": "steps/s", "cores": blas_threads(), "kind": "oracle",
                "sample": sample, "seconds": round(spent, 1)}
     if rank == 0:
