@@ -759,7 +759,6 @@ kfac_status launch_ikfac_update(kfac_ctx* h, int layer, float beta, cudaStream_t
   const InvJob* jobs = h->at<InvJob>(h->off_invjobs) + j0;
   int nmax = 0;
   for (int i = j0; i < j0 + nj; ++i) nmax = std::max(nmax, h->invjobs_host[i].n);
-  auto check = [](kfac_status e) { return e; };
   launch_pdl(ik_damped_split_kernel, dim3(elem_blocks(nmax), nj), dim3(256), 0, st, jobs,
              (float)std::sqrt(h->hp.damping));
   count_launch();
@@ -798,8 +797,8 @@ kfac_status launch_ikfac_update(kfac_ctx* h, int layer, float beta, cudaStream_t
   std::vector<TcProblem> pr;
   for (int which = 0; which < 3; ++which) {
     products(which, &pr);
-    if (kfac_status e = check(launch_gemm_tc_grouped(h, false, TC_EPI_SPLIT, pr.data(),
-                                                     (int)pr.size(), st)))
+    if (kfac_status e = launch_gemm_tc_grouped(h, false, TC_EPI_SPLIT, pr.data(),
+                                               (int)pr.size(), st))
       return e;
     if (which == 1) {   // S1 = (K^T F_d K)^T -> M^T = (1 + beta/2) I - (beta/2) S1
       launch_pdl(ik_affine_kernel, dim3(elem_blocks(nmax), nj), dim3(256), 0, st, jobs,
