@@ -1,0 +1,79 @@
+"""CPU checks of the host-side logic around the step: workload shapes, the
+benchmark's work accounting and schedule helpers.  No GPU and no library call."""
+import math
+
+import numpy as np
+import pytest
+
+import bench
+import oracle as O
+import workloads as W
+
+
+@pytest.mark.parametrize("name", ["c3", "c4", "c4bf16"])
+def test_conv_geometry_matches_layer_shapes(name):
+    """Every convolution's geometry gives its layer's d_in and row count, and the
+    oracle's patch matrix has that shape."""
+    cfg = W.get_config(name)
+    convs = [l for l in cfg.layers if l.conv is not None]
+    assert convs
+    for l in convs:
+        c = l.conv
+        assert c.c_in * c.kh * c.kw == l.d_in
+        assert c.batch * c.h_out * c.w_out == l.rows
+        assert c.h_out == O.conv_out_size(c.h, c.kh, c.sh, c.ph, c.dh)
+        assert c.w_out == O.conv_out_size(c.w, c.kw, c.sw, c.pw, c.dw)
+    # a small batch of the first convolution, through the oracle's im2col
+    li = cfg.layers.index(convs[0])
+    d = W.conv_inputs(cfg, li, 1, batch=1)
+    c = d["geom"]
+    P = O.im2col(d["x"], (c.kh, c.kw), (c.sh, c.sw), (c.ph, c.pw), (c.dh, c.dw))
+    assert P.shape == (c.h_out * c.w_out, convs[0].d_in)
+
+
+def test_conv_draws_are_seeded_and_distinct():
+    cfg = W.get_config("c3")
+    a = W.conv_inputs(cfg, 2, 1, batch=1)["x"]
+    b = W.conv_inputs(cfg, 2, 1, batch=1)["x"]
+    c = W.conv_inputs(cfg, 2, 2, batch=1)["x"]
+    assert np.array_equal(a, b) and not np.array_equal(a, c)
+    assert (a >= 0).all()                         # post-ReLU activations
+
+
+def test_qkv_ties_map_key_and_value_to_query():
+    cfg, layers = bench.bench_config("transformer4_qkv_tied")
+    ties = bench.qkv_ties(layers)
+    assert len(ties) == 8                          # k and v of 4 blocks
+    for li, src in ties.items():
+        blk, _, proj = layers[li].name.rpartition(".")
+        assert proj in ("k", "v") and layers[src].name == f"{blk}.q"
+        assert layers[li].n == layers[src].n and layers[li].kind == layers[src].kind == "kron"
+
+
+def test_work_accounting_of_the_variants():
+    """Shared A factors drop their products and inverses; an inverse-free refresh
+    counts 7 n^3 per factor; NCHW inputs read the tensors, not the patches."""
+    cfg, layers = bench.bench_config("transformer4_qkv_tied")
+    ties = set(bench.qkv_ties(layers))
+    base = bench.algorithmic(layers, 10)
+    tied = bench.algorithmic(layers, 10, tied=ties)
+    drop = sum(l.rows * l.n * (l.n + 1) for i, l in enumerate(layers) if i in ties)
+    assert math.isclose(base["factor_flop"] - tied["factor_flop"], drop, rel_tol=1e-12)
+    cfg2, layers2 = bench.bench_config("mlp4")
+    a = bench.algorithmic(layers2, 10)
+    b = bench.algorithmic(layers2, 10, ikfac=True)
+    assert math.isclose(b["invert_flop"], 7 * a["invert_flop"], rel_tol=1e-12)
+    cfg3, layers3 = bench.bench_config("resnet18_nchw")
+    u = bench.algorithmic(layers3, 20)
+    v = bench.algorithmic(layers3, 20, nchw=True)
+    assert v["factor_bytes"] < u["factor_bytes"]
+    assert v["factor_flop"] == u["factor_flop"]
+
+
+def test_stale_schedule_matches_bench_refresh_cadence():
+    """With no warm-up and equal cadences the stale schedule is the plain one
+    (refresh at t = 1, 1 + k, ...) shifted to start after the warm-up step."""
+    k = 10
+    flags = [O.stale_refresh(t, 1, k, k) for t in range(1, 42)]
+    plain = [(t - 1) % k == 0 for t in range(1, 42)]
+    assert [f[0] for f in flags] == plain and [f[1] for f in flags] == plain
