@@ -39,9 +39,10 @@
  *     the diagonal path (kfac_diag_factors*, kfac_diag_step*) use disjoint
  *     scratch and may overlap each other on different streams, as long as
  *     each touches different state (a layer's factors are read only by
- *     kfac_invert; preconditioning reads the inverses).  kfac_invert must not
- *     overlap any other call on the handle: it reads the factors and writes
- *     the inverses and shares the factor update's scratch.
+ *     kfac_invert; preconditioning reads the inverses).  kfac_invert and
+ *     kfac_ikfac_update must not overlap any other call on the handle: they
+ *     read the factors, write the inverses, and share the factor update's
+ *     and the preconditioning's scratch.
  */
 #ifndef KFAC_H
 #define KFAC_H
