@@ -29,7 +29,8 @@ Sources (page title, section):
     weight decay, and writes the parameter in place.
 
 Where the pages leave a step open, this module takes the reading below (each
-one is also listed in the repository's design notes):
+one is also listed, under the same number, in the repository's design notes;
+R9 to R17 there concern inputs and tolerances, not this module's arithmetic):
   R1  EMA starts from zero (F_0 = 0); ``ema_init="first"`` gives F_1 = F_new.
   R2  "decay xi" means the old value keeps weight xi: F <- xi F + (1-xi) F_new.
   R3  factor scale s = 1/M, M = number of rows (batch, or B*H*W for conv).
@@ -40,14 +41,14 @@ one is also listed in the repository's design notes):
   R7  diagonal step: P_ij = dW_ij / (g_i a_j + gamma), g and a the EMA diagonals.
   R8  a layer with a bias carries it as the last column of W-hat = [W | b] and
       its activations get a ones column: a-hat = [a | 1].
-  R9  a convolution's activation rows are its zero-padded input patches, one
+  R18 a convolution's activation rows are its zero-padded input patches, one
       per (image, output position), columns in weight order (c, i, j); its
       output-gradient rows are the channels at the same positions.
-  R10 stale factors: a step recomputes and re-inverts every factor during a
+  R19 stale factors: a step recomputes and re-inverts every factor during a
       warm-up of w steps, afterwards A every k_A and G every k_G steps counted
       from the end of the warm-up; a factor skipped on a step keeps both its
       running value and its inverse.
-  R11 inverse-free update: K (K K^T in place of (F + sqrt(gamma) I)^{-1}) is
+  R20 inverse-free update: K (K K^T in place of (F + sqrt(gamma) I)^{-1}) is
       seeded from the Cholesky refresh (K = L^{-T}) and stepped by
       K <- K (I - (beta/2)(K^T (F + sqrt(gamma) I) K - I)), beta in (0, 2);
       the preconditioner uses K K^T.  The page states only that the update is
@@ -218,7 +219,7 @@ def damped_inverse(F, damping: float) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # inverse-free factor update ("Structured Inverse-Free Natural Gradient" page,
 # abstract: an inverse-free K-FAC update by subtraction in the matrix-logarithm
-# space instead of an inversion; reading R11 below)
+# space instead of an inversion; reading R20 below)
 
 def ikfac_init(F, damping: float) -> np.ndarray:
     """K = L^{-T} for F + sqrt(gamma) I = L L^T, so that K K^T = (F + sqrt(gamma) I)^{-1}
@@ -291,7 +292,7 @@ def diag_precondition(gw_hat, gs, as_, damping: float) -> np.ndarray:
 # stale-factor schedule (Osawa et al. §5.4)
 
 def stale_refresh(t: int, warmup: int, every_a: int, every_g: int):
-    """Which factors a step t (1-based) recomputes and re-inverts (reading R10).
+    """Which factors a step t (1-based) recomputes and re-inverts (reading R19).
 
     Every step during the first ``warmup`` steps, while the Fisher changes
     fast; after that A every ``every_a`` steps and G every ``every_g`` steps

@@ -1,6 +1,6 @@
 """The inverse-free refresh on the GPU against the float64 oracle.
 
-Reading R11 (the "Structured Inverse-Free Natural Gradient" page gives only the
+Reading R20 (the "Structured Inverse-Free Natural Gradient" page gives only the
 idea: an inverse-free K-FAC update by subtraction in the matrix-logarithm
 space): K, with K K^T standing for (F + sqrt(gamma) I)^{-1}, is seeded by the
 Cholesky refresh (K = L^{-T}) and stepped by K <- K (I - (beta/2)(K^T F_d K - I)).
