@@ -624,7 +624,7 @@ def run_gpu(args, rank, world, peaks, peak_kind):
               "factor_tflops": round(factor_tfs, 3), "precond_tflops": round(precond_tfs, 3),
               "diag_gbs": round(diag_gbs, 1),
               "timed": (f"phases in order on one stream, {seq_steps} steps (the headline "
-                        "overlaps the factor update with the rest on steps without a refresh)"
+                        "runs them on three streams, see config.phase_overlap)"
                         if overlap else "the timed steps")}
     # dominant phase -> roofline
     names = ["factor", "invert", "precond", "diag"]
