@@ -283,6 +283,18 @@ def diag_factor(x, has_bias: int = 0, scale: Optional[float] = None) -> np.ndarr
     return s * np.sum(xh * xh, axis=0)
 
 
+def conv_diag_factors(x, gy, kernel, stride=(1, 1), pad=(0, 0), dilation=(1, 1),
+                      has_bias: int = 1, scale: Optional[float] = None):
+    """New diagonal factors of a 2-D convolution (reading R18): the diagonals of
+    conv_factors, s * column sums of squares of the input patches (bias entry
+    s*M) and of the output-gradient rows."""
+    P = im2col(x, kernel, stride, pad, dilation)
+    R = output_rows(gy)
+    if P.shape[0] != R.shape[0]:
+        raise ValueError("input patches and output gradient rows differ")
+    return diag_factor(R, 0, scale), diag_factor(P, has_bias, scale)
+
+
 def diag_precondition(gw_hat, gs, as_, damping: float) -> np.ndarray:
     """P_ij = dW_ij / (g_i a_j + gamma)  (reading R7)."""
     return _f64(gw_hat) / (np.outer(_f64(gs), _f64(as_)) + damping)

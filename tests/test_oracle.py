@@ -504,3 +504,33 @@ def test_ikfac_iteration_converges_to_the_lapack_inverse(beta):
         K = O.ikfac_update(K, F2, 1e-2, beta)
     np.testing.assert_allclose(O.ikfac_inverse(K), np.linalg.inv(F2 + 0.1 * np.eye(8)),
                                rtol=1e-9, atol=1e-9)
+
+
+@pytest.mark.parametrize("geom", CONV_GEOMS)
+def test_conv_diag_factors_are_the_diagonals_of_the_conv_factors(geom):
+    """Column sums of squares equal the diagonals of the full factors (a second
+    route: the matrix product and its diagonal)."""
+    B, C, H, Wd, kh, kw, sh, sw, ph, pw, dh, dw = geom
+    x = RNG.standard_normal((B, C, H, Wd))
+    Ho = O.conv_out_size(H, kh, sh, ph, dh)
+    Wo = O.conv_out_size(Wd, kw, sw, pw, dw)
+    gy = RNG.standard_normal((B, 5, Ho, Wo))
+    gn, an = O.conv_diag_factors(x, gy, (kh, kw), (sh, sw), (ph, pw), (dh, dw), 1)
+    A, G = O.conv_factors(x, gy, (kh, kw), (sh, sw), (ph, pw), (dh, dw), 1)
+    np.testing.assert_allclose(an, np.diag(A), rtol=1e-13)
+    np.testing.assert_allclose(gn, np.diag(G), rtol=1e-13)
+    assert an[-1] == pytest.approx(1.0)                # s * M for the ones column
+
+
+def test_conv_diag_factors_of_constant_image_closed_form():
+    """All-ones image, 3x3 kernel, pad 1, stride 1: tap (i, j) sees the image at
+    (H - |i-1|)(W - |j-1|) of the H*W positions."""
+    H, Wd = 5, 7
+    x = np.ones((2, 3, H, Wd))
+    gy = np.zeros((2, 4, H, Wd))
+    _, an = O.conv_diag_factors(x, gy, (3, 3), (1, 1), (1, 1), (1, 1), 1)
+    for c in range(3):
+        for i in range(3):
+            for j in range(3):
+                want = (H - abs(i - 1)) * (Wd - abs(j - 1)) / (H * Wd)
+                assert an[(c * 3 + i) * 3 + j] == pytest.approx(want, rel=1e-15)
