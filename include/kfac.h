@@ -206,6 +206,19 @@ kfac_status kfac_diag_factors(kfac_handle h, int layer, const void* a, int64_t l
                               const void* g, int64_t ldg, int64_t rows, double scale,
                               float* g_new, float* a_new, cudaStream_t stream);
 
+/* K5 for a 2-D convolution layer (any kind) from its NCHW tensors, without an
+ * unfolded input: g_new[i] = s sum over (image, position) of gy[b,i,oh,ow]^2
+ * (d_out entries); a_new[(c kh + i) kw + j] = s sum of the squares of the input
+ * patch column (c, i, j) as in kfac_update_factors_conv2d, and a_new[d_in] =
+ * s M when has_bias (n entries); s = scale, or 1/M for scale <= 0, with
+ * M = batch out_h out_w.  x, gy, geom and their checks as in
+ * kfac_update_factors_conv2d (both tensors required); kernels up to 7 x 7
+ * (else KFAC_ERR_UNSUPPORTED).  CAFIN Introduction (the diagonal factors of
+ * every layer, convolutions included); Osawa et al. §5.1. */
+kfac_status kfac_diag_factors_conv2d(kfac_handle h, int layer, const void* x, const void* gy,
+                                     const kfac_conv2d_geom* geom, double scale,
+                                     float* g_new, float* a_new, cudaStream_t stream);
+
 /* K5 for several layers in one launch: the same result as calling
  * kfac_diag_factors(layers[i], a[i], lda[i], g[i], ldg[i], rows[i], scale,
  * g_new[i], a_new[i]) for each i, up to the order of the floating-point sums

@@ -164,6 +164,14 @@ class Kfac:
                                      rows, float(scale), _ptr(g_new), _ptr(a_new),
                                      _stream(stream)), "kfac_diag_factors")
 
+    def diag_factors_conv2d(self, layer: int, x, gy, g_new, a_new, kernel, stride=1, padding=0,
+                            dilation=1, scale: float = 0.0, stream=None):
+        """kfac_diag_factors_conv2d: x [B, C, H, W] and gy [B, o, Ho, Wo], both contiguous."""
+        geom = conv2d_geom(x.shape, kernel, stride, padding, dilation)
+        _check(LIB.kfac_diag_factors_conv2d(self._h, layer, _ptr(x), _ptr(gy), ctypes.byref(geom),
+                                            float(scale), _ptr(g_new), _ptr(a_new),
+                                            _stream(stream)), "kfac_diag_factors_conv2d")
+
     def diag_factors_batched(self, layers, a_list, g_list, g_new, a_new, scale: float = 0.0,
                              stream=None):
         """kfac_diag_factors_batched over parallel lists of layers, inputs and output vectors."""

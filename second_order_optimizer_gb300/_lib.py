@@ -65,6 +65,7 @@ SIGNATURES = [
     ("kfac_update_factors_conv2d", _i, [_vp, _i, _vp, _vp, _pCG, _d, _vp]),
     ("kfac_update_factors_conv2d_batched", _i, [_vp, _i, _vp, _vp, _vp, _pCG, _d, _vp]),
     ("kfac_diag_factors", _i, [_vp, _i, _vp, _i64, _vp, _i64, _i64, _d, _vp, _vp, _vp]),
+    ("kfac_diag_factors_conv2d", _i, [_vp, _i, _vp, _vp, _pCG, _d, _vp, _vp, _vp]),
     ("kfac_diag_factors_batched", _i, [_vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _d, _vp, _vp,
                                        _vp]),
     ("kfac_invert", _i, [_vp, _i, _vp]),

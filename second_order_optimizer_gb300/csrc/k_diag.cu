@@ -485,6 +485,166 @@ kfac_status launch_diag_step_batched(kfac_ctx* h, int count, const int* layers,
   return flush();
 }
 
+namespace {
+
+// K5 for a 2-D convolution, from its NCHW tensors ------------------------------
+// A CTA takes one unit -- an input channel ci (its kh x kw patch columns) or an
+// output channel (its G column) -- over one range of images.  Every input element
+// x[b][ci][y][xx]^2 is added to each kernel tap (i, j) whose window reaches it:
+// y = oh*sh - ph + i*dh for some 0 <= oh < Ho, and the same along xx.  Partials go
+// to [split][column]; the last CTA of the launch (one ticket) adds them in split
+// order and writes both vectors.
+struct DiagConvParams {
+  const void* x;
+  const void* gy;
+  ConvSrc cs;
+  int o, has_bias, imgs_per_split;
+  int64_t rows;
+  float s;
+  float* part;     // [splits][C kh kw + o]
+  int* ticket;
+  float* g_new;
+  float* a_new;
+};
+
+template <typename T, int KM>
+__global__ void __launch_bounds__(kK5Threads) diag_conv_kernel(const __grid_constant__ DiagConvParams p) {
+  pdl_wait();
+  pdl_trigger();
+  const ConvSrc g = p.cs;
+  const int u = blockIdx.x, sp = blockIdx.y, tid = threadIdx.x;
+  const int khw = g.kh * g.kw, na = g.C * khw, ncols = na + p.o;
+  const int b0 = sp * p.imgs_per_split, b1 = min(g.B, b0 + p.imgs_per_split);
+  float acc[KM][KM];
+#pragma unroll
+  for (int i = 0; i < KM; ++i)
+#pragma unroll
+    for (int j = 0; j < KM; ++j) acc[i][j] = 0.f;
+  if (u < g.C) {
+    const T* x = static_cast<const T*>(p.x);
+    const int64_t hw = (int64_t)g.H * g.W;
+    for (int64_t e = (int64_t)b0 * hw + tid; e < (int64_t)b1 * hw; e += kK5Threads) {
+      const int64_t b = e / hw;
+      const int rem = (int)(e - b * hw), y = rem / g.W, xx = rem - y * g.W;
+      const float v = to_f32<T>(x[(b * g.C + u) * hw + rem]);
+      const float v2 = v * v;
+      bool vy[KM], vx[KM];
+#pragma unroll
+      for (int i = 0; i < KM; ++i) {
+        const int ty = y + g.ph - i * g.dh;
+        vy[i] = i < g.kh && ty >= 0 && ty % g.sh == 0 && ty / g.sh < g.Ho;
+      }
+#pragma unroll
+      for (int j = 0; j < KM; ++j) {
+        const int tx = xx + g.pw - j * g.dw;
+        vx[j] = j < g.kw && tx >= 0 && tx % g.sw == 0 && tx / g.sw < g.Wo;
+      }
+#pragma unroll
+      for (int i = 0; i < KM; ++i)
+#pragma unroll
+        for (int j = 0; j < KM; ++j)
+          if (vy[i] && vx[j]) acc[i][j] += v2;
+    }
+  } else {
+    const T* gy = static_cast<const T*>(p.gy);
+    const int oc = u - g.C;
+    const int64_t hwo = (int64_t)g.Ho * g.Wo;
+    for (int64_t e = (int64_t)b0 * hwo + tid; e < (int64_t)b1 * hwo; e += kK5Threads) {
+      const int64_t b = e / hwo;
+      const float v = to_f32<T>(gy[(b * p.o + oc) * hwo + (e - b * hwo)]);
+      acc[0][0] += v * v;
+    }
+  }
+  // block sums of the taps: warp shuffles, then the warps in order
+  __shared__ float red[kK5Threads / 32][KM * KM];
+  __shared__ int s_last;
+#pragma unroll
+  for (int i = 0; i < KM; ++i)
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      float v = acc[i][j];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if ((tid & 31) == 0) red[tid >> 5][i * KM + j] = v;
+    }
+  __syncthreads();
+  const int cnt = u < g.C ? khw : 1;
+  if (tid < cnt) {
+    const int i = u < g.C ? tid / g.kw : 0, j = u < g.C ? tid - (tid / g.kw) * g.kw : 0;
+    float v = 0.f;
+    for (int w = 0; w < kK5Threads / 32; ++w) v += red[w][i * KM + j];
+    const int col = u < g.C ? u * khw + tid : na + (u - g.C);
+    p.part[(size_t)sp * ncols + col] = v;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(p.ticket, 1) == (int)(gridDim.x * gridDim.y) - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int c = tid; c < ncols; c += kK5Threads) {
+    float v = 0.f;
+    for (int q = 0; q < (int)gridDim.y; ++q) v += __ldcg(p.part + (size_t)q * ncols + c);
+    v *= p.s;
+    if (c < na) p.a_new[c] = v;
+    else p.g_new[c - na] = v;
+  }
+  if (tid == 0) {
+    if (p.has_bias) p.a_new[na] = p.s * (float)p.rows;
+    *p.ticket = 0;
+  }
+}
+
+template <typename T>
+void launch_diag_conv_t(const DiagConvParams& p, int km, dim3 grid, cudaStream_t st) {
+  if (km == 1)
+    launch_pdl(diag_conv_kernel<T, 1>, grid, dim3(kK5Threads), 0, st, p);
+  else if (km == 3)
+    launch_pdl(diag_conv_kernel<T, 3>, grid, dim3(kK5Threads), 0, st, p);
+  else
+    launch_pdl(diag_conv_kernel<T, 7>, grid, dim3(kK5Threads), 0, st, p);
+}
+
+}  // namespace
+
+kfac_status launch_diag_factors_conv(kfac_ctx* h, int layer, const void* x, const void* gy,
+                                     const kfac_conv2d_geom& cg, double scale, float* g_new,
+                                     float* a_new, cudaStream_t st) {
+  const LayerInfo& L = h->layers[layer];
+  DiagConvParams p{};
+  const int ho = conv_out(cg.in_h, cg.kernel_h, cg.stride_h, cg.pad_h, cg.dilation_h);
+  const int wo = conv_out(cg.in_w, cg.kernel_w, cg.stride_w, cg.pad_w, cg.dilation_w);
+  p.cs = ConvSrc{cg.batch, cg.in_channels, cg.in_h, cg.in_w, cg.kernel_h, cg.kernel_w,
+                 cg.stride_h, cg.stride_w, cg.pad_h, cg.pad_w, cg.dilation_h, cg.dilation_w,
+                 ho, wo};
+  p.x = x;
+  p.gy = gy;
+  p.o = L.o;
+  p.has_bias = L.has_bias;
+  p.rows = (int64_t)cg.batch * ho * wo;
+  p.s = (float)(scale > 0 ? scale : 1.0 / (double)p.rows);
+  p.g_new = g_new;
+  p.a_new = a_new;
+  const int units = cg.in_channels + L.o;
+  const int64_t ncols = (int64_t)L.d_in + L.o;
+  int64_t splits = std::min<int64_t>(cg.batch, std::max<int64_t>(1, cdiv(2 * kNumSMs, units)));
+  splits = std::max<int64_t>(1, std::min<int64_t>(splits, (int64_t)(h->k5part_floats / ncols)));
+  p.imgs_per_split = (int)cdiv(cg.batch, splits);
+  splits = cdiv(cg.batch, p.imgs_per_split);
+  if (splits * ncols > (int64_t)h->k5part_floats) return KFAC_ERR_WORKSPACE;
+  p.part = h->at<float>(h->off_k5part);
+  p.ticket = h->at<int>(h->off_k5tickets);
+  const int km = std::max(cg.kernel_h, cg.kernel_w) == 1 ? 1
+                 : std::max(cg.kernel_h, cg.kernel_w) <= 3 ? 3 : 7;
+  const dim3 grid((unsigned)units, (unsigned)splits);
+  if (L.in_dtype == KFAC_BF16)
+    launch_diag_conv_t<__nv_bfloat16>(p, km, grid, st);
+  else
+    launch_diag_conv_t<float>(p, km, grid, st);
+  count_launch();
+  return check_launch();
+}
+
 }  // namespace kfac
 
 // ---------------------------------------------------------------------------

@@ -484,6 +484,20 @@ kfac_status kfac_diag_factors(kfac_handle h, int layer, const void* a, int64_t l
   return launch_diag_factors(h, layer, a, lda, g, ldg, rows, scale, g_new, a_new, stream);
 }
 
+kfac_status kfac_diag_factors_conv2d(kfac_handle h, int layer, const void* x, const void* gy,
+                                     const kfac_conv2d_geom* geom, double scale,
+                                     float* g_new, float* a_new, cudaStream_t stream) {
+  if (kfac_status e = check_layer(h, layer, -1)) return e;
+  const LayerInfo& L = h->layers[layer];
+  if (!geom || !x || !gy || !std::isfinite(scale)) return KFAC_ERR_INVALID_ARG;
+  if (!g_new || !a_new || !aligned(g_new, 4) || !aligned(a_new, 4)) return KFAC_ERR_INVALID_ARG;
+  int64_t rows = 0;
+  if (kfac_status e = check_conv(h, L, x, gy, *geom, &rows)) return e;
+  if (geom->kernel_h > 7 || geom->kernel_w > 7) return KFAC_ERR_UNSUPPORTED;
+  if (kfac_status e = ensure_device(h)) return e;
+  return launch_diag_factors_conv(h, layer, x, gy, *geom, scale, g_new, a_new, stream);
+}
+
 kfac_status kfac_diag_factors_batched(kfac_handle h, int count, const int* layers,
                                       const void* const* a, const int64_t* lda,
                                       const void* const* g, const int64_t* ldg,

@@ -154,6 +154,9 @@ kfac_status launch_update_factors(kfac_ctx* h, int layer, const void* a, int64_t
 kfac_status launch_diag_factors(kfac_ctx* h, int layer, const void* a, int64_t lda,
                                 const void* g, int64_t ldg, int64_t rows, double scale,
                                 float* g_new, float* a_new, cudaStream_t s);
+kfac_status launch_diag_factors_conv(kfac_ctx* h, int layer, const void* x, const void* gy,
+                                     const kfac_conv2d_geom& geom, double scale, float* g_new,
+                                     float* a_new, cudaStream_t s);
 kfac_status launch_diag_step(kfac_ctx* h, int layer, float decay, const float* g_new,
                              const float* a_new, const float* gw, const float* gb, float* pw,
                              float* pb, float* ow, float* ob, cudaStream_t s);

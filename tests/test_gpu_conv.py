@@ -6,6 +6,8 @@ oracle is fed the same rounded values), as for row-major inputs.  The gathered
 path runs the same products as kfac_update_factors_batched on the unfolded
 matrices, so the two must agree bit for bit.
 """
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -170,4 +172,60 @@ def test_conv_full_size_layers_match_oracle(cfg_name, li, dtype):
                             (cg.dh, cg.dw), 1)
     assert rel_fro(to_np(h.state(0, K.KFAC_STATE_A)), 0.05 * An) <= 1e-5
     assert rel_fro(to_np(h.state(0, K.KFAC_STATE_G)), 0.05 * Gn) <= 1e-5
+    assert h.get_status()[0] == 0
+
+
+@pytest.mark.parametrize("geom", GEOMS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_conv_diag_factors_match_oracle(geom, dtype):
+    """K5 from NCHW tensors: the diagonals of the convolution factors (elementwise
+    1e-5, as for row-major inputs)."""
+    from gpu_helpers import max_rel_elem
+    B, C, H, Wd, o, kh, kw, sh, sw, ph, pw, dh, dw, bias = geom
+    M = B * O.conv_out_size(H, kh, sh, ph, dh) * O.conv_out_size(Wd, kw, sw, pw, dw)
+    layer = _layer(geom, dtype)
+    h = K.Kfac([(K.KFAC_DIAG,) + tuple(layer[1:])], max_rows=M, **HP)
+    x, gy = _draw(B, C, H, Wd, o, kh, kw, sh, sw, ph, pw, dh, dw, dtype)
+    gn = torch.empty(o, device="cuda")
+    an = torch.empty(C * kh * kw + bias, device="cuda")
+    for _ in range(2):   # twice: the ticket and partials are left ready for reuse
+        h.diag_factors_conv2d(0, _dev(x, dtype), _dev(gy, dtype), gn, an, (kh, kw), (sh, sw),
+                              (ph, pw), (dh, dw))
+    g_ref, a_ref = O.conv_diag_factors(x, gy, (kh, kw), (sh, sw), (ph, pw), (dh, dw), bias)
+    assert max_rel_elem(to_np(an), a_ref) <= 1e-5, max_rel_elem(to_np(an), a_ref)
+    assert max_rel_elem(to_np(gn), g_ref) <= 1e-5, max_rel_elem(to_np(gn), g_ref)
+    assert h.get_status()[0] == 0
+
+
+def test_conv_diag_factors_full_size_stage1_layer():
+    """A ResNet-18 stage-1 3x3 convolution (batch 128, 64 channels, 32 x 32) on the
+    diagonal path, at full size."""
+    from gpu_helpers import max_rel_elem
+    cfg = W.get_config("c3")
+    L = cfg.layers[2]
+    cg = L.conv
+    d = W.conv_inputs(cfg, 2, 1)
+    h = K.Kfac([(K.KFAC_DIAG, L.d_out, L.d_in, 1, K.KFAC_F32)], max_rows=L.rows, **HP)
+    gn = torch.empty(L.d_out, device="cuda")
+    an = torch.empty(L.n, device="cuda")
+    h.diag_factors_conv2d(0, to_dev(d["x"]), to_dev(d["gy"]), gn, an, (cg.kh, cg.kw),
+                          (cg.sh, cg.sw), (cg.ph, cg.pw), (cg.dh, cg.dw))
+    g_ref, a_ref = O.conv_diag_factors(d["x"], d["gy"], (cg.kh, cg.kw), (cg.sh, cg.sw),
+                                       (cg.ph, cg.pw), (cg.dh, cg.dw), 1)
+    assert max_rel_elem(to_np(an), a_ref) <= 1e-5
+    assert max_rel_elem(to_np(gn), g_ref) <= 1e-5
+    assert h.get_status()[0] == 0
+
+
+def test_conv_diag_factors_rejects_large_kernels_and_bad_arguments():
+    h = K.Kfac([(K.KFAC_DIAG, 4, 3 * 81, 1, K.KFAC_F32), (K.KFAC_DIAG, 4, 27, 1, K.KFAC_F32)],
+               max_rows=2 * 100, **HP)
+    x = torch.zeros(2, 3, 10, 10, device="cuda")
+    gn, an = torch.empty(4, device="cuda"), torch.empty(3 * 81 + 1, device="cuda")
+    with pytest.raises(K.KfacError) as e:                 # 9 x 9 kernel
+        h.diag_factors_conv2d(0, x, torch.zeros(2, 4, 10, 10, device="cuda"), gn, an, 9, 1, 4)
+    assert e.value.code == 7
+    geom = K.conv2d_geom(x.shape, 3, 1, 1)                # no output gradient
+    assert K.LIB.kfac_diag_factors_conv2d(h._h, 1, x.data_ptr(), None, ctypes.byref(geom), 0.0,
+                                          gn.data_ptr(), an.data_ptr(), None) == 1
     assert h.get_status()[0] == 0
