@@ -14,6 +14,7 @@ steps outside the per-step CUDA events.  Rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -33,10 +34,14 @@ METRIC = "K-FAC precond steps/s; factor-GEMM TFLOP/s & diag-step GB/s vs GB300 p
 WORKLOADS = {"mlp4": "c2", "single_linear": "c1", "resnet18": "c3", "resnet50": "c4",
              "resnet50_bf16": "c4bf16", "transformer4": "c5",
              "resnet18_nchw": "c3", "resnet50_nchw": "c4", "resnet50_bf16_nchw": "c4bf16",
-             "transformer4_qkv_tied": "c5", "mlp4_ikfac": "c2"}
+             "transformer4_qkv_tied": "c5", "mlp4_ikfac": "c2",
+             "resnet18_diag_nchw": "c3"}
 # workloads whose convolutions hand the library their NCHW input and output
 # gradient (kfac_update_factors_conv2d_batched) instead of unfolded matrices
-NCHW_WORKLOADS = {"resnet18_nchw", "resnet50_nchw", "resnet50_bf16_nchw"}
+NCHW_WORKLOADS = {"resnet18_nchw", "resnet50_nchw", "resnet50_bf16_nchw", "resnet18_diag_nchw"}
+# workloads that put every layer on the diagonal path (AdaFisher-style, as the
+# CAFIN page trains ResNet-18), convolutions fed as NCHW tensors
+DIAG_WORKLOADS = {"resnet18_diag_nchw"}
 # workloads whose key and value projections share the query projection's A
 # factor (kfac_tie_a_factor: the three read the same input)
 TIED_WORKLOADS = {"transformer4_qkv_tied"}
@@ -126,6 +131,9 @@ def load_peaks():
 def bench_config(workload):
     cfg = Wl.get_config(WORKLOADS[workload])
     layers = list(cfg.layers)
+    if workload in DIAG_WORKLOADS:
+        import dataclasses
+        return cfg, [dataclasses.replace(l, kind="diag") for l in layers]
     if not cfg.diag_layers:
         import dataclasses
         layers += [dataclasses.replace(l, name=l.name + "_diag", kind="diag") for l in cfg.layers]
@@ -179,7 +187,10 @@ def algorithmic(layers, k, nchw=False, tied=(), ikfac=False):
             f["precond_bytes"] += 4 * (n * n + o * o + 2 * o * n) + 4 * 3 * o * n
         else:
             f["diag_bytes"] += 20 * o * n + 8 * (o + n)
-            if l.act != "bn":
+            if nchw and l.conv is not None:
+                c = l.conv
+                f["diagfac_bytes"] += (c.batch * c.c_in * c.h * c.w + M * o) * elt
+            elif l.act != "bn":
                 f["diagfac_bytes"] += M * (l.d_in + o) * elt
     return f
 
@@ -320,7 +331,15 @@ def oracle_steps_per_s(cfg, layers, budget_s=20.0, min_s=10.0, nchw=False, tied=
                           np.zeros(l.d_out) if l.has_bias else None)
         gw = np.zeros((l.d_out, l.d_in))
         gn, an = np.ones(l.d_out), np.ones(l.n)
+        li = cfg.layers.index(dataclasses.replace(l, kind="kron")) if l.conv is not None else -1
         ts = time.perf_counter()
+        if nchw and l.conv is not None:     # the new diagonal factors from the NCHW tensors
+            if l.name not in inputs:
+                inputs[l.name] = Wl.conv_inputs(cfg, li, 1)
+            c = inputs[l.name]["geom"]
+            ts = time.perf_counter()
+            gn, an = O.conv_diag_factors(inputs[l.name]["x"], inputs[l.name]["gy"], (c.kh, c.kw),
+                                         (c.sh, c.sw), (c.ph, c.pw), (c.dh, c.dw), l.has_bias)
         orc.step_diag(st, gn, an, gw, np.zeros(l.d_out) if l.has_bias else None)
         return time.perf_counter() - ts
 
@@ -381,7 +400,7 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     NB = 2
     data = []
     nchw = args.workload in NCHW_WORKLOADS
-    is_conv = lambda l: nchw and l.kind == "kron" and l.conv is not None
+    is_conv = lambda l: nchw and l.conv is not None
     for b in range(NB):
         per = []
         for li, l in enumerate(layers):
@@ -456,14 +475,21 @@ def run_gpu(args, rank, world, peaks, peak_kind):
 
     diag_idx = [li for li, l in enumerate(layers) if l.kind == "diag"]
     k5_groups = {}   # layers whose diagonal factors come from a and g, by input dtype
+    conv_diag = []   # convolutions on the diagonal path, fed as NCHW tensors
     for li in diag_idx:
-        if layers[li].act != "bn":
+        if is_conv(layers[li]):
+            conv_diag.append(li)
+        elif layers[li].act != "bn":
             k5_groups.setdefault(layers[li].in_dtype, []).append(li)
 
     def phase_diag(x):
         for grp in k5_groups.values():
             h.diag_factors_batched(grp, [x[li]["a"] for li in grp], [x[li]["g"] for li in grp],
                                    [gnew[li] for li in grp], [anew[li] for li in grp])
+        for li in conv_diag:
+            c = layers[li].conv
+            h.diag_factors_conv2d(li, x[li]["x"], x[li]["gy"], gnew[li], anew[li], (c.kh, c.kw),
+                                  (c.sh, c.sw), (c.ph, c.pw), (c.dh, c.dw))
         if diag_idx:
             bn = lambda li: layers[li].act == "bn"
             h.diag_step_batched(
@@ -674,6 +700,7 @@ def run_gpu(args, rank, world, peaks, peak_kind):
         "gpu_launches": int(launches), "wall_s": wall, "e2e": e2e,
         "config": {"workload": cfg.name + ("+diag_twins" if not cfg.diag_layers else "")
                    + ("+nchw_conv_inputs" if nchw else "")
+                   + ("+all_layers_diagonal" if args.workload in DIAG_WORKLOADS else "")
                    + ("+qkv_shared_A" if ties else "")
                    + ("+inverse_free_refresh" if ikfac else ""),
                    "kron_layers": sum(l.kind == "kron" for l in layers),
@@ -931,6 +958,7 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": cfg.name + ("+diag_twins" if not cfg.diag_layers else "")
                            + ("+nchw_conv_inputs" if args.workload in NCHW_WORKLOADS else "")
+                           + ("+all_layers_diagonal" if args.workload in DIAG_WORKLOADS else "")
                            + ("+qkv_shared_A" if args.workload in TIED_WORKLOADS else "")
                            + ("+inverse_free_refresh" if args.workload in IKFAC_WORKLOADS else ""),
                            "invert_every": cfg.invert_every},
