@@ -212,8 +212,9 @@ kfac_status kfac_diag_factors(kfac_handle h, int layer, const void* a, int64_t l
  * patch column (c, i, j) as in kfac_update_factors_conv2d, and a_new[d_in] =
  * s M when has_bias (n entries); s = scale, or 1/M for scale <= 0, with
  * M = batch out_h out_w.  x, gy, geom and their checks as in
- * kfac_update_factors_conv2d (both tensors required); kernels up to 7 x 7
- * (else KFAC_ERR_UNSUPPORTED).  CAFIN Introduction (the diagonal factors of
+ * kfac_update_factors_conv2d (both tensors required); in_h * in_w at most
+ * 51200 (one channel's squares are summed in shared memory; else
+ * KFAC_ERR_UNSUPPORTED).  CAFIN Introduction (the diagonal factors of
  * every layer, convolutions included); Osawa et al. §5.1. */
 kfac_status kfac_diag_factors_conv2d(kfac_handle h, int layer, const void* x, const void* gy,
                                      const kfac_conv2d_geom* geom, double scale,

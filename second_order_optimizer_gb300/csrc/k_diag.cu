@@ -489,11 +489,13 @@ namespace {
 
 // K5 for a 2-D convolution, from its NCHW tensors ------------------------------
 // A CTA takes one unit -- an input channel ci (its kh x kw patch columns) or an
-// output channel (its G column) -- over one range of images.  Every input element
-// x[b][ci][y][xx]^2 is added to each kernel tap (i, j) whose window reaches it:
-// y = oh*sh - ph + i*dh for some 0 <= oh < Ho, and the same along xx.  Partials go
-// to [split][column]; the last CTA of the launch (one ticket) adds them in split
-// order and writes both vectors.
+// output channel (its G column) -- over one range of images.  For an input
+// channel it first sums x[b][ci][y][xx]^2 over its images into a shared image
+// S[y][xx] (one pass over the input, coalesced along xx); patch column (i, j)
+// is then the sum of S over the tap's window, y = oh*sh - ph + i*dh,
+// xx = ow*sw - pw + j*dw for the output positions (oh, ow), in bounds.
+// Partials go to [split][column]; the last CTA of the launch (one ticket) adds
+// them in split order and writes both vectors.
 struct DiagConvParams {
   const void* x;
   const void* gy;
@@ -507,74 +509,66 @@ struct DiagConvParams {
   float* a_new;
 };
 
-template <typename T, int KM>
+constexpr size_t kConvSmemMax = 200 * 1024;   // S of one channel: H W floats
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  __syncthreads();   // red may still be read by the previous call
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int w = 0; w < kK5Threads / 32; ++w) t += red[w];   // warps in order
+  return t;
+}
+
+template <typename T>
 __global__ void __launch_bounds__(kK5Threads) diag_conv_kernel(const __grid_constant__ DiagConvParams p) {
   pdl_wait();
   pdl_trigger();
+  extern __shared__ float S[];
+  __shared__ float red[kK5Threads / 32];
+  __shared__ int s_last;
   const ConvSrc g = p.cs;
   const int u = blockIdx.x, sp = blockIdx.y, tid = threadIdx.x;
   const int khw = g.kh * g.kw, na = g.C * khw, ncols = na + p.o;
   const int b0 = sp * p.imgs_per_split, b1 = min(g.B, b0 + p.imgs_per_split);
-  float acc[KM][KM];
-#pragma unroll
-  for (int i = 0; i < KM; ++i)
-#pragma unroll
-    for (int j = 0; j < KM; ++j) acc[i][j] = 0.f;
   if (u < g.C) {
     const T* x = static_cast<const T*>(p.x);
-    const int64_t hw = (int64_t)g.H * g.W;
-    for (int64_t e = (int64_t)b0 * hw + tid; e < (int64_t)b1 * hw; e += kK5Threads) {
-      const int64_t b = e / hw;
-      const int rem = (int)(e - b * hw), y = rem / g.W, xx = rem - y * g.W;
-      const float v = to_f32<T>(x[(b * g.C + u) * hw + rem]);
-      const float v2 = v * v;
-      bool vy[KM], vx[KM];
-#pragma unroll
-      for (int i = 0; i < KM; ++i) {
-        const int ty = y + g.ph - i * g.dh;
-        vy[i] = i < g.kh && ty >= 0 && ty % g.sh == 0 && ty / g.sh < g.Ho;
+    const int hw = g.H * g.W;
+    for (int q = tid; q < hw; q += kK5Threads) {
+      float acc = 0.f;
+      for (int b = b0; b < b1; ++b) {
+        const float v = to_f32<T>(x[((int64_t)b * g.C + u) * hw + q]);
+        acc = fmaf(v, v, acc);
       }
-#pragma unroll
-      for (int j = 0; j < KM; ++j) {
-        const int tx = xx + g.pw - j * g.dw;
-        vx[j] = j < g.kw && tx >= 0 && tx % g.sw == 0 && tx / g.sw < g.Wo;
+      S[q] = acc;
+    }
+    __syncthreads();
+    const int hwo = g.Ho * g.Wo;
+    for (int t = 0; t < khw; ++t) {
+      const int i = t / g.kw, j = t - i * g.kw;
+      float v = 0.f;
+      for (int q = tid; q < hwo; q += kK5Threads) {
+        const int oh = q / g.Wo, ow = q - oh * g.Wo;
+        const int y = oh * g.sh - g.ph + i * g.dh, xx = ow * g.sw - g.pw + j * g.dw;
+        if ((unsigned)y < (unsigned)g.H && (unsigned)xx < (unsigned)g.W) v += S[y * g.W + xx];
       }
-#pragma unroll
-      for (int i = 0; i < KM; ++i)
-#pragma unroll
-        for (int j = 0; j < KM; ++j)
-          if (vy[i] && vx[j]) acc[i][j] += v2;
+      v = block_sum(v, red);
+      if (tid == 0) p.part[(size_t)sp * ncols + u * khw + t] = v;
     }
   } else {
     const T* gy = static_cast<const T*>(p.gy);
     const int oc = u - g.C;
     const int64_t hwo = (int64_t)g.Ho * g.Wo;
-    for (int64_t e = (int64_t)b0 * hwo + tid; e < (int64_t)b1 * hwo; e += kK5Threads) {
-      const int64_t b = e / hwo;
-      const float v = to_f32<T>(gy[(b * p.o + oc) * hwo + (e - b * hwo)]);
-      acc[0][0] += v * v;
-    }
-  }
-  // block sums of the taps: warp shuffles, then the warps in order
-  __shared__ float red[kK5Threads / 32][KM * KM];
-  __shared__ int s_last;
-#pragma unroll
-  for (int i = 0; i < KM; ++i)
-#pragma unroll
-    for (int j = 0; j < KM; ++j) {
-      float v = acc[i][j];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if ((tid & 31) == 0) red[tid >> 5][i * KM + j] = v;
-    }
-  __syncthreads();
-  const int cnt = u < g.C ? khw : 1;
-  if (tid < cnt) {
-    const int i = u < g.C ? tid / g.kw : 0, j = u < g.C ? tid - (tid / g.kw) * g.kw : 0;
     float v = 0.f;
-    for (int w = 0; w < kK5Threads / 32; ++w) v += red[w][i * KM + j];
-    const int col = u < g.C ? u * khw + tid : na + (u - g.C);
-    p.part[(size_t)sp * ncols + col] = v;
+    for (int b = b0; b < b1; ++b)
+      for (int64_t q = tid; q < hwo; q += kK5Threads) {
+        const float w = to_f32<T>(gy[((int64_t)b * p.o + oc) * hwo + q]);
+        v = fmaf(w, w, v);
+      }
+    v = block_sum(v, red);
+    if (tid == 0) p.part[(size_t)sp * ncols + na + oc] = v;
   }
   __threadfence();
   __syncthreads();
@@ -596,13 +590,11 @@ __global__ void __launch_bounds__(kK5Threads) diag_conv_kernel(const __grid_cons
 }
 
 template <typename T>
-void launch_diag_conv_t(const DiagConvParams& p, int km, dim3 grid, cudaStream_t st) {
-  if (km == 1)
-    launch_pdl(diag_conv_kernel<T, 1>, grid, dim3(kK5Threads), 0, st, p);
-  else if (km == 3)
-    launch_pdl(diag_conv_kernel<T, 3>, grid, dim3(kK5Threads), 0, st, p);
-  else
-    launch_pdl(diag_conv_kernel<T, 7>, grid, dim3(kK5Threads), 0, st, p);
+bool conv_smem_attr() {
+  static bool ok = cudaFuncSetAttribute(diag_conv_kernel<T>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kConvSmemMax) == cudaSuccess;
+  return ok;
 }
 
 }  // namespace
@@ -634,13 +626,16 @@ kfac_status launch_diag_factors_conv(kfac_ctx* h, int layer, const void* x, cons
   if (splits * ncols > (int64_t)h->k5part_floats) return KFAC_ERR_WORKSPACE;
   p.part = h->at<float>(h->off_k5part);
   p.ticket = h->at<int>(h->off_k5tickets);
-  const int km = std::max(cg.kernel_h, cg.kernel_w) == 1 ? 1
-                 : std::max(cg.kernel_h, cg.kernel_w) <= 3 ? 3 : 7;
+  const size_t smem = (size_t)cg.in_h * cg.in_w * sizeof(float);
+  if (smem > kConvSmemMax) return KFAC_ERR_UNSUPPORTED;
   const dim3 grid((unsigned)units, (unsigned)splits);
-  if (L.in_dtype == KFAC_BF16)
-    launch_diag_conv_t<__nv_bfloat16>(p, km, grid, st);
-  else
-    launch_diag_conv_t<float>(p, km, grid, st);
+  if (L.in_dtype == KFAC_BF16) {
+    if (!conv_smem_attr<__nv_bfloat16>()) return KFAC_ERR_CUDA;
+    launch_pdl(diag_conv_kernel<__nv_bfloat16>, grid, dim3(kK5Threads), smem, st, p);
+  } else {
+    if (!conv_smem_attr<float>()) return KFAC_ERR_CUDA;
+    launch_pdl(diag_conv_kernel<float>, grid, dim3(kK5Threads), smem, st, p);
+  }
   count_launch();
   return check_launch();
 }

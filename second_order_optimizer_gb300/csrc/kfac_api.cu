@@ -493,7 +493,6 @@ kfac_status kfac_diag_factors_conv2d(kfac_handle h, int layer, const void* x, co
   if (!g_new || !a_new || !aligned(g_new, 4) || !aligned(a_new, 4)) return KFAC_ERR_INVALID_ARG;
   int64_t rows = 0;
   if (kfac_status e = check_conv(h, L, x, gy, *geom, &rows)) return e;
-  if (geom->kernel_h > 7 || geom->kernel_w > 7) return KFAC_ERR_UNSUPPORTED;
   if (kfac_status e = ensure_device(h)) return e;
   return launch_diag_factors_conv(h, layer, x, gy, *geom, scale, g_new, a_new, stream);
 }

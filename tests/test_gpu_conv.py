@@ -217,14 +217,24 @@ def test_conv_diag_factors_full_size_stage1_layer():
     assert h.get_status()[0] == 0
 
 
-def test_conv_diag_factors_rejects_large_kernels_and_bad_arguments():
+def test_conv_diag_factors_large_kernel_and_limits():
+    """Any kernel size (a 9 x 9 one against the oracle); an image beyond the
+    shared-memory limit (240 x 240) is refused."""
+    from gpu_helpers import max_rel_elem
     h = K.Kfac([(K.KFAC_DIAG, 4, 3 * 81, 1, K.KFAC_F32), (K.KFAC_DIAG, 4, 27, 1, K.KFAC_F32)],
-               max_rows=2 * 100, **HP)
-    x = torch.zeros(2, 3, 10, 10, device="cuda")
+               max_rows=2 * 240 * 240, **HP)
+    x = torch.rand(2, 3, 10, 10, device="cuda")
+    gy = torch.randn(2, 4, 10, 10, device="cuda")
     gn, an = torch.empty(4, device="cuda"), torch.empty(3 * 81 + 1, device="cuda")
-    with pytest.raises(K.KfacError) as e:                 # 9 x 9 kernel
-        h.diag_factors_conv2d(0, x, torch.zeros(2, 4, 10, 10, device="cuda"), gn, an, 9, 1, 4)
+    h.diag_factors_conv2d(0, x, gy, gn, an, 9, 1, 4)
+    g_ref, a_ref = O.conv_diag_factors(to_np(x), to_np(gy), (9, 9), (1, 1), (4, 4), (1, 1), 1)
+    assert max_rel_elem(to_np(an), a_ref) <= 1e-5 and max_rel_elem(to_np(gn), g_ref) <= 1e-5
+    big = torch.zeros(2, 3, 240, 240, device="cuda")
+    with pytest.raises(K.KfacError) as e:
+        h.diag_factors_conv2d(1, big, torch.zeros(2, 4, 240, 240, device="cuda"), gn,
+                              torch.empty(28, device="cuda"), 3, 1, 1)
     assert e.value.code == 7
+    x = torch.zeros(2, 3, 10, 10, device="cuda")
     geom = K.conv2d_geom(x.shape, 3, 1, 1)                # no output gradient
     assert K.LIB.kfac_diag_factors_conv2d(h._h, 1, x.data_ptr(), None, ctypes.byref(geom), 0.0,
                                           gn.data_ptr(), an.data_ptr(), None) == 1
