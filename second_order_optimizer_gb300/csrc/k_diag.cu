@@ -536,13 +536,34 @@ __global__ void __launch_bounds__(kK5Threads) diag_conv_kernel(const __grid_cons
   if (u < g.C) {
     const T* x = static_cast<const T*>(p.x);
     const int hw = g.H * g.W;
-    for (int q = tid; q < hw; q += kK5Threads) {
-      float acc = 0.f;
-      for (int b = b0; b < b1; ++b) {
-        const float v = to_f32<T>(x[((int64_t)b * g.C + u) * hw + q]);
-        acc = fmaf(v, v, acc);
+    // 4 positions x 4 images per step: 16 independent loads in flight per thread
+    for (int q0 = tid; q0 < hw; q0 += 4 * kK5Threads) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      int b = b0;
+      for (; b + 4 <= b1; b += 4) {
+        float v[4][4];
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int q = q0 + k * kK5Threads;
+            v[bb][k] = q < hw ? to_f32<T>(x[((int64_t)(b + bb) * g.C + u) * hw + q]) : 0.f;
+          }
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) acc[k] = fmaf(v[bb][k], v[bb][k], acc[k]);
       }
-      S[q] = acc;
+      for (; b < b1; ++b)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int q = q0 + k * kK5Threads;
+          const float v = q < hw ? to_f32<T>(x[((int64_t)b * g.C + u) * hw + q]) : 0.f;
+          acc[k] = fmaf(v, v, acc[k]);
+        }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (q0 + k * kK5Threads < hw) S[q0 + k * kK5Threads] = acc[k];
     }
     __syncthreads();
     const int hwo = g.Ho * g.Wo;
@@ -561,12 +582,23 @@ __global__ void __launch_bounds__(kK5Threads) diag_conv_kernel(const __grid_cons
     const T* gy = static_cast<const T*>(p.gy);
     const int oc = u - g.C;
     const int64_t hwo = (int64_t)g.Ho * g.Wo;
-    float v = 0.f;
-    for (int b = b0; b < b1; ++b)
-      for (int64_t q = tid; q < hwo; q += kK5Threads) {
-        const float w = to_f32<T>(gy[((int64_t)b * p.o + oc) * hwo + q]);
-        v = fmaf(w, w, v);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int b = b0; b < b1; ++b) {
+      const T* row = gy + ((int64_t)b * p.o + oc) * hwo;
+      for (int64_t q0 = tid; q0 < hwo; q0 += 8 * kK5Threads) {   // 8 loads in flight
+        float w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int64_t q = q0 + (int64_t)k * kK5Threads;
+          w[k] = q < hwo ? to_f32<T>(row[q]) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] = fmaf(w[k], w[k], acc[k]);
       }
+    }
+    float v = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v += acc[k];
     v = block_sum(v, red);
     if (tid == 0) p.part[(size_t)sp * ncols + na + oc] = v;
   }
