@@ -651,7 +651,11 @@ kfac_status launch_diag_factors_conv(kfac_ctx* h, int layer, const void* x, cons
   p.a_new = a_new;
   const int units = cg.in_channels + L.o;
   const int64_t ncols = (int64_t)L.d_in + L.o;
-  int64_t splits = std::min<int64_t>(cg.batch, std::max<int64_t>(1, cdiv(2 * kNumSMs, units)));
+  // image splits: about 4096 elements of a unit per CTA (16 loads per thread),
+  // and at least two CTAs per SM
+  const int64_t per_img = std::max<int64_t>((int64_t)cg.in_h * cg.in_w, (int64_t)ho * wo);
+  int64_t splits = std::max<int64_t>(cdiv(2 * kNumSMs, units), cdiv(cg.batch * per_img, 4096));
+  splits = std::max<int64_t>(1, std::min<int64_t>(splits, cg.batch));
   splits = std::max<int64_t>(1, std::min<int64_t>(splits, (int64_t)(h->k5part_floats / ncols)));
   p.imgs_per_split = (int)cdiv(cg.batch, splits);
   splits = cdiv(cg.batch, p.imgs_per_split);
