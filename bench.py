@@ -205,7 +205,10 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # the raw samples (the bench line carries their summary); KFAC_CLOCKS_DIR keeps them
+        import tempfile
+        d = os.environ.get("KFAC_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(d, f"clocks_bench_{os.getpid()}.csv")
 
     def start(self):
         try:
