@@ -534,3 +534,52 @@ def test_conv_diag_factors_of_constant_image_closed_form():
             for j in range(3):
                 want = (H - abs(i - 1)) * (Wd - abs(j - 1)) / (H * Wd)
                 assert an[(c * 3 + i) * 3 + j] == pytest.approx(want, rel=1e-15)
+
+
+# ---------------------------------------------------------------- property checks (hypothesis)
+
+def _hyp():
+    return pytest.importorskip("hypothesis")
+
+
+def test_property_im2col_matches_unfold_on_random_geometries():
+    hyp = _hyp()
+    torch = pytest.importorskip("torch")
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=60, deadline=None)
+    @hyp.given(B=st.integers(1, 2), C=st.integers(1, 3), H=st.integers(1, 9), Wd=st.integers(1, 9),
+               kh=st.integers(1, 4), kw=st.integers(1, 4), sh=st.integers(1, 3), sw=st.integers(1, 3),
+               ph=st.integers(0, 2), pw=st.integers(0, 2), dh=st.integers(1, 2), dw=st.integers(1, 2))
+    def check(B, C, H, Wd, kh, kw, sh, sw, ph, pw, dh, dw):
+        hyp.assume(O.conv_out_size(H, kh, sh, ph, dh) >= 1 and O.conv_out_size(Wd, kw, sw, pw, dw) >= 1)
+        x = np.random.default_rng(B * 7 + C).standard_normal((B, C, H, Wd))
+        got = O.im2col(x, (kh, kw), (sh, sw), (ph, pw), (dh, dw))
+        u = torch.nn.functional.unfold(torch.from_numpy(x), (kh, kw), dilation=(dh, dw),
+                                       padding=(ph, pw), stride=(sh, sw))
+        np.testing.assert_array_equal(got, u.transpose(1, 2).reshape(-1, C * kh * kw).numpy())
+
+    check()
+
+
+def test_property_damped_inverse_and_factor_invariants():
+    """For random inputs: the factor is symmetric PSD with the bias entries s*M and
+    column means; the damped inverse times F + sqrt(gamma) I is the identity."""
+    hyp = _hyp()
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=40, deadline=None)
+    @hyp.given(M=st.integers(1, 40), d=st.integers(1, 12), seed=st.integers(0, 10**6),
+               gamma=st.sampled_from([1e-4, 1e-3, 1e-1]))
+    def check(M, d, seed, gamma):
+        a = np.random.default_rng(seed).standard_normal((M, d))
+        F = O.factor(a, 1)
+        assert np.array_equal(F, F.T)
+        assert np.linalg.eigvalsh(F).min() >= -1e-12 * max(1.0, np.abs(F).max())
+        assert F[d, d] == pytest.approx(1.0)
+        np.testing.assert_allclose(F[:d, d], a.mean(axis=0), rtol=1e-12, atol=1e-14)
+        Fi = O.damped_inverse(F, gamma)
+        np.testing.assert_allclose(Fi @ (F + math.sqrt(gamma) * np.eye(d + 1)), np.eye(d + 1),
+                                   atol=1e-8 * np.linalg.cond(F + math.sqrt(gamma) * np.eye(d + 1)))
+
+    check()
