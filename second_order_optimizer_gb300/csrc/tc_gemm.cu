@@ -1190,21 +1190,25 @@ struct PackGroup {
   int count;
 };
 
-template <typename T, bool kSplit>
+// One kernel per source kind (kConv: every job of the launch is a gathered one),
+// so the row-major pack keeps its small register footprint and occupancy.
+template <typename T, bool kSplit, bool kConv>
 __global__ void __launch_bounds__(256) pack_grouped_kernel(const __grid_constant__ PackGroup g) {
   pdl_wait();
   pdl_trigger();
   const int64_t b = blockIdx.x;
   int q = 0;
   while (q + 1 < g.count && b >= g.block_start[q + 1]) ++q;
-  const PackJob J = g.job[q];
-  const int64_t local = b - g.block_start[q], rt = (J.Kp + kPackRows - 1) / kPackRows;
-  if (J.conv)
-    pack_tile_conv<T, kSplit>(static_cast<const T*>(J.x), J.cs, J.d, J.n, J.M, J.Kp, J.hi, J.lo,
+  const PackJob& J = g.job[q];
+  const int64_t Kp = J.Kp, local = b - g.block_start[q], rt = (Kp + kPackRows - 1) / kPackRows;
+  if (kConv) {
+    const ConvSrc cs = J.cs;
+    pack_tile_conv<T, kSplit>(static_cast<const T*>(J.x), cs, J.d, J.n, J.M, Kp, J.hi, J.lo,
                               (local % rt) * kPackRows, (int)(local / rt) * 32);
-  else
-    pack_tile<T, kSplit>(static_cast<const T*>(J.x), J.ld, J.M, J.d, J.n, J.Kp, J.hi, J.lo,
+  } else {
+    pack_tile<T, kSplit>(static_cast<const T*>(J.x), J.ld, J.M, J.d, J.n, Kp, J.hi, J.lo,
                          (local % rt) * kPackRows, (int)(local / rt) * 32);
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1301,24 +1305,36 @@ kfac_status launch_wait_selftest(kfac_ctx* h, int64_t wait_cycles, cudaStream_t 
 
 kfac_status launch_pack_grouped(const PackJob* jobs, int count, bool bf16, cudaStream_t st) {
   PackGroup g;
-  std::memset(&g, 0, sizeof(g));
-  for (int c0 = 0; c0 < count; c0 += kMaxPackJobs) {
-    const int cnt = std::min(kMaxPackJobs, count - c0);
-    int64_t blocks = 0;
-    for (int q = 0; q < cnt; ++q) {
-      g.job[q] = jobs[c0 + q];
-      g.block_start[q] = blocks;
-      blocks += cdiv(jobs[c0 + q].Kp, kPackRows) * cdiv(jobs[c0 + q].n, 32);
+  for (int conv = 0; conv < 2; ++conv) {   // row-major jobs, then gathered ones
+    std::vector<const PackJob*> sel;
+    for (int q = 0; q < count; ++q)
+      if ((jobs[q].conv != 0) == (conv != 0)) sel.push_back(&jobs[q]);
+    for (size_t c0 = 0; c0 < sel.size(); c0 += kMaxPackJobs) {
+      std::memset(&g, 0, sizeof(g));
+      const int cnt = (int)std::min<size_t>(kMaxPackJobs, sel.size() - c0);
+      int64_t blocks = 0;
+      for (int q = 0; q < cnt; ++q) {
+        g.job[q] = *sel[c0 + q];
+        g.block_start[q] = blocks;
+        blocks += cdiv(g.job[q].Kp, kPackRows) * cdiv(g.job[q].n, 32);
+      }
+      g.block_start[cnt] = blocks;
+      g.count = cnt;
+      const dim3 grid((unsigned)blocks);
+      if (bf16) {
+        if (conv)
+          launch_pdl(pack_grouped_kernel<__nv_bfloat16, false, true>, grid, dim3(256), 0, st, g);
+        else
+          launch_pdl(pack_grouped_kernel<__nv_bfloat16, false, false>, grid, dim3(256), 0, st, g);
+      } else {
+        if (conv)
+          launch_pdl(pack_grouped_kernel<float, true, true>, grid, dim3(256), 0, st, g);
+        else
+          launch_pdl(pack_grouped_kernel<float, true, false>, grid, dim3(256), 0, st, g);
+      }
+      count_launch();
+      if (kfac_status e = check_launch()) return e;
     }
-    g.block_start[cnt] = blocks;
-    g.count = cnt;
-    const unsigned grid = (unsigned)blocks;
-    if (bf16)
-      launch_pdl(pack_grouped_kernel<__nv_bfloat16, false>, dim3(grid), dim3(256), 0, st, g);
-    else
-      launch_pdl(pack_grouped_kernel<float, true>, dim3(grid), dim3(256), 0, st, g);
-    count_launch();
-    if (kfac_status e = check_launch()) return e;
   }
   return KFAC_OK;
 }
