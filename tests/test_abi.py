@@ -159,8 +159,8 @@ def test_workspace_holds_the_inverse_factors_when_asked(lib):
 
 
 def test_header_is_plain_c(tmp_path):
-    """include/kfac.h compiles as C99 (no C++ in the boundary), with a call of
-    every declared function type-checked by the C compiler."""
+    """include/kfac.h compiles as C99 (no C++ in the boundary): its structs and
+    enums initialise and a declared function is called from a C translation unit."""
     import shutil
     import subprocess
     cc = shutil.which("gcc") or shutil.which("cc")
@@ -168,14 +168,14 @@ def test_header_is_plain_c(tmp_path):
     if not cc or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
         pytest.skip("no C compiler or CUDA headers")
     src = tmp_path / "use_kfac.c"
-    src.write_text('#include "kfac.h"\\n'
-                   "int main(void) {\\n"
-                   "  kfac_conv2d_geom g = {1, 1, 3, 3, 3, 3, 1, 1, 1, 1, 1, 1};\\n"
-                   "  kfac_hparams hp = {0.95, 1e-3, 1e-2, 0.9, 5e-4, KFAC_EMA_INIT_ZERO,\\n"
-                   "                     KFAC_MATH_3XTF32, 0};\\n"
-                   "  (void)g; (void)hp;\\n"
-                   "  return (int)kfac_launch_count();\\n"
-                   "}\\n")
+    src.write_text('#include "kfac.h"\n'
+                   "int main(void) {\n"
+                   "  kfac_conv2d_geom g = {1, 1, 3, 3, 3, 3, 1, 1, 1, 1, 1, 1};\n"
+                   "  kfac_hparams hp = {0.95, 1e-3, 1e-2, 0.9, 5e-4, KFAC_EMA_INIT_ZERO,\n"
+                   "                     KFAC_MATH_3XTF32, 0};\n"
+                   "  (void)g; (void)hp;\n"
+                   "  return (int)kfac_launch_count();\n"
+                   "}\n")
     r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror=implicit-function-declaration",
                         "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, "-fsyntax-only",
                         str(src)], capture_output=True, text=True)
