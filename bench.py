@@ -725,9 +725,9 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
     region.  The inputs of all layers are one packed pinned buffer (a diagonal twin
     shares its layer's tensors, so they are copied once), double-buffered on the
     device: the next step's copy runs on a copy stream while this step computes.
-    The parameter read-back runs on a second copy stream (both directions at
-    once); the next step's factor update (and refresh) overlap it, and its
-    parameter updates wait for it.  On
+    The step's updated parameters are snapshotted on the device (one device
+    copy, inside the timed region) and read back from the snapshot on a second
+    copy stream while the next step runs (both copy directions at once).  On
     steps without a refresh the factor update runs on a side stream alongside
     the preconditioning and the diagonal step (as in the timed steps).  With
     CUDA graphs (the default) the library calls of each phase are captured once
@@ -786,7 +786,11 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
     copy_out = torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event(), torch.cuda.Event()]
     ev_used = [torch.cuda.Event(), torch.cuda.Event()]
-    ev_done, ev_out = torch.cuda.Event(), torch.cuda.Event()
+    ev_done = torch.cuda.Event()
+    # each step's result is snapshotted on the device and read back from the
+    # snapshot, so the next step updates the live parameters without waiting
+    snaps = [torch.empty_like(params_flat) for _ in range(2)]
+    ev_out = [torch.cuda.Event(), torch.cuda.Event()]
     fside = torch.cuda.Stream(dev)
     dside = torch.cuda.Stream(dev)
     ev_djoin = torch.cuda.Event()
@@ -811,8 +815,6 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
         if overlap:                             # diagonal step alongside the KRON path
             ev_fork.record(main)
             dside.wait_event(ev_fork)
-            if i >= 1:
-                dside.wait_event(ev_out)        # previous step's parameters are read back
             with torch.cuda.stream(dside):
                 run("diag", b)
                 ev_djoin.record(dside)
@@ -826,8 +828,6 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
             run("factor", b)
             if (t - 1) % k == 0:
                 run_invert()
-        if i >= 1:
-            main.wait_event(ev_out)            # previous step's parameters are read back
         run("precond", b)
         if not overlap:
             run("diag", b)
@@ -836,17 +836,21 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
         if overlap:
             main.wait_event(ev_djoin)
         ev_used[b].record(main)
+        if i >= 2:
+            main.wait_event(ev_out[b])         # the read-back of two steps ago left snaps[b]
+        snaps[b].copy_(params_flat)            # this step's result
         ev_done.record(main)
-        with torch.cuda.stream(copy_out):      # device -> host on its own stream, so it
-            copy_out.wait_event(ev_done)       # runs alongside the next step's host -> device
-            outs.copy_(params_flat, non_blocking=True)
-            ev_out.record(copy_out)
+        with torch.cuda.stream(copy_out):      # device -> host on its own stream, alongside
+            copy_out.wait_event(ev_done)       # the next step and its host -> device copy
+            outs.copy_(snaps[b], non_blocking=True)
+            ev_out[b].record(copy_out)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
     return {"value": round(1.0 / dt, 3), "unit": "steps/s", "h2d_bytes_per_step": int(total),
             "d2h_bytes_per_step": int(params_flat.numel() * 4), "steps": steps,
-            "pipelined": "two copy streams: the next step's H2D during this step, this step's "
-                         "parameter D2H during the next step's factor update (both directions at once)"}
+            "pipelined": "two copy streams: the next step's H2D during this step; this step's "
+                         "parameters snapshotted on the device and read back (D2H) during the "
+                         "next step (both directions at once)"}
 
 
 # ----------------------------------------------------------------------------- micro
