@@ -123,3 +123,31 @@ def test_mlp_graph_replay_on_three_streams_matches_oracle():
         Wg = O.grad_hat(to_np(params[i][0]), to_np(params[i][1]))
         tol = 1e-4 if l.kind == "kron" else 1e-6
         assert rel_fro(Wg, states[i].W) <= tol, (l.name, rel_fro(Wg, states[i].W))
+
+
+def test_bench_prints_one_contract_line():
+    """`bench.py` on the single-linear set prints one JSON line with every key the
+    measurement contract asks for."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--workload",
+                        "single_linear", "--steps", "20", "--warmup", "3", "--no-cpu-baseline"],
+                       capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "e2e", "gpu_launches", "clocks"):
+        assert key in d, key
+    assert d["n_gpus"] == 1 and d["steps"] == 20 and d["value"] > 0 and d["gpu_launches"] > 0
+    roof = d["roofline"]
+    assert roof["bound"] in ("hbm", "tensor", "alu") and roof["peak"] > 0
+    assert roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"], rel=1e-3)
+    e = d["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]

@@ -77,3 +77,26 @@ def test_stale_schedule_matches_bench_refresh_cadence():
     flags = [O.stale_refresh(t, 1, k, k) for t in range(1, 42)]
     plain = [(t - 1) % k == 0 for t in range(1, 42)]
     assert [f[0] for f in flags] == plain and [f[1] for f in flags] == plain
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the float64 oracle on the host) prints one JSON
+    line with the contract's keys, on the GPU arm's metric and workload name."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--workload", "single_linear", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=300, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["unit"] == "steps/s" and d["higher_is_better"] is True and d["value"] > 0
+    assert d["config"]["workload"].startswith("single_linear_64x32_b128")
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "steps/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
