@@ -147,7 +147,7 @@ def test_bench_prints_one_contract_line():
     assert d["n_gpus"] == 1 and d["steps"] == 20 and d["value"] > 0 and d["gpu_launches"] > 0
     roof = d["roofline"]
     assert roof["bound"] in ("hbm", "tensor", "alu") and roof["peak"] > 0
-    assert roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"], rel=1e-3)
+    assert roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"], rel=1e-3, abs=1e-4)
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
