@@ -70,7 +70,8 @@ typedef enum { KFAC_KRON = 0, KFAC_DIAG = 1 } kfac_kind;
 typedef enum { KFAC_F32 = 0, KFAC_BF16 = 1 } kfac_dtype;
 /* Arithmetic of the preconditioning GEMMs.  3XTF32: fp32 operands split into
  * two TF32 halves, three tensor-core products, fp32 accumulation (matches fp32
- * to ~1e-6).  BF16: inverses and gradients rounded to bf16, fp32 accumulation. */
+ * to ~1e-6).  BF16 (inverses and gradients rounded to bf16) is reserved:
+ * kfac_create and kfac_set_hparams return KFAC_ERR_UNSUPPORTED for it. */
 typedef enum { KFAC_MATH_3XTF32 = 0, KFAC_MATH_BF16 = 1 } kfac_math;
 /* Start of the running averages: ZERO gives F_1 = (1-xi) F_new; FIRST gives F_1 = F_new. */
 typedef enum { KFAC_EMA_INIT_ZERO = 0, KFAC_EMA_INIT_FIRST = 1 } kfac_ema_init;
@@ -124,8 +125,13 @@ kfac_status kfac_workspace_size(const kfac_layer_desc* layers, int n_layers,
 kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_hparams* hp,
                         int64_t max_rows, void* d_workspace, size_t bytes, kfac_handle* out);
 
-/* Replace the hyper-parameters (schedules such as warm-up damping).  The new
- * damping takes effect at the next kfac_invert. */
+/* Replace the hyper-parameters (schedules such as warm-up damping, or a
+ * BatchNorm damping rho_BN * gamma set around the diagonal step of those
+ * layers).  Each value applies from the next call that uses it: the decay at
+ * the next factor update or diagonal step, the damping at the next refresh
+ * (kfac_invert*, kfac_ikfac_update) of KRON layers and the next kfac_diag_step
+ * of DIAG layers, lr, momentum and weight decay at the next update.  ikfac is
+ * fixed at kfac_create (a different value: KFAC_ERR_INVALID_ARG). */
 kfac_status kfac_set_hparams(kfac_handle h, const kfac_hparams* hp);
 
 /* K1: fold new factors into the running A and G of a KRON layer.
