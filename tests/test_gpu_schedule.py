@@ -200,3 +200,82 @@ def test_tie_rules():
     h.precondition(1, torch.zeros(16, 32, device="cuda"), torch.zeros(16, device="cuda"),
                    torch.empty(16, 32, device="cuda"), torch.empty(16, device="cuda"))
     assert h.get_status()[0] == 0
+
+
+def test_features_together_against_oracle():
+    """One handle mixing the features: a convolution from NCHW tensors, two linear
+    layers sharing one A, inverse-free refreshes, a stale A, a G-only Cholesky
+    refresh, and a convolution on the diagonal path.  Six steps against the oracle."""
+    gam = HP["damping"]
+    B, C, H, Wd, o_c = 4, 6, 9, 9, 10                  # conv 3x3, pad 1: 324 rows, n = 55
+    M, d, o = 324, 40, 24                               # two linear layers fed the same input
+    layers = [(K.KFAC_KRON, o_c, C * 9, 1, K.KFAC_F32), (K.KFAC_KRON, o, d, 1, K.KFAC_F32),
+              (K.KFAC_KRON, o, d, 1, K.KFAC_F32), (K.KFAC_DIAG, o_c, C * 9, 1, K.KFAC_F32)]
+    h = K.Kfac(layers, max_rows=M, ikfac=1, **HP)
+    h.tie_a_factor(2, 1)
+    orc = _orc()
+    shapes = [(o_c, C * 9), (o, d), (o, d), (o_c, C * 9)]
+    st, dev_p = [], []
+    for kind, (oo, dd) in zip(["kron", "kron", "kron", "diag"], shapes):
+        w0, b0 = _params(oo, dd)
+        st.append(O.LayerState(kind, oo, dd, 1, w0, b0))
+        dev_p.append((to_dev(w0), to_dev(b0)))
+    KA, KG = {}, {}
+    gn = torch.empty(o_c, device="cuda")
+    an = torch.empty(C * 9 + 1, device="cuda")
+    for t in range(1, 7):
+        x = np.maximum(RNG.standard_normal((B, C, H, Wd)), 0).astype(np.float32)
+        gy = (RNG.standard_normal((B, o_c, H, Wd)) * 1e-2).astype(np.float32)
+        a = np.maximum(RNG.standard_normal((M, d)), 0).astype(np.float32)
+        g1, g2 = [(RNG.standard_normal((M, o)) * 1e-2).astype(np.float32) for _ in range(2)]
+        grads = [((RNG.standard_normal((oo, dd)) * 1e-3).astype(np.float32),
+                  (RNG.standard_normal(oo) * 1e-3).astype(np.float32)) for oo, dd in shapes]
+        stale_a = t == 3                                 # A factors left as they are at step 3
+        # --- GPU
+        h.update_factors_conv2d(0, None if stale_a else to_dev(x), to_dev(gy), 3, 1, 1,
+                                in_shape=x.shape)
+        h.update_factors_batched([1, 2], [None if stale_a else to_dev(a), None],
+                                 [to_dev(g1), to_dev(g2)])
+        if t == 1:
+            h.invert(-1)
+        elif t == 4:
+            h.invert(-1, which=K.KFAC_FACTOR_G)          # Cholesky for G; A keeps its K
+        else:
+            h.ikfac_update(-1, beta=1.0)
+        h.precondition_batched([0, 1, 2], [to_dev(g[0]) for g in grads[:3]],
+                               [to_dev(g[1]) for g in grads[:3]], None, None,
+                               [p[0] for p in dev_p[:3]], [p[1] for p in dev_p[:3]])
+        h.diag_factors_conv2d(3, to_dev(x), to_dev(gy), gn, an, 3, 1, 1)
+        h.diag_step(3, gn, an, to_dev(grads[3][0]), to_dev(grads[3][1]), dev_p[3][0], dev_p[3][1])
+        # --- oracle
+        An_c, Gn_c = O.conv_factors(x, gy, (3, 3), (1, 1), (1, 1), (1, 1), 1)
+        ins = {0: (An_c, Gn_c), 1: (O.factor(a, 1), O.factor(g1, 0)), 2: (None, O.factor(g2, 0))}
+        for i in (0, 1, 2):
+            s = st[i]
+            if i != 2 and not stale_a:
+                s.A = O.ema(s.A, ins[i][0], orc.xi)
+            s.G = O.ema(s.G, ins[i][1], orc.xi)
+        for i in (0, 1, 2):
+            s, src = st[i], st[1] if i == 2 else st[i]
+            if t == 1:
+                if i != 2:
+                    KA[i] = O.ikfac_init(s.A, gam)
+                KG[i] = O.ikfac_init(s.G, gam)
+            elif t == 4:
+                KG[i] = O.ikfac_init(s.G, gam)
+            else:
+                if i != 2:
+                    KA[i] = O.ikfac_update(KA[i], s.A, gam, 1.0)
+                KG[i] = O.ikfac_update(KG[i], s.G, gam, 1.0)
+        for i in (0, 1, 2):
+            s = st[i]
+            Ainv = O.ikfac_inverse(KA[1 if i == 2 else i])
+            P = O.precondition(O.ikfac_inverse(KG[i]), O.grad_hat(*grads[i]), Ainv)
+            s.W, s.m = O.momentum_update(P, s.W, s.m, orc.lr, orc.mu, orc.wd)
+        gd, ad = O.conv_diag_factors(x, gy, (3, 3), (1, 1), (1, 1), (1, 1), 1)
+        orc.step_diag(st[3], gd, ad, *grads[3])
+        for i in range(4):
+            Wg = np.concatenate([to_np(dev_p[i][0]), to_np(dev_p[i][1])[:, None]], axis=1)
+            tol = 1e-4 if i < 3 else 1e-6
+            assert rel_fro(Wg, st[i].W) <= tol, (t, i, rel_fro(Wg, st[i].W))
+    assert h.get_status()[0] == 0
