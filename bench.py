@@ -91,9 +91,9 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # FFMA lanes x 2 flop x max SM
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=600)
+    p.add_argument("--steps", type=int, default=30)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--workload", default="mlp4", choices=sorted(WORKLOADS))
+    p.add_argument("--workload", default="transformer4", choices=sorted(WORKLOADS))
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -140,23 +140,20 @@ def bench_config(workload):
     return cfg, layers
 
 
-# ----------------------------------------------------------------------------- multi-rank
-
-def max_over_ranks(x: float, device=None) -> float:
-    """Max of a per-rank time over all ranks (identity when not distributed)."""
-    import torch
-    import torch.distributed as dist
-    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
-        return float(x)
-    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+def workload_name(cfg, workload):
+    """The layer set's name with the bench variant's suffixes (both arms print it)."""
+    return (cfg.name + ("+diag_twins" if not cfg.diag_layers else "")
+            + ("+nchw_conv_inputs" if workload in NCHW_WORKLOADS else "")
+            + ("+all_layers_diagonal" if workload in DIAG_WORKLOADS else "")
+            + ("+qkv_shared_A" if workload in TIED_WORKLOADS else "")
+            + ("+inverse_free_refresh" if workload in IKFAC_WORKLOADS else ""))
 
 
-def job_throughput(ms_per_step_max: float, world: int) -> float:
-    """Whole-job steps/s: every rank runs one replica step per step (weak scaling),
-    so the job completes `world` steps in the slowest rank's step time."""
-    return world * 1e3 / ms_per_step_max
+def path_dtype(layers):
+    """Arithmetic of the step: fp32 state, factors and preconditioning (3xTF32 on the
+    tensor cores, fp32-accurate); factor products read bf16 inputs where the layer
+    set has them."""
+    return "bf16-in/f32" if any(l.in_dtype == "bf16" for l in layers) else "f32"
 
 
 # ----------------------------------------------------------------------------- accounting
@@ -368,17 +365,18 @@ def oracle_steps_per_s(cfg, layers, budget_s=20.0, min_s=10.0, nchw=False, tied=
     if diag:
         t_total += dsum / passes * len(diag) / len(dsample)
     names = [l.name for l in sampled]
-    sample = (f"oracle fp64: factor+precond+update of {len(sampled)}/{len(kron)} KRON layers "
-              f"({', '.join(names[:4])}{'...' if len(names) > 4 else ''}) with one refresh "
-              f"amortised by {cfg.invert_every}, diag step of {len(dsample)}/{len(diag)} "
-              f"DIAG layers, {passes} pass(es) averaged; scaled to the full layer set by "
-              f"flop-weighted cost")
+    sample = (f"oracle fp64 (NumPy: matrix products through NumPy's BLAS, Cholesky and "
+              f"substitutions as column loops): factor+precond+update of {len(sampled)}/"
+              f"{len(kron)} KRON layers ({', '.join(names[:4])}{'...' if len(names) > 4 else ''})"
+              f" with one refresh amortised by {cfg.invert_every}, diag step of "
+              f"{len(dsample)}/{len(diag)} DIAG layers, {passes} pass(es) averaged; "
+              f"extrapolated to the full layer set by flop-weighted cost")
     return 1.0 / t_total, sample, time.perf_counter() - t0
 
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def run_gpu(args, rank, world, peaks, peak_kind):
+def run_gpu(args, peaks, peak_kind):
     import torch
     import second_order_optimizer_gb300 as K
 
@@ -407,10 +405,10 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     for b in range(NB):
         per = []
         for li, l in enumerate(layers):
-            x = Wl.layer_inputs_torch(cfg, srcidx[li], 1 + b + 1000 * rank, dev)
+            x = Wl.layer_inputs_torch(cfg, srcidx[li], 1 + b, dev)
             if is_conv(l):      # NCHW input and output gradient replace the unfolded a, g
                 del x["a"], x["g"]
-                c = Wl.conv_inputs_torch(cfg, srcidx[li], 1 + b + 1000 * rank, dev)
+                c = Wl.conv_inputs_torch(cfg, srcidx[li], 1 + b, dev)
                 x["x"], x["gy"] = c["x"], c["gy"]
             per.append(x)
         data.append(per)
@@ -597,8 +595,6 @@ def run_gpu(args, rank, world, peaks, peak_kind):
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     sampler = ClockSampler(dev.index)
-    if world > 1:
-        torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler.start()
     l0 = K.launch_count()
@@ -616,14 +612,11 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     launches = K.launch_count() - l0 + graph_launches
-    if world > 1:
-        torch.distributed.barrier()
     clocks = sampler.stop()
     code = h.get_status()[0]
     if code:
         raise RuntimeError(f"device status {code} in the timed region")
     ms_step = float(np.mean([evs[i][0].elapsed_time(evs[i][4]) for i in range(args.steps)]))
-    ms_step = max_over_ranks(ms_step, dev)
     refresh_steps = [i for i in range(args.steps) if refreshed[i]]
     inv_ms_refresh = (float(np.mean([evs[i][1].elapsed_time(evs[i][2]) for i in refresh_steps]))
                       if refresh_steps else 0.0)
@@ -701,11 +694,8 @@ def run_gpu(args, rank, world, peaks, peak_kind):
     return {
         "ms_per_step": ms_step, "phases": phases, "roofline": roof, "clocks": clocks,
         "gpu_launches": int(launches), "wall_s": wall, "e2e": e2e,
-        "config": {"workload": cfg.name + ("+diag_twins" if not cfg.diag_layers else "")
-                   + ("+nchw_conv_inputs" if nchw else "")
-                   + ("+all_layers_diagonal" if args.workload in DIAG_WORKLOADS else "")
-                   + ("+qkv_shared_A" if ties else "")
-                   + ("+inverse_free_refresh" if ikfac else ""),
+        "dtype": path_dtype(layers),
+        "config": {"workload": workload_name(cfg, args.workload),
                    "kron_layers": sum(l.kind == "kron" for l in layers),
                    "diag_layers": sum(l.kind == "diag" for l in layers),
                    "invert_every": k, "max_rows": max_rows,
@@ -796,11 +786,7 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
     ev_djoin = torch.cuda.Event()
     ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
     steps = max(3, min(args.steps, 50))
-    import torch.distributed as dist
-    multi = dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1
     torch.cuda.synchronize()
-    if multi:
-        dist.barrier()
     t0 = time.perf_counter()
     with torch.cuda.stream(copy):
         stage[0].copy_(host, non_blocking=True)
@@ -849,10 +835,8 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
             outs.copy_(snaps[b], non_blocking=True)
             ev_out[b].record(copy_out)
     torch.cuda.synchronize()
-    # whole job: every rank runs one replica step per step, in the slowest rank's time
-    dt = max_over_ranks((time.perf_counter() - t0) / steps, dev)
-    world = dist.get_world_size() if multi else 1
-    return {"value": round(world / dt, 3), "unit": "steps/s", "h2d_bytes_per_step": int(total),
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": round(1.0 / dt, 3), "unit": "steps/s", "h2d_bytes_per_step": int(total),
             "d2h_bytes_per_step": int(params_flat.numel() * 4), "steps": steps,
             "pipelined": "two copy streams: the next step's H2D during this step; this step's "
                          "parameters snapshotted on the device and read back (D2H) during the "
@@ -948,7 +932,7 @@ def main():
     cfg, layers = bench_config(args.workload)
 
     if args.impl == "reference":
-        if rank != 0:
+        if rank != 0:      # under torchrun: rank 0 alone times the oracle
             return
         per_step = []
         sample = None
@@ -969,11 +953,7 @@ def main():
                 "n_gpus": args.gpus, "steps": len(per_step), "warmup": args.warmup,
                 "ms_per_step": round(1e3 / value, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": cfg.name + ("+diag_twins" if not cfg.diag_layers else "")
-                           + ("+nchw_conv_inputs" if args.workload in NCHW_WORKLOADS else "")
-                           + ("+all_layers_diagonal" if args.workload in DIAG_WORKLOADS else "")
-                           + ("+qkv_shared_A" if args.workload in TIED_WORKLOADS else "")
-                           + ("+inverse_free_refresh" if args.workload in IKFAC_WORKLOADS else ""),
+                "config": {"workload": workload_name(cfg, args.workload),
                            "invert_every": cfg.invert_every},
                 "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": cores,
                                  "kind": "oracle", "sample": sample},
@@ -982,30 +962,33 @@ def main():
         print(json.dumps(line), flush=True)
         return
 
-    import torch
-    if world > 1:
-        torch.distributed.init_process_group("nccl")
-    res = run_gpu(args, rank, world, peaks, peak_kind)
+    if world > 1 or args.gpus != 1:
+        # The library is single-GPU: each process drives one GPU and its GEMM engine
+        # may pair CTAs that share tiles by TMA multicast, which stays within one
+        # process on one GPU.  There is no multi-rank mode.
+        print(f"bench.py: the GPU arm runs on one GPU only (WORLD_SIZE={world}, "
+              f"--gpus {args.gpus}); run it without torchrun and with --gpus 1",
+              file=sys.stderr, flush=True)
+        sys.exit(2)
+    res = run_gpu(args, peaks, peak_kind)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         v, sample, spent = oracle_steps_per_s(cfg, layers, budget_s=20.0,
                                               nchw=args.workload in NCHW_WORKLOADS,
                                               tied=args.workload in TIED_WORKLOADS,
                                               ikfac=args.workload in IKFAC_WORKLOADS)
         cpu = {"value": round(v, 6), "unit": "steps/s", "cores": blas_threads(), "kind": "oracle",
                "sample": sample, "seconds": round(spent, 1)}
-    if rank == 0:
-        value = job_throughput(res["ms_per_step"], world)
-        line = {"metric": METRIC, "value": round(value, 3), "unit": "steps/s", "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": round(res["ms_per_step"], 4), "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": res["config"], "phases": res["phases"], "roofline": res["roofline"],
-                "cpu_baseline": cpu, "e2e": res["e2e"], "gpu_launches": res["gpu_launches"],
-                "clocks": res["clocks"], "peaks": {"source": peak_kind, **peaks}}
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    value = 1e3 / res["ms_per_step"]
+    line = {"metric": METRIC, "value": round(value, 3), "unit": "steps/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(res["ms_per_step"], 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": res["dtype"],
+            "data": "synthetic", "config": res["config"], "phases": res["phases"],
+            "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"],
+            "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
+            "peaks": {"source": peak_kind, **peaks}}
+    print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

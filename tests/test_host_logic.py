@@ -100,3 +100,49 @@ def test_reference_arm_prints_one_contract_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "steps/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def _run_bench(args, env_extra):
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(root, "bench.py")] + args,
+                          capture_output=True, text=True, timeout=300, cwd=root, env=env)
+
+
+def test_gpu_arm_refuses_more_than_one_rank():
+    """The library is single-GPU: the GPU arm exits with a message (and no JSON
+    line) when started as one of several ranks or with --gpus > 1, before it
+    touches a GPU."""
+    r = _run_bench(["--workload", "single_linear"], {"WORLD_SIZE": "2", "RANK": "0"})
+    assert r.returncode == 2 and "one GPU only" in r.stderr
+    assert not [l for l in r.stdout.splitlines() if l.startswith("{")]
+    r = _run_bench(["--workload", "single_linear", "--gpus", "2"], {})
+    assert r.returncode == 2 and "one GPU only" in r.stderr
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    """Under torchrun the reference arm runs on rank 0 alone; other ranks exit 0."""
+    r = _run_bench(["--impl", "reference", "--workload", "single_linear", "--steps", "1"],
+                   {"WORLD_SIZE": "2", "RANK": "1"})
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_default_workload_is_the_transformer_set():
+    """With no flags the bench times the largest single-GPU layer set: four
+    transformer blocks (d_model 2048, FFN 8192, 16384 tokens, bf16 inputs)."""
+    import sys
+    old = sys.argv
+    sys.argv = ["bench.py"]
+    try:
+        a = bench.parse()
+    finally:
+        sys.argv = old
+    assert a.workload == "transformer4" and a.gpus == 1
+    cfg, layers = bench.bench_config(a.workload)
+    kron = [l for l in layers if l.kind == "kron"]
+    assert len(kron) == 24 and max(l.n for l in kron) == 8193 and max(l.d_out for l in kron) == 8192
+    assert all(l.rows == 16384 and l.in_dtype == "bf16" for l in kron)
+    assert bench.path_dtype(layers) == "bf16-in/f32"
