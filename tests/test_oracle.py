@@ -583,3 +583,83 @@ def test_property_damped_inverse_and_factor_invariants():
                                    atol=1e-8 * np.linalg.cond(F + math.sqrt(gamma) * np.eye(d + 1)))
 
     check()
+
+
+# ------------------------------------------------- the diagonal step as a whole
+
+def _diag_step_rational(st, g_new, a_new, gw_hat, xi, gamma, eta, mu, lam, first):
+    """One diagonal step in exact rationals, in the order the CAFIN page's Kernel
+    Fusion Strategy gives: EMA of the diagonal factors first, then the gradient
+    divided by the *updated* factors, then weight decay and momentum, then the
+    in-place parameter write.  st = (gs, as, W, m) as lists of Fractions."""
+    gs, as_, Wt, m = st
+    if first:
+        gs = list(g_new)
+        as_ = list(a_new)
+    else:
+        gs = [xi * o + (1 - xi) * v for o, v in zip(gs, g_new)]
+        as_ = [xi * o + (1 - xi) * v for o, v in zip(as_, a_new)]
+    P = [[gw_hat[i][j] / (gs[i] * as_[j] + gamma) for j in range(len(as_))]
+         for i in range(len(gs))]
+    m = [[mu * m[i][j] + P[i][j] + lam * Wt[i][j] for j in range(len(as_))]
+         for i in range(len(gs))]
+    Wt = [[Wt[i][j] - eta * m[i][j] for j in range(len(as_))] for i in range(len(gs))]
+    return (gs, as_, Wt, m), P
+
+
+@pytest.mark.parametrize("ema_init", ["zero", "first"])
+def test_step_diag_two_steps_exact_rationals(ema_init):
+    """KfacOracle.step_diag over two steps of a 2 x (1 + bias) layer against a
+    hand-worked case in exact rationals.  All inputs are small rationals, so the
+    float64 oracle agrees to a few ulps.  The order of the fused operations is
+    pinned too: the two plausible slips (preconditioning with the factors from
+    before the EMA; the EMA-first option applied at the wrong step) end far from
+    the exact parameters."""
+    F = Fraction
+    xi, gamma, eta, mu, lam = F(1, 2), F(1, 8), F(1, 4), F(1, 2), F(1, 4)
+    W0 = [[F(1), F(2)], [F(3), F(-1)]]                 # [W | b], o = 2, d_in = 1
+    steps = [([F(2), F(3)], [F(1), F(4)], [[F(1)], [F(2)]], [F(3), F(-4)]),
+             ([F(1), F(1, 2)], [F(2), F(1)], [[F(-1)], [F(1, 2)]], [F(1), F(2)])]
+    orc = O.KfacOracle(float(xi), float(gamma), float(eta), float(mu), float(lam), 1,
+                       ema_init=ema_init)
+    st = O.LayerState("diag", 2, 1, 1, np.array([[1.0], [3.0]]), np.array([2.0, -1.0]))
+    exact = ([F(0)] * 2, [F(0)] * 2, W0, [[F(0)] * 2 for _ in range(2)])
+    slip_first = exact          # EMA-first applied at step 2 instead of step 1
+    for t, (gn, an, gw, gb) in enumerate(steps, start=1):
+        gw_hat = [[gw[i][0], gb[i]] for i in range(2)]
+        P = orc.step_diag(st, np.array([float(v) for v in gn]), np.array([float(v) for v in an]),
+                          np.array([[float(v[0])] for v in gw]), np.array([float(v) for v in gb]))
+        first = ema_init == "first" and t == 1
+        exact, Pe = _diag_step_rational(exact, gn, an, gw_hat, xi, gamma, eta, mu, lam, first)
+        slip_first, _ = _diag_step_rational(slip_first, gn, an, gw_hat, xi, gamma, eta, mu, lam,
+                                            ema_init == "first" and t == 2)
+        for i in range(2):
+            assert st.gs[i] == pytest.approx(float(exact[0][i]), rel=1e-15, abs=0)
+            assert st.as_[i] == pytest.approx(float(exact[1][i]), rel=1e-15, abs=0)
+            for j in range(2):
+                assert P[i, j] == pytest.approx(float(Pe[i][j]), rel=1e-14, abs=0)
+                assert st.m[i, j] == pytest.approx(float(exact[3][i][j]), rel=1e-14, abs=1e-15)
+                assert st.W[i, j] == pytest.approx(float(exact[2][i][j]), rel=1e-14, abs=1e-15)
+    far = lambda A, B: max(abs(float(A[i][j] - B[i][j])) for i in range(2) for j in range(2))
+    Wpre = _two_steps_preconditioning_with_old_factors(steps, W0, xi, gamma, eta, mu, lam,
+                                                       ema_init == "first")
+    assert far(Wpre, exact[2]) > 1e-2
+    if ema_init == "first":
+        assert far(slip_first[2], exact[2]) > 1e-2
+
+
+def _two_steps_preconditioning_with_old_factors(steps, W0, xi, gamma, eta, mu, lam, first):
+    """The slip 'precondition with the factors from before the EMA', two steps."""
+    F = Fraction
+    gs, as_, Wt, m = [F(0)] * 2, [F(0)] * 2, [r[:] for r in W0], [[F(0)] * 2 for _ in range(2)]
+    for t, (gn, an, gw, gb) in enumerate(steps, start=1):
+        gw_hat = [[gw[i][0], gb[i]] for i in range(2)]
+        P = [[gw_hat[i][j] / (gs[i] * as_[j] + gamma) for j in range(2)] for i in range(2)]
+        if first and t == 1:
+            gs, as_ = list(gn), list(an)
+        else:
+            gs = [xi * o + (1 - xi) * v for o, v in zip(gs, gn)]
+            as_ = [xi * o + (1 - xi) * v for o, v in zip(as_, an)]
+        m = [[mu * m[i][j] + P[i][j] + lam * Wt[i][j] for j in range(2)] for i in range(2)]
+        Wt = [[Wt[i][j] - eta * m[i][j] for j in range(2)] for i in range(2)]
+    return Wt
