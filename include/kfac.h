@@ -369,13 +369,15 @@ const char* kfac_status_string(kfac_status s);
  * runs under another framework's allocator, or a plug-in whose host owns all
  * device allocations.  The paper has no counterpart to this entry point; it
  * computes exactly what kfac_diag_factors computes for a layer with these
- * dimensions (same kernel, same row splits, same results).
- * Scratch: a static device array of about 1.4 MiB (partial sums) plus 4 KiB
+ * dimensions (same kernel; on GPUs with at most 256 SMs the same row splits and
+ * so the same results).
+ * Scratch: a static device array of 1.5 MiB (partial sums) plus 4 KiB
  * (counters) that every GPU which loads the library keeps until process exit.
  * Limit: d_in + d_out <= 262144, else KFAC_ERR_WORKSPACE.  Allocates nothing:
- * no cudaMalloc/cudaFree, no allocating library call.  The first call on a
- * device looks up the array's device address on that device (make that first
- * call before any stream capture).  Every call shares the one array and it
+ * no cudaMalloc/cudaFree, no allocating library call.  Each call looks up the
+ * array's device address on the current device (a host-side query; the first
+ * call on a device may load the library's device code there, so make it before
+ * any stream capture).  Every call shares the one array and it
  * keeps the last call's contents: calls that overlap on the GPU (other
  * streams, other threads) race; order them.  Arguments as kfac_diag_factors
  * plus the layer shape: in_dtype is a kfac_dtype, scale <= 0 means 1/rows. */

@@ -78,11 +78,13 @@ class Kfac:
         self._hp = HParams(ema_decay, damping, lr, momentum, weight_decay, ema_init, math,
                            int(ikfac))
         self.max_rows = int(max_rows)
-        nbytes = ctypes.c_size_t(0)
-        _check(LIB.kfac_workspace_size(self._descs, self.n_layers, ctypes.byref(self._hp),
-                                       self.max_rows, ctypes.byref(nbytes)), "kfac_workspace_size")
-        self.workspace_bytes = nbytes.value
         dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        nbytes = ctypes.c_size_t(0)
+        with torch.cuda.device(dev):   # the plan depends on the device's SM count
+            _check(LIB.kfac_workspace_size(self._descs, self.n_layers, ctypes.byref(self._hp),
+                                           self.max_rows, ctypes.byref(nbytes)),
+                   "kfac_workspace_size")
+        self.workspace_bytes = nbytes.value
         # 256-byte alignment: torch's caching allocator returns 512-byte aligned blocks
         self.workspace = torch.empty(self.workspace_bytes, dtype=torch.uint8, device=dev)
         self._h = ctypes.c_void_p()

@@ -32,7 +32,7 @@ constexpr int64_t kK5MinRows = 32;
 // Row splits of K5: enough CTAs to cover the GPU twice, at least kK5MinRows rows each.
 int64_t k5_splits(int ncols, int64_t rows) {
   const int64_t cb = cdiv(ncols, kK5Threads);
-  int64_t s = cdiv(2 * kNumSMs, cb);
+  int64_t s = cdiv(2 * num_sms(), cb);
   s = std::min<int64_t>(s, cdiv(rows, kK5MinRows));
   return std::max<int64_t>(s, 1);
 }
@@ -355,7 +355,7 @@ int64_t k6_units(const LayerInfo& L, bool vec) {
 }
 
 unsigned k6_blocks(int64_t units) {
-  return (unsigned)std::max<int64_t>(std::min<int64_t>(cdiv(units, kDiagThreads), kNumSMs), 1);
+  return (unsigned)std::max<int64_t>(std::min<int64_t>(cdiv(units, kDiagThreads), num_sms()), 1);
 }
 
 }  // namespace
@@ -414,7 +414,7 @@ kfac_status launch_diag_factors_batched(kfac_ctx* h, int count, const int* layer
     const int ncols = L.d_in + L.o;
     const int64_t cb = cdiv(ncols, kK5Threads);
     const double share = (double)rows[i] * ncols / work;   // of 2 x SMs CTAs
-    int64_t splits = (int64_t)std::ceil(2.0 * kNumSMs * share / (double)cb);
+    int64_t splits = (int64_t)std::ceil(2.0 * num_sms() * share / (double)cb);
     splits = std::max<int64_t>(1, std::min<int64_t>(splits, cdiv(rows[i], kK5MinRows)));
     const size_t need = (size_t)splits * ncols;
     if (need > h->k5part_floats || (size_t)cb > h->k5tickets_ints) return KFAC_ERR_WORKSPACE;
@@ -654,7 +654,7 @@ kfac_status launch_diag_factors_conv(kfac_ctx* h, int layer, const void* x, cons
   // image splits: about 4096 elements of a unit per CTA (16 loads per thread),
   // and at least two CTAs per SM
   const int64_t per_img = std::max<int64_t>((int64_t)cg.in_h * cg.in_w, (int64_t)ho * wo);
-  int64_t splits = std::max<int64_t>(cdiv(2 * kNumSMs, units), cdiv(cg.batch * per_img, 4096));
+  int64_t splits = std::max<int64_t>(cdiv(2 * num_sms(), units), cdiv(cg.batch * per_img, 4096));
   splits = std::max<int64_t>(1, std::min<int64_t>(splits, cg.batch));
   splits = std::max<int64_t>(1, std::min<int64_t>(splits, (int64_t)(h->k5part_floats / ncols)));
   p.imgs_per_split = (int)cdiv(cg.batch, splits);
@@ -692,33 +692,22 @@ namespace {
 
 constexpr int kStaticMaxCols = 262144;                  // d_in + d_out limit
 constexpr int kStaticMaxColBlocks = kStaticMaxCols / kK5Threads;   // 1024
-// splits * cols <= (ceil(2*SMs / blocks)) * blocks * 256 <= 2*SMs*256 + cols
-constexpr size_t kStaticScratchFloats = 2 * kNumSMs * kK5Threads + kStaticMaxCols;
+// splits * cols <= ceil(2 SMs / blocks) * blocks * 256 <= 2 SMs * 256 + cols (SMs <= kMaxSMs)
+constexpr size_t kStaticScratchFloats = 2 * kMaxSMs * kK5Threads + kStaticMaxCols;
 
 static __device__ __align__(256) float g_k5_static_part[kStaticScratchFloats];
 static __device__ __align__(256) int g_k5_static_tickets[kStaticMaxColBlocks];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_static_mutex;
-float* g_static_part_ptr[kMaxDevices] = {};
-int* g_static_tickets_ptr[kMaxDevices] = {};
-
-// Device addresses of the static arrays on the current device, looked up once
-// per device (the names above are host-side stand-ins, not device addresses).
+// Device addresses of the static arrays on the current device.  The names above
+// are host-side stand-ins, not device addresses; the lookup is a cheap host call,
+// made on every call so that no address outlives the context it came from.
 kfac_status static_scratch(float** part, int** tickets) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KFAC_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_static_mutex);
-  if (!g_static_part_ptr[dev]) {
-    void* p = nullptr;
-    void* t = nullptr;
-    if (cudaGetSymbolAddress(&p, g_k5_static_part) != cudaSuccess) return KFAC_ERR_CUDA;
-    if (cudaGetSymbolAddress(&t, g_k5_static_tickets) != cudaSuccess) return KFAC_ERR_CUDA;
-    g_static_part_ptr[dev] = static_cast<float*>(p);
-    g_static_tickets_ptr[dev] = static_cast<int*>(t);
-  }
-  *part = g_static_part_ptr[dev];
-  *tickets = g_static_tickets_ptr[dev];
+  void* p = nullptr;
+  void* t = nullptr;
+  if (cudaGetSymbolAddress(&p, g_k5_static_part) != cudaSuccess) return KFAC_ERR_CUDA;
+  if (cudaGetSymbolAddress(&t, g_k5_static_tickets) != cudaSuccess) return KFAC_ERR_CUDA;
+  *part = static_cast<float*>(p);
+  *tickets = static_cast<int*>(t);
   return KFAC_OK;
 }
 
@@ -748,7 +737,9 @@ extern "C" kfac_status kfac_diag_factors_static(const void* a, int64_t lda, cons
   p.ldg = ldg;
   p.rows = rows;
   const int ncols = d_in + d_out;
-  const int64_t sp = k5_splits(ncols, rows);
+  // the row splits fill the GPU twice over, within what the static array holds
+  const int64_t sp = std::max<int64_t>(
+      1, std::min<int64_t>(k5_splits(ncols, rows), (int64_t)(kStaticScratchFloats / ncols)));
   p.rows_per_split = cdiv(rows, sp);
   p.splits = (int)cdiv(rows, p.rows_per_split);
   p.d_in = d_in;

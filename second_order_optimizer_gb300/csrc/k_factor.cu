@@ -147,7 +147,6 @@ kfac_status launch_syrk_simt_grouped(const SyrkJob* d_jobs, int njobs, int max_t
 }
 
 namespace {
-constexpr int kTargetCtas = 2 * kNumSMs;
 constexpr int64_t kMaxRowsPerSplit = 8192;
 constexpr int64_t kMinRowsPerSplit = 256;
 }  // namespace
@@ -158,7 +157,7 @@ constexpr int64_t kMinRowsPerSplit = 256;
 static int64_t split_count_before_rounding(int n, int64_t rows) {
   int nt = (int)cdiv(n, SyrkTile::BM);
   int64_t tiles = (int64_t)nt * (nt + 1) / 2;
-  int64_t s = cdiv(kTargetCtas, tiles);
+  int64_t s = cdiv(2 * num_sms(), tiles);   // two CTAs per SM
   s = std::min<int64_t>(s, std::max<int64_t>(1, rows / kMinRowsPerSplit));
   s = std::max<int64_t>(s, cdiv(rows, kMaxRowsPerSplit));
   return std::max<int64_t>(s, 1);

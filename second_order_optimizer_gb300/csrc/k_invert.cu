@@ -452,7 +452,7 @@ kfac_status launch_outer_update(kfac_ctx* h, int j0, int nj, int K0, int W, cuda
   int64_t max_elems = 0;
   auto flush = [&]() -> kfac_status {
     if (pr.empty()) return KFAC_OK;
-    const unsigned blocks = (unsigned)std::min<int64_t>(cdiv(max_elems, 256), 4 * kNumSMs);
+    const unsigned blocks = (unsigned)std::min<int64_t>(cdiv(max_elems, 256), 4 * num_sms());
     launch_pdl(panel_split_kernel, dim3(dim3(blocks, pg.count)), dim3(256), 0, st, pg);
     count_launch();
     kfac_status e = check_launch();

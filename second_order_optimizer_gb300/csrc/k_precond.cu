@@ -88,7 +88,7 @@ kfac_status launch_precondition(kfac_ctx* h, int layer, const float* gw, int64_t
   float* x_lo = x_hi + (size_t)L.n * op;
   {
     const int64_t total = (int64_t)L.o * L.n;
-    const unsigned blocks = (unsigned)std::min<int64_t>(cdiv(total, 256), 4 * kNumSMs);
+    const unsigned blocks = (unsigned)std::min<int64_t>(cdiv(total, 256), 4 * num_sms());
     launch_pdl(gradhat_pack_kernel, dim3(blocks), dim3(256), 0, st, gw, ldgw, gb, L.o, L.d_in, L.n, np, g_hi, g_lo);
     count_launch();
     if (kfac_status e = check_launch()) return e;
@@ -137,7 +137,7 @@ kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layer
   size_t used = 0;  // floats
   auto flush = [&]() -> kfac_status {
     if (ng == 0) return KFAC_OK;
-    const unsigned blocks = (unsigned)std::min<int64_t>(cdiv(max_elems, 256), 4 * kNumSMs);
+    const unsigned blocks = (unsigned)std::min<int64_t>(cdiv(max_elems, 256), 4 * num_sms());
     launch_pdl(gradhat_pack_grouped_kernel, dim3(dim3(blocks, ng)), dim3(256), 0, st, gp);
     count_launch();
     kfac_status e = check_launch();

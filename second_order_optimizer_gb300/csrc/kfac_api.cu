@@ -10,6 +10,22 @@
 namespace kfac {
 
 static std::atomic<unsigned long long> g_launches{0};
+
+int num_sms() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev];   // 0: not queried yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
+  if (dev < kMaxDev) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1)
+    v = 1;
+  if (dev < kMaxDev) cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
 void count_launch(int n) { g_launches.fetch_add((unsigned long long)n); }
 kfac_status check_launch() {
   return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
@@ -107,7 +123,7 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, const kfa
         inv_pack_sum += align_up(tc_pack_bytes(L.o, L.o, false));
       }
       pack_sum += align_up(tc_pack_bytes(L.n, max_rows, bf)) + align_up(tc_pack_bytes(L.o, max_rows, bf));
-      tickets = std::max({tickets, t1, t2, (size_t)16 * kNumSMs});   // split-K: tile x cluster rank
+      tickets = std::max({tickets, t1, t2, (size_t)16 * num_sms()});   // split-K: tile x cluster rank
       k4 = std::max(k4, 2 * o * np + 2 * n * op);
       // batched K4 aligns each of its four arrays (dW-hat and X^T halves) separately
       k4_sum += 2 * (align_up(o * np * sizeof(float)) + align_up(n * op * sizeof(float))) /
@@ -138,7 +154,7 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, const kfa
   P->k4tmp_floats = k4;
   P->off_k4tmp = take(k4 * sizeof(float));
   // batched K5 spreads about 2 x SMs CTAs over the group, one part row per CTA
-  k5 = std::max(k5, (size_t)256 * (2 * kNumSMs + k5t));
+  k5 = std::max(k5, (size_t)256 * (2 * num_sms() + k5t));
   P->k5part_floats = k5;
   P->off_k5part = take(k5 * sizeof(float));
   P->off_k5tickets = take(k5t * sizeof(int));

@@ -10,7 +10,12 @@
 
 namespace kfac {
 
-constexpr int kNumSMs = 152;           // GB300: 2 dies x 76 SMs
+// Multiprocessor count of the current device (queried once per device).  Grids,
+// split counts and the workspace plan are sized from it.
+int num_sms();
+// Bound on the SM count for the one statically sized scratch array
+// (kfac_diag_factors_static).
+constexpr int kMaxSMs = 256;
 constexpr int kTcInverseMinN = 512;    // inverse assembly X^T X on the tensor cores from this n
 constexpr size_t kAlign = 256;
 

@@ -1344,7 +1344,7 @@ size_t tc_pack_bytes(int n, int64_t max_rows, bool bf16) {
   return (size_t)n * Kp * (bf16 ? 2 : 8);
 }
 
-size_t tc_part_floats() { return (size_t)kNumSMs * 128 * 256; }
+size_t tc_part_floats() { return (size_t)num_sms() * 128 * 256; }
 
 // Split-K shape for `s` wanted splits of a reduction of length K: clusters of
 // csize = min(8, s) splits (the portable cluster size) times `groups` cluster
@@ -1381,6 +1381,7 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
                            const TcOperand& B, bool same_ab, bool upper, int64_t M, int64_t N,
                            int64_t K, const TcEpilogue& e, cudaStream_t st) {
   constexpr int BM = 128;
+  const int sms = num_sms();
   // Tile width: 128 x 256 halves the shared-memory traffic per MMA flop of
   // 128 x 128, which pays on long reductions or when there are tiles enough to
   // fill the GPU; short, small products keep 128 x 128 for parallelism.
@@ -1388,11 +1389,11 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
     const int tm = (int)cdiv(M, BM), tn = (int)cdiv(N, bn);
     return upper ? upper_tile_count(tm, tn, bn / BM) : (int64_t)tm * tn;
   };
-  const int BN = ((bf16 && K >= 8192) || count(256) >= kNumSMs) ? 256 : 128;
+  const int BN = ((bf16 && K >= 8192) || count(256) >= sms) ? 256 : 128;
   // With at least a wave of tiles and no split-K, neighbouring tiles of one
   // column run as a cluster pair that loads the shared B tile once: each CTA
   // fetches half of its rows and multicasts them to both.
-  const bool mc = count(BN) >= kNumSMs;
+  const bool mc = count(BN) >= sms;
   const int b_box = mc ? BN / 2 : BN;
   CUtensorMap ah, al, bh, bl;
   if (!make_map(&ah, A.hi, bf16, A.rows, K, A.pitch, BM)) return KFAC_ERR_CUDA;
@@ -1423,14 +1424,14 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
   // epilogue, reduction: ~8 us measured) relative to the tile's whole main loop
   // at the tensor rate of one SM.
   int64_t want = 1;
-  if (tiles < kNumSMs) {
-    const double sm_rate = (bf16 ? 2.25e15 : 1.1e15 / 3.0) / kNumSMs;   // flop/s per SM
+  if (tiles < sms) {
+    const double sm_rate = (bf16 ? 2.25e15 : 1.1e15 / 3.0) / sms;   // flop/s per SM
     const double t_tile = 2.0 * BM * BN * (double)K / sm_rate;          // seconds
     const double c0 = 8e-6 / t_tile;
     double best = 1.0 + c0;
-    const int64_t smax = std::max<int64_t>(1, std::min<int64_t>(K / 256, 4 * kNumSMs));
+    const int64_t smax = std::max<int64_t>(1, std::min<int64_t>(K / 256, 4 * sms));
     for (int64_t sp = 2; sp <= smax; ++sp) {
-      const double cost = (double)cdiv(tiles * sp, kNumSMs) * (1.0 / (double)sp + c0);
+      const double cost = (double)cdiv(tiles * sp, sms) * (1.0 / (double)sp + c0);
       if (cost < best - 1e-12) {
         best = cost;
         want = sp;
@@ -1463,7 +1464,7 @@ kfac_status launch_persistent_kernel(const GroupedTc& g, cudaStream_t st) {
                                              (int)PersistCfg<kBF16>::SMEM) == cudaSuccess;
   if (!attr_ok) return KFAC_ERR_CUDA;
   const int total = g.block_start[g.count];
-  const unsigned grid = (unsigned)std::min<int>(total, kNumSMs);
+  const unsigned grid = (unsigned)std::min<int>(total, num_sms());
   launch_pdl(gemm_tc_persistent_kernel<kBF16, EPI>, dim3(grid), dim3(TcCfg<kBF16, 128>::THREADS),
              PersistCfg<kBF16>::SMEM, st, g);
   count_launch();
@@ -1512,6 +1513,7 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
   }
   constexpr int BM = 128, BN = 128;
   constexpr size_t NT = (size_t)BM * BN;
+  const int sms = num_sms();
   const int unit = bf16 ? kKsubBf16 : kKsubTf32;
   // A product that fills a wave of 128 x 256 tiles by itself runs on its own
   // (wide tiles, multicast pairs); the rest share grouped launches.
@@ -1520,7 +1522,7 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
     const TcProblem& pr = probs[q];
     const int tm = (int)cdiv(pr.M, BM), tn = (int)cdiv(pr.N, 256);
     const int64_t wide = pr.upper ? upper_tile_count(tm, tn, 2) : (int64_t)tm * tn;
-    if (wide >= kNumSMs) {
+    if (wide >= sms) {
       if (kfac_status e = launch_gemm_tc(h, pr.layer, bf16, epi, pr.A, pr.B, pr.same_ab, pr.upper,
                                          pr.M, pr.N, pr.K, pr.e, st))
         return e;
@@ -1539,7 +1541,7 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
     total_units += tiles[q] * cdiv(pr.K, unit);
   }
   // k-steps per CTA if the whole group were spread over one wave
-  const int64_t chunk = std::max<int64_t>(2, cdiv(total_units, kNumSMs));
+  const int64_t chunk = std::max<int64_t>(2, cdiv(total_units, sms));
   for (int q = 0; q < count; ++q)
     want[q] = std::max<int64_t>(1, cdiv(cdiv(probs[q].K, unit), chunk));
   std::unique_ptr<GroupedTc> g(new GroupedTc());
