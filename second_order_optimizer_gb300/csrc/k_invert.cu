@@ -28,6 +28,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <memory>
 #include <vector>
 
 namespace kfac {
@@ -37,6 +38,7 @@ namespace {
 constexpr int NB = 64;
 constexpr int kOuterW = 512;      // outer panel width of the two-level Cholesky
 constexpr int kOuterMaxN = 1536;  // handles whose factors are all this small stay one panel
+constexpr int kTcLevelMin = 512;  // doubling levels of this block size and wider: tensor cores
 using PTile = SimtTile<64, 64, 32, 4, 4>;   // 256 threads, 32-deep k chunks
 
 __global__ void __launch_bounds__(256) inv_prep_kernel(const InvJob* jobs, float sqrt_gamma) {
@@ -250,17 +252,6 @@ __global__ void __launch_bounds__(256) chol_panel_kernel(const InvJob* jobs, int
     }
 }
 
-__device__ __forceinline__ void lower_tile_coords(int t, int* ti, int* tj) {
-  // t enumerates (ti, tj) with tj <= ti row by row: (0,0), (1,0), (1,1), (2,0), ...
-  int r = 0;
-  while (t > r) {
-    t -= r + 1;
-    ++r;
-  }
-  *ti = r;
-  *tj = t;
-}
-
 // L[i][j] -= sum_t L[i][k+t] L[j][k+t] over the trailing lower tiles (ti >= tj,
 // counted from the first trailing block), for block columns below `cend` (the
 // end of the current outer panel; the tensor cores update the rest).  part: 1
@@ -422,6 +413,64 @@ __global__ void __launch_bounds__(256) inv_split_kernel(const InvJob* jobs) {
   }
 }
 
+// Operands of the tensor-core doubling levels: blocks of L and X split into TF32
+// halves, dst[r][c] (row pitch dp) = src[r][c], or src[c][r] for a transposed
+// block.  One CTA moves a 32 x 32 tile through shared memory (loads and stores
+// both coalesced).
+struct BlockPack {
+  const float* src;   // block origin, row pitch ld
+  int64_t ld;
+  float* hi;
+  float* lo;
+  int64_t dp;
+  int rows, cols;     // of the destination block
+  int trans;          // 1: dst[r][c] = src[c * ld + r]
+};
+constexpr int kMaxBlockPacks = 192;
+struct BlockPackGroup {
+  BlockPack job[kMaxBlockPacks];
+  int tile_start[kMaxBlockPacks + 1];
+  int count;
+};
+
+__global__ void __launch_bounds__(256) block_pack_kernel(const __grid_constant__ BlockPackGroup g) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float t[32][33];
+  const int b = blockIdx.x;
+  int q = 0;
+  while (q + 1 < g.count && b >= g.tile_start[q + 1]) ++q;
+  const BlockPack J = g.job[q];
+  const int local = b - g.tile_start[q];
+  const int tcols = (J.cols + 31) / 32;
+  const int tr = local / tcols, tcl = local % tcols;   // destination tile
+  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int i = ty + 8 * u;
+    float v = 0.f;
+    if (!J.trans) {   // source row i of the tile = destination row i
+      const int r = tr * 32 + i, c = tcl * 32 + tx;
+      if (r < J.rows && c < J.cols) v = J.src[(int64_t)r * J.ld + c];
+      t[i][tx] = v;
+    } else {          // source row i of the tile = destination column i
+      const int r = tr * 32 + tx, c = tcl * 32 + i;
+      if (r < J.rows && c < J.cols) v = J.src[(int64_t)c * J.ld + r];
+      t[tx][i] = v;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int r = tr * 32 + ty + 8 * u, c = tcl * 32 + tx;
+    if (r >= J.rows || c >= J.cols) continue;
+    const float v = t[ty + 8 * u][tx];
+    const float hi = tc::to_tf32(v);
+    J.hi[(int64_t)r * J.dp + c] = hi;
+    J.lo[(int64_t)r * J.dp + c] = tc::to_tf32(v - hi);
+  }
+}
+
 int level_tiles_host(int n, int s) {
   int total = 0;
   for (int p = 0;; ++p) {
@@ -436,6 +485,108 @@ int level_tiles_host(int n, int s) {
 }  // namespace
 
 size_t inv_y_floats(int n) { return (size_t)n * n; }
+
+// One doubling level on the tensor cores, for every factor with pairs at this
+// level (pair (T, B): T = [t0, t0 + s), B = [b0, b1), b0 = t0 + s):
+//   Y^T  = (L_BT X_TT)^T         product 1: A = L_BT, B = X_TT^T, K = s; stored as
+//                                TF32 halves (the next product's operand)
+//   X_BT = -(Y^T X_BB^T)^T        product 2: A = Y^T, B = X_BB, K = |B|; stored as
+//                                fp32 straight into X (transposed store, alpha = -1)
+// The operand blocks (L_BT, X_TT^T, X_BB as TF32 halves) are packed first.
+// Scratch per factor: L_BT and Y^T halves in its Y buffer (n^2 floats), X_TT^T
+// and X_BB halves in its inverse halves (n x np each, written only after the
+// levels).  Returns KFAC_ERR_WORKSPACE, before any launch, when a factor's
+// blocks do not fit: the caller then runs the level on the CUDA cores.
+kfac_status launch_tri_level_tc(kfac_ctx* h, int j0, int nj, int s, cudaStream_t st) {
+  struct PairOps {
+    BlockPack lbt, xtt, xbb;
+    TcProblem p1, p2;
+  };
+  std::vector<PairOps> ops;
+  auto al = [](size_t f) { return (f + 31) / 32 * 32; };   // 128-byte aligned sub-buffers
+  for (int i = j0; i < j0 + nj; ++i) {
+    const InvJob& J = h->invjobs_host[i];
+    const int n = J.n;
+    size_t yoff = 0, foff = 0;
+    for (int p = 0;; ++p) {
+      const int t0 = 2 * p * s, b0 = t0 + s;
+      if (b0 >= n) break;
+      const int b1 = std::min(b0 + s, n), mb = b1 - b0;
+      const int64_t mbp = tc_pitch(mb, false);
+      float* lbt_hi = J.Y + yoff;
+      float* lbt_lo = lbt_hi + al((size_t)mb * s);
+      float* yt_hi = lbt_lo + al((size_t)mb * s);
+      float* yt_lo = yt_hi + al((size_t)s * mbp);
+      yoff += 2 * al((size_t)mb * s) + 2 * al((size_t)s * mbp);
+      float* xtt_hi = J.Finv_hi + foff;
+      float* xtt_lo = J.Finv_lo + foff;
+      float* xbb_hi = xtt_hi + al((size_t)s * s);
+      float* xbb_lo = xtt_lo + al((size_t)s * s);
+      foff += al((size_t)s * s) + al((size_t)mb * mbp);
+      if (yoff > inv_y_floats(n) || foff > (size_t)n * J.np) return KFAC_ERR_WORKSPACE;
+      PairOps o{};
+      o.lbt = BlockPack{J.L + (int64_t)b0 * n + t0, n, lbt_hi, lbt_lo, s, mb, s, 0};
+      o.xtt = BlockPack{J.X + (int64_t)t0 * n + t0, n, xtt_hi, xtt_lo, s, s, s, 1};
+      o.xbb = BlockPack{J.X + (int64_t)b0 * n + b0, n, xbb_hi, xbb_lo, mbp, mb, mb, 0};
+      o.p1.A = TcOperand{lbt_hi, lbt_lo, mb, s};
+      o.p1.B = TcOperand{xtt_hi, xtt_lo, s, s};
+      o.p1.M = mb;
+      o.p1.N = s;
+      o.p1.K = s;
+      o.p1.e.out_hi = yt_hi;
+      o.p1.e.out_lo = yt_lo;
+      o.p1.e.ldo = mbp;
+      o.p1.layer = J.layer;
+      o.p1.kmode = 1;   // X_TT lower: column c sums over t >= c
+      o.p2.A = TcOperand{yt_hi, yt_lo, s, mbp};
+      o.p2.B = TcOperand{xbb_hi, xbb_lo, mb, mbp};
+      o.p2.M = s;
+      o.p2.N = mb;
+      o.p2.K = mb;
+      o.p2.e.out_hi = J.X + (int64_t)b0 * n + t0;
+      o.p2.e.out_lo = nullptr;
+      o.p2.e.ldo = n;
+      o.p2.e.alpha = -1.f;
+      o.p2.layer = J.layer;
+      o.p2.kmode = 2;   // X_BB lower: column r sums over t <= r
+      ops.push_back(o);
+    }
+  }
+  if (ops.empty()) return KFAC_OK;
+  // packs, in launches of up to kMaxBlockPacks blocks
+  std::unique_ptr<BlockPackGroup> g(new BlockPackGroup());
+  std::memset(g.get(), 0, sizeof(BlockPackGroup));
+  int tiles = 0;
+  auto flush = [&]() -> kfac_status {
+    if (g->count == 0) return KFAC_OK;
+    g->tile_start[g->count] = tiles;
+    launch_pdl(block_pack_kernel, dim3((unsigned)tiles), dim3(256), 0, st, *g);
+    count_launch();
+    std::memset(g.get(), 0, sizeof(BlockPackGroup));
+    tiles = 0;
+    return check_launch();
+  };
+  auto add = [&](const BlockPack& b) -> kfac_status {
+    if (g->count == kMaxBlockPacks)
+      if (kfac_status e = flush()) return e;
+    g->job[g->count] = b;
+    g->tile_start[g->count] = tiles;
+    tiles += (int)(cdiv(b.rows, 32) * cdiv(b.cols, 32));
+    ++g->count;
+    return KFAC_OK;
+  };
+  std::vector<TcProblem> p1, p2;
+  for (const PairOps& o : ops) {
+    for (const BlockPack* b : {&o.lbt, &o.xtt, &o.xbb})
+      if (kfac_status e = add(*b)) return e;
+    p1.push_back(o.p1);
+    p2.push_back(o.p2);
+  }
+  if (kfac_status e = flush()) return e;
+  if (kfac_status e = launch_gemm_tc_grouped(h, false, TC_EPI_SPLIT, p1.data(), (int)p1.size(), st))
+    return e;
+  return launch_gemm_tc_grouped(h, false, TC_EPI_SPLIT, p2.data(), (int)p2.size(), st);
+}
 
 // L22 <- L22 - P P^T for every factor whose size reaches past the outer panel
 // [K0, K0 + W): P = L[K0 + W :, K0 : K0 + W] split into TF32 halves, then one
@@ -582,6 +733,11 @@ kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
   }
   if (kfac_status e = join_side()) return e;
   for (int s = NB; s < nmax; s *= 2) {
+    if (s >= kTcLevelMin) {   // the wide levels on the tensor cores
+      kfac_status e = launch_tri_level_tc(h, j0, nj, s, st);
+      if (e == KFAC_OK) continue;
+      if (e != KFAC_ERR_WORKSPACE) return e;
+    }
     const int tiles = level_tiles_host(nmax, s);
     int tmax = tiles;
     for (int i = j0; i < j0 + nj; ++i) tmax = std::max(tmax, level_tiles_host(h->invjobs_host[i].n, s));
@@ -603,7 +759,7 @@ kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
   for (int i = j0; i < j0 + nj; ++i) {
     const InvJob& J = h->invjobs_host[i];
     if (J.n < kTcInverseMinN) continue;
-    big.push_back(SyrkSpec{J.X, J.n, J.n, J.n, J.n, J.layer, 1.f, 0.f, J.Finv});
+    big.push_back(SyrkSpec{J.X, J.n, J.n, J.n, J.n, J.layer, 1.f, 0.f, J.Finv, 1});   // X lower
   }
   if (!big.empty())
     if (kfac_status e = launch_syrk_tc_batched(h, big.data(), (int)big.size(), st)) return e;

@@ -215,7 +215,7 @@ struct TcEpilogue {
   float* C;
   int64_t ldc;
   float* out_hi;         // SPLIT: C^T stored as TF32 halves, out[c * ldo + r]
-  float* out_lo;
+  float* out_lo;         //   (null: alpha C^T stored as fp32 in out_hi)
   int64_t ldo;
   int d_in;              // PRECOND: C = P^T (n x o): C[j][i] = P[i][j]; j >= d_in is the bias
   float eta, mu, lambda;
@@ -223,7 +223,7 @@ struct TcEpilogue {
 };
 kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcOperand& A,
                            const TcOperand& B, bool same_ab, bool upper, int64_t M, int64_t N,
-                           int64_t K, const TcEpilogue& e, cudaStream_t st);
+                           int64_t K, const TcEpilogue& e, cudaStream_t st, int kmode = 0);
 // One product of a grouped launch.
 struct TcProblem {
   TcOperand A, B;
@@ -231,6 +231,9 @@ struct TcProblem {
   int64_t M, N, K;
   TcEpilogue e;
   int layer;
+  // reduction range per output tile, for products with a triangular operand:
+  // 0 all of K; 1 k >= the tile's first column; 2 k < the tile's last column + 1
+  int kmode;
 };
 kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProblem* probs,
                                    int count, cudaStream_t st);
@@ -270,6 +273,7 @@ struct SyrkSpec {
   int d, n, layer;
   float alpha, beta;
   float* F;
+  int kmode;   // TcProblem::kmode (1: x lower triangular, n x n)
 };
 kfac_status launch_syrk_tc_batched(kfac_ctx* h, const SyrkSpec* specs, int count, cudaStream_t st);
 size_t inv_y_floats(int n);

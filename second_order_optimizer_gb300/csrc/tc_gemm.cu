@@ -4,7 +4,8 @@
 //   with one of three fused epilogues:
 //     SYRK     F <- beta F + alpha C on tiles on/above the diagonal, plus mirrors (K1,
 //              with A = B = X = x-hat^T)
-//     SPLIT    store C^T as TF32 halves (hi, lo), ready to be the next product's operand
+//     SPLIT    store C^T as TF32 halves (hi, lo), ready to be the next product's operand;
+//              with no lo buffer, alpha C^T as fp32
 //     PRECOND  P^T = C; optional momentum / weight-decay / lr update of W in place (K4)
 //
 // Osawa et al., "Large-Scale Distributed Second-Order Optimization Using
@@ -85,6 +86,7 @@ struct GemmTcParams {
   int csize;             // splits per thread-block cluster, reduced through DSMEM (1: none)
   int mc;                // cluster pairs share the B tile by TMA multicast (no split-K)
   int64_t k_per_split;   // multiple of ksub
+  int kmode;             // reduction range per tile (TcProblem::kmode)
   int ksub;              // k elements per TMEM drain (multiple of BK)
   float* part;           // this product's cluster partials [tile][groups][BM][BN]
   int* tickets;          // this product's tickets [tile][csize]
@@ -138,6 +140,19 @@ __device__ __forceinline__ void upper_tile(int t, int tiles_m, int R, int* ti, i
   }
   *ti = t;
   *tj = j;
+}
+
+// Reduction range of a tile whose columns start at c0 (width bn), for products
+// with a triangular operand: kmode 0 the whole [0, K); 1 k >= c0 (the operand
+// that carries the output column is zero for k below it, as a lower-triangular
+// X in X^T X); 2 k < c0 + bn (zero for k past the column, as a lower-triangular
+// right factor stored row-major).  c0 is a multiple of every k-block.
+__host__ __device__ inline void k_range(int kmode, int64_t K, int64_t c0, int bn, int64_t* klo,
+                                        int64_t* khi) {
+  *klo = 0;
+  *khi = K;
+  if (kmode == 1) *klo = c0 < K ? c0 : K;
+  else if (kmode == 2) *khi = c0 + bn < K ? c0 + bn : K;
 }
 
 // One output tile (and one k-split of it).
@@ -204,8 +219,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
   pdl_wait();
   pdl_trigger();
 
-  const int64_t kbeg = (int64_t)split * p.k_per_split;
-  const int64_t kend = min(p.K, kbeg + p.k_per_split);
+  int64_t kbeg = (int64_t)split * p.k_per_split;
+  int64_t kend = min(p.K, kbeg + p.k_per_split);
+  {   // structurally zero parts of the reduction (triangular operands) are skipped
+    int64_t klo, khi;
+    k_range(p.kmode, p.K, (int64_t)tj * C::BN, C::BN, &klo, &khi);
+    kbeg = max(kbeg, klo);
+    kend = min(kend, khi);
+  }
   const int nkb = kend > kbeg ? (int)((kend - kbeg + C::BK - 1) / C::BK) : 0;
   const int kb_per_sub = p.ksub / C::BK;
   const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
@@ -410,13 +431,21 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
           if (ok) E.C[gc * E.ldc + gr] = v;
         }
       } else if (EPI == TC_EPI_SPLIT) {
+        if (E.out_lo) {
 #pragma unroll
-        for (int c = 0; c < C::CW; ++c) {
-          const int64_t gc = c0 + h * C::CW + c;
-          if (gc >= pN) continue;
-          const float hi = tc::to_tf32(sum[c]);
-          E.out_hi[gc * E.ldo + gr] = hi;
-          E.out_lo[gc * E.ldo + gr] = tc::to_tf32(sum[c] - hi);
+          for (int c = 0; c < C::CW; ++c) {
+            const int64_t gc = c0 + h * C::CW + c;
+            if (gc >= pN) continue;
+            const float hi = tc::to_tf32(sum[c]);
+            E.out_hi[gc * E.ldo + gr] = hi;
+            E.out_lo[gc * E.ldo + gr] = tc::to_tf32(sum[c] - hi);
+          }
+        } else {   // alpha C^T as fp32
+#pragma unroll
+          for (int c = 0; c < C::CW; ++c) {
+            const int64_t gc = c0 + h * C::CW + c;
+            if (gc < pN) E.out_hi[gc * E.ldo + gr] = E.alpha * sum[c];
+          }
         }
       } else {  // PRECOND: row gr = column j of P, column gc = row i
         const bool wcol = gr < E.d_in;
@@ -621,6 +650,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
       const int64_t gr = r0 + r, gc = c0 + c;
       if (gr >= pM || gc >= pN) continue;
       const float v = T[r * C::TPAD + c];
+      if (!E.out_lo) {   // alpha C^T as fp32
+        E.out_hi[gc * E.ldo + gr] = E.alpha * v;
+        continue;
+      }
       const float hi = tc::to_tf32(v);
       E.out_hi[gc * E.ldo + gr] = hi;
       E.out_lo[gc * E.ldo + gr] = tc::to_tf32(v - hi);
@@ -787,7 +820,13 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
   pdl_trigger();
   auto a_ptr = [&](int s, int lo) { return smem + (size_t)s * C::STAGE_BYTES + lo * C::HALF_BYTES; };
   auto b_ptr = [&](int s, int lo) { return a_ptr(s, lo) + C::A_BYTES; };
-  auto nkb_of = [&](int q) { return (int)((g.prob[q].K + C::BK - 1) / C::BK); };
+  // k-blocks of tile (q, tj): [kb_lo, kb_lo + nkb) (TcProblem::kmode)
+  auto kblocks = [&](int q, int tj, int* kb_lo) {
+    int64_t klo, khi;
+    k_range(g.prob[q].kmode, g.prob[q].K, (int64_t)tj * C::BN, C::BN, &klo, &khi);
+    *kb_lo = (int)(klo / C::BK);
+    return khi > klo ? (int)((khi - klo + C::BK - 1) / C::BK) : 0;
+  };
   const int kb_per_sub = g.prob[0].ksub / C::BK;
 
   if (warp == 0) {
@@ -801,7 +840,8 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
         const CUtensorMap* m = &g.maps[4 * q];
         const bool a_in_b = g.prob[q].same_ab && ti == tj;
         const uint32_t bytes = (a_in_b ? C::B_BYTES : C::HALF_BYTES) * (kBF16 ? 1 : 2);
-        const int nkb = nkb_of(q);
+        int kb_lo;
+        const int nkb = kblocks(q, tj, &kb_lo);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
             *abort_flag = 1;
@@ -809,7 +849,7 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
             ok = false;
             break;
           }
-          const int k0 = kb * C::BK;
+          const int k0 = (kb_lo + kb) * C::BK;
           tc::mbar_expect_tx(&full[stage], bytes);
           if (!a_in_b) tc::tma_load_2d(a_ptr(stage, 0), &m[0], &full[stage], k0, ti * C::BM);
           tc::tma_load_2d(b_ptr(stage, 0), &m[2], &full[stage], k0, tj * C::BN);
@@ -835,7 +875,8 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
         int q, ti, tj;
         grouped_tile(g, t, &q, &ti, &tj);
         const bool a_in_b = g.prob[q].same_ab && ti == tj;
-        const int nkb = nkb_of(q);
+        int kb_lo;
+        const int nkb = kblocks(q, tj, &kb_lo);
         const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
         for (int sub = 0; sub < nsub && ok; ++sub, ++gsub) {
           const int buf = gsub % PC::ACC, use = gsub / PC::ACC;
@@ -901,7 +942,8 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
       const int64_t pM = g.prob[q].M, pN = g.prob[q].N;
       const int64_t r0 = (int64_t)ti * C::BM, c0 = (int64_t)tj * C::BN + h * CW;
       const int64_t gr = r0 + row;
-      const int nkb = nkb_of(q);
+      int kb_lo;
+      const int nkb = kblocks(q, tj, &kb_lo);
       const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
       if (gr < pM) {   // the tile's epilogue inputs into L2 while the drains run
         if (EPI == TC_EPI_SYRK && E.beta != 0.f) {
@@ -977,7 +1019,7 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
           __syncwarp();
         }
       } else if (EPI == TC_EPI_SPLIT) {
-        if (gr < pM) {
+        if (gr < pM && E.out_lo) {
 #pragma unroll
           for (int c = 0; c < CW; ++c) {
             const int64_t gc = c0 + c;
@@ -985,6 +1027,12 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
             const float hi = tc::to_tf32(sum[c]);
             E.out_hi[gc * E.ldo + gr] = hi;
             E.out_lo[gc * E.ldo + gr] = tc::to_tf32(sum[c] - hi);
+          }
+        } else if (gr < pM) {   // alpha C^T as fp32
+#pragma unroll
+          for (int c = 0; c < CW; ++c) {
+            const int64_t gc = c0 + c;
+            if (gc < pN) E.out_hi[gc * E.ldo + gr] = E.alpha * sum[c];
           }
         }
       } else {  // PRECOND: row gr = column j of P, column gc = row i
@@ -1379,7 +1427,7 @@ kfac_status dispatch(bool bf16, int epi, unsigned grid, const CUtensorMap& ah,
 
 kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcOperand& A,
                            const TcOperand& B, bool same_ab, bool upper, int64_t M, int64_t N,
-                           int64_t K, const TcEpilogue& e, cudaStream_t st) {
+                           int64_t K, const TcEpilogue& e, cudaStream_t st, int kmode) {
   constexpr int BM = 128;
   const int sms = num_sms();
   // Tile width: 128 x 256 halves the shared-memory traffic per MMA flop of
@@ -1413,6 +1461,7 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
   p.tiles_n = (int)cdiv(N, BN);
   p.upper = upper ? 1 : 0;
   p.same_ab = same_ab ? 1 : 0;
+  p.kmode = kmode;
   const int64_t tiles = count(BN);
   // enough CTAs for one wave when the output has fewer tiles than SMs
   const int unit = bf16 ? kKsubBf16 : kKsubTf32;
@@ -1509,7 +1558,7 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
   if (count == 1) {
     const TcProblem& q = probs[0];
     return launch_gemm_tc(h, q.layer, bf16, epi, q.A, q.B, q.same_ab, q.upper, q.M, q.N, q.K,
-                          q.e, st);
+                          q.e, st, q.kmode);
   }
   constexpr int BM = 128, BN = 128;
   constexpr size_t NT = (size_t)BM * BN;
@@ -1524,7 +1573,7 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
     const int64_t wide = pr.upper ? upper_tile_count(tm, tn, 2) : (int64_t)tm * tn;
     if (wide >= sms) {
       if (kfac_status e = launch_gemm_tc(h, pr.layer, bf16, epi, pr.A, pr.B, pr.same_ab, pr.upper,
-                                         pr.M, pr.N, pr.K, pr.e, st))
+                                         pr.M, pr.N, pr.K, pr.e, st, pr.kmode))
         return e;
     } else {
       small.push_back(pr);
@@ -1606,6 +1655,7 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
       pp.tiles_n = (int)cdiv(pr.N, BN);
       pp.upper = pr.upper ? 1 : 0;
       pp.same_ab = pr.same_ab ? 1 : 0;
+      pp.kmode = pr.kmode;
       pp.splits = sh.splits;
       pp.csize = sh.csize;
       pp.k_per_split = sh.kps;
@@ -1701,6 +1751,7 @@ kfac_status launch_syrk_tc_batched(kfac_ctx* h, const SyrkSpec* specs, int count
     t.e.C = q.F;
     t.e.ldc = q.n;
     t.layer = q.layer;
+    t.kmode = q.kmode;
     pr.push_back(t);
   }
   return flush();

@@ -108,7 +108,7 @@ def test_factor_strided_input():
 # ------------------------------------------------------------------ K2/K3 inverse
 
 @pytest.mark.parametrize("n_in,o", [(0, 1), (27, 64), (63, 5), (64, 100), (128, 129), (299, 300),
-                                    (512, 65), (1100, 1030), (1600, 700)])
+                                    (512, 65), (1100, 1030), (1600, 700), (2048, 2049)])
 def test_invert_matches_oracle(n_in, o):
     """Ainv/Ginv vs the oracle's textbook Cholesky inverse of the same (GPU) factor.
     Handles with a factor above 1536 take the two-level path (512-column outer
