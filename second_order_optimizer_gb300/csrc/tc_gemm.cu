@@ -1145,16 +1145,6 @@ __device__ __forceinline__ void pack_tile(const T* __restrict__ x, int64_t ld, i
   }
 }
 
-template <typename T, bool kSplit>
-__global__ void __launch_bounds__(256) pack_kernel(const T* __restrict__ x, int64_t ld, int64_t M,
-                                                    int d, int n, int64_t Kp, void* out_hi,
-                                                    void* out_lo) {
-  pdl_wait();
-  pdl_trigger();
-  pack_tile<T, kSplit>(x, ld, M, d, n, Kp, out_hi, out_lo, (int64_t)blockIdx.x * kPackRows,
-                       blockIdx.y * 32);
-}
-
 // Gathered pack: X[c][r] for rows r of the input patches of a 2-D convolution
 // over the NCHW tensor x (column c = (channel, kernel row, kernel column), zero
 // outside the image; c = d is the ones column), or of an NCHW output gradient
@@ -1237,6 +1227,75 @@ struct PackGroup {
   int64_t block_start[kMaxPackJobs + 1];
   int count;
 };
+
+// bf16 pack of a row-major x-hat with 4-byte aligned column pairs (even ld, 4-byte
+// aligned base): a CTA moves a 64-row x 64-column tile.  Each thread loads
+// column pairs (c, c + 1) of two rows as 32-bit words, turns each 2 x 2 block
+// around with byte permutes, and the words go through shared memory (pitch 33,
+// conflict-free both ways) so that the stores, too, are 32-bit words along rows
+// of X (128 contiguous bytes per warp).
+constexpr int kPackBf2 = 64;
+__device__ __forceinline__ uint32_t bf16_bits_at(const __nv_bfloat16* x, int64_t off, int c,
+                                                 int d, int n) {
+  if (c < d) return (uint32_t)__bfloat16_as_ushort(x[off + c]);
+  return c == d && c < n ? 0x3F80u : 0u;   // the ones column (1.0), then nothing
+}
+__device__ __forceinline__ void pack_tile_bf16x2(const __nv_bfloat16* __restrict__ x, int64_t ld,
+                                                 int64_t M, int d, int n, int64_t Kp,
+                                                 __nv_bfloat16* out, int64_t r0, int c0) {
+  __shared__ uint32_t s0[32][33], s1[32][33];
+  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;   // 32 x 8
+  const int c = c0 + 2 * tx;
+  uint32_t w[8];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int64_t r = r0 + 2 * (ty + 8 * u) + e;
+      uint32_t v = 0u;
+      if (r < M) {
+        if (c + 1 < d)
+          v = __ldg(reinterpret_cast<const unsigned int*>(x + r * ld + c));
+        else
+          v = bf16_bits_at(x, r * ld, c, d, n) | (bf16_bits_at(x, r * ld, c + 1, d, n) << 16);
+      }
+      w[2 * u + e] = v;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int br = ty + 8 * u;
+    s0[tx][br] = __byte_perm(w[2 * u], w[2 * u + 1], 0x5410);   // column c, rows 2br, 2br+1
+    s1[tx][br] = __byte_perm(w[2 * u], w[2 * u + 1], 0x7632);   // column c + 1
+  }
+  __syncthreads();
+  const int64_t rr = r0 + 2 * tx;
+  if (rr >= Kp) return;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int bc = ty + 8 * u;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int cc = c0 + 2 * bc + e;
+      if (cc >= n) continue;
+      *reinterpret_cast<uint32_t*>(out + (int64_t)cc * Kp + rr) = e ? s1[bc][tx] : s0[bc][tx];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) pack_grouped_bf16x2_kernel(const __grid_constant__ PackGroup g) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t b = blockIdx.x;
+  int q = 0;
+  while (q + 1 < g.count && b >= g.block_start[q + 1]) ++q;
+  const PackJob& J = g.job[q];
+  const int64_t Kp = J.Kp, local = b - g.block_start[q], rt = (Kp + kPackBf2 - 1) / kPackBf2;
+  pack_tile_bf16x2(static_cast<const __nv_bfloat16*>(J.x), J.ld, J.M, J.d, J.n, Kp,
+                   static_cast<__nv_bfloat16*>(J.hi), (local % rt) * kPackBf2,
+                   (int)(local / rt) * kPackBf2);
+}
+
 
 // One kernel per source kind (kConv: every job of the launch is a gathered one),
 // so the row-major pack keeps its small register footprint and occupancy.
@@ -1360,16 +1419,23 @@ kfac_status launch_pack_grouped(const PackJob* jobs, int count, bool bf16, cudaS
     for (size_t c0 = 0; c0 < sel.size(); c0 += kMaxPackJobs) {
       std::memset(&g, 0, sizeof(g));
       const int cnt = (int)std::min<size_t>(kMaxPackJobs, sel.size() - c0);
+      // bf16 row-major sources whose column pairs are 4-byte aligned take the paired pack
+      bool pairs = bf16 && !conv;
+      for (int q = 0; q < cnt && pairs; ++q)
+        pairs = sel[c0 + q]->ld % 2 == 0 && (uintptr_t)sel[c0 + q]->x % 4 == 0;
       int64_t blocks = 0;
       for (int q = 0; q < cnt; ++q) {
         g.job[q] = *sel[c0 + q];
         g.block_start[q] = blocks;
-        blocks += cdiv(g.job[q].Kp, kPackRows) * cdiv(g.job[q].n, 32);
+        blocks += pairs ? cdiv(g.job[q].Kp, kPackBf2) * cdiv(g.job[q].n, kPackBf2)
+                        : cdiv(g.job[q].Kp, kPackRows) * cdiv(g.job[q].n, 32);
       }
       g.block_start[cnt] = blocks;
       g.count = cnt;
       const dim3 grid((unsigned)blocks);
-      if (bf16) {
+      if (pairs) {
+        launch_pdl(pack_grouped_bf16x2_kernel, grid, dim3(256), 0, st, g);
+      } else if (bf16) {
         if (conv)
           launch_pdl(pack_grouped_kernel<__nv_bfloat16, false, true>, grid, dim3(256), 0, st, g);
         else
@@ -1686,15 +1752,16 @@ kfac_status launch_syrk_tc(kfac_ctx* h, int layer, const void* x, int64_t ld, in
   void* hi = h->ws + h->off_tcpack;
   void* lo = bf16 ? nullptr : (void*)(h->ws + h->off_tcpack + (size_t)n * Kp * 4);
   {
-    dim3 grid((unsigned)cdiv(Kp, kPackRows), (unsigned)cdiv(n, 32));
-    if (bf16)
-      launch_pdl(pack_kernel<__nv_bfloat16, false>, grid, dim3(256), 0, st,
-                 static_cast<const __nv_bfloat16*>(x), ld, rows, d, n, Kp, hi, (void*)nullptr);
-    else
-      launch_pdl(pack_kernel<float, true>, grid, dim3(256), 0, st, static_cast<const float*>(x),
-                 ld, rows, d, n, Kp, hi, lo);
-    count_launch();
-    if (kfac_status e = check_launch()) return e;
+    PackJob j{};
+    j.x = x;
+    j.ld = ld;
+    j.M = rows;
+    j.d = d;
+    j.n = n;
+    j.Kp = Kp;
+    j.hi = hi;
+    j.lo = lo;
+    if (kfac_status e = launch_pack_grouped(&j, 1, bf16, st)) return e;
   }
   TcOperand X{hi, lo, n, Kp};
   TcEpilogue e{};

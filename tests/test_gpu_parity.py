@@ -54,6 +54,10 @@ def _dev_in(x, dtype):
 @pytest.mark.parametrize("M,d_in,o,bias,dtype", [
     (1000, 300, 200, 1, "f32"), (129, 7, 130, 0, "f32"), (5000, 64, 16, 1, "f32"),
     (1, 1, 1, 1, "f32"), (777, 257, 129, 1, "bf16"), (20000, 27, 64, 1, "f32"),
+    # bf16 column pairs: the ones column inside a pair (63 + 1), starting one (64 + 1),
+    # a G width with an odd last pair (33), a single input column, a ragged row count
+    (130, 63, 64, 1, "bf16"), (100, 64, 33, 1, "bf16"), (1000, 1, 3, 1, "bf16"),
+    (4099, 130, 7, 0, "bf16"),
 ])
 def test_factor_update_matches_oracle(M, d_in, o, bias, dtype):
     kd = K.KFAC_BF16 if dtype == "bf16" else K.KFAC_F32
@@ -93,6 +97,19 @@ def test_factor_constant_input_converges():
         h.update_factors(0, da, dg)
     Ag = to_np(h.state(0, K.KFAC_STATE_A))
     assert rel_fro(Ag, C * (1 - 0.95 ** 120)) <= 1e-5
+
+
+@pytest.mark.parametrize("width", [71, 72])
+def test_factor_strided_bf16_input(width):
+    """bf16 inputs as column slices of a wider tensor: an odd row pitch (element-wise
+    pack) and an even one (column-pair pack)."""
+    M, d_in, o = 333, 50, 21
+    h = K.Kfac([(K.KFAC_KRON, o, d_in, 1, K.KFAC_BF16)], max_rows=M, **HP)
+    big_a, big_g = _inputs(M, width, width, dtype="bf16")
+    ta, tg = _dev_in(big_a, "bf16"), _dev_in(big_g, "bf16")
+    h.update_factors(0, ta[:, :d_in], tg[:, :o])
+    assert rel_fro(to_np(h.state(0, K.KFAC_STATE_A)), 0.05 * O.factor(big_a[:, :d_in], 1)) <= 1e-5
+    assert rel_fro(to_np(h.state(0, K.KFAC_STATE_G)), 0.05 * O.factor(big_g[:, :o], 0)) <= 1e-5
 
 
 def test_factor_strided_input():
