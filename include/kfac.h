@@ -389,6 +389,11 @@ kfac_status kfac_diag_factors_static(const void* a, int64_t lda, const void* g, 
 /* Diagnostics: number of kernels this library has launched in this process. */
 unsigned long long kfac_launch_count(void);
 
+/* Diagnostics: the CUDA runtime's description of the last launch error behind a
+ * KFAC_ERR_CUDA return in this process ("no error" if there was none).  Static
+ * string; not cleared by later successful calls. */
+const char* kfac_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif

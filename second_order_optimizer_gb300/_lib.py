@@ -48,7 +48,10 @@ class Conv2dGeom(ctypes.Structure):
 class KfacError(RuntimeError):
     def __init__(self, code: int, what: str):
         self.code = code
-        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)} ({status_string(code)})")
+        msg = f"{what}: {STATUS_NAMES.get(code, code)} ({status_string(code)})"
+        if STATUS_NAMES.get(code) == "KFAC_ERR_CUDA":
+            msg += f": {LIB.kfac_last_cuda_error().decode()}"
+        super().__init__(msg)
 
 
 _vp, _i, _i64, _d, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_size_t
@@ -83,6 +86,7 @@ SIGNATURES = [
     ("kfac_destroy", _i, [_vp]),
     ("kfac_status_string", ctypes.c_char_p, [_i]),
     ("kfac_launch_count", ctypes.c_ulonglong, []),
+    ("kfac_last_cuda_error", ctypes.c_char_p, []),
     ("kfac_diag_factors_static", _i, [_vp, _i64, _vp, _i64, _i64, _i, _i, _i, _i, _d, _vp, _vp,
                                       _vp]),
 ]

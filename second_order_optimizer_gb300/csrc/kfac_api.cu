@@ -27,8 +27,13 @@ int num_sms() {
   return v;
 }
 void count_launch(int n) { g_launches.fetch_add((unsigned long long)n); }
+static std::atomic<int> g_last_cuda_error{0};
+
 kfac_status check_launch() {
-  return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) return KFAC_OK;
+  g_last_cuda_error.store((int)e);
+  return KFAC_ERR_CUDA;
 }
 
 namespace {
@@ -337,6 +342,10 @@ const char* kfac_status_string(kfac_status s) {
 }
 
 unsigned long long kfac_launch_count(void) { return g_launches.load(); }
+
+const char* kfac_last_cuda_error(void) {
+  return cudaGetErrorString((cudaError_t)g_last_cuda_error.load());
+}
 
 kfac_status kfac_workspace_size(const kfac_layer_desc* layers, int n_layers,
                                 const kfac_hparams* hp, int64_t max_rows, size_t* bytes) {

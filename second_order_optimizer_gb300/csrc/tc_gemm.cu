@@ -748,29 +748,40 @@ gemm_tc_grouped_kernel(const __grid_constant__ GroupedTc g) {
 // The grouped products without split-K, one CTA per SM looping over tiles
 // (tile t, t + gridDim.x, ...).  The TMA and MMA warps run on into the next
 // tile while the drain warps finish the previous tile's epilogue: the TMEM
-// accumulator is a ring of 4 buffers (512 columns), so the MMA can run up to
-// four drain periods ahead.  The stage buffers stay busy meanwhile, so these
-// epilogues read their global inputs straight into registers (lanes on rows,
-// coalesced; prefetched into L2 when the tile starts) and the SYRK direct half
-// is transposed through a per-warp 32 x 33 buffer.
-template <bool kBF16>
+// accumulator is a ring of 512 columns (4 buffers of 128 x 128, or 2 of 128 x 256),
+// so the MMA can run up to that many drain periods ahead.  The stage buffers
+// stay busy meanwhile, so these epilogues read their global inputs straight
+// into registers (lanes on rows, coalesced; prefetched into L2 when the tile
+// starts) and the SYRK direct half is transposed through a per-warp buffer.
+// Each drain thread holds 64 accumulator columns of one row: 8 drain warps for
+// 128-wide tiles, 16 for 256-wide ones (four per TMEM lane quarter).
+template <bool kBF16, int BN>
 struct PersistCfg {
-  using C = TcCfg<kBF16, 128>;
-  static constexpr int ACC = 4;
-  static constexpr int TMEM_COLS = ACC * 128;
-  static constexpr int XP = 33;                                   // transpose pitch
-  static constexpr int XPOSE_BYTES = C::EPI_WARPS * 32 * XP * 4;
-  static constexpr size_t SMEM = 1024 + (size_t)C::STAGES * C::STAGE_BYTES + XPOSE_BYTES + 256;
+  using C = TcCfg<kBF16, BN>;                       // operand tiles: A 128 rows, B BN rows
+  static constexpr int R = BN / 128;
+  static constexpr int EPI_WARPS = BN / 16;         // 4 per 64 columns
+  static constexpr int CW = 64;                     // accumulator columns per drain thread
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int ACC = 512 / BN;              // TMEM ring: 512 columns
+  static constexpr int TMEM_COLS = ACC * BN;
+  static constexpr int XW = BN == 128 ? 32 : 8;     // columns per transpose chunk
+  static constexpr int XP = XW + 1;                 // transpose pitch
+  static constexpr int XPOSE_BYTES = EPI_WARPS * 32 * XP * 4;
+  static constexpr int FIT = (232448 - 1024 - 256 - XPOSE_BYTES) / C::STAGE_BYTES;
+  static constexpr int STAGES = FIT < C::STAGES ? FIT : C::STAGES;
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * C::STAGE_BYTES + XPOSE_BYTES + 256;
+  static_assert(STAGES >= 2, "at least double-buffered operand stages");
   static_assert(SMEM <= 232448, "fits the per-CTA shared memory");
 };
 
+template <int R>
 __device__ __forceinline__ void grouped_tile(const GroupedTc& g, int t, int* q, int* ti, int* tj) {
   int k = 0;
   while (k + 1 < g.count && t >= g.block_start[k + 1]) ++k;
   const int local = t - g.block_start[k];
   const GemmTcParams& p = g.prob[k];
   if (p.upper) {
-    upper_tile(local, p.tiles_m, 1, ti, tj);
+    upper_tile(local, p.tiles_m, R, ti, tj);
   } else {
     *ti = local / p.tiles_n;
     *tj = local % p.tiles_n;
@@ -778,18 +789,18 @@ __device__ __forceinline__ void grouped_tile(const GroupedTc& g, int t, int* q, 
   *q = k;
 }
 
-template <bool kBF16, int EPI>
-__global__ void __launch_bounds__(TcCfg<kBF16, 128>::THREADS, 1)
-gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
-  using C = TcCfg<kBF16, 128>;
-  using PC = PersistCfg<kBF16>;
-  constexpr int CW = C::CW;   // 64 columns per drain thread
+template <bool kBF16, int EPI, int BN>
+__device__ __forceinline__ void persistent_body(const GroupedTc& g) {
+  using PC = PersistCfg<kBF16, BN>;
+  using C = typename PC::C;
+  constexpr int CW = PC::CW;
+  constexpr int STAGES = PC::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  float* xbuf = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + PC::XPOSE_BYTES);
-  uint64_t* empty = full + C::STAGES;
-  uint64_t* acc_full = empty + C::STAGES;
+  float* xbuf = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + PC::XPOSE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + PC::ACC;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + PC::ACC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -797,13 +808,13 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
   const int total = g.block_start[g.count];
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < PC::ACC; ++b) {
       tc::mbar_init(&acc_full[b], 1);
-      tc::mbar_init(&acc_empty[b], 32 * C::EPI_WARPS);
+      tc::mbar_init(&acc_empty[b], 32 * PC::EPI_WARPS);
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -823,9 +834,13 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
   // k-blocks of tile (q, tj): [kb_lo, kb_lo + nkb) (TcProblem::kmode)
   auto kblocks = [&](int q, int tj, int* kb_lo) {
     int64_t klo, khi;
-    k_range(g.prob[q].kmode, g.prob[q].K, (int64_t)tj * C::BN, C::BN, &klo, &khi);
+    k_range(g.prob[q].kmode, g.prob[q].K, (int64_t)tj * BN, BN, &klo, &khi);
     *kb_lo = (int)(klo / C::BK);
     return khi > klo ? (int)((khi - klo + C::BK - 1) / C::BK) : 0;
+  };
+  // same operand and the A rows inside the B tile: read A out of B's shared memory
+  auto a_in_b = [&](int q, int ti, int tj) {
+    return (g.prob[q].same_ab && ti / PC::R == tj) ? ti % PC::R + 1 : 0;
   };
   const int kb_per_sub = g.prob[0].ksub / C::BK;
 
@@ -836,10 +851,10 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         int q, ti, tj;
-        grouped_tile(g, t, &q, &ti, &tj);
+        grouped_tile<PC::R>(g, t, &q, &ti, &tj);
         const CUtensorMap* m = &g.maps[4 * q];
-        const bool a_in_b = g.prob[q].same_ab && ti == tj;
-        const uint32_t bytes = (a_in_b ? C::B_BYTES : C::HALF_BYTES) * (kBF16 ? 1 : 2);
+        const int aib = a_in_b(q, ti, tj);
+        const uint32_t bytes = (aib ? C::B_BYTES : C::HALF_BYTES) * (kBF16 ? 1 : 2);
         int kb_lo;
         const int nkb = kblocks(q, tj, &kb_lo);
         for (int kb = 0; kb < nkb; ++kb) {
@@ -851,13 +866,13 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
           }
           const int k0 = (kb_lo + kb) * C::BK;
           tc::mbar_expect_tx(&full[stage], bytes);
-          if (!a_in_b) tc::tma_load_2d(a_ptr(stage, 0), &m[0], &full[stage], k0, ti * C::BM);
-          tc::tma_load_2d(b_ptr(stage, 0), &m[2], &full[stage], k0, tj * C::BN);
+          if (!aib) tc::tma_load_2d(a_ptr(stage, 0), &m[0], &full[stage], k0, ti * C::BM);
+          tc::tma_load_2d(b_ptr(stage, 0), &m[2], &full[stage], k0, tj * BN);
           if (!kBF16) {
-            if (!a_in_b) tc::tma_load_2d(a_ptr(stage, 1), &m[1], &full[stage], k0, ti * C::BM);
-            tc::tma_load_2d(b_ptr(stage, 1), &m[3], &full[stage], k0, tj * C::BN);
+            if (!aib) tc::tma_load_2d(a_ptr(stage, 1), &m[1], &full[stage], k0, ti * C::BM);
+            tc::tma_load_2d(b_ptr(stage, 1), &m[3], &full[stage], k0, tj * BN);
           }
-          if (++stage == C::STAGES) {
+          if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
@@ -866,15 +881,15 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
     }
   } else if (warp == 1) {
     if (lane == 0) {  // ------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = tc::make_idesc(kBF16 ? 1 : 2, C::BM, C::BN);
+      constexpr uint32_t idesc = tc::make_idesc(kBF16 ? 1 : 2, C::BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int gsub = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         int q, ti, tj;
-        grouped_tile(g, t, &q, &ti, &tj);
-        const bool a_in_b = g.prob[q].same_ab && ti == tj;
+        grouped_tile<PC::R>(g, t, &q, &ti, &tj);
+        const int aib = a_in_b(q, ti, tj);
         int kb_lo;
         const int nkb = kblocks(q, tj, &kb_lo);
         const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
@@ -887,7 +902,7 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
             break;
           }
           tc::tc_fence_after();
-          const uint32_t d = tmem + (uint32_t)(buf * C::BN);
+          const uint32_t d = tmem + (uint32_t)(buf * BN);
           const int kb0 = sub * kb_per_sub, kb1 = min(nkb, kb0 + kb_per_sub);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!tc::mbar_wait(&full[stage], phase, abort_flag)) {
@@ -897,11 +912,13 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
               break;
             }
             tc::tc_fence_after();
-            const uint32_t a_hi = tc::smem_u32(a_in_b ? b_ptr(stage, 0) : a_ptr(stage, 0));
+            const int lo1 = kBF16 ? 0 : 1;
+            const uint32_t a_hi = tc::smem_u32(aib ? b_ptr(stage, 0) + (aib - 1) * C::A_BYTES
+                                                   : a_ptr(stage, 0));
             const uint32_t b_hi = tc::smem_u32(b_ptr(stage, 0));
-            const uint32_t a_lo = tc::smem_u32(a_in_b ? b_ptr(stage, kBF16 ? 0 : 1)
-                                                      : a_ptr(stage, kBF16 ? 0 : 1));
-            const uint32_t b_lo = tc::smem_u32(b_ptr(stage, kBF16 ? 0 : 1));
+            const uint32_t a_lo = tc::smem_u32(aib ? b_ptr(stage, lo1) + (aib - 1) * C::A_BYTES
+                                                   : a_ptr(stage, lo1));
+            const uint32_t b_lo = tc::smem_u32(b_ptr(stage, lo1));
 #pragma unroll
             for (int kk = 0; kk < C::BK / C::KMMA; ++kk) {
               const uint32_t off = kk * 32;
@@ -919,7 +936,7 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
               }
             }
             tc::umma_commit(&empty[stage]);
-            if (++stage == C::STAGES) {
+            if (++stage == STAGES) {
               stage = 0;
               phase ^= 1;
             }
@@ -930,17 +947,17 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
     }
   } else {  // ------------------------------------------------ drain + epilogue
     const int qd = warp & 3;                 // TMEM lane quarter this warp may access
-    const int h = (warp - 2) >> 2;           // column half: [CW h, CW h + CW)
+    const int h = (warp - 2) >> 2;           // column block: [CW h, CW h + CW)
     const int row = 32 * qd + lane;
     float* xb = xbuf + (warp - 2) * 32 * PC::XP;
     int gsub = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       int q, ti, tj;
-      grouped_tile(g, t, &q, &ti, &tj);
+      grouped_tile<PC::R>(g, t, &q, &ti, &tj);
       const TcEpilogue E = g.prob[q].e;   // by value (see gemm_body)
       const int64_t pM = g.prob[q].M, pN = g.prob[q].N;
-      const int64_t r0 = (int64_t)ti * C::BM, c0 = (int64_t)tj * C::BN + h * CW;
+      const int64_t r0 = (int64_t)ti * C::BM, c0 = (int64_t)tj * BN + h * CW;
       const int64_t gr = r0 + row;
       int kb_lo;
       const int nkb = kblocks(q, tj, &kb_lo);
@@ -972,13 +989,24 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
           break;
         }
         tc::tc_fence_after();
+        if (BN == 128) {
 #pragma unroll
-        for (int cc = 0; cc < CW / 32; ++cc) {
-          float v[32];
-          tc::tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) +
-                            (uint32_t)(buf * C::BN + h * CW + cc * 32), v);
+          for (int cc = 0; cc < CW / 32; ++cc) {
+            float v[32];
+            tc::tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) +
+                              (uint32_t)(buf * BN + h * CW + cc * 32), v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sum[cc * 32 + i] += v[i];
+            for (int i = 0; i < 32; ++i) sum[cc * 32 + i] += v[i];
+          }
+        } else {   // fewer registers per drain thread (16 drain warps)
+#pragma unroll
+          for (int cc = 0; cc < CW / 16; ++cc) {
+            float v[16];
+            tc::tmem_ld16(tmem + ((uint32_t)(32 * qd) << 16) +
+                              (uint32_t)(buf * BN + h * CW + cc * 16), v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sum[cc * 16 + i] += v[i];
+          }
         }
         tc::tc_fence_before();
         tc::mbar_arrive(&acc_empty[buf]);
@@ -986,35 +1014,39 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
       if (!ok) break;
       if (EPI == TC_EPI_SYRK) {
         // mirror F[gc][gr] from registers, old value from the same place
+        constexpr int EB = BN == 128 ? 16 : 8;   // loads in flight (fewer registers when wide)
 #pragma unroll
-        for (int cc = 0; cc < CW; cc += 16) {
-          float old[16];
+        for (int cc = 0; cc < CW; cc += EB) {
+          float old[EB];
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
+          for (int u = 0; u < EB; ++u) {
             const int64_t gc = c0 + cc + u;
             const bool okc = gr < pM && gc < pN && gr <= gc;
             old[u] = (okc && E.beta != 0.f) ? __ldcg(E.C + gc * E.ldc + gr) : 0.f;
           }
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
+          for (int u = 0; u < EB; ++u) {
             const int64_t gc = c0 + cc + u;
             const float v = fmaf(E.beta, old[u], E.alpha * sum[cc + u]);
             sum[cc + u] = v;
             if (gr < pM && gc < pN && gr <= gc) E.C[gc * E.ldc + gr] = v;
           }
         }
-        // direct half F[gr][gc] (gr < gc): 32 x 32 blocks transposed through the
-        // warp's buffer so that lanes run along gc
+        // direct half F[gr][gc] (gr < gc): blocks of 32 rows x XW columns turned
+        // through the warp's buffer so that lanes run along gc
+        constexpr int RPI = 32 / PC::XW;   // rows per store instruction
 #pragma unroll
-        for (int j2 = 0; j2 < CW / 32; ++j2) {
+        for (int j2 = 0; j2 < CW / PC::XW; ++j2) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) xb[lane * PC::XP + c] = sum[j2 * 32 + c];
+          for (int c = 0; c < PC::XW; ++c) xb[lane * PC::XP + c] = sum[j2 * PC::XW + c];
           __syncwarp();
-          const int64_t gcol = c0 + j2 * 32 + lane;
+          const int cl = lane % PC::XW;
+          const int64_t gcol = c0 + j2 * PC::XW + cl;
 #pragma unroll 8
-          for (int r = 0; r < 32; ++r) {
+          for (int it = 0; it < 32 / RPI; ++it) {
+            const int r = it * RPI + lane / PC::XW;
             const int64_t grr = r0 + 32 * qd + r;
-            if (grr < pM && gcol < pN && grr < gcol) E.C[grr * E.ldc + gcol] = xb[r * PC::XP + lane];
+            if (grr < pM && gcol < pN && grr < gcol) E.C[grr * E.ldc + gcol] = xb[r * PC::XP + cl];
           }
           __syncwarp();
         }
@@ -1037,12 +1069,13 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
         }
       } else {  // PRECOND: row gr = column j of P, column gc = row i
         const bool wcol = gr < E.d_in;
+        constexpr int EB = BN == 128 ? 16 : 8;
         if (gr < pM) {
 #pragma unroll
-          for (int cc = 0; cc < CW; cc += 16) {
-            float w[16], m[16];
+          for (int cc = 0; cc < CW; cc += EB) {
+            float w[EB], m[EB];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < EB; ++u) {
               const int64_t i = c0 + cc + u;
               w[u] = m[u] = 0.f;
               if (E.pw && i < pN) {
@@ -1051,7 +1084,7 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
               }
             }
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < EB; ++u) {
               const int64_t i = c0 + cc + u;
               if (i >= pN) continue;
               const float pr = sum[cc + u];
@@ -1081,6 +1114,27 @@ gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, PC::TMEM_COLS);
 }
+
+// 128-wide tiles: 320 threads; 256-wide tiles: 576 threads (18 warps, so two of
+// the four SM sub-partitions hold five warps of their 16384 registers: at most
+// 102 registers a thread, 96 in steps of 8).
+template <bool kBF16, int EPI>
+__global__ void __launch_bounds__(PersistCfg<kBF16, 128>::THREADS, 1)
+gemm_tc_persistent_kernel(const __grid_constant__ GroupedTc g) {
+  persistent_body<kBF16, EPI, 128>(g);
+}
+template <bool kBF16, int EPI>
+__global__ void __maxnreg__(96) gemm_tc_persistent_wide_kernel(const __grid_constant__ GroupedTc g) {
+  persistent_body<kBF16, EPI, 256>(g);
+}
+template <bool kBF16, int EPI, int BN>
+struct PersistKernel {
+  static constexpr auto fn = gemm_tc_persistent_kernel<kBF16, EPI>;
+};
+template <bool kBF16, int EPI>
+struct PersistKernel<kBF16, EPI, 256> {
+  static constexpr auto fn = gemm_tc_persistent_wide_kernel<kBF16, EPI>;
+};
 
 // ------------------------------------------------------------ wait self-test
 // One thread waits, through the same bounded wait as the GEMM pipeline's
@@ -1491,6 +1545,9 @@ kfac_status dispatch(bool bf16, int epi, unsigned grid, const CUtensorMap& ah,
   return launch_kernel<false, BN, TC_EPI_PRECOND>(grid, ah, al, bh, bl, p, st);
 }
 
+kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProblem* probs,
+                                   int count, cudaStream_t st);
+
 kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcOperand& A,
                            const TcOperand& B, bool same_ab, bool upper, int64_t M, int64_t N,
                            int64_t K, const TcEpilogue& e, cudaStream_t st, int kmode) {
@@ -1503,6 +1560,20 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
     const int tm = (int)cdiv(M, BM), tn = (int)cdiv(N, bn);
     return upper ? upper_tile_count(tm, tn, bn / BM) : (int64_t)tm * tn;
   };
+  if (count(256) >= sms) {   // a wave of wide tiles at least: the persistent kernel
+    TcProblem pr{};
+    pr.A = A;
+    pr.B = B;
+    pr.same_ab = same_ab;
+    pr.upper = upper;
+    pr.M = M;
+    pr.N = N;
+    pr.K = K;
+    pr.e = e;
+    pr.layer = layer;
+    pr.kmode = kmode;
+    return launch_wide_persistent(h, bf16, epi, &pr, 1, st);
+  }
   const int BN = ((bf16 && K >= 8192) || count(256) >= sms) ? 256 : 128;
   // With at least a wave of tiles and no split-K, neighbouring tiles of one
   // column run as a cluster pair that loads the shared B tile once: each CTA
@@ -1572,23 +1643,93 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
                    : dispatch<128>(bf16, epi, grid, ah, al, bh, bl, p, st);
 }
 
-template <bool kBF16, int EPI>
+template <bool kBF16, int EPI, int BN>
 kfac_status launch_persistent_kernel(const GroupedTc& g, cudaStream_t st) {
-  static bool attr_ok = cudaFuncSetAttribute(gemm_tc_persistent_kernel<kBF16, EPI>,
+  using PC = PersistCfg<kBF16, BN>;
+  static bool attr_ok = cudaFuncSetAttribute(PersistKernel<kBF16, EPI, BN>::fn,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)PersistCfg<kBF16>::SMEM) == cudaSuccess;
-  if (!attr_ok) return KFAC_ERR_CUDA;
+                                             (int)PC::SMEM) == cudaSuccess;
+  if (!attr_ok) {
+    check_launch();   // records the attribute error, if it is still pending
+    return KFAC_ERR_CUDA;
+  }
   const int total = g.block_start[g.count];
   const unsigned grid = (unsigned)std::min<int>(total, num_sms());
-  launch_pdl(gemm_tc_persistent_kernel<kBF16, EPI>, dim3(grid), dim3(TcCfg<kBF16, 128>::THREADS),
-             PersistCfg<kBF16>::SMEM, st, g);
+  launch_pdl(PersistKernel<kBF16, EPI, BN>::fn, dim3(grid), dim3(PC::THREADS), PC::SMEM, st, g);
   count_launch();
   return check_launch();
 }
 
+// k elements per TMEM drain of the 256-wide persistent bf16 products: 32 MMAs
+// (drift ~2e-6 relative per drain period), long enough that the drain warps
+// finish a tile's epilogue while the MMA runs one period ahead.
+constexpr int kKsubBf16Wide = 512;
+
+// Products that fill at least a wave of 128 x 256 tiles by themselves, no
+// split-K: persistent launches of up to kMaxGroup of them, 256-wide tiles, each
+// tile's epilogue overlapped with the next tile's main loop.
+kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProblem* probs,
+                                   int count, cudaStream_t st) {
+  constexpr int BM = 128, BN = 256;
+  const int unit = bf16 ? kKsubBf16Wide : kKsubTf32;
+  std::unique_ptr<GroupedTc> g(new GroupedTc());
+  for (int c0 = 0; c0 < count; c0 += kMaxGroup) {
+    std::memset(g.get(), 0, sizeof(GroupedTc));
+    const int cnt = std::min(kMaxGroup, count - c0);
+    int blocks = 0;
+    for (int i = 0; i < cnt; ++i) {
+      const TcProblem& pr = probs[c0 + i];
+      CUtensorMap* m = &g->maps[4 * i];
+      if (!make_map(&m[0], pr.A.hi, bf16, pr.A.rows, pr.K, pr.A.pitch, BM)) return KFAC_ERR_CUDA;
+      if (!make_map(&m[2], pr.B.hi, bf16, pr.B.rows, pr.K, pr.B.pitch, BN)) return KFAC_ERR_CUDA;
+      if (bf16) {
+        m[1] = m[0];
+        m[3] = m[2];
+      } else {
+        if (!make_map(&m[1], pr.A.lo, false, pr.A.rows, pr.K, pr.A.pitch, BM)) return KFAC_ERR_CUDA;
+        if (!make_map(&m[3], pr.B.lo, false, pr.B.rows, pr.K, pr.B.pitch, BN)) return KFAC_ERR_CUDA;
+      }
+      GemmTcParams& pp = g->prob[i];
+      pp.M = pr.M;
+      pp.N = pr.N;
+      pp.K = pr.K;
+      pp.tiles_m = (int)cdiv(pr.M, BM);
+      pp.tiles_n = (int)cdiv(pr.N, BN);
+      pp.upper = pr.upper ? 1 : 0;
+      pp.same_ab = pr.same_ab ? 1 : 0;
+      pp.kmode = pr.kmode;
+      pp.splits = 1;
+      pp.csize = 1;
+      pp.k_per_split = cdiv(pr.K, unit) * unit;
+      pp.ksub = unit;
+      pp.status = h->status();
+      pp.layer = pr.layer;
+      pp.e = pr.e;
+      g->block_start[i] = blocks;
+      blocks += (int)(pr.upper ? upper_tile_count(pp.tiles_m, pp.tiles_n, BN / BM)
+                               : (int64_t)pp.tiles_m * pp.tiles_n);
+    }
+    g->block_start[cnt] = blocks;
+    g->count = cnt;
+    g->csize = 1;
+    kfac_status e;
+    if (epi == TC_EPI_SYRK)
+      e = bf16 ? launch_persistent_kernel<true, TC_EPI_SYRK, BN>(*g, st)
+               : launch_persistent_kernel<false, TC_EPI_SYRK, BN>(*g, st);
+    else if (bf16)
+      e = KFAC_ERR_UNSUPPORTED;
+    else if (epi == TC_EPI_SPLIT)
+      e = launch_persistent_kernel<false, TC_EPI_SPLIT, BN>(*g, st);
+    else
+      e = launch_persistent_kernel<false, TC_EPI_PRECOND, BN>(*g, st);
+    if (e) return e;
+  }
+  return KFAC_OK;
+}
+
 template <bool kBF16, int EPI>
 kfac_status launch_grouped_kernel(unsigned grid, const GroupedTc& g, cudaStream_t st) {
-  if (g.csize == 1 && g.prob[0].splits == 1) return launch_persistent_kernel<kBF16, EPI>(g, st);
+  if (g.csize == 1 && g.prob[0].splits == 1) return launch_persistent_kernel<kBF16, EPI, 128>(g, st);
   static bool attr_ok = cudaFuncSetAttribute(gemm_tc_grouped_kernel<kBF16, EPI>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)TcCfg<kBF16, 128>::SMEM) == cudaSuccess;
@@ -1630,21 +1771,19 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
   constexpr size_t NT = (size_t)BM * BN;
   const int sms = num_sms();
   const int unit = bf16 ? kKsubBf16 : kKsubTf32;
-  // A product that fills a wave of 128 x 256 tiles by itself runs on its own
-  // (wide tiles, multicast pairs); the rest share grouped launches.
-  std::vector<TcProblem> small;
+  // Products that fill a wave of 128 x 256 tiles by themselves go to the wide
+  // persistent launches; the rest share grouped launches.
+  std::vector<TcProblem> small, wide_probs;
   for (int q = 0; q < count; ++q) {
     const TcProblem& pr = probs[q];
     const int tm = (int)cdiv(pr.M, BM), tn = (int)cdiv(pr.N, 256);
     const int64_t wide = pr.upper ? upper_tile_count(tm, tn, 2) : (int64_t)tm * tn;
-    if (wide >= sms) {
-      if (kfac_status e = launch_gemm_tc(h, pr.layer, bf16, epi, pr.A, pr.B, pr.same_ab, pr.upper,
-                                         pr.M, pr.N, pr.K, pr.e, st, pr.kmode))
-        return e;
-    } else {
-      small.push_back(pr);
-    }
+    (wide >= sms ? wide_probs : small).push_back(pr);
   }
+  if (!wide_probs.empty())
+    if (kfac_status e = launch_wide_persistent(h, bf16, epi, wide_probs.data(),
+                                               (int)wide_probs.size(), st))
+      return e;
   if (small.empty()) return KFAC_OK;
   if ((int)small.size() < count) return launch_gemm_tc_grouped(h, bf16, epi, small.data(), (int)small.size(), st);
   std::vector<int64_t> tiles(count), want(count);
