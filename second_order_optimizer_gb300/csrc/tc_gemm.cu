@@ -789,6 +789,114 @@ __device__ __forceinline__ void grouped_tile(const GroupedTc& g, int t, int* q, 
   *q = k;
 }
 
+// Epilogue of a drained tile from registers (the persistent kernels): this thread
+// holds accumulator row gr for the CW columns from c0.  Every store runs along
+// rows across the warp (C^T-oriented), except the SYRK direct half, which goes
+// through the warp's transpose buffer xb (32 rows x XW columns at a time).  EB
+// global loads are kept in flight.
+template <int EPI, int CW, int XW, int EB>
+__device__ __forceinline__ void epilogue_from_registers(const TcEpilogue& E, float (&sum)[CW],
+                                                        float* xb, int lane, int qd, int64_t r0,
+                                                        int64_t c0, int64_t gr, int64_t pM,
+                                                        int64_t pN) {
+  constexpr int XP = XW + 1;
+  if (EPI == TC_EPI_SYRK) {
+    // mirror F[gc][gr] from registers, old value from the same place
+#pragma unroll
+    for (int cc = 0; cc < CW; cc += EB) {
+      float old[EB];
+#pragma unroll
+      for (int u = 0; u < EB; ++u) {
+        const int64_t gc = c0 + cc + u;
+        const bool okc = gr < pM && gc < pN && gr <= gc;
+        old[u] = (okc && E.beta != 0.f) ? __ldcg(E.C + gc * E.ldc + gr) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < EB; ++u) {
+        const int64_t gc = c0 + cc + u;
+        const float v = fmaf(E.beta, old[u], E.alpha * sum[cc + u]);
+        sum[cc + u] = v;
+        if (gr < pM && gc < pN && gr <= gc) E.C[gc * E.ldc + gr] = v;
+      }
+    }
+    // direct half F[gr][gc] (gr < gc): blocks of 32 rows x XW columns turned
+    // through the warp's buffer so that lanes run along gc
+    constexpr int RPI = 32 / XW;   // rows per store instruction
+#pragma unroll
+    for (int j2 = 0; j2 < CW / XW; ++j2) {
+#pragma unroll
+      for (int c = 0; c < XW; ++c) xb[lane * XP + c] = sum[j2 * XW + c];
+      __syncwarp();
+      const int cl = lane % XW;
+      const int64_t gcol = c0 + j2 * XW + cl;
+#pragma unroll 8
+      for (int it = 0; it < 32 / RPI; ++it) {
+        const int r = it * RPI + lane / XW;
+        const int64_t grr = r0 + 32 * qd + r;
+        if (grr < pM && gcol < pN && grr < gcol) E.C[grr * E.ldc + gcol] = xb[r * XP + cl];
+      }
+      __syncwarp();
+    }
+  } else if (EPI == TC_EPI_SPLIT) {
+    if (gr < pM && E.out_lo) {
+#pragma unroll
+      for (int c = 0; c < CW; ++c) {
+        const int64_t gc = c0 + c;
+        if (gc >= pN) continue;
+        const float hi = tc::to_tf32(sum[c]);
+        E.out_hi[gc * E.ldo + gr] = hi;
+        E.out_lo[gc * E.ldo + gr] = tc::to_tf32(sum[c] - hi);
+      }
+    } else if (gr < pM) {   // alpha C^T as fp32
+#pragma unroll
+      for (int c = 0; c < CW; ++c) {
+        const int64_t gc = c0 + c;
+        if (gc < pN) E.out_hi[gc * E.ldo + gr] = E.alpha * sum[c];
+      }
+    }
+  } else {  // PRECOND: row gr = column j of P, column gc = row i
+    const bool wcol = gr < E.d_in;
+    if (gr < pM) {
+#pragma unroll
+      for (int cc = 0; cc < CW; cc += EB) {
+        float w[EB], m[EB];
+#pragma unroll
+        for (int u = 0; u < EB; ++u) {
+          const int64_t i = c0 + cc + u;
+          w[u] = m[u] = 0.f;
+          if (E.pw && i < pN) {
+            w[u] = wcol ? __ldcg(E.pw + i * E.d_in + gr) : __ldcg(E.pb + i);
+            m[u] = wcol ? __ldcg(E.mw + i * E.d_in + gr) : __ldcg(E.mb + i);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < EB; ++u) {
+          const int64_t i = c0 + cc + u;
+          if (i >= pN) continue;
+          const float pr = sum[cc + u];
+          const float mn = fmaf(E.mu, m[u], fmaf(E.lambda, w[u], pr));
+          const float wn = fmaf(-E.eta, mn, w[u]);
+          if (wcol) {
+            const int64_t x = i * E.d_in + gr;
+            if (E.ow) E.ow[x] = pr;
+            if (E.pw) {
+              E.mw[x] = mn;
+              E.pw[x] = wn;
+            }
+          } else {
+            if (E.ob) E.ob[i] = pr;
+            if (E.pb) {
+              E.mb[i] = mn;
+              E.pb[i] = wn;
+            }
+          }
+        }
+      }
+    }
+  }
+
+}
+
 template <bool kBF16, int EPI, int BN>
 __device__ __forceinline__ void persistent_body(const GroupedTc& g) {
   using PC = PersistCfg<kBF16, BN>;
@@ -1012,102 +1120,8 @@ __device__ __forceinline__ void persistent_body(const GroupedTc& g) {
         tc::mbar_arrive(&acc_empty[buf]);
       }
       if (!ok) break;
-      if (EPI == TC_EPI_SYRK) {
-        // mirror F[gc][gr] from registers, old value from the same place
-        constexpr int EB = BN == 128 ? 16 : 8;   // loads in flight (fewer registers when wide)
-#pragma unroll
-        for (int cc = 0; cc < CW; cc += EB) {
-          float old[EB];
-#pragma unroll
-          for (int u = 0; u < EB; ++u) {
-            const int64_t gc = c0 + cc + u;
-            const bool okc = gr < pM && gc < pN && gr <= gc;
-            old[u] = (okc && E.beta != 0.f) ? __ldcg(E.C + gc * E.ldc + gr) : 0.f;
-          }
-#pragma unroll
-          for (int u = 0; u < EB; ++u) {
-            const int64_t gc = c0 + cc + u;
-            const float v = fmaf(E.beta, old[u], E.alpha * sum[cc + u]);
-            sum[cc + u] = v;
-            if (gr < pM && gc < pN && gr <= gc) E.C[gc * E.ldc + gr] = v;
-          }
-        }
-        // direct half F[gr][gc] (gr < gc): blocks of 32 rows x XW columns turned
-        // through the warp's buffer so that lanes run along gc
-        constexpr int RPI = 32 / PC::XW;   // rows per store instruction
-#pragma unroll
-        for (int j2 = 0; j2 < CW / PC::XW; ++j2) {
-#pragma unroll
-          for (int c = 0; c < PC::XW; ++c) xb[lane * PC::XP + c] = sum[j2 * PC::XW + c];
-          __syncwarp();
-          const int cl = lane % PC::XW;
-          const int64_t gcol = c0 + j2 * PC::XW + cl;
-#pragma unroll 8
-          for (int it = 0; it < 32 / RPI; ++it) {
-            const int r = it * RPI + lane / PC::XW;
-            const int64_t grr = r0 + 32 * qd + r;
-            if (grr < pM && gcol < pN && grr < gcol) E.C[grr * E.ldc + gcol] = xb[r * PC::XP + cl];
-          }
-          __syncwarp();
-        }
-      } else if (EPI == TC_EPI_SPLIT) {
-        if (gr < pM && E.out_lo) {
-#pragma unroll
-          for (int c = 0; c < CW; ++c) {
-            const int64_t gc = c0 + c;
-            if (gc >= pN) continue;
-            const float hi = tc::to_tf32(sum[c]);
-            E.out_hi[gc * E.ldo + gr] = hi;
-            E.out_lo[gc * E.ldo + gr] = tc::to_tf32(sum[c] - hi);
-          }
-        } else if (gr < pM) {   // alpha C^T as fp32
-#pragma unroll
-          for (int c = 0; c < CW; ++c) {
-            const int64_t gc = c0 + c;
-            if (gc < pN) E.out_hi[gc * E.ldo + gr] = E.alpha * sum[c];
-          }
-        }
-      } else {  // PRECOND: row gr = column j of P, column gc = row i
-        const bool wcol = gr < E.d_in;
-        constexpr int EB = BN == 128 ? 16 : 8;
-        if (gr < pM) {
-#pragma unroll
-          for (int cc = 0; cc < CW; cc += EB) {
-            float w[EB], m[EB];
-#pragma unroll
-            for (int u = 0; u < EB; ++u) {
-              const int64_t i = c0 + cc + u;
-              w[u] = m[u] = 0.f;
-              if (E.pw && i < pN) {
-                w[u] = wcol ? __ldcg(E.pw + i * E.d_in + gr) : __ldcg(E.pb + i);
-                m[u] = wcol ? __ldcg(E.mw + i * E.d_in + gr) : __ldcg(E.mb + i);
-              }
-            }
-#pragma unroll
-            for (int u = 0; u < EB; ++u) {
-              const int64_t i = c0 + cc + u;
-              if (i >= pN) continue;
-              const float pr = sum[cc + u];
-              const float mn = fmaf(E.mu, m[u], fmaf(E.lambda, w[u], pr));
-              const float wn = fmaf(-E.eta, mn, w[u]);
-              if (wcol) {
-                const int64_t x = i * E.d_in + gr;
-                if (E.ow) E.ow[x] = pr;
-                if (E.pw) {
-                  E.mw[x] = mn;
-                  E.pw[x] = wn;
-                }
-              } else {
-                if (E.ob) E.ob[i] = pr;
-                if (E.pb) {
-                  E.mb[i] = mn;
-                  E.pb[i] = wn;
-                }
-              }
-            }
-          }
-        }
-      }
+      epilogue_from_registers<EPI, CW, PC::XW, BN == 128 ? 16 : 8>(E, sum, xb, lane, qd, r0, c0, gr,
+                                                                   pM, pN);
     }
   }
   tc::tc_fence_before();
@@ -1135,6 +1149,275 @@ template <bool kBF16, int EPI>
 struct PersistKernel<kBF16, EPI, 256> {
   static constexpr auto fn = gemm_tc_persistent_wide_kernel<kBF16, EPI>;
 };
+
+// ------------------------------------------------------- CTA-pair persistent
+// Products with a wave of 256 x 256 tiles: clusters of two CTAs share each MMA
+// (tcgen05 cta_group::2): a tile's 256 rows are 128 in each CTA's shared memory
+// and TMEM, and each CTA loads half of the tile's 256 B rows, which the pair's
+// MMA reads from both.  Per SM that is half the B operand traffic of a
+// single-CTA 128 x 256 tile (TMA writes and MMA reads of shared memory).
+//   both CTAs  warp 0      TMA producer: its A rows and its half of B, completing
+//                          on the even CTA's stage barrier (cta_group::2 loads)
+//   even CTA   warp 1      MMA issuer; commits release both CTAs' stages and
+//                          signal both CTAs' accumulator barriers
+//   both CTAs  warps 2-17  drain + epilogue of the CTA's 128 rows (as the
+//                          single-CTA persistent kernel), one arrival per warp on
+//                          the even CTA's accumulator-empty barrier
+// The pair loops over tiles t = pair, pair + pairs, ...; every wait is bounded.
+template <bool kBF16>
+struct PairCfg {
+  static constexpr int BM = 128, BN = 256;           // per CTA: 128 rows x 256 columns
+  static constexpr int ELT = kBF16 ? 2 : 4;
+  static constexpr int BK = 128 / ELT;
+  static constexpr int KMMA = 32 / ELT;
+  static constexpr int A_BYTES = BM * 128;           // 16 KB
+  static constexpr int BH_BYTES = (BN / 2) * 128;    // this CTA's half of B: 16 KB
+  static constexpr int HALF_BYTES = A_BYTES + BH_BYTES;
+  static constexpr int STAGE_BYTES = kBF16 ? HALF_BYTES : 2 * HALF_BYTES;
+  static constexpr int EPI_WARPS = 16, CW = 64;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int ACC = 2, TMEM_COLS = 512;
+  static constexpr int XW = 8, XP = 9;
+  static constexpr int XPOSE_BYTES = EPI_WARPS * 32 * XP * 4;
+  static constexpr int FIT = (232448 - 1024 - 512 - XPOSE_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = FIT < 6 ? FIT : 6;
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + XPOSE_BYTES + 512;
+  static_assert(STAGES >= 3, "operand stages");
+  static_assert(SMEM <= 232448, "fits the per-CTA shared memory");
+};
+
+template <bool kBF16, int EPI>
+__device__ __forceinline__ void pair_body(const GroupedTc& g) {
+  using PC = PairCfg<kBF16>;
+  constexpr int CW = PC::CW, BN = PC::BN, STAGES = PC::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  float* xbuf = reinterpret_cast<float*>(smem + STAGES * PC::STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * PC::STAGE_BYTES + PC::XPOSE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + PC::ACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + PC::ACC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int total = g.block_start[g.count];
+  const uint32_t rank = tc::cluster_rank();
+  const int pair = (int)(blockIdx.x / 2), npairs = (int)(gridDim.x / 2);
+  // a role that gives up stops the peer CTA's roles too
+  const uint32_t peer_abort = tc::mapa((const void*)abort_flag, rank ^ 1u);
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    tc::st_cluster_u32(peer_abort, 1u);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < PC::ACC; ++b) {
+      tc::mbar_init(&acc_full[b], 1);
+      tc::mbar_init(&acc_empty[b], 2 * PC::EPI_WARPS);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc_pair(tmem_slot, PC::TMEM_COLS);
+    tc::tmem_relinquish_pair();
+  }
+  tc::tc_fence_before();
+  __syncwarp();
+  tc::cluster_sync();   // both CTAs' barriers initialised and TMEM allocated
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();
+  auto a_ptr = [&](int s, int lo) { return smem + (size_t)s * PC::STAGE_BYTES + lo * PC::HALF_BYTES; };
+  auto b_ptr = [&](int s, int lo) { return a_ptr(s, lo) + PC::A_BYTES; };
+  auto kblocks = [&](int q, int tj, int* kb_lo) {
+    int64_t klo, khi;
+    k_range(g.prob[q].kmode, g.prob[q].K, (int64_t)tj * BN, BN, &klo, &khi);
+    *kb_lo = (int)(klo / PC::BK);
+    return khi > klo ? (int)((khi - klo + PC::BK - 1) / PC::BK) : 0;
+  };
+  // same operand, diagonal tile: this CTA's A rows are its half of B
+  auto a_in_b = [&](int q, int ti, int tj) { return g.prob[q].same_ab && ti == tj; };
+  const int kb_per_sub = g.prob[0].ksub / PC::BK;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ------------------------------------------ TMA producer
+      const uint32_t full0 = tc::mapa(full, 0);   // the even CTA's stage barriers
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = pair; t < total && ok; t += npairs) {
+        int q, ti, tj;
+        grouped_tile<1>(g, t, &q, &ti, &tj);
+        const CUtensorMap* m = &g.maps[4 * q];
+        const bool aib = a_in_b(q, ti, tj);
+        const uint32_t bytes = (aib ? PC::BH_BYTES : PC::HALF_BYTES) * (kBF16 ? 1 : 2);
+        const int arow = ti * 256 + (int)rank * PC::BM, brow = tj * BN + (int)rank * (BN / 2);
+        int kb_lo;
+        const int nkb = kblocks(q, tj, &kb_lo);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+            give_up();
+            report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 21);
+            ok = false;
+            break;
+          }
+          const int k0 = (kb_lo + kb) * PC::BK;
+          const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
+          if (rank == 0) tc::mbar_expect_tx(&full[stage], 2 * bytes);   // both CTAs' loads
+          if (!aib) tc::tma_load_2d_pair(a_ptr(stage, 0), &m[0], fb, k0, arow);
+          tc::tma_load_2d_pair(b_ptr(stage, 0), &m[2], fb, k0, brow);
+          if (!kBF16) {
+            if (!aib) tc::tma_load_2d_pair(a_ptr(stage, 1), &m[1], fb, k0, arow);
+            tc::tma_load_2d_pair(b_ptr(stage, 1), &m[3], fb, k0, brow);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {  // ------------------------------ MMA issuer
+      constexpr uint32_t idesc = tc::make_idesc(kBF16 ? 1 : 2, 256, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int gsub = 0;
+      bool ok = true;
+      for (int t = pair; t < total && ok; t += npairs) {
+        int q, ti, tj;
+        grouped_tile<1>(g, t, &q, &ti, &tj);
+        const bool aib = a_in_b(q, ti, tj);
+        int kb_lo;
+        const int nkb = kblocks(q, tj, &kb_lo);
+        const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
+        for (int sub = 0; sub < nsub && ok; ++sub, ++gsub) {
+          const int buf = gsub % PC::ACC, use = gsub / PC::ACC;
+          if (!tc::mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag)) {
+            report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 22);
+            give_up();
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t d = tmem + (uint32_t)(buf * BN);
+          const int kb0 = sub * kb_per_sub, kb1 = min(nkb, kb0 + kb_per_sub);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!tc::mbar_wait(&full[stage], phase, abort_flag)) {
+              report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 23);
+              give_up();
+              ok = false;
+              break;
+            }
+            tc::tc_fence_after();
+            const int lo1 = kBF16 ? 0 : 1;
+            const uint32_t a_hi = tc::smem_u32(aib ? b_ptr(stage, 0) : a_ptr(stage, 0));
+            const uint32_t b_hi = tc::smem_u32(b_ptr(stage, 0));
+            const uint32_t a_lo = tc::smem_u32(aib ? b_ptr(stage, lo1) : a_ptr(stage, lo1));
+            const uint32_t b_lo = tc::smem_u32(b_ptr(stage, lo1));
+#pragma unroll
+            for (int kk = 0; kk < PC::BK / PC::KMMA; ++kk) {
+              const uint32_t off = kk * 32;
+              const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+              if (kBF16) {
+                tc::umma_f16_pair(d, tc::sdesc_kmajor_sw128(a_hi + off),
+                                  tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
+              } else {
+                tc::umma_tf32_pair(d, tc::sdesc_kmajor_sw128(a_hi + off),
+                                   tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
+                tc::umma_tf32_pair(d, tc::sdesc_kmajor_sw128(a_hi + off),
+                                   tc::sdesc_kmajor_sw128(b_lo + off), idesc, 1u);
+                tc::umma_tf32_pair(d, tc::sdesc_kmajor_sw128(a_lo + off),
+                                   tc::sdesc_kmajor_sw128(b_hi + off), idesc, 1u);
+              }
+            }
+            tc::umma_commit_pair(&empty[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (ok) tc::umma_commit_pair(&acc_full[buf]);
+        }
+      }
+    }
+  } else {  // ------------------------------------------------ drain + epilogue
+    const int qd = warp & 3;                 // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;           // column block: [CW h, CW h + CW)
+    const int row = 32 * qd + lane;
+    float* xb = xbuf + (warp - 2) * 32 * PC::XP;
+    const uint32_t acc_empty0 = tc::mapa(acc_empty, 0);
+    int gsub = 0;
+    bool ok = true;
+    for (int t = pair; t < total && ok; t += npairs) {
+      int q, ti, tj;
+      grouped_tile<1>(g, t, &q, &ti, &tj);
+      const TcEpilogue E = g.prob[q].e;   // by value (see gemm_body)
+      const int64_t pM = g.prob[q].M, pN = g.prob[q].N;
+      const int64_t r0 = (int64_t)ti * 256 + rank * PC::BM, c0 = (int64_t)tj * BN + h * CW;
+      const int64_t gr = r0 + row;
+      int kb_lo;
+      const int nkb = kblocks(q, tj, &kb_lo);
+      const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
+      if (gr < pM) {   // the tile's epilogue inputs into L2 while the drains run
+        if (EPI == TC_EPI_SYRK && E.beta != 0.f) {
+          for (int c = 0; c < CW; ++c) {
+            const int64_t gc = c0 + c;
+            if (gc < pN && gr <= gc) tc::prefetch_l2(E.C + gc * E.ldc + gr);
+          }
+        } else if (EPI == TC_EPI_PRECOND && E.pw && gr < E.d_in) {
+          for (int c = 0; c < CW; ++c) {
+            const int64_t i = c0 + c;
+            if (i >= pN) break;
+            tc::prefetch_l2(E.pw + i * E.d_in + gr);
+            tc::prefetch_l2(E.mw + i * E.d_in + gr);
+          }
+        }
+      }
+      float sum[CW];
+#pragma unroll
+      for (int c = 0; c < CW; ++c) sum[c] = 0.f;
+      for (int sub = 0; sub < nsub; ++sub, ++gsub) {
+        const int buf = gsub % PC::ACC, use = gsub / PC::ACC;
+        if (!tc::mbar_wait(&acc_full[buf], use & 1, abort_flag)) {
+          report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 24);
+          give_up();
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < CW / 16; ++cc) {
+          float v[16];
+          tc::tmem_ld16(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * BN + h * CW + cc * 16),
+                        v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sum[cc * 16 + i] += v[i];
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_cluster(acc_empty0 + (uint32_t)(buf * sizeof(uint64_t)));
+      }
+      if (!ok) break;
+      epilogue_from_registers<EPI, CW, PC::XW, 8>(E, sum, xb, lane, qd, r0, c0, gr, pM, pN);
+    }
+  }
+  tc::tc_fence_before();
+  __syncwarp();
+  tc::cluster_sync();   // every MMA of the pair has completed; no peer arrival is pending
+  if (warp == 1) tc::tmem_dealloc_pair(tmem, PC::TMEM_COLS);
+}
+
+template <bool kBF16, int EPI>
+__global__ void __maxnreg__(96) gemm_tc_pair_kernel(const __grid_constant__ GroupedTc g) {
+  pair_body<kBF16, EPI>(g);
+}
 
 // ------------------------------------------------------------ wait self-test
 // One thread waits, through the same bounded wait as the GEMM pipeline's
@@ -1423,6 +1706,12 @@ bool set_smem_attr() {
 // partial sum moves to fp32 registers.
 constexpr int kKsubTf32 = 128;
 constexpr int kKsubBf16 = 256;
+// k elements per TMEM drain of the 256-wide persistent bf16 products: 32 MMAs
+// (drift ~2e-6 relative per drain period), long enough that the drain warps
+// finish a tile's epilogue while the MMA runs one period ahead.
+constexpr int kKsubBf16Wide = 512;
+// Products with a wave of wide tiles run on CTA pairs (256 x 256 tiles).
+constexpr bool kWidePairs = true;
 
 template <bool kBF16, int BN, int EPI>
 kfac_status launch_kernel(unsigned grid, const CUtensorMap& ah, const CUtensorMap& al,
@@ -1546,7 +1835,7 @@ kfac_status dispatch(bool bf16, int epi, unsigned grid, const CUtensorMap& ah,
 }
 
 kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProblem* probs,
-                                   int count, cudaStream_t st);
+                                   int count, cudaStream_t st, bool pair);
 
 kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcOperand& A,
                            const TcOperand& B, bool same_ab, bool upper, int64_t M, int64_t N,
@@ -1572,7 +1861,7 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
     pr.e = e;
     pr.layer = layer;
     pr.kmode = kmode;
-    return launch_wide_persistent(h, bf16, epi, &pr, 1, st);
+    return launch_wide_persistent(h, bf16, epi, &pr, 1, st, kWidePairs);
   }
   const int BN = ((bf16 && K >= 8192) || count(256) >= sms) ? 256 : 128;
   // With at least a wave of tiles and no split-K, neighbouring tiles of one
@@ -1660,17 +1949,47 @@ kfac_status launch_persistent_kernel(const GroupedTc& g, cudaStream_t st) {
   return check_launch();
 }
 
-// k elements per TMEM drain of the 256-wide persistent bf16 products: 32 MMAs
-// (drift ~2e-6 relative per drain period), long enough that the drain warps
-// finish a tile's epilogue while the MMA runs one period ahead.
-constexpr int kKsubBf16Wide = 512;
+
+template <bool kBF16, int EPI>
+kfac_status launch_pair_kernel(const GroupedTc& g, cudaStream_t st) {
+  using PC = PairCfg<kBF16>;
+  static bool attr_ok = cudaFuncSetAttribute(gemm_tc_pair_kernel<kBF16, EPI>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)PC::SMEM) == cudaSuccess;
+  if (!attr_ok) {
+    check_launch();
+    return KFAC_ERR_CUDA;
+  }
+  const int total = g.block_start[g.count];
+  const int pairs = std::max(1, std::min<int>(total, num_sms() / 2));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * pairs));
+  cfg.blockDim = dim3(PC::THREADS);
+  cfg.dynamicSmemBytes = PC::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<kBF16, EPI>, g);
+  count_launch();
+  return check_launch();
+}
 
 // Products that fill at least a wave of 128 x 256 tiles by themselves, no
-// split-K: persistent launches of up to kMaxGroup of them, 256-wide tiles, each
-// tile's epilogue overlapped with the next tile's main loop.
+// split-K: persistent launches of up to kMaxGroup of them, each tile's epilogue
+// overlapped with the next tile's main loop.  256 x 256 tiles on CTA pairs
+// (pair), or 128 x 256 tiles on single CTAs.
 kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProblem* probs,
-                                   int count, cudaStream_t st) {
-  constexpr int BM = 128, BN = 256;
+                                   int count, cudaStream_t st, bool pair) {
+  constexpr int BN = 256;
+  const int BM = pair ? 256 : 128;                   // rows of a tile
+  const int box_a = 128, box_b = pair ? 128 : BN;    // rows of A and B each CTA loads
   const int unit = bf16 ? kKsubBf16Wide : kKsubTf32;
   std::unique_ptr<GroupedTc> g(new GroupedTc());
   for (int c0 = 0; c0 < count; c0 += kMaxGroup) {
@@ -1680,14 +1999,16 @@ kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProb
     for (int i = 0; i < cnt; ++i) {
       const TcProblem& pr = probs[c0 + i];
       CUtensorMap* m = &g->maps[4 * i];
-      if (!make_map(&m[0], pr.A.hi, bf16, pr.A.rows, pr.K, pr.A.pitch, BM)) return KFAC_ERR_CUDA;
-      if (!make_map(&m[2], pr.B.hi, bf16, pr.B.rows, pr.K, pr.B.pitch, BN)) return KFAC_ERR_CUDA;
+      if (!make_map(&m[0], pr.A.hi, bf16, pr.A.rows, pr.K, pr.A.pitch, box_a)) return KFAC_ERR_CUDA;
+      if (!make_map(&m[2], pr.B.hi, bf16, pr.B.rows, pr.K, pr.B.pitch, box_b)) return KFAC_ERR_CUDA;
       if (bf16) {
         m[1] = m[0];
         m[3] = m[2];
       } else {
-        if (!make_map(&m[1], pr.A.lo, false, pr.A.rows, pr.K, pr.A.pitch, BM)) return KFAC_ERR_CUDA;
-        if (!make_map(&m[3], pr.B.lo, false, pr.B.rows, pr.K, pr.B.pitch, BN)) return KFAC_ERR_CUDA;
+        if (!make_map(&m[1], pr.A.lo, false, pr.A.rows, pr.K, pr.A.pitch, box_a))
+          return KFAC_ERR_CUDA;
+        if (!make_map(&m[3], pr.B.lo, false, pr.B.rows, pr.K, pr.B.pitch, box_b))
+          return KFAC_ERR_CUDA;
       }
       GemmTcParams& pp = g->prob[i];
       pp.M = pr.M;
@@ -1713,15 +2034,26 @@ kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProb
     g->count = cnt;
     g->csize = 1;
     kfac_status e;
-    if (epi == TC_EPI_SYRK)
+    if (pair) {
+      if (epi == TC_EPI_SYRK)
+        e = bf16 ? launch_pair_kernel<true, TC_EPI_SYRK>(*g, st)
+                 : launch_pair_kernel<false, TC_EPI_SYRK>(*g, st);
+      else if (bf16)
+        e = KFAC_ERR_UNSUPPORTED;
+      else if (epi == TC_EPI_SPLIT)
+        e = launch_pair_kernel<false, TC_EPI_SPLIT>(*g, st);
+      else
+        e = launch_pair_kernel<false, TC_EPI_PRECOND>(*g, st);
+    } else if (epi == TC_EPI_SYRK) {
       e = bf16 ? launch_persistent_kernel<true, TC_EPI_SYRK, BN>(*g, st)
                : launch_persistent_kernel<false, TC_EPI_SYRK, BN>(*g, st);
-    else if (bf16)
+    } else if (bf16) {
       e = KFAC_ERR_UNSUPPORTED;
-    else if (epi == TC_EPI_SPLIT)
+    } else if (epi == TC_EPI_SPLIT) {
       e = launch_persistent_kernel<false, TC_EPI_SPLIT, BN>(*g, st);
-    else
+    } else {
       e = launch_persistent_kernel<false, TC_EPI_PRECOND, BN>(*g, st);
+    }
     if (e) return e;
   }
   return KFAC_OK;
@@ -1782,7 +2114,7 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
   }
   if (!wide_probs.empty())
     if (kfac_status e = launch_wide_persistent(h, bf16, epi, wide_probs.data(),
-                                               (int)wide_probs.size(), st))
+                                               (int)wide_probs.size(), st, kWidePairs))
       return e;
   if (small.empty()) return KFAC_OK;
   if ((int)small.size() < count) return launch_gemm_tc_grouped(h, bf16, epi, small.data(), (int)small.size(), st);
