@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(256) inv_split_kernel(const InvJob* jobs) {
 
 // Operands of the tensor-core doubling levels: blocks of L and X split into TF32
 // halves, dst[r][c] (row pitch dp) = src[r][c], or src[c][r] for a transposed
-// block.  One CTA moves a 32 x 32 tile through shared memory (loads and stores
+// block.  One CTA moves a 64 x 64 tile through shared memory (loads and stores
 // both coalesced).
 struct BlockPack {
   const float* src;   // block origin, row pitch ld
@@ -433,41 +433,48 @@ struct BlockPackGroup {
   int count;
 };
 
+constexpr int kBP = 64;   // block-pack tile: 64 x 64, 16 loads in flight per thread
 __global__ void __launch_bounds__(256) block_pack_kernel(const __grid_constant__ BlockPackGroup g) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float t[32][33];
+  __shared__ float t[kBP][kBP + 1];
   const int b = blockIdx.x;
   int q = 0;
   while (q + 1 < g.count && b >= g.tile_start[q + 1]) ++q;
   const BlockPack J = g.job[q];
   const int local = b - g.tile_start[q];
-  const int tcols = (J.cols + 31) / 32;
+  const int tcols = (J.cols + kBP - 1) / kBP;
   const int tr = local / tcols, tcl = local % tcols;   // destination tile
   const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+  float v[16];
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int i = ty + 8 * u;
-    float v = 0.f;
+  for (int u = 0; u < 16; ++u) {
+    const int i = ty + 8 * (u >> 1), j = tx + 32 * (u & 1);
+    v[u] = 0.f;
     if (!J.trans) {   // source row i of the tile = destination row i
-      const int r = tr * 32 + i, c = tcl * 32 + tx;
-      if (r < J.rows && c < J.cols) v = J.src[(int64_t)r * J.ld + c];
-      t[i][tx] = v;
+      const int r = tr * kBP + i, c = tcl * kBP + j;
+      if (r < J.rows && c < J.cols) v[u] = J.src[(int64_t)r * J.ld + c];
     } else {          // source row i of the tile = destination column i
-      const int r = tr * 32 + tx, c = tcl * 32 + i;
-      if (r < J.rows && c < J.cols) v = J.src[(int64_t)c * J.ld + r];
-      t[tx][i] = v;
+      const int r = tr * kBP + j, c = tcl * kBP + i;
+      if (r < J.rows && c < J.cols) v[u] = J.src[(int64_t)c * J.ld + r];
     }
+  }
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const int i = ty + 8 * (u >> 1), j = tx + 32 * (u & 1);
+    if (!J.trans) t[i][j] = v[u];
+    else t[j][i] = v[u];
   }
   __syncthreads();
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int r = tr * 32 + ty + 8 * u, c = tcl * 32 + tx;
+  for (int u = 0; u < 16; ++u) {
+    const int i = ty + 8 * (u >> 1), j = tx + 32 * (u & 1);
+    const int r = tr * kBP + i, c = tcl * kBP + j;
     if (r >= J.rows || c >= J.cols) continue;
-    const float v = t[ty + 8 * u][tx];
-    const float hi = tc::to_tf32(v);
+    const float w = t[i][j];
+    const float hi = tc::to_tf32(w);
     J.hi[(int64_t)r * J.dp + c] = hi;
-    J.lo[(int64_t)r * J.dp + c] = tc::to_tf32(v - hi);
+    J.lo[(int64_t)r * J.dp + c] = tc::to_tf32(w - hi);
   }
 }
 
@@ -571,7 +578,7 @@ kfac_status launch_tri_level_tc(kfac_ctx* h, int j0, int nj, int s, cudaStream_t
       if (kfac_status e = flush()) return e;
     g->job[g->count] = b;
     g->tile_start[g->count] = tiles;
-    tiles += (int)(cdiv(b.rows, 32) * cdiv(b.cols, 32));
+    tiles += (int)(cdiv(b.rows, kBP) * cdiv(b.cols, kBP));
     ++g->count;
     return KFAC_OK;
   };

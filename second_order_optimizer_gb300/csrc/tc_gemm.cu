@@ -39,6 +39,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <memory>
 #include <mutex>
@@ -2130,6 +2131,36 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
   const int64_t chunk = std::max<int64_t>(2, cdiv(total_units, sms));
   for (int q = 0; q < count; ++q)
     want[q] = std::max<int64_t>(1, cdiv(cdiv(probs[q].K, unit), chunk));
+  // The products that need no split run on CTA pairs (256 x 256 tiles) when that
+  // is faster after wave quantisation: a pair tile is four 128 x 128 tiles of work
+  // on two SMs at about 0.75 of the single-CTA time per flop (measured: the pair's
+  // MMA is fed twice the operand bytes per shared-memory byte).
+  {
+    std::vector<TcProblem> unsplit;
+    double t1 = 0, t2 = 0, k1 = 0, k2 = 0;
+    for (int q = 0; q < count; ++q) {
+      if (want[q] != 1) continue;
+      const TcProblem& pr = probs[q];
+      const int tm = (int)cdiv(pr.M, 256), tn = (int)cdiv(pr.N, 256);
+      const int64_t pt = pr.upper ? upper_tile_count(tm, tn, 1) : (int64_t)tm * tn;
+      t1 += (double)tiles[q];
+      k1 += (double)tiles[q] * (double)pr.K;
+      t2 += (double)pt;
+      k2 += (double)pt * (double)pr.K;
+      unsplit.push_back(pr);
+    }
+    if (!unsplit.empty() && t2 >= sms / 2) {
+      const double cost1 = std::ceil(t1 / sms) * (k1 / t1);
+      const double cost2 = std::ceil(t2 / (sms / 2)) * 2.0 * 0.75 * (k2 / t2);
+      if (cost2 < cost1) {
+        if (kfac_status e = launch_wide_persistent(h, bf16, epi, unsplit.data(),
+                                                   (int)unsplit.size(), st, true))
+          return e;
+        for (int q = 0; q < count; ++q)
+          if (want[q] == 1) want[q] = 0;   // done
+      }
+    }
+  }
   std::unique_ptr<GroupedTc> g(new GroupedTc());
   for (int pass = 0; pass < 2; ++pass) {   // pass 0: unsplit products; pass 1: split ones
     const int csize = pass == 0 ? 1 : 8;
@@ -2157,7 +2188,7 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
       return e;
     };
     for (int q = 0; q < count; ++q) {
-      if ((want[q] > 1) != (pass == 1)) continue;
+      if (want[q] == 0 || (want[q] > 1) != (pass == 1)) continue;
       const TcProblem& pr = probs[q];
       SplitShape sh{1, 1, cdiv(pr.K, unit) * unit};
       if (pass == 1) {
