@@ -35,7 +35,8 @@ WORKLOADS = {"mlp4": "c2", "single_linear": "c1", "resnet18": "c3", "resnet50": 
              "resnet50_bf16": "c4bf16", "transformer4": "c5",
              "resnet18_nchw": "c3", "resnet50_nchw": "c4", "resnet50_bf16_nchw": "c4bf16",
              "transformer4_qkv_tied": "c5", "mlp4_ikfac": "c2",
-             "resnet18_diag_nchw": "c3"}
+             "resnet18_diag_nchw": "c3", "mlp4_ikfac_bf16": "c2",
+             "transformer4_ikfac_bf16": "c5"}
 # workloads whose convolutions hand the library their NCHW input and output
 # gradient (kfac_update_factors_conv2d_batched) instead of unfolded matrices
 NCHW_WORKLOADS = {"resnet18_nchw", "resnet50_nchw", "resnet50_bf16_nchw", "resnet18_diag_nchw"}
@@ -46,8 +47,10 @@ DIAG_WORKLOADS = {"resnet18_diag_nchw"}
 # factor (kfac_tie_a_factor: the three read the same input)
 TIED_WORKLOADS = {"transformer4_qkv_tied"}
 # workloads whose refreshes after the first are inverse-free steps
-# (kfac_ikfac_update, beta = 1) instead of Cholesky inversions
-IKFAC_WORKLOADS = {"mlp4_ikfac"}
+# (kfac_ikfac_update, beta = 1) instead of Cholesky inversions: products in 3xTF32,
+# or on bf16 tensor cores
+IKFAC_WORKLOADS = {"mlp4_ikfac", "mlp4_ikfac_bf16", "transformer4_ikfac_bf16"}
+IKFAC_BF16_WORKLOADS = {"mlp4_ikfac_bf16", "transformer4_ikfac_bf16"}
 
 
 def qkv_ties(layers):
@@ -146,19 +149,21 @@ def workload_name(cfg, workload):
             + ("+nchw_conv_inputs" if workload in NCHW_WORKLOADS else "")
             + ("+all_layers_diagonal" if workload in DIAG_WORKLOADS else "")
             + ("+qkv_shared_A" if workload in TIED_WORKLOADS else "")
-            + ("+inverse_free_refresh" if workload in IKFAC_WORKLOADS else ""))
+            + ("+inverse_free_refresh" if workload in IKFAC_WORKLOADS else "")
+            + ("_bf16" if workload in IKFAC_BF16_WORKLOADS else ""))
 
 
-def path_dtype(layers):
+def path_dtype(layers, workload=None):
     """Arithmetic of the step: fp32 state, factors and preconditioning (3xTF32 on the
     tensor cores, fp32-accurate); factor products read bf16 inputs where the layer
-    set has them."""
-    return "bf16-in/f32" if any(l.in_dtype == "bf16" for l in layers) else "f32"
+    set has them; the bf16 inverse-free variants refresh with bf16 products."""
+    d = "bf16-in/f32" if any(l.in_dtype == "bf16" for l in layers) else "f32"
+    return d + ("+bf16-refresh" if workload in IKFAC_BF16_WORKLOADS else "")
 
 
 # ----------------------------------------------------------------------------- accounting
 
-def algorithmic(layers, k, nchw=False, tied=(), ikfac=False):
+def algorithmic(layers, k, nchw=False, tied=(), ikfac=False, ikfac_bf16=False):
     """Per-step algorithmic flops and bytes of each phase (fp32 state, input dtype as given).
     nchw: convolutions read their NCHW input and output gradient, not unfolded matrices.
     tied: indices of layers whose A is another layer's (no A product or inverse)."""
@@ -178,8 +183,10 @@ def algorithmic(layers, k, nchw=False, tied=(), ikfac=False):
                 f["factor_bytes"] += M * (l.d_in * own_a + o) * elt
             f["factor_bytes"] += 2 * 4 * (n * n * own_a + o * o)
             # Cholesky n^3/3 + L^-1 n^3/3 + X^T X n^3/3; inverse-free: three n^3 products
-            # (2 n^3 each) and K K^T (n^3, upper triangle)
-            f["invert_flop"] += (7 if ikfac else 1) * (n ** 3 * own_a + o ** 3) / k
+            # (2 n^3 each) and K K^T (n^3, upper triangle); with bf16 products the first
+            # one reads F_d as a hi/lo pair (a reduction of 2n: 4 n^3)
+            per = 9 if ikfac_bf16 else 7 if ikfac else 1
+            f["invert_flop"] += per * (n ** 3 * own_a + o ** 3) / k
             f["precond_flop"] += 2 * o * n * n + 2 * o * o * n
             f["precond_bytes"] += 4 * (n * n + o * o + 2 * o * n) + 4 * 3 * o * n
         else:
@@ -390,8 +397,10 @@ def run_gpu(args, peaks, peak_kind):
              for l in layers]
     max_rows = max(l.rows for l in layers)
     ikfac = args.workload in IKFAC_WORKLOADS
+    mode = (K.KFAC_IKFAC_BF16 if args.workload in IKFAC_BF16_WORKLOADS
+            else K.KFAC_IKFAC_TF32 if ikfac else K.KFAC_IKFAC_OFF)
     h = K.Kfac(descs, ema_decay=hp.ema_decay, damping=hp.damping, lr=hp.lr, momentum=hp.momentum,
-               weight_decay=hp.weight_decay, max_rows=max_rows, device=dev, ikfac=int(ikfac))
+               weight_decay=hp.weight_decay, max_rows=max_rows, device=dev, ikfac=mode)
     ties = qkv_ties(layers) if args.workload in TIED_WORKLOADS else {}
     for li, src in ties.items():
         h.tie_a_factor(li, src)
@@ -634,7 +643,7 @@ def run_gpu(args, peaks, peak_kind):
     ph = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
                    for i in range(seq_steps)])  # ms: factor, invert, precond, diag
 
-    acc = algorithmic(layers, k, nchw, set(ties), ikfac)
+    acc = algorithmic(layers, k, nchw, set(ties), ikfac, args.workload in IKFAC_BF16_WORKLOADS)
     phase_ms = ph.mean(axis=0)
     phase_ms[1] = inv_ms_refresh / k   # invert, amortised over the refresh period
     factor_tfs = acc["factor_flop"] / (phase_ms[0] * 1e-3) / 1e12
@@ -694,7 +703,7 @@ def run_gpu(args, peaks, peak_kind):
     return {
         "ms_per_step": ms_step, "phases": phases, "roofline": roof, "clocks": clocks,
         "gpu_launches": int(launches), "wall_s": wall, "e2e": e2e,
-        "dtype": path_dtype(layers),
+        "dtype": path_dtype(layers, args.workload),
         "config": {"workload": workload_name(cfg, args.workload),
                    "kron_layers": sum(l.kind == "kron" for l in layers),
                    "diag_layers": sum(l.kind == "diag" for l in layers),

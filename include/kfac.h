@@ -84,6 +84,10 @@ typedef struct {
   int in_dtype;  /* kfac_dtype of the activations a and output gradients g (KRON)  */
 } kfac_layer_desc;
 
+/* Inverse-free refresh (kfac_ikfac_update): off, products in 3xTF32, or
+ * products on bf16 tensor cores (fp32 accumulate and fp32 master K). */
+typedef enum { KFAC_IKFAC_OFF = 0, KFAC_IKFAC_TF32 = 1, KFAC_IKFAC_BF16 = 2 } kfac_ikfac_mode;
+
 typedef struct {
   double ema_decay;     /* xi in [0,1): F <- xi F + (1-xi) F_new                     */
   double damping;       /* gamma > 0: KRON inverts F + sqrt(gamma) I; DIAG divides by g a + gamma */
@@ -92,8 +96,9 @@ typedef struct {
   double weight_decay;  /* lambda: u = P + lambda W ; m <- mu m + u ; W <- W - eta m */
   int ema_init;         /* kfac_ema_init                                             */
   int math;             /* kfac_math                                                 */
-  int ikfac;            /* 0/1: keep inverse factors K for kfac_ikfac_update (fixed at
-                           kfac_create; 32 n^2 extra workspace bytes per n x n factor) */
+  int ikfac;            /* kfac_ikfac_mode: keep inverse factors K for kfac_ikfac_update
+                           (fixed at kfac_create; 32 n^2 extra workspace bytes per n x n
+                           factor either way) */
 } kfac_hparams;
 
 typedef struct kfac_ctx* kfac_handle;
@@ -265,10 +270,16 @@ kfac_status kfac_invert_factors(kfac_handle h, int layer, int which, cudaStream_
  *   K <- K (I - (beta/2) (K^T (F + sqrt(gamma) I) K - I)),
  * the first-order form of K exp(-(beta/2) E) (E vanishes at the exact inverse),
  * and sets the layer's inverse to K K^T, which kfac_precondition then uses.
- * Every product runs on the tensor cores (3xTF32); no factorisation.  K is
- * seeded by each kfac_invert of the factor (K = L^{-T}, exactly the inverse
- * factor), so a factor needs one kfac_invert before its first update.
- * Requires a handle created with hp->ikfac = 1 (else KFAC_ERR_UNSUPPORTED),
+ * Every product runs on the tensor cores; no factorisation.  With
+ * hp->ikfac = KFAC_IKFAC_TF32 the products are 3xTF32 (fp32 accuracy).  With
+ * KFAC_IKFAC_BF16 (the page: stable in low precision) they run on bf16 tensor
+ * cores with fp32 accumulation: K^T is kept in fp32 and gains the step's
+ * correction -(beta/2) K E in fp32, F + sqrt(gamma) I enters as a bf16 hi/lo
+ * pair, and K K^T is a bf16 SYRK (inverses within ~5e-3 of the fp64 iteration
+ * on the tests' factors).  K is seeded by each kfac_invert of the factor
+ * (K = L^{-T}, exactly the inverse factor), so a factor needs one kfac_invert
+ * before its first update.
+ * Requires a handle created with hp->ikfac != 0 (else KFAC_ERR_UNSUPPORTED),
  * 0 < beta < 2 (else KFAC_ERR_INVALID_ARG), and an inverted factor (else
  * KFAC_ERR_STATE).  A tied A is stepped with its source.  Like kfac_invert,
  * it must not overlap other calls of the handle. */

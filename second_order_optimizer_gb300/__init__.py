@@ -14,6 +14,7 @@ import os
 from typing import Optional, Sequence
 
 from ._lib import (LIB, KFAC_KRON, KFAC_DIAG, KFAC_F32, KFAC_BF16, KFAC_MATH_3XTF32,
+                   KFAC_IKFAC_OFF, KFAC_IKFAC_TF32, KFAC_IKFAC_BF16,
                    KFAC_FACTOR_A, KFAC_FACTOR_G,
                    KFAC_MATH_BF16, KFAC_EMA_INIT_ZERO, KFAC_EMA_INIT_FIRST, KFAC_STATE_A,
                    KFAC_STATE_G, KFAC_STATE_AINV, KFAC_STATE_GINV, KFAC_STATE_MOMENTUM,
@@ -24,6 +25,7 @@ __all__ = ["Kfac", "diag_factors_static", "conv2d_geom", "LayerDesc", "HParams",
            "KfacError", "status_string", "launch_count",
            "KFAC_KRON", "KFAC_DIAG", "KFAC_F32", "KFAC_BF16", "KFAC_MATH_3XTF32",
            "KFAC_MATH_BF16", "KFAC_EMA_INIT_ZERO", "KFAC_EMA_INIT_FIRST", "KFAC_FACTOR_A",
+           "KFAC_IKFAC_OFF", "KFAC_IKFAC_TF32", "KFAC_IKFAC_BF16",
            "KFAC_FACTOR_G", "LIB"]
 
 
@@ -197,7 +199,8 @@ class Kfac:
 
     def ikfac_update(self, layer: int = -1, beta: float = 1.0, stream=None):
         """kfac_ikfac_update: one inverse-free step of the inverse factors (handle
-        created with ikfac=1); the layer's inverses become K K^T."""
+        created with ikfac=KFAC_IKFAC_TF32 or KFAC_IKFAC_BF16); the layer's inverses
+        become K K^T."""
         _check(LIB.kfac_ikfac_update(self._h, layer, float(beta), _stream(stream)),
                "kfac_ikfac_update")
 

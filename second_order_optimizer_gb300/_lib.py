@@ -18,6 +18,7 @@ KFAC_KRON, KFAC_DIAG = 0, 1
 KFAC_F32, KFAC_BF16 = 0, 1
 KFAC_MATH_3XTF32, KFAC_MATH_BF16 = 0, 1
 KFAC_EMA_INIT_ZERO, KFAC_EMA_INIT_FIRST = 0, 1
+KFAC_IKFAC_OFF, KFAC_IKFAC_TF32, KFAC_IKFAC_BF16 = 0, 1, 2
 KFAC_FACTOR_A, KFAC_FACTOR_G = 1, 2
 (KFAC_STATE_A, KFAC_STATE_G, KFAC_STATE_AINV, KFAC_STATE_GINV, KFAC_STATE_MOMENTUM,
  KFAC_STATE_GDIAG, KFAC_STATE_ADIAG) = range(7)

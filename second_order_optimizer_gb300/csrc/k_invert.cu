@@ -656,7 +656,7 @@ kfac_status launch_outer_update(kfac_ctx* h, int j0, int nj, int K0, int W, cuda
   return flush();
 }
 
-kfac_status launch_ikfac_seed(const InvJob* jobs, int nj, int nmax, cudaStream_t st);
+kfac_status launch_ikfac_seed(const InvJob* jobs, int nj, int nmax, bool bf16, cudaStream_t st);
 
 kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
   // job range: the table section of the wanted factors (both, A only, G only),
@@ -774,7 +774,7 @@ kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
   count_launch();
   if (kfac_status e = check_launch()) return e;
   // inverse-free update: K = X^T (so K K^T = X^T X = F_d^{-1}), and K^T = X
-  if (h->hp.ikfac) return launch_ikfac_seed(jobs, nj, nmax, st);
+  if (h->hp.ikfac) return launch_ikfac_seed(jobs, nj, nmax, h->hp.ikfac == KFAC_IKFAC_BF16, st);
   return KFAC_OK;
 }
 
@@ -889,6 +889,95 @@ __global__ void __launch_bounds__(256) ik_transpose_kernel(const InvJob* jobs) {
   }
 }
 
+// ---- bf16 products (handles created with ikfac = KFAC_IKFAC_BF16).  The step
+// is the same; its three products run on bf16 tensor cores (fp32 accumulate)
+// and the correction is added to an fp32 master of K^T:
+//   FF <- [hi | lo]  of F_d in bf16 (hi = bf16(F_d), lo = bf16(F_d - hi))
+//   Gb <- (F_d K)^T  = ([hi lo] [K; K])^T            (bf16; reduction length 2n)
+//   G  <- (K^T F_d K)^T                               (fp32)
+//   Wb <- -(beta/2) (G - I)                            (bf16)
+//   D  <- (K Wb^T)^T = (K (-(beta/2) E))^T             (fp32)
+//   K^T <- K^T + D (fp32 master); its bf16 copies; F_d^{-1} <- K K^T (bf16 SYRK)
+// Rounding F_d to bf16 in one piece would move the iteration's fixed point by
+// about 2^-8 cond(F_d)^(1/2) relative; its hi/lo pair keeps 16 mantissa bits.
+// bf16 arrays share the fp32 arrays' storage with a row pitch of 2 np elements:
+//   FF, Wb in S1_hi;  [K^T | K^T] in K_lo;  Gb in S2_hi;  K in K_hi;
+//   G in S1_lo, D in S2_lo (fp32, pitch np);  the master K^T in Kt_hi.
+__device__ __forceinline__ __nv_bfloat16* bf16_at(float* base) {
+  return reinterpret_cast<__nv_bfloat16*>(base);
+}
+
+// from_x = 1: from X = L^{-1} (fp32, pitch n) after a Cholesky refresh: the master
+// K^T = X, and its bf16 copies [K^T | K^T] and K.  from_x = 0: after a step: the
+// master gains D, then the same copies.
+__global__ void __launch_bounds__(256) ikb_set_kernel(const InvJob* jobs, int from_x) {
+  pdl_wait();
+  pdl_trigger();
+  const InvJob J = jobs[blockIdx.y];
+  const int tn = (J.n + kTT - 1) / kTT;
+  if ((int)blockIdx.x >= tn * tn) return;
+  const int r0 = (blockIdx.x / tn) * kTT, c0 = (blockIdx.x % tn) * kTT;
+  const int64_t pb = 2 * (int64_t)J.np;
+  __shared__ float t[kTT][kTT + 1];
+  const int tx = threadIdx.x % kTT, ty = threadIdx.x / kTT;   // 32 x 8
+  __nv_bfloat16* kk = bf16_at(J.K_lo);
+  __nv_bfloat16* kb = bf16_at(J.K_hi);
+  for (int rr = ty; rr < kTT; rr += 8) {
+    const int r = r0 + rr, c = c0 + tx;
+    float v = 0.f;
+    if (r < J.n && c < J.n) {
+      const int64_t x = (int64_t)r * J.np + c;
+      if (from_x) {
+        v = J.X[(int64_t)r * J.n + c];
+      } else {
+        v = J.Kt_hi[x] + J.S2_lo[x];
+      }
+      J.Kt_hi[x] = v;
+      const __nv_bfloat16 b = __float2bfloat16_rn(v);
+      kk[(int64_t)r * pb + c] = b;
+      kk[(int64_t)r * pb + J.n + c] = b;
+    }
+    t[rr][tx] = v;
+  }
+  __syncthreads();
+  for (int cc = ty; cc < kTT; cc += 8) {   // K[c][r] = K^T[r][c]
+    const int c = c0 + cc, r = r0 + tx;
+    if (r < J.n && c < J.n) kb[(int64_t)c * pb + r] = __float2bfloat16_rn(t[tx][cc]);
+  }
+}
+
+// FF <- [bf16(F_d) | bf16(F_d - bf16(F_d))]
+__global__ void __launch_bounds__(256) ikb_damped_kernel(const InvJob* jobs, float sqrt_gamma) {
+  pdl_wait();
+  pdl_trigger();
+  const InvJob J = jobs[blockIdx.y];
+  const int64_t nn = (int64_t)J.n * J.n, pb = 2 * (int64_t)J.np;
+  __nv_bfloat16* ff = bf16_at(J.S1_hi);
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / J.n, c = e % J.n;
+    const float v = J.F[e] + (r == c ? sqrt_gamma : 0.f);
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    ff[r * pb + c] = hi;
+    ff[r * pb + J.n + c] = __float2bfloat16_rn(v - __bfloat162float(hi));
+  }
+}
+
+// Wb <- bf16(-(beta/2) (G - I)),  G fp32 in S1_lo
+__global__ void __launch_bounds__(256) ikb_w_kernel(const InvJob* jobs, float half_beta) {
+  pdl_wait();
+  pdl_trigger();
+  const InvJob J = jobs[blockIdx.y];
+  const int64_t nn = (int64_t)J.n * J.n, pb = 2 * (int64_t)J.np;
+  __nv_bfloat16* w = bf16_at(J.S1_hi);
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / J.n, c = e % J.n;
+    const float g = J.S1_lo[r * J.np + c] - (r == c ? 1.f : 0.f);
+    w[r * pb + c] = __float2bfloat16_rn(-half_beta * g);
+  }
+}
+
 unsigned elem_blocks(int nmax) {
   return (unsigned)std::min<int64_t>(cdiv((int64_t)nmax * nmax, 256), 1024);
 }
@@ -899,8 +988,85 @@ unsigned tile_blocks(int nmax) {
 
 }  // namespace
 
-kfac_status launch_ikfac_seed(const InvJob* jobs, int nj, int nmax, cudaStream_t st) {
-  launch_pdl(ik_seed_kernel, dim3(tile_blocks(nmax), nj), dim3(256), 0, st, jobs);
+kfac_status launch_ikfac_seed(const InvJob* jobs, int nj, int nmax, bool bf16, cudaStream_t st) {
+  if (bf16)
+    launch_pdl(ikb_set_kernel, dim3(tile_blocks(nmax), nj), dim3(256), 0, st, jobs, 1);
+  else
+    launch_pdl(ik_seed_kernel, dim3(tile_blocks(nmax), nj), dim3(256), 0, st, jobs);
+  count_launch();
+  return check_launch();
+}
+
+// One inverse-free step with bf16 products (see ikb_set_kernel above).
+kfac_status launch_ikfac_update_bf16(kfac_ctx* h, const InvJob* jobs, int j0, int nj, int nmax,
+                                     float beta, cudaStream_t st) {
+  launch_pdl(ikb_damped_kernel, dim3(elem_blocks(nmax), nj), dim3(256), 0, st, jobs,
+             (float)std::sqrt(h->hp.damping));
+  count_launch();
+  if (kfac_status e = check_launch()) return e;
+  std::vector<TcProblem> pr;
+  auto bfp = [](float* p) { return static_cast<const void*>(p); };
+  for (int which = 0; which < 3; ++which) {
+    pr.clear();
+    for (int i = j0; i < j0 + nj; ++i) {
+      const InvJob& J = h->invjobs_host[i];
+      const int64_t pb = 2 * (int64_t)J.np;
+      TcProblem q{};
+      q.M = q.N = J.n;
+      q.layer = J.layer;
+      q.e.alpha = 1.f;
+      if (which == 0) {          // Gb <- (F_d K)^T: [hi lo] . [K; K], bf16 out
+        q.A = TcOperand{bfp(J.S1_hi), nullptr, J.n, pb};
+        q.B = TcOperand{bfp(J.K_lo), nullptr, J.n, pb};
+        q.K = 2 * (int64_t)J.n;
+        q.e.out_hi = J.S2_hi;
+        q.e.out_bf16 = 1;
+        q.e.ldo = pb;
+      } else if (which == 1) {   // G <- (K^T F_d K)^T, fp32 out
+        q.A = TcOperand{bfp(J.K_lo), nullptr, J.n, pb};
+        q.B = TcOperand{bfp(J.S2_hi), nullptr, J.n, pb};
+        q.K = J.n;
+        q.e.out_hi = J.S1_lo;
+        q.e.ldo = J.np;
+      } else {                   // D <- (K Wb^T)^T, fp32 out
+        q.A = TcOperand{bfp(J.K_hi), nullptr, J.n, pb};
+        q.B = TcOperand{bfp(J.S1_hi), nullptr, J.n, pb};
+        q.K = J.n;
+        q.e.out_hi = J.S2_lo;
+        q.e.ldo = J.np;
+      }
+      pr.push_back(q);
+    }
+    if (kfac_status e = launch_gemm_tc_grouped(h, true, TC_EPI_SPLIT, pr.data(), (int)pr.size(), st))
+      return e;
+    if (which == 1) {
+      launch_pdl(ikb_w_kernel, dim3(elem_blocks(nmax), nj), dim3(256), 0, st, jobs, 0.5f * beta);
+      count_launch();
+      if (kfac_status e = check_launch()) return e;
+    }
+  }
+  launch_pdl(ikb_set_kernel, dim3(tile_blocks(nmax), nj), dim3(256), 0, st, jobs, 0);
+  count_launch();
+  if (kfac_status e = check_launch()) return e;
+  pr.clear();
+  for (int i = j0; i < j0 + nj; ++i) {   // F_d^{-1} <- K K^T (bf16 SYRK, fp32 result)
+    const InvJob& J = h->invjobs_host[i];
+    TcProblem q{};
+    q.M = q.N = q.K = J.n;
+    q.layer = J.layer;
+    q.A = TcOperand{bfp(J.K_hi), nullptr, J.n, 2 * (int64_t)J.np};
+    q.B = q.A;
+    q.same_ab = true;
+    q.upper = true;
+    q.e.alpha = 1.f;
+    q.e.beta = 0.f;
+    q.e.C = J.Finv;
+    q.e.ldc = J.n;
+    pr.push_back(q);
+  }
+  if (kfac_status e = launch_gemm_tc_grouped(h, true, TC_EPI_SYRK, pr.data(), (int)pr.size(), st))
+    return e;
+  launch_pdl(inv_split_kernel, dim3(elem_blocks(nmax), nj), dim3(256), 0, st, jobs);
   count_launch();
   return check_launch();
 }
@@ -922,6 +1088,8 @@ kfac_status launch_ikfac_update(kfac_ctx* h, int layer, float beta, cudaStream_t
   const InvJob* jobs = h->at<InvJob>(h->off_invjobs) + j0;
   int nmax = 0;
   for (int i = j0; i < j0 + nj; ++i) nmax = std::max(nmax, h->invjobs_host[i].n);
+  if (h->hp.ikfac == KFAC_IKFAC_BF16)
+    return launch_ikfac_update_bf16(h, jobs, j0, nj, nmax, beta, st);
   launch_pdl(ik_damped_split_kernel, dim3(elem_blocks(nmax), nj), dim3(256), 0, st, jobs,
              (float)std::sqrt(h->hp.damping));
   count_launch();

@@ -46,7 +46,8 @@ bool valid_hp(const kfac_hparams* hp) {
     return false;
   if (hp->ema_init != KFAC_EMA_INIT_ZERO && hp->ema_init != KFAC_EMA_INIT_FIRST) return false;
   if (hp->math != KFAC_MATH_3XTF32 && hp->math != KFAC_MATH_BF16) return false;
-  if (hp->ikfac != 0 && hp->ikfac != 1) return false;
+  if (hp->ikfac != KFAC_IKFAC_OFF && hp->ikfac != KFAC_IKFAC_TF32 && hp->ikfac != KFAC_IKFAC_BF16)
+    return false;
   return true;
 }
 

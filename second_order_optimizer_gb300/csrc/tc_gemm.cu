@@ -5,7 +5,7 @@
 //     SYRK     F <- beta F + alpha C on tiles on/above the diagonal, plus mirrors (K1,
 //              with A = B = X = x-hat^T)
 //     SPLIT    store C^T as TF32 halves (hi, lo), ready to be the next product's operand;
-//              with no lo buffer, alpha C^T as fp32
+//              with no lo buffer, alpha C^T as fp32 (or as bf16: out_bf16)
 //     PRECOND  P^T = C; optional momentum / weight-decay / lr update of W in place (K4)
 //
 // Osawa et al., "Large-Scale Distributed Second-Order Optimization Using
@@ -171,7 +171,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_last = reinterpret_cast<int*>(tmem_slot + 2);
-  static_assert(EPI == TC_EPI_SYRK || !kBF16, "bf16 operands are used by the factor update only");
+  static_assert(EPI != TC_EPI_PRECOND || !kBF16, "preconditioning products read TF32 halves");
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   int ti, tj;
@@ -432,7 +432,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
           if (ok) E.C[gc * E.ldc + gr] = v;
         }
       } else if (EPI == TC_EPI_SPLIT) {
-        if (E.out_lo) {
+        if (E.out_bf16) {   // alpha C^T as bf16
+          __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(E.out_hi);
+#pragma unroll
+          for (int c = 0; c < C::CW; ++c) {
+            const int64_t gc = c0 + h * C::CW + c;
+            if (gc < pN) ob[gc * E.ldo + gr] = __float2bfloat16_rn(E.alpha * sum[c]);
+          }
+        } else if (E.out_lo) {
 #pragma unroll
           for (int c = 0; c < C::CW; ++c) {
             const int64_t gc = c0 + h * C::CW + c;
@@ -651,6 +658,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
       const int64_t gr = r0 + r, gc = c0 + c;
       if (gr >= pM || gc >= pN) continue;
       const float v = T[r * C::TPAD + c];
+      if (E.out_bf16) {   // alpha C^T as bf16
+        reinterpret_cast<__nv_bfloat16*>(E.out_hi)[gc * E.ldo + gr] = __float2bfloat16_rn(E.alpha * v);
+        continue;
+      }
       if (!E.out_lo) {   // alpha C^T as fp32
         E.out_hi[gc * E.ldo + gr] = E.alpha * v;
         continue;
@@ -839,7 +850,14 @@ __device__ __forceinline__ void epilogue_from_registers(const TcEpilogue& E, flo
       __syncwarp();
     }
   } else if (EPI == TC_EPI_SPLIT) {
-    if (gr < pM && E.out_lo) {
+    if (gr < pM && E.out_bf16) {   // alpha C^T as bf16
+      __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(E.out_hi);
+#pragma unroll
+      for (int c = 0; c < CW; ++c) {
+        const int64_t gc = c0 + c;
+        if (gc < pN) ob[gc * E.ldo + gr] = __float2bfloat16_rn(E.alpha * sum[c]);
+      }
+    } else if (gr < pM && E.out_lo) {
 #pragma unroll
       for (int c = 0; c < CW; ++c) {
         const int64_t gc = c0 + c;
@@ -1830,8 +1848,10 @@ kfac_status dispatch(bool bf16, int epi, unsigned grid, const CUtensorMap& ah,
   if (epi == TC_EPI_SYRK)
     return bf16 ? launch_kernel<true, BN, TC_EPI_SYRK>(grid, ah, al, bh, bl, p, st)
                 : launch_kernel<false, BN, TC_EPI_SYRK>(grid, ah, al, bh, bl, p, st);
+  if (epi == TC_EPI_SPLIT)
+    return bf16 ? launch_kernel<true, BN, TC_EPI_SPLIT>(grid, ah, al, bh, bl, p, st)
+                : launch_kernel<false, BN, TC_EPI_SPLIT>(grid, ah, al, bh, bl, p, st);
   if (bf16) return KFAC_ERR_UNSUPPORTED;
-  if (epi == TC_EPI_SPLIT) return launch_kernel<false, BN, TC_EPI_SPLIT>(grid, ah, al, bh, bl, p, st);
   return launch_kernel<false, BN, TC_EPI_PRECOND>(grid, ah, al, bh, bl, p, st);
 }
 
@@ -2039,19 +2059,21 @@ kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProb
       if (epi == TC_EPI_SYRK)
         e = bf16 ? launch_pair_kernel<true, TC_EPI_SYRK>(*g, st)
                  : launch_pair_kernel<false, TC_EPI_SYRK>(*g, st);
+      else if (epi == TC_EPI_SPLIT)
+        e = bf16 ? launch_pair_kernel<true, TC_EPI_SPLIT>(*g, st)
+                 : launch_pair_kernel<false, TC_EPI_SPLIT>(*g, st);
       else if (bf16)
         e = KFAC_ERR_UNSUPPORTED;
-      else if (epi == TC_EPI_SPLIT)
-        e = launch_pair_kernel<false, TC_EPI_SPLIT>(*g, st);
       else
         e = launch_pair_kernel<false, TC_EPI_PRECOND>(*g, st);
     } else if (epi == TC_EPI_SYRK) {
       e = bf16 ? launch_persistent_kernel<true, TC_EPI_SYRK, BN>(*g, st)
                : launch_persistent_kernel<false, TC_EPI_SYRK, BN>(*g, st);
+    } else if (epi == TC_EPI_SPLIT) {
+      e = bf16 ? launch_persistent_kernel<true, TC_EPI_SPLIT, BN>(*g, st)
+               : launch_persistent_kernel<false, TC_EPI_SPLIT, BN>(*g, st);
     } else if (bf16) {
       e = KFAC_ERR_UNSUPPORTED;
-    } else if (epi == TC_EPI_SPLIT) {
-      e = launch_persistent_kernel<false, TC_EPI_SPLIT, BN>(*g, st);
     } else {
       e = launch_persistent_kernel<false, TC_EPI_PRECOND, BN>(*g, st);
     }
@@ -2175,10 +2197,11 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
       if (epi == TC_EPI_SYRK)
         e = bf16 ? launch_grouped_kernel<true, TC_EPI_SYRK>(blocks, *g, st)
                  : launch_grouped_kernel<false, TC_EPI_SYRK>(blocks, *g, st);
+      else if (epi == TC_EPI_SPLIT)
+        e = bf16 ? launch_grouped_kernel<true, TC_EPI_SPLIT>(blocks, *g, st)
+                 : launch_grouped_kernel<false, TC_EPI_SPLIT>(blocks, *g, st);
       else if (bf16)
         e = KFAC_ERR_UNSUPPORTED;
-      else if (epi == TC_EPI_SPLIT)
-        e = launch_grouped_kernel<false, TC_EPI_SPLIT>(blocks, *g, st);
       else
         e = launch_grouped_kernel<false, TC_EPI_PRECOND>(blocks, *g, st);
       std::memset(g.get(), 0, sizeof(GroupedTc));

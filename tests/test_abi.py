@@ -85,7 +85,7 @@ def test_workspace_size_rejects_bad_arguments(lib):
         ([(0, 4, 4, 1, 0)], _hp(lib, damping=0.0)),
         ([(0, 4, 4, 1, 0)], _hp(lib, damping=float("nan"))),
         ([(0, 4, 4, 1, 0)], _hp(lib, math=7)),
-        ([(0, 4, 4, 1, 0)], _hp(lib, ikfac=2)),
+        ([(0, 4, 4, 1, 0)], _hp(lib, ikfac=3)),
     ]
     for layers, h in bad:
         d = _descs(lib, layers)

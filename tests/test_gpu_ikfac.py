@@ -8,7 +8,10 @@ Cholesky refresh (K = L^{-T}) and stepped by K <- K (I - (beta/2)(K^T F_d K - I)
 Tolerances (relative Frobenius).  Each step is four 3xTF32 products (~1e-6
 relative each) on operands rounded to TF32 halves (~2.4e-7), so T steps
 accumulate about 4e-6 T: the inverses K K^T after 5 steps are held to 5e-5;
-the preconditioned update W to 1e-4, as for the Cholesky path.
+the preconditioned update W to 1e-4, as for the Cholesky path.  With the
+products on bf16 tensor cores (KFAC_IKFAC_BF16; the page: stable in low
+precision) the inverses and the preconditioned gradients are held to the bf16
+path's 2e-2 against the float64 iteration.
 """
 import ctypes
 
@@ -101,6 +104,54 @@ def test_inverse_free_steps_match_oracle(beta):
             assert ea <= 5e-5 and eg <= 5e-5, (t, i, ea, eg)
             Wg = np.concatenate([to_np(pw[i]), to_np(pb[i])[:, None]], axis=1)
             assert rel_fro(Wg, s.W) <= 1e-4, (t, i, rel_fro(Wg, s.W))
+    assert h.get_status()[0] == 0
+
+
+@pytest.mark.parametrize("beta", [0.5, 1.0])
+def test_inverse_free_steps_bf16_match_oracle(beta):
+    """The schedule above with the products on bf16 tensor cores: step 1 refreshes
+    by Cholesky (seeds K), steps 2-6 take one bf16 inverse-free step of every K.
+    The inverses K K^T and the preconditioned gradients P against the float64
+    oracle's iteration from the same seed: 2e-2 (the bf16 path's tolerance)."""
+    shapes = [(900, 1024, 1024), (600, 299, 130), (300, 64, 17)]   # (M, d_in, o)
+    h = K.Kfac([(K.KFAC_KRON, o, d, 1, K.KFAC_F32) for _, d, o in shapes],
+               max_rows=max(M for M, _, _ in shapes), ikfac=K.KFAC_IKFAC_BF16, **HP)
+    idx = list(range(len(shapes)))
+    A = [np.zeros((d + 1, d + 1)) for _, d, _ in shapes]
+    G = [np.zeros((o, o)) for _, _, o in shapes]
+    KA, KG = [None] * 3, [None] * 3
+    pw = [to_dev(np.zeros((o, d), np.float32)) for _, d, o in shapes]
+    pb = [to_dev(np.zeros(o, np.float32)) for _, _, o in shapes]
+    worst = {"inv": 0.0, "P": 0.0}
+    for t in range(1, 7):
+        ins = [_draw(M, d, o) for M, d, o in shapes]
+        h.update_factors_batched(idx, [to_dev(x[0]) for x in ins], [to_dev(x[1]) for x in ins])
+        if t == 1:
+            h.invert(-1)
+        else:
+            h.ikfac_update(-1, beta=beta)
+        ow = [torch.empty(o, d, device="cuda") for _, d, o in shapes]
+        ob = [torch.empty(o, device="cuda") for _, _, o in shapes]
+        h.precondition_batched(idx, [to_dev(x[2]) for x in ins], [to_dev(x[3]) for x in ins],
+                               ow, ob, pw, pb)
+        for i, x in enumerate(ins):
+            A[i] = O.ema(A[i], O.factor(x[0], 1), HP["ema_decay"])
+            G[i] = O.ema(G[i], O.factor(x[1], 0), HP["ema_decay"])
+            if t == 1:
+                KA[i], KG[i] = O.ikfac_init(A[i], GAMMA), O.ikfac_init(G[i], GAMMA)
+            else:
+                KA[i] = O.ikfac_update(KA[i], A[i], GAMMA, beta)
+                KG[i] = O.ikfac_update(KG[i], G[i], GAMMA, beta)
+            Ainv, Ginv = O.ikfac_inverse(KA[i]), O.ikfac_inverse(KG[i])
+            ea = rel_fro(to_np(h.state(i, K.KFAC_STATE_AINV)), Ainv)
+            eg = rel_fro(to_np(h.state(i, K.KFAC_STATE_GINV)), Ginv)
+            P = O.precondition(Ginv, O.grad_hat(x[2], x[3]), Ainv)
+            ep = rel_fro(O.grad_hat(to_np(ow[i]), to_np(ob[i])), P)
+            worst["inv"] = max(worst["inv"], ea, eg)
+            worst["P"] = max(worst["P"], ep)
+            assert ea <= 2e-2 and eg <= 2e-2 and ep <= 2e-2, (t, i, ea, eg, ep)
+    print(f"bf16 inverse-free steps, beta {beta}: worst inverse {worst['inv']:.2e}, "
+          f"worst P {worst['P']:.2e}")
     assert h.get_status()[0] == 0
 
 
