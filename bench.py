@@ -36,7 +36,7 @@ WORKLOADS = {"mlp4": "c2", "single_linear": "c1", "resnet18": "c3", "resnet50": 
              "resnet18_nchw": "c3", "resnet50_nchw": "c4", "resnet50_bf16_nchw": "c4bf16",
              "transformer4_qkv_tied": "c5", "mlp4_ikfac": "c2",
              "resnet18_diag_nchw": "c3", "mlp4_ikfac_bf16": "c2",
-             "transformer4_ikfac_bf16": "c5"}
+             "transformer4_ikfac_bf16": "c5", "transformer1": "c5b1"}
 # workloads whose convolutions hand the library their NCHW input and output
 # gradient (kfac_update_factors_conv2d_batched) instead of unfolded matrices
 NCHW_WORKLOADS = {"resnet18_nchw", "resnet50_nchw", "resnet50_bf16_nchw", "resnet18_diag_nchw"}
@@ -103,6 +103,9 @@ def parse():
     p.add_argument("--no-graphs", action="store_true", help="time eager calls, not CUDA graphs")
     p.add_argument("--no-overlap", action="store_true",
                    help="run the phases of a step one after another on one stream")
+    p.add_argument("--nvtx", action="store_true",
+                   help="NVTX ranges factor/invert/precond/diag around the phases of eager steps "
+                        "(for profiler filters; use with --no-graphs)")
     # single-kernel mode: time one phase on one layer shape (not the headline line)
     p.add_argument("--micro", choices=["factor", "precond", "invert", "diag"], default=None)
     p.add_argument("--n", type=int, default=8193, help="micro: A dimension (d_in + 1)")
@@ -508,17 +511,25 @@ def run_gpu(args, peaks, peak_kind):
                 [x[li]["grad_w"] for li in diag_idx], [x[li]["grad_b"] for li in diag_idx],
                 [params[li][0] for li in diag_idx], [params[li][1] for li in diag_idx])
 
+    import contextlib
+    rng = ((lambda name: torch.cuda.nvtx.range(name)) if args.nvtx
+           else (lambda name: contextlib.nullcontext()))
+
     def step(t, x, ev=None):
         """The eager step through the public API (used for warm-up and end-to-end)."""
         if ev: ev[0].record(stream)
-        phase_factor(x)
+        with rng("factor"):
+            phase_factor(x)
         if ev: ev[1].record(stream)
         if (t - 1) % k == 0:
-            phase_invert() if t == 1 else phase_refresh()
+            with rng("invert"):
+                phase_invert() if t == 1 else phase_refresh()
         if ev: ev[2].record(stream)
-        phase_precond(x)
+        with rng("precond"):
+            phase_precond(x)
         if ev: ev[3].record(stream)
-        phase_diag(x)
+        with rng("diag"):
+            phase_diag(x)
         if ev: ev[4].record(stream)
 
     t = 0

@@ -63,14 +63,18 @@ __global__ void __launch_bounds__(256) gradhat_pack_grouped_kernel(
   pdl_wait();
   pdl_trigger();
   const GradPackJob J = g.job[blockIdx.y];  // by value: no reloads after each store
-  const int64_t total = (int64_t)J.o * J.n;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t i = e / J.n, j = e % J.n;
-    const float v = j < J.d_in ? J.gw[i * J.ld + j] : J.gb[i];
-    const float h = tc::to_tf32(v);
-    J.hi[i * J.np + j] = h;
-    J.lo[i * J.np + j] = tc::to_tf32(v - h);
+  // a CTA takes whole rows (no index division), its threads along the row
+  for (int i = blockIdx.x; i < J.o; i += gridDim.x) {
+    const float* src = J.gw + (int64_t)i * J.ld;
+    float* hi = J.hi + (int64_t)i * J.np;
+    float* lo = J.lo + (int64_t)i * J.np;
+#pragma unroll 4
+    for (int j = threadIdx.x; j < J.n; j += blockDim.x) {
+      const float v = j < J.d_in ? __ldg(src + j) : J.gb[i];
+      const float h = tc::to_tf32(v);
+      hi[j] = h;
+      lo[j] = tc::to_tf32(v - h);
+    }
   }
 }
 
@@ -133,11 +137,11 @@ kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layer
   GradPackGroup gp;
   std::memset(&gp, 0, sizeof(gp));
   int ng = 0;
-  int64_t max_elems = 0;
+  int64_t max_rows = 0;
   size_t used = 0;  // floats
   auto flush = [&]() -> kfac_status {
     if (ng == 0) return KFAC_OK;
-    const unsigned blocks = (unsigned)std::min<int64_t>(cdiv(max_elems, 256), 4 * num_sms());
+    const unsigned blocks = (unsigned)std::min<int64_t>(max_rows, 4 * num_sms());
     launch_pdl(gradhat_pack_grouped_kernel, dim3(dim3(blocks, ng)), dim3(256), 0, st, gp);
     count_launch();
     kfac_status e = check_launch();
@@ -146,7 +150,7 @@ kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layer
     p1.clear();
     p2.clear();
     ng = 0;
-    max_elems = 0;
+    max_rows = 0;
     used = 0;
     return e;
   };
@@ -173,7 +177,7 @@ kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layer
     j.n = L.n;
     j.hi = g_hi;
     j.lo = g_lo;
-    max_elems = std::max<int64_t>(max_elems, (int64_t)L.o * L.n);
+    max_rows = std::max<int64_t>(max_rows, L.o);
     TcProblem q1{};
     q1.A = TcOperand{g_hi, g_lo, L.o, np};   // X = grad-hat . Ainv, stored as X^T
     q1.B = TcOperand{h->at<float>(L.Ainv_hi), h->at<float>(L.Ainv_lo), L.n, np};

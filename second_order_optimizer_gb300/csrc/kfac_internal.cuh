@@ -279,7 +279,7 @@ struct SyrkSpec {
 kfac_status launch_syrk_tc_batched(kfac_ctx* h, const SyrkSpec* specs, int count, cudaStream_t st);
 size_t inv_y_floats(int n);
 // scratch of the batched entry points (a group of layers is packed together)
-constexpr size_t kBatchScratchBudget = size_t(256) << 20;
+constexpr size_t kBatchScratchBudget = size_t(1) << 30;
 size_t tc_pack_bytes(int n, int64_t max_rows, bool bf16);
 size_t tc_part_floats();
 

@@ -193,23 +193,24 @@ def resnet50_imagenet(dtype: str = "f32") -> Config:
                   g_std=1e-4, grad_mode="iid")
 
 
-def transformer4() -> Config:
+def transformer4(blocks: int = 4) -> Config:
     """4 transformer blocks, d_model 2048, FFN 8192, 16384 tokens, bf16 a and g.
 
     Each block: Q, K, V, O projections (2048 -> 2048), FFN up (2048 -> 8192) and
     down (8192 -> 2048); all with bias.  The diagonal-path twins cover the same
-    201.4M parameters.
+    201.4M parameters.  ``blocks`` < 4: the first blocks alone (same layers and
+    draws), a small case of the same products for profiler captures.
     """
     T = 16384
     L: List[Layer] = []
-    for b in range(4):
+    for b in range(blocks):
         for nm in ("q", "k", "v", "o"):
             L.append(Layer(f"b{b}.{nm}", "kron", 2048, 2048, 1, T, "normal", "bf16"))
         L.append(Layer(f"b{b}.up", "kron", 8192, 2048, 1, T, "normal", "bf16"))
         L.append(Layer(f"b{b}.down", "kron", 2048, 8192, 1, T, "normal", "bf16"))
     L += [dataclasses.replace(l, name=l.name + "_diag", kind="diag") for l in list(L)]
-    return Config(5, "transformer4_d2048_ffn8192_t16384", L, steps=10, invert_every=10,
-                  g_std=1e-5, grad_mode="iid")
+    name = "transformer4_d2048_ffn8192_t16384" if blocks == 4 else f"transformer{blocks}_block"
+    return Config(5, name, L, steps=10, invert_every=10, g_std=1e-5, grad_mode="iid")
 
 
 CONFIGS = {
@@ -219,6 +220,7 @@ CONFIGS = {
     "c4": resnet50_imagenet,
     "c4bf16": lambda: resnet50_imagenet("bf16"),
     "c5": transformer4,
+    "c5b1": lambda: transformer4(1),
 }
 
 
