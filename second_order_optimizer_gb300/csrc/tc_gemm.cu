@@ -88,6 +88,7 @@ struct GemmTcParams {
   int mc;                // cluster pairs share the B tile by TMA multicast (no split-K)
   int64_t k_per_split;   // multiple of ksub
   int kmode;             // reduction range per tile (TcProblem::kmode)
+  int colmajor;          // persistent kernels: tiles column by column (grouped_tile)
   int ksub;              // k elements per TMEM drain (multiple of BK)
   float* part;           // this product's cluster partials [tile][groups][BM][BN]
   int* tickets;          // this product's tickets [tile][csize]
@@ -786,6 +787,38 @@ struct PersistCfg {
   static_assert(SMEM <= 232448, "fits the per-CTA shared memory");
 };
 
+// Tile order of the persistent kernels, so that the tiles running at the same time
+// (about one per SM) read each operand block from DRAM once and from L2 after.
+// Upper-triangle (SYRK) products: blocks of kTileBlock x kTileBlock tiles, block
+// columns in turn, tile columns inside a block.  Other products: along the
+// longer side of the output, so that the larger operand is read once per launch
+// and the smaller one is re-read (colmajor when M < N).
+constexpr int kTileBlock = 8;
+__host__ __device__ inline void upper_tile_blocked(int t, int tiles_m, int tiles_n, int* ti,
+                                                   int* tj) {
+  constexpr int S = kTileBlock;
+  const int nbj = (tiles_n + S - 1) / S;
+  for (int bj = 0; bj < nbj; ++bj) {
+    const int c0 = bj * S, c1 = c0 + S < tiles_n ? c0 + S : tiles_n;
+    for (int bi = 0; bi <= bj; ++bi) {
+      const int r0 = bi * S;
+      if (r0 >= tiles_m) break;
+      const int r1 = r0 + S < tiles_m ? r0 + S : tiles_m;
+      for (int c = c0; c < c1; ++c) {   // rows r0 <= r < min(r1, c + 1) of column c
+        const int hi = c + 1 < r1 ? c + 1 : r1;
+        const int k = hi > r0 ? hi - r0 : 0;
+        if (t < k) {
+          *ti = r0 + t;
+          *tj = c;
+          return;
+        }
+        t -= k;
+      }
+    }
+  }
+  *ti = *tj = 0;   // t beyond the triangle: not reached
+}
+
 template <int R>
 __device__ __forceinline__ void grouped_tile(const GroupedTc& g, int t, int* q, int* ti, int* tj) {
   int k = 0;
@@ -793,7 +826,13 @@ __device__ __forceinline__ void grouped_tile(const GroupedTc& g, int t, int* q, 
   const int local = t - g.block_start[k];
   const GemmTcParams& p = g.prob[k];
   if (p.upper) {
-    upper_tile(local, p.tiles_m, R, ti, tj);
+    if (R == 1)
+      upper_tile_blocked(local, p.tiles_m, p.tiles_n, ti, tj);
+    else
+      upper_tile(local, p.tiles_m, R, ti, tj);
+  } else if (p.colmajor) {
+    *ti = local % p.tiles_m;
+    *tj = local / p.tiles_m;
   } else {
     *ti = local / p.tiles_n;
     *tj = local % p.tiles_n;
@@ -2040,6 +2079,7 @@ kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProb
       pp.upper = pr.upper ? 1 : 0;
       pp.same_ab = pr.same_ab ? 1 : 0;
       pp.kmode = pr.kmode;
+      pp.colmajor = pr.M < pr.N ? 1 : 0;
       pp.splits = 1;
       pp.csize = 1;
       pp.k_per_split = cdiv(pr.K, unit) * unit;
@@ -2247,6 +2287,7 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
       pp.upper = pr.upper ? 1 : 0;
       pp.same_ab = pr.same_ab ? 1 : 0;
       pp.kmode = pr.kmode;
+      pp.colmajor = pr.M < pr.N ? 1 : 0;
       pp.splits = sh.splits;
       pp.csize = sh.csize;
       pp.k_per_split = sh.kps;
