@@ -36,7 +36,8 @@ WORKLOADS = {"mlp4": "c2", "single_linear": "c1", "resnet18": "c3", "resnet50": 
              "resnet18_nchw": "c3", "resnet50_nchw": "c4", "resnet50_bf16_nchw": "c4bf16",
              "transformer4_qkv_tied": "c5", "mlp4_ikfac": "c2",
              "resnet18_diag_nchw": "c3", "mlp4_ikfac_bf16": "c2",
-             "transformer4_ikfac_bf16": "c5", "transformer1": "c5b1"}
+             "transformer4_ikfac_bf16": "c5", "transformer1": "c5b1",
+             "transformer4_bf16_precond": "c5", "mlp4_bf16_precond": "c2"}
 # workloads whose convolutions hand the library their NCHW input and output
 # gradient (kfac_update_factors_conv2d_batched) instead of unfolded matrices
 NCHW_WORKLOADS = {"resnet18_nchw", "resnet50_nchw", "resnet50_bf16_nchw", "resnet18_diag_nchw"}
@@ -51,6 +52,8 @@ TIED_WORKLOADS = {"transformer4_qkv_tied"}
 # or on bf16 tensor cores
 IKFAC_WORKLOADS = {"mlp4_ikfac", "mlp4_ikfac_bf16", "transformer4_ikfac_bf16"}
 IKFAC_BF16_WORKLOADS = {"mlp4_ikfac_bf16", "transformer4_ikfac_bf16"}
+# workloads whose preconditioning products run in bf16 (hp.math = KFAC_MATH_BF16)
+BF16_PRECOND_WORKLOADS = {"transformer4_bf16_precond", "mlp4_bf16_precond"}
 
 
 def qkv_ties(layers):
@@ -153,7 +156,8 @@ def workload_name(cfg, workload):
             + ("+all_layers_diagonal" if workload in DIAG_WORKLOADS else "")
             + ("+qkv_shared_A" if workload in TIED_WORKLOADS else "")
             + ("+inverse_free_refresh" if workload in IKFAC_WORKLOADS else "")
-            + ("_bf16" if workload in IKFAC_BF16_WORKLOADS else ""))
+            + ("_bf16" if workload in IKFAC_BF16_WORKLOADS else "")
+            + ("+bf16_preconditioning" if workload in BF16_PRECOND_WORKLOADS else ""))
 
 
 def path_dtype(layers, workload=None):
@@ -161,7 +165,8 @@ def path_dtype(layers, workload=None):
     tensor cores, fp32-accurate); factor products read bf16 inputs where the layer
     set has them; the bf16 inverse-free variants refresh with bf16 products."""
     d = "bf16-in/f32" if any(l.in_dtype == "bf16" for l in layers) else "f32"
-    return d + ("+bf16-refresh" if workload in IKFAC_BF16_WORKLOADS else "")
+    return (d + ("+bf16-refresh" if workload in IKFAC_BF16_WORKLOADS else "")
+            + ("+bf16-precond" if workload in BF16_PRECOND_WORKLOADS else ""))
 
 
 # ----------------------------------------------------------------------------- accounting
@@ -403,7 +408,9 @@ def run_gpu(args, peaks, peak_kind):
     mode = (K.KFAC_IKFAC_BF16 if args.workload in IKFAC_BF16_WORKLOADS
             else K.KFAC_IKFAC_TF32 if ikfac else K.KFAC_IKFAC_OFF)
     h = K.Kfac(descs, ema_decay=hp.ema_decay, damping=hp.damping, lr=hp.lr, momentum=hp.momentum,
-               weight_decay=hp.weight_decay, max_rows=max_rows, device=dev, ikfac=mode)
+               weight_decay=hp.weight_decay, max_rows=max_rows, device=dev, ikfac=mode,
+               math=(K.KFAC_MATH_BF16 if args.workload in BF16_PRECOND_WORKLOADS
+                     else K.KFAC_MATH_3XTF32))
     ties = qkv_ties(layers) if args.workload in TIED_WORKLOADS else {}
     for li, src in ties.items():
         h.tie_a_factor(li, src)
@@ -679,15 +686,24 @@ def run_gpu(args, peaks, peak_kind):
         flop = acc["factor_flop"] if dom == "factor" else acc["precond_flop"]
         ms = phase_ms[0] if dom == "factor" else phase_ms[2]
         ach = flop / (ms * 1e-3) / 1e12
-        kern = ("pack_grouped_kernel + gemm_tc (persistent or split-K grouped) with the SYRK "
-                "epilogue (3xTF32, tcgen05)"
+        # the products' own arithmetic sets the peak: bf16 operands (bf16 inputs in the
+        # factor phase, bf16 preconditioning) against the bf16 peak, fp32 operands
+        # (three TF32 products each) against the TF32 peak
+        bf = (all(l.in_dtype == "bf16" for l in layers if l.kind == "kron") if dom == "factor"
+              else args.workload in BF16_PRECOND_WORKLOADS)
+        arith = "bf16" if bf else "3xTF32"
+        peak = peaks["bf16_tflops"] if bf else tf32_peak
+        kern = (f"pack_grouped + gemm_tc_pair/persistent (tcgen05) with the SYRK epilogue ({arith})"
                 if dom == "factor" else
-                "gradhat_pack_grouped_kernel + gemm_tc (persistent or split-K grouped) with the "
-                "SPLIT epilogue, then the PRECOND epilogue (3xTF32, tcgen05)")
-        roof = {"bound": "tensor", "achieved": round(ach, 3), "peak": round(tf32_peak, 1),
+                f"gradhat_pack_grouped + gemm_tc_pair/persistent (tcgen05) with the SPLIT epilogue, "
+                f"then the PRECOND epilogue ({arith})")
+        roof = {"bound": "tensor", "achieved": round(ach, 3), "peak": round(peak, 1),
                 "unit": "TFLOP/s", "kernel": kern, "timed": "one batched library call (the phase)",
-                "issued_frac": round(3 * ach / tf32_peak, 4),
-                "note": "algorithmic flops (upper triangle for factors); 3xTF32 issues 3x"}
+                "arithmetic": arith}
+        if not bf:
+            roof["issued_frac"] = round(3 * ach / tf32_peak, 4)
+        roof["note"] = ("algorithmic flops (upper triangle for factors)"
+                        + ("" if bf else "; 3xTF32 issues 3x"))
     else:
         ach = acc["invert_flop"] * k / (inv_ms_refresh * 1e-3) / 1e12
         roof = {"bound": "alu", "achieved": round(ach, 3), "peak": round(FP32_ALU_TFLOPS, 1),
@@ -703,7 +719,8 @@ def run_gpu(args, peaks, peak_kind):
     roof["phase"] = dom
     roof["peak_source"] = {
         "hbm": f"{peak_kind} HBM copy bandwidth",
-        "tensor": f"{peak_kind} bf16 dense x 1.1/2.25 (nominal TF32:bf16 ratio)",
+        "tensor": (f"{peak_kind} bf16 dense (burst)" if roof.get("arithmetic") == "bf16" else
+                   f"{peak_kind} bf16 dense (burst) x 1.1/2.25 (nominal TF32:bf16 ratio)"),
         "alu": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz"}[roof["bound"]]
 
     e2e = None

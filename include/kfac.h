@@ -70,8 +70,11 @@ typedef enum { KFAC_KRON = 0, KFAC_DIAG = 1 } kfac_kind;
 typedef enum { KFAC_F32 = 0, KFAC_BF16 = 1 } kfac_dtype;
 /* Arithmetic of the preconditioning GEMMs.  3XTF32: fp32 operands split into
  * two TF32 halves, three tensor-core products, fp32 accumulation (matches fp32
- * to ~1e-6).  BF16 (inverses and gradients rounded to bf16) is reserved:
- * kfac_create and kfac_set_hparams return KFAC_ERR_UNSUPPORTED for it. */
+ * to ~1e-6).  BF16: the inverses (rounded at each refresh), the gradient and
+ * the intermediate X = dW-hat A^{-1} rounded to bf16, one bf16 tensor-core
+ * product each with fp32 accumulation; factors, EMA, inverses and the
+ * momentum / parameter update stay fp32 (P within ~1e-2 of fp32).  Fixed at
+ * kfac_create (kfac_set_hparams rejects a change). */
 typedef enum { KFAC_MATH_3XTF32 = 0, KFAC_MATH_BF16 = 1 } kfac_math;
 /* Start of the running averages: ZERO gives F_1 = (1-xi) F_new; FIRST gives F_1 = F_new. */
 typedef enum { KFAC_EMA_INIT_ZERO = 0, KFAC_EMA_INIT_FIRST = 1 } kfac_ema_init;

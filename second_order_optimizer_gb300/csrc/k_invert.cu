@@ -397,16 +397,23 @@ __global__ void __launch_bounds__(256) panel_split_kernel(const __grid_constant_
   }
 }
 
-// Finv -> TF32 halves with a 16-byte row pitch, the operand form of the K4 products.
-__global__ void __launch_bounds__(256) inv_split_kernel(const InvJob* jobs) {
+// Finv -> the operand form of the K4 products: TF32 halves with a 16-byte row
+// pitch (np), or, for bf16 preconditioning, bf16 values in the hi array with a
+// row pitch of 2 np elements.
+__global__ void __launch_bounds__(256) inv_split_kernel(const InvJob* jobs, int bf16) {
   pdl_wait();
   pdl_trigger();
   const InvJob J = jobs[blockIdx.y];
   const int64_t nn = (int64_t)J.n * J.n;
+  __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(J.Finv_hi);
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
        e += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = e / J.n, c = e % J.n;
     const float v = J.Finv[e];
+    if (bf16) {
+      ob[r * 2 * J.np + c] = __float2bfloat16_rn(v);
+      continue;
+    }
     const float hi = tc::to_tf32(v);
     J.Finv_hi[r * J.np + c] = hi;
     J.Finv_lo[r * J.np + c] = tc::to_tf32(v - hi);
@@ -740,7 +747,15 @@ kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
   }
   if (kfac_status e = join_side()) return e;
   for (int s = NB; s < nmax; s *= 2) {
-    if (s >= kTcLevelMin) {   // the wide levels on the tensor cores
+    // the wide levels on the tensor cores, when they carry a few waves of work:
+    // at least about four 128 x 128 x 512 tiles per SM over all factors' pairs
+    // (smaller levels run faster as the CUDA-core tiles below)
+    double level_fma = 0;
+    for (int i = j0; i < j0 + nj; ++i) {
+      const int n = h->invjobs_host[i].n;
+      for (int b0 = s; b0 < n; b0 += 2 * s) level_fma += 2.0 * (double)s * s * std::min(s, n - b0);
+    }
+    if (s >= kTcLevelMin && level_fma >= 4.0 * num_sms() * 128 * 128 * 512) {
       kfac_status e = launch_tri_level_tc(h, j0, nj, s, st);
       if (e == KFAC_OK) continue;
       if (e != KFAC_ERR_WORKSPACE) return e;
@@ -770,7 +785,8 @@ kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
   }
   if (!big.empty())
     if (kfac_status e = launch_syrk_tc_batched(h, big.data(), (int)big.size(), st)) return e;
-  launch_pdl(inv_split_kernel, dim3(dim3((unsigned)std::min<int64_t>(cdiv((int64_t)nmax * nmax, 256), 1024), nj)), dim3(256), 0, st, jobs);
+  launch_pdl(inv_split_kernel, dim3(dim3((unsigned)std::min<int64_t>(cdiv((int64_t)nmax * nmax, 256), 1024), nj)), dim3(256), 0, st, jobs,
+             (int)(h->hp.math == KFAC_MATH_BF16));
   count_launch();
   if (kfac_status e = check_launch()) return e;
   // inverse-free update: K = X^T (so K K^T = X^T X = F_d^{-1}), and K^T = X
@@ -1066,7 +1082,8 @@ kfac_status launch_ikfac_update_bf16(kfac_ctx* h, const InvJob* jobs, int j0, in
   }
   if (kfac_status e = launch_gemm_tc_grouped(h, true, TC_EPI_SYRK, pr.data(), (int)pr.size(), st))
     return e;
-  launch_pdl(inv_split_kernel, dim3(elem_blocks(nmax), nj), dim3(256), 0, st, jobs);
+  launch_pdl(inv_split_kernel, dim3(elem_blocks(nmax), nj), dim3(256), 0, st, jobs,
+             (int)(h->hp.math == KFAC_MATH_BF16));
   count_launch();
   return check_launch();
 }
@@ -1144,7 +1161,8 @@ kfac_status launch_ikfac_update(kfac_ctx* h, int layer, float beta, cudaStream_t
   products(3, &pr);
   if (kfac_status e = launch_gemm_tc_grouped(h, false, TC_EPI_SYRK, pr.data(), (int)pr.size(), st))
     return e;
-  launch_pdl(inv_split_kernel, dim3(elem_blocks(nmax), nj), dim3(256), 0, st, jobs);
+  launch_pdl(inv_split_kernel, dim3(elem_blocks(nmax), nj), dim3(256), 0, st, jobs,
+             (int)(h->hp.math == KFAC_MATH_BF16));
   count_launch();
   return check_launch();
 }

@@ -28,30 +28,13 @@ namespace kfac {
 
 namespace {
 
-__global__ void __launch_bounds__(256) gradhat_pack_kernel(const float* __restrict__ gw, int64_t ld,
-                                                           const float* __restrict__ gb, int o,
-                                                           int d_in, int n, int64_t np,
-                                                           float* hi, float* lo) {
-  pdl_wait();
-  pdl_trigger();
-  const int64_t total = (int64_t)o * n;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t i = e / n, j = e % n;
-    const float v = j < d_in ? gw[i * ld + j] : gb[i];
-    const float h = tc::to_tf32(v);
-    hi[i * np + j] = h;
-    lo[i * np + j] = tc::to_tf32(v - h);
-  }
-}
-
 struct GradPackJob {
   const float* gw;
   const float* gb;
   int64_t ld, np;
   int o, d_in, n;
   float* hi;
-  float* lo;
+  float* lo;      // null: bf16 values in hi, row pitch 2 np elements
 };
 constexpr int kMaxGradPack = 16;
 struct GradPackGroup {
@@ -66,6 +49,13 @@ __global__ void __launch_bounds__(256) gradhat_pack_grouped_kernel(
   // a CTA takes whole rows (no index division), its threads along the row
   for (int i = blockIdx.x; i < J.o; i += gridDim.x) {
     const float* src = J.gw + (int64_t)i * J.ld;
+    if (!J.lo) {   // bf16 operand
+      __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(J.hi) + (int64_t)i * 2 * J.np;
+#pragma unroll 4
+      for (int j = threadIdx.x; j < J.n; j += blockDim.x)
+        b[j] = __float2bfloat16_rn(j < J.d_in ? __ldg(src + j) : J.gb[i]);
+      continue;
+    }
     float* hi = J.hi + (int64_t)i * J.np;
     float* lo = J.lo + (int64_t)i * J.np;
 #pragma unroll 4
@@ -83,46 +73,11 @@ __global__ void __launch_bounds__(256) gradhat_pack_grouped_kernel(
 kfac_status launch_precondition(kfac_ctx* h, int layer, const float* gw, int64_t ldgw,
                                 const float* gb, float* ow, float* ob, float* pw, float* pb,
                                 cudaStream_t st) {
-  const LayerInfo& L = h->layers[layer];
-  const int64_t np = tc_pitch(L.n, false), op = tc_pitch(L.o, false);
-  if ((size_t)(2 * L.o * np + 2 * L.n * op) > h->k4tmp_floats) return KFAC_ERR_WORKSPACE;
-  float* g_hi = h->at<float>(h->off_k4tmp);
-  float* g_lo = g_hi + (size_t)L.o * np;
-  float* x_hi = g_lo + (size_t)L.o * np;
-  float* x_lo = x_hi + (size_t)L.n * op;
-  {
-    const int64_t total = (int64_t)L.o * L.n;
-    const unsigned blocks = (unsigned)std::min<int64_t>(cdiv(total, 256), 4 * num_sms());
-    launch_pdl(gradhat_pack_kernel, dim3(blocks), dim3(256), 0, st, gw, ldgw, gb, L.o, L.d_in, L.n, np, g_hi, g_lo);
-    count_launch();
-    if (kfac_status e = check_launch()) return e;
-  }
-  // X = grad-hat . Ainv  [o x n] (Ainv symmetric), stored transposed as X^T [n x o]
-  TcOperand Ainv{h->at<float>(L.Ainv_hi), h->at<float>(L.Ainv_lo), L.n, np};
-  TcOperand G{g_hi, g_lo, L.o, np};
-  TcEpilogue e1{};
-  e1.out_hi = x_hi;
-  e1.out_lo = x_lo;
-  e1.ldo = op;
-  if (kfac_status e = launch_gemm_tc(h, layer, false, TC_EPI_SPLIT, G, Ainv, false, false, L.o,
-                                     L.n, L.n, e1, st))
-    return e;
-  TcOperand Ginv{h->at<float>(L.Ginv_hi), h->at<float>(L.Ginv_lo), L.o, op};
-  TcOperand XT{x_hi, x_lo, L.n, op};
-  TcEpilogue e2{};
-  e2.d_in = L.d_in;
-  e2.eta = (float)h->hp.lr;
-  e2.mu = (float)h->hp.momentum;
-  e2.lambda = (float)h->hp.weight_decay;
-  e2.ow = ow;
-  e2.ob = ob;
-  e2.pw = pw;
-  e2.pb = pb;
-  e2.mw = h->at<float>(L.m);
-  e2.mb = e2.mw + (size_t)L.o * L.d_in;
-  // P^T = X^T . Ginv  [n x o]: P = Ginv . X (Ginv symmetric), computed transposed
-  return launch_gemm_tc(h, layer, false, TC_EPI_PRECOND, XT, Ginv, false, false, L.n, L.o, L.o,
-                        e2, st);
+  // one layer through the batched path (the products of a group of one layer are
+  // single products there)
+  return launch_precondition_batched(h, 1, &layer, &gw, &ldgw, &gb, ow ? &ow : nullptr,
+                                     ob ? &ob : nullptr, pw ? &pw : nullptr, pb ? &pb : nullptr,
+                                     st);
 }
 
 // Several layers at once: one pack launch for all gradients, then each of the two
@@ -133,6 +88,9 @@ kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layer
                                         const float* const* gb, float* const* ow,
                                         float* const* ob, float* const* pw, float* const* pb,
                                         cudaStream_t st) {
+  // bf16 preconditioning: gradients, inverses and X^T as bf16 (row pitch 2 np / 2 op
+  // elements, in the storage of the TF32 hi halves), one bf16 product each
+  const bool bf = h->hp.math == KFAC_MATH_BF16;
   std::vector<TcProblem> p1, p2;
   GradPackGroup gp;
   std::memset(&gp, 0, sizeof(gp));
@@ -145,8 +103,8 @@ kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layer
     launch_pdl(gradhat_pack_grouped_kernel, dim3(dim3(blocks, ng)), dim3(256), 0, st, gp);
     count_launch();
     kfac_status e = check_launch();
-    if (e == KFAC_OK) e = launch_gemm_tc_grouped(h, false, TC_EPI_SPLIT, p1.data(), ng, st);
-    if (e == KFAC_OK) e = launch_gemm_tc_grouped(h, false, TC_EPI_PRECOND, p2.data(), ng, st);
+    if (e == KFAC_OK) e = launch_gemm_tc_grouped(h, bf, TC_EPI_SPLIT, p1.data(), ng, st);
+    if (e == KFAC_OK) e = launch_gemm_tc_grouped(h, bf, TC_EPI_PRECOND, p2.data(), ng, st);
     p1.clear();
     p2.clear();
     ng = 0;
@@ -176,22 +134,25 @@ kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layer
     j.d_in = L.d_in;
     j.n = L.n;
     j.hi = g_hi;
-    j.lo = g_lo;
+    j.lo = bf ? nullptr : g_lo;
     max_rows = std::max<int64_t>(max_rows, L.o);
+    const int64_t npb = bf ? 2 * np : np, opb = bf ? 2 * op : op;   // operand pitches
     TcProblem q1{};
-    q1.A = TcOperand{g_hi, g_lo, L.o, np};   // X = grad-hat . Ainv, stored as X^T
-    q1.B = TcOperand{h->at<float>(L.Ainv_hi), h->at<float>(L.Ainv_lo), L.n, np};
+    q1.A = TcOperand{g_hi, bf ? nullptr : g_lo, L.o, npb};   // X = grad-hat . Ainv, as X^T
+    q1.B = TcOperand{h->at<float>(L.Ainv_hi), bf ? nullptr : h->at<float>(L.Ainv_lo), L.n, npb};
     q1.M = L.o;
     q1.N = L.n;
     q1.K = L.n;
     q1.e.out_hi = x_hi;
-    q1.e.out_lo = x_lo;
-    q1.e.ldo = op;
+    q1.e.out_lo = bf ? nullptr : x_lo;
+    q1.e.out_bf16 = bf ? 1 : 0;
+    q1.e.alpha = 1.f;
+    q1.e.ldo = opb;
     q1.layer = layers[i];
     p1.push_back(q1);
     TcProblem q2{};
-    q2.A = TcOperand{x_hi, x_lo, L.n, op};   // P^T = X^T . Ginv
-    q2.B = TcOperand{h->at<float>(L.Ginv_hi), h->at<float>(L.Ginv_lo), L.o, op};
+    q2.A = TcOperand{x_hi, bf ? nullptr : x_lo, L.n, opb};   // P^T = X^T . Ginv
+    q2.B = TcOperand{h->at<float>(L.Ginv_hi), bf ? nullptr : h->at<float>(L.Ginv_lo), L.o, opb};
     q2.M = L.n;
     q2.N = L.o;
     q2.K = L.o;

@@ -367,7 +367,6 @@ kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_
   size_t need = 0;
   if (kfac_status e = kfac_workspace_size(layers, n_layers, hp, max_rows, &need)) return e;
   if (!d_workspace || !aligned(d_workspace, kAlign) || bytes < need) return KFAC_ERR_WORKSPACE;
-  if (hp->math != KFAC_MATH_3XTF32) return KFAC_ERR_UNSUPPORTED;
   Plan P;
   make_plan(layers, n_layers, max_rows, hp, &P);
   kfac_ctx* h = new (std::nothrow) kfac_ctx();
@@ -421,7 +420,7 @@ kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_
 kfac_status kfac_set_hparams(kfac_handle h, const kfac_hparams* hp) {
   if (!h || !valid_hp(hp)) return KFAC_ERR_INVALID_ARG;
   if (hp->ikfac != h->hp.ikfac) return KFAC_ERR_INVALID_ARG;   // fixed at creation
-  if (hp->math != KFAC_MATH_3XTF32) return KFAC_ERR_UNSUPPORTED;
+  if (hp->math != h->hp.math) return KFAC_ERR_INVALID_ARG;     // the inverses' storage form
   h->hp = *hp;
   return KFAC_OK;
 }

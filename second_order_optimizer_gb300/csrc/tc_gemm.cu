@@ -172,7 +172,6 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_last = reinterpret_cast<int*>(tmem_slot + 2);
-  static_assert(EPI != TC_EPI_PRECOND || !kBF16, "preconditioning products read TF32 halves");
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   int ti, tj;
@@ -1890,8 +1889,8 @@ kfac_status dispatch(bool bf16, int epi, unsigned grid, const CUtensorMap& ah,
   if (epi == TC_EPI_SPLIT)
     return bf16 ? launch_kernel<true, BN, TC_EPI_SPLIT>(grid, ah, al, bh, bl, p, st)
                 : launch_kernel<false, BN, TC_EPI_SPLIT>(grid, ah, al, bh, bl, p, st);
-  if (bf16) return KFAC_ERR_UNSUPPORTED;
-  return launch_kernel<false, BN, TC_EPI_PRECOND>(grid, ah, al, bh, bl, p, st);
+  return bf16 ? launch_kernel<true, BN, TC_EPI_PRECOND>(grid, ah, al, bh, bl, p, st)
+              : launch_kernel<false, BN, TC_EPI_PRECOND>(grid, ah, al, bh, bl, p, st);
 }
 
 kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProblem* probs,
@@ -2102,20 +2101,18 @@ kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProb
       else if (epi == TC_EPI_SPLIT)
         e = bf16 ? launch_pair_kernel<true, TC_EPI_SPLIT>(*g, st)
                  : launch_pair_kernel<false, TC_EPI_SPLIT>(*g, st);
-      else if (bf16)
-        e = KFAC_ERR_UNSUPPORTED;
       else
-        e = launch_pair_kernel<false, TC_EPI_PRECOND>(*g, st);
+        e = bf16 ? launch_pair_kernel<true, TC_EPI_PRECOND>(*g, st)
+                 : launch_pair_kernel<false, TC_EPI_PRECOND>(*g, st);
     } else if (epi == TC_EPI_SYRK) {
       e = bf16 ? launch_persistent_kernel<true, TC_EPI_SYRK, BN>(*g, st)
                : launch_persistent_kernel<false, TC_EPI_SYRK, BN>(*g, st);
     } else if (epi == TC_EPI_SPLIT) {
       e = bf16 ? launch_persistent_kernel<true, TC_EPI_SPLIT, BN>(*g, st)
                : launch_persistent_kernel<false, TC_EPI_SPLIT, BN>(*g, st);
-    } else if (bf16) {
-      e = KFAC_ERR_UNSUPPORTED;
     } else {
-      e = launch_persistent_kernel<false, TC_EPI_PRECOND, BN>(*g, st);
+      e = bf16 ? launch_persistent_kernel<true, TC_EPI_PRECOND, BN>(*g, st)
+               : launch_persistent_kernel<false, TC_EPI_PRECOND, BN>(*g, st);
     }
     if (e) return e;
   }
@@ -2240,10 +2237,9 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
       else if (epi == TC_EPI_SPLIT)
         e = bf16 ? launch_grouped_kernel<true, TC_EPI_SPLIT>(blocks, *g, st)
                  : launch_grouped_kernel<false, TC_EPI_SPLIT>(blocks, *g, st);
-      else if (bf16)
-        e = KFAC_ERR_UNSUPPORTED;
       else
-        e = launch_grouped_kernel<false, TC_EPI_PRECOND>(blocks, *g, st);
+        e = bf16 ? launch_grouped_kernel<true, TC_EPI_PRECOND>(blocks, *g, st)
+                 : launch_grouped_kernel<false, TC_EPI_PRECOND>(blocks, *g, st);
       std::memset(g.get(), 0, sizeof(GroupedTc));
       g->csize = csize;
       blocks = 0;

@@ -219,6 +219,58 @@ def test_precondition_and_update_match_oracle(M, d_in, o, bias):
     assert h.get_status()[0] == 0
 
 
+@pytest.mark.parametrize("batched", [False, True])
+def test_bf16_preconditioning_within_the_bf16_tolerance(batched):
+    """hp.math = KFAC_MATH_BF16: the inverses (at each refresh), the gradient and
+    X = dW-hat A^{-1} rounded to bf16, one bf16 tensor-core product each (fp32
+    accumulate); factors, inverses and the update stay fp32.  P, m and W against
+    the float64 oracle's step at the bf16 path's 2e-2 (relative Frobenius), three
+    steps with a refresh at the first and third; ragged and bias-less shapes."""
+    shapes = [(1000, 300, 200, 1), (600, 129, 70, 0), (1500, 1024, 1030, 1)]   # M, d_in, o, bias
+    h = K.Kfac([(K.KFAC_KRON, o, d, b, K.KFAC_F32) for _, d, o, b in shapes],
+               max_rows=max(M for M, *_ in shapes), math=K.KFAC_MATH_BF16, **HP)
+    orc = _orc(invert_every=2)
+    st, pw, pb = [], [], []
+    for _, d, o, b in shapes:
+        w0 = (RNG.standard_normal((o, d)) * 0.1).astype(np.float32)
+        b0 = (RNG.standard_normal(o) * 0.1).astype(np.float32) if b else None
+        st.append(O.LayerState("kron", o, d, b, w0, b0))
+        pw.append(to_dev(w0))
+        pb.append(to_dev(b0) if b else None)
+    worst = 0.0
+    for t in range(3):
+        ins = []
+        for M, d, o, b in shapes:
+            a, g = _inputs(M, d, o)
+            gw = (RNG.standard_normal((o, d)) * 1e-3).astype(np.float32)
+            gb = (RNG.standard_normal(o) * 1e-3).astype(np.float32) if b else None
+            ins.append((a, g, gw, gb))
+        for li, (a, g, _, _) in enumerate(ins):
+            h.update_factors(li, to_dev(a), to_dev(g))
+        if t % 2 == 0:
+            h.invert(-1)
+        ow = [torch.empty(o, d, device="cuda") for _, d, o, _ in shapes]
+        ob = [torch.empty(o, device="cuda") if b else None for _, _, o, b in shapes]
+        gws = [to_dev(x[2]) for x in ins]
+        gbs = [to_dev(x[3]) if x[3] is not None else None for x in ins]
+        if batched:
+            h.precondition_batched(list(range(len(shapes))), gws, gbs, ow, ob, pw, pb)
+        else:
+            for li in range(len(shapes)):
+                h.precondition(li, gws[li], gbs[li], ow[li], ob[li], pw[li], pb[li])
+        for li, (a, g, gw, gb) in enumerate(ins):
+            b = shapes[li][3]
+            P = orc.step_kron(st[li], a, g, gw, gb)
+            errs = [rel_fro(O.grad_hat(to_np(ow[li]), to_np(ob[li]) if b else None), P),
+                    rel_fro(O.grad_hat(to_np(pw[li]), to_np(pb[li]) if b else None), st[li].W)]
+            mw, mb = h.momentum(li)
+            errs.append(rel_fro(O.grad_hat(to_np(mw), to_np(mb) if b else None), st[li].m))
+            worst = max(worst, errs[0])
+            assert max(errs) <= 2e-2, (t, li, errs)
+    print(f"bf16 preconditioning ({'batched' if batched else 'per layer'}): worst P {worst:.2e}")
+    assert h.get_status()[0] == 0
+
+
 # ------------------------------------------------------------------ K5 / K6 diagonal
 
 @pytest.mark.parametrize("M,d_in,o,bias,dtype", [(3000, 257, 100, 1, "f32"), (50, 3, 2, 0, "f32"),
