@@ -839,6 +839,39 @@ __device__ __forceinline__ void grouped_tile(const GroupedTc& g, int t, int* q, 
   *q = k;
 }
 
+// Start of a drained tile's running sum.  SYRK with an EMA (beta != 0) starts from
+// the old factor value, read from where the epilogue will write it (the mirror
+// half, row gc, column gr <= gc), so that the loads run while the tile's first
+// partial accumulates and the epilogue has none.  With |alpha| <= |beta| the sum
+// starts at C_old and takes each drained partial times alpha / beta (epilogue
+// scale beta); otherwise it starts at (beta / alpha) C_old and takes the partials
+// as they are (epilogue scale alpha): either way the scaled sum is
+// beta C_old + alpha S, and no factor above 1 can overflow.  Returns the
+// partials' scale; *oscale is the epilogue's.
+template <int EPI, int CW>
+__device__ __forceinline__ float sum_init(const TcEpilogue& E, float (&sum)[CW], int64_t c0,
+                                          int64_t gr, int64_t pM, int64_t pN, float* oscale) {
+  if (EPI == TC_EPI_SYRK && E.beta != 0.f) {
+    const bool by_beta = fabsf(E.alpha) <= fabsf(E.beta);
+    const float r = by_beta ? 1.f : E.beta / E.alpha;
+#pragma unroll
+    for (int c = 0; c < CW; ++c) {
+      const int64_t gc = c0 + c;
+      sum[c] = (gr < pM && gc < pN && gr <= gc) ? __ldcg(E.C + gc * E.ldc + gr) : 0.f;
+    }
+    if (!by_beta) {
+#pragma unroll
+      for (int c = 0; c < CW; ++c) sum[c] *= r;
+    }
+    *oscale = by_beta ? E.beta : E.alpha;
+    return by_beta ? E.alpha / E.beta : 1.f;
+  }
+#pragma unroll
+  for (int c = 0; c < CW; ++c) sum[c] = 0.f;
+  *oscale = E.alpha;
+  return 1.f;
+}
+
 // Epilogue of a drained tile from registers (the persistent kernels): this thread
 // holds accumulator row gr for the CW columns from c0.  Every store runs along
 // rows across the warp (C^T-oriented), except the SYRK direct half, which goes
@@ -848,27 +881,19 @@ template <int EPI, int CW, int XW, int EB>
 __device__ __forceinline__ void epilogue_from_registers(const TcEpilogue& E, float (&sum)[CW],
                                                         float* xb, int lane, int qd, int64_t r0,
                                                         int64_t c0, int64_t gr, int64_t pM,
-                                                        int64_t pN) {
+                                                        int64_t pN, float oscale) {
   constexpr int XP = XW + 1;
   if (EPI == TC_EPI_SYRK) {
-    // mirror F[gc][gr] from registers, old value from the same place
+    // mirror F[gc][gr]: oscale * (the running sum started by sum_init)
 #pragma unroll
-    for (int cc = 0; cc < CW; cc += EB) {
-      float old[EB];
-#pragma unroll
-      for (int u = 0; u < EB; ++u) {
-        const int64_t gc = c0 + cc + u;
-        const bool okc = gr < pM && gc < pN && gr <= gc;
-        old[u] = (okc && E.beta != 0.f) ? __ldcg(E.C + gc * E.ldc + gr) : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < EB; ++u) {
-        const int64_t gc = c0 + cc + u;
-        const float v = fmaf(E.beta, old[u], E.alpha * sum[cc + u]);
-        sum[cc + u] = v;
-        if (gr < pM && gc < pN && gr <= gc) E.C[gc * E.ldc + gr] = v;
-      }
+    for (int c = 0; c < CW; ++c) {
+      const int64_t gc = c0 + c;
+      const float v = oscale * sum[c];
+      sum[c] = v;
+      if (gr < pM && gc < pN && gr <= gc) E.C[gc * E.ldc + gr] = v;
     }
+  }
+  if (EPI == TC_EPI_SYRK) {
     // direct half F[gr][gc] (gr < gc): blocks of 32 rows x XW columns turned
     // through the warp's buffer so that lanes run along gc
     constexpr int RPI = 32 / XW;   // rows per store instruction
@@ -1128,12 +1153,7 @@ __device__ __forceinline__ void persistent_body(const GroupedTc& g) {
       const int nkb = kblocks(q, tj, &kb_lo);
       const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
       if (gr < pM) {   // the tile's epilogue inputs into L2 while the drains run
-        if (EPI == TC_EPI_SYRK && E.beta != 0.f) {
-          for (int c = 0; c < CW; ++c) {
-            const int64_t gc = c0 + c;
-            if (gc < pN && gr <= gc) tc::prefetch_l2(E.C + gc * E.ldc + gr);
-          }
-        } else if (EPI == TC_EPI_PRECOND && E.pw && gr < E.d_in) {
+        if (EPI == TC_EPI_PRECOND && E.pw && gr < E.d_in) {
           for (int c = 0; c < CW; ++c) {
             const int64_t i = c0 + c;
             if (i >= pN) break;
@@ -1143,8 +1163,8 @@ __device__ __forceinline__ void persistent_body(const GroupedTc& g) {
         }
       }
       float sum[CW];
-#pragma unroll
-      for (int c = 0; c < CW; ++c) sum[c] = 0.f;
+      float oscale;
+      const float kin = sum_init<EPI, CW>(E, sum, c0, gr, pM, pN, &oscale);
       for (int sub = 0; sub < nsub; ++sub, ++gsub) {
         const int buf = gsub % PC::ACC, use = gsub / PC::ACC;
         if (!tc::mbar_wait(&acc_full[buf], use & 1, abort_flag)) {
@@ -1161,7 +1181,7 @@ __device__ __forceinline__ void persistent_body(const GroupedTc& g) {
             tc::tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) +
                               (uint32_t)(buf * BN + h * CW + cc * 32), v);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) sum[cc * 32 + i] += v[i];
+            for (int i = 0; i < 32; ++i) sum[cc * 32 + i] = fmaf(kin, v[i], sum[cc * 32 + i]);
           }
         } else {   // fewer registers per drain thread (16 drain warps)
 #pragma unroll
@@ -1170,7 +1190,7 @@ __device__ __forceinline__ void persistent_body(const GroupedTc& g) {
             tc::tmem_ld16(tmem + ((uint32_t)(32 * qd) << 16) +
                               (uint32_t)(buf * BN + h * CW + cc * 16), v);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) sum[cc * 16 + i] += v[i];
+            for (int i = 0; i < 16; ++i) sum[cc * 16 + i] = fmaf(kin, v[i], sum[cc * 16 + i]);
           }
         }
         tc::tc_fence_before();
@@ -1178,7 +1198,7 @@ __device__ __forceinline__ void persistent_body(const GroupedTc& g) {
       }
       if (!ok) break;
       epilogue_from_registers<EPI, CW, PC::XW, BN == 128 ? 16 : 8>(E, sum, xb, lane, qd, r0, c0, gr,
-                                                                   pM, pN);
+                                                                   pM, pN, oscale);
     }
   }
   tc::tc_fence_before();
@@ -1422,13 +1442,9 @@ __device__ __forceinline__ void pair_body(const GroupedTc& g) {
       int kb_lo;
       const int nkb = kblocks(q, tj, &kb_lo);
       const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
-      if (gr < pM) {   // the tile's epilogue inputs into L2 while the drains run
-        if (EPI == TC_EPI_SYRK && E.beta != 0.f) {
-          for (int c = 0; c < CW; ++c) {
-            const int64_t gc = c0 + c;
-            if (gc < pN && gr <= gc) tc::prefetch_l2(E.C + gc * E.ldc + gr);
-          }
-        } else if (EPI == TC_EPI_PRECOND && E.pw && gr < E.d_in) {
+      auto prefetch_epilogue = [&]() {   // the tile's epilogue inputs into L2
+        if (gr >= pM) return;
+        if (EPI == TC_EPI_PRECOND && E.pw && gr < E.d_in) {
           for (int c = 0; c < CW; ++c) {
             const int64_t i = c0 + c;
             if (i >= pN) break;
@@ -1436,11 +1452,13 @@ __device__ __forceinline__ void pair_body(const GroupedTc& g) {
             tc::prefetch_l2(E.mw + i * E.d_in + gr);
           }
         }
-      }
+      };
+      const int pf_sub = max(0, nsub - 2);   // late enough that the lines stay in L2
       float sum[CW];
-#pragma unroll
-      for (int c = 0; c < CW; ++c) sum[c] = 0.f;
+      float oscale;
+      const float kin = sum_init<EPI, CW>(E, sum, c0, gr, pM, pN, &oscale);
       for (int sub = 0; sub < nsub; ++sub, ++gsub) {
+        if (sub == pf_sub) prefetch_epilogue();
         const int buf = gsub % PC::ACC, use = gsub / PC::ACC;
         if (!tc::mbar_wait(&acc_full[buf], use & 1, abort_flag)) {
           report_error(g.prob[q].status, KFAC_ERR_TIMEOUT, g.prob[q].layer, 24);
@@ -1455,14 +1473,14 @@ __device__ __forceinline__ void pair_body(const GroupedTc& g) {
           tc::tmem_ld16(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * BN + h * CW + cc * 16),
                         v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) sum[cc * 16 + i] += v[i];
+          for (int i = 0; i < 16; ++i) sum[cc * 16 + i] = fmaf(kin, v[i], sum[cc * 16 + i]);
         }
         tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive_cluster(acc_empty0 + (uint32_t)(buf * sizeof(uint64_t)));
+        if (lane == 0) tc::mbar_arrive_remote(acc_empty0 + (uint32_t)(buf * sizeof(uint64_t)));
       }
       if (!ok) break;
-      epilogue_from_registers<EPI, CW, PC::XW, 8>(E, sum, xb, lane, qd, r0, c0, gr, pM, pN);
+      epilogue_from_registers<EPI, CW, PC::XW, 8>(E, sum, xb, lane, qd, r0, c0, gr, pM, pN, oscale);
     }
   }
   tc::tc_fence_before();
@@ -1763,10 +1781,13 @@ bool set_smem_attr() {
 // partial sum moves to fp32 registers.
 constexpr int kKsubTf32 = 128;
 constexpr int kKsubBf16 = 256;
-// k elements per TMEM drain of the 256-wide persistent bf16 products: 32 MMAs
-// (drift ~2e-6 relative per drain period), long enough that the drain warps
-// finish a tile's epilogue while the MMA runs one period ahead.
-constexpr int kKsubBf16Wide = 512;
+// k elements per TMEM drain of the 256-wide persistent and CTA-pair bf16 products:
+// 64 MMAs.  Measured on a 16384-row SYRK of o = 8192 against float64: 3.4e-7
+// relative at 512, 7.1e-7 at 1024, 1.9e-6 at 2048, 2.4e-5 with no drain.  Each
+// drain costs the drain warps about 2000 cycles and the pair's two accumulators
+// let the MMA run only two drain periods ahead of a tile's epilogue, so 1024 is
+// about 7% faster than 512 on that SYRK.
+constexpr int kKsubBf16Wide = 1024;
 // Products with a wave of wide tiles run on CTA pairs (256 x 256 tiles).
 constexpr bool kWidePairs = true;
 

@@ -167,9 +167,14 @@ __device__ __forceinline__ uint32_t mapa(const void* p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
+// Arrive on an mbarrier of either CTA of the pair (cluster address), with the
+// default release semantics at CTA scope.  The drain warps use it to hand a TMEM
+// accumulator back to the MMA issuer of the even CTA: their tcgen05.ld have
+// completed (tcgen05.wait::ld) before it, and a cluster-scope release would
+// first wait for the warp's epilogue stores to become visible to the cluster,
+// which the MMA issuer does not read.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // Every thread of both CTAs (warps need not be converged).
 __device__ __forceinline__ void cluster_sync() {
