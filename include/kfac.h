@@ -152,16 +152,23 @@ kfac_status kfac_set_hparams(kfac_handle h, const kfac_hparams* hp);
  * likewise; not both.  With the EMA_INIT_FIRST option each factor's first
  * update replaces it.
  * Osawa et al. §3.2 (factors), §3.4 (symmetry: only the upper triangle is
- * computed; the lower is its mirror); CAFIN Introduction (EMA of the factors). */
+ * computed; the lower is its mirror); CAFIN Introduction (EMA of the factors).
+ * bf16 inputs with lda (ldg) a multiple of 8, 16-byte aligned, and (for A with a
+ * bias) d_in a multiple of 64 are read in place by the tensor cores when the
+ * factor fills a wave of CTA pairs (the others are first packed into the
+ * workspace); the ones column then comes from a [max_rows x 64] bf16 matrix the
+ * workspace holds for handles with such layers. */
 kfac_status kfac_update_factors(kfac_handle h, int layer, const void* a, int64_t lda,
                                 const void* g, int64_t ldg, int64_t rows, double scale,
                                 cudaStream_t stream);
 
 /* K1 for several KRON layers in one pass: the same result as calling
  * kfac_update_factors(layers[i], a[i], lda[i], g[i], ldg[i], rows[i], scale)
- * for each i, but all inputs are packed in one launch and all the factor
+ * for each i, but the inputs are packed in one launch and all the factor
  * products run as one grouped tensor-core launch, so small layers fill the GPU
- * together.  Host arrays of length count; each layer at most once; all layers
+ * together; bf16 inputs that kfac_update_factors would read in place are read in
+ * place when together they fill a wave of CTA pairs, in one further launch.
+ * Host arrays of length count; each layer at most once; all layers
  * of one in_dtype.  Layers beyond what the workspace's batch scratch holds are
  * processed in further groups. */
 kfac_status kfac_update_factors_batched(kfac_handle h, int count, const int* layers,

@@ -211,8 +211,22 @@ kfac_status launch_update_factors_batched(kfac_ctx* h, int count, const int* lay
   const bool bf16 = h->layers[layers[0]].in_dtype == KFAC_BF16;
   const size_t elt = bf16 ? 2 : 8;  // packed bytes per element (bf16, or two TF32 halves)
   std::vector<PackJob> pj;
-  std::vector<TcProblem> pr;
+  std::vector<TcProblem> pr, direct;
   size_t used = 0;
+  // bf16 inputs that the CTA-pair SYRK can read in place (launch_syrk_direct) skip
+  // the pack, when together they fill at least one wave of CTA pairs
+  auto direct_ok = [&](int i, int w) {
+    const LayerInfo& L = h->layers[layers[i]];
+    const void* src = w == 0 ? a[i] : g[i];
+    return bf16 && !geoms && src &&
+           syrk_direct_layout_ok(h, src, w == 0 ? lda[i] : ldg[i], rows[i],
+                                 w == 0 ? L.d_in : L.o, w == 0 ? L.has_bias : 0);
+  };
+  int64_t direct_tiles = 0;
+  for (int i = 0; i < count; ++i)
+    for (int w = 0; w < 2; ++w)
+      if (direct_ok(i, w)) direct_tiles += syrk_pair_tiles(w == 0 ? h->layers[layers[i]].n : h->layers[layers[i]].o);
+  const bool use_direct = direct_tiles >= num_sms() / 2;
   auto flush = [&]() -> kfac_status {
     if (pr.empty()) return KFAC_OK;
     kfac_status e = launch_pack_grouped(pj.data(), (int)pj.size(), bf16, st);
@@ -225,8 +239,9 @@ kfac_status launch_update_factors_batched(kfac_ctx* h, int count, const int* lay
   for (int i = 0; i < count; ++i) {
     const LayerInfo& L = h->layers[layers[i]];
     const int64_t Kp = tc_pitch(rows[i], bf16);
-    const size_t bA = a[i] ? align_up((size_t)L.n * Kp * elt) : 0;
-    const size_t bG = g[i] ? align_up((size_t)L.o * Kp * elt) : 0;
+    const bool dA = use_direct && direct_ok(i, 0), dG = use_direct && direct_ok(i, 1);
+    const size_t bA = a[i] && !dA ? align_up((size_t)L.n * Kp * elt) : 0;
+    const size_t bG = g[i] && !dG ? align_up((size_t)L.o * Kp * elt) : 0;
     if (bA + bG > h->tcpack_bytes) return KFAC_ERR_WORKSPACE;
     if (used + bA + bG > h->tcpack_bytes)
       if (kfac_status e = flush()) return e;
@@ -237,6 +252,23 @@ kfac_status launch_update_factors_batched(kfac_ctx* h, int count, const int* lay
       const float decay = w == 0 ? decay_a[i] : decay_g[i];
       const float alpha = (float)((1.0 - (double)decay) * s);
       const int n = w == 0 ? L.n : L.o;
+      if (w == 0 ? dA : dG) {
+        TcProblem q{};
+        q.A = TcOperand{src, nullptr, w == 0 ? L.d_in : L.o, w == 0 ? lda[i] : ldg[i]};
+        q.B = q.A;
+        q.same_ab = true;
+        q.upper = true;
+        q.M = q.N = n;
+        q.K = rows[i];
+        q.bias_col = (w == 0 && L.has_bias) ? L.d_in : -1;
+        q.e.alpha = alpha;
+        q.e.beta = decay;
+        q.e.C = h->at<float>(w == 0 ? L.A : L.G);
+        q.e.ldc = n;
+        q.layer = layers[i];
+        direct.push_back(q);
+        continue;
+      }
       char* hi = h->ws + h->off_tcpack + used;
       char* lo = bf16 ? nullptr : hi + (size_t)n * Kp * 4;
       used += w == 0 ? bA : bG;
@@ -277,7 +309,8 @@ kfac_status launch_update_factors_batched(kfac_ctx* h, int count, const int* lay
       pr.push_back(q);
     }
   }
-  return flush();
+  if (kfac_status e = flush()) return e;
+  return direct.empty() ? KFAC_OK : launch_syrk_direct(h, direct.data(), (int)direct.size(), st);
 }
 
 }  // namespace kfac

@@ -65,6 +65,8 @@ struct Plan {
   size_t off_part_k4, off_tickets_k4;
   size_t off_k5part, k5part_floats, off_k5tickets, k5tickets_ints, off_invjobs, total;
   size_t off_tcpack, tcpack_bytes;
+  size_t off_ones;
+  int64_t ones_rows;
   int n_invjobs, max_kron_n;
 };
 
@@ -81,6 +83,7 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, const kfa
   size_t part = 0, tickets = 0, k4 = 0, k5 = 0, k5t = 0, tcpack = 0;
   size_t pack_sum = 0, k4_sum = 0, inv_pack_sum = 0;   // what a batch over every KRON layer would use
   int ninv = 0, maxn = 0;
+  bool ones = false;   // a bf16 KRON layer whose bias column the direct SYRK reads as ones
   for (int i = 0; i < nl; ++i) {
     const kfac_layer_desc& d = descs[i];
     LayerInfo L{};
@@ -115,6 +118,7 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, const kfa
       part = std::max(part, k1_scratch_floats(L.n, max_rows, &t1));
       part = std::max(part, k1_scratch_floats(L.o, max_rows, &t2));
       const bool bf = d.in_dtype == KFAC_BF16;
+      ones = ones || (bf && d.has_bias && d.d_in % 64 == 0);
       part = std::max(part, tc_part_floats());
       // a batched group of one layer holds its A and G packs at once
       tcpack = std::max(tcpack, align_up(tc_pack_bytes(L.n, max_rows, bf)) +
@@ -159,6 +163,8 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, const kfa
   P->off_tcpack = take(tcpack);
   P->k4tmp_floats = k4;
   P->off_k4tmp = take(k4 * sizeof(float));
+  P->ones_rows = ones ? max_rows : 0;
+  P->off_ones = take((size_t)P->ones_rows * 64 * 2);
   // batched K5 spreads about 2 x SMs CTAs over the group, one part row per CTA
   k5 = std::max(k5, (size_t)256 * (2 * num_sms() + k5t));
   P->k5part_floats = k5;
@@ -389,6 +395,8 @@ kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_
   h->off_tickets_k4 = P.off_tickets_k4;
   h->off_tcpack = P.off_tcpack;
   h->tcpack_bytes = P.tcpack_bytes;
+  h->off_ones = P.off_ones;
+  h->ones_rows = P.ones_rows;
   h->off_k4tmp = P.off_k4tmp;
   h->k4tmp_floats = P.k4tmp_floats;
   h->off_k5part = P.off_k5part;
@@ -407,6 +415,11 @@ kfac_status kfac_create(const kfac_layer_desc* layers, int n_layers, const kfac_
     }
   }
   bool ok = cudaMemset(d_workspace, 0, need) == cudaSuccess;
+  if (h->ones_rows > 0) {   // bf16 1.0 = 0x3f80 in the first element of each 128-byte row
+    char* o = h->ws + h->off_ones;
+    ok = ok && cudaMemset2D(o, 128, 0x80, 1, (size_t)h->ones_rows) == cudaSuccess;
+    ok = ok && cudaMemset2D(o + 1, 128, 0x3f, 1, (size_t)h->ones_rows) == cudaSuccess;
+  }
   ok = ok && write_inv_tables(h) == KFAC_OK;
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {

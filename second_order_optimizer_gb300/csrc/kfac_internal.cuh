@@ -122,6 +122,8 @@ struct kfac_ctx {
   size_t off_part_k4 = 0, off_tickets_k4 = 0;
   // K1 tensor-core operand pack (X = x-hat^T, TF32 halves or bf16)
   size_t off_tcpack = 0, tcpack_bytes = 0;
+  size_t off_ones = 0;    // bf16 [ones_rows x 64]: column 0 ones, the rest zeros
+  int64_t ones_rows = 0;  // 0: no such matrix (no bf16 layer with a bias)
   // K4 scratch: dW-hat halves [o x n_p] x2, then X^T halves [n x o_p] x2
   size_t off_k4tmp = 0, k4tmp_floats = 0;
   // K5 row-split partials and tickets
@@ -235,7 +237,20 @@ struct TcProblem {
   // reduction range per output tile, for products with a triangular operand:
   // 0 all of K; 1 k >= the tile's first column; 2 k < the tile's last column + 1
   int kmode;
+  // launch_syrk_direct only: A.hi is the caller's bf16 [K x A.rows] array (row
+  // pitch A.pitch elements, features contiguous) read as an MN-major operand;
+  // feature bias_col (a multiple of 64, or -1) reads as ones
+  int bias_col;
 };
+// bf16 SYRKs straight from the callers' [rows x d] arrays on CTA pairs, without a
+// pack: every problem has A.lo == null, same_ab, upper, M = N = n.
+kfac_status launch_syrk_direct(kfac_ctx* h, const TcProblem* probs, int count, cudaStream_t st);
+// Whether x can feed launch_syrk_direct: bf16, 16-byte aligned rows, a bias
+// column starting its own 64-feature chunk, rows within the ones matrix.
+bool syrk_direct_layout_ok(const kfac_ctx* h, const void* x, int64_t ld, int64_t rows, int d,
+                           int has_bias);
+// CTA-pair tiles (256 x 256) of an n x n SYRK's upper triangle.
+int64_t syrk_pair_tiles(int n);
 kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProblem* probs,
                                    int count, cudaStream_t st);
 kfac_status launch_syrk_tc(kfac_ctx* h, int layer, const void* x, int64_t ld, int64_t rows, int d,

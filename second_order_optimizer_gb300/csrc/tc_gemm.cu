@@ -90,6 +90,8 @@ struct GemmTcParams {
   int kmode;             // reduction range per tile (TcProblem::kmode)
   int colmajor;          // persistent kernels: tiles column by column (grouped_tile)
   int ksub;              // k elements per TMEM drain (multiple of BK)
+  int bias_col;          // MN-major pair SYRK: feature read from the ones map (or -1)
+  int mn_full;           //   features in whole 64-feature chunks (64 floor(d / 64))
   float* part;           // this product's cluster partials [tile][groups][BM][BN]
   int* tickets;          // this product's tickets [tile][csize]
   DevStatus* status;
@@ -1249,6 +1251,7 @@ struct PairCfg {
   static constexpr int KMMA = 32 / ELT;
   static constexpr int A_BYTES = BM * 128;           // 16 KB
   static constexpr int BH_BYTES = (BN / 2) * 128;    // this CTA's half of B: 16 KB
+  static constexpr int MN_CHUNK = 64 * 128;          // MN-major: 64 features x 64 k
   static constexpr int HALF_BYTES = A_BYTES + BH_BYTES;
   static constexpr int STAGE_BYTES = kBF16 ? HALF_BYTES : 2 * HALF_BYTES;
   static constexpr int EPI_WARPS = 16, CW = 64;
@@ -1263,9 +1266,10 @@ struct PairCfg {
   static_assert(SMEM <= 232448, "fits the per-CTA shared memory");
 };
 
-template <bool kBF16, int EPI>
+template <bool kBF16, int EPI, bool kMN>
 __device__ __forceinline__ void pair_body(const GroupedTc& g) {
   using PC = PairCfg<kBF16>;
+  static_assert(!kMN || (kBF16 && EPI == TC_EPI_SYRK), "MN-major operands: bf16 SYRK");
   constexpr int CW = PC::CW, BN = PC::BN, STAGES = PC::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -1347,11 +1351,35 @@ __device__ __forceinline__ void pair_body(const GroupedTc& g) {
           const int k0 = (kb_lo + kb) * PC::BK;
           const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
           if (rank == 0) tc::mbar_expect_tx(&full[stage], 2 * bytes);   // both CTAs' loads
-          if (!aib) tc::tma_load_2d_pair(a_ptr(stage, 0), &m[0], fb, k0, arow);
-          tc::tma_load_2d_pair(b_ptr(stage, 0), &m[2], fb, k0, brow);
-          if (!kBF16) {
-            if (!aib) tc::tma_load_2d_pair(a_ptr(stage, 1), &m[1], fb, k0, arow);
-            tc::tma_load_2d_pair(b_ptr(stage, 1), &m[3], fb, k0, brow);
+          if constexpr (kMN) {
+            // features [row0, row0 + 128) of k rows [k0, k0 + 64) as two 64-feature
+            // chunks; the bias feature's chunk from the ones map
+            // (m[2]: both chunks in one box, for blocks of whole chunks without the
+            // bias feature; m[0] per chunk, zero past d; m[1] the ones matrix)
+            const int bias = g.prob[q].bias_col, full = g.prob[q].mn_full;
+            auto load_mn = [&](uint8_t* dst, int row0) {
+              if (row0 + 128 <= full && (bias < row0 || bias >= row0 + 128)) {
+                tc::tma_load_3d_pair(dst, &m[2], fb, 0, k0, row0 / 64);
+                return;
+              }
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                const int f = row0 + 64 * c;
+                if (f == bias)
+                  tc::tma_load_2d_pair(dst + c * PC::MN_CHUNK, &m[1], fb, 0, k0);
+                else
+                  tc::tma_load_2d_pair(dst + c * PC::MN_CHUNK, &m[0], fb, f, k0);
+              }
+            };
+            if (!aib) load_mn(a_ptr(stage, 0), arow);
+            load_mn(b_ptr(stage, 0), brow);
+          } else {
+            if (!aib) tc::tma_load_2d_pair(a_ptr(stage, 0), &m[0], fb, k0, arow);
+            tc::tma_load_2d_pair(b_ptr(stage, 0), &m[2], fb, k0, brow);
+            if (!kBF16) {
+              if (!aib) tc::tma_load_2d_pair(a_ptr(stage, 1), &m[1], fb, k0, arow);
+              tc::tma_load_2d_pair(b_ptr(stage, 1), &m[3], fb, k0, brow);
+            }
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -1402,7 +1430,11 @@ __device__ __forceinline__ void pair_body(const GroupedTc& g) {
             for (int kk = 0; kk < PC::BK / PC::KMMA; ++kk) {
               const uint32_t off = kk * 32;
               const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-              if (kBF16) {
+              if (kMN) {   // 16 k = two 8-row groups further down both operands
+                tc::umma_f16_pair(d, tc::sdesc_mnmajor_sw128(a_hi + kk * 2048, PC::MN_CHUNK),
+                                  tc::sdesc_mnmajor_sw128(b_hi + kk * 2048, PC::MN_CHUNK),
+                                  idesc | tc::kIdescMnA | tc::kIdescMnB, acc);
+              } else if (kBF16) {
                 tc::umma_f16_pair(d, tc::sdesc_kmajor_sw128(a_hi + off),
                                   tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
               } else {
@@ -1489,9 +1521,9 @@ __device__ __forceinline__ void pair_body(const GroupedTc& g) {
   if (warp == 1) tc::tmem_dealloc_pair(tmem, PC::TMEM_COLS);
 }
 
-template <bool kBF16, int EPI>
+template <bool kBF16, int EPI, bool kMN>
 __global__ void __maxnreg__(96) gemm_tc_pair_kernel(const __grid_constant__ GroupedTc g) {
-  pair_body<kBF16, EPI>(g);
+  pair_body<kBF16, EPI, kMN>(g);
 }
 
 // ------------------------------------------------------------ wait self-test
@@ -1758,6 +1790,23 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t rows, int64_t
   CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                   const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// bf16 [rows x 64 chunks] (pitch in elements) seen as [chunks][rows][64]: a box
+// of 2 chunks x 64 rows x 64 elements lands in shared memory as two 64-row MN-major
+// chunk tiles (128-byte swizzle), the layout two 2-D boxes of make_map would give.
+bool make_chunk_map(CUtensorMap* m, const void* base, int64_t rows, int64_t chunks,
+                    int64_t pitch) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64u, (cuuint64_t)rows, (cuuint64_t)chunks};
+  cuuint64_t strides[2] = {(cuuint64_t)(pitch * 2), 128u};
+  cuuint32_t box[3] = {64u, 64u, 2u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -2030,10 +2079,10 @@ kfac_status launch_persistent_kernel(const GroupedTc& g, cudaStream_t st) {
 }
 
 
-template <bool kBF16, int EPI>
+template <bool kBF16, int EPI, bool kMN = false>
 kfac_status launch_pair_kernel(const GroupedTc& g, cudaStream_t st) {
   using PC = PairCfg<kBF16>;
-  static bool attr_ok = cudaFuncSetAttribute(gemm_tc_pair_kernel<kBF16, EPI>,
+  static bool attr_ok = cudaFuncSetAttribute(gemm_tc_pair_kernel<kBF16, EPI, kMN>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)PC::SMEM) == cudaSuccess;
   if (!attr_ok) {
@@ -2056,7 +2105,7 @@ kfac_status launch_pair_kernel(const GroupedTc& g, cudaStream_t st) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<kBF16, EPI>, g);
+  cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<kBF16, EPI, kMN>, g);
   count_launch();
   return check_launch();
 }
@@ -2081,6 +2130,7 @@ kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProb
       CUtensorMap* m = &g->maps[4 * i];
       if (!make_map(&m[0], pr.A.hi, bf16, pr.A.rows, pr.K, pr.A.pitch, box_a)) return KFAC_ERR_CUDA;
       if (!make_map(&m[2], pr.B.hi, bf16, pr.B.rows, pr.K, pr.B.pitch, box_b)) return KFAC_ERR_CUDA;
+      GemmTcParams& pp = g->prob[i];
       if (bf16) {
         m[1] = m[0];
         m[3] = m[2];
@@ -2090,7 +2140,6 @@ kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProb
         if (!make_map(&m[3], pr.B.lo, false, pr.B.rows, pr.K, pr.B.pitch, box_b))
           return KFAC_ERR_CUDA;
       }
-      GemmTcParams& pp = g->prob[i];
       pp.M = pr.M;
       pp.N = pr.N;
       pp.K = pr.K;
@@ -2136,6 +2185,75 @@ kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProb
                : launch_persistent_kernel<false, TC_EPI_PRECOND, BN>(*g, st);
     }
     if (e) return e;
+  }
+  return KFAC_OK;
+}
+
+int64_t syrk_pair_tiles(int n) {
+  const int t = (int)cdiv(n, 256);
+  return (int64_t)t * (t + 1) / 2;
+}
+
+bool syrk_direct_layout_ok(const kfac_ctx* h, const void* x, int64_t ld, int64_t rows, int d,
+                           int has_bias) {
+  if (ld % 8 != 0 || reinterpret_cast<uintptr_t>(x) % 16 != 0 || rows < 1) return false;
+  if (has_bias && (d % 64 != 0 || h->ones_rows < rows)) return false;
+  return true;
+}
+
+// The factor SYRKs of bf16 layers read straight from the callers' activations:
+// a [K x d] row-major array is, for C = X^T X, an MN-major operand (features
+// contiguous), which the bf16 MMA takes through its transpose bits.  Tensor maps
+// over x load 64 features x 64 k per box; the ones column of x-hat (feature d of
+// a layer with a bias) loads from a [K x 64] matrix whose first column is one.
+// Saves the pack's read and write of every input.  CTA pairs as in
+// launch_wide_persistent; groups of kMaxGroup.
+kfac_status launch_syrk_direct(kfac_ctx* h, const TcProblem* probs, int count, cudaStream_t st) {
+  constexpr int BN = 256;
+  std::unique_ptr<GroupedTc> g(new GroupedTc());
+  for (int c0 = 0; c0 < count; c0 += kMaxGroup) {
+    std::memset(g.get(), 0, sizeof(GroupedTc));
+    const int cnt = std::min(kMaxGroup, count - c0);
+    int blocks = 0;
+    for (int i = 0; i < cnt; ++i) {
+      const TcProblem& pr = probs[c0 + i];
+      CUtensorMap* m = &g->maps[4 * i];
+      if (!make_map(&m[0], pr.A.hi, true, pr.K, pr.A.rows, pr.A.pitch, 64)) return KFAC_ERR_CUDA;
+      if (pr.bias_col >= 0) {
+        if (!make_map(&m[1], h->ws + h->off_ones, true, pr.K, 64, 64, 64)) return KFAC_ERR_CUDA;
+      } else {
+        m[1] = m[0];
+      }
+      const int full = (int)(pr.A.rows / 64 * 64);
+      if (full >= 64) {
+        if (!make_chunk_map(&m[2], pr.A.hi, pr.K, pr.A.rows / 64, pr.A.pitch)) return KFAC_ERR_CUDA;
+      } else {
+        m[2] = m[0];
+      }
+      m[3] = m[1];
+      GemmTcParams& pp = g->prob[i];
+      pp.M = pr.M;
+      pp.N = pr.N;
+      pp.K = pr.K;
+      pp.tiles_m = pp.tiles_n = (int)cdiv(pr.M, BN);
+      pp.upper = 1;
+      pp.same_ab = 1;
+      pp.splits = 1;
+      pp.csize = 1;
+      pp.k_per_split = cdiv(pr.K, kKsubBf16Wide) * kKsubBf16Wide;
+      pp.ksub = kKsubBf16Wide;
+      pp.bias_col = pr.bias_col;
+      pp.mn_full = full;
+      pp.status = h->status();
+      pp.layer = pr.layer;
+      pp.e = pr.e;
+      g->block_start[i] = blocks;
+      blocks += (int)syrk_pair_tiles((int)pr.M);
+    }
+    g->block_start[cnt] = blocks;
+    g->count = cnt;
+    g->csize = 1;
+    if (kfac_status e = launch_pair_kernel<true, TC_EPI_SYRK, true>(*g, st)) return e;
   }
   return KFAC_OK;
 }
@@ -2329,7 +2447,23 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
 kfac_status launch_syrk_tc(kfac_ctx* h, int layer, const void* x, int64_t ld, int64_t rows, int d,
                            int n, int has_bias, bool bf16, float alpha, float beta, float* F,
                            cudaStream_t st) {
-  (void)has_bias;  // n > d exactly when the ones column is present
+  if (bf16 && syrk_direct_layout_ok(h, x, ld, rows, d, has_bias) &&
+      syrk_pair_tiles(n) >= num_sms() / 2) {   // in place, no pack (launch_syrk_direct)
+    TcProblem q{};
+    q.A = TcOperand{x, nullptr, d, ld};
+    q.B = q.A;
+    q.same_ab = true;
+    q.upper = true;
+    q.M = q.N = n;
+    q.K = rows;
+    q.bias_col = has_bias ? d : -1;
+    q.e.alpha = alpha;
+    q.e.beta = beta;
+    q.e.C = F;
+    q.e.ldc = n;
+    q.layer = layer;
+    return launch_syrk_direct(h, &q, 1, st);
+  }
   const int64_t Kp = tc_pitch(rows, bf16);
   if ((size_t)n * Kp * (bf16 ? 2 : 8) > h->tcpack_bytes) return KFAC_ERR_WORKSPACE;
   void* hi = h->ws + h->off_tcpack;

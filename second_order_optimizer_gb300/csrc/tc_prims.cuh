@@ -193,6 +193,15 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
       : "memory");
 }
+// The same for a 3-D tensor map (coordinates x innermost).
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
+      : "memory");
+}
 // One warp of each CTA of the pair, together.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -251,6 +260,22 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   d |= (uint64_t)2 << 61;              // 128-byte swizzle
   return d;
 }
+
+// MN-major operand written by TMA with 128-byte swizzle: each 128-byte row holds
+// 64 consecutive M (or N) elements of one k, 8-row groups (8 k) 1024 bytes apart,
+// 64-element M (N) chunks `chunk_bytes` apart.  Selected per operand by the
+// instruction descriptor's transpose bits (bf16 only).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t chunk_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((chunk_bytes >> 4) & 0x3FFFu) << 16;   // leading byte offset: next chunk
+  d |= (uint64_t)(1024 >> 4) << 32;                       // stride byte offset: next 8 k
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// Instruction-descriptor bits: A and B MN-major (transposed).
+constexpr uint32_t kIdescMnA = 1u << 15, kIdescMnB = 1u << 16;
 
 // 32 consecutive TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {

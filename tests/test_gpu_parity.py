@@ -112,6 +112,61 @@ def test_factor_strided_bf16_input(width):
     assert rel_fro(to_np(h.state(0, K.KFAC_STATE_G)), 0.05 * O.factor(big_g[:, :o], 0)) <= 1e-5
 
 
+@pytest.mark.parametrize("d_in,o,bias,pad", [
+    (3072, 3072, 1, 0),   # ones column from the ones matrix (a chunk of its own)
+    (3008, 3100, 1, 8),   # strided rows (pitch d + 8), G with a ragged last chunk
+    (3072, 3000, 0, 0),   # no bias
+    (3000, 3100, 1, 0),   # d_in not a multiple of 64: A through the pack, G in place
+    (3072, 3072, 1, 3),   # row pitch not a 16-byte multiple: both through the pack
+])
+def test_factor_bf16_in_place_syrk_matches_oracle(d_in, o, bias, pad):
+    """bf16 factors wide enough for a wave of CTA pairs read the activations in place
+    as MN-major operands (no pack); three EMA steps against the oracle, with a row
+    count that leaves a ragged last k block."""
+    M = 1000
+    h = K.Kfac([(K.KFAC_KRON, o, d_in, bias, K.KFAC_BF16)], max_rows=M, **HP)
+    A = np.zeros((d_in + bias,) * 2)
+    G = np.zeros((o, o))
+    for step in range(3):
+        big_a, big_g = _inputs(M, d_in + pad, o + pad, dtype="bf16")
+        ta, tg = _dev_in(big_a, "bf16"), _dev_in(big_g, "bf16")
+        h.update_factors(0, ta[:, :d_in], tg[:, :o])
+        A = O.ema(A, O.factor(big_a[:, :d_in], bias), 0.95)
+        G = O.ema(G, O.factor(big_g[:, :o], 0), 0.95)
+        Ag, Gg = to_np(h.state(0, K.KFAC_STATE_A)), to_np(h.state(0, K.KFAC_STATE_G))
+        assert rel_fro(Ag, A) <= 1e-5, (step, rel_fro(Ag, A))
+        assert rel_fro(Gg, G) <= 1e-5, (step, rel_fro(Gg, G))
+        assert np.array_equal(Ag, Ag.T) and np.array_equal(Gg, Gg.T)
+    assert h.get_status()[0] == 0
+
+
+def test_factor_bf16_batched_in_place_and_packed_mix():
+    """A batched bf16 call whose wide factors fill a wave of CTA pairs: those read in
+    place, the rest (d_in not a multiple of 64) through the pack, one handle, two
+    steps; batched equals per-layer calls and the oracle."""
+    shapes = [(1024, 1024, 1)] * 5 + [(1000, 1030, 1), (1024, 700, 0)]
+    descs = [(K.KFAC_KRON, o, d, b, K.KFAC_BF16) for d, o, b in shapes]
+    M = 777
+    hb = K.Kfac(descs, max_rows=M, **HP)
+    hs = K.Kfac(descs, max_rows=M, **HP)
+    ins = [_inputs(M, d, o, dtype="bf16") for (_, o, d, b, _) in descs]
+    for step in range(2):
+        a_l = [_dev_in(a, "bf16") for a, _ in ins]
+        g_l = [_dev_in(g, "bf16") for _, g in ins]
+        hb.update_factors_batched(list(range(len(descs))), a_l, g_l)
+        for li in range(len(descs)):
+            hs.update_factors(li, a_l[li], g_l[li])
+    for li, (_, o, d, b, _) in enumerate(descs):
+        a, g = ins[li]
+        for which, ref in ((K.KFAC_STATE_A, O.factor(a, b)), (K.KFAC_STATE_G, O.factor(g, 0))):
+            ref = ref * (1 - 0.95 ** 2)
+            xb, xs = to_np(hb.state(li, which)), to_np(hs.state(li, which))
+            assert rel_fro(xb, ref) <= 1e-5, (li, which, rel_fro(xb, ref))
+            assert rel_fro(xs, ref) <= 1e-5, (li, which, rel_fro(xs, ref))
+            assert np.array_equal(xb, xb.T)
+    assert hb.get_status()[0] == 0
+
+
 def test_factor_strided_input():
     M, d_in, o = 400, 50, 20
     h = K.Kfac([(K.KFAC_KRON, o, d_in, 1, K.KFAC_F32)], max_rows=M, **HP)
