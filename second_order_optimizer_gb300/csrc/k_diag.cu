@@ -29,10 +29,12 @@ constexpr int kDiagThreads = 1024;
 constexpr int kK5Threads = 256;
 constexpr int64_t kK5MinRows = 32;
 
-// Row splits of K5: enough CTAs to cover the GPU twice, at least kK5MinRows rows each.
+// Row splits of K5: enough CTAs for four per SM (rows in flight to cover the HBM
+// latency), at least kK5MinRows rows each.
+constexpr int kK5CtasPerSm = 4;
 int64_t k5_splits(int ncols, int64_t rows) {
   const int64_t cb = cdiv(ncols, kK5Threads);
-  int64_t s = cdiv(2 * num_sms(), cb);
+  int64_t s = cdiv(kK5CtasPerSm * num_sms(), cb);
   s = std::min<int64_t>(s, cdiv(rows, kK5MinRows));
   return std::max<int64_t>(s, 1);
 }
@@ -215,7 +217,7 @@ __device__ __forceinline__ void diag_factor_body(const DiagFactorParams& p, int 
                                : static_cast<const T*>(p.g) + (c - p.d_in);
     const int64_t ld = c < p.d_in ? p.lda : p.ldg;
     // compensated (Kahan) sum: the kernel is bound by HBM, the extra flops are free.
-    // Rows in batches of 8: the loads of a batch are independent and issue
+    // Rows in batches of 16: the loads of a batch are independent and issue
     // together; the compensated adds then run in row order.
     float acc = 0.f, comp = 0.f;
     auto kahan = [&](float v) {
@@ -225,12 +227,12 @@ __device__ __forceinline__ void diag_factor_body(const DiagFactorParams& p, int 
       acc = t;
     };
     int64_t r = r0;
-    for (; r + 8 <= r1; r += 8) {
-      float v[8];
+    for (; r + 16 <= r1; r += 16) {
+      float v[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = to_f32<T>(base[(r + u) * ld]);
+      for (int u = 0; u < 16; ++u) v[u] = to_f32<T>(base[(r + u) * ld]);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) kahan(v[u]);
+      for (int u = 0; u < 16; ++u) kahan(v[u]);
     }
     for (; r < r1; ++r) kahan(to_f32<T>(base[r * ld]));
     p.part[(size_t)split * ncols + c] = acc;
@@ -378,7 +380,7 @@ kfac_status launch_diag_factors(kfac_ctx* h, int layer, const void* a, int64_t l
 }
 
 // Several layers (one input dtype) per launch.  Row splits are shared out so the
-// whole group covers the GPU about twice; each job gets its own partials and
+// whole group has about kK5CtasPerSm CTAs per SM; each job gets its own partials and
 // tickets; a group is cut where the scratch or the job table is full.
 kfac_status launch_diag_factors_batched(kfac_ctx* h, int count, const int* layers,
                                         const void* const* a, const int64_t* lda,
@@ -413,8 +415,8 @@ kfac_status launch_diag_factors_batched(kfac_ctx* h, int count, const int* layer
     const LayerInfo& L = h->layers[layers[i]];
     const int ncols = L.d_in + L.o;
     const int64_t cb = cdiv(ncols, kK5Threads);
-    const double share = (double)rows[i] * ncols / work;   // of 2 x SMs CTAs
-    int64_t splits = (int64_t)std::ceil(2.0 * num_sms() * share / (double)cb);
+    const double share = (double)rows[i] * ncols / work;   // of kK5CtasPerSm x SMs CTAs
+    int64_t splits = (int64_t)std::ceil((double)kK5CtasPerSm * num_sms() * share / (double)cb);
     splits = std::max<int64_t>(1, std::min<int64_t>(splits, cdiv(rows[i], kK5MinRows)));
     const size_t need = (size_t)splits * ncols;
     if (need > h->k5part_floats || (size_t)cb > h->k5tickets_ints) return KFAC_ERR_WORKSPACE;
@@ -737,7 +739,7 @@ extern "C" kfac_status kfac_diag_factors_static(const void* a, int64_t lda, cons
   p.ldg = ldg;
   p.rows = rows;
   const int ncols = d_in + d_out;
-  // the row splits fill the GPU twice over, within what the static array holds
+  // the row splits as the handle's K5 has them, within what the static array holds
   const int64_t sp = std::max<int64_t>(
       1, std::min<int64_t>(k5_splits(ncols, rows), (int64_t)(kStaticScratchFloats / ncols)));
   p.rows_per_split = cdiv(rows, sp);

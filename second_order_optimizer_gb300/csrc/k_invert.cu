@@ -45,14 +45,17 @@ __global__ void __launch_bounds__(256) inv_prep_kernel(const InvJob* jobs, float
   pdl_wait();
   pdl_trigger();
   const InvJob J = jobs[blockIdx.y];
-  const int64_t nn = (int64_t)J.n * J.n;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = e / J.n, c = e % J.n;
-    // both triangles (F is symmetric): the tensor-core trailing updates of large
-    // factors read either triangle and keep the trailing block symmetric
-    J.L[e] = r == c ? J.F[e] + sqrt_gamma : J.F[e];
-    J.X[e] = 0.f;
+  // rows over the grid, columns over the threads (no index division per element);
+  // both triangles (F is symmetric): the tensor-core trailing updates of large
+  // factors read either triangle and keep the trailing block symmetric
+  for (int r = blockIdx.x; r < J.n; r += gridDim.x) {
+    const int64_t row = (int64_t)r * J.n;
+#pragma unroll 4
+    for (int c = threadIdx.x; c < J.n; c += blockDim.x) {
+      const float f = J.F[row + c];
+      J.L[row + c] = r == c ? f + sqrt_gamma : f;
+      J.X[row + c] = 0.f;
+    }
   }
 }
 
@@ -386,14 +389,14 @@ __global__ void __launch_bounds__(256) panel_split_kernel(const __grid_constant_
   pdl_wait();
   pdl_trigger();
   const PanelPack P = g.job[blockIdx.y];
-  const int64_t total = P.rows * g.W;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = e / g.W, c = e % g.W;
-    const float v = P.src[r * P.ld + c];
-    const float hi = tc::to_tf32(v);
-    P.hi[e] = hi;
-    P.lo[e] = tc::to_tf32(v - hi);
+  for (int64_t r = blockIdx.x; r < P.rows; r += gridDim.x) {
+#pragma unroll 2
+    for (int c = threadIdx.x; c < g.W; c += blockDim.x) {
+      const float v = P.src[r * P.ld + c];
+      const float hi = tc::to_tf32(v);
+      P.hi[r * g.W + c] = hi;
+      P.lo[r * g.W + c] = tc::to_tf32(v - hi);
+    }
   }
 }
 
@@ -404,19 +407,24 @@ __global__ void __launch_bounds__(256) inv_split_kernel(const InvJob* jobs, int 
   pdl_wait();
   pdl_trigger();
   const InvJob J = jobs[blockIdx.y];
-  const int64_t nn = (int64_t)J.n * J.n;
   __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(J.Finv_hi);
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = e / J.n, c = e % J.n;
-    const float v = J.Finv[e];
+  for (int64_t r = blockIdx.x; r < J.n; r += gridDim.x) {
+    const float* src = J.Finv + r * J.n;
     if (bf16) {
-      ob[r * 2 * J.np + c] = __float2bfloat16_rn(v);
+      __nv_bfloat16* d = ob + r * 2 * J.np;
+#pragma unroll 4
+      for (int c = threadIdx.x; c < J.n; c += blockDim.x) d[c] = __float2bfloat16_rn(src[c]);
       continue;
     }
-    const float hi = tc::to_tf32(v);
-    J.Finv_hi[r * J.np + c] = hi;
-    J.Finv_lo[r * J.np + c] = tc::to_tf32(v - hi);
+    float* dh = J.Finv_hi + r * J.np;
+    float* dl = J.Finv_lo + r * J.np;
+#pragma unroll 4
+    for (int c = threadIdx.x; c < J.n; c += blockDim.x) {
+      const float v = src[c];
+      const float hi = tc::to_tf32(v);
+      dh[c] = hi;
+      dl[c] = tc::to_tf32(v - hi);
+    }
   }
 }
 
@@ -852,15 +860,14 @@ __global__ void __launch_bounds__(256) ik_damped_split_kernel(const InvJob* jobs
   pdl_wait();
   pdl_trigger();
   const InvJob J = jobs[blockIdx.y];
-  const int64_t nn = (int64_t)J.n * J.n;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = e / J.n, c = e % J.n;
-    const float v = J.F[e] + (r == c ? sqrt_gamma : 0.f);
-    const float hi = tc::to_tf32(v);
-    J.S1_hi[r * J.np + c] = hi;
-    J.S1_lo[r * J.np + c] = tc::to_tf32(v - hi);
-  }
+  for (int64_t r = blockIdx.x; r < J.n; r += gridDim.x)
+#pragma unroll 4
+    for (int c = threadIdx.x; c < J.n; c += blockDim.x) {
+      const float v = J.F[r * J.n + c] + (r == c ? sqrt_gamma : 0.f);
+      const float hi = tc::to_tf32(v);
+      J.S1_hi[r * J.np + c] = hi;
+      J.S1_lo[r * J.np + c] = tc::to_tf32(v - hi);
+    }
 }
 
 // S1 <- split(c1 I - c2 S1)
@@ -868,15 +875,15 @@ __global__ void __launch_bounds__(256) ik_affine_kernel(const InvJob* jobs, floa
   pdl_wait();
   pdl_trigger();
   const InvJob J = jobs[blockIdx.y];
-  const int64_t nn = (int64_t)J.n * J.n;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = e / J.n, c = e % J.n, x = r * J.np + c;
-    const float v = fmaf(-c2, J.S1_hi[x] + J.S1_lo[x], r == c ? c1 : 0.f);
-    const float hi = tc::to_tf32(v);
-    J.S1_hi[x] = hi;
-    J.S1_lo[x] = tc::to_tf32(v - hi);
-  }
+  for (int64_t r = blockIdx.x; r < J.n; r += gridDim.x)
+#pragma unroll 4
+    for (int c = threadIdx.x; c < J.n; c += blockDim.x) {
+      const int64_t x = r * J.np + c;
+      const float v = fmaf(-c2, J.S1_hi[x] + J.S1_lo[x], r == c ? c1 : 0.f);
+      const float hi = tc::to_tf32(v);
+      J.S1_hi[x] = hi;
+      J.S1_lo[x] = tc::to_tf32(v - hi);
+    }
 }
 
 // K <- (K^T)^T, both halves, through 32 x 33 shared tiles
@@ -967,16 +974,16 @@ __global__ void __launch_bounds__(256) ikb_damped_kernel(const InvJob* jobs, flo
   pdl_wait();
   pdl_trigger();
   const InvJob J = jobs[blockIdx.y];
-  const int64_t nn = (int64_t)J.n * J.n, pb = 2 * (int64_t)J.np;
+  const int64_t pb = 2 * (int64_t)J.np;
   __nv_bfloat16* ff = bf16_at(J.S1_hi);
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = e / J.n, c = e % J.n;
-    const float v = J.F[e] + (r == c ? sqrt_gamma : 0.f);
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    ff[r * pb + c] = hi;
-    ff[r * pb + J.n + c] = __float2bfloat16_rn(v - __bfloat162float(hi));
-  }
+  for (int64_t r = blockIdx.x; r < J.n; r += gridDim.x)
+#pragma unroll 4
+    for (int c = threadIdx.x; c < J.n; c += blockDim.x) {
+      const float v = J.F[r * J.n + c] + (r == c ? sqrt_gamma : 0.f);
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      ff[r * pb + c] = hi;
+      ff[r * pb + J.n + c] = __float2bfloat16_rn(v - __bfloat162float(hi));
+    }
 }
 
 // Wb <- bf16(-(beta/2) (G - I)),  G fp32 in S1_lo
@@ -984,14 +991,14 @@ __global__ void __launch_bounds__(256) ikb_w_kernel(const InvJob* jobs, float ha
   pdl_wait();
   pdl_trigger();
   const InvJob J = jobs[blockIdx.y];
-  const int64_t nn = (int64_t)J.n * J.n, pb = 2 * (int64_t)J.np;
+  const int64_t pb = 2 * (int64_t)J.np;
   __nv_bfloat16* w = bf16_at(J.S1_hi);
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < nn;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = e / J.n, c = e % J.n;
-    const float g = J.S1_lo[r * J.np + c] - (r == c ? 1.f : 0.f);
-    w[r * pb + c] = __float2bfloat16_rn(-half_beta * g);
-  }
+  for (int64_t r = blockIdx.x; r < J.n; r += gridDim.x)
+#pragma unroll 4
+    for (int c = threadIdx.x; c < J.n; c += blockDim.x) {
+      const float g = J.S1_lo[r * J.np + c] - (r == c ? 1.f : 0.f);
+      w[r * pb + c] = __float2bfloat16_rn(-half_beta * g);
+    }
 }
 
 unsigned elem_blocks(int nmax) {

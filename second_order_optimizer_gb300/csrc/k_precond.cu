@@ -35,6 +35,7 @@ struct GradPackJob {
   int o, d_in, n;
   float* hi;
   float* lo;      // null: bf16 values in hi, row pitch 2 np elements
+  int vec;        // rows of gw, hi and lo 16-byte aligned: float4 over the weight columns
 };
 constexpr int kMaxGradPack = 16;
 struct GradPackGroup {
@@ -46,20 +47,46 @@ __global__ void __launch_bounds__(256) gradhat_pack_grouped_kernel(
   pdl_wait();
   pdl_trigger();
   const GradPackJob J = g.job[blockIdx.y];  // by value: no reloads after each store
-  // a CTA takes whole rows (no index division), its threads along the row
+  // a CTA takes whole rows (no index division), its threads along the row; with
+  // J.vec the weight columns go four at a time and the rest (the bias) one by one
+  const int j0 = J.vec ? J.d_in / 4 * 4 : 0;
   for (int i = blockIdx.x; i < J.o; i += gridDim.x) {
     const float* src = J.gw + (int64_t)i * J.ld;
     if (!J.lo) {   // bf16 operand
       __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(J.hi) + (int64_t)i * 2 * J.np;
+#pragma unroll 2
+      for (int j = 4 * threadIdx.x; j < j0; j += 4 * blockDim.x) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(src + j));
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(v.x, v.y), p1 = __floats2bfloat162_rn(v.z, v.w);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&p0);
+        u.y = *reinterpret_cast<uint32_t*>(&p1);
+        *reinterpret_cast<uint2*>(b + j) = u;
+      }
 #pragma unroll 4
-      for (int j = threadIdx.x; j < J.n; j += blockDim.x)
+      for (int j = j0 + threadIdx.x; j < J.n; j += blockDim.x)
         b[j] = __float2bfloat16_rn(j < J.d_in ? __ldg(src + j) : J.gb[i]);
       continue;
     }
     float* hi = J.hi + (int64_t)i * J.np;
     float* lo = J.lo + (int64_t)i * J.np;
+#pragma unroll 2
+    for (int j = 4 * threadIdx.x; j < j0; j += 4 * blockDim.x) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(src + j));
+      float4 h, l;
+      h.x = tc::to_tf32(v.x);
+      h.y = tc::to_tf32(v.y);
+      h.z = tc::to_tf32(v.z);
+      h.w = tc::to_tf32(v.w);
+      l.x = tc::to_tf32(v.x - h.x);
+      l.y = tc::to_tf32(v.y - h.y);
+      l.z = tc::to_tf32(v.z - h.z);
+      l.w = tc::to_tf32(v.w - h.w);
+      *reinterpret_cast<float4*>(hi + j) = h;
+      *reinterpret_cast<float4*>(lo + j) = l;
+    }
 #pragma unroll 4
-    for (int j = threadIdx.x; j < J.n; j += blockDim.x) {
+    for (int j = j0 + threadIdx.x; j < J.n; j += blockDim.x) {
       const float v = j < J.d_in ? __ldg(src + j) : J.gb[i];
       const float h = tc::to_tf32(v);
       hi[j] = h;
@@ -135,6 +162,8 @@ kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layer
     j.n = L.n;
     j.hi = g_hi;
     j.lo = bf ? nullptr : g_lo;
+    auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+    j.vec = ldgw[i] % 4 == 0 && np % 4 == 0 && al16(gw[i]) && al16(g_hi) && (bf || al16(g_lo));
     max_rows = std::max<int64_t>(max_rows, L.o);
     const int64_t npb = bf ? 2 * np : np, opb = bf ? 2 * op : op;   // operand pitches
     TcProblem q1{};

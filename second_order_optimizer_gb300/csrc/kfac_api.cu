@@ -165,8 +165,8 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, const kfa
   P->off_k4tmp = take(k4 * sizeof(float));
   P->ones_rows = ones ? max_rows : 0;
   P->off_ones = take((size_t)P->ones_rows * 64 * 2);
-  // batched K5 spreads about 2 x SMs CTAs over the group, one part row per CTA
-  k5 = std::max(k5, (size_t)256 * (2 * num_sms() + k5t));
+  // batched K5 spreads about 4 x SMs CTAs over the group, one part row per CTA
+  k5 = std::max(k5, (size_t)256 * (4 * num_sms() + k5t));
   P->k5part_floats = k5;
   P->off_k5part = take(k5 * sizeof(float));
   P->off_k5tickets = take(k5t * sizeof(int));

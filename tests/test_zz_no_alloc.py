@@ -8,7 +8,7 @@ through the C ABI and check it against the handle-based kfac_diag_factors and
 against the float64 oracle on the same inputs, twice in a row, so that state the
 shared array keeps between calls cannot leak into the next result; two more
 cases reach the array's edges: the most row splits (one column block, rows
-enough for two CTAs per SM) and the largest layer width it takes.
+enough for four CTAs per SM) and the largest layer width it takes.
 """
 import ctypes
 
@@ -82,10 +82,10 @@ def test_static_entry_point_matches_handle_entry_point_twice():
             h.close()
 
 
-@pytest.mark.parametrize("M,d_in,o", [(10000, 200, 56), (64, 200000, 62144)])
+@pytest.mark.parametrize("M,d_in,o", [(20000, 200, 56), (64, 200000, 62144)])
 def test_static_entry_point_at_the_edges_of_its_array(M, d_in, o):
-    """(10000, 200 + 56): one column block split over the most rows the array
-    holds (two CTAs per SM); (64, 200000 + 62144): the widest layer it takes
+    """(20000, 200 + 56): one column block split over the most rows the array
+    holds (four CTAs per SM); (64, 200000 + 62144): the widest layer it takes
     (d_in + d_out = 262144).  Both against the oracle, twice in a row."""
     gen = torch.Generator(device="cuda")
     gen.manual_seed(77)
