@@ -36,7 +36,8 @@ namespace kfac {
 namespace {
 
 constexpr int NB = 64;
-constexpr int kOuterW = 512;      // outer panel width of the two-level Cholesky
+constexpr int kOuterW = 512;      // outer panel width of the blocked Cholesky
+constexpr int kMidW = 256;        // half of an outer panel: its second half gets the first on the tensor cores
 constexpr int kOuterMaxN = 1536;  // handles whose factors are all this small stay one panel
 constexpr int kTcLevelMin = 512;  // doubling levels of this block size and wider: tensor cores
 using PTile = SimtTile<64, 64, 32, 4, 4>;   // 256 threads, 32-deep k chunks
@@ -671,6 +672,69 @@ kfac_status launch_outer_update(kfac_ctx* h, int j0, int nj, int K0, int W, cuda
   return flush();
 }
 
+// Inside an outer panel: L[e:, e:c] <- L[e:, e:c] - P Q^T for every factor whose
+// size reaches past e = H0 + MW, with P = L[e:, H0:e] (MW columns, split into
+// TF32 halves) and Q = its rows [e, c) (c the end of the outer panel): one
+// grouped 3xTF32 product with the transposed fp32 store accumulating into L
+// (C^T = Q P^T, alpha -1, beta 1).  Q's rows are the first of P's, so one pack
+// serves both operands.  The square [e, c)^2 gets both triangles, which keeps
+// it symmetric for the steps that factor it.
+kfac_status launch_mid_update(kfac_ctx* h, int j0, int nj, int H0, int MW, int c,
+                              cudaStream_t st) {
+  const int e0 = H0 + MW;
+  PanelPackGroup pg;
+  std::memset(&pg, 0, sizeof(pg));
+  pg.W = MW;
+  std::vector<TcProblem> pr;
+  size_t used = 0;
+  int64_t max_rows = 0;
+  auto flush = [&]() -> kfac_status {
+    if (pr.empty()) return KFAC_OK;
+    const unsigned blocks = (unsigned)std::min<int64_t>(max_rows, 4 * num_sms());
+    launch_pdl(panel_split_kernel, dim3(dim3(blocks, pg.count)), dim3(256), 0, st, pg);
+    count_launch();
+    kfac_status e = check_launch();
+    if (e == KFAC_OK) e = launch_gemm_tc_grouped(h, false, TC_EPI_SPLIT, pr.data(), (int)pr.size(), st);
+    pr.clear();
+    pg.count = 0;
+    used = 0;
+    max_rows = 0;
+    return e;
+  };
+  for (int i = j0; i < j0 + nj; ++i) {
+    const InvJob& J = h->invjobs_host[i];
+    if (J.n <= e0) continue;
+    const int64_t m = J.n - e0;
+    const size_t raw = (size_t)m * MW * 8, bytes = align_up(raw);
+    if (raw > h->tcpack_bytes) return KFAC_ERR_WORKSPACE;
+    if (used + raw > h->tcpack_bytes || pg.count == kMaxPanelPacks)
+      if (kfac_status e = flush()) return e;
+    float* hi = reinterpret_cast<float*>(h->ws + h->off_tcpack + used);
+    float* lo = hi + (size_t)m * MW;
+    used += bytes;
+    PanelPack& pp = pg.job[pg.count++];
+    pp.src = J.L + (int64_t)e0 * J.n + H0;
+    pp.ld = J.n;
+    pp.rows = m;
+    pp.hi = hi;
+    pp.lo = lo;
+    max_rows = std::max<int64_t>(max_rows, m);
+    TcProblem t{};
+    t.A = TcOperand{hi, lo, std::min<int64_t>(c, J.n) - e0, MW};   // Q: rows [e0, c)
+    t.B = TcOperand{hi, lo, m, MW};                                   // P: rows [e0, n)
+    t.M = t.A.rows;
+    t.N = m;
+    t.K = MW;
+    t.e.alpha = -1.f;
+    t.e.beta = 1.f;
+    t.e.out_hi = J.L + (int64_t)e0 * J.n + e0;   // C^T[c][r] = L[e0 + c][e0 + r]
+    t.e.ldo = J.n;
+    t.layer = J.layer;
+    pr.push_back(t);
+  }
+  return flush();
+}
+
 kfac_status launch_ikfac_seed(const InvJob* jobs, int nj, int nmax, bool bf16, cudaStream_t st);
 
 kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
@@ -717,9 +781,11 @@ kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
     return sync_err(cudaStreamWaitEvent(st, h->ev_rest, 0));
   };
   const int W = nmax > kOuterMaxN ? kOuterW : (int)cdiv(nmax, NB) * NB;
+  const int MW = W == kOuterW ? kMidW : W;   // inner steps update their half panel only
   for (int K0 = 0; K0 < nmax; K0 += W) {
-    const int cend = K0 + W;
-    for (int k = K0; k < std::min(cend, nmax); k += NB) {
+   for (int H0 = K0; H0 < std::min(K0 + W, nmax); H0 += MW) {
+    const int cend = H0 + MW;   // the inner steps' trailing updates stop here
+    for (int k = H0; k < std::min(cend, nmax); k += NB) {
       launch_pdl(chol_diag_kernel, dim3(nj), dim3(256), 0, st, jobs, k, h->status());
       count_launch();
       const int rest = nmax - k - NB;
@@ -748,7 +814,12 @@ kfac_status launch_invert(kfac_ctx* h, int layer, int which, cudaStream_t st) {
       }
       if (kfac_status e = check_launch()) return e;
     }
-    if (cend < nmax) {
+    if (cend < std::min(K0 + W, nmax)) {   // the second half of the outer panel
+      if (kfac_status e = join_side()) return e;
+      if (kfac_status e = launch_mid_update(h, j0, nj, H0, MW, K0 + W, st)) return e;
+    }
+   }
+    if (K0 + W < nmax) {
       if (kfac_status e = join_side()) return e;
       if (kfac_status e = launch_outer_update(h, j0, nj, K0, W, st)) return e;
     }

@@ -217,7 +217,7 @@ struct TcEpilogue {
   float* C;
   int64_t ldc;
   float* out_hi;         // SPLIT: C^T stored as TF32 halves, out[c * ldo + r]
-  float* out_lo;         //   (null: alpha C^T stored as fp32 in out_hi)
+  float* out_lo;         //   (null: alpha C^T + beta out stored as fp32 in out_hi)
   int out_bf16;          //   1: alpha C^T stored as bf16 in out_hi (a bf16 array)
   int64_t ldo;
   int d_in;              // PRECOND: C = P^T (n x o): C[j][i] = P[i][j]; j >= d_in is the bias

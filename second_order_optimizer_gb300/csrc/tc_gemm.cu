@@ -450,11 +450,13 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
             E.out_hi[gc * E.ldo + gr] = hi;
             E.out_lo[gc * E.ldo + gr] = tc::to_tf32(sum[c] - hi);
           }
-        } else {   // alpha C^T as fp32
+        } else {   // alpha C^T (+ beta C_old^T) as fp32
 #pragma unroll
           for (int c = 0; c < C::CW; ++c) {
             const int64_t gc = c0 + h * C::CW + c;
-            if (gc < pN) E.out_hi[gc * E.ldo + gr] = E.alpha * sum[c];
+            if (gc >= pN) continue;
+            float* o = E.out_hi + gc * E.ldo + gr;
+            *o = E.beta != 0.f ? fmaf(E.beta, *o, E.alpha * sum[c]) : E.alpha * sum[c];
           }
         }
       } else {  // PRECOND: row gr = column j of P, column gc = row i
@@ -664,8 +666,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
         reinterpret_cast<__nv_bfloat16*>(E.out_hi)[gc * E.ldo + gr] = __float2bfloat16_rn(E.alpha * v);
         continue;
       }
-      if (!E.out_lo) {   // alpha C^T as fp32
-        E.out_hi[gc * E.ldo + gr] = E.alpha * v;
+      if (!E.out_lo) {   // alpha C^T (+ beta C_old^T) as fp32
+        float* o = E.out_hi + gc * E.ldo + gr;
+        *o = E.beta != 0.f ? fmaf(E.beta, *o, E.alpha * v) : E.alpha * v;
         continue;
       }
       const float hi = tc::to_tf32(v);
@@ -931,11 +934,13 @@ __device__ __forceinline__ void epilogue_from_registers(const TcEpilogue& E, flo
         E.out_hi[gc * E.ldo + gr] = hi;
         E.out_lo[gc * E.ldo + gr] = tc::to_tf32(sum[c] - hi);
       }
-    } else if (gr < pM) {   // alpha C^T as fp32
+    } else if (gr < pM) {   // alpha C^T (+ beta C_old^T) as fp32
 #pragma unroll
       for (int c = 0; c < CW; ++c) {
         const int64_t gc = c0 + c;
-        if (gc < pN) E.out_hi[gc * E.ldo + gr] = E.alpha * sum[c];
+        if (gc >= pN) continue;
+        float* o = E.out_hi + gc * E.ldo + gr;
+        *o = E.beta != 0.f ? fmaf(E.beta, *o, E.alpha * sum[c]) : E.alpha * sum[c];
       }
     }
   } else {  // PRECOND: row gr = column j of P, column gc = row i

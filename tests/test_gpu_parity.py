@@ -180,12 +180,14 @@ def test_factor_strided_input():
 # ------------------------------------------------------------------ K2/K3 inverse
 
 @pytest.mark.parametrize("n_in,o", [(0, 1), (27, 64), (63, 5), (64, 100), (128, 129), (299, 300),
-                                    (512, 65), (1100, 1030), (1600, 700), (2048, 2049)])
+                                    (512, 65), (1100, 1030), (1600, 700), (2048, 2049),
+                                    (1800, 2300)])
 def test_invert_matches_oracle(n_in, o):
     """Ainv/Ginv vs the oracle's textbook Cholesky inverse of the same (GPU) factor.
-    Handles with a factor above 1536 take the two-level path (512-column outer
-    panels, tensor-core trailing updates): 1601 leaves a ragged last panel and
-    block."""
+    Handles with a factor above 1536 take the blocked path (512-column outer
+    panels, their second 256-column halves and the trailing block updated on the
+    tensor cores): 1601 leaves a ragged last panel and block; 1801 with 2300 ends
+    9 rows past a half-panel boundary while the other factor goes on."""
     bias = 1
     d_in = max(n_in, 1)
     M = 2 * (d_in + 1) + 3
