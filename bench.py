@@ -69,15 +69,19 @@ def qkv_ties(layers):
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TF32_PER_BF16 = 1.1 / 2.25          # nominal dense ratio
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of each phase's
-# launches in one step of the mlp4 workload, from one ncu capture of
-#   python bench.py --steps 2 --warmup 1 --no-e2e --no-cpu-baseline --no-overlap
-# (the last timed step's graph replay; ncu does not count writes that are still in
-# L2 when a kernel ends).  Valid only for the kernel sources with this digest: any
+# launches in one step of the transformer workload: one ncu capture per phase of
+#   python bench.py --workload transformer1 --steps 2 --warmup 1 --no-e2e \
+#       --no-cpu-baseline --no-graphs --nvtx
+# (ncu --nvtx --nvtx-include "<phase>/", the last step's launches) on the
+# one-block set, times four: the four blocks are the same layers, batched into
+# the same kinds of launches (ncu does not count writes that are still in L2
+# when a kernel ends).  Valid only for the kernel sources with this digest: any
 # change to them reports null until the counters are taken again.
 MEASURED_TRAFFIC = {
-    "workload": "mlp4",
-    "sources_sha256": "bb3814a5f0655052b058c49847b8615104db8caf9d3d04d34901c520525366d4",
-    "bytes": {"factor": 104.89e6, "precond": 150.22e6, "diag": 68.05e6},
+    "workload": "transformer4",
+    "sources_sha256": "7162a262dfd93db3f5df7edf3f8e95b96e40d942a0a1ae1b3bbeadc84945b65d",
+    "bytes": {"factor": 4 * 8.0019e9, "precond": 4 * 5.7630e9, "diag": 4 * 2.1918e9},
+    "note": "one-block capture (transformer1) x 4",
 }
 
 
@@ -713,7 +717,8 @@ def run_gpu(args, peaks, peak_kind):
     if (args.workload == MEASURED_TRAFFIC["workload"] and dom in MEASURED_TRAFFIC["bytes"]
             and sources_digest() == MEASURED_TRAFFIC["sources_sha256"]):
         roof["traffic"] = MEASURED_TRAFFIC["bytes"][dom]
-        roof["traffic_note"] = "DRAM bytes per step of the phase's launches (ncu, same sources)"
+        roof["traffic_note"] = ("DRAM bytes per step of the phase's launches (ncu, same sources; "
+                                + MEASURED_TRAFFIC["note"] + ")")
         if dom == "precond":
             roof["algorithmic_bytes"] = acc.get("precond_bytes")
     roof["phase"] = dom
