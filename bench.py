@@ -411,8 +411,15 @@ def run_gpu(args, peaks, peak_kind):
     ikfac = args.workload in IKFAC_WORKLOADS
     mode = (K.KFAC_IKFAC_BF16 if args.workload in IKFAC_BF16_WORKLOADS
             else K.KFAC_IKFAC_TF32 if ikfac else K.KFAC_IKFAC_OFF)
+    # The inverse-free step K <- K(I - (beta/2)(K^T F_d K - I)) contracts only while
+    # K^T F_d K stays near I: with the EMA starting from zero a factor grows about
+    # 8x between the first refresh (the Cholesky seed) and the next, and beta = 1
+    # steps then diverge (inverse error 0.6, 30, 1e11 at steps 11, 21, 31).  Those
+    # variants start the EMA from the first factor, so that K follows the batch-to-
+    # batch changes only.
     h = K.Kfac(descs, ema_decay=hp.ema_decay, damping=hp.damping, lr=hp.lr, momentum=hp.momentum,
                weight_decay=hp.weight_decay, max_rows=max_rows, device=dev, ikfac=mode,
+               ema_init=K.KFAC_EMA_INIT_FIRST if ikfac else K.KFAC_EMA_INIT_ZERO,
                math=(K.KFAC_MATH_BF16 if args.workload in BF16_PRECOND_WORKLOADS
                      else K.KFAC_MATH_3XTF32))
     ties = qkv_ties(layers) if args.workload in TIED_WORKLOADS else {}
@@ -881,11 +888,14 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
             outs[i:i + 1].copy_(metric[i:i + 1], non_blocking=True)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
-    if not all(math.isfinite(v) for v in outs[:warm + steps].tolist()):
-        raise RuntimeError("end-to-end step produced a non-finite parameter sum")
+    finite = all(math.isfinite(v) for v in outs[:warm + steps].tolist())
+    if not finite:
+        print("bench.py: the end-to-end steps' parameter sums are not finite (the "
+              "trajectory diverged)", file=sys.stderr, flush=True)
     return {"value": round(1.0 / dt, 3), "unit": "steps/s", "h2d_bytes_per_step": int(total),
             "d2h_bytes_per_step": 4, "steps": steps, "warmup": warm,
             "result": "sum of all updated parameters (fp32, reduced on the device)",
+            "result_finite": finite,
             "pipelined": "the next step's H2D on a copy stream during this step; the result's "
                          "D2H on a second copy stream"}
 
