@@ -1248,15 +1248,18 @@ struct PersistKernel<kBF16, EPI, 256> {
 //                          single-CTA persistent kernel), one arrival per warp on
 //                          the even CTA's accumulator-empty barrier
 // The pair loops over tiles t = pair, pair + pairs, ...; every wait is bounded.
-template <bool kBF16>
+// kMN (the in-place bf16 SYRK): stages of 128 k rows, so that each operand's
+// stage is one 32 KB box; 64-row stages (two boxes of 16 KB per stage and
+// operand, six stages) ran the transformer factor phase 8% slower.
+template <bool kBF16, bool kMN = false>
 struct PairCfg {
   static constexpr int BM = 128, BN = 256;           // per CTA: 128 rows x 256 columns
   static constexpr int ELT = kBF16 ? 2 : 4;
-  static constexpr int BK = 128 / ELT;
+  static constexpr int BK = kMN ? 128 : 128 / ELT;
   static constexpr int KMMA = 32 / ELT;
-  static constexpr int A_BYTES = BM * 128;           // 16 KB
-  static constexpr int BH_BYTES = (BN / 2) * 128;    // this CTA's half of B: 16 KB
-  static constexpr int MN_CHUNK = 64 * 128;          // MN-major: 64 features x 64 k
+  static constexpr int A_BYTES = BM * BK * ELT;      // K-major: 128-byte rows, 16 KB
+  static constexpr int BH_BYTES = (BN / 2) * BK * ELT;   // this CTA's half of B
+  static constexpr int MN_CHUNK = BK * 128;          // MN-major: 64 features x BK k
   static constexpr int HALF_BYTES = A_BYTES + BH_BYTES;
   static constexpr int STAGE_BYTES = kBF16 ? HALF_BYTES : 2 * HALF_BYTES;
   static constexpr int EPI_WARPS = 16, CW = 64;
@@ -1273,7 +1276,7 @@ struct PairCfg {
 
 template <bool kBF16, int EPI, bool kMN>
 __device__ __forceinline__ void pair_body(const GroupedTc& g) {
-  using PC = PairCfg<kBF16>;
+  using PC = PairCfg<kBF16, kMN>;
   static_assert(!kMN || (kBF16 && EPI == TC_EPI_SYRK), "MN-major operands: bf16 SYRK");
   constexpr int CW = PC::CW, BN = PC::BN, STAGES = PC::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -1357,7 +1360,7 @@ __device__ __forceinline__ void pair_body(const GroupedTc& g) {
           const uint32_t fb = full0 + (uint32_t)(stage * sizeof(uint64_t));
           if (rank == 0) tc::mbar_expect_tx(&full[stage], 2 * bytes);   // both CTAs' loads
           if constexpr (kMN) {
-            // features [row0, row0 + 128) of k rows [k0, k0 + 64) as two 64-feature
+            // features [row0, row0 + 128) of k rows [k0, k0 + BK) as two 64-feature
             // chunks; the bias feature's chunk from the ones map
             // (m[2]: both chunks in one box, for blocks of whole chunks without the
             // bias feature; m[0] per chunk, zero past d; m[1] the ones matrix)
@@ -1800,15 +1803,15 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t rows, int64_t
 }
 
 // bf16 [rows x 64 chunks] (pitch in elements) seen as [chunks][rows][64]: a box
-// of 2 chunks x 64 rows x 64 elements lands in shared memory as two 64-row MN-major
+// of 2 chunks x box_rows rows x 64 elements lands in shared memory as two MN-major
 // chunk tiles (128-byte swizzle), the layout two 2-D boxes of make_map would give.
 bool make_chunk_map(CUtensorMap* m, const void* base, int64_t rows, int64_t chunks,
-                    int64_t pitch) {
+                    int64_t pitch, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {64u, (cuuint64_t)rows, (cuuint64_t)chunks};
   cuuint64_t strides[2] = {(cuuint64_t)(pitch * 2), 128u};
-  cuuint32_t box[3] = {64u, 64u, 2u};
+  cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 2u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -2086,7 +2089,7 @@ kfac_status launch_persistent_kernel(const GroupedTc& g, cudaStream_t st) {
 
 template <bool kBF16, int EPI, bool kMN = false>
 kfac_status launch_pair_kernel(const GroupedTc& g, cudaStream_t st) {
-  using PC = PairCfg<kBF16>;
+  using PC = PairCfg<kBF16, kMN>;
   static bool attr_ok = cudaFuncSetAttribute(gemm_tc_pair_kernel<kBF16, EPI, kMN>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)PC::SMEM) == cudaSuccess;
@@ -2208,9 +2211,11 @@ bool syrk_direct_layout_ok(const kfac_ctx* h, const void* x, int64_t ld, int64_t
 
 // The factor SYRKs of bf16 layers read straight from the callers' activations:
 // a [K x d] row-major array is, for C = X^T X, an MN-major operand (features
-// contiguous), which the bf16 MMA takes through its transpose bits.  Tensor maps
-// over x load 64 features x 64 k per box; the ones column of x-hat (feature d of
-// a layer with a bias) loads from a [K x 64] matrix whose first column is one.
+// contiguous), which the bf16 MMA takes through its transpose bits.  A 3-D tensor
+// map over x loads 128 features x 128 k per box (2-D maps, 64 features per box,
+// for blocks with the bias feature or a ragged edge); the ones column of x-hat
+// (feature d of a layer with a bias) loads from a [K x 64] matrix whose first
+// column is one.
 // Saves the pack's read and write of every input.  CTA pairs as in
 // launch_wide_persistent; groups of kMaxGroup.
 kfac_status launch_syrk_direct(kfac_ctx* h, const TcProblem* probs, int count, cudaStream_t st) {
@@ -2223,15 +2228,16 @@ kfac_status launch_syrk_direct(kfac_ctx* h, const TcProblem* probs, int count, c
     for (int i = 0; i < cnt; ++i) {
       const TcProblem& pr = probs[c0 + i];
       CUtensorMap* m = &g->maps[4 * i];
-      if (!make_map(&m[0], pr.A.hi, true, pr.K, pr.A.rows, pr.A.pitch, 64)) return KFAC_ERR_CUDA;
+      constexpr int kb = PairCfg<true, true>::BK;   // k rows per box
+      if (!make_map(&m[0], pr.A.hi, true, pr.K, pr.A.rows, pr.A.pitch, kb)) return KFAC_ERR_CUDA;
       if (pr.bias_col >= 0) {
-        if (!make_map(&m[1], h->ws + h->off_ones, true, pr.K, 64, 64, 64)) return KFAC_ERR_CUDA;
+        if (!make_map(&m[1], h->ws + h->off_ones, true, pr.K, 64, 64, kb)) return KFAC_ERR_CUDA;
       } else {
         m[1] = m[0];
       }
       const int full = (int)(pr.A.rows / 64 * 64);
       if (full >= 64) {
-        if (!make_chunk_map(&m[2], pr.A.hi, pr.K, pr.A.rows / 64, pr.A.pitch)) return KFAC_ERR_CUDA;
+        if (!make_chunk_map(&m[2], pr.A.hi, pr.K, pr.A.rows / 64, pr.A.pitch, kb)) return KFAC_ERR_CUDA;
       } else {
         m[2] = m[0];
       }
