@@ -79,8 +79,8 @@ TF32_PER_BF16 = 1.1 / 2.25          # nominal dense ratio
 # change to them reports null until the counters are taken again.
 MEASURED_TRAFFIC = {
     "workload": "transformer4",
-    "sources_sha256": "7162a262dfd93db3f5df7edf3f8e95b96e40d942a0a1ae1b3bbeadc84945b65d",
-    "bytes": {"factor": 4 * 8.0019e9, "precond": 4 * 5.7630e9, "diag": 4 * 2.1918e9},
+    "sources_sha256": "27fe7c11b1ea5427c03acc4a13ce8c2c283b0ce1af959d4a0ee107e10ac8ebe5",
+    "bytes": {"factor": 4 * 5.0232e9, "precond": 4 * 5.7630e9, "diag": 4 * 2.1917e9},
     "note": "one-block capture (transformer1) x 4",
 }
 
