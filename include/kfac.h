@@ -63,7 +63,7 @@ typedef enum {
   KFAC_ERR_NOT_PD = 4,       /* device: damped factor not positive definite        */
   KFAC_ERR_TIMEOUT = 5,      /* device: a bounded pipeline wait gave up            */
   KFAC_ERR_CUDA = 6,         /* a CUDA runtime call or launch failed               */
-  KFAC_ERR_UNSUPPORTED = 7   /* valid request this build does not implement        */
+  KFAC_ERR_UNSUPPORTED = 7   /* valid request the library does not implement       */
 } kfac_status;
 
 typedef enum { KFAC_KRON = 0, KFAC_DIAG = 1 } kfac_kind;

@@ -343,7 +343,7 @@ const char* kfac_status_string(kfac_status s) {
     case KFAC_ERR_NOT_PD: return "damped factor is not positive definite";
     case KFAC_ERR_TIMEOUT: return "device pipeline wait timed out";
     case KFAC_ERR_CUDA: return "CUDA runtime error";
-    case KFAC_ERR_UNSUPPORTED: return "unsupported by this build";
+    case KFAC_ERR_UNSUPPORTED: return "unsupported by the library";
   }
   return "unknown status";
 }
