@@ -237,6 +237,9 @@ struct TcProblem {
   // reduction range per output tile, for products with a triangular operand:
   // 0 all of K; 1 k >= the tile's first column; 2 k < the tile's last column + 1
   int kmode;
+  // 3xTF32 products on CTA pairs or wide persistent tiles: k elements per TMEM
+  // drain (0: the default, 128; a multiple of 32); every problem of a call the same
+  int drain_k;
   // launch_syrk_direct only: A.hi is the caller's bf16 [K x A.rows] array (row
   // pitch A.pitch elements, features contiguous) read as an MN-major operand;
   // feature bias_col (a multiple of 64, or -1) reads as ones

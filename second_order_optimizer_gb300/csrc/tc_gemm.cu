@@ -2127,11 +2127,12 @@ kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProb
   constexpr int BN = 256;
   const int BM = pair ? 256 : 128;                   // rows of a tile
   const int box_a = 128, box_b = pair ? 128 : BN;    // rows of A and B each CTA loads
-  const int unit = bf16 ? kKsubBf16Wide : kKsubTf32;
   std::unique_ptr<GroupedTc> g(new GroupedTc());
   for (int c0 = 0; c0 < count; c0 += kMaxGroup) {
     std::memset(g.get(), 0, sizeof(GroupedTc));
     const int cnt = std::min(kMaxGroup, count - c0);
+    // one drain period for the launch (the kernel reads it from its first problem)
+    const int unit = bf16 ? kKsubBf16Wide : probs[c0].drain_k > 0 ? probs[c0].drain_k : kKsubTf32;
     int blocks = 0;
     for (int i = 0; i < cnt; ++i) {
       const TcProblem& pr = probs[c0 + i];
