@@ -1839,12 +1839,13 @@ bool set_smem_attr() {
 constexpr int kKsubTf32 = 128;
 constexpr int kKsubBf16 = 256;
 // k elements per TMEM drain of the 256-wide persistent and CTA-pair bf16 products:
-// 64 MMAs.  Measured on a 16384-row SYRK of o = 8192 against float64: 3.4e-7
-// relative at 512, 7.1e-7 at 1024, 1.9e-6 at 2048, 2.4e-5 with no drain.  Each
-// drain costs the drain warps about 2000 cycles and the pair's two accumulators
-// let the MMA run only two drain periods ahead of a tile's epilogue, so 1024 is
-// about 7% faster than 512 on that SYRK.
-constexpr int kKsubBf16Wide = 1024;
+// 128 MMAs.  Measured on a 16384-row SYRK of o = 8192 against float64: 3.4e-7
+// relative at 512, 7.1e-7 at 1024, 1.9e-6 at 2048, 2.4e-5 with no drain (the
+// factor gate is 1e-5).  Each drain costs the drain warps about 2000 cycles and
+// the pair's two accumulators let the MMA run only two drain periods ahead of a
+// tile's epilogue: the transformer factor phase takes 7.65 ms at 1024 and
+// 7.34 ms at 2048.
+constexpr int kKsubBf16Wide = 2048;
 // Products with a wave of wide tiles run on CTA pairs (256 x 256 tiles).
 constexpr bool kWidePairs = true;
 
