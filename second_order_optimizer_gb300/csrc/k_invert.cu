@@ -401,9 +401,10 @@ __global__ void __launch_bounds__(256) panel_split_kernel(const __grid_constant_
   }
 }
 
-// Finv -> the operand form of the K4 products: TF32 halves with a 16-byte row
-// pitch (np), or, for bf16 preconditioning, bf16 values in the hi array with a
-// row pitch of 2 np elements.
+// Finv -> the operand form of the K4 products (the inverses are their B
+// operands): TF32 hi and bf16 correction pairs (tc::corr_pair, B form) with a
+// 16-byte row pitch (np), or, for bf16 preconditioning, bf16 values in the hi
+// array with a row pitch of 2 np elements.
 __global__ void __launch_bounds__(256) inv_split_kernel(const InvJob* jobs, int bf16) {
   pdl_wait();
   pdl_trigger();
@@ -418,14 +419,9 @@ __global__ void __launch_bounds__(256) inv_split_kernel(const InvJob* jobs, int 
       continue;
     }
     float* dh = J.Finv_hi + r * J.np;
-    float* dl = J.Finv_lo + r * J.np;
+    uint32_t* dl = reinterpret_cast<uint32_t*>(J.Finv_lo) + r * J.np;
 #pragma unroll 4
-    for (int c = threadIdx.x; c < J.n; c += blockDim.x) {
-      const float v = src[c];
-      const float hi = tc::to_tf32(v);
-      dh[c] = hi;
-      dl[c] = tc::to_tf32(v - hi);
-    }
+    for (int c = threadIdx.x; c < J.n; c += blockDim.x) dh[c] = tc::corr_pair(src[c], true, &dl[c]);
   }
 }
 

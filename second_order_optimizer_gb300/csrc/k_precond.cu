@@ -9,14 +9,20 @@
 // (precondition, then momentum and weight decay, then the in-place write),
 // fused here into the epilogue of the second product.
 //
-// Both products run on the tensor cores in 3xTF32 (fp32 accuracy):
-//   pack     dW-hat = [dW | db] -> TF32 halves [o x n_p]
-//   X    =   dW-hat . Ainv        M = o, N = n, K = n   epilogue stores X^T as TF32 halves
+// Both products run on the tensor cores with fp32 operands split as
+// v = h + r, h the TF32 rounding: the product of the h's in TF32 plus the two
+// cross terms h_a r_b + r_a h_b in one bf16 MMA over bf16 roundings of h and r
+// (tc::corr_pair).  That is two MMA issues per 8 k against three for 3xTF32,
+// and the dropped parts (r_a r_b, the bf16 rounding of the cross terms) are
+// about 2^-20 of each product: P within ~1e-6 of its exact value at
+// cond(F) = 2e4 against ~1e-7 for 3xTF32.
+//   pack     dW-hat = [dW | db] -> hi [o x n_p] + correction pairs (A form)
+//   X    =   dW-hat . Ainv        M = o, N = n, K = n   epilogue stores X^T (hi + A-form pairs)
 //   P^T  =   X^T . Ginv           M = n, N = o, K = o   epilogue: P out and/or W, m update
 // (Ainv and Ginv are symmetric.)  Storing X^T keeps every operand K-major, and
 // with the products oriented this way each epilogue thread, which holds one
 // accumulator row, writes to consecutive addresses across a warp.  Ainv/Ginv
-// halves are produced once per refresh by the inverse pass.
+// operands (hi + B-form pairs) are produced once per refresh by the inverse pass.
 #include "kfac_internal.cuh"
 #include "tc_prims.cuh"
 
@@ -34,7 +40,8 @@ struct GradPackJob {
   int64_t ld, np;
   int o, d_in, n;
   float* hi;
-  float* lo;      // null: bf16 values in hi, row pitch 2 np elements
+  float* lo;      // correction pairs (tc::corr_pair, A form); null: bf16 values
+                  // in hi, row pitch 2 np elements
   int vec;        // rows of gw, hi and lo 16-byte aligned: float4 over the weight columns
 };
 constexpr int kMaxGradPack = 16;
@@ -68,30 +75,24 @@ __global__ void __launch_bounds__(256) gradhat_pack_grouped_kernel(
         b[j] = __float2bfloat16_rn(j < J.d_in ? __ldg(src + j) : J.gb[i]);
       continue;
     }
+    // TF32 + bf16-correction form (A operand)
     float* hi = J.hi + (int64_t)i * J.np;
-    float* lo = J.lo + (int64_t)i * J.np;
+    uint32_t* lo = reinterpret_cast<uint32_t*>(J.lo) + (int64_t)i * J.np;
 #pragma unroll 2
     for (int j = 4 * threadIdx.x; j < j0; j += 4 * blockDim.x) {
       const float4 v = __ldg(reinterpret_cast<const float4*>(src + j));
-      float4 h, l;
-      h.x = tc::to_tf32(v.x);
-      h.y = tc::to_tf32(v.y);
-      h.z = tc::to_tf32(v.z);
-      h.w = tc::to_tf32(v.w);
-      l.x = tc::to_tf32(v.x - h.x);
-      l.y = tc::to_tf32(v.y - h.y);
-      l.z = tc::to_tf32(v.z - h.z);
-      l.w = tc::to_tf32(v.w - h.w);
+      float4 h;
+      uint4 l;
+      h.x = tc::corr_pair(v.x, false, &l.x);
+      h.y = tc::corr_pair(v.y, false, &l.y);
+      h.z = tc::corr_pair(v.z, false, &l.z);
+      h.w = tc::corr_pair(v.w, false, &l.w);
       *reinterpret_cast<float4*>(hi + j) = h;
-      *reinterpret_cast<float4*>(lo + j) = l;
+      *reinterpret_cast<uint4*>(lo + j) = l;
     }
 #pragma unroll 4
-    for (int j = j0 + threadIdx.x; j < J.n; j += blockDim.x) {
-      const float v = j < J.d_in ? __ldg(src + j) : J.gb[i];
-      const float h = tc::to_tf32(v);
-      hi[j] = h;
-      lo[j] = tc::to_tf32(v - h);
-    }
+    for (int j = j0 + threadIdx.x; j < J.n; j += blockDim.x)
+      hi[j] = tc::corr_pair(j < J.d_in ? __ldg(src + j) : J.gb[i], false, &lo[j]);
   }
 }
 
@@ -175,13 +176,16 @@ kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layer
     max_rows = std::max<int64_t>(max_rows, L.o);
     const int64_t npb = bf ? 2 * np : np, opb = bf ? 2 * op : op;   // operand pitches
     TcProblem q1{};
-    q1.A = TcOperand{g_hi, bf ? nullptr : g_lo, L.o, npb};   // X = grad-hat . Ainv, as X^T
-    q1.B = TcOperand{h->at<float>(L.Ainv_hi), bf ? nullptr : h->at<float>(L.Ainv_lo), L.n, npb};
+    const int corr = bf ? 0 : 1;
+    q1.A = TcOperand{g_hi, bf ? nullptr : g_lo, L.o, npb, corr};   // X = grad-hat . Ainv, as X^T
+    q1.B = TcOperand{h->at<float>(L.Ainv_hi), bf ? nullptr : h->at<float>(L.Ainv_lo), L.n, npb,
+                     corr};
     q1.M = L.o;
     q1.N = L.n;
     q1.K = L.n;
     q1.e.out_hi = x_hi;
     q1.e.out_lo = bf ? nullptr : x_lo;
+    q1.e.out_corr = corr;
     q1.e.out_bf16 = bf ? 1 : 0;
     q1.e.alpha = 1.f;
     q1.e.ldo = opb;
@@ -189,8 +193,9 @@ kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layer
     q1.drain_k = kPrecondDrainK;
     p1.push_back(q1);
     TcProblem q2{};
-    q2.A = TcOperand{x_hi, bf ? nullptr : x_lo, L.n, opb};   // P^T = X^T . Ginv
-    q2.B = TcOperand{h->at<float>(L.Ginv_hi), bf ? nullptr : h->at<float>(L.Ginv_lo), L.o, opb};
+    q2.A = TcOperand{x_hi, bf ? nullptr : x_lo, L.n, opb, corr};   // P^T = X^T . Ginv
+    q2.B = TcOperand{h->at<float>(L.Ginv_hi), bf ? nullptr : h->at<float>(L.Ginv_lo), L.o, opb,
+                     corr};
     q2.M = L.n;
     q2.N = L.o;
     q2.K = L.o;

@@ -81,8 +81,8 @@ struct InvJob {
   float* X;         // L^{-1} (n x n, lower; upper zero)
   float* Y;         // level scratch (n x n/2 + tile slack)
   float* Finv;      // result (n x n, pitch n)
-  float* Finv_hi;   // result as TF32 halves, pitch np (operands of the K4 products)
-  float* Finv_lo;
+  float* Finv_hi;   // result as a K4 operand, pitch np: TF32 hi and the bf16
+  float* Finv_lo;   //   correction pairs of tc::corr_pair (B form)
   // inverse-free update (handles created with ikfac): K and K^T as TF32 halves,
   // and two scratch operands, all n x np; null otherwise
   float *K_hi, *K_lo, *Kt_hi, *Kt_lo, *S1_hi, *S1_lo, *S2_hi, *S2_lo;
@@ -209,8 +209,9 @@ kfac_status launch_precondition_batched(kfac_ctx* h, int count, const int* layer
 enum { TC_EPI_SYRK = 0, TC_EPI_SPLIT = 1, TC_EPI_PRECOND = 2 };
 struct TcOperand {       // K-major operand: rows x K, row pitch in elements (16-byte multiple)
   const void* hi;        // fp32 TF32-high half, or bf16 values
-  const void* lo;        // fp32 TF32-low half (unused for bf16)
-  int64_t rows, pitch;
+  const void* lo;        // fp32 TF32-low half (unused for bf16), or with corr the
+  int64_t rows, pitch;   //   bf16 correction pairs of tc::corr_pair (A or B form
+  int corr;              //   by the operand's role); both operands of a product agree
 };
 struct TcEpilogue {
   float alpha, beta;     // SYRK: F <- beta F + alpha C (upper + mirror)
@@ -218,6 +219,7 @@ struct TcEpilogue {
   int64_t ldc;
   float* out_hi;         // SPLIT: C^T stored as TF32 halves, out[c * ldo + r]
   float* out_lo;         //   (null: alpha C^T + beta out stored as fp32 in out_hi)
+  int out_corr;          //   1: out_lo receives C^T's bf16 correction pairs (A form)
   int out_bf16;          //   1: alpha C^T stored as bf16 in out_hi (a bf16 array)
   int64_t ldo;
   int d_in;              // PRECOND: C = P^T (n x o): C[j][i] = P[i][j]; j >= d_in is the bias

@@ -4,8 +4,9 @@
 //   with one of three fused epilogues:
 //     SYRK     F <- beta F + alpha C on tiles on/above the diagonal, plus mirrors (K1,
 //              with A = B = X = x-hat^T)
-//     SPLIT    store C^T as TF32 halves (hi, lo), ready to be the next product's operand;
-//              with no lo buffer, alpha C^T as fp32 (or as bf16: out_bf16)
+//     SPLIT    store C^T as TF32 halves (hi, lo), or as TF32 hi and bf16 correction
+//              pairs (out_corr), ready to be the next product's operand; with no lo
+//              buffer, alpha C^T as fp32 (or as bf16: out_bf16)
 //     PRECOND  P^T = C; optional momentum / weight-decay / lr update of W in place (K4)
 //
 // Osawa et al., "Large-Scale Distributed Second-Order Optimization Using
@@ -21,6 +22,8 @@
 //         -> X = x-hat^T [n x Kp], K-major, so both MMA operands are K-major
 //         tiles.  fp32 input is split into TF32 halves hi = rna(x),
 //         lo = rna(x - hi) (3xTF32: hi*hi + hi*lo + lo*hi carries ~21 bits).
+//         Operands with TcOperand::corr replace the two cross MMAs by one bf16
+//         MMA over (hi, x - hi) pairs (tc::corr_pair; ~20 bits).
 //  syrk:  one 128 x 128 output tile per CTA (split-K over rows when the
 //         triangle has fewer tiles than SMs), warp-specialised:
 //           warp 0  TMA producer   (SW128 tiles of 128 rows x 128 bytes)
@@ -92,6 +95,7 @@ struct GemmTcParams {
   int ksub;              // k elements per TMEM drain (multiple of BK)
   int bias_col;          // MN-major pair SYRK: feature read from the ones map (or -1)
   int mn_full;           //   features in whole 64-feature chunks (64 floor(d / 64))
+  int corr;              // fp32 operands in the TF32 + bf16-correction form (TcOperand::corr)
   float* part;           // this product's cluster partials [tile][groups][BM][BN]
   int* tickets;          // this product's tickets [tile][csize]
   DevStatus* status;
@@ -157,6 +161,15 @@ __host__ __device__ inline void k_range(int kmode, int64_t K, int64_t c0, int bn
   *khi = K;
   if (kmode == 1) *klo = c0 < K ? c0 : K;
   else if (kmode == 2) *khi = c0 + bn < K ? c0 + bn : K;
+}
+
+// SPLIT output entry C^T[gc][gr] = v in the TF32 + bf16-correction form (an A
+// operand of the next product): the TF32 hi in out_hi, the bf16 pair of
+// tc::corr_pair in out_lo.
+__device__ __forceinline__ void store_corr(const TcEpilogue& E, int64_t gc, int64_t gr, float v) {
+  uint32_t pr;
+  E.out_hi[gc * E.ldo + gr] = tc::corr_pair(v, false, &pr);
+  reinterpret_cast<uint32_t*>(E.out_lo)[gc * E.ldo + gr] = pr;
 }
 
 // One output tile (and one k-split of it).
@@ -278,6 +291,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
   } else if (warp == 1) {
     if (lane == 0) {  // ------------------------------------------ MMA issuer
       constexpr uint32_t idesc = tc::make_idesc(kBF16 ? 1 : 2, C::BM, C::BN);
+      constexpr uint32_t idesc_c = tc::make_idesc(1, C::BM, C::BN);   // bf16 corrections
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -310,6 +324,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
             if (kBF16) {
               tc::umma_f16(d, tc::sdesc_kmajor_sw128(a_hi + off), tc::sdesc_kmajor_sw128(b_hi + off),
                            idesc, acc);
+            } else if (p.corr) {
+              tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_hi + off),
+                            tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
+              tc::umma_f16(d, tc::sdesc_kmajor_sw128(a_lo + off),
+                           tc::sdesc_kmajor_sw128(b_lo + off), idesc_c, 1u);
             } else {
               tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_hi + off),
                             tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
@@ -440,6 +459,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
           for (int c = 0; c < C::CW; ++c) {
             const int64_t gc = c0 + h * C::CW + c;
             if (gc < pN) ob[gc * E.ldo + gr] = __float2bfloat16_rn(E.alpha * sum[c]);
+          }
+        } else if (E.out_lo && E.out_corr) {
+#pragma unroll
+          for (int c = 0; c < C::CW; ++c) {
+            const int64_t gc = c0 + h * C::CW + c;
+            if (gc < pN) store_corr(E, gc, gr, sum[c]);
           }
         } else if (E.out_lo) {
 #pragma unroll
@@ -669,6 +694,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* map_a_hi, const CUt
       if (!E.out_lo) {   // alpha C^T (+ beta C_old^T) as fp32
         float* o = E.out_hi + gc * E.ldo + gr;
         *o = E.beta != 0.f ? fmaf(E.beta, *o, E.alpha * v) : E.alpha * v;
+        continue;
+      }
+      if (E.out_corr) {
+        store_corr(E, gc, gr, v);
         continue;
       }
       const float hi = tc::to_tf32(v);
@@ -925,6 +954,10 @@ __device__ __forceinline__ void epilogue_from_registers(const TcEpilogue& E, flo
         const int64_t gc = c0 + c;
         if (gc < pN) ob[gc * E.ldo + gr] = __float2bfloat16_rn(E.alpha * sum[c]);
       }
+    } else if (gr < pM && E.out_lo && E.out_corr) {
+#pragma unroll
+      for (int c = 0; c < CW; ++c)
+        if (c0 + c < pN) store_corr(E, c0 + c, gr, sum[c]);
     } else if (gr < pM && E.out_lo) {
 #pragma unroll
       for (int c = 0; c < CW; ++c) {
@@ -1079,6 +1112,7 @@ __device__ __forceinline__ void persistent_body(const GroupedTc& g) {
   } else if (warp == 1) {
     if (lane == 0) {  // ------------------------------------------ MMA issuer
       constexpr uint32_t idesc = tc::make_idesc(kBF16 ? 1 : 2, C::BM, BN);
+      constexpr uint32_t idesc_c = tc::make_idesc(1, C::BM, BN);   // bf16 corrections
       int stage = 0;
       uint32_t phase = 0;
       int gsub = 0;
@@ -1087,6 +1121,7 @@ __device__ __forceinline__ void persistent_body(const GroupedTc& g) {
         int q, ti, tj;
         grouped_tile<PC::R>(g, t, &q, &ti, &tj);
         const int aib = a_in_b(q, ti, tj);
+        const bool corr = !kBF16 && g.prob[q].corr != 0;
         int kb_lo;
         const int nkb = kblocks(q, tj, &kb_lo);
         const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
@@ -1123,6 +1158,11 @@ __device__ __forceinline__ void persistent_body(const GroupedTc& g) {
               if (kBF16) {
                 tc::umma_f16(d, tc::sdesc_kmajor_sw128(a_hi + off),
                              tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
+              } else if (corr) {
+                tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_hi + off),
+                              tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
+                tc::umma_f16(d, tc::sdesc_kmajor_sw128(a_lo + off),
+                             tc::sdesc_kmajor_sw128(b_lo + off), idesc_c, 1u);
               } else {
                 tc::umma_tf32(d, tc::sdesc_kmajor_sw128(a_hi + off),
                               tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
@@ -1399,6 +1439,7 @@ __device__ __forceinline__ void pair_body(const GroupedTc& g) {
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {  // ------------------------------ MMA issuer
       constexpr uint32_t idesc = tc::make_idesc(kBF16 ? 1 : 2, 256, BN);
+      constexpr uint32_t idesc_c = tc::make_idesc(1, 256, BN);   // bf16 corrections
       int stage = 0;
       uint32_t phase = 0;
       int gsub = 0;
@@ -1407,6 +1448,7 @@ __device__ __forceinline__ void pair_body(const GroupedTc& g) {
         int q, ti, tj;
         grouped_tile<1>(g, t, &q, &ti, &tj);
         const bool aib = a_in_b(q, ti, tj);
+        const bool corr = !kBF16 && g.prob[q].corr != 0;
         int kb_lo;
         const int nkb = kblocks(q, tj, &kb_lo);
         const int nsub = (nkb + kb_per_sub - 1) / kb_per_sub;
@@ -1445,6 +1487,11 @@ __device__ __forceinline__ void pair_body(const GroupedTc& g) {
               } else if (kBF16) {
                 tc::umma_f16_pair(d, tc::sdesc_kmajor_sw128(a_hi + off),
                                   tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
+              } else if (corr) {
+                tc::umma_tf32_pair(d, tc::sdesc_kmajor_sw128(a_hi + off),
+                                   tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
+                tc::umma_f16_pair(d, tc::sdesc_kmajor_sw128(a_lo + off),
+                                  tc::sdesc_kmajor_sw128(b_lo + off), idesc_c, 1u);
               } else {
                 tc::umma_tf32_pair(d, tc::sdesc_kmajor_sw128(a_hi + off),
                                    tc::sdesc_kmajor_sw128(b_hi + off), idesc, acc);
@@ -1975,11 +2022,18 @@ kfac_status dispatch(bool bf16, int epi, unsigned grid, const CUtensorMap& ah,
 kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProblem* probs,
                                    int count, cudaStream_t st, bool pair);
 
+// the correction form pairs an A form with a B form: both operands or neither,
+// fp32 operands in distinct arrays
+bool corr_ok(bool bf16, const TcOperand& A, const TcOperand& B, bool same_ab) {
+  return A.corr == B.corr && (!A.corr || (!bf16 && !same_ab));
+}
+
 kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcOperand& A,
                            const TcOperand& B, bool same_ab, bool upper, int64_t M, int64_t N,
                            int64_t K, const TcEpilogue& e, cudaStream_t st, int kmode) {
   constexpr int BM = 128;
   const int sms = num_sms();
+  if (!corr_ok(bf16, A, B, same_ab)) return KFAC_ERR_INVALID_ARG;
   // Tile width: 128 x 256 halves the shared-memory traffic per MMA flop of
   // 128 x 128, which pays on long reductions or when there are tiles enough to
   // fill the GPU; short, small products keep 128 x 128 for parallelism.
@@ -2026,6 +2080,7 @@ kfac_status launch_gemm_tc(kfac_ctx* h, int layer, bool bf16, int epi, const TcO
   p.upper = upper ? 1 : 0;
   p.same_ab = same_ab ? 1 : 0;
   p.kmode = kmode;
+  p.corr = A.corr;
   const int64_t tiles = count(BN);
   // enough CTAs for one wave when the output has fewer tiles than SMs
   const int unit = bf16 ? kKsubBf16 : kKsubTf32;
@@ -2159,6 +2214,7 @@ kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProb
       pp.same_ab = pr.same_ab ? 1 : 0;
       pp.kmode = pr.kmode;
       pp.colmajor = pr.M < pr.N ? 1 : 0;
+      pp.corr = pr.A.corr;
       pp.splits = 1;
       pp.csize = 1;
       pp.k_per_split = cdiv(pr.K, unit) * unit;
@@ -2306,6 +2362,8 @@ kfac_status launch_grouped_kernel(unsigned grid, const GroupedTc& g, cudaStream_
 // cut when the split-K scratch is full.
 kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProblem* probs,
                                    int count, cudaStream_t st) {
+  for (int q = 0; q < count; ++q)
+    if (!corr_ok(bf16, probs[q].A, probs[q].B, probs[q].same_ab)) return KFAC_ERR_INVALID_ARG;
   if (count == 1) {
     const TcProblem& q = probs[0];
     return launch_gemm_tc(h, q.layer, bf16, epi, q.A, q.B, q.same_ab, q.upper, q.M, q.N, q.K,
@@ -2436,6 +2494,7 @@ kfac_status launch_gemm_tc_grouped(kfac_ctx* h, bool bf16, int epi, const TcProb
       pp.same_ab = pr.same_ab ? 1 : 0;
       pp.kmode = pr.kmode;
       pp.colmajor = pr.M < pr.N ? 1 : 0;
+      pp.corr = pr.A.corr;
       pp.splits = sh.splits;
       pp.csize = sh.csize;
       pp.k_per_split = sh.kps;

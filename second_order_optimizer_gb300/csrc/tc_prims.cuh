@@ -6,6 +6,7 @@
 // and winds down instead of spinning forever.
 #pragma once
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -318,6 +319,20 @@ __device__ __forceinline__ float to_tf32(float x) {
   uint32_t r;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
   return __uint_as_float(r);
+}
+
+// Operand form of the TF32 + bf16-correction products.  A value v enters as
+// its TF32 rounding h (the hi array) and, in the lo array, as one 4-byte pair
+// of bf16 roundings: (h, r) for an A operand, (r, h) for a B operand (first
+// element at the lower address), r = v - h (exact in fp32).  One bf16 MMA over a
+// 32-byte slice (8 k, 16 bf16) then adds sum_k h_a r_b + r_a h_b to the TF32
+// product of the hi arrays.  A pair takes the 4-byte slot the fp32 lo half
+// would, so both forms share tensor maps, pitches and zero fill past K.
+__device__ __forceinline__ float corr_pair(float v, bool b_role, uint32_t* pair) {
+  const float h = to_tf32(v), r = v - h;
+  __nv_bfloat162 p = b_role ? __floats2bfloat162_rn(r, h) : __floats2bfloat162_rn(h, r);
+  *pair = *reinterpret_cast<uint32_t*>(&p);   // .x at the lower address
+  return h;
 }
 
 __device__ __forceinline__ uint32_t elect_one_lane() { return (threadIdx.x & 31) == 0; }
