@@ -79,8 +79,8 @@ TF32_PER_BF16 = 1.1 / 2.25          # nominal dense ratio
 # change to them reports null until the counters are taken again.
 MEASURED_TRAFFIC = {
     "workload": "transformer4",
-    "sources_sha256": "e73ba1b58766fb08dc1da5daff882ff4720aa52585035f1671257f18088a1554",
-    "bytes": {"factor": 4 * 5.0215e9, "precond": 4 * 6.0260e9, "diag": 4 * 2.1914e9},
+    "sources_sha256": "378cd6490eaf782a16df3d1c43a8aede07757215eb5312f9a94f18aa0e5c236d",
+    "bytes": {"factor": 4 * 5.0202e9, "precond": 4 * 6.5459e9, "diag": 4 * 2.1923e9},
     "note": "one-block capture (transformer1) x 4",
 }
 
@@ -165,8 +165,9 @@ def workload_name(cfg, workload):
 
 
 def path_dtype(layers, workload=None):
-    """Arithmetic of the step: fp32 state, factors and preconditioning (3xTF32 on the
-    tensor cores, fp32-accurate); factor products read bf16 inputs where the layer
+    """Arithmetic of the step: fp32 state, factors and preconditioning (fp32 operands
+    on the tensor cores: 3xTF32 factor products, TF32 + bf16-correction
+    preconditioning products); factor products read bf16 inputs where the layer
     set has them; the bf16 inverse-free variants refresh with bf16 products."""
     d = "bf16-in/f32" if any(l.in_dtype == "bf16" for l in layers) else "f32"
     return (d + ("+bf16-refresh" if workload in IKFAC_BF16_WORKLOADS else "")
@@ -699,10 +700,12 @@ def run_gpu(args, peaks, peak_kind):
         ach = flop / (ms * 1e-3) / 1e12
         # the products' own arithmetic sets the peak: bf16 operands (bf16 inputs in the
         # factor phase, bf16 preconditioning) against the bf16 peak, fp32 operands
-        # (three TF32 products each) against the TF32 peak
+        # against the TF32 peak (factor products: three TF32 MMAs per k step;
+        # preconditioning: one TF32 MMA and one bf16 correction MMA of the same time)
         bf = (all(l.in_dtype == "bf16" for l in layers if l.kind == "kron") if dom == "factor"
               else args.workload in BF16_PRECOND_WORKLOADS)
-        arith = "bf16" if bf else "3xTF32"
+        issue = 3 if dom == "factor" else 2
+        arith = "bf16" if bf else "3xTF32" if dom == "factor" else "TF32+bf16-corrections"
         peak = peaks["bf16_tflops"] if bf else tf32_peak
         kern = (f"pack_grouped + gemm_tc_pair/persistent (tcgen05) with the SYRK epilogue ({arith})"
                 if dom == "factor" else
@@ -712,9 +715,9 @@ def run_gpu(args, peaks, peak_kind):
                 "unit": "TFLOP/s", "kernel": kern, "timed": "one batched library call (the phase)",
                 "arithmetic": arith}
         if not bf:
-            roof["issued_frac"] = round(3 * ach / tf32_peak, 4)
+            roof["issued_frac"] = round(issue * ach / tf32_peak, 4)
         roof["note"] = ("algorithmic flops (upper triangle for factors)"
-                        + ("" if bf else "; 3xTF32 issues 3x"))
+                        + ("" if bf else f"; {arith} issues {issue}x TF32 MMA time"))
     else:
         ach = acc["invert_flop"] * k / (inv_ms_refresh * 1e-3) / 1e12
         roof = {"bound": "alu", "achieved": round(ach, 3), "peak": round(FP32_ALU_TFLOPS, 1),

@@ -68,9 +68,11 @@ typedef enum {
 
 typedef enum { KFAC_KRON = 0, KFAC_DIAG = 1 } kfac_kind;
 typedef enum { KFAC_F32 = 0, KFAC_BF16 = 1 } kfac_dtype;
-/* Arithmetic of the preconditioning GEMMs.  3XTF32: fp32 operands split into
- * two TF32 halves, three tensor-core products, fp32 accumulation (matches fp32
- * to ~1e-6).  BF16: the inverses (rounded at each refresh), the gradient and
+/* Arithmetic of the preconditioning GEMMs.  3XTF32 (fp32 accuracy): each fp32
+ * operand v = h + r with h its TF32 rounding; a TF32 tensor-core product of the
+ * h's plus one bf16 product that adds both cross terms h r' + r h' (from bf16
+ * roundings of h and r), fp32 accumulation: the products within ~1e-6 of fp32
+ * (the name is kept from the three-product form it replaces).  BF16: the inverses (rounded at each refresh), the gradient and
  * the intermediate X = dW-hat A^{-1} rounded to bf16, one bf16 tensor-core
  * product each with fp32 accumulation; factors, EMA, inverses and the
  * momentum / parameter update stay fp32 (P within ~1e-2 of fp32).  Fixed at
