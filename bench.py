@@ -765,8 +765,11 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
     """Same step through the public API from pinned host memory: every step copies its
     inputs host -> device and reads its result back, inside the timed region.  The
     inputs of all layers are one packed pinned buffer (a diagonal twin shares its
-    layer's tensors, so they are copied once), double-buffered on the device: the
-    next step's copy runs on a copy stream while this step computes.  The step's
+    layer's tensors, so they are copied once), copied into a ring of E2E_BUFFERS
+    device staging buffers on a copy stream that runs up to E2E_BUFFERS - 1 steps
+    ahead of the compute (a data loader's prefetch): the copy engine keeps
+    streaming through a refresh step, which computes longer than a copy takes.  A
+    buffer is refilled only after the step that read it has finished.  The step's
     result is a metric of the updated parameters, the sum of all of them (every
     updated value enters it; the parameters themselves stay on the device, as in
     training), reduced on the device in fp32 and read back (D2H, 4 bytes) on a
@@ -774,9 +777,10 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
     side stream alongside the preconditioning and the diagonal step (as in the
     timed steps).  With CUDA graphs (the default) the library calls of each phase
     are captured once per staging buffer and replayed, as the timed steps do;
-    --no-graphs makes them eagerly every step.  Three untimed iterations of the
-    same loop come first: in a fresh process the first passes of the copy
-    engines over the newly pinned buffer ran at about half speed."""
+    --no-graphs makes them eagerly every step.  Three untimed steps come first, as
+    a pass of their own (in a fresh process the first passes of the copy engines
+    over the newly pinned buffer ran at about half speed); the timed pass starts
+    from an idle GPU, so every copy of a timed step is inside the timed region."""
     phase_factor, phase_invert, phase_precond, phase_diag = phases
     import torch
     first = {}
@@ -795,7 +799,8 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
     for li, key, o, v in entries:
         nb = v.numel() * v.element_size()
         host[o:o + nb].copy_(v.contiguous().view(-1).view(torch.uint8).cpu())
-    stage = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+    nbuf = E2E_BUFFERS
+    stage = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(nbuf)]
 
     def views(buf):
         per_src = {}
@@ -805,12 +810,12 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
                 stage[buf][o:o + nb].view(v.dtype).view(v.shape)
         return [per_src[first[srcidx[li]]] for li in range(len(layers))]
 
-    xs = [views(0), views(1)]
+    xs = [views(bb) for bb in range(nbuf)]
     if invert_graph is not None:      # capture each phase on each staging buffer
         import second_order_optimizer_gb300 as K  # noqa: F401
         torch.cuda.synchronize()
         gph = {}
-        for bb in range(2):
+        for bb in range(nbuf):
             for name, fn in (("factor", phase_factor), ("precond", phase_precond),
                              ("diag", phase_diag)):
                 gg = torch.cuda.CUDAGraph()
@@ -824,74 +829,81 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
         run = lambda name, bb: {"factor": phase_factor, "precond": phase_precond,
                                 "diag": phase_diag}[name](xs[bb])
         run_invert = phase_invert
-    outs = torch.empty(steps_cap(args) + 3, dtype=torch.float32, pin_memory=True)
+    steps = steps_cap(args)
+    warm = 3   # untimed steps: the first DMA passes over a fresh pinned buffer are slow
+    outs = torch.empty(warm + steps, dtype=torch.float32, pin_memory=True)
+    metric = torch.empty(warm + steps, dtype=torch.float32, device=dev)
     main = torch.cuda.current_stream(dev)
     copy = torch.cuda.Stream(dev)
     copy_out = torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event(), torch.cuda.Event()]
-    ev_used = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_used = [torch.cuda.Event() for _ in range(nbuf)]
     ev_done = torch.cuda.Event()
-    metric = torch.empty(steps_cap(args) + 3, dtype=torch.float32, device=dev)
     fside = torch.cuda.Stream(dev)
     dside = torch.cuda.Stream(dev)
     ev_djoin = torch.cuda.Event()
     ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
-    steps = steps_cap(args)
-    warm = 3   # untimed iterations: the first DMA passes over a fresh pinned buffer are slow
+    tt = [t]
+
+    def issue_copy(j):
+        """Inputs of step j of a pass into buffer j % nbuf, once step j - nbuf (the
+        last reader of that buffer, already issued) has finished."""
+        bb = j % nbuf
+        with torch.cuda.stream(copy):
+            if j >= nbuf:
+                copy.wait_event(ev_used[bb])
+            stage[bb].copy_(host, non_blocking=True)
+            ev_in[bb].record(copy)
+
+    def one_pass(count, base):
+        for j in range(min(nbuf, count)):
+            issue_copy(j)
+        for j in range(count):
+            tt[0] += 1
+            t_ = tt[0]
+            b = j % nbuf
+            main.wait_event(ev_in[b])
+            if overlap:                             # diagonal step alongside the KRON path
+                ev_fork.record(main)
+                dside.wait_event(ev_fork)
+                with torch.cuda.stream(dside):
+                    run("diag", b)
+                    ev_djoin.record(dside)
+            if overlap and (t_ - 1) % k != 0:      # factor update alongside the rest
+                ev_fork.record(main)
+                fside.wait_event(ev_fork)
+                with torch.cuda.stream(fside):
+                    run("factor", b)
+                    ev_join.record(fside)
+            else:
+                run("factor", b)
+                if (t_ - 1) % k == 0:
+                    run_invert()
+            run("precond", b)
+            if not overlap:
+                run("diag", b)
+            if overlap and (t_ - 1) % k != 0:
+                main.wait_event(ev_join)
+            if overlap:
+                main.wait_event(ev_djoin)
+            ev_used[b].record(main)
+            if j + nbuf < count:                    # refill this buffer for step j + nbuf
+                issue_copy(j + nbuf)
+            i = base + j
+            torch.sum(params_flat, dim=0, out=metric[i])   # the step's result
+            ev_done.record(main)
+            with torch.cuda.stream(copy_out):      # device -> host on its own stream
+                copy_out.wait_event(ev_done)
+                outs[i:i + 1].copy_(metric[i:i + 1], non_blocking=True)
+
+    torch.cuda.synchronize()
+    one_pass(warm, 0)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    with torch.cuda.stream(copy):
-        stage[0].copy_(host, non_blocking=True)
-        ev_in[0].record(copy)
-    for i in range(warm + steps):
-        t += 1
-        b = i % 2
-        if i == warm:   # the timed region: steps warm .. warm + steps - 1, all their copies
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            with torch.cuda.stream(copy):
-                stage[b].copy_(host, non_blocking=True)
-                ev_in[b].record(copy)
-        main.wait_event(ev_in[b])
-        if i + 1 < warm + steps and i + 1 != warm:   # next step's inputs, behind this step
-            nb_ = (i + 1) % 2
-            with torch.cuda.stream(copy):
-                if i >= 1:
-                    copy.wait_event(ev_used[nb_])   # the step that read that buffer is done
-                stage[nb_].copy_(host, non_blocking=True)
-                ev_in[nb_].record(copy)
-        if overlap:                             # diagonal step alongside the KRON path
-            ev_fork.record(main)
-            dside.wait_event(ev_fork)
-            with torch.cuda.stream(dside):
-                run("diag", b)
-                ev_djoin.record(dside)
-        if overlap and (t - 1) % k != 0:       # factor update alongside the rest
-            ev_fork.record(main)
-            fside.wait_event(ev_fork)
-            with torch.cuda.stream(fside):
-                run("factor", b)
-                ev_join.record(fside)
-        else:
-            run("factor", b)
-            if (t - 1) % k == 0:
-                run_invert()
-        run("precond", b)
-        if not overlap:
-            run("diag", b)
-        if overlap and (t - 1) % k != 0:
-            main.wait_event(ev_join)
-        if overlap:
-            main.wait_event(ev_djoin)
-        ev_used[b].record(main)
-        torch.sum(params_flat, dim=0, out=metric[i])   # the step's result
-        ev_done.record(main)
-        with torch.cuda.stream(copy_out):      # device -> host on its own stream
-            copy_out.wait_event(ev_done)
-            outs[i:i + 1].copy_(metric[i:i + 1], non_blocking=True)
+    one_pass(steps, warm)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
-    finite = all(math.isfinite(v) for v in outs[:warm + steps].tolist())
+    finite = all(math.isfinite(v) for v in outs.tolist())
     if not finite:
         print("bench.py: the end-to-end steps' parameter sums are not finite (the "
               "trajectory diverged)", file=sys.stderr, flush=True)
@@ -899,8 +911,13 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
             "d2h_bytes_per_step": 4, "steps": steps, "warmup": warm,
             "result": "sum of all updated parameters (fp32, reduced on the device)",
             "result_finite": finite,
-            "pipelined": "the next step's H2D on a copy stream during this step; the result's "
-                         "D2H on a second copy stream"}
+            "pipelined": (f"H2D of each step's inputs on a copy stream into a ring of {nbuf} "
+                          "device buffers, up to {} steps ahead of the compute; the result's "
+                          "D2H on a second copy stream").format(nbuf - 1)}
+
+
+# staging buffers of the end-to-end leg (5.64 GB each on the transformer set)
+E2E_BUFFERS = 4
 
 
 def steps_cap(args):
