@@ -2183,6 +2183,13 @@ kfac_status launch_wide_persistent(kfac_ctx* h, bool bf16, int epi, const TcProb
   constexpr int BN = 256;
   const int BM = pair ? 256 : 128;                   // rows of a tile
   const int box_a = 128, box_b = pair ? 128 : BN;    // rows of A and B each CTA loads
+  // Longest reductions first: a launch hands its tiles to the CTAs round-robin in
+  // problem order, so its last, partly filled round then holds the shortest tiles
+  // (the transformer set's preconditioning: 10.30 -> 9.93-10.02 ms).
+  std::vector<TcProblem> by_k(probs, probs + count);
+  std::stable_sort(by_k.begin(), by_k.end(),
+                   [](const TcProblem& a, const TcProblem& b) { return a.K > b.K; });
+  probs = by_k.data();
   std::unique_ptr<GroupedTc> g(new GroupedTc());
   for (int c0 = 0; c0 < count; c0 += kMaxGroup) {
     std::memset(g.get(), 0, sizeof(GroupedTc));
