@@ -79,8 +79,8 @@ TF32_PER_BF16 = 1.1 / 2.25          # nominal dense ratio
 # change to them reports null until the counters are taken again.
 MEASURED_TRAFFIC = {
     "workload": "transformer4",
-    "sources_sha256": "378cd6490eaf782a16df3d1c43a8aede07757215eb5312f9a94f18aa0e5c236d",
-    "bytes": {"factor": 4 * 5.0202e9, "precond": 4 * 6.5459e9, "diag": 4 * 2.1923e9},
+    "sources_sha256": "06ac010d6a1eedbb1cabf33e5097d1730a8966b3ae1d75ec029dd8ed5ba99391",
+    "bytes": {"factor": 4 * 5.0208e9, "precond": 4 * 5.8851e9, "diag": 4 * 2.1920e9},
     "note": "one-block capture (transformer1) x 4",
 }
 
@@ -108,8 +108,12 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graphs", action="store_true", help="time eager calls, not CUDA graphs")
-    p.add_argument("--no-overlap", action="store_true",
-                   help="run the phases of a step one after another on one stream")
+    p.add_argument("--schedule", choices=["auto", "serial", "overlap"], default="auto",
+                   help="serial: the phases of a step in order on one stream; overlap: the "
+                        "diagonal step, and on steps without a refresh the factor update, on "
+                        "side streams alongside the preconditioning; auto (default): the "
+                        "faster of the two over one refresh period each, measured untimed "
+                        "before the timed steps")
     p.add_argument("--nvtx", action="store_true",
                    help="NVTX ranges factor/invert/precond/diag around the phases of eager steps "
                         "(for profiler filters; use with --no-graphs)")
@@ -630,7 +634,27 @@ def run_gpu(args, peaks, peak_kind):
         return (kernels_in[("factor", b)] + kernels_in[("precond", b)] + kernels_in[("diag", b)]
                 + (kernels_in[("invert", 0)] if refresh else 0))
 
-    overlap = bool(graphs) and not args.no_overlap
+    def calibrate():
+        """Untimed: one refresh period of steps in each schedule; the faster wins."""
+        nonlocal t
+        cost = {}
+        for ov in (False, True):
+            e = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(k)]
+            for i in range(k):
+                t += 1
+                flush.zero_()
+                step_graph(t, t % NB, e[i], ov)
+            torch.cuda.synchronize()
+            cost[ov] = sum(e[i][0].elapsed_time(e[i][4]) for i in range(k))
+        return cost[True] < cost[False], cost
+
+    calibration = None
+    if not graphs or args.schedule == "serial":
+        overlap = False
+    elif args.schedule == "overlap":
+        overlap = True
+    else:
+        overlap, calibration = calibrate()
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     sampler = ClockSampler(dev.index)
@@ -754,8 +778,13 @@ def run_gpu(args, peaks, peak_kind):
                    "cuda_graphs": not args.no_graphs,
                    "phase_overlap": ("three streams: the diagonal step (DIAG layers) alongside "
                                      "the KRON path every step; the factor update alongside "
-                                     "preconditioning on steps without a refresh")
-                                    if (not args.no_graphs and not args.no_overlap) else "none",
+                                     "preconditioning on steps without a refresh"
+                                     if overlap else
+                                     "none: the phases of a step in order on one stream"),
+                   "schedule": args.schedule + (
+                       "" if calibration is None else
+                       " (untimed calibration over {} steps each: serial {:.2f} ms, "
+                       "overlap {:.2f} ms)".format(k, calibration[False], calibration[True])),
                    "l2": "flushed between steps (256 MiB write, outside the per-step events)"},
     }
 
