@@ -204,7 +204,74 @@ struct DiagFactorParams {
   int* tickets;    // [col_blocks]
   float* g_new;
   float* a_new;
+  int vec;         // rows of a and g 16-byte aligned, d_in and o whole 16-byte groups
 };
+
+// Squares of this CTA's rows [r0, r1) summed per column, with 16-byte loads:
+// thread (tx, ty) owns the 16 / sizeof(T) adjacent columns at tx and the rows
+// r0 + ty, r0 + ty + RG, ... (RG row groups), so each warp reads whole row
+// segments; eight rows' loads are in flight per thread (eight times the bytes of
+// the one-column form).  Each column's RG partials are then added in row-group
+// order through shared memory: column cb * 256 + threadIdx.x of the result.
+template <typename T>
+__device__ __forceinline__ float diag_colsum_vec(const DiagFactorParams& p, int cb, int64_t r0,
+                                                 int64_t r1) {
+  constexpr int V = 16 / (int)sizeof(T);      // columns per thread
+  constexpr int TPR = kK5Threads / V;         // threads across the 256-column block
+  constexpr int RG = kK5Threads / TPR;        // row groups
+  constexpr int B = 8;                        // rows per batch of loads
+  __shared__ float red[RG][kK5Threads];
+  const int tx = threadIdx.x % TPR, ty = threadIdx.x / TPR;
+  const int c0 = cb * kK5Threads + tx * V;
+  float acc[V], comp[V];
+#pragma unroll
+  for (int e = 0; e < V; ++e) acc[e] = comp[e] = 0.f;
+  auto add = [&](const uint4& w) {
+    float x[V];
+    if constexpr (sizeof(T) == 2) {
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        x[2 * h] = __uint_as_float(u[h] << 16);            // lower address
+        x[2 * h + 1] = __uint_as_float(u[h] & 0xffff0000u);
+      }
+    } else {
+      x[0] = __uint_as_float(w.x);
+      x[1] = __uint_as_float(w.y);
+      x[2] = __uint_as_float(w.z);
+      x[3] = __uint_as_float(w.w);
+    }
+#pragma unroll
+    for (int e = 0; e < V; ++e) {   // compensated (Kahan) sum per column
+      const float y = fmaf(x[e], x[e], -comp[e]);
+      const float t = acc[e] + y;
+      comp[e] = (t - acc[e]) - y;
+      acc[e] = t;
+    }
+  };
+  if (c0 < p.d_in + p.o) {
+    const T* base = c0 < p.d_in ? static_cast<const T*>(p.a) + c0
+                                : static_cast<const T*>(p.g) + (c0 - p.d_in);
+    const int64_t ld = c0 < p.d_in ? p.lda : p.ldg;
+    int64_t r = r0 + ty;
+    for (; r + (int64_t)(B - 1) * RG < r1; r += (int64_t)B * RG) {
+      uint4 w[B];
+#pragma unroll
+      for (int u = 0; u < B; ++u)
+        w[u] = __ldg(reinterpret_cast<const uint4*>(base + (r + (int64_t)u * RG) * ld));
+#pragma unroll
+      for (int u = 0; u < B; ++u) add(w[u]);
+    }
+    for (; r < r1; r += RG) add(__ldg(reinterpret_cast<const uint4*>(base + r * ld)));
+  }
+#pragma unroll
+  for (int e = 0; e < V; ++e) red[ty][tx * V + e] = acc[e];
+  __syncthreads();
+  float v = 0.f;
+#pragma unroll
+  for (int y = 0; y < RG; ++y) v += red[y][threadIdx.x];
+  return v;
+}
 
 template <typename T>
 __device__ __forceinline__ void diag_factor_body(const DiagFactorParams& p, int cb, int split) {
@@ -212,7 +279,10 @@ __device__ __forceinline__ void diag_factor_body(const DiagFactorParams& p, int 
   const int ncols = p.d_in + p.o;
   const int64_t r0 = (int64_t)split * p.rows_per_split;
   const int64_t r1 = min(p.rows, r0 + p.rows_per_split);
-  if (c < ncols) {
+  if (p.vec) {
+    const float v = diag_colsum_vec<T>(p, cb, r0, r1);
+    if (c < ncols) p.part[(size_t)split * ncols + c] = v;
+  } else if (c < ncols) {
     const T* base = c < p.d_in ? static_cast<const T*>(p.a) + c
                                : static_cast<const T*>(p.g) + (c - p.d_in);
     const int64_t ld = c < p.d_in ? p.lda : p.ldg;
@@ -296,6 +366,15 @@ size_t k5_scratch_floats(int n_plus_o, int64_t max_rows) {
 
 namespace {
 
+// K5's 16-byte-load form applies: both inputs' rows start on 16-byte boundaries
+// and d_in and o are whole 16-byte groups (no group straddles a and g or passes
+// a row's end)
+int k5_vec(const void* a, int64_t lda, const void* g, int64_t ldg, int d_in, int o, size_t elt) {
+  const int64_t V = 16 / (int64_t)elt;
+  auto al16 = [](const void* q) { return q && ((uintptr_t)q & 15) == 0; };
+  return al16(a) && al16(g) && lda % V == 0 && ldg % V == 0 && d_in % V == 0 && o % V == 0;
+}
+
 DiagFactorParams k5_params(const LayerInfo& L, const void* a, int64_t lda, const void* g,
                            int64_t ldg, int64_t rows, double scale, float* g_new, float* a_new,
                            int64_t splits, float* part, int* tickets) {
@@ -316,6 +395,7 @@ DiagFactorParams k5_params(const LayerInfo& L, const void* a, int64_t lda, const
   p.tickets = tickets;
   p.g_new = g_new;
   p.a_new = a_new;
+  p.vec = k5_vec(a, lda, g, ldg, L.d_in, L.o, L.in_dtype == KFAC_BF16 ? 2 : 4);
   return p;
 }
 
@@ -753,6 +833,7 @@ extern "C" kfac_status kfac_diag_factors_static(const void* a, int64_t lda, cons
   p.tickets = tickets;
   p.g_new = g_new;
   p.a_new = a_new;
+  p.vec = k5_vec(a, lda, g, ldg, d_in, d_out, es);
   if ((size_t)p.splits * ncols > kStaticScratchFloats) return KFAC_ERR_WORKSPACE;
   // the tickets must start at zero; a call interrupted earlier may have left them dirty
   if (cudaMemsetAsync(tickets, 0, sizeof(int) * p.col_blocks, stream) != cudaSuccess)

@@ -331,7 +331,11 @@ def test_bf16_preconditioning_within_the_bf16_tolerance(batched):
 # ------------------------------------------------------------------ K5 / K6 diagonal
 
 @pytest.mark.parametrize("M,d_in,o,bias,dtype", [(3000, 257, 100, 1, "f32"), (50, 3, 2, 0, "f32"),
-                                                 (2500, 640, 64, 1, "bf16")])
+                                                 (2500, 640, 64, 1, "bf16"),
+                                                 # 16-byte-load form: ragged rows, a partial
+                                                 # last column block
+                                                 (3001, 256, 100, 1, "f32"),
+                                                 (777, 328, 40, 0, "bf16"), (5, 8, 8, 1, "bf16")])
 def test_diag_factors_match_oracle(M, d_in, o, bias, dtype):
     kd = K.KFAC_BF16 if dtype == "bf16" else K.KFAC_F32
     h = K.Kfac([(K.KFAC_DIAG, o, d_in, bias, kd)], max_rows=M, **HP)
