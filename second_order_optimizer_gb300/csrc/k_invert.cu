@@ -123,15 +123,22 @@ __global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int 
   __shared__ float X[NB * AP];
   __shared__ float Y[32 * 33];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {   // all sixteen loads in flight before the first shared-memory store
+    constexpr int U = NB * NB / 256;
+    float v[U];
 #pragma unroll
-  for (int u = 0; u < NB * NB / 256; ++u) {
-    const int e = tid + 256 * u;
-    const int r = e / NB, c = e % NB;
-    float v = 0.f;
-    if (r < b && c <= r) v = J.L[(int64_t)(k + r) * n + k + c];
-    else if (r == c) v = 1.f;
-    A[r * AP + c] = v;
-    X[r * AP + c] = 0.f;
+    for (int u = 0; u < U; ++u) {
+      const int e = tid + 256 * u;
+      const int r = e / NB, c = e % NB;
+      v[u] = (r < b && c <= r) ? J.L[(int64_t)(k + r) * n + k + c] : (r == c ? 1.f : 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = tid + 256 * u;
+      const int r = e / NB, c = e % NB;
+      A[r * AP + c] = v[u];
+      X[r * AP + c] = 0.f;
+    }
   }
   __syncthreads();
   for (int p = 0; p < NB / SB; ++p) {
@@ -221,6 +228,17 @@ __global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int 
   // X off-diagonal blocks: pairs (T, B) of size 16, then 32
   diag_inverse_level<SB>(A, X, Y, tid);
   diag_inverse_level<2 * SB>(A, X, Y, tid);
+  if (b == NB) {   // a whole block: constant index arithmetic
+#pragma unroll
+    for (int u = 0; u < NB * NB / 256; ++u) {
+      const int e = tid + 256 * u;
+      const int r = e / NB, c = e % NB;
+      const int64_t g = (int64_t)(k + r) * n + k + c;
+      J.L[g] = (c <= r) ? A[r * AP + c] : 0.f;
+      J.X[g] = (c <= r) ? X[r * AP + c] : 0.f;
+    }
+    return;
+  }
 #pragma unroll 4
   for (int e = tid; e < b * b; e += 256) {
     const int r = e / b, c = e % b;
