@@ -79,8 +79,8 @@ TF32_PER_BF16 = 1.1 / 2.25          # nominal dense ratio
 # change to them reports null until the counters are taken again.
 MEASURED_TRAFFIC = {
     "workload": "transformer4",
-    "sources_sha256": "06ac010d6a1eedbb1cabf33e5097d1730a8966b3ae1d75ec029dd8ed5ba99391",
-    "bytes": {"factor": 4 * 5.0208e9, "precond": 4 * 5.8851e9, "diag": 4 * 2.1920e9},
+    "sources_sha256": "01f688b110dee83ca755aba2746646d20070dd7abf121623ac9cec7bf4c5db7a",
+    "bytes": {"factor": 4 * 5.0213e9, "precond": 4 * 6.1024e9, "diag": 4 * 2.1914e9},
     "note": "one-block capture (transformer1) x 4",
 }
 
