@@ -63,19 +63,21 @@ __global__ void __launch_bounds__(256) inv_prep_kernel(const InvJob* jobs, float
 // Diagonal block b x b (b <= 64) at (k, k): L_kk = chol(block) and X_kk = L_kk^{-1}.
 // The block sits in shared memory (rows >= b padded with the identity) and is
 // factored in 16-column sub-panels:
-//   (a) one warp factors the 16 x 16 diagonal sub-block D and inverts it: lane r
-//       holds row r of D and of D^{-1} in registers; each column's multipliers
-//       reach the other lanes by warp shuffles, so the 16 dependent steps need
-//       no block barrier;
-//   (b) the rows below become L_below = A_below D^{-T} (a product with D^{-1});
+//   (a) one warp factors the 16 x 16 diagonal sub-block D = L_D L_D^T: lane r
+//       holds row r in registers; each column's multipliers reach the other
+//       lanes by warp shuffles, so the 16 dependent steps need no block barrier;
+//   (b) the rows below become L_below = A_below L_D^{-T}, one thread per row by
+//       forward substitution;
 //   (c) the trailing lower triangle: A <- A - L_below L_below^T.
-// X_kk's diagonal 16-blocks are the D^{-1}; its off-diagonal blocks follow by
-// doubling over block pairs, X_BT = -X_BB (L_BT X_TT).  A pivot that is not > 0
-// and finite is recorded (first failing column), replaced by 1, and reported
-// once per sub-panel.
-// (A per-column version that kept the whole block in registers of 256 threads
-// paid a block barrier and shared-memory round trip per column, ~1500 cycles per
-// column on GB300; this one spends ~220 cycles per column in the warp.)
+// X_kk then follows from its diagonal 1 / L_ii by doubling over block pairs of
+// size 1 to 32, X_BT = -X_BB (L_BT X_TT).  A pivot that is not > 0 and finite is
+// recorded (first failing column), replaced by 1, and reported once per
+// sub-panel.
+// (Measured on GB300 with clock stamps: a per-column version that kept the
+// whole block in registers of 256 threads paid a block barrier and a
+// shared-memory round trip per column, ~1500 cycles a column; forming each D^{-1}
+// inside the warp's pivot loop as well, ~420 cycles a column and 42.8k cycles
+// for the block; this form ~205 cycles a column and 29.6k for the block.)
 constexpr int SB = 16;       // sub-panel width
 constexpr int AP = NB + 1;   // shared row pitch (floats)
 constexpr unsigned kFull = 0xffffffffu;
@@ -86,10 +88,12 @@ constexpr unsigned kFull = 0xffffffffu;
 // nonzero terms in the same order) with fixed trip counts the compiler unrolls.
 template <int SZ>
 __device__ __forceinline__ void diag_inverse_level(const float* A, float* X, float* Y, int tid) {
-  constexpr int PER = (NB / (2 * SZ)) * SZ * SZ / 256;   // outputs per thread
+  constexpr int TOT = (NB / (2 * SZ)) * SZ * SZ;   // outputs of the level
+  constexpr int PER = (TOT + 255) / 256;           // per thread, at most
 #pragma unroll
   for (int u = 0; u < PER; ++u) {
     const int e = tid + 256 * u;
+    if (TOT % 256 != 0 && e >= TOT) break;
     const int pr = e / (SZ * SZ), i = (e / SZ) % SZ, c = e % SZ;
     const int T0 = pr * 2 * SZ, B0 = T0 + SZ;
     float acc = 0.f;
@@ -101,6 +105,7 @@ __device__ __forceinline__ void diag_inverse_level(const float* A, float* X, flo
 #pragma unroll
   for (int u = 0; u < PER; ++u) {
     const int e = tid + 256 * u;
+    if (TOT % 256 != 0 && e >= TOT) break;
     const int pr = e / (SZ * SZ), i = (e / SZ) % SZ, c = e % SZ;
     const int T0 = pr * 2 * SZ, B0 = T0 + SZ;
     float acc = 0.f;
@@ -111,7 +116,7 @@ __device__ __forceinline__ void diag_inverse_level(const float* A, float* X, flo
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int k,
+__global__ void __launch_bounds__(256, 1) chol_diag_kernel(const InvJob* jobs, int k,
                                                         DevStatus* st) {
   pdl_wait();
   pdl_trigger();
@@ -145,13 +150,11 @@ __global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int 
     const int o = p * SB;
     if (warp == 0) {   // (a)
       const int r = lane & (SB - 1);   // lanes 16..31 mirror 0..15
-      float s[SB], t[SB];
+      float s[SB];
 #pragma unroll
-      for (int c = 0; c < SB; ++c) {
-        s[c] = (c <= r) ? A[(o + r) * AP + o + c] : 0.f;
-        t[c] = (c == r) ? 1.f : 0.f;
-      }
+      for (int c = 0; c < SB; ++c) s[c] = (c <= r) ? A[(o + r) * AP + o + c] : 0.f;
       int bad = -1;
+      float rinv = 0.f;   // 1 / L_rr
 #pragma unroll
       for (int j = 0; j < SB; ++j) {
         float d = __shfl_sync(kFull, s[j], j);
@@ -161,51 +164,41 @@ __global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int 
         const float inv = rsqrtf(d), sq = d * inv;
         const float l = r > j ? s[j] * inv : 0.f;
         s[j] = r == j ? sq : (r > j ? l : s[j]);
+        rinv = r == j ? inv : rinv;
 #pragma unroll
         for (int c = j + 1; c < SB; ++c) s[c] = fmaf(-l, __shfl_sync(kFull, l, c), s[c]);
-#pragma unroll
-        for (int c = 0; c <= j; ++c) {
-          const float tj = __shfl_sync(kFull, t[c], j) * inv;
-          t[c] = r == j ? tj : fmaf(-l, tj, t[c]);
-        }
       }
       if (bad >= 0 && o + bad < b && lane == 0)
         report_error(st, KFAC_ERR_NOT_PD, J.layer, k + o + bad);
       if (lane < SB) {
 #pragma unroll
         for (int c = 0; c < SB; ++c)
-          if (c <= r) {
-            A[(o + r) * AP + o + c] = s[c];
-            X[(o + r) * AP + o + c] = t[c];
-          }
+          if (c <= r) A[(o + r) * AP + o + c] = s[c];
+        X[(o + r) * AP + o + r] = rinv;   // X_kk's diagonal
       }
     }
     __syncthreads();
     const int nr = NB - o - SB;   // rows below the sub-block
     if (nr > 0) {
-      // (b) thread: column c = tid % 16 with row c of D^{-1} in registers
-      float outv[3];
-      {
-        const int c = tid % SB;
-        float dr[SB];
+      // (b) the rows below: L_below = A_below L_D^{-T}, one thread per row by
+      // forward substitution, x_c = (a_c - sum_{m<c} x_m L_D[c][m]) / L_D[c][c]
+      if (tid < nr) {
+        const int i = o + SB + tid;
+        float x[SB];
 #pragma unroll
-        for (int m = 0; m < SB; ++m) dr[m] = X[(o + c) * AP + o + m];   // 0 for m > c
+        for (int c = 0; c < SB; ++c) x[c] = A[i * AP + o + c];
 #pragma unroll
-        for (int u = 0; u < 3; ++u) {
-          const int i = o + SB + tid / SB + 16 * u;
-          float acc = 0.f;
-          if (i < NB) {
+        for (int c = 0; c < SB; ++c) {
+          float a0 = x[c], a1 = 0.f;   // two chains
 #pragma unroll
-            for (int m = 0; m < SB; ++m) acc = fmaf(A[i * AP + o + m], dr[m], acc);
+          for (int m = 0; m < c; ++m) {
+            if (m & 1) a1 = fmaf(-x[m], A[(o + c) * AP + o + m], a1);
+            else a0 = fmaf(-x[m], A[(o + c) * AP + o + m], a0);
           }
-          outv[u] = acc;
+          x[c] = (a0 + a1) * X[(o + c) * AP + o + c];
         }
-      }
-      __syncthreads();
 #pragma unroll
-      for (int u = 0; u < 3; ++u) {
-        const int i = o + SB + tid / SB + 16 * u;
-        if (i < NB) A[i * AP + o + tid % SB] = outv[u];
+        for (int c = 0; c < SB; ++c) A[i * AP + o + c] = x[c];
       }
       __syncthreads();
       // (c) thread: column jj with row jj of L_below in registers; rows i >= jj
@@ -225,7 +218,11 @@ __global__ void __launch_bounds__(256) chol_diag_kernel(const InvJob* jobs, int 
       __syncthreads();
     }
   }
-  // X off-diagonal blocks: pairs (T, B) of size 16, then 32
+  // X_kk = L_kk^{-1} from its diagonal by doubling over block pairs of size 1 to 32
+  diag_inverse_level<1>(A, X, Y, tid);
+  diag_inverse_level<2>(A, X, Y, tid);
+  diag_inverse_level<4>(A, X, Y, tid);
+  diag_inverse_level<8>(A, X, Y, tid);
   diag_inverse_level<SB>(A, X, Y, tid);
   diag_inverse_level<2 * SB>(A, X, Y, tid);
   if (b == NB) {   // a whole block: constant index arithmetic
