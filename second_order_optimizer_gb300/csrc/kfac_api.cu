@@ -152,7 +152,7 @@ bool make_plan(const kfac_layer_desc* descs, int nl, int64_t max_rows, const kfa
   // batched calls pack a group of layers at once, within a fixed budget
   tcpack = std::max(tcpack, std::min(pack_sum, kBatchScratchBudget));
   tcpack = std::max(tcpack, std::min(inv_pack_sum, kBatchScratchBudget));
-  k4 = std::max(k4, std::min(k4_sum, kBatchScratchBudget / sizeof(float)));
+  k4 = std::max(k4, std::min(k4_sum, kPrecondScratchBudget / sizeof(float)));
   P->part_floats = part;
   P->off_part = take(part * sizeof(float));
   P->n_tickets = tickets;
