@@ -79,8 +79,8 @@ TF32_PER_BF16 = 1.1 / 2.25          # nominal dense ratio
 # change to them reports null until the counters are taken again.
 MEASURED_TRAFFIC = {
     "workload": "transformer4",
-    "sources_sha256": "01f688b110dee83ca755aba2746646d20070dd7abf121623ac9cec7bf4c5db7a",
-    "bytes": {"factor": 4 * 5.0213e9, "precond": 4 * 6.1024e9, "diag": 4 * 2.1914e9},
+    "sources_sha256": "d8ab3a112f64c63580eb8c0972e60a17e89071e9854f8d25919b82d4f048d78f",
+    "bytes": {"factor": 4 * 5.0206e9, "precond": 4 * 6.0922e9, "diag": 4 * 2.1913e9},
     "note": "one-block capture (transformer1) x 4",
 }
 
@@ -824,7 +824,7 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
             entries.append((li, key, off, v))
             off += (nb + 255) // 256 * 256
     total = off
-    host = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    host, host_release = pinned_host_buffer(total)
     for li, key, o, v in entries:
         nb = v.numel() * v.element_size()
         host[o:o + nb].copy_(v.contiguous().view(-1).view(torch.uint8).cpu())
@@ -932,6 +932,7 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
     one_pass(steps, warm)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
+    host_release()
     finite = all(math.isfinite(v) for v in outs.tolist())
     if not finite:
         print("bench.py: the end-to-end steps' parameter sums are not finite (the "
@@ -943,6 +944,39 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
             "pipelined": (f"H2D of each step's inputs on a copy stream into a ring of {nbuf} "
                           "device buffers, up to {} steps ahead of the compute; the result's "
                           "D2H on a second copy stream").format(nbuf - 1)}
+
+
+def pinned_host_buffer(nbytes):
+    """Page-locked host buffer for the end-to-end inputs and a function that
+    releases it: an anonymous mapping with transparent huge pages requested,
+    touched and registered with CUDA.  Host-to-device copies from a buffer of the
+    CUDA host allocator fell to 77-97 GB/s on a box after a long GPU test run
+    (the pages it got were small and scattered), where this one kept 209 GB/s.
+    Falls back to the allocator when the registration is refused."""
+    import ctypes
+    import mmap
+    import torch
+    try:
+        cudart = torch.cuda.cudart()
+        buf = mmap.mmap(-1, nbytes, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        try:
+            buf.madvise(mmap.MADV_HUGEPAGE)
+        except (AttributeError, OSError):
+            pass
+        addr = ctypes.addressof(ctypes.c_char.from_buffer(buf))
+        ctypes.memset(addr, 0, nbytes)           # fault every page in now
+        if int(cudart.cudaHostRegister(addr, nbytes, 0)) != 0:
+            raise RuntimeError("cudaHostRegister refused")
+    except Exception:
+        return torch.empty(nbytes, dtype=torch.uint8, pin_memory=True), lambda: None
+    t = torch.frombuffer(buf, dtype=torch.uint8)
+
+    def release():
+        torch.cuda.synchronize()
+        cudart.cudaHostUnregister(addr)
+
+    release.keep = buf   # the mapping lives as long as the tensor's user holds this
+    return t, release
 
 
 # staging buffers of the end-to-end leg (5.64 GB each on the transformer set)
