@@ -79,7 +79,7 @@ TF32_PER_BF16 = 1.1 / 2.25          # nominal dense ratio
 # change to them reports null until the counters are taken again.
 MEASURED_TRAFFIC = {
     "workload": "transformer4",
-    "sources_sha256": "d8ab3a112f64c63580eb8c0972e60a17e89071e9854f8d25919b82d4f048d78f",
+    "sources_sha256": "e66b847f4ef68f3548bb96384ed532fa0088f8aa4b2e22ff53357cad465b581c",
     "bytes": {"factor": 4 * 5.0206e9, "precond": 4 * 6.0922e9, "diag": 4 * 2.1913e9},
     "note": "one-block capture (transformer1) x 4",
 }

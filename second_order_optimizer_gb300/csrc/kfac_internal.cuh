@@ -302,8 +302,8 @@ size_t inv_y_floats(int n);
 constexpr size_t kBatchScratchBudget = size_t(1) << 30;
 // the batched preconditioning's gradient and X^T operands: room for every layer
 // of a large set in one group (the transformer set's 24 layers take 3.2 GB), so
-// that its two products run as one pass each (transformer preconditioning
-// 10.2 -> 9.9 ms with the phases in order on one stream)
+// that one pack and one round of product launches serve them all (transformer
+// preconditioning 10.2 -> 9.9 ms with the phases in order on one stream)
 constexpr size_t kPrecondScratchBudget = size_t(4) << 30;
 size_t tc_pack_bytes(int n, int64_t max_rows, bool bf16);
 size_t tc_part_floats();
