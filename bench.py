@@ -806,10 +806,11 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
     side stream alongside the preconditioning and the diagonal step (as in the
     timed steps).  With CUDA graphs (the default) the library calls of each phase
     are captured once per staging buffer and replayed, as the timed steps do;
-    --no-graphs makes them eagerly every step.  Three untimed steps come first, as
-    a pass of their own (in a fresh process the first passes of the copy engines
-    over the newly pinned buffer ran at about half speed); the timed pass starts
-    from an idle GPU, so every copy of a timed step is inside the timed region."""
+    --no-graphs makes them eagerly every step.  Two untimed steps per staging
+    buffer come first, as a pass of their own (in a fresh process the first passes
+    of the copy engines over the newly pinned buffer ran at about half speed); the
+    timed pass starts from an idle GPU, so every copy of a timed step is inside
+    the timed region."""
     phase_factor, phase_invert, phase_precond, phase_diag = phases
     import torch
     first = {}
@@ -859,7 +860,7 @@ def run_e2e(args, layers, x_dev, params_flat, srcidx, t, dev, phases, k, overlap
                                 "diag": phase_diag}[name](xs[bb])
         run_invert = phase_invert
     steps = steps_cap(args)
-    warm = 3   # untimed steps: the first DMA passes over a fresh pinned buffer are slow
+    warm = 2 * E2E_BUFFERS   # untimed steps: the first DMA passes over a fresh buffer are slow
     outs = torch.empty(warm + steps, dtype=torch.float32, pin_memory=True)
     metric = torch.empty(warm + steps, dtype=torch.float32, device=dev)
     main = torch.cuda.current_stream(dev)
