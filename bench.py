@@ -79,8 +79,8 @@ TF32_PER_BF16 = 1.1 / 2.25          # nominal dense ratio
 # change to them reports null until the counters are taken again.
 MEASURED_TRAFFIC = {
     "workload": "transformer4",
-    "sources_sha256": "e66b847f4ef68f3548bb96384ed532fa0088f8aa4b2e22ff53357cad465b581c",
-    "bytes": {"factor": 4 * 5.0206e9, "precond": 4 * 6.0922e9, "diag": 4 * 2.1913e9},
+    "sources_sha256": "b1caf7e8f7732ac757d2c11dd5ac8ff7d08c12d00c66c558b8ef3ae09d12a1c0",
+    "bytes": {"factor": 4 * 5.0202e9, "precond": 4 * 6.0914e9, "diag": 4 * 2.1917e9},
     "note": "one-block capture (transformer1) x 4",
 }
 

@@ -48,14 +48,17 @@ __global__ void __launch_bounds__(256) inv_prep_kernel(const InvJob* jobs, float
   const InvJob J = jobs[blockIdx.y];
   // rows over the grid, columns over the threads (no index division per element);
   // both triangles (F is symmetric): the tensor-core trailing updates of large
-  // factors read either triangle and keep the trailing block symmetric
+  // factors read either triangle and keep the trailing block symmetric.  X needs
+  // no clearing: every refresh rewrites its lower triangle (diagonal blocks with
+  // their zeros above the diagonal, then every block below by the doubling
+  // levels), and its strict upper triangle outside the diagonal blocks, zero
+  // since kfac_create, is never written.
   for (int r = blockIdx.x; r < J.n; r += gridDim.x) {
     const int64_t row = (int64_t)r * J.n;
 #pragma unroll 4
     for (int c = threadIdx.x; c < J.n; c += blockDim.x) {
       const float f = J.F[row + c];
       J.L[row + c] = r == c ? f + sqrt_gamma : f;
-      J.X[row + c] = 0.f;
     }
   }
 }

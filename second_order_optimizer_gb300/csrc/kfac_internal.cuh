@@ -78,7 +78,8 @@ template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16
 struct InvJob {
   const float* F;   // running factor (n x n, symmetric)
   float* L;         // Cholesky factor, in place (n x n, lower; upper zeroed)
-  float* X;         // L^{-1} (n x n, lower; upper zero)
+  float* X;         // L^{-1} (n x n, lower; the strict upper triangle stays zero
+                    //   from kfac_create: no kernel writes it)
   float* Y;         // level scratch (n x n/2 + tile slack)
   float* Finv;      // result (n x n, pitch n)
   float* Finv_hi;   // result as a K4 operand, pitch np: TF32 hi and the bf16
